@@ -1,0 +1,401 @@
+"""CPU pins of the oracle: forward pieces against closed forms, library
+routines (scipy SH / rotations) and brute force.  None of these re-types the
+oracle's own formula; each checks it against something independent."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import scenes
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split()
+            vals[k] = float(v)
+    return vals
+
+
+def test_memory_figures_of_the_pages():
+    g = _golden("memory_figures.txt")
+    assert g["xyz"] + g["scale"] + g["rotation"] + g["opacity"] + g["sh_coeffs"] == g[
+        "params_per_gaussian"] == scenes.NPARAM
+    # SH degree 3: (3+1)^2 coefficients per colour channel, 3 channels
+    assert (3 + 1) ** 2 * 3 == g["sh_coeffs"]
+    # params + two Adam moments, fp32
+    assert g["params_per_gaussian"] * g["bytes_per_param"] * 3 == g["bytes_per_gaussian_with_adam"]
+    assert abs(g["mi300x_hbm_gb"] * 1e9 / g["bytes_per_gaussian_with_adam"] / 1e6
+               - g["mi300x_max_gaussians_millions"]) < 1.0
+    assert abs(g["params_per_gaussian"] * g["bytes_per_param"] * 1e6 / 1e9
+               - g["gb_per_million_gaussians"]) < 1e-12
+    assert abs(g["params_per_gaussian"] * g["bytes_per_param"] * g["largest_run_gaussians"] / 1e9
+               - g["largest_run_gb"]) < 1e-3
+
+
+# --------------------------------------------------------------------------
+# spherical harmonics
+
+
+def _real_sh_scipy(l, m, d):
+    """Real SH from scipy's complex Y_l^m (Condon-Shortley phase included):
+    m>0: sqrt2 Re Y_l^m, m<0: sqrt2 Im Y_l^|m|, m=0: Y_l^0."""
+    from scipy.special import sph_harm_y
+    x, y, z = d
+    theta = math.acos(max(-1.0, min(1.0, z)))
+    phi = math.atan2(y, x)
+    Y = sph_harm_y(l, abs(m), theta, phi)
+    if m > 0:
+        return math.sqrt(2.0) * Y.real
+    if m < 0:
+        return math.sqrt(2.0) * Y.imag
+    return Y.real
+
+
+def test_sh_basis_matches_scipy(oracle_mod):
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        d = rng.standard_normal(3)
+        d /= np.linalg.norm(d)
+        got = oracle_mod.sh_basis(d)
+        k = 0
+        for l in range(4):
+            for m in range(-l, l + 1):
+                assert got[k] == pytest.approx(_real_sh_scipy(l, m, d), abs=1e-12), (l, m)
+                k += 1
+
+
+def test_sh_basis_orthonormal_by_exact_quadrature(oracle_mod):
+    # Gauss-Legendre in cos(theta) x uniform phi integrates polynomials of
+    # degree <= 6 on the sphere exactly.
+    xs, ws = np.polynomial.legendre.leggauss(8)
+    nphi = 16
+    G = np.zeros((16, 16))
+    for ct, w in zip(xs, ws):
+        st = math.sqrt(1 - ct * ct)
+        for j in range(nphi):
+            ph = 2 * math.pi * j / nphi
+            Y = oracle_mod.sh_basis([st * math.cos(ph), st * math.sin(ph), ct])
+            G += w * (2 * math.pi / nphi) * np.outer(Y, Y)
+    assert np.abs(G - np.eye(16)).max() < 1e-12
+
+
+def test_quat_to_rot_matches_scipy(oracle_mod):
+    from scipy.spatial.transform import Rotation
+    rng = np.random.default_rng(1)
+    for _ in range(20):
+        q = rng.standard_normal(4)
+        q /= np.linalg.norm(q)
+        ref = Rotation.from_quat([q[1], q[2], q[3], q[0]]).as_matrix()  # scipy: (x,y,z,w)
+        assert np.abs(oracle_mod.quat_to_rot(q) - ref).max() < 1e-14
+
+
+# --------------------------------------------------------------------------
+# projection
+
+
+def _one_gaussian(mu, log_scale, q, logit, sh=None):
+    p = np.zeros((59, 1))
+    p[0:3, 0] = mu
+    p[3:6, 0] = log_scale
+    p[6:10, 0] = q
+    p[10, 0] = logit
+    if sh is not None:
+        p[11:59, 0] = np.asarray(sh).reshape(48)
+    return p
+
+
+def _cam(fx=256.0, fy=256.0, cx=128.0, cy=128.0, W=256, H=256, R=None, t=None):
+    return scenes.camera(np.eye(3) if R is None else R, np.zeros(3) if t is None else t, fx, fy, cx,
+                         cy, W, H)
+
+
+@pytest.mark.parametrize("z,s,q", [(4.0, 0.05, (1, 0, 0, 0)), (2.5, 0.01, (0.3, -0.5, 0.7, 0.1)),
+                                   (10.0, 0.2, (0.5, 0.5, 0.5, 0.5))])
+def test_isotropic_gaussian_on_axis_closed_form(oracle_mod, z, s, q):
+    f = 300.0
+    q = np.asarray(q, float) / np.linalg.norm(q)
+    p = _one_gaussian([0, 0, z], [math.log(s)] * 3, q, 0.0)
+    pr = oracle_mod.project(p, [_cam(fx=f, fy=f)])
+    var = f * f * s * s / (z * z) + 0.3
+    assert pr["mean2d"][0] == pytest.approx([128.0, 128.0], abs=1e-12)
+    assert pr["conic"][0] == pytest.approx([1 / var, 0.0, 1 / var], rel=1e-12, abs=1e-15)
+    assert pr["radius"][0] == math.ceil(3 * math.sqrt(var))
+    assert pr["depth"][0] == pytest.approx(z)
+
+
+def test_sh_degree0_colour_closed_form(oracle_mod):
+    sh = np.zeros((16, 3))
+    sh[0] = [0.4, -0.2, 1.3]
+    rng = np.random.default_rng(5)
+    for _ in range(5):
+        mu = [rng.uniform(-1, 1), rng.uniform(-1, 1), rng.uniform(2, 6)]
+        p = _one_gaussian(mu, [-3] * 3, [1, 0, 0, 0], 0.3, sh)
+        pr = oracle_mod.project(p, [_cam()])
+        expect = np.maximum(0.5 + sh[0] / (2 * math.sqrt(math.pi)), 0.0)
+        assert pr["color"][0] == pytest.approx(expect, abs=1e-14)
+        assert pr["opacity"][0] == pytest.approx(1 / (1 + math.exp(-0.3)))
+
+
+def test_view_dependent_colour_uses_camera_centre(oracle_mod):
+    """colour = 0.5 + sum_k Y_k(d) sh_k with d the unit vector from the
+    camera centre to the mean; Y_k from scipy."""
+    rng = np.random.default_rng(6)
+    for _ in range(5):
+        pos = rng.uniform(-3, 3, 3) + np.array([0, 0, -8.0])
+        cam = scenes.look_at(pos, (0, 0, 0), (0, 1, 0.2), 200, 200, 128, 96)
+        mu = rng.uniform(-0.5, 0.5, 3)
+        sh = rng.normal(0, 0.3, (16, 3))
+        sh[0] += 1.5
+        p = _one_gaussian(mu, [-2.5] * 3, [1, 0, 0, 0], 0.0, sh)
+        pr = oracle_mod.project(p, [cam])
+        assert pr["radius"][0] > 0
+        d = mu - pos
+        d /= np.linalg.norm(d)
+        Y = [_real_sh_scipy(l, m, d) for l in range(4) for m in range(-l, l + 1)]
+        expect = np.maximum(0.5 + np.asarray(Y) @ sh, 0.0)
+        assert pr["color"][0] == pytest.approx(expect, abs=1e-12)
+
+
+def _pinhole(p, cam):
+    return np.array([cam["fx"] * p[0] / p[2] + cam["cx"], cam["fy"] * p[1] / p[2] + cam["cy"]])
+
+
+def _fd_jacobian(fn, p, h=1e-6):
+    J = np.zeros((2, 3))
+    for i in range(3):
+        e = np.zeros(3)
+        e[i] = h
+        J[:, i] = (fn(p + e) - fn(p - e)) / (2 * h)
+    return J
+
+
+@pytest.mark.parametrize("clamp", [False, True])
+def test_ewa_covariance_is_linearised_pinhole(oracle_mod, clamp):
+    """cov2 = J W Sigma W^T J^T + 0.3 I with J the Jacobian of the pinhole
+    map (finite differences), evaluated at the point clamped to 1.3x the half
+    field of view; Sigma from scipy's rotation."""
+    from scipy.spatial.transform import Rotation
+    rng = np.random.default_rng(7 + clamp)
+    for _ in range(5):
+        Rw = Rotation.random(random_state=rng).as_matrix()
+        cam = _cam(fx=220.0, fy=180.0, cx=128.0, cy=100.0, W=256, H=200, R=Rw,
+                   t=rng.uniform(-1, 1, 3) + [0, 0, 6])
+        pc = np.array([rng.uniform(-0.3, 0.3), rng.uniform(-0.3, 0.3), 1.0]) * rng.uniform(3, 8)
+        if clamp:
+            pc[0] = 2.0 * 1.3 * (0.5 * 256 / 220.0) * pc[2]  # x/z twice the clamp limit
+        mu = Rw.T @ (pc - cam["t"])
+        q = rng.standard_normal(4)
+        q /= np.linalg.norm(q)
+        ls = rng.uniform(-1.5, -0.5, 3)
+        p = _one_gaussian(mu, ls, q, 0.0)
+        pr = oracle_mod.project(p, [cam])
+        Rq = Rotation.from_quat([q[1], q[2], q[3], q[0]]).as_matrix()
+        Sig = Rq @ np.diag(np.exp(2 * ls)) @ Rq.T
+        pj = pc.copy()
+        if clamp:
+            pj[0] = 1.3 * (0.5 * 256 / 220.0) * pc[2]
+        J = _fd_jacobian(lambda x: _pinhole(x, cam), pj)
+        cov2 = J @ Rw @ Sig @ Rw.T @ J.T + 0.3 * np.eye(2)
+        if not clamp:
+            inv = np.linalg.inv(cov2)
+            assert pr["conic"][0] == pytest.approx([inv[0, 0], inv[0, 1], inv[1, 1]], rel=1e-7)
+            assert pr["mean2d"][0] == pytest.approx(_pinhole(pc, cam), rel=1e-12)
+        else:
+            # clamped rows may be culled (footprint off-screen); project the
+            # covariance through the oracle's conic when visible
+            if pr["radius"][0] > 0:
+                inv = np.linalg.inv(cov2)
+                assert pr["conic"][0] == pytest.approx([inv[0, 0], inv[0, 1], inv[1, 1]], rel=1e-7)
+        lam = np.linalg.eigvalsh(cov2).max()
+        if pr["radius"][0] > 0:
+            assert pr["radius"][0] == math.ceil(3 * math.sqrt(lam))
+
+
+def test_culling_near_plane_and_offscreen(oracle_mod):
+    cam = _cam()
+    p = np.concatenate([_one_gaussian([0, 0, 0.005], [-3] * 3, [1, 0, 0, 0], 0.0),
+                        _one_gaussian([0, 0, -2.0], [-3] * 3, [1, 0, 0, 0], 0.0),
+                        _one_gaussian([50.0, 0, 2.0], [-3] * 3, [1, 0, 0, 0], 0.0),
+                        _one_gaussian([0, 0, 3.0], [-3] * 3, [1, 0, 0, 0], 0.0)], axis=1)
+    pr = oracle_mod.project(p, [cam])
+    assert list(pr["radius"][:3]) == [0, 0, 0] and list(pr["tiles"][:3]) == [0, 0, 0]
+    assert pr["radius"][3] > 0 and pr["tiles"][3] > 0
+
+
+def test_footprint_rect_covers_radius_disc(oracle_mod):
+    """Every in-image pixel centre within `radius` of the mean lies in a tile
+    of the rectangle."""
+    rng = np.random.default_rng(11)
+    W, H, tile = 200, 120, 16
+    tx, ty = (W + tile - 1) // tile, (H + tile - 1) // tile
+    ys, xs = np.mgrid[0:H, 0:W]
+    for _ in range(200):
+        mx, my = rng.uniform(-40, W + 40), rng.uniform(-40, H + 40)
+        r = int(rng.integers(1, 60))
+        x0, x1, y0, y1 = oracle_mod.tile_rect(mx, my, r, tile, tx, ty)
+        inside = (xs + 0.5 - np.float32(mx)) ** 2 + (ys + 0.5 - np.float32(my)) ** 2 <= r * r
+        ptx, pty = xs // tile, ys // tile
+        in_rect = (ptx >= x0) & (ptx < x1) & (pty >= y0) & (pty < y1)
+        assert not np.any(inside & ~in_rect)
+
+
+def test_binning_brute_force(oracle_mod):
+    """Enumerate every (row, tile) pair by a direct containment test, sort the
+    (key, id) tuples with Python's sort and compare bit for bit."""
+    cfg = scenes.make("tiny_2k_256", n_override=300)
+    cams = [cfg["cams"][0], scenes.camera(np.eye(3), [0.3, -0.2, 0.5], 256, 256, 128, 128, 256, 256)]
+    n = 300
+    pr = oracle_mod.project(cfg["params"], cams)
+    m32 = pr["mean2d"].astype(np.float32)
+    d32 = pr["depth"].astype(np.float32)
+    keys, vals, ranges = oracle_mod.bin_and_sort(n, 2, m32, pr["radius"], d32, 256, 256)
+    tile = np.float32(16)
+    T = 16 * 16
+    items = []
+    for r in range(2 * n):
+        if pr["radius"][r] <= 0:
+            continue
+        fr = np.float32(pr["radius"][r])
+        mx, my = m32[r]
+        x0 = min(max(math.floor(np.float32(mx - fr) / tile), 0), 16)
+        x1 = min(max(math.ceil(np.float32(mx + fr) / tile), 0), 16)
+        y0 = min(max(math.floor(np.float32(my - fr) / tile), 0), 16)
+        y1 = min(max(math.ceil(np.float32(my + fr) / tile), 0), 16)
+        view, g = divmod(r, n)
+        for t in range(T):
+            tx_, ty_ = t % 16, t // 16
+            if x0 <= tx_ < x1 and y0 <= ty_ < y1:
+                dbits = int(np.array([d32[r]], np.float32).view(np.uint32)[0])
+                items.append((((view * T + t) << 32) | dbits, g))
+    items.sort()
+    assert keys.size == len(items) == int(pr["tiles"].sum())
+    assert [int(k) for k in keys] == [k for k, _ in items]
+    assert [int(v) for v in vals] == [v for _, v in items]
+    for f in range(2 * T):
+        sel = [i for i, (k, _) in enumerate(items) if (k >> 32) == f]
+        if sel:
+            assert list(ranges[f]) == [sel[0], sel[-1] + 1]
+        else:
+            assert list(ranges[f]) == [0, 0]
+
+
+# --------------------------------------------------------------------------
+# compositing
+
+
+def _centre_scene(logits, depths, colors_dc, W=64, H=64, px=(20, 33)):
+    """Gaussians on the optical axis of a camera whose principal point sits on
+    the centre of pixel px; degree-0 colour only."""
+    k = len(logits)
+    p = np.concatenate([
+        _one_gaussian([0, 0, depths[i]], [-2.5] * 3, [1, 0, 0, 0], logits[i],
+                      np.concatenate([colors_dc[i], np.zeros(45)])) for i in range(k)], axis=1)
+    cam = _cam(fx=60.0, fy=60.0, cx=px[0] + 0.5, cy=px[1] + 0.5, W=W, H=H)
+    return p, cam
+
+
+def test_single_gaussian_at_pixel_centre(oracle_mod):
+    for logit in (-2.0, 0.0, 1.5, 6.0):
+        dc = np.array([0.7, -0.1, 0.25])
+        p, cam = _centre_scene([logit], [3.0], [dc])
+        pr, _, fw = oracle_mod.render(p, [cam])
+        a = min(0.99, 1 / (1 + math.exp(-logit)))
+        col = np.maximum(0.5 + dc / (2 * math.sqrt(math.pi)), 0)
+        assert fw["image"][0, :, 33, 20] == pytest.approx(a * col, abs=1e-14)
+        assert fw["T_final"][0, 33, 20] == pytest.approx(1 - a, abs=1e-14)
+        assert fw["n_contrib"][0, 33, 20] == 1
+
+
+def test_stack_transmittance_is_product(oracle_mod):
+    rng = np.random.default_rng(3)
+    k = 6
+    logits = rng.uniform(-1.0, 1.0, k)
+    depths = np.sort(rng.uniform(2, 8, k))[::-1]  # given back to front
+    dcs = rng.uniform(-0.5, 1.0, (k, 3))
+    p, cam = _centre_scene(list(logits), list(depths), list(dcs))
+    pr, _, fw = oracle_mod.render(p, [cam])
+    order = np.argsort(depths)  # front to back
+    a = 1 / (1 + np.exp(-logits[order]))
+    cols = np.maximum(0.5 + dcs[order] / (2 * math.sqrt(math.pi)), 0)
+    T = np.concatenate([[1.0], np.cumprod(1 - a)])
+    assert fw["T_final"][0, 33, 20] == pytest.approx(T[-1], rel=1e-13)
+    expect = (cols * (a * T[:-1])[:, None]).sum(0)
+    assert fw["image"][0, :, 33, 20] == pytest.approx(expect, rel=1e-13)
+
+
+def test_two_gaussians_closed_form(oracle_mod):
+    dcs = [np.array([1.0, 0.2, -0.3]), np.array([-0.4, 0.9, 0.5])]
+    p, cam = _centre_scene([0.4, -0.7], [2.0, 5.0], dcs)
+    _, _, fw = oracle_mod.render(p, [cam])
+    a1, a2 = 1 / (1 + math.exp(-0.4)), 1 / (1 + math.exp(0.7))
+    c1, c2 = [np.maximum(0.5 + d / (2 * math.sqrt(math.pi)), 0) for d in dcs]
+    assert fw["image"][0, :, 33, 20] == pytest.approx(a1 * c1 + (1 - a1) * a2 * c2, rel=1e-13)
+
+
+def test_early_termination_excludes_stopping_gaussian(oracle_mod):
+    """alpha 0.85 each: T = 0.15^k; the 5th would take T below 1e-4, so it
+    and everything behind it is excluded."""
+    logit = math.log(0.85 / 0.15)
+    k = 8
+    dcs = [np.array([0.3 * i, 0.1, 0.2]) for i in range(k)]
+    p, cam = _centre_scene([logit] * k, [2.0 + i for i in range(k)], dcs)
+    _, _, fw = oracle_mod.render(p, [cam])
+    a = 0.85
+    cols = [np.maximum(0.5 + d / (2 * math.sqrt(math.pi)), 0) for d in dcs]
+    expect = sum(cols[i] * a * 0.15 ** i for i in range(4))
+    assert fw["n_contrib"][0, 33, 20] == 4
+    assert fw["T_final"][0, 33, 20] == pytest.approx(0.15 ** 4, rel=1e-12)
+    assert fw["image"][0, :, 33, 20] == pytest.approx(expect, rel=1e-12)
+
+
+def test_brute_mode_equals_tiled_mode(oracle_mod):
+    """Block size alters no pixel: per-pixel global (depth, id) order with the
+    footprint test gives exactly the tiled result ("On Scaling Up 3D Gaussian
+    Splatting Training", answer (1) on the pixel block size)."""
+    cfg = scenes.make("tiny_2k_256", n_override=500)
+    cams = cfg["cams"]
+    pr, (keys, vals, ranges), fw = oracle_mod.render(cfg["params"], cams)
+    feats = dict(pr)
+    feats["depth"] = pr["depth"].astype(np.float32).astype(np.float64)
+    bf = oracle_mod.raster_fwd_brute(500, 1, 256, 256, feats)
+    assert np.array_equal(bf["image"], fw["image"])
+    assert np.array_equal(bf["T_final"], fw["T_final"])
+
+
+def test_rigid_motion_invariance(oracle_mod):
+    """Moving the world and the camera by the same rigid motion leaves the
+    image unchanged (degree-0 colour, so SH need no rotation).  Catches a
+    transposed camera rotation or a wrong quaternion convention."""
+    from scipy.spatial.transform import Rotation
+    cfg = scenes.make("tiny_2k_256", n_override=400)
+    p = cfg["params"].astype(np.float64)
+    p[14:] = 0.0
+    cam = cfg["cams"][0]
+    _, _, fw0 = oracle_mod.render(p, [cam])
+    rng = np.random.default_rng(9)
+    Q = Rotation.random(random_state=rng)
+    Qm = Q.as_matrix()
+    tau = rng.uniform(-2, 2, 3)
+    p2 = p.copy()
+    p2[0:3] = Qm @ p[0:3] + tau[:, None]
+    qx, qy, qz, qw = Q.as_quat()
+    w, x, y, z = p[6], p[7], p[8], p[9]
+    p2[6] = qw * w - qx * x - qy * y - qz * z
+    p2[7] = qw * x + qx * w + qy * z - qz * y
+    p2[8] = qw * y - qx * z + qy * w + qz * x
+    p2[9] = qw * z + qx * y - qy * x + qz * w
+    R2 = cam["R"] @ Qm.T
+    cam2 = scenes.camera(R2, cam["t"] - R2 @ tau, cam["fx"], cam["fy"], cam["cx"], cam["cy"],
+                         cam["width"], cam["height"])
+    pr1, _, fw1 = oracle_mod.render(p2, [cam2])
+    ok = pr1["flags"] == 0
+    assert ok.mean() > 0.9
+    assert np.abs(fw1["image"] - fw0["image"]).max() < 1e-9

@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Benchmark of the 3D Gaussian Splatting training step on GB300.
+
+Workload: 3,000,000 Gaussians in 256 clusters, a batch of 4 cameras at
+1920x1080 on a 30 m ring, SH degree 3, L1 loss, dense Adam over the 59
+parameters (the 1080p / 3M-Gaussian configuration the headline metric is
+quoted on).  Synthetic, seeded inputs (no dataset).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` = train iterations/s over the whole
+job; the fwd+bwd compositing rate (Mpix/s) and Gaussians/s are extra keys.
+Multi-GPU runs are independent replicas (the step has no exchange on one
+GPU), so value = N x iterations / max-over-ranks time ("scaling": "weak").
+--impl reference times the CPU oracle (the plain reference implementation of
+the method) on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "ring_3m_4x1080p"
+METRIC = "train iters/s and fwd+bwd Mpix/s at 1080p/3M Gaussians; % HBM roofline"
+UNIT = "iters/s"
+
+# Algorithmic work per unit ("Work per unit").
+FWD_FLOP_TESTED = 13     # per tested pair: dx, dy, power, alpha (+1 exp)
+FWD_FLOP_INCLUDED = 9    # per composited pair: transmittance, weight, colour
+BWD_FLOP_EVAL = 13       # per pair visited below the last contributor (+1 exp)
+BWD_FLOP_INCLUDED = 44   # per contributing pair: gradients of colour, alpha, geometry
+PROJ_READ = 236          # B per Gaussian: 59 fp32 parameters
+SPLAT_BYTES = 48         # B per visible (view, Gaussian) row
+CULLED_BYTES = 8         # B per culled row (radius, tiles)
+ADAM_BYTES = 59 * 28     # B per Gaussian: read p, g, m, v; write p, m, v
+LOSS_BYTES = 36          # B per pixel: image, target read, gradient written (3 channels)
+PROJ_BWD_BYTES = 472     # B per Gaussian: parameters read, gradient written
+PROJ_BWD_ROW = 60        # B per visible row: 36 gradient + 24 conic/colour
+
+FP32_LANES_PER_SM = 128
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("sm_max_mhz", 2070.0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 2070.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the workload
+
+
+def oracle_sample(cfg, gauss_frac, n_tiles, seed, cache):
+    """One training step of the oracle on a bounded sample: projection,
+    binning, projection backward and Adam over a contiguous 1/`1/gauss_frac`
+    block of the Gaussians (their cost is linear in the count), compositing
+    forward and backward on `n_tiles` random non-empty tiles of the full
+    scene's lists (cost per tile).  Returns (extrapolated seconds per full
+    step, detail)."""
+    import numpy as np
+
+    import oracle
+    params = cfg["params"]
+    cams = cfg["cams"]
+    n = params.shape[1]
+    V = len(cams)
+    W, H = cams[0]["width"], cams[0]["height"]
+    if "full" not in cache:  # full lists for the tile sample (set-up, untimed)
+        pr = oracle.project(params.astype(np.float64), cams)
+        keys, vals, ranges = oracle.bin_and_sort(n, V, pr["mean2d"].astype(np.float32),
+                                                 pr["radius"], pr["depth"].astype(np.float32), W, H)
+        cache["full"] = (pr, vals, ranges)
+    pr, vals, ranges = cache["full"]
+    rng = np.random.default_rng(seed)
+    m = max(1, int(n * gauss_frac))
+    a = int(rng.integers(0, n - m + 1))
+    sub = np.ascontiguousarray(params[:, a:a + m].astype(np.float64))
+    t = {}
+    t0 = time.perf_counter()
+    spr = oracle.project(sub, cams)
+    t["project"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.bin_and_sort(m, V, spr["mean2d"].astype(np.float32), spr["radius"],
+                        spr["depth"].astype(np.float32), W, H)
+    t["bin"] = time.perf_counter() - t0
+    nonempty = np.nonzero(ranges[:, 1] > ranges[:, 0])[0]
+    sel = rng.choice(nonempty, min(n_tiles, nonempty.size), replace=False)
+    t0 = time.perf_counter()
+    fw = oracle.raster_fwd(n, V, W, H, pr, vals, ranges, tile_sel=sel)
+    t["raster_fwd"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    loss, g_img = oracle.loss_l1(fw["image"], cfg["target"])
+    t["loss"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    g2 = oracle.raster_bwd(n, V, W, H, pr, vals, ranges, g_img, tile_sel=sel)
+    t["raster_bwd"] = time.perf_counter() - t0
+    sg2 = {k: np.ascontiguousarray(v.reshape(V, n, -1)[:, a:a + m].reshape(V * m, -1).squeeze())
+           for k, v in g2.items()}
+    t0 = time.perf_counter()
+    grad, _ = oracle.project_bwd(sub, cams, sg2)
+    t["project_bwd"] = time.perf_counter() - t0
+    mm, vv = np.zeros_like(sub), np.zeros_like(sub)
+    t0 = time.perf_counter()
+    oracle.adam(sub, grad, mm, vv, 1, cfg["lr"])
+    t["adam"] = time.perf_counter() - t0
+    lin = 1.0 / (m / n)
+    tile_scale = nonempty.size / sel.size
+    full = ((t["project"] + t["bin"] + t["project_bwd"] + t["adam"]) * lin +
+            (t["raster_fwd"] + t["raster_bwd"]) * tile_scale + t["loss"])
+    sample = ("oracle step: projection, binning, projection backward and Adam on %d of %d "
+              "Gaussians (x%.0f), compositing fwd+bwd on %d of %d non-empty tiles (x%.1f), "
+              "L1 loss on the full batch; 1 thread" % (m, n, lin, sel.size, nonempty.size,
+                                                     tile_scale))
+    return full, sum(t.values()), sample, t
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    import scenes
+    cfg = scenes.make(args.workload)
+    cache = {}
+    walls, fulls = [], []
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        full, wall, sample, _ = oracle_sample(cfg, 1.0 / 16, 16, 100 + i, cache)
+        if i >= args.warmup:
+            fulls.append(full)
+            walls.append(wall)
+    sec = sum(fulls) / len(fulls)
+    value = 1.0 / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample, "value": value,
+                             "unit": UNIT},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+
+def our_arm(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import gaussian_splatting_differentiable_gs_gb300 as gs
+    import scenes
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = scenes.make(args.workload)
+    cams = cfg["cams"]
+    V = len(cams)
+    W, H = cams[0]["width"], cams[0]["height"]
+    n = cfg["params"].shape[1]
+    params0 = torch.tensor(cfg["params"], device=dev)
+    target_host = torch.from_numpy(cfg["target"]).pin_memory()
+    target = target_host.to(dev)
+    step = gs.TrainStep(params0.clone(), cams, target, lr=cfg["lr"], sparse=cfg["sparse_adam"])
+    stream = torch.cuda.current_stream()
+    passes = (gs.gs_key_bits(V, W, H) + 7) // 8
+    kernels_per_step = 12 + passes
+
+    # warm-up (sizes the intersection buffers)
+    for _ in range(max(args.warmup, 3)):
+        step.step()
+    torch.cuda.synchronize()
+
+    # work counts of this step (instrumented forward, outside the timed region)
+    counts = torch.zeros(2, dtype=torch.int64, device=dev)
+    step.project()
+    step.bin_and_sort()
+    step.rasterize_fwd(counts=counts)
+    torch.cuda.synchronize()
+    tested, included = [int(x) for x in counts.cpu()]
+    bwd_eval = int(step.n_contrib.to(torch.int64).sum().item())
+    visible_rows = int((step.splats.view(torch.int32)[:, 10] > 0).sum().item())
+    I = step.n_isect
+
+    names = ["project", "bin_and_sort", "rasterize_fwd", "loss_l1", "rasterize_bwd",
+             "project_bwd", "adam"]
+    calls = [step.project, step.bin_and_sort, step.rasterize_fwd, step.loss_l1,
+             step.rasterize_bwd, step.project_bwd, step.adam]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+          for _ in range(args.steps)]
+
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        for i, fn in enumerate(calls):
+            fn()
+            ev[k][i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world)
+    per_kernel = {nm: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
+                  for i, nm in enumerate(names)}
+    ms_step = total_ms / args.steps
+    value = world * args.steps / (total_ms / 1e3)
+
+    # end to end through the public API: pinned host target in, loss out
+    torch.cuda.synchronize()
+    barrier(world)
+    w0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    losses = []
+    for _ in range(args.steps):
+        step.target.copy_(target_host, non_blocking=True)
+        step.step()
+        losses.append(step.loss.item())
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_wall = time.perf_counter() - w0
+    e2e_value = world * args.steps / (e2e_ms / 1e3)
+
+    # roofline accounting
+    hbm_peak, sm_max, peak_kind = peaks()
+    sm_mhz = clock_info["sm_mhz"] if clock_info else sm_max
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    fp32_peak_tflops = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    fwd_flops = FWD_FLOP_TESTED * tested + FWD_FLOP_INCLUDED * included
+    bwd_flops = BWD_FLOP_EVAL * bwd_eval + BWD_FLOP_INCLUDED * included
+    rows = V * n
+    kern = {
+        "rasterize_fwd": ("alu", fwd_flops / 1e12, "TFLOP/s", fp32_peak_tflops),
+        "rasterize_bwd": ("alu", bwd_flops / 1e12, "TFLOP/s", fp32_peak_tflops),
+        "project": ("hbm", (PROJ_READ * n + SPLAT_BYTES * visible_rows +
+                            CULLED_BYTES * (rows - visible_rows)) / 1e9, "GB/s", hbm_peak),
+        "bin_and_sort": ("hbm", (12 * rows + 20 * visible_rows + 12 * I +
+                                 (24 * passes + 8) * I + 8 * I) / 1e9, "GB/s", hbm_peak),
+        "loss_l1": ("hbm", LOSS_BYTES * V * W * H / 1e9, "GB/s", hbm_peak),
+        "project_bwd": ("hbm", (PROJ_BWD_BYTES * n + PROJ_BWD_ROW * visible_rows) / 1e9, "GB/s",
+                        hbm_peak),
+        "adam": ("hbm", ADAM_BYTES * n / 1e9, "GB/s", hbm_peak),
+    }
+    kernels = {}
+    for nm, (bound, work, unit, peak) in kern.items():
+        ach = work / (per_kernel[nm] / 1e3)
+        kernels[nm] = {"ms": round(per_kernel[nm], 4), "bound": bound, "achieved": round(ach, 3),
+                       "peak": round(peak, 2), "unit": unit, "frac": round(ach / peak, 4)}
+    dom = max(kern, key=lambda k: per_kernel[k])
+    d = kernels[dom]
+    roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac"], "traffic": None,
+                "peak_source": (peak_kind + " HBM copy") if d["bound"] == "hbm" else
+                ("FP32 lanes x 2 x median SM clock %.0f MHz, %d SMs" % (sm_mhz, sms))}
+    raster_ms = per_kernel["rasterize_fwd"] + per_kernel["loss_l1"] + per_kernel["rasterize_bwd"]
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "gaussians": n, "views": V, "width": W,
+                       "height": H, "intersections": I, "l2": "inputs larger than L2 "
+                       "(708 MB parameters, 2.1 GB with Adam state)", "adam": "sparse" if
+                       cfg["sparse_adam"] else "dense"},
+            "mpix_per_s": round(V * W * H / (raster_ms / 1e3) / 1e6, 2),
+            "gaussians_per_s": round(n * V / (ms_step / 1e3), 1),
+            "gpu_launches": kernels_per_step * args.steps,
+            "e2e": {"value": round(e2e_value, 4), "unit": UNIT,
+                    "h2d_bytes_per_step": int(target_host.numel() * 4), "d2h_bytes_per_step": 4,
+                    "wall_s": round(e2e_wall, 3)},
+            "roofline": roofline, "kernels": kernels,
+            "work": {"pairs_tested_fwd": tested, "pairs_included": included,
+                     "pairs_bwd": bwd_eval, "visible_rows": visible_rows},
+            "loss_first_last": [round(losses[0], 6), round(losses[-1], 6)],
+            "clocks": clock_info}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        full, wall, sample, _ = oracle_sample(cfg, 1.0 / 8, 64, 7, {})
+        line["cpu_baseline"] = {"value": 1.0 / full, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": sample, "sample_wall_s": round(wall, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        our_arm(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

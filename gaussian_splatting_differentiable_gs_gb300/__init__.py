@@ -1,0 +1,330 @@
+"""GB300 (sm_103a) 3D Gaussian Splatting training step.
+
+Python binding of libgs103.so (include/gs.h).  Each gs_* function here only
+marshals arguments -- torch tensors to device pointers, camera dicts to the
+C struct, the current CUDA stream -- and calls the C ABI function of the same
+name; every step of the computation runs in the library's CUDA kernels.
+PyTorch provides device memory and streams only.
+
+There is no fallback: if libgs103.so is missing or cannot be loaded, every
+call raises GSError (run `python -c "import __graft_entry__ as g; g.build()"`
+or `python gaussian_splatting_differentiable_gs_gb300/build.py`).
+"""
+import ctypes as C
+import math
+import os
+
+import torch
+
+NPARAM = 59
+TILE = 16
+MAX_VIEWS = 16
+SPLAT_FLOATS = 12  # 48-byte gs_splat / gs_splat_grad records
+
+GS_OK, GS_ERR_INVALID_ARG, GS_ERR_CAPACITY, GS_ERR_TIMEOUT, GS_ERR_CUDA, GS_ERR_DEVICE_CHECK = range(6)
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgs103.so")
+
+
+class GSError(RuntimeError):
+    def __init__(self, what, status):
+        super().__init__("%s failed: %s (status %d)" % (what, status_string(status), status))
+        self.status = status
+
+
+class Camera(C.Structure):
+    _fields_ = [("R", C.c_float * 9), ("t", C.c_float * 3), ("fx", C.c_float), ("fy", C.c_float),
+                ("cx", C.c_float), ("cy", C.c_float), ("width", C.c_int32),
+                ("height", C.c_int32), ("near_z", C.c_float), ("far_z", C.c_float)]
+
+
+_lib = None
+
+
+def lib():
+    """Loads libgs103.so once; raises GSError-like RuntimeError if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libgs103.so not built: %s is missing (run build())" % LIB_PATH)
+    L = C.CDLL(LIB_PATH)
+    vp, i64, i32, f32, sz = C.c_void_p, C.c_int64, C.c_int32, C.c_float, C.c_size_t
+    L.gs_project.argtypes = [i64, vp, vp, i32, vp, vp]
+    L.gs_bin_workspace_bytes.argtypes = [i64, i64]
+    L.gs_bin_workspace_bytes.restype = sz
+    L.gs_key_bits.argtypes = [i32, i32, i32]
+    L.gs_key_bits.restype = i32
+    L.gs_bin_and_sort.argtypes = [i64, i32, vp, i32, i32, vp, sz, i64, vp, vp, vp, vp, vp]
+    L.gs_workspace_status.argtypes = [vp, vp]
+    L.gs_rasterize_fwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+    L.gs_rasterize_fwd_counted.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.gs_loss_l1.argtypes = [vp, vp, i64, vp, vp, vp]
+    L.gs_rasterize_bwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp]
+    L.gs_adam_step.argtypes = [i64, vp, vp, vp, vp, i64, f32, f32, f32, f32, vp, vp]
+    L.gs_status_string.argtypes = [C.c_int]
+    L.gs_status_string.restype = C.c_char_p
+    L.gs_version.restype = i32
+    for name in ("gs_project", "gs_bin_and_sort", "gs_workspace_status", "gs_rasterize_fwd",
+                 "gs_rasterize_fwd_counted", "gs_loss_l1", "gs_rasterize_bwd", "gs_project_bwd", "gs_adam_step"):
+        getattr(L, name).restype = C.c_int
+    _lib = L
+    return L
+
+
+def status_string(status):
+    return lib().gs_status_string(int(status)).decode()
+
+
+def version():
+    return int(lib().gs_version())
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+
+
+def cameras_struct(cams):
+    if not 1 <= len(cams) <= MAX_VIEWS:
+        raise ValueError("1..%d cameras" % MAX_VIEWS)
+    arr = (Camera * len(cams))()
+    for i, c in enumerate(cams):
+        R = [float(v) for v in torch.as_tensor(c["R"], dtype=torch.float64).reshape(9)]
+        t = [float(v) for v in torch.as_tensor(c["t"], dtype=torch.float64).reshape(3)]
+        arr[i].R[:] = R
+        arr[i].t[:] = t
+        arr[i].fx, arr[i].fy = float(c["fx"]), float(c["fy"])
+        arr[i].cx, arr[i].cy = float(c["cx"]), float(c["cy"])
+        arr[i].width, arr[i].height = int(c["width"]), int(c["height"])
+        arr[i].near_z = float(c["near_z"])
+        arr[i].far_z = float(c["far_z"]) if math.isfinite(float(c["far_z"])) else float("inf")
+    return arr
+
+
+def _dev(t, dtype, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _check(what, status):
+    if status != GS_OK:
+        raise GSError(what, status)
+
+
+def tiles_per_view(width, height):
+    return ((width + TILE - 1) // TILE) * ((height + TILE - 1) // TILE)
+
+
+# --------------------------------------------------------------------------
+# the C ABI, one wrapper per function
+
+
+def gs_project(params, cams, splats, stream=None):
+    n = params.shape[1]
+    cs = cameras_struct(cams)
+    _check("gs_project", lib().gs_project(n, _dev(params, torch.float32, "params"), C.cast(cs, C.c_void_p),
+                                          len(cams), _dev(splats, torch.float32, "splats"),
+                                          _stream(stream)))
+
+
+def gs_bin_workspace_bytes(n_rows, capacity):
+    return int(lib().gs_bin_workspace_bytes(n_rows, capacity))
+
+
+def gs_key_bits(n_views, width, height):
+    return int(lib().gs_key_bits(n_views, width, height))
+
+
+def gs_bin_and_sort(n, n_views, splats, width, height, workspace, capacity, keys, vals, ranges,
+                    stream=None):
+    """Returns (status, n_isect); status is GS_OK or GS_ERR_CAPACITY, other
+    statuses raise GSError."""
+    out = C.c_int64(0)
+    st = lib().gs_bin_and_sort(n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+                               _dev(workspace, torch.uint8, "workspace"), workspace.numel(), capacity,
+                               _dev(keys, torch.int64, "keys"), _dev(vals, torch.int32, "vals"),
+                               _dev(ranges, torch.int64, "ranges"), C.byref(out), _stream(stream))
+    if st not in (GS_OK, GS_ERR_CAPACITY):
+        raise GSError("gs_bin_and_sort", st)
+    return st, int(out.value)
+
+
+def gs_workspace_status(workspace, stream=None):
+    return int(lib().gs_workspace_status(_dev(workspace, torch.uint8, "workspace"), _stream(stream)))
+
+
+def gs_rasterize_fwd(n, n_views, splats, width, height, vals, ranges, bg, image, T_final, n_contrib,
+                     stream=None):
+    bgv = (C.c_float * 3)(*[float(b) for b in bg])
+    _check("gs_rasterize_fwd", lib().gs_rasterize_fwd(
+        n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(image, torch.float32, "image"), _dev(T_final, torch.float32, "T_final"),
+        _dev(n_contrib, torch.int32, "n_contrib"), _stream(stream)))
+
+
+def gs_rasterize_fwd_counted(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
+                             n_contrib, counts, stream=None):
+    bgv = (C.c_float * 3)(*[float(b) for b in bg])
+    _check("gs_rasterize_fwd_counted", lib().gs_rasterize_fwd_counted(
+        n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(image, torch.float32, "image"), _dev(T_final, torch.float32, "T_final"),
+        _dev(n_contrib, torch.int32, "n_contrib"), _dev(counts, torch.int64, "counts"),
+        _stream(stream)))
+
+
+def gs_loss_l1(image, target, loss, dL_dimage, stream=None):
+    _check("gs_loss_l1", lib().gs_loss_l1(_dev(image, torch.float32, "image"),
+                                          _dev(target, torch.float32, "target"), image.numel(),
+                                          _dev(loss, torch.float32, "loss"),
+                                          _dev(dL_dimage, torch.float32, "dL_dimage"),
+                                          _stream(stream)))
+
+
+def gs_rasterize_bwd(n, n_views, splats, width, height, vals, ranges, bg, T_final, n_contrib,
+                     dL_dimage, grads, stream=None):
+    bgv = (C.c_float * 3)(*[float(b) for b in bg])
+    _check("gs_rasterize_bwd", lib().gs_rasterize_bwd(
+        n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(T_final, torch.float32, "T_final"), _dev(n_contrib, torch.int32, "n_contrib"),
+        _dev(dL_dimage, torch.float32, "dL_dimage"), _dev(grads, torch.float32, "grads"),
+        _stream(stream)))
+
+
+def gs_project_bwd(params, cams, splats, grads, grad, visible=None, stream=None):
+    n = params.shape[1]
+    cs = cameras_struct(cams)
+    _check("gs_project_bwd", lib().gs_project_bwd(
+        n, _dev(params, torch.float32, "params"), C.cast(cs, C.c_void_p), len(cams),
+        _dev(splats, torch.float32, "splats"), _dev(grads, torch.float32, "grads"),
+        _dev(grad, torch.float32, "grad"), _dev(visible, torch.uint8, "visible"), _stream(stream)))
+
+
+def gs_adam_step(params, grad, m, v, step, lr, beta1=0.9, beta2=0.999, eps=1e-8, visible=None,
+                 stream=None):
+    n = params.shape[1]
+    _check("gs_adam_step", lib().gs_adam_step(
+        n, _dev(params, torch.float32, "params"), _dev(grad, torch.float32, "grad"),
+        _dev(m, torch.float32, "m"), _dev(v, torch.float32, "v"), int(step), float(lr),
+        float(beta1), float(beta2), float(eps), _dev(visible, torch.uint8, "visible"),
+        _stream(stream)))
+
+
+# --------------------------------------------------------------------------
+# buffers + one training step, in call order
+
+
+class TrainStep:
+    """Owns the device buffers of one training problem (allocated through
+    torch) and runs the seven library calls of a step in order.
+
+    params: CUDA float32 [59][n]; target: CUDA float32 [V][3][H][W].
+    sparse: use the visibility-masked Adam update."""
+
+    def __init__(self, params, cams, target, lr=1e-3, betas=(0.9, 0.999), eps=1e-8,
+                 sparse=False, bg=(0.0, 0.0, 0.0), capacity=None):
+        lib()
+        dev = params.device
+        self.params = params
+        self.cams = list(cams)
+        self.V = len(cams)
+        self.n = params.shape[1]
+        self.W, self.H = int(cams[0]["width"]), int(cams[0]["height"])
+        self.T = tiles_per_view(self.W, self.H)
+        self.target = target
+        self.lr, self.betas, self.eps, self.sparse, self.bg = lr, betas, eps, sparse, tuple(bg)
+        rows = self.V * self.n
+        f32 = dict(device=dev, dtype=torch.float32)
+        self.splats = torch.empty((rows, SPLAT_FLOATS), **f32)
+        self.grads2d = torch.empty((rows, SPLAT_FLOATS), **f32)
+        self.grad = torch.empty_like(params)
+        self.m = torch.zeros_like(params)
+        self.v = torch.zeros_like(params)
+        self.visible = torch.zeros(self.n, device=dev, dtype=torch.uint8)
+        self.image = torch.empty((self.V, 3, self.H, self.W), **f32)
+        self.dL_dimage = torch.empty_like(self.image)
+        self.T_final = torch.empty((self.V, self.H, self.W), **f32)
+        self.n_contrib = torch.empty((self.V, self.H, self.W), device=dev, dtype=torch.int32)
+        self.loss = torch.zeros(1, **f32)
+        self.ranges = torch.empty((self.V * self.T, 2), device=dev, dtype=torch.int64)
+        self.t = 0
+        self.n_isect = 0
+        self._alloc_isect(capacity if capacity is not None else max(1024, 4 * rows))
+
+    def _alloc_isect(self, capacity):
+        dev = self.params.device
+        self.capacity = int(capacity)
+        self.keys = torch.empty(max(self.capacity, 1), device=dev, dtype=torch.int64)
+        self.vals = torch.empty(max(self.capacity, 1), device=dev, dtype=torch.int32)
+        ws = gs_bin_workspace_bytes(self.V * self.n, self.capacity)
+        self.workspace = torch.empty(ws, device=dev, dtype=torch.uint8)
+
+    # the seven library calls of a step, in order
+    def project(self, stream=None):
+        gs_project(self.params, self.cams, self.splats, stream)
+
+    def bin_and_sort(self, stream=None):
+        st, I = gs_bin_and_sort(self.n, self.V, self.splats, self.W, self.H, self.workspace,
+                                self.capacity, self.keys, self.vals, self.ranges, stream)
+        if st == GS_ERR_CAPACITY:
+            self._alloc_isect(int(I * 1.25) + 1024)
+            st, I = gs_bin_and_sort(self.n, self.V, self.splats, self.W, self.H, self.workspace,
+                                    self.capacity, self.keys, self.vals, self.ranges, stream)
+            _check("gs_bin_and_sort", st)
+        self.n_isect = I
+
+    def rasterize_fwd(self, stream=None, counts=None):
+        if counts is None:
+            gs_rasterize_fwd(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges,
+                             self.bg, self.image, self.T_final, self.n_contrib, stream)
+        else:
+            gs_rasterize_fwd_counted(self.n, self.V, self.splats, self.W, self.H, self.vals,
+                                     self.ranges, self.bg, self.image, self.T_final, self.n_contrib,
+                                     counts, stream)
+
+    def loss_l1(self, stream=None):
+        gs_loss_l1(self.image, self.target, self.loss, self.dL_dimage, stream)
+
+    def rasterize_bwd(self, stream=None):
+        gs_rasterize_bwd(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges, self.bg,
+                         self.T_final, self.n_contrib, self.dL_dimage, self.grads2d, stream)
+
+    def project_bwd(self, stream=None):
+        gs_project_bwd(self.params, self.cams, self.splats, self.grads2d, self.grad, self.visible,
+                       stream)
+
+    def adam(self, stream=None):
+        self.t += 1
+        gs_adam_step(self.params, self.grad, self.m, self.v, self.t, self.lr, self.betas[0],
+                     self.betas[1], self.eps, self.visible if self.sparse else None, stream)
+
+    def forward(self, stream=None):
+        self.project(stream)
+        self.bin_and_sort(stream)
+        self.rasterize_fwd(stream)
+        return self.image
+
+    def backward(self, stream=None):
+        self.loss_l1(stream)
+        self.rasterize_bwd(stream)
+        self.project_bwd(stream)
+
+    def update(self, stream=None):
+        self.adam(stream)
+
+    def step(self, stream=None):
+        self.forward(stream)
+        self.backward(stream)
+        self.update(stream)
+        return self.loss

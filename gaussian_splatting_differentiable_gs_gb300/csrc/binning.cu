@@ -1,0 +1,543 @@
+// binning.cu -- gs_bin_and_sort: per-tile depth-sorted intersection lists.
+//
+// "per-tile sorted lists of Gaussian-to-pixel intersections" ("AMD ROCm team
+// open-sources distributed 3D Gaussian Splatting training", per-tile
+// intersection bullet).  Stages, all in-house kernels:
+//   1. single-pass exclusive scan of the per-row tile counts with decoupled
+//      look-back (Merrill & Garland, cited in "A Scalable PyTorch Abstraction
+//      for Multi-GPU Gaussian Splatting", references);
+//   2. key emission, one thread per projected row;
+//   3. one histogram pass giving the digit counts of every radix pass;
+//   4. stable LSD radix sort, 8-bit digits, one kernel per pass that ranks its
+//      partition, resolves the partition's global digit offsets by decoupled
+//      look-back and scatters ("onesweep"; radix sorting per Merrill &
+//      Grimshaw, same reference list);
+//   5. tile range extraction.
+//
+// Device waits: the look-backs are the only waits.  Each partition takes its
+// index from an atomic ticket, so it only ever waits for partitions that are
+// already running.  Every wait is bounded; when a bound is hit the partition
+// publishes an error flag (successors propagate it), writes nothing, sets
+// the workspace status word and returns.
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gs_internal.cuh"
+
+namespace gs {
+namespace {
+
+constexpr int kScanThreads = 256;
+constexpr int kScanItems = 8;
+constexpr int kScanPart = kScanThreads * kScanItems;   // rows per scan partition
+
+constexpr int kSortThreads = 256;
+constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSortKpt = 16;                            // keys per thread
+constexpr int kSortPart = kSortThreads * kSortKpt;      // keys per sort partition
+constexpr int kRadix = 256;
+constexpr int kMaxPasses = 8;
+
+constexpr uint32_t kSpinLimit = 1u << 22;               // x ~100 ns sleep: >0.4 s
+
+constexpr uint64_t kFlagAgg = 1, kFlagInc = 2, kFlagErr = 3;
+
+// Workspace header, at offset 0 of the caller's workspace.
+struct WsHeader {
+  unsigned long long total;        // intersections I (written by the scan)
+  unsigned int error;              // sticky device status (0 = ok)
+  unsigned int scan_ticket;
+  unsigned int pass_ticket[kMaxPasses];
+  unsigned int pad[52];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+struct WsLayout {
+  size_t hist, digit_start, offsets, scan_status, sort_status, keys_alt, vals_alt, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int64_t n_rows, int64_t capacity) {
+  WsLayout L;
+  size_t off = sizeof(WsHeader);
+  L.hist = off;        off += align256(sizeof(uint32_t) * kMaxPasses * kRadix);
+  L.digit_start = off; off += align256(sizeof(uint32_t) * kMaxPasses * kRadix);
+  L.offsets = off;     off += align256(sizeof(int64_t) * (size_t)(n_rows > 0 ? n_rows : 1));
+  L.scan_status = off; off += align256(sizeof(uint64_t) * (size_t)div_up(n_rows > 0 ? n_rows : 1, kScanPart));
+  L.sort_status = off;
+  off += align256(sizeof(uint64_t) * kRadix * (size_t)div_up(capacity > 0 ? capacity : 1, kSortPart));
+  L.keys_alt = off;    off += align256(sizeof(uint64_t) * (size_t)(capacity > 0 ? capacity : 1));
+  L.vals_alt = off;    off += align256(sizeof(uint32_t) * (size_t)(capacity > 0 ? capacity : 1));
+  L.total = off;
+  return L;
+}
+
+__device__ __forceinline__ uint64_t ld_volatile(const uint64_t* p) {
+  return *reinterpret_cast<const volatile uint64_t*>(p);
+}
+__device__ __forceinline__ void st_volatile(uint64_t* p, uint64_t v) {
+  *reinterpret_cast<volatile uint64_t*>(p) = v;
+}
+
+// ---------------------------------------------------------------------------
+// 1. scan of tile counts -> inclusive int64 offsets, total I.
+// Scan status word: value << 2 | flag.
+__global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(
+    int64_t n_rows, const int4* __restrict__ splat_tail, int64_t* __restrict__ offsets,
+    uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
+  __shared__ int s_part;
+  __shared__ long long s_warp[kScanThreads / 32];
+  __shared__ long long s_prefix;
+  __shared__ int s_err;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_part = (int)atomicAdd(&hdr->scan_ticket, 1u);
+    s_err = 0;
+  }
+  __syncthreads();
+  const int64_t part = s_part;
+  const int64_t base = part * kScanPart + (int64_t)tid * kScanItems;
+  int64_t v[kScanItems];
+  long long sum = 0;
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t r = base + i;
+    // the tile count is the 4th word of the record's last 16 bytes
+    v[i] = r < n_rows ? (int64_t)splat_tail[3 * r + 2].w : 0;
+    sum += v[i];
+  }
+  // block-wide inclusive scan of the per-thread sums
+  long long incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < kScanThreads / 32 ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kScanThreads / 32) s_warp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const long long block_total = s_warp[kScanThreads / 32 - 1];
+  const long long thread_excl = incl - sum + (warp > 0 ? s_warp[warp - 1] : 0);
+  // decoupled look-back (thread 0)
+  if (tid == 0) {
+    long long prefix = 0;
+    if (part == 0) {
+      st_volatile(&status[0], ((uint64_t)block_total << 2) | kFlagInc);
+    } else {
+      st_volatile(&status[part], ((uint64_t)block_total << 2) | kFlagAgg);
+      int64_t j = part - 1;
+      bool err = false;
+      while (j >= 0) {
+        uint64_t s;
+        uint32_t spins = 0;
+        while (((s = ld_volatile(&status[j])) & 3u) == 0) {
+          if (++spins > kSpinLimit) break;
+          __nanosleep(100);
+        }
+        const uint64_t f = s & 3u;
+        if (f == 0 || f == kFlagErr) { err = true; break; }
+        prefix += (long long)(s >> 2);
+        if (f == kFlagInc) break;
+        --j;
+      }
+      if (err) {
+        st_volatile(&status[part], kFlagErr);
+        atomicOr(&hdr->error, 1u);
+        s_err = 1;
+      } else {
+        __threadfence();
+        st_volatile(&status[part], ((uint64_t)(prefix + block_total) << 2) | kFlagInc);
+      }
+    }
+    s_prefix = prefix;
+    if (!s_err && (part + 1) * kScanPart >= n_rows) hdr->total = (unsigned long long)(prefix + block_total);
+  }
+  __syncthreads();
+  if (s_err) return;
+  long long run = s_prefix + thread_excl;
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    run += v[i];
+    if (base + i < n_rows) offsets[base + i] = run;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. emission of (key, id) pairs, one thread per row.
+// A row whose rectangle disagrees with its stored tile count (records not
+// produced by gs_project) writes nothing and raises the device-check bit, so
+// emission never leaves the row's scanned slot range.
+__global__ void __launch_bounds__(256) emit_kernel(int64_t n, int64_t n_rows, int32_t tiles_x,
+                                                   int32_t tiles_y, int64_t T,
+                                                   const float4* __restrict__ splats,
+                                                   const int64_t* __restrict__ offsets,
+                                                   uint64_t* __restrict__ keys,
+                                                   uint32_t* __restrict__ vals,
+                                                   WsHeader* __restrict__ hdr) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_rows) return;
+  const float4 tail = splats[3 * r + 2];
+  const int32_t tiles = __float_as_int(tail.w);
+  if (tiles <= 0) return;
+  const float4 head = splats[3 * r];
+  const int32_t radius = __float_as_int(tail.z);
+  int32_t x0, x1, y0, y1;
+  tile_rect(head.x, head.y, radius, tiles_x, tiles_y, x0, x1, y0, y1);
+  if ((int64_t)(x1 - x0) * (y1 - y0) != tiles) {
+    atomicOr(&hdr->error, 2u);
+    return;
+  }
+  const int64_t view = r / n;
+  const uint32_t g = (uint32_t)(r - view * n);
+  const uint64_t dbits = (uint64_t)__float_as_uint(tail.y);
+  int64_t o = offsets[r] - tiles;
+  for (int32_t ty = y0; ty < y1; ++ty)
+    for (int32_t tx = x0; tx < x1; ++tx) {
+      const uint64_t flat = (uint64_t)(view * T + (int64_t)ty * tiles_x + tx);
+      keys[o] = (flat << 32) | dbits;
+      vals[o] = g;
+      ++o;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 3. digit histograms of every pass in one read of the keys.
+__global__ void __launch_bounds__(256) hist_kernel(int64_t count, int32_t passes,
+                                                   const uint64_t* __restrict__ keys,
+                                                   uint32_t* __restrict__ hist) {
+  __shared__ uint32_t sh[kMaxPasses * kRadix];
+  for (int i = threadIdx.x; i < kMaxPasses * kRadix; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t base = warp_global * 32; base < count; base += nwarps * 32) {
+    const int64_t i = base + lane;
+    const bool valid = i < count;
+    const uint64_t k = valid ? keys[i] : 0;
+    for (int p = 0; p < passes; ++p) {
+      const uint32_t d = valid ? (uint32_t)((k >> (8 * p)) & 0xFF) : 256u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      if (d < 256u && lane == __ffs(peers) - 1) atomicAdd(&sh[p * kRadix + d], __popc(peers));
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x)
+    if (sh[i]) atomicAdd(&hist[i], sh[i]);
+}
+
+// exclusive scan of each pass's 256 digit counts; one block per pass
+__global__ void __launch_bounds__(kRadix) hist_scan_kernel(const uint32_t* __restrict__ hist,
+                                                           uint32_t* __restrict__ digit_start) {
+  __shared__ uint32_t s_w[kRadix / 32];
+  const int p = blockIdx.x, d = threadIdx.x, lane = d & 31, warp = d >> 5;
+  const uint32_t c = hist[p * kRadix + d];
+  uint32_t incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  uint32_t add = 0;
+  for (int w = 0; w < warp; ++w) add += s_w[w];
+  digit_start[p * kRadix + d] = add + incl - c;
+}
+
+// ---------------------------------------------------------------------------
+// 4. one stable radix pass (onesweep).  Sort status word:
+//    value << 8 | tag << 2 | flag, tag = pass + 1 (stale entries of an earlier
+//    pass read as not ready).
+struct SortSmem {
+  uint32_t warp_hist[kSortWarps][kRadix];
+  uint32_t local_start[kRadix];
+  unsigned long long global_base[kRadix];
+  uint32_t scan_w[kSortWarps];
+  int part;
+  int err;
+  uint64_t keys[kSortPart];
+  uint32_t vals[kSortPart];
+};
+
+__global__ void __launch_bounds__(kSortThreads) onesweep_kernel(
+    int64_t count, int32_t pass, const uint64_t* __restrict__ keys_in,
+    const uint32_t* __restrict__ vals_in, uint64_t* __restrict__ keys_out,
+    uint32_t* __restrict__ vals_out, const uint32_t* __restrict__ digit_start,
+    uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SortSmem& S = *reinterpret_cast<SortSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int shift = 8 * pass;
+  const uint64_t tag = (uint64_t)(pass + 1) << 2;
+  for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&S.warp_hist[0][0])[i] = 0;
+  if (tid == 0) {
+    S.part = (int)atomicAdd(&hdr->pass_ticket[pass], 1u);
+    S.err = 0;
+  }
+  __syncthreads();
+  const int64_t part = S.part;
+  const int64_t pbase = part * kSortPart;
+  const int64_t wbase = pbase + (int64_t)warp * 32 * kSortKpt;
+  // load (warp-striped: item i of lane l is element wbase + 32 i + l) and rank
+  uint64_t key[kSortKpt];
+  uint32_t val[kSortKpt];
+  uint32_t rank[kSortKpt];
+#pragma unroll
+  for (int i = 0; i < kSortKpt; ++i) {
+    const int64_t idx = wbase + 32 * i + lane;
+    const bool valid = idx < count;
+    key[i] = valid ? keys_in[idx] : 0ull;
+    val[i] = valid ? vals_in[idx] : 0u;
+  }
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < kSortKpt; ++i) {
+    const int64_t idx = wbase + 32 * i + lane;
+    const uint32_t d = idx < count ? (uint32_t)((key[i] >> shift) & 0xFF) : 256u;
+    const uint32_t peers = __match_any_sync(0xffffffffu, d);
+    uint32_t basec = 0;
+    if (d < 256u) basec = S.warp_hist[warp][d];
+    __syncwarp();
+    if (d < 256u && lane == __ffs(peers) - 1) S.warp_hist[warp][d] = basec + __popc(peers);
+    __syncwarp();
+    rank[i] = basec + __popc(peers & lt_mask);
+  }
+  __syncthreads();
+  // per digit: exclusive prefix over warps, partition count
+  const int d = tid;  // kSortThreads == kRadix
+  uint32_t run = 0;
+#pragma unroll
+  for (int w = 0; w < kSortWarps; ++w) {
+    const uint32_t c = S.warp_hist[w][d];
+    S.warp_hist[w][d] = run;
+    run += c;
+  }
+  const uint32_t my_count = run;
+  // publish the aggregate before anything else, so successors can proceed
+  if (part == 0)
+    st_volatile(&status[d], ((uint64_t)my_count << 8) | tag | kFlagInc);
+  else
+    st_volatile(&status[part * kRadix + d], ((uint64_t)my_count << 8) | tag | kFlagAgg);
+  // exclusive scan of counts over digits -> local start of each digit
+  {
+    uint32_t incl = my_count;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) S.scan_w[warp] = incl;
+    __syncthreads();
+    uint32_t add = 0;
+    for (int w = 0; w < warp; ++w) add += S.scan_w[w];
+    S.local_start[d] = add + incl - my_count;
+  }
+  // look back for this digit
+  unsigned long long excl = 0;
+  if (part > 0) {
+    int64_t j = part - 1;
+    bool err = false;
+    while (j >= 0) {
+      uint64_t s;
+      uint32_t spins = 0;
+      for (;;) {
+        s = ld_volatile(&status[j * kRadix + d]);
+        const uint64_t f = s & 3u;
+        if (f == kFlagErr) break;
+        if (f != 0 && (s & 0xFCu) == tag) break;
+        if (++spins > kSpinLimit) { s = kFlagErr; break; }
+        __nanosleep(100);
+      }
+      const uint64_t f = s & 3u;
+      if (f == kFlagErr) { err = true; break; }
+      excl += (unsigned long long)(s >> 8);
+      if (f == kFlagInc) break;
+      --j;
+    }
+    if (err) {
+      st_volatile(&status[part * kRadix + d], tag | kFlagErr);
+      atomicOr(&hdr->error, 1u);
+      S.err = 1;
+    } else {
+      st_volatile(&status[part * kRadix + d], ((uint64_t)(excl + my_count) << 8) | tag | kFlagInc);
+    }
+  }
+  S.global_base[d] = (unsigned long long)digit_start[pass * kRadix + d] + excl;
+  __syncthreads();
+  if (S.err) return;
+  // place the partition in smem in sorted (digit-major, stable) order
+#pragma unroll
+  for (int i = 0; i < kSortKpt; ++i) {
+    const int64_t idx = wbase + 32 * i + lane;
+    if (idx < count) {
+      const uint32_t dd = (uint32_t)((key[i] >> shift) & 0xFF);
+      const uint32_t pos = S.local_start[dd] + S.warp_hist[warp][dd] + rank[i];
+      S.keys[pos] = key[i];
+      S.vals[pos] = val[i];
+    }
+  }
+  __syncthreads();
+  const int64_t n_here = count - pbase < kSortPart ? count - pbase : kSortPart;
+  for (int j = tid; j < n_here; j += kSortThreads) {
+    const uint64_t k = S.keys[j];
+    const uint32_t dd = (uint32_t)((k >> shift) & 0xFF);
+    const unsigned long long gpos = S.global_base[dd] + (unsigned long long)(j - S.local_start[dd]);
+    if (gpos < (unsigned long long)count) {
+      keys_out[gpos] = k;
+      vals_out[gpos] = S.vals[j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 5. [first, last + 1) of each (view, tile) in the sorted keys.
+__global__ void __launch_bounds__(256) ranges_kernel(int64_t count, uint64_t n_flat,
+                                                     const uint64_t* __restrict__ keys,
+                                                     int64_t* __restrict__ ranges) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const uint64_t f = keys[i] >> 32;
+  if (f >= n_flat) return;
+  if (i == 0 || (keys[i - 1] >> 32) != f) ranges[2 * f] = i;
+  if (i == count - 1 || (keys[i + 1] >> 32) != f) ranges[2 * f + 1] = i + 1;
+}
+
+int bit_length(uint64_t v) {
+  int b = 0;
+  while (v) { ++b; v >>= 1; }
+  return b;
+}
+
+}  // namespace
+}  // namespace gs
+
+using namespace gs;
+
+extern "C" size_t gs_bin_workspace_bytes(int64_t n_rows, int64_t capacity) {
+  if (n_rows < 0 || capacity < 0) return 0;
+  return ws_layout(n_rows, capacity).total;
+}
+
+extern "C" int32_t gs_key_bits(int32_t n_views, int32_t width, int32_t height) {
+  if (n_views < 1 || width < 1 || height < 1) return 0;
+  const int64_t flat = (int64_t)n_views * tiles_per_view(width, height);
+  const int b = bit_length((uint64_t)(flat - 1));
+  return 32 + (b > 0 ? b : 1);
+}
+
+extern "C" gs_status gs_workspace_status(void* workspace, void* stream) {
+  if (!workspace) return GS_ERR_INVALID_ARG;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
+  unsigned int err = 0;
+  GS_CUDA(cudaMemcpyAsync(&err, &hdr->error, sizeof(err), cudaMemcpyDeviceToHost,
+                          (cudaStream_t)stream));
+  GS_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  if (err) {
+    GS_CUDA(cudaMemsetAsync(&hdr->error, 0, sizeof(unsigned int), (cudaStream_t)stream));
+    return (err & 1u) ? GS_ERR_TIMEOUT : GS_ERR_DEVICE_CHECK;
+  }
+  return GS_OK;
+}
+
+extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat* splats,
+                                     int32_t width, int32_t height, void* workspace,
+                                     size_t ws_bytes, int64_t capacity, uint64_t* keys,
+                                     uint32_t* vals, int64_t* ranges, int64_t* n_isect,
+                                     void* stream) {
+  if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
+      height < 1 || capacity < 0 || capacity > (int64_t)0xFFFFFFFFll || !n_isect || !workspace)
+    return GS_ERR_INVALID_ARG;
+  const int64_t n_rows = n * n_views;
+  const WsLayout L = ws_layout(n_rows, capacity);
+  if (ws_bytes < L.total || !aligned16(workspace)) return GS_ERR_INVALID_ARG;
+  if (!ranges || (n_rows > 0 && (!splats || !aligned16(splats))) ||
+      (capacity > 0 && (!keys || !vals)))
+    return GS_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  uint32_t* digit_start = reinterpret_cast<uint32_t*>(ws + L.digit_start);
+  int64_t* offsets = reinterpret_cast<int64_t*>(ws + L.offsets);
+  uint64_t* scan_status = reinterpret_cast<uint64_t*>(ws + L.scan_status);
+  uint64_t* sort_status = reinterpret_cast<uint64_t*>(ws + L.sort_status);
+  uint64_t* keys_alt = reinterpret_cast<uint64_t*>(ws + L.keys_alt);
+  uint32_t* vals_alt = reinterpret_cast<uint32_t*>(ws + L.vals_alt);
+  const int64_t T = tiles_per_view(width, height);
+  const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE, tiles_y = (height + GS_TILE - 1) / GS_TILE;
+  if (n_views * T > (int64_t)0xFFFFFFFFll) return GS_ERR_INVALID_ARG;  // flat index in 32 key bits
+
+  // 1. scan (tickets, total and histograms reset; the status word is kept)
+  GS_CUDA(cudaMemsetAsync(&hdr->scan_ticket, 0, sizeof(WsHeader) - offsetof(WsHeader, scan_ticket), st));
+  GS_CUDA(cudaMemsetAsync(&hdr->total, 0, sizeof(hdr->total), st));
+  GS_CUDA(cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, st));
+  const int64_t scan_parts = div_up(n_rows, kScanPart);
+  if (n_rows > 0) {
+    GS_CUDA(cudaMemsetAsync(scan_status, 0, sizeof(uint64_t) * (size_t)scan_parts, st));
+    scan_tiles_kernel<<<(unsigned)scan_parts, kScanThreads, 0, st>>>(
+        n_rows, reinterpret_cast<const int4*>(splats), offsets, scan_status, hdr);
+    GS_CHECK_LAUNCH();
+  }
+  struct { unsigned long long total; unsigned int error; unsigned int pad; } h{};
+  GS_CUDA(cudaMemcpyAsync(&h, hdr, 16, cudaMemcpyDeviceToHost, st));
+  GS_CUDA(cudaStreamSynchronize(st));
+  if (h.error) {
+    GS_CUDA(cudaMemsetAsync(&hdr->error, 0, sizeof(unsigned int), st));
+    return (h.error & 1u) ? GS_ERR_TIMEOUT : GS_ERR_DEVICE_CHECK;
+  }
+  const int64_t I = (int64_t)h.total;
+  *n_isect = I;
+  if (I > capacity) return GS_ERR_CAPACITY;
+  GS_CUDA(cudaMemsetAsync(ranges, 0, sizeof(int64_t) * 2 * (size_t)(n_views * T), st));
+  if (I == 0) return GS_OK;
+
+  // 2. emission into the buffer that ends up holding the sorted result
+  const int passes = (gs_key_bits(n_views, width, height) + 7) / 8;
+  uint64_t* k_a = (passes % 2 == 0) ? keys : keys_alt;
+  uint32_t* v_a = (passes % 2 == 0) ? vals : vals_alt;
+  uint64_t* k_b = (passes % 2 == 0) ? keys_alt : keys;
+  uint32_t* v_b = (passes % 2 == 0) ? vals_alt : vals;
+  emit_kernel<<<(unsigned)div_up(n_rows, 256), 256, 0, st>>>(n, n_rows, tiles_x, tiles_y, T,
+                                                              reinterpret_cast<const float4*>(splats),
+                                                              offsets, k_a, v_a, hdr);
+  GS_CHECK_LAUNCH();
+  // 3. histograms
+  {
+    int dev = 0, sms = 0;
+    GS_CUDA(cudaGetDevice(&dev));
+    GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const int64_t want = div_up(I, 256 * 16);
+    const unsigned blocks = (unsigned)(want < 4 * sms ? (want > 0 ? want : 1) : 4 * sms);
+    hist_kernel<<<blocks, 256, 0, st>>>(I, passes, k_a, hist);
+    GS_CHECK_LAUNCH();
+  }
+  hist_scan_kernel<<<passes, kRadix, 0, st>>>(hist, digit_start);
+  GS_CHECK_LAUNCH();
+  // 4. radix passes
+  const int64_t sort_parts = div_up(I, kSortPart);
+  GS_CUDA(cudaMemsetAsync(sort_status, 0, sizeof(uint64_t) * kRadix * (size_t)sort_parts, st));
+  const size_t smem = sizeof(SortSmem);
+  GS_CUDA(cudaFuncSetAttribute(onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  for (int p = 0; p < passes; ++p) {
+    onesweep_kernel<<<(unsigned)sort_parts, kSortThreads, smem, st>>>(
+        I, p, k_a, v_a, k_b, v_b, digit_start, sort_status, hdr);
+    GS_CHECK_LAUNCH();
+    uint64_t* tk = k_a; k_a = k_b; k_b = tk;
+    uint32_t* tv = v_a; v_a = v_b; v_b = tv;
+  }
+  // 5. ranges
+  ranges_kernel<<<(unsigned)div_up(I, 256), 256, 0, st>>>(I, (uint64_t)(n_views * T), keys, ranges);
+  GS_CHECK_LAUNCH();
+  return GS_OK;
+}

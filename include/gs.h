@@ -1,0 +1,241 @@
+/*
+ * gs.h -- C ABI of the GB300 3D Gaussian Splatting training-step library
+ * (libgs103.so, CUDA kernels for sm_103a).
+ *
+ * One training step on one GPU is
+ *   gs_project -> gs_bin_and_sort -> gs_rasterize_fwd -> gs_loss_l1 ->
+ *   gs_rasterize_bwd -> gs_project_bwd -> gs_adam_step
+ * Forward-only rendering is the first three calls.
+ *
+ * Source pages (title, section) for what the step computes:
+ *  [S1] "On Scaling Up 3D Gaussian Splatting Training": answer on the storage
+ *       requirement (59 fp32 parameters per Gaussian: 3 xyz, 3 scale,
+ *       4 rotation, 1 opacity, 48 SH); answer (1) on the 16x16 pixel blocks,
+ *       whose size alters no pixel value; RetinaGS comparison (opacity
+ *       saturation depth, i.e. early termination); independent-gradients
+ *       answer (gradients averaged over the views of a batch).
+ *  [S2] "AMD ROCm team open-sources distributed 3D Gaussian Splatting
+ *       training": memory-footprint bullet (Adam, two moment vectors, SH
+ *       degree 3, 708 B per Gaussian); per-tile intersection bullet (per-tile
+ *       sorted lists of Gaussian-to-pixel intersections).
+ *  [S3] "ByteSplat": abstract (forward and backward rasterization).
+ *  [S4] "A Scalable PyTorch Abstraction for Multi-GPU Gaussian Splatting":
+ *       references (Kerbl et al. 3D Gaussian Splatting, which defines the
+ *       projection, SH colour and compositing model; Kingma & Ba, Adam;
+ *       Merrill & Garland, single-pass prefix scan with decoupled look-back;
+ *       Merrill & Grimshaw, radix sorting).
+ *
+ * Conventions for every call:
+ *  - Ownership: the caller owns and allocates every buffer.  The library
+ *    allocates no memory, host or device.
+ *  - Pointers are DEVICE pointers unless marked (host).  Device buffers must
+ *    be 16-byte aligned (any cudaMalloc / torch allocation is).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  Only gs_bin_and_sort and gs_workspace_status
+ *    synchronise the stream.
+ *  - Errors: arguments are validated on the host before anything is
+ *    enqueued; an invalid call returns GS_ERR_INVALID_ARG and launches
+ *    nothing.  A failed launch returns GS_ERR_CUDA.  Errors the device
+ *    detects (a bounded wait that ran out) are written to a status word in
+ *    the binning workspace and returned by the next synchronising call.  No
+ *    call prints, aborts or exits.
+ *  - Cameras are passed by value from host memory (up to GS_MAX_VIEWS) and
+ *    must all share one width and height.
+ */
+#ifndef GS_H
+#define GS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GS_NPARAM 59     /* parameters per Gaussian [S1]                     */
+#define GS_TILE 16       /* pixel block edge [S1]                             */
+#define GS_MAX_VIEWS 16  /* cameras per call                                  */
+
+typedef enum gs_status {
+  GS_OK = 0,
+  GS_ERR_INVALID_ARG = 1,  /* a pointer, size or camera failed validation      */
+  GS_ERR_CAPACITY = 2,     /* intersections exceed the caller's capacity       */
+  GS_ERR_TIMEOUT = 3,      /* a bounded device-side wait ran out               */
+  GS_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed             */
+  GS_ERR_DEVICE_CHECK = 5  /* a device-side consistency check failed           */
+} gs_status;
+
+/* Pinhole camera, OpenCV axes (+x right, +y down, +z forward).
+ * p_cam = R p_world + t, R row-major.  Pixel (u, v) samples the image plane
+ * at (u + 0.5, v + 0.5); mean2d = (fx x/z + cx, fy y/z + cy).
+ * Gaussians with z < near_z or z > far_z are culled (far_z may be +inf). */
+typedef struct gs_camera {
+  float R[9];
+  float t[3];
+  float fx, fy, cx, cy;
+  int32_t width, height;
+  float near_z, far_z;
+} gs_camera;
+
+/* Projected Gaussian, one per (view, Gaussian) row r = view * n + g.
+ * 48 bytes, so one record is three 16-byte vectors.  A culled row has
+ * radius = 0 and tiles = 0 (its other fields are unspecified except
+ * color_b = depth = 0). */
+typedef struct gs_splat {
+  float mean_x, mean_y;     /* projected mean, pixels                          */
+  float conic_a, conic_b;   /* inverse 2D covariance [[a, b], [b, c]]          */
+  float conic_c, opacity;   /* opacity = sigmoid(logit)                        */
+  float color_r, color_g;   /* SH degree-3 colour, clamped at 0                */
+  float color_b, depth;     /* depth = camera-space z                          */
+  int32_t radius;           /* ceil(3 sqrt(lambda_max)), 0 = culled            */
+  int32_t tiles;            /* tiles in the footprint rectangle                */
+} gs_splat;
+
+/* Gradient of the loss w.r.t. one projected row, same row indexing.
+ * 48 bytes; pad entries are written as 0. */
+typedef struct gs_splat_grad {
+  float mean_x, mean_y;
+  float conic_a, conic_b;
+  float conic_c, opacity;
+  float color_r, color_g;
+  float color_b, pad0, pad1, pad2;
+} gs_splat_grad;
+
+/* ---------------------------------------------------------------------- */
+/* gs_project -- EWA projection of every Gaussian into every view, SH
+ * degree-3 colour, sigmoid opacity, footprint radius and tile count, culling.
+ * Defines the "3D-to-2D Gaussian transformations" of [S1] (rendering-speed
+ * answer) with the model of [S4] (Kerbl et al.).
+ *   n         Gaussians (>= 0, < 2^32)
+ *   params    [59][n] fp32, row-major: rows 0-2 mean, 3-5 log-scale,
+ *             6-9 quaternion (w,x,y,z), 10 opacity logit, 11+3k+c SH
+ *             coefficient k of channel c  [S1]
+ *   cams      (host) n_views cameras, 1 <= n_views <= GS_MAX_VIEWS
+ *   splats    [n_views * n] output records
+ * Returns GS_ERR_INVALID_ARG for bad sizes/cameras or NULL pointers with
+ * n > 0. */
+gs_status gs_project(int64_t n, const float* params, const gs_camera* cams, int32_t n_views,
+                     gs_splat* splats, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* Workspace for gs_bin_and_sort, in bytes, for n_rows = n_views * n
+ * projected rows and room for `capacity` intersections. */
+size_t gs_bin_workspace_bytes(int64_t n_rows, int64_t capacity);
+
+/* Number of radix-sort key bits used for n_views views of a width x height
+ * image: 32 depth bits plus the bits of the flattened (view, tile) index. */
+int32_t gs_key_bits(int32_t n_views, int32_t width, int32_t height);
+
+/* gs_bin_and_sort -- per-tile depth-sorted intersection lists [S2]:
+ *  1. exclusive scan of per-row tile counts (single pass, decoupled
+ *     look-back [S4 Merrill & Garland]) -> total I (read back to the host:
+ *     the one synchronisation of the step);
+ *  2. one (key, id) pair per row and tile of its footprint rectangle, rows in
+ *     order and tiles row-major, key = (view * T + tile) << 32 | bits(depth),
+ *     T = ceil(W/16) * ceil(H/16);
+ *  3. stable LSD radix sort of the pairs on gs_key_bits() key bits, 8 bits
+ *     per pass, onesweep style [S4 Merrill & Grimshaw];
+ *  4. ranges[(view * T + tile)] = [first, last + 1) of each tile's pairs,
+ *     [0, 0) when empty.
+ * The sorted order is the unique order of (key, id): ties of equal depth
+ * fall back to Gaussian id.
+ *   splats     [n_views * n] from gs_project
+ *   workspace  ws_bytes >= gs_bin_workspace_bytes(n_views * n, capacity)
+ *   capacity   length of keys/vals (<= 2^32 - 1)
+ *   keys, vals [capacity] output: sorted keys and Gaussian ids
+ *   ranges     [n_views * T][2] int64 output
+ *   n_isect    (host) receives I, also when I > capacity
+ * Returns GS_ERR_CAPACITY (nothing emitted, ranges untouched) when
+ * I > capacity; GS_ERR_TIMEOUT if a device wait of the previous call on this
+ * workspace ran out; GS_ERR_DEVICE_CHECK if a record's tile count did not
+ * match its rectangle (that row emits nothing).  n_views * T must be below
+ * 2^32. */
+gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
+                          int32_t height, void* workspace, size_t ws_bytes, int64_t capacity,
+                          uint64_t* keys, uint32_t* vals, int64_t* ranges, int64_t* n_isect,
+                          void* stream);
+
+/* Synchronises `stream` and returns (and clears) the device status word of a
+ * binning workspace: GS_OK, GS_ERR_TIMEOUT or GS_ERR_DEVICE_CHECK. */
+gs_status gs_workspace_status(void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* gs_rasterize_fwd -- per-tile front-to-back alpha compositing [S3] over
+ * the sorted lists.  Per pixel (centre (u+0.5, v+0.5)), for each pair of its
+ * tile's list in order: power = -(a dx^2 + c dy^2)/2 - b dx dy,
+ * alpha = min(0.99, opacity e^power); pairs with alpha < 1/255 are skipped;
+ * the pair that would take transmittance below 1e-4 stops the pixel and is
+ * excluded [S1 opacity saturation]; C = sum c alpha T + T_final bg.
+ *   vals, ranges  from gs_bin_and_sort
+ *   bg            (host) background colour [3]
+ *   image         [n_views][3][H][W]
+ *   T_final       [n_views][H][W] final transmittance
+ *   n_contrib     [n_views][H][W] 1 + list position of the last included
+ *                 pair (0 = none) */
+gs_status gs_rasterize_fwd(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
+                           int32_t height, const uint32_t* vals, const int64_t* ranges,
+                           const float* bg, float* image, float* T_final, int32_t* n_contrib,
+                           void* stream);
+
+/* gs_rasterize_fwd_counted -- gs_rasterize_fwd with the same outputs that
+ * also adds to counts[0] the pairs tested (list entries visited before each
+ * pixel stopped) and to counts[1] the pairs composited.  Work accounting for
+ * the compositing roofline; not part of the training step.
+ *   counts  device uint64[2], accumulated (zero it first) */
+gs_status gs_rasterize_fwd_counted(int64_t n, int32_t n_views, const gs_splat* splats,
+                                   int32_t width, int32_t height, const uint32_t* vals,
+                                   const int64_t* ranges, const float* bg, float* image,
+                                   float* T_final, int32_t* n_contrib, uint64_t* counts,
+                                   void* stream);
+
+/* gs_loss_l1 -- L = mean |image - target| over `count` values and
+ * dL/dimage = sign(image - target) / count (sign(0) = 0).  Helper beyond the
+ * six step calls; the configs of the step use an L1 photometric loss.
+ *   loss  device scalar, overwritten */
+gs_status gs_loss_l1(const float* image, const float* target, int64_t count, float* loss,
+                     float* dL_dimage, void* stream);
+
+/* gs_rasterize_bwd -- analytic backward of gs_rasterize_fwd [S3]: each
+ * pixel walks its list back to front from n_contrib, rebuilding
+ * T_i = T_{i+1} / (1 - alpha_i) from T_final and the colour composited
+ * behind each pair; per-pair gradients are reduced per warp before global
+ * atomics.
+ *   grads  [n_views * n] output, zeroed by this call, then accumulated. */
+gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
+                           int32_t height, const uint32_t* vals, const int64_t* ranges,
+                           const float* bg, const float* T_final, const int32_t* n_contrib,
+                           const float* dL_dimage, gs_splat_grad* grads, void* stream);
+
+/* gs_project_bwd -- chain rule from the per-row gradients back to the 59
+ * parameters, summed over the views (the 1/n_views average of [S1] comes
+ * from the loss normalisation):
+ * colour -> SH coefficients and view direction -> mean; conic -> 2D
+ * covariance -> (J, Sigma) -> (mean, quaternion, log-scale); opacity ->
+ * logit.  The derivative is exact where the step is differentiable; through
+ * an active clamp (alpha cap, colour at 0, the J field-of-view clamp) the
+ * clamped quantity contributes 0.
+ *   grad     [59][n] output (overwritten)
+ *   visible  [n] output or NULL: 1 if the Gaussian has radius > 0 in any
+ *            view, else 0 */
+gs_status gs_project_bwd(int64_t n, const float* params, const gs_camera* cams, int32_t n_views,
+                         const gs_splat* splats, const gs_splat_grad* grads, float* grad,
+                         uint8_t* visible, void* stream);
+
+/* gs_adam_step -- Adam [S4 Kingma & Ba; S2 two moments] over the [59][n]
+ * parameters, fused in one pass:
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ *   p -= lr (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps),   t = step >= 1.
+ * visible == NULL: dense, every column updated.  Otherwise sparse: columns
+ * with visible[g] == 0 keep p, m and v unchanged (t stays global). */
+gs_status gs_adam_step(int64_t n, float* params, const float* grad, float* m, float* v,
+                       int64_t step, float lr, float beta1, float beta2, float eps,
+                       const uint8_t* visible, void* stream);
+
+/* ---------------------------------------------------------------------- */
+const char* gs_status_string(gs_status status);
+int32_t gs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GS_H */

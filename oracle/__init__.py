@@ -53,7 +53,7 @@ def lib():
         L.or_loss_l1.argtypes = [i64, vp, vp, vp]
         L.or_loss_l1.restype = dbl
         L.or_raster_bwd.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                    vp, vp, vp]
+                                    i64, vp, vp, vp, vp]
         L.or_project_bwd.argtypes = [i64, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp]
         L.or_adam.argtypes = [i64, i64, vp, vp, vp, vp, i64, dbl, dbl, dbl, dbl, vp]
         _lib = L
@@ -182,7 +182,7 @@ def loss_l1(image, target):
 
 
 def raster_bwd(n, n_views, width, height, feats, vals, ranges, dL_dimage, bg=(0.0, 0.0, 0.0),
-               tile=TILE):
+               tile=TILE, tile_sel=None):
     rows = n * n_views
     m, co = _f64(feats["mean2d"]), _f64(feats["conic"])
     op, col = _f64(feats["opacity"]), _f64(feats["color"])
@@ -192,8 +192,10 @@ def raster_bwd(n, n_views, width, height, feats, vals, ranges, dL_dimage, bg=(0.
     bgv = _f64(bg)
     out = dict(mean2d=np.zeros((rows, 2)), conic=np.zeros((rows, 3)), opacity=np.zeros(rows),
                color=np.zeros((rows, 3)))
+    sel = None if tile_sel is None else np.ascontiguousarray(tile_sel, np.int64)
     lib().or_raster_bwd(n, n_views, width, height, tile, _p(m), _p(co), _p(op), _p(col),
-                        _p(vals), _p(ranges), _p(bgv), _p(g_img), _p(out["mean2d"]),
+                        _p(vals), _p(ranges), _p(bgv), _p(g_img), _p(sel),
+                        0 if sel is None else sel.size, _p(out["mean2d"]),
                         _p(out["conic"]), _p(out["opacity"]), _p(out["color"]))
     return out
 

@@ -533,8 +533,9 @@ double or_loss_l1(int64_t n, const double* image, const double* target, double* 
 void or_raster_bwd(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
                    const double* mean2d, const double* conic, const double* opacity,
                    const double* color, const uint32_t* vals, const int64_t* ranges,
-                   const double bg[3], const double* dL_dimage, double* g_mean2d,
-                   double* g_conic, double* g_opacity, double* g_color) {
+                   const double bg[3], const double* dL_dimage, const int64_t* tile_sel,
+                   int64_t n_sel, double* g_mean2d, double* g_conic, double* g_opacity,
+                   double* g_color) {
   const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
   const int64_t T = (int64_t)tx * ty;
   const int64_t HW = (int64_t)width * height;
@@ -553,7 +554,9 @@ void or_raster_bwd(int64_t n, int32_t n_views, int32_t width, int32_t height, in
   double* inc_raw = (double*)malloc(sizeof(double) * (size_t)max_len);
   double* inc_dx = (double*)malloc(sizeof(double) * (size_t)max_len);
   double* inc_dy = (double*)malloc(sizeof(double) * (size_t)max_len);
-  for (int64_t flat = 0; flat < n_views * T; ++flat) {
+  const int64_t n_tiles = tile_sel ? n_sel : n_views * T;
+  for (int64_t it = 0; it < n_tiles; ++it) {
+    const int64_t flat = tile_sel ? tile_sel[it] : it;
     const int64_t view = flat / T, t = flat % T;
     const int32_t tile_x = (int32_t)(t % tx), tile_y = (int32_t)(t / tx);
     const int64_t start = ranges[2 * flat], end = ranges[2 * flat + 1];

@@ -122,12 +122,14 @@ double or_loss_l1(int64_t n, const double* image, const double* target, double* 
 
 /* Backward compositing: recomputes the forward per pixel (transmittance by
  * forward product) and accumulates per-row gradients (overwritten):
- * g_mean2d[r][2], g_conic[r][3], g_opacity[r], g_color[r][3]. */
+ * g_mean2d[r][2], g_conic[r][3], g_opacity[r], g_color[r][3].  tile_sel/n_sel
+ * as in or_raster_fwd (NULL = all tiles). */
 void or_raster_bwd(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
                    const double* mean2d, const double* conic, const double* opacity,
                    const double* color, const uint32_t* vals, const int64_t* ranges,
-                   const double bg[3], const double* dL_dimage, double* g_mean2d,
-                   double* g_conic, double* g_opacity, double* g_color);
+                   const double bg[3], const double* dL_dimage, const int64_t* tile_sel,
+                   int64_t n_sel, double* g_mean2d, double* g_conic, double* g_opacity,
+                   double* g_color);
 
 /* Backward through projection and SH colour, summed over views:
  * grad[59][n] (overwritten); visible[n] (may be NULL) = 1 if radius > 0 in

@@ -1,0 +1,86 @@
+"""Helpers shared by the GPU parity tests: packing oracle outputs into the
+library's 48-byte records, fp32-rounded cameras so both sides see identical
+inputs, and the comparison metrics with their tolerances."""
+import numpy as np
+
+import scenes
+
+# Tolerances.  The pages fix three of them (images max-abs 1e-5 on [0,1]
+# colour, gradients and Adam results relative L2 1e-4, intersection lists
+# bit-exact).  The rest are derived from fp32 arithmetic.
+IMAGE_MAX_ABS = 1e-5
+GRAD_REL_L2 = 1e-4
+ADAM_REL_L2 = 1e-4
+# a pixel whose threshold decisions lie within this relative distance of a
+# cut-off may legitimately be decided differently in fp32 (exp error of the
+# fast exponential ~2 ulp + argument rounding ~ |power| ulp, << 1e-5)
+MARGIN = 1e-5
+MAX_FLAGGED_FRACTION = 2e-3
+
+
+def f32_cams(cams):
+    """Cameras with every value rounded to fp32, as the library receives them."""
+    out = []
+    for c in cams:
+        out.append(scenes.camera(np.float32(c["R"]).astype(np.float64),
+                                 np.float32(c["t"]).astype(np.float64),
+                                 np.float32(c["fx"]), np.float32(c["fy"]), np.float32(c["cx"]),
+                                 np.float32(c["cy"]), c["width"], c["height"],
+                                 np.float32(c["near_z"]), np.float32(c["far_z"])))
+    return out
+
+
+def pack_records(pr):
+    """Oracle projection (dict of fp64 arrays) -> float32 [rows][12] records."""
+    rows = pr["radius"].shape[0]
+    rec = np.zeros((rows, 12), np.float32)
+    rec[:, 0:2] = pr["mean2d"]
+    rec[:, 2:5] = pr["conic"]
+    rec[:, 5] = pr["opacity"]
+    rec[:, 6:9] = pr["color"]
+    rec[:, 9] = pr["depth"]
+    ints = rec.view(np.int32)
+    ints[:, 10] = pr["radius"]
+    ints[:, 11] = pr["tiles"]
+    return rec
+
+
+def unpack_records(rec):
+    rec = np.asarray(rec, np.float32)
+    ints = rec.view(np.int32)
+    return dict(mean2d=rec[:, 0:2].astype(np.float64), conic=rec[:, 2:5].astype(np.float64),
+                opacity=rec[:, 5].astype(np.float64), color=rec[:, 6:9].astype(np.float64),
+                depth=rec[:, 9].astype(np.float64), radius=ints[:, 10].copy(),
+                tiles=ints[:, 11].copy())
+
+
+def feats32(pr):
+    """The fp32 values of the projected features, as fp64 arrays."""
+    return unpack_records(pack_records(pr))
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
+
+
+def grads_to_rows(g):
+    """[rows][12] gradient records -> dict of fp64 arrays."""
+    g = np.asarray(g, np.float64)
+    return dict(mean2d=g[:, 0:2], conic=g[:, 2:5], opacity=g[:, 5], color=g[:, 6:9])
+
+
+def rows_to_grads(d):
+    rows = d["opacity"].shape[0]
+    g = np.zeros((rows, 12), np.float32)
+    g[:, 0:2] = d["mean2d"]
+    g[:, 2:5] = d["conic"]
+    g[:, 5] = d["opacity"]
+    g[:, 6:9] = d["color"]
+    return g
+
+
+PARAM_GROUPS = {"mean": (0, 3), "log_scale": (3, 6), "quat": (6, 10), "opacity": (10, 11),
+                "sh_dc": (11, 14), "sh_rest": (14, 59)}

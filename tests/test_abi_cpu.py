@@ -1,0 +1,92 @@
+"""CPU checks of the C-ABI library: it loads, exports every function that
+include/gs.h declares, and its host-side helpers and argument validation
+behave as documented.  No call here reaches the GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gslib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import gaussian_splatting_differentiable_gs_gb300 as gs
+    return gs
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^[a-z_0-9 \*]*?\b(gs_[a-z0-9_]+)\s*\(", src, re.M))
+    return names
+
+
+def test_every_declared_symbol_is_exported(gslib):
+    names = _declared()
+    assert {"gs_project", "gs_bin_and_sort", "gs_rasterize_fwd", "gs_rasterize_bwd",
+            "gs_project_bwd", "gs_adam_step"} <= names
+    lib = C.CDLL(gslib.LIB_PATH)
+    for name in sorted(names):
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(gslib):
+    assert gslib.version() >= 100
+    assert gslib.status_string(0) == "ok"
+    assert "capacity" in gslib.status_string(2)
+    assert gslib.status_string(99) == "unknown status"
+
+
+def test_key_bits_and_workspace(gslib):
+    # 256x256, 1 view: 256 tiles -> 8 bits of tile index + 32 depth bits
+    assert gslib.gs_key_bits(1, 256, 256) == 40
+    assert gslib.gs_key_bits(1, 1024, 768) == 44
+    assert gslib.gs_key_bits(4, 1920, 1080) == 47
+    assert gslib.gs_key_bits(8, 1920, 1080) == 48
+    assert gslib.gs_key_bits(1, 3840, 2160) == 47
+    assert gslib.gs_key_bits(1, 16, 16) == 33
+    a = gslib.gs_bin_workspace_bytes(1000, 10_000)
+    b = gslib.gs_bin_workspace_bytes(1000, 20_000)
+    assert a > 12 * 10_000 and b - a >= 12 * 10_000
+    assert gslib.gs_bin_workspace_bytes(-1, 0) == 0
+
+
+def test_invalid_arguments_return_before_any_launch(gslib):
+    L = gslib.lib()
+    cams = gslib.cameras_struct([dict(R=[1, 0, 0, 0, 1, 0, 0, 0, 1], t=[0, 0, 0], fx=1, fy=1, cx=0,
+                                      cy=0, width=16, height=16, near_z=0.01, far_z=1e9)])
+    cp = C.cast(cams, C.c_void_p)
+    assert L.gs_project(10, None, cp, 0, None, None) == gslib.GS_ERR_INVALID_ARG   # 0 views
+    assert L.gs_project(10, None, cp, 1, None, None) == gslib.GS_ERR_INVALID_ARG   # NULL params
+    assert L.gs_project(-1, None, cp, 1, None, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_project(0, None, cp, 1, None, None) == gslib.GS_OK                 # empty
+    bad = gslib.cameras_struct([dict(R=[1, 0, 0, 0, 1, 0, 0, 0, 1], t=[0, 0, 0], fx=1, fy=1, cx=0,
+                                     cy=0, width=0, height=16, near_z=0.01, far_z=1e9)])
+    assert L.gs_project(0, None, C.cast(bad, C.c_void_p), 1, None, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_adam_step(5, None, None, None, None, 0, 1e-3, 0.9, 0.999, 1e-8, None,
+                          None) == gslib.GS_ERR_INVALID_ARG                        # step 0
+    assert L.gs_adam_step(5, None, None, None, None, 1, 1e-3, 0.9, 0.999, 1e-8, None,
+                          None) == gslib.GS_ERR_INVALID_ARG                        # NULL
+    out = C.c_int64(0)
+    assert L.gs_bin_and_sort(10, 1, None, 16, 16, None, 0, 0, None, None, None, C.byref(out),
+                             None) == gslib.GS_ERR_INVALID_ARG                     # no workspace
+    assert L.gs_rasterize_fwd(10, 1, None, 16, 16, None, None, None, None, None, None,
+                              None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_rasterize_bwd(10, 17, None, 16, 16, None, None, None, None, None, None, None,
+                              None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_project_bwd(10, None, cp, 1, None, None, None, None,
+                            None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_loss_l1(None, None, -1, None, None, None) == gslib.GS_ERR_INVALID_ARG
+
+
+def test_no_fallback_when_library_missing(gslib, monkeypatch):
+    monkeypatch.setattr(gslib, "_lib", None)
+    monkeypatch.setattr(gslib, "LIB_PATH", "/nonexistent/libgs103.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        gslib.lib()

@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gaussians", type=int, default=None,
+                    help="override the Gaussian count (smaller profiling cases)")
     return ap.parse_args()
 
 
@@ -225,7 +227,7 @@ def reference_arm(args, rank, world):
     if rank != 0:
         return
     import scenes
-    cfg = scenes.make(args.workload)
+    cfg = scenes.make(args.workload, n_override=args.gaussians)
     cache = {}
     walls, fulls = [], []
     sample = ""
@@ -261,7 +263,7 @@ def our_arm(args, rank, world, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    cfg = scenes.make(args.workload)
+    cfg = scenes.make(args.workload, n_override=args.gaussians)
     cams = cfg["cams"]
     V = len(cams)
     W, H = cams[0]["width"], cams[0]["height"]

@@ -268,7 +268,7 @@ class TrainStep:
         self.keys = torch.empty(max(self.capacity, 1), device=dev, dtype=torch.int64)
         self.vals = torch.empty(max(self.capacity, 1), device=dev, dtype=torch.int32)
         ws = gs_bin_workspace_bytes(self.V * self.n, self.capacity)
-        self.workspace = torch.empty(ws, device=dev, dtype=torch.uint8)
+        self.workspace = torch.zeros(ws, device=dev, dtype=torch.uint8)  # zeroed header
 
     # the seven library calls of a step, in order
     def project(self, stream=None):

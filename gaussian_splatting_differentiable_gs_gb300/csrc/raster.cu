@@ -5,13 +5,23 @@
 // "On Scaling Up 3D Gaussian Splatting Training": 16x16 pixel blocks and the
 // opacity saturation depth at which a pixel stops).
 //
-// One CTA per (view, 16x16 tile), one pixel per thread.  Warps cover 8x4
-// pixel blocks, so the per-pair skip/stop decisions of a warp are spatially
-// coherent.  The tile's Gaussians are gathered by id into shared memory in
-// batches of 256 with cp.async, double buffered: the next batch is in flight
-// while the current one is composited.  The block stops as soon as every
-// pixel has saturated (barrier count), and the backward starts each warp at
-// its own last contributor.
+// One CTA per (view, 16x16 tile).  The tile's Gaussians are gathered by id
+// into shared memory in batches of 256 with cp.async, double buffered: the
+// next batch is in flight while the current one is composited.
+//
+// Clustered scenes make most pairs skips (alpha < 1/255) and leave a few
+// pixels of a tile unsaturated long after the rest have stopped.  Two
+// measures keep the lanes busy:
+//  - an exp-free pre-filter: a pair whose exponent lies below
+//    -ln(255 opacity) - 1e-3 is certainly below 1/255 and is skipped without
+//    evaluating exp; every other pair takes the exact test, so decisions are
+//    those of the definition;
+//  - forward: pixel state lives in shared memory and, at every batch, the
+//    still-open pixels are packed onto the first threads of the CTA, so the
+//    per-pair loop runs on full warps and finished warps stop issuing.
+//  - backward: a pair's gradient is reduced across the warp only when several
+//    lanes contribute; one to four contributors add straight into the
+//    shared accumulator.
 #include <stdint.h>
 
 #include "gs_internal.cuh"
@@ -19,7 +29,9 @@
 namespace gs {
 namespace {
 
-constexpr int kRT = 256;  // threads per CTA = pixels per tile
+constexpr int kRT = 256;      // threads per CTA = pixels per tile
+constexpr int kWarps = kRT / 32;
+constexpr float kPrefilterMargin = 1e-3f;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -44,17 +56,33 @@ __device__ __forceinline__ float pair_power(float dx, float dy, float ca, float 
   return __fmaf_rn(-0.5f, s, -t);
 }
 
+// Exponent below which alpha = opacity e^power is certainly < 1/255.
+__device__ __forceinline__ float skip_threshold(float opacity) {
+  return -__logf(255.0f * opacity) - kPrefilterMargin;
+}
+
 struct Batch {
-  float4 a[kRT];   // mean_x, mean_y, conic_a, conic_b
-  float4 b[kRT];   // conic_c, opacity, color_r, color_g
-  float c[kRT];    // color_b
+  float4 a[kRT];     // mean_x, mean_y, conic_a, conic_b
+  float4 b[kRT];     // conic_c, opacity, color_r, color_g
+  float c[kRT];      // color_b
+  float thr[kRT];    // skip_threshold(opacity)
 };
 
-__device__ __forceinline__ void pixel_of(int tid, int tile_x, int tile_y, int& px, int& py) {
-  const int warp = tid >> 5, lane = tid & 31;
+// Pixel p of the tile (0..255), in 8x4 blocks per warp.
+__device__ __forceinline__ void pixel_of(int p, int tile_x, int tile_y, int& px, int& py) {
+  const int warp = p >> 5, lane = p & 31;
   px = tile_x * GS_TILE + (warp & 1) * 8 + (lane & 7);
   py = tile_y * GS_TILE + (warp >> 1) * 4 + (lane >> 3);
 }
+
+struct FwdSmem {
+  Batch b[2];
+  float T[kRT], C0[kRT], C1[kRT], C2[kRT];   // pixel state, by pixel
+  int32_t last[kRT];
+  int32_t done[kRT];
+  int32_t list[kRT];                          // open pixels, packed
+  int32_t wcount[kWarps];
+};
 
 // kCount: also accumulate the pairs tested / included into counts[0..1]
 // (instrumentation for work accounting; the compositing is identical).
@@ -64,25 +92,25 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
     const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
     float bg2, float* __restrict__ image, float* __restrict__ T_final,
     int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ counts) {
-  __shared__ Batch sb[2];
+  __shared__ FwdSmem S;
   unsigned long long n_tested = 0, n_included = 0;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t flat = blockIdx.x;
   const int64_t view = flat / T;
   const int32_t tile = (int32_t)(flat - view * T);
   const int tile_x = tile % tiles_x, tile_y = tile / tiles_x;
-  int px, py;
-  pixel_of(tid, tile_x, tile_y, px, py);
-  const bool inside = px < W && py < H;
-  const float pxc = (float)px + 0.5f, pyc = (float)py + 0.5f;
+  {
+    int px, py;
+    pixel_of(tid, tile_x, tile_y, px, py);
+    S.T[tid] = 1.f;
+    S.C0[tid] = S.C1[tid] = S.C2[tid] = 0.f;
+    S.last[tid] = 0;
+    S.done[tid] = (px < W && py < H) ? 0 : 1;
+  }
   const int64_t start = ranges[2 * flat], end = ranges[2 * flat + 1];
   const int64_t len = end - start;
   const int nb = (int)((len + kRT - 1) / kRT);
   const float4* vsplat = splats + 3 * view * n;
-
-  float Tr = 1.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
-  int32_t last = 0;
-  int done = inside ? 0 : 1;
 
   auto issue = [&](int k) {
     const int64_t e = start + (int64_t)k * kRT + tid;
@@ -90,7 +118,7 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
       // ids come from gs_bin_and_sort; clamping keeps a corrupt list in bounds
       const uint32_t id = min(__ldg(vals + e), (uint32_t)(n - 1));
       const float4* src = vsplat + 3 * (int64_t)id;
-      Batch& B = sb[k & 1];
+      Batch& B = S.b[k & 1];
       cp_async16(&B.a[tid], src);
       cp_async16(&B.b[tid], src + 1);
       cp_async4(&B.c[tid], src + 2);
@@ -102,40 +130,75 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
   for (int k = 0; k < nb; ++k) {
     if (k + 1 < nb) issue(k + 1); else cp_async_commit();
     cp_async_wait<1>();
-    if (__syncthreads_count(done) == kRT) break;
-    const Batch& B = sb[k & 1];
+    __syncthreads();  // batch k landed; state of the previous batch written
+    Batch& B = S.b[k & 1];
     const int cnt = (int)min((int64_t)kRT, len - (int64_t)k * kRT);
-    if (!done) {
+    if (tid < cnt) B.thr[tid] = skip_threshold(B.b[tid].y);
+    // pack the open pixels onto the first m threads
+    const bool open = !S.done[tid];
+    const unsigned bal = __ballot_sync(0xffffffffu, open);
+    if (lane == 0) S.wcount[warp] = __popc(bal);
+    __syncthreads();
+    int off = 0, m = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = S.wcount[w];
+      off += w < warp ? c : 0;
+      m += c;
+    }
+    if (m == 0) break;
+    if (open) S.list[off + __popc(bal & ((1u << lane) - 1u))] = tid;
+    __syncthreads();
+    if (tid < m) {
+      const int p = S.list[tid];
+      int px, py;
+      pixel_of(p, tile_x, tile_y, px, py);
+      const float pxc = (float)px + 0.5f, pyc = (float)py + 0.5f;
+      float Tr = S.T[p], C0 = S.C0[p], C1 = S.C1[p], C2 = S.C2[p];
+      int32_t last = S.last[p];
+      int done = 0;
+      const int32_t base1 = k * kRT + 1;  // 1-based list position of entry 0
       for (int j = 0; j < cnt; ++j) {
         const float4 A = B.a[j];
         const float4 Bv = B.b[j];
         if (kCount) ++n_tested;
         const float dx = __fsub_rn(pxc, A.x), dy = __fsub_rn(pyc, A.y);
         const float power = pair_power(dx, dy, A.z, A.w, Bv.x);
+        if (power < B.thr[j]) continue;
         const float alpha = fminf(kAlphaMax, __fmul_rn(Bv.y, __expf(power)));
         if (alpha < kAlphaMin) continue;
         const float Tn = __fmul_rn(Tr, __fsub_rn(1.f, alpha));
         if (Tn < kTMin) { done = 1; break; }
-        if (kCount) ++n_included;
-        const float w = alpha * Tr;
-        C0 += w * Bv.z;
-        C1 += w * Bv.w;
-        C2 += w * B.c[j];
+        const float w = __fmul_rn(alpha, Tr);
+        C0 = __fmaf_rn(w, Bv.z, C0);
+        C1 = __fmaf_rn(w, Bv.w, C1);
+        C2 = __fmaf_rn(w, B.c[j], C2);
         Tr = Tn;
-        last = k * kRT + j + 1;
+        last = base1 + j;
+        if (kCount) ++n_included;
       }
+      S.T[p] = Tr;
+      S.C0[p] = C0; S.C1[p] = C1; S.C2[p] = C2;
+      S.last[p] = last;
+      S.done[p] = done;
     }
-    __syncthreads();
+    __syncthreads();  // buffer k & 1 free for batch k + 2
   }
   cp_async_wait<0>();
-  if (inside) {
-    const int64_t HW = (int64_t)W * H;
-    const int64_t pix = (int64_t)py * W + px;
-    image[(view * 3 + 0) * HW + pix] = C0 + Tr * bg0;
-    image[(view * 3 + 1) * HW + pix] = C1 + Tr * bg1;
-    image[(view * 3 + 2) * HW + pix] = C2 + Tr * bg2;
-    T_final[view * HW + pix] = Tr;
-    n_contrib[view * HW + pix] = last;
+  __syncthreads();
+  {
+    int px, py;
+    pixel_of(tid, tile_x, tile_y, px, py);
+    if (px < W && py < H) {
+      const int64_t HW = (int64_t)W * H;
+      const int64_t pix = (int64_t)py * W + px;
+      const float Tr = S.T[tid];
+      image[(view * 3 + 0) * HW + pix] = S.C0[tid] + Tr * bg0;
+      image[(view * 3 + 1) * HW + pix] = S.C1[tid] + Tr * bg1;
+      image[(view * 3 + 2) * HW + pix] = S.C2[tid] + Tr * bg2;
+      T_final[view * HW + pix] = Tr;
+      n_contrib[view * HW + pix] = S.last[tid];
+    }
   }
   if (kCount) {
 #pragma unroll
@@ -143,7 +206,7 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
       n_tested += __shfl_xor_sync(0xffffffffu, n_tested, o);
       n_included += __shfl_xor_sync(0xffffffffu, n_included, o);
     }
-    if ((tid & 31) == 0) {
+    if (lane == 0) {
       atomicAdd(&counts[0], n_tested);
       atomicAdd(&counts[1], n_included);
     }
@@ -224,10 +287,12 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
     if (k + 1 < nb) issue(k + 1); else cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
-    const Batch& B = S.b[k & 1];
+    Batch& B = S.b[k & 1];
     const int hi = max_last - k * kRT;
     const int cnt = min(kRT, hi);
     const int lo = hi - cnt;
+    if (tid < cnt) B.thr[tid] = skip_threshold(B.b[tid].y);
+    __syncthreads();
     // positions at or above the warp's last contributor cannot contribute
     const int jtop = min(cnt, warp_last - lo);
     for (int j = jtop - 1; j >= 0; --j) {
@@ -241,43 +306,54 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
         const float4 Bv = B.b[j];
         const float dx = __fsub_rn(pxc, A.x), dy = __fsub_rn(pyc, A.y);
         const float power = pair_power(dx, dy, A.z, A.w, Bv.x);
-        const float e = __expf(power);
-        const float raw = __fmul_rn(Bv.y, e);
-        const float alpha = fminf(kAlphaMax, raw);
-        if (alpha >= kAlphaMin) {
-          contrib = true;
-          const float cb = B.c[j];
-          const float oma = 1.f - alpha;
-          const float rinv = 1.f / oma;
-          const float Ti = Tr * rinv;
-          const float w = alpha * Ti;
-          v[6] = w * g0;
-          v[7] = w * g1;
-          v[8] = w * g2;
-          const float dalpha = (g0 * Bv.z + g1 * Bv.w + g2 * cb) * Ti -
-                               (g0 * S0 + g1 * S1 + g2 * S2) * rinv;
-          S0 += w * Bv.z;
-          S1 += w * Bv.w;
-          S2 += w * cb;
-          Tr = Ti;
-          if (raw < kAlphaMax) {
-            const float dpow = dalpha * raw;
-            v[5] = dalpha * e;
-            v[0] = dpow * (A.z * dx + A.w * dy);
-            v[1] = dpow * (A.w * dx + Bv.x * dy);
-            v[2] = -0.5f * dpow * dx * dx;
-            v[3] = -dpow * dx * dy;
-            v[4] = -0.5f * dpow * dy * dy;
+        if (power >= B.thr[j]) {
+          const float e = __expf(power);
+          const float raw = __fmul_rn(Bv.y, e);
+          const float alpha = fminf(kAlphaMax, raw);
+          if (alpha >= kAlphaMin) {
+            contrib = true;
+            const float cb = B.c[j];
+            const float oma = 1.f - alpha;
+            const float rinv = 1.f / oma;
+            const float Ti = Tr * rinv;
+            const float w = alpha * Ti;
+            v[6] = w * g0;
+            v[7] = w * g1;
+            v[8] = w * g2;
+            const float dalpha = (g0 * Bv.z + g1 * Bv.w + g2 * cb) * Ti -
+                                 (g0 * S0 + g1 * S1 + g2 * S2) * rinv;
+            S0 += w * Bv.z;
+            S1 += w * Bv.w;
+            S2 += w * cb;
+            Tr = Ti;
+            if (raw < kAlphaMax) {
+              const float dpow = dalpha * raw;
+              v[5] = dalpha * e;
+              v[0] = dpow * (A.z * dx + A.w * dy);
+              v[1] = dpow * (A.w * dx + Bv.x * dy);
+              v[2] = -0.5f * dpow * dx * dx;
+              v[3] = -dpow * dx * dy;
+              v[4] = -0.5f * dpow * dy * dy;
+            }
           }
         }
       }
-      if (__any_sync(0xffffffffu, contrib)) {
+      const unsigned bal = __ballot_sync(0xffffffffu, contrib);
+      if (bal) {
+        if (__popc(bal) <= 4) {
+          if (contrib) {
 #pragma unroll
-        for (int c = 0; c < 9; ++c) v[c] = warp_sum(v[c]);
-        if (lane == 0) {
+            for (int c = 0; c < 9; ++c)
+              if (v[c] != 0.f) atomicAdd(&S.acc[j][c], v[c]);
+          }
+        } else {
 #pragma unroll
-          for (int c = 0; c < 9; ++c)
-            if (v[c] != 0.f) atomicAdd(&S.acc[j][c], v[c]);
+          for (int c = 0; c < 9; ++c) v[c] = warp_sum(v[c]);
+          if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < 9; ++c)
+              if (v[c] != 0.f) atomicAdd(&S.acc[j][c], v[c]);
+          }
         }
       }
     }

@@ -140,7 +140,10 @@ int32_t gs_key_bits(int32_t n_views, int32_t width, int32_t height);
  * The sorted order is the unique order of (key, id): ties of equal depth
  * fall back to Gaussian id.
  *   splats     [n_views * n] from gs_project
- *   workspace  ws_bytes >= gs_bin_workspace_bytes(n_views * n, capacity)
+ *   workspace  ws_bytes >= gs_bin_workspace_bytes(n_views * n, capacity);
+ *              its first 256 bytes (a status header) must be zero before the
+ *              first call (e.g. cudaMemset once after allocation); calls keep
+ *              it consistent afterwards
  *   capacity   length of keys/vals (<= 2^32 - 1)
  *   keys, vals [capacity] output: sorted keys and Gaussian ids
  *   ranges     [n_views * T][2] int64 output

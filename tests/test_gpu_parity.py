@@ -83,7 +83,7 @@ def _gpu_bin(gs, n, V, rec32, W, H, capacity=None):
     rows = n * V
     T = gs.tiles_per_view(W, H)
     cap = capacity if capacity is not None else max(1, int(rec32.view(np.int32)[:, 11].astype(np.int64).sum()))
-    ws = torch.empty(gs.gs_bin_workspace_bytes(rows, cap), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(gs.gs_bin_workspace_bytes(rows, cap), dtype=torch.uint8, device="cuda")
     keys = torch.empty(max(cap, 1), dtype=torch.int64, device="cuda")
     vals = torch.empty(max(cap, 1), dtype=torch.int32, device="cuda")
     ranges = torch.full((V * T, 2), -7, dtype=torch.int64, device="cuda")

@@ -10,18 +10,20 @@
 // next batch is in flight while the current one is composited.
 //
 // Clustered scenes make most pairs skips (alpha < 1/255) and leave a few
-// pixels of a tile unsaturated long after the rest have stopped.  Two
-// measures keep the lanes busy:
-//  - an exp-free pre-filter: a pair whose exponent lies below
-//    -ln(255 opacity) - 1e-3 is certainly below 1/255 and is skipped without
-//    evaluating exp; every other pair takes the exact test, so decisions are
-//    those of the definition;
+// pixels of a tile unsaturated long after the rest have stopped.  Measures
+// that cut the work without changing any decision or the order of
+// accumulation:
+//  - staging: for every entry of a batch, the exponent below which alpha is
+//    certainly < 1/255 (-ln(255 opacity) - 1e-3) and the bounding box of the
+//    ellipse where it is not; the exact alpha test decides everything inside;
+//  - each warp walks only the entries whose box touches its pixels (a
+//    ballot-compacted sub-list that keeps list order);
 //  - forward: pixel state lives in shared memory and, at every batch, the
 //    still-open pixels are packed onto the first threads of the CTA, so the
-//    per-pair loop runs on full warps and finished warps stop issuing.
-//  - backward: a pair's gradient is reduced across the warp only when several
-//    lanes contribute; one to four contributors add straight into the
-//    shared accumulator.
+//    per-pair loop runs on full warps and finished warps stop issuing;
+//  - backward: a pair's gradient is reduced across the warp only when more
+//    than two lanes contribute, by recursive halving (8 values in 9
+//    shuffles); one or two contributors add straight into shared memory.
 #include <stdint.h>
 
 #include "gs_internal.cuh"
@@ -56,17 +58,52 @@ __device__ __forceinline__ float pair_power(float dx, float dy, float ca, float 
   return __fmaf_rn(-0.5f, s, -t);
 }
 
-// Exponent below which alpha = opacity e^power is certainly < 1/255.
-__device__ __forceinline__ float skip_threshold(float opacity) {
-  return -__logf(255.0f * opacity) - kPrefilterMargin;
-}
-
 struct Batch {
   float4 a[kRT];     // mean_x, mean_y, conic_a, conic_b
   float4 b[kRT];     // conic_c, opacity, color_r, color_g
   float c[kRT];      // color_b
-  float thr[kRT];    // skip_threshold(opacity)
+  float thr[kRT];    // exponent below which alpha < 1/255 for sure
+  float4 box[kRT];   // x0, x1, y0, y1 of the region where it may not be
 };
+
+// Staging of entry j of a landed batch: skip threshold and bounding box of
+// the ellipse -(d^T Q d)/2 >= thr, Q = [[a, b], [b, c]]:
+// half-widths sqrt(-2 thr (Q^-1)_xx) and sqrt(-2 thr (Q^-1)_yy), padded.
+__device__ __forceinline__ void stage_entry(Batch& B, int j) {
+  const float4 A = B.a[j];
+  const float4 Bv = B.b[j];
+  const float thr = -__logf(255.0f * Bv.y) - kPrefilterMargin;
+  B.thr[j] = thr;
+  float4 box = make_float4(INFINITY, -INFINITY, INFINITY, -INFINITY);
+  if (thr < 0.f) {
+    const float q = -2.f * thr;
+    const float det = A.z * Bv.x - A.w * A.w;
+    const float hw = sqrtf(q * Bv.x / det) * 1.0001f + 1e-3f;
+    const float hh = sqrtf(q * A.z / det) * 1.0001f + 1e-3f;
+    box = make_float4(A.x - hw, A.x + hw, A.y - hh, A.y + hh);  // NaN compares keep the entry
+  }
+  B.box[j] = box;
+}
+
+__device__ __forceinline__ bool box_hits(const float4& b, float x0, float x1, float y0, float y1) {
+  return !(b.y < x0 || b.x > x1 || b.w < y0 || b.z > y1);
+}
+
+// Writes into wl[0..] the entries j < cnt (ascending) whose box meets the
+// rectangle; returns their number.  Whole-warp call.
+__device__ __forceinline__ int warp_sublist(const Batch& B, int cnt, float x0, float x1, float y0,
+                                            float y1, uint16_t* wl, int lane) {
+  int n = 0;
+  for (int c0 = 0; c0 < cnt; c0 += 32) {
+    const int j = c0 + lane;
+    const bool hit = j < cnt && box_hits(B.box[j], x0, x1, y0, y1);
+    const unsigned bal = __ballot_sync(0xffffffffu, hit);
+    if (hit) wl[n + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)j;
+    n += __popc(bal);
+  }
+  __syncwarp();
+  return n;
+}
 
 // Pixel p of the tile (0..255), in 8x4 blocks per warp.
 __device__ __forceinline__ void pixel_of(int p, int tile_x, int tile_y, int& px, int& py) {
@@ -82,10 +119,12 @@ struct FwdSmem {
   int32_t done[kRT];
   int32_t list[kRT];                          // open pixels, packed
   int32_t wcount[kWarps];
+  uint16_t wl[kWarps][kRT];                   // per-warp entry sub-lists
 };
 
 // kCount: also accumulate the pairs tested / included into counts[0..1]
-// (instrumentation for work accounting; the compositing is identical).
+// (instrumentation for work accounting: "tested" counts every list entry a
+// pixel passes before it stops, whether or not its box was visited).
 template <bool kCount>
 __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
     int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
@@ -133,7 +172,7 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
     __syncthreads();  // batch k landed; state of the previous batch written
     Batch& B = S.b[k & 1];
     const int cnt = (int)min((int64_t)kRT, len - (int64_t)k * kRT);
-    if (tid < cnt) B.thr[tid] = skip_threshold(B.b[tid].y);
+    if (tid < cnt) stage_entry(B, tid);
     // pack the open pixels onto the first m threads
     const bool open = !S.done[tid];
     const unsigned bal = __ballot_sync(0xffffffffu, open);
@@ -149,38 +188,49 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
     if (m == 0) break;
     if (open) S.list[off + __popc(bal & ((1u << lane) - 1u))] = tid;
     __syncthreads();
-    if (tid < m) {
-      const int p = S.list[tid];
+    if (warp * 32 < m) {
+      const bool worker = tid < m;
+      const int p = worker ? S.list[tid] : 0;
       int px, py;
       pixel_of(p, tile_x, tile_y, px, py);
       const float pxc = (float)px + 0.5f, pyc = (float)py + 0.5f;
-      float Tr = S.T[p], C0 = S.C0[p], C1 = S.C1[p], C2 = S.C2[p];
-      int32_t last = S.last[p];
-      int done = 0;
-      const int32_t base1 = k * kRT + 1;  // 1-based list position of entry 0
-      for (int j = 0; j < cnt; ++j) {
-        const float4 A = B.a[j];
-        const float4 Bv = B.b[j];
-        if (kCount) ++n_tested;
-        const float dx = __fsub_rn(pxc, A.x), dy = __fsub_rn(pyc, A.y);
-        const float power = pair_power(dx, dy, A.z, A.w, Bv.x);
-        if (power < B.thr[j]) continue;
-        const float alpha = fminf(kAlphaMax, __fmul_rn(Bv.y, __expf(power)));
-        if (alpha < kAlphaMin) continue;
-        const float Tn = __fmul_rn(Tr, __fsub_rn(1.f, alpha));
-        if (Tn < kTMin) { done = 1; break; }
-        const float w = __fmul_rn(alpha, Tr);
-        C0 = __fmaf_rn(w, Bv.z, C0);
-        C1 = __fmaf_rn(w, Bv.w, C1);
-        C2 = __fmaf_rn(w, B.c[j], C2);
-        Tr = Tn;
-        last = base1 + j;
-        if (kCount) ++n_included;
+      const float x0 = __reduce_min_sync(0xffffffffu, worker ? px : 1 << 30) + 0.5f;
+      const float x1 = __reduce_max_sync(0xffffffffu, worker ? px : -(1 << 30)) + 0.5f;
+      const float y0 = __reduce_min_sync(0xffffffffu, worker ? py : 1 << 30) + 0.5f;
+      const float y1 = __reduce_max_sync(0xffffffffu, worker ? py : -(1 << 30)) + 0.5f;
+      uint16_t* wl = S.wl[warp];
+      const int nw = warp_sublist(B, cnt, x0, x1, y0, y1, wl, lane);
+      if (worker) {
+        float Tr = S.T[p], C0 = S.C0[p], C1 = S.C1[p], C2 = S.C2[p];
+        int32_t last = S.last[p];
+        int done = 0;
+        int stop_j = cnt;
+        const int32_t base1 = k * kRT + 1;  // 1-based list position of entry 0
+        for (int i = 0; i < nw; ++i) {
+          const int j = wl[i];
+          const float4 A = B.a[j];
+          const float4 Bv = B.b[j];
+          const float dx = __fsub_rn(pxc, A.x), dy = __fsub_rn(pyc, A.y);
+          const float power = pair_power(dx, dy, A.z, A.w, Bv.x);
+          if (power < B.thr[j]) continue;
+          const float alpha = fminf(kAlphaMax, __fmul_rn(Bv.y, __expf(power)));
+          if (alpha < kAlphaMin) continue;
+          const float Tn = __fmul_rn(Tr, __fsub_rn(1.f, alpha));
+          if (Tn < kTMin) { done = 1; stop_j = j + 1; break; }
+          const float w = __fmul_rn(alpha, Tr);
+          C0 = __fmaf_rn(w, Bv.z, C0);
+          C1 = __fmaf_rn(w, Bv.w, C1);
+          C2 = __fmaf_rn(w, B.c[j], C2);
+          Tr = Tn;
+          last = base1 + j;
+          if (kCount) ++n_included;
+        }
+        if (kCount) n_tested += stop_j;
+        S.T[p] = Tr;
+        S.C0[p] = C0; S.C1[p] = C1; S.C2[p] = C2;
+        S.last[p] = last;
+        S.done[p] = done;
       }
-      S.T[p] = Tr;
-      S.C0[p] = C0; S.C1[p] = C1; S.C2[p] = C2;
-      S.last[p] = last;
-      S.done[p] = done;
     }
     __syncthreads();  // buffer k & 1 free for batch k + 2
   }
@@ -219,10 +269,37 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Warp sum of 8 values by recursive halving: at each of three exchange
+// rounds a lane keeps half of its values and sends the other half to its
+// partner, then two plain rounds finish.  9 shuffles instead of 40.  Lane L
+// returns the warp sum of value ((L>>4)&1)*4 + ((L>>3)&1)*2 + ((L>>2)&1).
+__device__ __forceinline__ float warp_sum8(const float v[8], int lane) {
+  const bool h1 = lane & 16, h2 = lane & 8, h3 = lane & 4;
+  float k1[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = h1 ? v[4 + i] : v[i];
+    const float send = h1 ? v[i] : v[4 + i];
+    k1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+  float k2[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = h2 ? k1[2 + i] : k1[i];
+    const float send = h2 ? k1[i] : k1[2 + i];
+    k2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float k3 = (h3 ? k2[1] : k2[0]) + __shfl_xor_sync(0xffffffffu, h3 ? k2[0] : k2[1], 4);
+  k3 += __shfl_xor_sync(0xffffffffu, k3, 2);
+  k3 += __shfl_xor_sync(0xffffffffu, k3, 1);
+  return k3;
+}
+
 struct BwdSmem {
   Batch b[2];
   uint32_t id[2][kRT];
   float acc[kRT][9];
+  uint16_t wl[kWarps][kRT];
   int max_last;
 };
 
@@ -232,7 +309,7 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
     float bg2, const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
     const float* __restrict__ dL_dimage, float4* __restrict__ grads) {
   __shared__ BwdSmem S;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t flat = blockIdx.x;
   const int64_t view = flat / T;
   const int32_t tile = (int32_t)(flat - view * T);
@@ -241,6 +318,9 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
   pixel_of(tid, tile_x, tile_y, px, py);
   const bool inside = px < W && py < H;
   const float pxc = (float)px + 0.5f, pyc = (float)py + 0.5f;
+  // pixel-centre rectangle of this warp's 8x4 block
+  const float wx0 = (float)(tile_x * GS_TILE + (warp & 1) * 8) + 0.5f, wx1 = wx0 + 7.f;
+  const float wy0 = (float)(tile_y * GS_TILE + (warp >> 1) * 4) + 0.5f, wy1 = wy0 + 3.f;
   const int64_t start = ranges[2 * flat];
   const int64_t HW = (int64_t)W * H;
   const int64_t pix = (int64_t)py * W + px;
@@ -291,11 +371,14 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
     const int hi = max_last - k * kRT;
     const int cnt = min(kRT, hi);
     const int lo = hi - cnt;
-    if (tid < cnt) B.thr[tid] = skip_threshold(B.b[tid].y);
+    if (tid < cnt) stage_entry(B, tid);
     __syncthreads();
     // positions at or above the warp's last contributor cannot contribute
-    const int jtop = min(cnt, warp_last - lo);
-    for (int j = jtop - 1; j >= 0; --j) {
+    const int jtop = max(0, min(cnt, warp_last - lo));
+    uint16_t* wl = S.wl[warp];
+    const int nw = warp_sublist(B, jtop, wx0, wx1, wy0, wy1, wl, lane);
+    for (int i = nw - 1; i >= 0; --i) {
+      const int j = wl[i];
       const int pos = lo + j;
       float v[9];
 #pragma unroll
@@ -340,20 +423,21 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
       }
       const unsigned bal = __ballot_sync(0xffffffffu, contrib);
       if (bal) {
-        if (__popc(bal) <= 4) {
+        if (__popc(bal) <= 2) {
           if (contrib) {
 #pragma unroll
-            for (int c = 0; c < 9; ++c)
-              if (v[c] != 0.f) atomicAdd(&S.acc[j][c], v[c]);
+            for (int c = 0; c < 9; ++c) atomicAdd(&S.acc[j][c], v[c]);
           }
         } else {
-#pragma unroll
-          for (int c = 0; c < 9; ++c) v[c] = warp_sum(v[c]);
-          if (lane == 0) {
-#pragma unroll
-            for (int c = 0; c < 9; ++c)
-              if (v[c] != 0.f) atomicAdd(&S.acc[j][c], v[c]);
+          // values 0..7 end on lanes 0,4,...,28 (one shared atomic each);
+          // value 8 by a plain butterfly on lane 0
+          const float s8 = warp_sum8(v, lane);
+          const float s9 = warp_sum(v[8]);
+          if ((lane & 3) == 0) {
+            const int c = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+            atomicAdd(&S.acc[j][c], s8);
           }
+          if (lane == 0) atomicAdd(&S.acc[j][8], s9);
         }
       }
     }

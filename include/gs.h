@@ -162,6 +162,32 @@ gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat* splats, in
  * binning workspace: GS_OK, GS_ERR_TIMEOUT or GS_ERR_DEVICE_CHECK. */
 gs_status gs_workspace_status(void* workspace, void* stream);
 
+/* gs_bin_and_sort_static -- gs_bin_and_sort for callers that cannot allocate
+ * device memory: an application whose own allocator owns the whole GPU and
+ * gives out no extra buffers, a frame loop that must not stall on an
+ * allocation, or a plug-in that only receives its input and output buffers.
+ * The scratch lives in one array inside the library (14 MiB, held by every
+ * GPU that loads the library until the process exits); the call allocates
+ * nothing.  The source pages have no counterpart to this entry point; it is
+ * an interface convenience over gs_bin_and_sort, with the same arguments
+ * minus the workspace and the same results.
+ *   limits   n_views * n <= GS_BIN_STATIC_MAX_ROWS and
+ *            capacity <= GS_BIN_STATIC_MAX_ISECT, else GS_ERR_INVALID_ARG
+ *            (I > capacity still returns GS_ERR_CAPACITY)
+ *   set-up   the first call on a device (with that device current) looks up
+ *            the array's device address and zeroes its status header, with a
+ *            device-wide synchronisation; make that first call before any
+ *            stream capture
+ *   sharing  every call uses the same array, which keeps the last call's
+ *            contents: calls that overlap on the GPU (other streams, other
+ *            host threads) race; serialise them */
+#define GS_BIN_STATIC_MAX_ROWS 65536
+#define GS_BIN_STATIC_MAX_ISECT 1048576
+gs_status gs_bin_and_sort_static(int64_t n, int32_t n_views, const gs_splat* splats,
+                                 int32_t width, int32_t height, int64_t capacity,
+                                 uint64_t* keys, uint32_t* vals, int64_t* ranges,
+                                 int64_t* n_isect, void* stream);
+
 /* ---------------------------------------------------------------------- */
 /* gs_rasterize_fwd -- per-tile front-to-back alpha compositing [S3] over
  * the sorted lists.  Per pixel (centre (u+0.5, v+0.5)), for each pair of its

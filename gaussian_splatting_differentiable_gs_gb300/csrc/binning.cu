@@ -436,6 +436,26 @@ extern "C" int32_t gs_key_bits(int32_t n_views, int32_t width, int32_t height) {
   return 32 + (b > 0 ? b : 1);
 }
 
+extern "C" gs_status gs_selftest_lookback_timeout(void* workspace, size_t ws_bytes, void* stream) {
+  // One scan partition is launched with ticket 1, so it looks back at
+  // partition 0, which never runs: its bounded wait must run out, flag the
+  // error and return.  Reads and writes no row data (zero rows).
+  const WsLayout L = ws_layout(1, 1);
+  if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return GS_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  uint64_t* scan_status = reinterpret_cast<uint64_t*>(ws + L.scan_status);
+  GS_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
+  GS_CUDA(cudaMemsetAsync(scan_status, 0, sizeof(uint64_t) * 2, st));
+  const unsigned one = 1;
+  GS_CUDA(cudaMemcpyAsync(&hdr->scan_ticket, &one, sizeof(one), cudaMemcpyHostToDevice, st));
+  scan_tiles_kernel<<<1, kScanThreads, 0, st>>>(0, nullptr, reinterpret_cast<int64_t*>(ws + L.offsets),
+                                               scan_status, hdr);
+  GS_CHECK_LAUNCH();
+  return gs_workspace_status(workspace, stream);
+}
+
 extern "C" gs_status gs_workspace_status(void* workspace, void* stream) {
   if (!workspace) return GS_ERR_INVALID_ARG;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);

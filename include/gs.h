@@ -162,6 +162,13 @@ gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat* splats, in
  * binning workspace: GS_OK, GS_ERR_TIMEOUT or GS_ERR_DEVICE_CHECK. */
 gs_status gs_workspace_status(void* workspace, void* stream);
 
+/* Self-test of the bounded device waits: runs one look-back partition whose
+ * predecessor never publishes, so its wait runs out (about a second); the
+ * kernel flags the error and returns, and the call synchronises and returns
+ * GS_ERR_TIMEOUT (GS_OK would mean the bound failed).  The context stays
+ * usable.  Needs ws_bytes >= gs_bin_workspace_bytes(1, 1); overwrites it. */
+gs_status gs_selftest_lookback_timeout(void* workspace, size_t ws_bytes, void* stream);
+
 /* gs_bin_and_sort_static -- gs_bin_and_sort for callers that cannot allocate
  * device memory: an application whose own allocator owns the whole GPU and
  * gives out no extra buffers, a frame loop that must not stall on an

@@ -274,7 +274,8 @@ def our_arm(args, rank, world, local):
     step = gs.TrainStep(params0.clone(), cams, target, lr=cfg["lr"], sparse=cfg["sparse_adam"])
     stream = torch.cuda.current_stream()
     passes = (gs.gs_key_bits(V, W, H) + 7) // 8
-    kernels_per_step = 12 + passes
+    # project, scan, emit, digit scan, P passes, ranges, fwd, loss, bwd, project_bwd, adam
+    kernels_per_step = 10 + passes
 
     # warm-up (sizes the intersection buffers)
     for _ in range(max(args.warmup, 3)):

@@ -6,8 +6,8 @@
 //   1. single-pass exclusive scan of the per-row tile counts with decoupled
 //      look-back (Merrill & Garland, cited in "A Scalable PyTorch Abstraction
 //      for Multi-GPU Gaussian Splatting", references);
-//   2. key emission, one thread per projected row;
-//   3. one histogram pass giving the digit counts of every radix pass;
+//   2-3. key emission, one thread per projected row, counting the digits of
+//      every radix pass on the way (no separate histogram read of the keys);
 //   4. stable LSD radix sort, 8-bit digits, one kernel per pass that ranks its
 //      partition, resolves the partition's global digit offsets by decoupled
 //      look-back and scatters ("onesweep"; radix sorting per Merrill &
@@ -28,12 +28,12 @@ namespace gs {
 namespace {
 
 constexpr int kScanThreads = 256;
-constexpr int kScanItems = 8;
+constexpr int kScanItems = 16;
 constexpr int kScanPart = kScanThreads * kScanItems;   // rows per scan partition
 
-constexpr int kSortThreads = 256;
+constexpr int kSortThreads = 512;
 constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kSortKpt = 16;                            // keys per thread
+constexpr int kSortKpt = 8;                             // keys per thread
 constexpr int kSortPart = kSortThreads * kSortKpt;      // keys per sort partition
 constexpr int kRadix = 256;
 constexpr int kMaxPasses = 8;
@@ -173,63 +173,52 @@ __global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// 2. emission of (key, id) pairs, one thread per row.
-// A row whose rectangle disagrees with its stored tile count (records not
-// produced by gs_project) writes nothing and raises the device-check bit, so
-// emission never leaves the row's scanned slot range.
+// 2. emission of (key, id) pairs, one thread per row, and the digit
+//    histograms of every radix pass.  The low 32 key bits (depth) are the same
+//    for all keys of a row, so their digits are counted once per row with the
+//    row's tile count as weight; the tile digits are counted per key.
+//    A row whose rectangle disagrees with its stored tile count (records not
+//    produced by gs_project) writes nothing and raises the device-check bit, so
+//    emission never leaves the row's scanned slot range.
 __global__ void __launch_bounds__(256) emit_kernel(int64_t n, int64_t n_rows, int32_t tiles_x,
-                                                   int32_t tiles_y, int64_t T,
+                                                   int32_t tiles_y, int64_t T, int32_t passes,
                                                    const float4* __restrict__ splats,
                                                    const int64_t* __restrict__ offsets,
                                                    uint64_t* __restrict__ keys,
                                                    uint32_t* __restrict__ vals,
+                                                   uint32_t* __restrict__ hist,
                                                    WsHeader* __restrict__ hdr) {
-  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= n_rows) return;
-  const float4 tail = splats[3 * r + 2];
-  const int32_t tiles = __float_as_int(tail.w);
-  if (tiles <= 0) return;
-  const float4 head = splats[3 * r];
-  const int32_t radius = __float_as_int(tail.z);
-  int32_t x0, x1, y0, y1;
-  tile_rect(head.x, head.y, radius, tiles_x, tiles_y, x0, x1, y0, y1);
-  if ((int64_t)(x1 - x0) * (y1 - y0) != tiles) {
-    atomicOr(&hdr->error, 2u);
-    return;
-  }
-  const int64_t view = r / n;
-  const uint32_t g = (uint32_t)(r - view * n);
-  const uint64_t dbits = (uint64_t)__float_as_uint(tail.y);
-  int64_t o = offsets[r] - tiles;
-  for (int32_t ty = y0; ty < y1; ++ty)
-    for (int32_t tx = x0; tx < x1; ++tx) {
-      const uint64_t flat = (uint64_t)(view * T + (int64_t)ty * tiles_x + tx);
-      keys[o] = (flat << 32) | dbits;
-      vals[o] = g;
-      ++o;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// 3. digit histograms of every pass in one read of the keys.
-__global__ void __launch_bounds__(256) hist_kernel(int64_t count, int32_t passes,
-                                                   const uint64_t* __restrict__ keys,
-                                                   uint32_t* __restrict__ hist) {
   __shared__ uint32_t sh[kMaxPasses * kRadix];
-  for (int i = threadIdx.x; i < kMaxPasses * kRadix; i += blockDim.x) sh[i] = 0;
+  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x) sh[i] = 0;
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t base = warp_global * 32; base < count; base += nwarps * 32) {
-    const int64_t i = base + lane;
-    const bool valid = i < count;
-    const uint64_t k = valid ? keys[i] : 0;
-    for (int p = 0; p < passes; ++p) {
-      const uint32_t d = valid ? (uint32_t)((k >> (8 * p)) & 0xFF) : 256u;
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (d < 256u && lane == __ffs(peers) - 1) atomicAdd(&sh[p * kRadix + d], __popc(peers));
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < n_rows;
+       r += (int64_t)gridDim.x * blockDim.x) {
+    const float4 tail = splats[3 * r + 2];
+    const int32_t tiles = __float_as_int(tail.w);
+    if (tiles <= 0) continue;
+    const float4 head = splats[3 * r];
+    const int32_t radius = __float_as_int(tail.z);
+    int32_t x0, x1, y0, y1;
+    tile_rect(head.x, head.y, radius, tiles_x, tiles_y, x0, x1, y0, y1);
+    if ((int64_t)(x1 - x0) * (y1 - y0) != tiles) {
+      atomicOr(&hdr->error, 2u);
+      continue;
     }
+    const int64_t view = r / n;
+    const uint32_t g = (uint32_t)(r - view * n);
+    const uint32_t dbits = __float_as_uint(tail.y);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) atomicAdd(&sh[p * kRadix + ((dbits >> (8 * p)) & 0xFF)], (uint32_t)tiles);
+    int64_t o = offsets[r] - tiles;
+    for (int32_t ty = y0; ty < y1; ++ty)
+      for (int32_t tx = x0; tx < x1; ++tx) {
+        const uint64_t flat = (uint64_t)(view * T + (int64_t)ty * tiles_x + tx);
+        keys[o] = (flat << 32) | (uint64_t)dbits;
+        vals[o] = g;
+        ++o;
+        for (int p = 4; p < passes; ++p)
+          atomicAdd(&sh[p * kRadix + ((flat >> (8 * (p - 4))) & 0xFF)], 1u);
+      }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x)
@@ -270,7 +259,7 @@ struct SortSmem {
   uint32_t vals[kSortPart];
 };
 
-__global__ void __launch_bounds__(kSortThreads) onesweep_kernel(
+__global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(
     int64_t count, int32_t pass, const uint64_t* __restrict__ keys_in,
     const uint32_t* __restrict__ vals_in, uint64_t* __restrict__ keys_out,
     uint32_t* __restrict__ vals_out, const uint32_t* __restrict__ digit_start,
@@ -314,66 +303,70 @@ __global__ void __launch_bounds__(kSortThreads) onesweep_kernel(
     rank[i] = basec + __popc(peers & lt_mask);
   }
   __syncthreads();
-  // per digit: exclusive prefix over warps, partition count
-  const int d = tid;  // kSortThreads == kRadix
-  uint32_t run = 0;
+  // per digit (threads 0..255, i.e. warps 0..7): exclusive prefix over warps,
+  // partition count, aggregate published first so successors can proceed
+  const bool dthread = tid < kRadix;
+  const int d = tid;
+  uint32_t my_count = 0, incl = 0;
+  if (dthread) {
+    uint32_t run = 0;
 #pragma unroll
-  for (int w = 0; w < kSortWarps; ++w) {
-    const uint32_t c = S.warp_hist[w][d];
-    S.warp_hist[w][d] = run;
-    run += c;
-  }
-  const uint32_t my_count = run;
-  // publish the aggregate before anything else, so successors can proceed
-  if (part == 0)
-    st_volatile(&status[d], ((uint64_t)my_count << 8) | tag | kFlagInc);
-  else
-    st_volatile(&status[part * kRadix + d], ((uint64_t)my_count << 8) | tag | kFlagAgg);
-  // exclusive scan of counts over digits -> local start of each digit
-  {
-    uint32_t incl = my_count;
+    for (int w = 0; w < kSortWarps; ++w) {
+      const uint32_t c = S.warp_hist[w][d];
+      S.warp_hist[w][d] = run;
+      run += c;
+    }
+    my_count = run;
+    if (part == 0)
+      st_volatile(&status[d], ((uint64_t)my_count << 8) | tag | kFlagInc);
+    else
+      st_volatile(&status[part * kRadix + d], ((uint64_t)my_count << 8) | tag | kFlagAgg);
+    incl = my_count;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
     if (lane == 31) S.scan_w[warp] = incl;
-    __syncthreads();
+  }
+  __syncthreads();
+  if (dthread) {
+    // exclusive scan of the counts over digits -> local start of each digit
     uint32_t add = 0;
     for (int w = 0; w < warp; ++w) add += S.scan_w[w];
     S.local_start[d] = add + incl - my_count;
-  }
-  // look back for this digit
-  unsigned long long excl = 0;
-  if (part > 0) {
-    int64_t j = part - 1;
-    bool err = false;
-    while (j >= 0) {
-      uint64_t s;
-      uint32_t spins = 0;
-      for (;;) {
-        s = ld_volatile(&status[j * kRadix + d]);
+    // look back for this digit
+    unsigned long long excl = 0;
+    if (part > 0) {
+      int64_t j = part - 1;
+      bool err = false;
+      while (j >= 0) {
+        uint64_t s;
+        uint32_t spins = 0;
+        for (;;) {
+          s = ld_volatile(&status[j * kRadix + d]);
+          const uint64_t f = s & 3u;
+          if (f == kFlagErr) break;
+          if (f != 0 && (s & 0xFCu) == tag) break;
+          if (++spins > kSpinLimit) { s = kFlagErr; break; }
+          __nanosleep(100);
+        }
         const uint64_t f = s & 3u;
-        if (f == kFlagErr) break;
-        if (f != 0 && (s & 0xFCu) == tag) break;
-        if (++spins > kSpinLimit) { s = kFlagErr; break; }
-        __nanosleep(100);
+        if (f == kFlagErr) { err = true; break; }
+        excl += (unsigned long long)(s >> 8);
+        if (f == kFlagInc) break;
+        --j;
       }
-      const uint64_t f = s & 3u;
-      if (f == kFlagErr) { err = true; break; }
-      excl += (unsigned long long)(s >> 8);
-      if (f == kFlagInc) break;
-      --j;
+      if (err) {
+        st_volatile(&status[part * kRadix + d], tag | kFlagErr);
+        atomicOr(&hdr->error, 1u);
+        S.err = 1;
+      } else {
+        st_volatile(&status[part * kRadix + d], ((uint64_t)(excl + my_count) << 8) | tag | kFlagInc);
+      }
     }
-    if (err) {
-      st_volatile(&status[part * kRadix + d], tag | kFlagErr);
-      atomicOr(&hdr->error, 1u);
-      S.err = 1;
-    } else {
-      st_volatile(&status[part * kRadix + d], ((uint64_t)(excl + my_count) << 8) | tag | kFlagInc);
-    }
+    S.global_base[d] = (unsigned long long)digit_start[pass * kRadix + d] + excl;
   }
-  S.global_base[d] = (unsigned long long)digit_start[pass * kRadix + d] + excl;
   __syncthreads();
   if (S.err) return;
   // place the partition in smem in sorted (digit-major, stable) order
@@ -522,26 +515,21 @@ extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat*
   GS_CUDA(cudaMemsetAsync(ranges, 0, sizeof(int64_t) * 2 * (size_t)(n_views * T), st));
   if (I == 0) return GS_OK;
 
-  // 2. emission into the buffer that ends up holding the sorted result
   const int passes = (gs_key_bits(n_views, width, height) + 7) / 8;
   uint64_t* k_a = (passes % 2 == 0) ? keys : keys_alt;
   uint32_t* v_a = (passes % 2 == 0) ? vals : vals_alt;
   uint64_t* k_b = (passes % 2 == 0) ? keys_alt : keys;
   uint32_t* v_b = (passes % 2 == 0) ? vals_alt : vals;
-  emit_kernel<<<(unsigned)div_up(n_rows, 256), 256, 0, st>>>(n, n_rows, tiles_x, tiles_y, T,
+  // 2-3. emission into the buffer that ends up holding the sorted result, with
+  //      the digit histograms of every pass
+  int dev = 0, sms = 0;
+  GS_CUDA(cudaGetDevice(&dev));
+  GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t emit_blocks = div_up(n_rows, 256) < 8 * sms ? div_up(n_rows, 256) : 8 * sms;
+  emit_kernel<<<(unsigned)emit_blocks, 256, 0, st>>>(n, n_rows, tiles_x, tiles_y, T, passes,
                                                               reinterpret_cast<const float4*>(splats),
-                                                              offsets, k_a, v_a, hdr);
+                                                              offsets, k_a, v_a, hist, hdr);
   GS_CHECK_LAUNCH();
-  // 3. histograms
-  {
-    int dev = 0, sms = 0;
-    GS_CUDA(cudaGetDevice(&dev));
-    GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    const int64_t want = div_up(I, 256 * 16);
-    const unsigned blocks = (unsigned)(want < 4 * sms ? (want > 0 ? want : 1) : 4 * sms);
-    hist_kernel<<<blocks, 256, 0, st>>>(I, passes, k_a, hist);
-    GS_CHECK_LAUNCH();
-  }
   hist_scan_kernel<<<passes, kRadix, 0, st>>>(hist, digit_start);
   GS_CHECK_LAUNCH();
   // 4. radix passes

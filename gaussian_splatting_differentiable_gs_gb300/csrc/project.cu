@@ -186,7 +186,7 @@ __device__ __forceinline__ void view_geom(const Gauss& G, const CamK& C, ViewGeo
   V.ok = V.det > 0.0f;
 }
 
-__global__ void __launch_bounds__(128) project_fwd_kernel(int64_t n, const float* __restrict__ params,
+__global__ void __launch_bounds__(128, 4) project_fwd_kernel(int64_t n, const float* __restrict__ params,
                                                           const __grid_constant__ CamSet cs,
                                                           float4* __restrict__ out) {
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(128) project_fwd_kernel(int64_t n, const float
   }
 }
 
-__global__ void __launch_bounds__(128) project_bwd_kernel(int64_t n, const float* __restrict__ params,
+__global__ void __launch_bounds__(128, 4) project_bwd_kernel(int64_t n, const float* __restrict__ params,
                                                           const __grid_constant__ CamSet cs,
                                                           const float4* __restrict__ splats,
                                                           const float4* __restrict__ grads,

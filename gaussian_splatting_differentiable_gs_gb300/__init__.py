@@ -260,7 +260,9 @@ class TrainStep:
         self.ranges = torch.empty((self.V * self.T, 2), device=dev, dtype=torch.int64)
         self.t = 0
         self.n_isect = 0
-        self._alloc_isect(capacity if capacity is not None else max(1024, 4 * rows))
+        # a first guess, bounded so that very large scenes do not reserve sort
+        # buffers for 4 intersections per row; grown on GS_ERR_CAPACITY
+        self._alloc_isect(capacity if capacity is not None else max(1024, min(4 * rows, 1 << 24)))
 
     def _alloc_isect(self, capacity):
         dev = self.params.device

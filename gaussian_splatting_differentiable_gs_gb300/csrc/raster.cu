@@ -13,9 +13,10 @@
 // pixels of a tile unsaturated long after the rest have stopped.  Measures
 // that cut the work without changing any decision or the order of
 // accumulation:
-//  - staging: for every entry of a batch, the exponent below which alpha is
-//    certainly < 1/255 (-ln(255 opacity) - 1e-3) and the bounding box of the
-//    ellipse where it is not; the exact alpha test decides everything inside;
+//  - staging: for every entry of a batch, its exponent expanded about the
+//    tile pixel where it peaks (exact per-pixel offsets, see below) and the
+//    bounding box of the ellipse where alpha may reach 1/255; pairs outside
+//    it are skipped, the exact alpha test decides everything inside;
 //  - each warp walks only the entries whose box touches its pixels (a
 //    ballot-compacted sub-list that keeps list order);
 //  - forward: pixel state lives in shared memory and, at every batch, the
@@ -33,15 +34,10 @@ namespace {
 
 constexpr int kRT = 256;      // threads per CTA = pixels per tile
 constexpr int kWarps = kRT / 32;
-constexpr float kPrefilterMargin = 1e-3f;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
-  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
@@ -49,56 +45,196 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// The pair terms with a fixed rounding sequence, shared by the forward and
-// the backward so both take identical skip decisions:
-//   power = -(a dx^2 + c dy^2)/2 - b dx dy,   raw alpha = opacity e^power.
-__device__ __forceinline__ float pair_power(float dx, float dy, float ca, float cb, float cc) {
-  const float s = __fmaf_rn(__fmul_rn(ca, dx), dx, __fmul_rn(__fmul_rn(cc, dy), dy));
-  const float t = __fmul_rn(__fmul_rn(cb, dx), dy);
-  return __fmaf_rn(-0.5f, s, -t);
+// ---------------------------------------------------------------------------
+// Pair exponent.  The pages define, for pixel centre p and a projected
+// Gaussian (mean m, conic Q = [[a, b], [b, c]], opacity o),
+//   power = -(d^T Q d)/2,  d = p - m,   raw alpha = o e^power.
+// Evaluated literally in fp32 this loses accuracy when m lies far from the
+// tile (street-level views put the means of elongated ground footprints
+// thousands of pixels off screen): p - m then rounds, and Q, near-singular,
+// turns a 1e-3 px rounding of d into an error of order one in the exponent.
+// So each entry is expanded, once per tile at staging, about a pixel centre
+// z of the tile (the one where its exponent is largest):
+//   ln o + power(p) = P + G.l - (l^T Q l)/2,   l = p - z,
+//   P = ln o - (e^T Q e)/2,  G = -Q e,  e = z - m,
+// with P and G computed by error-free transformations to about twice fp32
+// precision.  l is a small integer vector, exact, and the terms are of the
+// size of the exponent near the footprint, so the per-pair evaluation is as
+// accurate as for a Gaussian centred on the tile.  Folding ln o into P turns
+// the 1/255 test into a test on the exponent alone.
+
+// Knuth's two-sum: s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// a1 b1 + a2 b2 as s + e (FMA two-products, then a two-sum of the leading
+// parts): the dot product to about twice fp32 precision.
+__device__ __forceinline__ void dot2(float a1, float b1, float a2, float b2, float& s, float& e) {
+  const float p1 = __fmul_rn(a1, b1), e1 = __fmaf_rn(a1, b1, -p1);
+  const float p2 = __fmul_rn(a2, b2), e2 = __fmaf_rn(a2, b2, -p2);
+  float t;
+  two_sum(p1, p2, s, t);
+  e = __fadd_rn(t, __fadd_rn(e1, e2));
+}
+
+struct Expansion {
+  float P, gx, gy;  // ln o - (e^T Q e)/2 and -Q e, rounded once
+  float ex, ey;     // e = z - m, rounded
+};
+
+__device__ __forceinline__ Expansion expand_at(float zx, float zy, float mx, float my, float a,
+                                               float b, float c, float lno) {
+  float ex, exl, ey, eyl;
+  two_sum(zx, -mx, ex, exl);
+  two_sum(zy, -my, ey, eyl);
+  float qx, qxl, qy, qyl;  // Q e
+  dot2(a, ex, b, ey, qx, qxl);
+  qxl = __fmaf_rn(a, exl, __fmaf_rn(b, eyl, qxl));
+  dot2(b, ex, c, ey, qy, qyl);
+  qyl = __fmaf_rn(b, exl, __fmaf_rn(c, eyl, qyl));
+  float s, sl;  // e^T Q e
+  dot2(ex, qx, ey, qy, s, sl);
+  sl = __fmaf_rn(ex, qxl, __fmaf_rn(ey, qyl, __fmaf_rn(exl, qx, __fmaf_rn(eyl, qy, sl))));
+  Expansion r;
+  r.P = __fmaf_rn(-0.5f, s, __fmaf_rn(-0.5f, sl, lno));
+  r.gx = -__fadd_rn(qx, qxl);
+  r.gy = -__fadd_rn(qy, qyl);
+  r.ex = ex;
+  r.ey = ey;
+  return r;
+}
+
+// A box bound in grid indices, clamped to [-1, 16] (NaN -> -1).
+__device__ __forceinline__ signed char clamp_index(float v) {
+  return (signed char)fminf(fmaxf(v, -1.f), 16.f);
+}
+
+// Pixel-centre grid index (0..15) of the tile nearest to coordinate v.
+__device__ __forceinline__ float snap(float v, float origin) {
+  return fminf(fmaxf(rintf(__fsub_rn(__fsub_rn(v, origin), 0.5f)), 0.f), 15.f);
 }
 
 struct Batch {
-  float4 a[kRT];     // mean_x, mean_y, conic_a, conic_b
-  float4 b[kRT];     // conic_c, opacity, color_r, color_g
-  float c[kRT];      // color_b
-  float thr[kRT];    // exponent below which alpha < 1/255 for sure
-  float4 box[kRT];   // x0, x1, y0, y1 of the region where it may not be
+  float4 a[kRT];     // as loaded: mean_x, mean_y, conic_a, conic_b
+                     // staged:    G_x, G_y, P, -a/2
+  float4 b[kRT];     // as loaded: conic_c, opacity, color_r, color_g
+                     // staged:    -b, -c/2, z_x, z_y (grid index in the tile)
+  float4 c[kRT];     // as loaded: color_b, depth, radius, tiles
+                     // staged:    color_r, color_g, color_b, opacity
+  char4 box[kRT];    // grid-index box (x0, x1, y0, y1) outside of which
+                     // alpha < 1/255 for sure; clamped to [-1, 16]
 };
 
-// Staging of entry j of a landed batch: skip threshold and bounding box of
-// the ellipse -(d^T Q d)/2 >= thr, Q = [[a, b], [b, c]]:
-// half-widths sqrt(-2 thr (Q^-1)_xx) and sqrt(-2 thr (Q^-1)_yy), padded.
-__device__ __forceinline__ void stage_entry(Batch& B, int j) {
+// ln 255, and the exponent below which a pair is skipped without computing
+// alpha: alpha = e^exponent < 1/255 there with a margin of 1e-3 (>> the
+// rounding error of the exponent).
+constexpr float kLn255 = 5.5412635451584f;
+constexpr float kPrefilterMargin = 1e-3f;
+constexpr float kExpSkip = -kLn255 - kPrefilterMargin;
+
+// Staging of entry j of a landed batch for the tile with origin (ox, oy):
+// expansion point, expansion, and the bounding box of the ellipse
+// d^T Q d <= 2 (ln(255 o) + margin), half-widths sqrt(q (Q^-1)_xx) and
+// sqrt(q (Q^-1)_yy), det Q by Kahan's compensated 2x2 determinant (the plain
+// a c - b^2 cancels for elongated footprints).  e_out (backward only)
+// receives e = z - m.
+__device__ __forceinline__ void stage_entry(Batch& B, int j, float ox, float oy, float2* e_out) {
   const float4 A = B.a[j];
   const float4 Bv = B.b[j];
-  const float thr = -__logf(255.0f * Bv.y) - kPrefilterMargin;
-  B.thr[j] = thr;
-  float4 box = make_float4(INFINITY, -INFINITY, INFINITY, -INFINITY);
-  if (thr < 0.f) {
-    const float q = -2.f * thr;
-    const float det = A.z * Bv.x - A.w * A.w;
-    const float hw = sqrtf(q * Bv.x / det) * 1.0001f + 1e-3f;
-    const float hh = sqrtf(q * A.z / det) * 1.0001f + 1e-3f;
-    box = make_float4(A.x - hw, A.x + hw, A.y - hh, A.y + hh);  // NaN compares keep the entry
+  const float4 Cv = B.c[j];
+  const float mx = A.x, my = A.y, ca = A.z, cb = A.w, cc = Bv.x, o = Bv.y;
+  const float lno = __logf(o);
+  // Expansion point: the maximum of the exponent over the tile's pixel-centre
+  // box, snapped to the grid.  Inside the box that is the mean; outside, the
+  // better of the maxima along the (at most two) edges that face the mean.
+  const float x0 = ox + 0.5f, x1 = ox + 15.5f, y0 = oy + 0.5f, y1 = oy + 15.5f;
+  const bool inx = mx >= x0 && mx <= x1, iny = my >= y0 && my <= y1;
+  float kx, ky;
+  Expansion E;
+  if (inx && iny) {
+    kx = snap(mx, ox);
+    ky = snap(my, oy);
+    E = expand_at(ox + kx + 0.5f, oy + ky + 0.5f, mx, my, ca, cb, cc, lno);
+  } else {
+    kx = -1.f;
+    ky = -1.f;
+    E.P = -INFINITY;
+    if (!inx) {  // edge x = X: exponent largest at y = my - (b/c)(X - mx)
+      const float X = mx < x0 ? x0 : x1;
+      const float ys = __fsub_rn(my, __fmul_rn(__fdiv_rn(cb, cc), __fsub_rn(X, mx)));
+      const float gx = snap(X, ox), gy = snap(ys, oy);
+      E = expand_at(ox + gx + 0.5f, oy + gy + 0.5f, mx, my, ca, cb, cc, lno);
+      kx = gx;
+      ky = gy;
+    }
+    if (!iny) {  // edge y = Y: exponent largest at x = mx - (b/a)(Y - my)
+      const float Y = my < y0 ? y0 : y1;
+      const float xs = __fsub_rn(mx, __fmul_rn(__fdiv_rn(cb, ca), __fsub_rn(Y, my)));
+      const float gx = snap(xs, ox), gy = snap(Y, oy);
+      const Expansion E2 = expand_at(ox + gx + 0.5f, oy + gy + 0.5f, mx, my, ca, cb, cc, lno);
+      if (kx < 0.f || E2.P > E.P) {
+        kx = gx;
+        ky = gy;
+        E = E2;
+      }
+    }
+  }
+  B.a[j] = make_float4(E.gx, E.gy, E.P, -0.5f * ca);
+  B.b[j] = make_float4(-cb, -0.5f * cc, kx, ky);
+  B.c[j] = make_float4(Bv.z, Bv.w, Cv.x, o);
+  if (e_out) e_out[j] = make_float2(E.ex, E.ey);
+  // bounding box in grid indices of the tile: the ellipse centre sits at
+  // index k - e
+  char4 box = make_char4(16, -1, 16, -1);  // empty
+  const float q = 2.f * (kLn255 + lno + kPrefilterMargin);
+  if (q > 0.f) {
+    const float w = __fmul_rn(cb, cb);
+    const float det = __fadd_rn(__fmaf_rn(ca, cc, -w), __fmaf_rn(-cb, cb, w));
+    const float hw = sqrtf(q * cc / det) * 1.0001f + 1e-3f;
+    const float hh = sqrtf(q * ca / det) * 1.0001f + 1e-3f;
+    if (hw >= 0.f && hh >= 0.f) {  // false for NaN (an indefinite Q): keep all
+      const float cxk = kx - E.ex, cyk = ky - E.ey;
+      box = make_char4(clamp_index(floorf(cxk - hw)), clamp_index(ceilf(cxk + hw)),
+                       clamp_index(floorf(cyk - hh)), clamp_index(ceilf(cyk + hh)));
+    } else {
+      box = make_char4(-1, 16, -1, 16);
+    }
   }
   B.box[j] = box;
 }
 
-__device__ __forceinline__ bool box_hits(const float4& b, float x0, float x1, float y0, float y1) {
+// ln o + power of a staged entry at the pixel with grid index (ix, iy), with
+// a fixed rounding sequence shared by the forward and the backward so both
+// take identical decisions.  t1, t2 return partial sums the backward reuses:
+//   t1 = G_x - a l_x / 2 - b l_y,   t2 = G_y - c l_y / 2.
+__device__ __forceinline__ float pair_exponent(const float4& A, const float4& Bv, float ix,
+                                               float iy, float& lx, float& ly, float& t1,
+                                               float& t2) {
+  lx = __fsub_rn(ix, Bv.z);
+  ly = __fsub_rn(iy, Bv.w);
+  t1 = __fmaf_rn(A.w, lx, __fmaf_rn(Bv.x, ly, A.x));
+  t2 = __fmaf_rn(Bv.y, ly, A.y);
+  return __fmaf_rn(lx, t1, __fmaf_rn(ly, t2, A.z));
+}
+
+__device__ __forceinline__ bool box_hits(char4 b, int x0, int x1, int y0, int y1) {
   return !(b.y < x0 || b.x > x1 || b.w < y0 || b.z > y1);
 }
 
 // Writes into wl[0..] the entries j < cnt (ascending) whose box meets the
-// rectangle; returns their number.  Whole-warp call.
-__device__ __forceinline__ int warp_sublist(const Batch& B, int cnt, float x0, float x1, float y0,
-                                            float y1, uint16_t* wl, int lane) {
+// grid-index rectangle [x0, x1] x [y0, y1]; returns their number.  Whole-warp
+// call.
+__device__ __forceinline__ int warp_sublist(const Batch& B, int cnt, int x0, int x1, int y0,
+                                            int y1, uint8_t* wl, int lane) {
   int n = 0;
   for (int c0 = 0; c0 < cnt; c0 += 32) {
     const int j = c0 + lane;
     const bool hit = j < cnt && box_hits(B.box[j], x0, x1, y0, y1);
     const unsigned bal = __ballot_sync(0xffffffffu, hit);
-    if (hit) wl[n + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)j;
+    if (hit) wl[n + __popc(bal & ((1u << lane) - 1u))] = (uint8_t)j;
     n += __popc(bal);
   }
   __syncwarp();
@@ -114,12 +250,12 @@ __device__ __forceinline__ void pixel_of(int p, int tile_x, int tile_y, int& px,
 
 struct FwdSmem {
   Batch b[2];
-  float T[kRT], C0[kRT], C1[kRT], C2[kRT];   // pixel state, by pixel
+  float T[kRT], Tl[kRT], C0[kRT], C1[kRT], C2[kRT];   // pixel state, by pixel
   int32_t last[kRT];
   int32_t done[kRT];
   int32_t list[kRT];                          // open pixels, packed
   int32_t wcount[kWarps];
-  uint16_t wl[kWarps][kRT];                   // per-warp entry sub-lists
+  uint8_t wl[kWarps][kRT];                   // per-warp entry sub-lists
 };
 
 // kCount: also accumulate the pairs tested / included into counts[0..1]
@@ -138,10 +274,12 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
   const int64_t view = flat / T;
   const int32_t tile = (int32_t)(flat - view * T);
   const int tile_x = tile % tiles_x, tile_y = tile / tiles_x;
+  const float ox = (float)(tile_x * GS_TILE), oy = (float)(tile_y * GS_TILE);
   {
     int px, py;
     pixel_of(tid, tile_x, tile_y, px, py);
     S.T[tid] = 1.f;
+    S.Tl[tid] = 0.f;
     S.C0[tid] = S.C1[tid] = S.C2[tid] = 0.f;
     S.last[tid] = 0;
     S.done[tid] = (px < W && py < H) ? 0 : 1;
@@ -160,7 +298,7 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
       Batch& B = S.b[k & 1];
       cp_async16(&B.a[tid], src);
       cp_async16(&B.b[tid], src + 1);
-      cp_async4(&B.c[tid], src + 2);
+      cp_async16(&B.c[tid], src + 2);
     }
     cp_async_commit();
   };
@@ -172,7 +310,7 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
     __syncthreads();  // batch k landed; state of the previous batch written
     Batch& B = S.b[k & 1];
     const int cnt = (int)min((int64_t)kRT, len - (int64_t)k * kRT);
-    if (tid < cnt) stage_entry(B, tid);
+    if (tid < cnt) stage_entry(B, tid, ox, oy, nullptr);
     // pack the open pixels onto the first m threads
     const bool open = !S.done[tid];
     const unsigned bal = __ballot_sync(0xffffffffu, open);
@@ -193,15 +331,21 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
       const int p = worker ? S.list[tid] : 0;
       int px, py;
       pixel_of(p, tile_x, tile_y, px, py);
-      const float pxc = (float)px + 0.5f, pyc = (float)py + 0.5f;
-      const float x0 = __reduce_min_sync(0xffffffffu, worker ? px : 1 << 30) + 0.5f;
-      const float x1 = __reduce_max_sync(0xffffffffu, worker ? px : -(1 << 30)) + 0.5f;
-      const float y0 = __reduce_min_sync(0xffffffffu, worker ? py : 1 << 30) + 0.5f;
-      const float y1 = __reduce_max_sync(0xffffffffu, worker ? py : -(1 << 30)) + 0.5f;
-      uint16_t* wl = S.wl[warp];
+      const int kx = px - tile_x * GS_TILE, ky = py - tile_y * GS_TILE;  // grid index
+      const float ix = (float)kx, iy = (float)ky;
+      const int x0 = __reduce_min_sync(0xffffffffu, worker ? kx : 1 << 30);
+      const int x1 = __reduce_max_sync(0xffffffffu, worker ? kx : -(1 << 30));
+      const int y0 = __reduce_min_sync(0xffffffffu, worker ? ky : 1 << 30);
+      const int y1 = __reduce_max_sync(0xffffffffu, worker ? ky : -(1 << 30));
+      uint8_t* wl = S.wl[warp];
       const int nw = warp_sublist(B, cnt, x0, x1, y0, y1, wl, lane);
       if (worker) {
-        float Tr = S.T[p], C0 = S.C0[p], C1 = S.C1[p], C2 = S.C2[p];
+        // T is carried as an unevaluated sum Tr + Tl, so its rounding error
+        // does not grow with the number of contributors (city-scale lists
+        // reach 10^4 entries); the colour of this batch is summed apart and
+        // added once at the end of the batch.
+        float Tr = S.T[p], Tl = S.Tl[p];
+        float C0 = 0.f, C1 = 0.f, C2 = 0.f;
         int32_t last = S.last[p];
         int done = 0;
         int stop_j = cnt;
@@ -210,24 +354,33 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
           const int j = wl[i];
           const float4 A = B.a[j];
           const float4 Bv = B.b[j];
-          const float dx = __fsub_rn(pxc, A.x), dy = __fsub_rn(pyc, A.y);
-          const float power = pair_power(dx, dy, A.z, A.w, Bv.x);
-          if (power < B.thr[j]) continue;
-          const float alpha = fminf(kAlphaMax, __fmul_rn(Bv.y, __expf(power)));
+          float lx, ly, t1, t2;
+          const float ex = pair_exponent(A, Bv, ix, iy, lx, ly, t1, t2);
+          if (ex < kExpSkip) continue;
+          const float alpha = fminf(kAlphaMax, __expf(ex));
           if (alpha < kAlphaMin) continue;
-          const float Tn = __fmul_rn(Tr, __fsub_rn(1.f, alpha));
+          const float om = __fsub_rn(1.f, alpha);
+          const float oml = __fsub_rn(__fsub_rn(1.f, om), alpha);  // 1 - alpha = om + oml
+          const float ph = __fmul_rn(Tr, om);
+          const float lo = __fmaf_rn(Tr, oml, __fmaf_rn(Tl, om, __fmaf_rn(Tr, om, -ph)));
+          const float Tn = __fadd_rn(ph, lo);
           if (Tn < kTMin) { done = 1; stop_j = j + 1; break; }
           const float w = __fmul_rn(alpha, Tr);
-          C0 = __fmaf_rn(w, Bv.z, C0);
-          C1 = __fmaf_rn(w, Bv.w, C1);
-          C2 = __fmaf_rn(w, B.c[j], C2);
+          const float4 Cv = B.c[j];
+          C0 = __fmaf_rn(w, Cv.x, C0);
+          C1 = __fmaf_rn(w, Cv.y, C1);
+          C2 = __fmaf_rn(w, Cv.z, C2);
+          Tl = __fsub_rn(lo, __fsub_rn(Tn, ph));
           Tr = Tn;
           last = base1 + j;
           if (kCount) ++n_included;
         }
         if (kCount) n_tested += stop_j;
         S.T[p] = Tr;
-        S.C0[p] = C0; S.C1[p] = C1; S.C2[p] = C2;
+        S.Tl[p] = Tl;
+        S.C0[p] = __fadd_rn(S.C0[p], C0);
+        S.C1[p] = __fadd_rn(S.C1[p], C1);
+        S.C2[p] = __fadd_rn(S.C2[p], C2);
         S.last[p] = last;
         S.done[p] = done;
       }
@@ -297,13 +450,14 @@ __device__ __forceinline__ float warp_sum8(const float v[8], int lane) {
 
 struct BwdSmem {
   Batch b[2];
+  float2 e[2][kRT];  // e = z - m of the staged entries
   uint32_t id[2][kRT];
   float acc[kRT][9];
-  uint16_t wl[kWarps][kRT];
+  uint8_t wl[kWarps][kRT];
   int max_last;
 };
 
-__global__ void __launch_bounds__(kRT) raster_bwd_kernel(
+__global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
     int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
     const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
     float bg2, const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
@@ -314,13 +468,14 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
   const int64_t view = flat / T;
   const int32_t tile = (int32_t)(flat - view * T);
   const int tile_x = tile % tiles_x, tile_y = tile / tiles_x;
+  const float ox = (float)(tile_x * GS_TILE), oy = (float)(tile_y * GS_TILE);
   int px, py;
   pixel_of(tid, tile_x, tile_y, px, py);
   const bool inside = px < W && py < H;
-  const float pxc = (float)px + 0.5f, pyc = (float)py + 0.5f;
-  // pixel-centre rectangle of this warp's 8x4 block
-  const float wx0 = (float)(tile_x * GS_TILE + (warp & 1) * 8) + 0.5f, wx1 = wx0 + 7.f;
-  const float wy0 = (float)(tile_y * GS_TILE + (warp >> 1) * 4) + 0.5f, wy1 = wy0 + 3.f;
+  const float ix = (float)(px - tile_x * GS_TILE), iy = (float)(py - tile_y * GS_TILE);
+  // grid-index rectangle of this warp's 8x4 block
+  const int wx0 = (warp & 1) * 8, wx1 = wx0 + 7;
+  const int wy0 = (warp >> 1) * 4, wy1 = wy0 + 3;
   const int64_t start = ranges[2 * flat];
   const int64_t HW = (int64_t)W * H;
   const int64_t pix = (int64_t)py * W + px;
@@ -357,7 +512,7 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
       S.id[k & 1][tid] = id;
       cp_async16(&B.a[tid], src);
       cp_async16(&B.b[tid], src + 1);
-      cp_async4(&B.c[tid], src + 2);
+      cp_async16(&B.c[tid], src + 2);
     }
     cp_async_commit();
   };
@@ -371,11 +526,12 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
     const int hi = max_last - k * kRT;
     const int cnt = min(kRT, hi);
     const int lo = hi - cnt;
-    if (tid < cnt) stage_entry(B, tid);
+    float2* E = S.e[k & 1];
+    if (tid < cnt) stage_entry(B, tid, ox, oy, E);
     __syncthreads();
     // positions at or above the warp's last contributor cannot contribute
     const int jtop = max(0, min(cnt, warp_last - lo));
-    uint16_t* wl = S.wl[warp];
+    uint8_t* wl = S.wl[warp];
     const int nw = warp_sublist(B, jtop, wx0, wx1, wy0, wy1, wl, lane);
     for (int i = nw - 1; i >= 0; --i) {
       const int j = wl[i];
@@ -387,15 +543,14 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
       if (pos < last) {
         const float4 A = B.a[j];
         const float4 Bv = B.b[j];
-        const float dx = __fsub_rn(pxc, A.x), dy = __fsub_rn(pyc, A.y);
-        const float power = pair_power(dx, dy, A.z, A.w, Bv.x);
-        if (power >= B.thr[j]) {
-          const float e = __expf(power);
-          const float raw = __fmul_rn(Bv.y, e);
+        float lx, ly, t1, t2;
+        const float ex = pair_exponent(A, Bv, ix, iy, lx, ly, t1, t2);
+        if (ex >= kExpSkip) {
+          const float raw = __expf(ex);
           const float alpha = fminf(kAlphaMax, raw);
           if (alpha >= kAlphaMin) {
             contrib = true;
-            const float cb = B.c[j];
+            const float4 Cv = B.c[j];
             const float oma = 1.f - alpha;
             const float rinv = 1.f / oma;
             const float Ti = Tr * rinv;
@@ -403,17 +558,21 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
             v[6] = w * g0;
             v[7] = w * g1;
             v[8] = w * g2;
-            const float dalpha = (g0 * Bv.z + g1 * Bv.w + g2 * cb) * Ti -
+            const float dalpha = (g0 * Cv.x + g1 * Cv.y + g2 * Cv.z) * Ti -
                                  (g0 * S0 + g1 * S1 + g2 * S2) * rinv;
-            S0 += w * Bv.z;
-            S1 += w * Bv.w;
-            S2 += w * cb;
+            S0 += w * Cv.x;
+            S1 += w * Cv.y;
+            S2 += w * Cv.z;
             Tr = Ti;
             if (raw < kAlphaMax) {
+              // dL/dpower; the opacity gradient is dL/dpower / o, applied at
+              // the flush (d alpha / d o = e^power = alpha / o)
               const float dpow = dalpha * raw;
-              v[5] = dalpha * e;
-              v[0] = dpow * (A.z * dx + A.w * dy);
-              v[1] = dpow * (A.w * dx + Bv.x * dy);
+              const float2 e = E[j];
+              const float dx = lx + e.x, dy = ly + e.y;  // p - m
+              v[5] = dpow;
+              v[0] = -dpow * (t1 + A.w * lx);              // dpow (Q d)_x
+              v[1] = -dpow * (t2 + Bv.y * ly + Bv.x * lx);  // dpow (Q d)_y
               v[2] = -0.5f * dpow * dx * dx;
               v[3] = -dpow * dx * dy;
               v[4] = -0.5f * dpow * dy * dy;
@@ -449,8 +608,9 @@ __global__ void __launch_bounds__(kRT) raster_bwd_kernel(
       for (int c = 0; c < 9; ++c) nz |= a[c] != 0.f;
       if (nz) {
         float4* dst = grads + 3 * (view * n + (int64_t)S.id[k & 1][tid]);
+        const float dop = a[5] / B.c[tid].w;
         atomicAdd(dst, make_float4(a[0], a[1], a[2], a[3]));
-        atomicAdd(dst + 1, make_float4(a[4], a[5], a[6], a[7]));
+        atomicAdd(dst + 1, make_float4(a[4], dop, a[6], a[7]));
         atomicAdd(reinterpret_cast<float*>(dst + 2), a[8]);
       }
 #pragma unroll

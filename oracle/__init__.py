@@ -42,6 +42,9 @@ def lib():
         L.or_sh_basis.argtypes = [vp, vp]
         L.or_quat_to_rot.argtypes = [vp, vp]
         L.or_project.argtypes = [i64, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.or_project_mt.argtypes = [i64, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32]
+        L.or_bin_select.argtypes = [i64, i32, vp, vp, vp, i32, i32, i32, vp, i64, vp, vp]
+        L.or_bin_select.restype = i64
         L.or_tile_rect.argtypes = [C.c_float, C.c_float, i32, i32, i32, i32, vp]
         L.or_count_isect.argtypes = [i64, vp, vp, i32, i32, i32]
         L.or_count_isect.restype = i64
@@ -94,8 +97,9 @@ def quat_to_rot(q):
     return out.reshape(3, 3)
 
 
-def project(params, cams, tile=TILE):
-    """params: [59][n] -> dict of per-row arrays (rows = view*n + g)."""
+def project(params, cams, tile=TILE, threads=1):
+    """params: [59][n] -> dict of per-row arrays (rows = view*n + g).
+    threads > 1 splits the Gaussians over POSIX threads (same result)."""
     params = _f64(params)
     n = params.shape[1]
     V = len(cams)
@@ -105,9 +109,10 @@ def project(params, cams, tile=TILE):
                radius=np.zeros(rows, np.int32), tiles=np.zeros(rows, np.int32),
                flags=np.zeros(rows, np.uint8))
     cs = cameras_struct(cams)
-    lib().or_project(n, _p(params), V, C.cast(cs, C.c_void_p), tile, _p(out["mean2d"]),
-                     _p(out["conic"]), _p(out["depth"]), _p(out["color"]), _p(out["opacity"]),
-                     _p(out["radius"]), _p(out["tiles"]), _p(out["flags"]))
+    lib().or_project_mt(n, _p(params), V, C.cast(cs, C.c_void_p), tile, _p(out["mean2d"]),
+                        _p(out["conic"]), _p(out["depth"]), _p(out["color"]),
+                        _p(out["opacity"]), _p(out["radius"]), _p(out["tiles"]),
+                        _p(out["flags"]), int(threads))
     return out
 
 
@@ -137,6 +142,22 @@ def bin_and_sort(n, n_views, mean2d_f32, radius, depth_f32, width, height, tile=
     lib().or_bin(n, n_views, _p(m), _p(r), _p(d), tile, width, height, _p(keys), _p(vals),
                  _p(ranges))
     return keys[:total], vals[:total], ranges
+
+
+def bin_select(n, n_views, mean2d_f32, radius, depth_f32, width, height, tile_sel, tile=TILE):
+    """Brute-force sorted lists of the selected flattened tiles.
+    -> vals u32[total], ranges i64[len(tile_sel)][2] into vals."""
+    m = np.ascontiguousarray(mean2d_f32, np.float32)
+    r = np.ascontiguousarray(radius, np.int32)
+    d = np.ascontiguousarray(depth_f32, np.float32)
+    sel = np.ascontiguousarray(tile_sel, np.int64)
+    total = lib().or_bin_select(n, n_views, _p(m), _p(r), _p(d), tile, width, height, _p(sel),
+                                sel.size, None, None)
+    vals = np.zeros(max(total, 1), np.uint32)
+    ranges = np.zeros((sel.size, 2), np.int64)
+    lib().or_bin_select(n, n_views, _p(m), _p(r), _p(d), tile, width, height, _p(sel), sel.size,
+                        _p(vals), _p(ranges))
+    return vals[:total], ranges
 
 
 def raster_fwd(n, n_views, width, height, feats, vals, ranges, bg=(0.0, 0.0, 0.0), tile=TILE,

@@ -18,7 +18,7 @@ def build(force: bool = False) -> str:
                                              os.path.getmtime(os.path.join(HERE, "gs_oracle.h")))):
         return LIB
     cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
-           "-fno-fast-math", "-D_DEFAULT_SOURCE", SRC, "-o", LIB + ".tmp", "-lm"]
+           "-fno-fast-math", "-D_DEFAULT_SOURCE", SRC, "-o", LIB + ".tmp", "-lm", "-lpthread"]
     subprocess.check_call(cmd)
     os.replace(LIB + ".tmp", LIB)
     return LIB

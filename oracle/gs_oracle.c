@@ -28,6 +28,7 @@
 #include "gs_oracle.h"
 
 #include <math.h>
+#include <pthread.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -297,14 +298,29 @@ static void project_one(const double* params, int64_t n, int64_t g, const or_cam
   s->visible = 1;
 }
 
-void or_project(int64_t n, const double* params, int32_t n_views, const or_camera* cams,
-                int32_t tile, double* mean2d, double* conic, double* depth, double* color,
-                double* opacity, int32_t* radius, int32_t* tiles, uint8_t* flags) {
+typedef struct proj_job {
+  int64_t n, g0, g1;
+  const double* params;
+  int32_t n_views;
+  const or_camera* cams;
+  int32_t tile;
+  double *mean2d, *conic, *depth, *color, *opacity;
+  int32_t *radius, *tiles;
+  uint8_t* flags;
+} proj_job;
+
+/* Projection of Gaussians g0 <= g < g1 into every view. */
+static void project_range(const proj_job* j) {
+  const int64_t n = j->n;
+  double *mean2d = j->mean2d, *conic = j->conic, *depth = j->depth, *color = j->color,
+         *opacity = j->opacity;
+  int32_t *radius = j->radius, *tiles = j->tiles;
+  uint8_t* flags = j->flags;
   proj_state s;
-  for (int32_t v = 0; v < n_views; ++v)
-    for (int64_t g = 0; g < n; ++g) {
+  for (int32_t v = 0; v < j->n_views; ++v)
+    for (int64_t g = j->g0; g < j->g1; ++g) {
       const int64_t r = (int64_t)v * n + g;
-      project_one(params, n, g, &cams[v], tile, &s);
+      project_one(j->params, n, g, &j->cams[v], j->tile, &s);
       if (flags) flags[r] = s.flags;
       if (!s.visible) {
         mean2d[2 * r] = mean2d[2 * r + 1] = 0.0;
@@ -325,6 +341,41 @@ void or_project(int64_t n, const double* params, int32_t n_views, const or_camer
       radius[r] = s.radius;
       tiles[r] = s.tiles;
     }
+}
+
+static void* project_thread(void* arg) {
+  project_range((const proj_job*)arg);
+  return NULL;
+}
+
+void or_project_mt(int64_t n, const double* params, int32_t n_views, const or_camera* cams,
+                   int32_t tile, double* mean2d, double* conic, double* depth, double* color,
+                   double* opacity, int32_t* radius, int32_t* tiles, uint8_t* flags,
+                   int32_t threads) {
+  if (threads < 1) threads = 1;
+  if (threads > 64) threads = 64;
+  proj_job jobs[64];
+  pthread_t tid[64];
+  int started[64] = {0};
+  for (int32_t t = 0; t < threads; ++t) {
+    proj_job j = {n, n * t / threads, n * (t + 1) / threads, params, n_views, cams, tile,
+                  mean2d, conic, depth, color, opacity, radius, tiles, flags};
+    jobs[t] = j;
+  }
+  for (int32_t t = 1; t < threads; ++t)
+    started[t] = pthread_create(&tid[t], NULL, project_thread, &jobs[t]) == 0;
+  project_range(&jobs[0]);
+  for (int32_t t = 1; t < threads; ++t) {
+    if (started[t]) pthread_join(tid[t], NULL);
+    else project_range(&jobs[t]);  /* no thread: do its share here */
+  }
+}
+
+void or_project(int64_t n, const double* params, int32_t n_views, const or_camera* cams,
+                int32_t tile, double* mean2d, double* conic, double* depth, double* color,
+                double* opacity, int32_t* radius, int32_t* tiles, uint8_t* flags) {
+  or_project_mt(n, params, n_views, cams, tile, mean2d, conic, depth, color, opacity, radius,
+                tiles, flags, 1);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -392,6 +443,56 @@ void or_bin(int64_t n, int32_t n_views, const float* mean2d, const int32_t* radi
   free(items);
 }
 
+typedef struct dk { uint32_t dbits; uint32_t id; } dk;
+
+static int dk_cmp(const void* pa, const void* pb) {
+  const dk* a = (const dk*)pa;
+  const dk* b = (const dk*)pb;
+  if (a->dbits != b->dbits) return a->dbits < b->dbits ? -1 : 1;
+  if (a->id != b->id) return a->id < b->id ? -1 : 1;
+  return 0;
+}
+
+/* Brute-force lists of selected tiles: every row of the tile's view whose
+ * fp32 rectangle covers the tile, ordered by (depth bits, id). */
+int64_t or_bin_select(int64_t n, int32_t n_views, const float* mean2d, const int32_t* radius,
+                      const float* depth, int32_t tile, int32_t width, int32_t height,
+                      const int64_t* tile_sel, int64_t n_sel, uint32_t* out_vals,
+                      int64_t* out_ranges) {
+  const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
+  const int64_t T = (int64_t)tx * ty;
+  int64_t total = 0;
+  int32_t rect[4];
+  (void)n_views;
+  for (int64_t s = 0; s < n_sel; ++s) {
+    const int64_t flat = tile_sel[s], view = flat / T, t = flat % T;
+    const int32_t sx = (int32_t)(t % tx), sy = (int32_t)(t / tx);
+    const int64_t begin = total;
+    for (int64_t g = 0; g < n; ++g) {
+      const int64_t r = view * n + g;
+      if (radius[r] <= 0) continue;
+      or_tile_rect(mean2d[2 * r], mean2d[2 * r + 1], radius[r], tile, tx, ty, rect);
+      if (sx < rect[0] || sx >= rect[1] || sy < rect[2] || sy >= rect[3]) continue;
+      if (out_vals) out_vals[total] = (uint32_t)g;
+      ++total;
+    }
+    if (out_vals) {
+      const int64_t m = total - begin;
+      dk* items = (dk*)malloc(sizeof(dk) * (size_t)(m > 0 ? m : 1));
+      for (int64_t i = 0; i < m; ++i) {
+        items[i].dbits = float_bits(depth[view * n + out_vals[begin + i]]);
+        items[i].id = out_vals[begin + i];
+      }
+      qsort(items, (size_t)m, sizeof(dk), dk_cmp);
+      for (int64_t i = 0; i < m; ++i) out_vals[begin + i] = items[i].id;
+      free(items);
+      out_ranges[2 * s] = begin;
+      out_ranges[2 * s + 1] = total;
+    }
+  }
+  return total;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Compositing of one pair: returns the un-capped alpha o*exp(power) and the
  * power through *power_out. */
@@ -454,16 +555,6 @@ void or_raster_fwd(int64_t n, int32_t n_views, int32_t width, int32_t height, in
         if (margin) margin[view * HW + pix] = mg;
       }
   }
-}
-
-typedef struct dk { uint32_t dbits; uint32_t id; } dk;
-
-static int dk_cmp(const void* pa, const void* pb) {
-  const dk* a = (const dk*)pa;
-  const dk* b = (const dk*)pb;
-  if (a->dbits != b->dbits) return a->dbits < b->dbits ? -1 : 1;
-  if (a->id != b->id) return a->id < b->id ? -1 : 1;
-  return 0;
 }
 
 void or_raster_fwd_brute(int64_t n, int32_t n_views, int32_t width, int32_t height,

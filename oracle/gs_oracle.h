@@ -72,6 +72,13 @@ void or_project(int64_t n, const double* params, int32_t n_views, const or_camer
                 int32_t tile, double* mean2d, double* conic, double* depth, double* color,
                 double* opacity, int32_t* radius, int32_t* tiles, uint8_t* flags);
 
+/* or_project split over `threads` POSIX threads by Gaussian index; the
+ * outputs are identical for any thread count. */
+void or_project_mt(int64_t n, const double* params, int32_t n_views, const or_camera* cams,
+                   int32_t tile, double* mean2d, double* conic, double* depth, double* color,
+                   double* opacity, int32_t* radius, int32_t* tiles, uint8_t* flags,
+                   int32_t threads);
+
 /* Tile rectangle of one projected row, evaluated in fp32:
  * [x0,x1) x [y0,y1) in tile units, clamped to the tile grid. */
 void or_tile_rect(float mx, float my, int32_t radius, int32_t tile, int32_t tiles_x,
@@ -90,6 +97,17 @@ int64_t or_count_isect(int64_t n_rows, const float* mean2d, const int32_t* radiu
 void or_bin(int64_t n, int32_t n_views, const float* mean2d, const int32_t* radius,
             const float* depth, int32_t tile, int32_t width, int32_t height,
             uint64_t* keys, uint32_t* vals, int64_t* ranges);
+
+/* The sorted list of each selected flattened tile (view*T + tile) by brute
+ * force: every row of that view whose tile rectangle covers it, ordered by
+ * (float_bits(depth), id) -- the same lists or_bin produces for those tiles.
+ * Returns the total length; with out_vals NULL it only counts.  Otherwise
+ * out_vals receives the concatenated ids and out_ranges[2*s..2*s+1] the
+ * [start, end) of selection s. */
+int64_t or_bin_select(int64_t n, int32_t n_views, const float* mean2d, const int32_t* radius,
+                      const float* depth, int32_t tile, int32_t width, int32_t height,
+                      const int64_t* tile_sel, int64_t n_sel, uint32_t* out_vals,
+                      int64_t* out_ranges);
 
 /* Forward compositing over the sorted per-tile lists (tiled mode).
  * features are fp64 arrays indexed by row; vals hold gaussian ids (row =

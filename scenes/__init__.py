@@ -67,6 +67,29 @@ def _common_params(rng, means, logscale_mu, logscale_sd):
     return p
 
 
+CHUNK = 4_000_000
+
+
+def _chunked_params(n, seed, draw_means, logscale_mu, logscale_sd):
+    """Large scenes: Gaussians are drawn in chunks of CHUNK, chunk c from its
+    own PCG64 stream seeded by (seed, c), in parallel threads, straight into
+    one float32 [59][n] array (bounded temporaries, same result for any thread
+    count).  draw_means(rng, m) -> (m, 3) means of one chunk."""
+    import concurrent.futures as cf
+    import os
+    p = np.empty((NPARAM, n), np.float32)
+
+    def fill(c):
+        a, b = c * CHUNK, min(n, (c + 1) * CHUNK)
+        rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, c])))
+        p[:, a:b] = _common_params(rng, draw_means(rng, b - a), logscale_mu, logscale_sd)
+
+    chunks = range((n + CHUNK - 1) // CHUNK)
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, chunks))
+    return p
+
+
 def uniform_scene(n, xy, z, seed, logscale=(-3.0, 0.5)):
     """Means x, y ~ U[-xy, xy], z ~ U[z0, z1]; the rest as the tiny config."""
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -116,22 +139,27 @@ def make(name, n_override=None):
         v = rng.uniform(0, H, 64)
         zc = rng.uniform(4.0, 12.0, 64)
         centres = np.stack([(u - W / 2) * zc / f, (v - H / 2) * zc / f, zc], axis=1)
-        which = rng.integers(0, 64, size=n)
-        means = centres[which] + rng.normal(0.0, 0.1, size=(n, 3))
-        params = _common_params(rng, means, -3.0, 0.5)
+
+        def dense_means(r, m):
+            return centres[r.integers(0, 64, size=m)] + r.normal(0.0, 0.1, size=(m, 3))
+
+        params = _chunked_params(n, seed, dense_means, -3.0, 0.5)
         cams = [camera(np.eye(3), np.zeros(3), f, f, W / 2, H / 2, W, H)]
         steps, sparse = 1, False
     elif idx == 5:
         n = n_override or 100_000_000
         rng = np.random.Generator(np.random.PCG64(seed))
         heights = rng.uniform(0.0, 40.0, size=(20, 20))
-        x = rng.uniform(0.0, 1000.0, n)
-        y = rng.uniform(0.0, 1000.0, n)
-        cx_ = np.minimum((x // 50).astype(np.int64), 19)
-        cy_ = np.minimum((y // 50).astype(np.int64), 19)
-        means = np.stack([x, y, heights[cx_, cy_]], axis=1)
-        params = _common_params(rng, means, -2.0, 0.8)
         cams = city_cameras(rng)
+
+        def city_means(r, m):
+            x = r.uniform(0.0, 1000.0, m)
+            y = r.uniform(0.0, 1000.0, m)
+            cx_ = np.minimum((x // 50).astype(np.int64), 19)
+            cy_ = np.minimum((y // 50).astype(np.int64), 19)
+            return np.stack([x, y, heights[cx_, cy_]], axis=1)
+
+        params = _chunked_params(n, seed, city_means, -2.0, 0.8)
         steps, sparse = 1, True
     else:
         raise KeyError(name)

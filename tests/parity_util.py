@@ -13,9 +13,29 @@ GRAD_REL_L2 = 1e-4
 ADAM_REL_L2 = 1e-4
 # a pixel whose threshold decisions lie within this relative distance of a
 # cut-off may legitimately be decided differently in fp32 (exp error of the
-# fast exponential ~2 ulp + argument rounding ~ |power| ulp, << 1e-5)
+# fast exponential ~2 ulp + argument rounding ~ |power| ulp, << 1e-5; the
+# transmittance is carried to ~2 ulp whatever the number of contributors)
 MARGIN = 1e-5
-MAX_FLAGGED_FRACTION = 2e-3
+
+
+def flagged_allowance(n_pixels, n_pairs, margin=MARGIN):
+    """Upper bound on the pixels flagged by `margin`, from the geometry of the
+    cut-offs (a Poisson count: mean bound E, allowance E + 4 sqrt(E) + 1).
+
+    Alpha cut-offs (1/255 and 0.99): for one Gaussian the pixels whose alpha
+    lies within relative m of a level form an elliptic ring of area
+    4 pi m sqrt(det Sigma) (the region where the power exceeds -p has area
+    2 pi p sqrt(det Sigma)), while the tile rectangle of the pixels that test
+    it holds at least (2r)^2 >= 36 lambda_max >= 36 sqrt(det Sigma) pixels.  A
+    tested pair is thus in one band with probability <= pi m / 9, in either
+    of the two <= 2 pi m / 9.
+
+    Transmittance cut-off (1e-4): the transmittance of a pixel falls by a
+    factor (1 - alpha) <= 1 - 1/255 per contributor, so the values it takes
+    hit a band of relative width 2m about 1e-4 with probability <= 2m / (1/255)
+    = 510 m per pixel."""
+    e = 2.0 * np.pi / 9.0 * margin * n_pairs + 510.0 * margin * n_pixels
+    return e + 4.0 * np.sqrt(e) + 1.0
 
 
 def f32_cams(cams):

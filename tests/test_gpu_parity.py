@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import scenes
-from parity_util import (ADAM_REL_L2, GRAD_REL_L2, IMAGE_MAX_ABS, MARGIN, MAX_FLAGGED_FRACTION,
+from parity_util import (ADAM_REL_L2, GRAD_REL_L2, IMAGE_MAX_ABS, MARGIN, flagged_allowance,
                          PARAM_GROUPS, f32_cams, feats32, grads_to_rows, pack_records, rel_l2,
                          rows_to_grads, unpack_records)
 
@@ -198,7 +198,7 @@ def test_rasterize_fwd_matches_oracle(case):
     err = np.abs(img - fw["image"]).max(axis=1)
     print("flagged pixel fraction %.2e, max err unflagged %.2e, flagged %.2e" %
           (frac, err[ok].max(), err[~ok].max() if (~ok).any() else 0.0))
-    assert frac <= MAX_FLAGGED_FRACTION
+    assert (~ok).sum() <= flagged_allowance(ok.size, int(fw["pairs"].sum()))
     assert err[ok].max() <= IMAGE_MAX_ABS
     assert np.abs(T_final.cpu().numpy() - fw["T_final"])[ok].max() <= IMAGE_MAX_ABS
     assert np.array_equal(n_contrib.cpu().numpy()[ok], fw["n_contrib"][ok])
@@ -306,3 +306,92 @@ def test_train_step_end_to_end(case):
     mo, vo = np.zeros_like(po), np.zeros_like(po)
     oracle.adam(po, grad_o, mo, vo, 1, 1e-3)
     assert rel_l2(step.params.cpu().numpy(), po) <= ADAM_REL_L2
+
+
+def _far_footprints(seed=91, W=256, H=192):
+    """Projected records (fp32) of a street-level situation: elongated
+    footprints whose means lie 50..4000 px off screen with the long axis
+    pointing across the image, mixed with ordinary small splats inside it."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    n_far, n_small = 240, 360
+    n = n_far + n_small
+    mean = np.empty((n, 2))
+    dist = 10.0 ** rng.uniform(np.log10(50.0), np.log10(4000.0), n_far)
+    ang = rng.uniform(0, 2 * np.pi, n_far)
+    centre = np.array([W / 2, H / 2])
+    mean[:n_far] = centre + dist[:, None] * np.stack([np.cos(ang), np.sin(ang)], 1)
+    axis = ang + np.pi + rng.normal(0, 0.02, n_far)  # towards the image, with jitter
+    s_long = dist / rng.uniform(1.5, 3.0, n_far)
+    s_short = rng.uniform(0.2, 2.0, n_far)
+    mean[n_far:] = rng.uniform(-8, [W + 8, H + 8], (n_small, 2))
+    th = rng.uniform(0, np.pi, n_small)
+    s1, s2 = np.exp(rng.normal(0.5, 0.6, (2, n_small)))
+    axis = np.concatenate([axis, th])
+    sl = np.concatenate([s_long, s1])
+    ss = np.concatenate([s_short, s2])
+    c, s = np.cos(axis), np.sin(axis)
+    R = np.stack([np.stack([c, -s], -1), np.stack([s, c], -1)], -2)
+    D = np.zeros((n, 2, 2))
+    D[:, 0, 0], D[:, 1, 1] = sl ** 2, ss ** 2
+    cov = R @ D @ np.swapaxes(R, 1, 2) + 0.3 * np.eye(2)
+    inv = np.linalg.inv(cov)
+    lam = np.linalg.eigvalsh(cov)[:, 1]
+    radius = np.ceil(3.0 * np.sqrt(lam)).astype(np.int32)
+    rec = np.zeros((n, 12), np.float32)
+    rec[:, 0:2] = mean
+    rec[:, 2:5] = np.stack([inv[:, 0, 0], inv[:, 0, 1], inv[:, 1, 1]], 1)
+    rec[:, 5] = rng.uniform(0.02, 1.0, n)
+    rec[:, 6:9] = rng.random((n, 3))
+    rec[:, 9] = rng.uniform(1.0, 50.0, n)
+    ints = rec.view(np.int32)
+    ints[:, 10] = radius
+    tx, ty = (W + 15) // 16, (H + 15) // 16
+    for i in range(n):
+        x0, x1, y0, y1 = oracle.tile_rect(rec[i, 0], rec[i, 1], int(radius[i]), 16, tx, ty)
+        ints[i, 11] = max(0, x1 - x0) * max(0, y1 - y0)
+    ints[ints[:, 11] == 0, 10] = 0
+    return n, W, H, rec
+
+
+def test_far_elongated_footprints():
+    """Binning and compositing (forward and backward) where the means lie far
+    off screen: pixel offsets of thousands of px and near-singular conics,
+    which the literal fp32 exponent gets wrong by order one."""
+    import oracle
+    gs = _gs()
+    n, W, H, rec = _far_footprints()
+    f32 = unpack_records(rec)
+    print("rows %d, on-screen footprints %d, max |mean| %.0f px" %
+          (n, int((f32["radius"] > 0).sum()), np.abs(f32["mean2d"]).max()))
+    _, vals, ranges = oracle.bin_and_sort(n, 1, rec[:, 0:2], f32["radius"], rec[:, 9], W, H)
+    st, I, _, vals_d, ranges_d, _ = _gpu_bin(gs, n, 1, rec, W, H)
+    assert st == gs.GS_OK and I == vals.size
+    assert np.array_equal(vals_d[:I].cpu().numpy().view(np.uint32), vals)
+    assert np.array_equal(ranges_d.cpu().numpy(), ranges)
+    fw = oracle.raster_fwd(n, 1, W, H, f32, vals, ranges)
+    image = torch.empty((1, 3, H, W), device="cuda")
+    T_final = torch.empty((1, H, W), device="cuda")
+    n_contrib = torch.empty((1, H, W), dtype=torch.int32, device="cuda")
+    splats = _cuda(rec)
+    gs.gs_rasterize_fwd(n, 1, splats, W, H, vals_d, ranges_d, (0, 0, 0), image, T_final, n_contrib)
+    ok = fw["margin"] > MARGIN
+    err = np.abs(image.cpu().numpy() - fw["image"]).max(axis=1)
+    print("pairs %d, flagged %d, max err %.2e, max T err %.2e" %
+          (int(fw["pairs"].sum()), int((~ok).sum()), err[ok].max(),
+           np.abs(T_final.cpu().numpy() - fw["T_final"])[ok].max()))
+    assert (~ok).sum() <= flagged_allowance(ok.size, int(fw["pairs"].sum()))
+    assert err[ok].max() <= IMAGE_MAX_ABS
+    assert np.array_equal(n_contrib.cpu().numpy()[ok], fw["n_contrib"][ok])
+    target = scenes.target_images(1, W, H, 91)
+    _, g_img = oracle.loss_l1(fw["image"], target)
+    g_img = g_img.astype(np.float32)
+    g2 = oracle.raster_bwd(n, 1, W, H, f32, vals, ranges, g_img)
+    grads = torch.empty((n, 12), device="cuda")
+    gs.gs_rasterize_bwd(n, 1, splats, W, H, vals_d, ranges_d, (0, 0, 0), T_final, n_contrib,
+                        _cuda(g_img), grads)
+    g = grads_to_rows(grads.cpu().numpy())
+    for f in ("mean2d", "conic", "opacity", "color"):
+        e = rel_l2(g[f], g2[f])
+        print("%s rel-L2 %.2e" % (f, e))
+        assert e <= GRAD_REL_L2, f

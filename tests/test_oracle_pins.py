@@ -285,6 +285,22 @@ def test_binning_brute_force(oracle_mod):
             assert list(ranges[f]) == [sel[0], sel[-1] + 1]
         else:
             assert list(ranges[f]) == [0, 0]
+    # per-tile brute-force lists (used on scenes too large to bin on the CPU)
+    tsel = np.array([0, 17, 100, 255, T + 3, T + 136, 2 * T - 1], np.int64)
+    svals, sranges = oracle_mod.bin_select(n, 2, m32, pr["radius"], d32, 256, 256, tsel)
+    for i, f in enumerate(tsel):
+        want = [v for k, v in items if (k >> 32) == f]
+        a, b = sranges[i]
+        assert [int(v) for v in svals[a:b]] == want
+
+
+def test_threaded_projection_is_identical(oracle_mod):
+    cfg = scenes.make("tiny_2k_256", n_override=1001)
+    cams = [cfg["cams"][0], scenes.camera(np.eye(3), [0.3, -0.2, 0.5], 256, 256, 128, 128, 256, 256)]
+    one = oracle_mod.project(cfg["params"], cams)
+    many = oracle_mod.project(cfg["params"], cams, threads=5)
+    for k in one:
+        assert np.array_equal(one[k], many[k]), k
 
 
 # --------------------------------------------------------------------------

@@ -150,6 +150,7 @@ __device__ __forceinline__ void stage_entry(Batch& B, int j, float ox, float oy,
   // Expansion point: the maximum of the exponent over the tile's pixel-centre
   // box, snapped to the grid.  Inside the box that is the mean; outside, the
   // better of the maxima along the (at most two) edges that face the mean.
+  // Only the choice of z depends on the edge slopes, so they are approximate.
   const float x0 = ox + 0.5f, x1 = ox + 15.5f, y0 = oy + 0.5f, y1 = oy + 15.5f;
   const bool inx = mx >= x0 && mx <= x1, iny = my >= y0 && my <= y1;
   float kx, ky;
@@ -164,7 +165,7 @@ __device__ __forceinline__ void stage_entry(Batch& B, int j, float ox, float oy,
     E.P = -INFINITY;
     if (!inx) {  // edge x = X: exponent largest at y = my - (b/c)(X - mx)
       const float X = mx < x0 ? x0 : x1;
-      const float ys = __fsub_rn(my, __fmul_rn(__fdiv_rn(cb, cc), __fsub_rn(X, mx)));
+      const float ys = __fsub_rn(my, __fmul_rn(__fdividef(cb, cc), __fsub_rn(X, mx)));
       const float gx = snap(X, ox), gy = snap(ys, oy);
       E = expand_at(ox + gx + 0.5f, oy + gy + 0.5f, mx, my, ca, cb, cc, lno);
       kx = gx;
@@ -172,7 +173,7 @@ __device__ __forceinline__ void stage_entry(Batch& B, int j, float ox, float oy,
     }
     if (!iny) {  // edge y = Y: exponent largest at x = mx - (b/a)(Y - my)
       const float Y = my < y0 ? y0 : y1;
-      const float xs = __fsub_rn(mx, __fmul_rn(__fdiv_rn(cb, ca), __fsub_rn(Y, my)));
+      const float xs = __fsub_rn(mx, __fmul_rn(__fdividef(cb, ca), __fsub_rn(Y, my)));
       const float gx = snap(xs, ox), gy = snap(Y, oy);
       const Expansion E2 = expand_at(ox + gx + 0.5f, oy + gy + 0.5f, mx, my, ca, cb, cc, lno);
       if (kx < 0.f || E2.P > E.P) {
@@ -186,19 +187,22 @@ __device__ __forceinline__ void stage_entry(Batch& B, int j, float ox, float oy,
   B.b[j] = make_float4(-cb, -0.5f * cc, kx, ky);
   B.c[j] = make_float4(Bv.z, Bv.w, Cv.x, o);
   if (e_out) e_out[j] = make_float2(E.ex, E.ey);
-  // bounding box in grid indices of the tile: the ellipse centre sits at
-  // index k - e
+  // bounding box in grid indices of the tile: pixel k's centre is at index
+  // coordinate k and the ellipse centre at k - e; the padding (1e-3 px +
+  // 1e-4 hw) exceeds the rounding of k - e (|e| <= hw + 16 when the ellipse
+  // reaches the tile)
   char4 box = make_char4(16, -1, 16, -1);  // empty
   const float q = 2.f * (kLn255 + lno + kPrefilterMargin);
   if (q > 0.f) {
     const float w = __fmul_rn(cb, cb);
     const float det = __fadd_rn(__fmaf_rn(ca, cc, -w), __fmaf_rn(-cb, cb, w));
-    const float hw = sqrtf(q * cc / det) * 1.0001f + 1e-3f;
-    const float hh = sqrtf(q * ca / det) * 1.0001f + 1e-3f;
+    const float qr = q * __frcp_rn(det);  // inf for det 0, < 0 if indefinite
+    const float hw = sqrtf(qr * cc) * 1.0001f + 1e-3f;
+    const float hh = sqrtf(qr * ca) * 1.0001f + 1e-3f;
     if (hw >= 0.f && hh >= 0.f) {  // false for NaN (an indefinite Q): keep all
       const float cxk = kx - E.ex, cyk = ky - E.ey;
-      box = make_char4(clamp_index(floorf(cxk - hw)), clamp_index(ceilf(cxk + hw)),
-                       clamp_index(floorf(cyk - hh)), clamp_index(ceilf(cyk + hh)));
+      box = make_char4(clamp_index(ceilf(cxk - hw)), clamp_index(floorf(cxk + hw)),
+                       clamp_index(ceilf(cyk - hh)), clamp_index(floorf(cyk + hh)));
     } else {
       box = make_char4(-1, 16, -1, 16);
     }

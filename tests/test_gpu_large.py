@@ -318,7 +318,7 @@ def test_city_100m_sparse():
     cs = np.sort(cols[rng.choice(cols.size, min(200_000, cols.size), replace=False)])
     csd = torch.from_numpy(cs).cuda()
     g_sel = step.grad[:, csd].cpu().numpy().astype(np.float64)
-    po = params[:, cs].astype(np.float64)
+    po = np.ascontiguousarray(params[:, cs], dtype=np.float64)
     mo, vo = np.zeros_like(po), np.zeros_like(po)
     oracle.adam(po, g_sel, mo, vo, 1, cfg["lr"])
     assert rel_l2(dev_params[:, csd].cpu().numpy(), po) <= ADAM_REL_L2

@@ -149,40 +149,26 @@ __device__ __forceinline__ void stage_entry(Batch& B, int j, float ox, float oy,
   const float lno = __logf(o);
   // Expansion point: the maximum of the exponent over the tile's pixel-centre
   // box, snapped to the grid.  Inside the box that is the mean; outside, the
-  // better of the maxima along the (at most two) edges that face the mean.
-  // Only the choice of z depends on the edge slopes, so they are approximate.
+  // better of the maxima along the (at most two) edges that face the mean,
+  // compared by a plain fp32 quadratic (a wrong pick can only happen between
+  // near-equal candidates, either of which serves).  Only the choice of z
+  // depends on these approximate values; selects keep the warp converged.
   const float x0 = ox + 0.5f, x1 = ox + 15.5f, y0 = oy + 0.5f, y1 = oy + 15.5f;
   const bool inx = mx >= x0 && mx <= x1, iny = my >= y0 && my <= y1;
-  float kx, ky;
-  Expansion E;
-  if (inx && iny) {
-    kx = snap(mx, ox);
-    ky = snap(my, oy);
-    E = expand_at(ox + kx + 0.5f, oy + ky + 0.5f, mx, my, ca, cb, cc, lno);
-  } else {
-    kx = -1.f;
-    ky = -1.f;
-    E.P = -INFINITY;
-    if (!inx) {  // edge x = X: exponent largest at y = my - (b/c)(X - mx)
-      const float X = mx < x0 ? x0 : x1;
-      const float ys = __fsub_rn(my, __fmul_rn(__fdividef(cb, cc), __fsub_rn(X, mx)));
-      const float gx = snap(X, ox), gy = snap(ys, oy);
-      E = expand_at(ox + gx + 0.5f, oy + gy + 0.5f, mx, my, ca, cb, cc, lno);
-      kx = gx;
-      ky = gy;
-    }
-    if (!iny) {  // edge y = Y: exponent largest at x = mx - (b/a)(Y - my)
-      const float Y = my < y0 ? y0 : y1;
-      const float xs = __fsub_rn(mx, __fmul_rn(__fdividef(cb, ca), __fsub_rn(Y, my)));
-      const float gx = snap(xs, ox), gy = snap(Y, oy);
-      const Expansion E2 = expand_at(ox + gx + 0.5f, oy + gy + 0.5f, mx, my, ca, cb, cc, lno);
-      if (kx < 0.f || E2.P > E.P) {
-        kx = gx;
-        ky = gy;
-        E = E2;
-      }
-    }
-  }
+  const float X = mx < x0 ? x0 : x1, Y = my < y0 ? y0 : y1;
+  const float ys = my - __fdividef(cb, cc) * (X - mx);  // edge x = X
+  const float xs = mx - __fdividef(cb, ca) * (Y - my);  // edge y = Y
+  const float c1x = !inx ? X : (!iny ? xs : mx), c1y = !inx ? ys : (!iny ? Y : my);
+  const float c2x = (!inx && !iny) ? xs : c1x, c2y = (!inx && !iny) ? Y : c1y;
+  const float k1x = snap(c1x, ox), k1y = snap(c1y, oy);
+  const float k2x = snap(c2x, ox), k2y = snap(c2y, oy);
+  const float d1x = ox + k1x + 0.5f - mx, d1y = oy + k1y + 0.5f - my;
+  const float d2x = ox + k2x + 0.5f - mx, d2y = oy + k2y + 0.5f - my;
+  const float s1 = ca * d1x * d1x + 2.f * cb * d1x * d1y + cc * d1y * d1y;
+  const float s2 = ca * d2x * d2x + 2.f * cb * d2x * d2y + cc * d2y * d2y;
+  const bool second = s2 < s1;
+  const float kx = second ? k2x : k1x, ky = second ? k2y : k1y;
+  const Expansion E = expand_at(ox + kx + 0.5f, oy + ky + 0.5f, mx, my, ca, cb, cc, lno);
   B.a[j] = make_float4(E.gx, E.gy, E.P, -0.5f * ca);
   B.b[j] = make_float4(-cb, -0.5f * cc, kx, ky);
   B.c[j] = make_float4(Bv.z, Bv.w, Cv.x, o);
@@ -196,10 +182,12 @@ __device__ __forceinline__ void stage_entry(Batch& B, int j, float ox, float oy,
   if (q > 0.f) {
     const float w = __fmul_rn(cb, cb);
     const float det = __fadd_rn(__fmaf_rn(ca, cc, -w), __fmaf_rn(-cb, cb, w));
-    const float qr = q * __frcp_rn(det);  // inf for det 0, < 0 if indefinite
-    const float hw = sqrtf(qr * cc) * 1.0001f + 1e-3f;
-    const float hh = sqrtf(qr * ca) * 1.0001f + 1e-3f;
-    if (hw >= 0.f && hh >= 0.f) {  // false for NaN (an indefinite Q): keep all
+    // approximate division and square root: the 1e-4 relative padding covers
+    // their few-ulp errors; det 0 gives inf or NaN, an indefinite Q NaN
+    const float qx = __fdividef(q * cc, det), qy = __fdividef(q * ca, det);
+    const float hw = qx * rsqrtf(qx) * 1.0001f + 1e-3f;
+    const float hh = qy * rsqrtf(qy) * 1.0001f + 1e-3f;
+    if (hw >= 0.f && hh >= 0.f && hw < 1e30f && hh < 1e30f) {  // else keep all
       const float cxk = kx - E.ex, cyk = ky - E.ey;
       box = make_char4(clamp_index(ceilf(cxk - hw)), clamp_index(floorf(cxk + hw)),
                        clamp_index(ceilf(cyk - hh)), clamp_index(floorf(cyk + hh)));
@@ -212,15 +200,13 @@ __device__ __forceinline__ void stage_entry(Batch& B, int j, float ox, float oy,
 
 // ln o + power of a staged entry at the pixel with grid index (ix, iy), with
 // a fixed rounding sequence shared by the forward and the backward so both
-// take identical decisions.  t1, t2 return partial sums the backward reuses:
-//   t1 = G_x - a l_x / 2 - b l_y,   t2 = G_y - c l_y / 2.
+// take identical decisions; (lx, ly) = l, the exact offsets from z.
 __device__ __forceinline__ float pair_exponent(const float4& A, const float4& Bv, float ix,
-                                               float iy, float& lx, float& ly, float& t1,
-                                               float& t2) {
+                                               float iy, float& lx, float& ly) {
   lx = __fsub_rn(ix, Bv.z);
   ly = __fsub_rn(iy, Bv.w);
-  t1 = __fmaf_rn(A.w, lx, __fmaf_rn(Bv.x, ly, A.x));
-  t2 = __fmaf_rn(Bv.y, ly, A.y);
+  const float t1 = __fmaf_rn(A.w, lx, __fmaf_rn(Bv.x, ly, A.x));  // G_x - a l_x/2 - b l_y
+  const float t2 = __fmaf_rn(Bv.y, ly, A.y);                      // G_y - c l_y/2
   return __fmaf_rn(lx, t1, __fmaf_rn(ly, t2, A.z));
 }
 
@@ -358,8 +344,8 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
           const int j = wl[i];
           const float4 A = B.a[j];
           const float4 Bv = B.b[j];
-          float lx, ly, t1, t2;
-          const float ex = pair_exponent(A, Bv, ix, iy, lx, ly, t1, t2);
+          float lx, ly;
+          const float ex = pair_exponent(A, Bv, ix, iy, lx, ly);
           if (ex < kExpSkip) continue;
           const float alpha = fminf(kAlphaMax, __expf(ex));
           if (alpha < kAlphaMin) continue;
@@ -547,8 +533,8 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
       if (pos < last) {
         const float4 A = B.a[j];
         const float4 Bv = B.b[j];
-        float lx, ly, t1, t2;
-        const float ex = pair_exponent(A, Bv, ix, iy, lx, ly, t1, t2);
+        float lx, ly;
+        const float ex = pair_exponent(A, Bv, ix, iy, lx, ly);
         if (ex >= kExpSkip) {
           const float raw = __expf(ex);
           const float alpha = fminf(kAlphaMax, raw);
@@ -569,17 +555,17 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
             S2 += w * Cv.z;
             Tr = Ti;
             if (raw < kAlphaMax) {
-              // dL/dpower; the opacity gradient is dL/dpower / o, applied at
-              // the flush (d alpha / d o = e^power = alpha / o)
+              // moments of dL/dpower over the entry's pixels in the offsets
+              // l = p - z; the flush turns them into the mean, conic and
+              // opacity gradients with d = l + e
               const float dpow = dalpha * raw;
-              const float2 e = E[j];
-              const float dx = lx + e.x, dy = ly + e.y;  // p - m
+              const float p1 = dpow * lx, p2 = dpow * ly;
+              v[0] = p1;
+              v[1] = p2;
+              v[2] = p1 * lx;
+              v[3] = p1 * ly;
+              v[4] = p2 * ly;
               v[5] = dpow;
-              v[0] = -dpow * (t1 + A.w * lx);              // dpow (Q d)_x
-              v[1] = -dpow * (t2 + Bv.y * ly + Bv.x * lx);  // dpow (Q d)_y
-              v[2] = -0.5f * dpow * dx * dx;
-              v[3] = -dpow * dx * dy;
-              v[4] = -0.5f * dpow * dy * dy;
             }
           }
         }
@@ -612,9 +598,24 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
       for (int c = 0; c < 9; ++c) nz |= a[c] != 0.f;
       if (nz) {
         float4* dst = grads + 3 * (view * n + (int64_t)S.id[k & 1][tid]);
-        const float dop = a[5] / B.c[tid].w;
-        atomicAdd(dst, make_float4(a[0], a[1], a[2], a[3]));
-        atomicAdd(dst + 1, make_float4(a[4], dop, a[6], a[7]));
+        // with s = sum dL/dpower, sx = sum dL/dpower l_x, ... and d = l + e:
+        //   dL/dm = Q sum dL/dpower d = Q (sx, sy) - s G   (G = -Q e, staged
+        //   to full precision: Q e itself cancels for far, elongated
+        //   footprints),  dL/d(a, b, c) = -(1/2, 1, 1/2) sum dL/dpower
+        //   (d_x^2, d_x d_y, d_y^2),  dL/do = s / o
+        const float s0 = a[5], sx = a[0], sy = a[1];
+        const float2 e = E[tid];
+        const float4 A = B.a[tid], Bv = B.b[tid];
+        const float ca = -2.f * A.w, cb = -Bv.x, cc = -2.f * Bv.y;
+        const float gmx = ca * sx + cb * sy - s0 * A.x;
+        const float gmy = cb * sx + cc * sy - s0 * A.y;
+        const float dy = sy + e.y * s0;  // sum dL/dpower d_y
+        const float gca = -0.5f * (a[2] + e.x * (2.f * sx + e.x * s0));
+        const float gcb = -(a[3] + e.x * dy + e.y * sx);
+        const float gcc = -0.5f * (a[4] + e.y * (2.f * sy + e.y * s0));
+        const float dop = s0 / B.c[tid].w;  // staged opacity
+        atomicAdd(dst, make_float4(gmx, gmy, gca, gcb));
+        atomicAdd(dst + 1, make_float4(gcc, dop, a[6], a[7]));
         atomicAdd(reinterpret_cast<float*>(dst + 2), a[8]);
       }
 #pragma unroll

@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate", action="store_true",
+                    help="composite with three calls (forward, L1 loss, backward) instead of the "
+                         "fused one")
     ap.add_argument("--gaussians", type=int, default=None,
                     help="override the Gaussian count (smaller profiling cases)")
     return ap.parse_args()
@@ -155,15 +158,21 @@ class ClockSampler:
 
 # DRAM bytes (read + write) per launch of the compositing kernels, from one
 # ncu capture of this workload at full size (profiles/
-# raster_kernels_ring_3m_4x1080p.md).  They describe the kernel source whose
+# raster_kernels_ring_3m_4x1080p.md, profiles/fused_vs_separate_ring_3m_4x1080p.md).  They describe the kernel source whose
 # SHA-256 is given; for any other source the figure is unknown (null).
 TRAFFIC = {
+    "rasterize_fused": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
+                        "sha256": "2bdee8392e9c24e2cf8617b04e6359b705d32ed7f7d59986c50f16f646c24145",
+                        "workload": "ring_3m_4x1080p", "bytes": 2520894720 + 477008384},
     "rasterize_fwd": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                      "sha256": "29e3111df48ccc312acdc4168a98e0e4c1257f70e45b91e2754c691acdebe27c",
-                      "workload": "ring_3m_4x1080p", "bytes": 1299473152 + 166023168},
+                      "sha256": "2bdee8392e9c24e2cf8617b04e6359b705d32ed7f7d59986c50f16f646c24145",
+                      "workload": "ring_3m_4x1080p", "bytes": 1274763264 + 165787648},
     "rasterize_bwd": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                      "sha256": "29e3111df48ccc312acdc4168a98e0e4c1257f70e45b91e2754c691acdebe27c",
-                      "workload": "ring_3m_4x1080p", "bytes": 1865764096 + 274212608},
+                      "sha256": "2bdee8392e9c24e2cf8617b04e6359b705d32ed7f7d59986c50f16f646c24145",
+                      "workload": "ring_3m_4x1080p", "bytes": 1865142272 + 273531648},
+    "loss_l1": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu",
+                "sha256": "1b3c39884400d63f87b874f6bcd6364883bd4f7cef6e3efb5109988a49505279",
+                "workload": "ring_3m_4x1080p", "bytes": 199116288 + 38548224},
 }
 
 
@@ -306,11 +315,14 @@ def our_arm(args, rank, world, local):
     params0 = torch.tensor(cfg["params"], device=dev)
     target_host = torch.from_numpy(cfg["target"]).pin_memory()
     target = target_host.to(dev)
-    step = gs.TrainStep(params0.clone(), cams, target, lr=cfg["lr"], sparse=cfg["sparse_adam"])
+    fused = not args.separate
+    step = gs.TrainStep(params0.clone(), cams, target, lr=cfg["lr"], sparse=cfg["sparse_adam"],
+                        fused=fused)
     stream = torch.cuda.current_stream()
     passes = (gs.gs_key_bits(V, W, H) + 7) // 8
-    # project, scan, emit, digit scan, P passes, ranges, fwd, loss, bwd, project_bwd, adam
-    kernels_per_step = 10 + passes
+    # project, scan, emit, digit scan, P passes, ranges, (fused | fwd, loss, bwd), project_bwd,
+    # adam
+    kernels_per_step = (8 if fused else 10) + passes
 
     # warm-up (sizes the intersection buffers)
     for _ in range(max(args.warmup, 3)):
@@ -328,10 +340,15 @@ def our_arm(args, rank, world, local):
     visible_rows = int((step.splats.view(torch.int32)[:, 10] > 0).sum().item())
     I = step.n_isect
 
-    names = ["project", "bin_and_sort", "rasterize_fwd", "loss_l1", "rasterize_bwd",
-             "project_bwd", "adam"]
-    calls = [step.project, step.bin_and_sort, step.rasterize_fwd, step.loss_l1,
-             step.rasterize_bwd, step.project_bwd, step.adam]
+    if fused:
+        names = ["project", "bin_and_sort", "rasterize_fused", "project_bwd", "adam"]
+        calls = [step.project, step.bin_and_sort, step.rasterize_fused, step.project_bwd,
+                 step.adam]
+    else:
+        names = ["project", "bin_and_sort", "rasterize_fwd", "loss_l1", "rasterize_bwd",
+                 "project_bwd", "adam"]
+        calls = [step.project, step.bin_and_sort, step.rasterize_fwd, step.loss_l1,
+                 step.rasterize_bwd, step.project_bwd, step.adam]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
           for _ in range(args.steps)]
 
@@ -394,6 +411,12 @@ def our_arm(args, rank, world, local):
                         hbm_peak),
         "adam": ("hbm", ADAM_BYTES * n / 1e9, "GB/s", hbm_peak),
     }
+    if fused:
+        # one kernel does the forward, the loss and the backward
+        kern["rasterize_fused"] = ("alu", (fwd_flops + bwd_flops) / 1e12, "TFLOP/s",
+                                   fp32_peak_tflops)
+        for nm in ("rasterize_fwd", "rasterize_bwd", "loss_l1"):
+            del kern[nm]
     kernels = {}
     for nm, (bound, work, unit, peak) in kern.items():
         ach = work / (per_kernel[nm] / 1e3)
@@ -407,7 +430,8 @@ def our_arm(args, rank, world, local):
                 "traffic": traffic_of(dom, args.workload, args.gaussians),
                 "peak_source": (peak_kind + " HBM copy") if d["bound"] == "hbm" else
                 ("FP32 lanes x 2 x median SM clock %.0f MHz, %d SMs" % (sm_mhz, sms))}
-    raster_ms = per_kernel["rasterize_fwd"] + per_kernel["loss_l1"] + per_kernel["rasterize_bwd"]
+    raster_ms = (per_kernel["rasterize_fused"] if fused else
+                 per_kernel["rasterize_fwd"] + per_kernel["loss_l1"] + per_kernel["rasterize_bwd"])
     line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -415,7 +439,8 @@ def our_arm(args, rank, world, local):
             "config": {"workload": args.workload, "gaussians": n, "views": V, "width": W,
                        "height": H, "intersections": I, "l2": "inputs larger than L2 "
                        "(708 MB parameters, 2.1 GB with Adam state)", "adam": "sparse" if
-                       cfg["sparse_adam"] else "dense"},
+                       cfg["sparse_adam"] else "dense", "compositing": "fused" if fused else
+                       "separate"},
             "mpix_per_s": round(V * W * H / (raster_ms / 1e3) / 1e6, 2),
             "gaussians_per_s": round(n * V / (ms_step / 1e3), 1),
             "gpu_launches": kernels_per_step * args.steps,

@@ -61,6 +61,8 @@ def lib():
     L.gs_rasterize_fwd_counted.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     L.gs_loss_l1.argtypes = [vp, vp, i64, vp, vp, vp]
     L.gs_rasterize_bwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.gs_rasterize_fused.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     vp]
     L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp]
     L.gs_adam_step.argtypes = [i64, vp, vp, vp, vp, i64, f32, f32, f32, f32, vp, vp]
     L.gs_status_string.argtypes = [C.c_int]
@@ -202,6 +204,17 @@ def gs_rasterize_bwd(n, n_views, splats, width, height, vals, ranges, bg, T_fina
         _stream(stream)))
 
 
+def gs_rasterize_fused(n, n_views, splats, width, height, vals, ranges, bg, target, image,
+                       T_final, n_contrib, loss, grads, stream=None):
+    bgv = (C.c_float * 3)(*[float(b) for b in bg])
+    _check("gs_rasterize_fused", lib().gs_rasterize_fused(
+        n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(target, torch.float32, "target"), _dev(image, torch.float32, "image"),
+        _dev(T_final, torch.float32, "T_final"), _dev(n_contrib, torch.int32, "n_contrib"),
+        _dev(loss, torch.float32, "loss"), _dev(grads, torch.float32, "grads"), _stream(stream)))
+
+
 def gs_project_bwd(params, cams, splats, grads, grad, visible=None, stream=None):
     n = params.shape[1]
     cs = cameras_struct(cams)
@@ -230,10 +243,17 @@ class TrainStep:
     torch) and runs the seven library calls of a step in order.
 
     params: CUDA float32 [59][n]; target: CUDA float32 [V][3][H][W].
-    sparse: use the visibility-masked Adam update."""
+    sparse: use the visibility-masked Adam update.
+    fused: step() composites forward, L1 loss and backward in one call
+    (gs_rasterize_fused) instead of three.
+    sqrt_batch_lr: scale the learning rate by sqrt(V) for a batch of V views
+    ("On Scaling Up 3D Gaussian Splatting Training", independent-gradients
+    answer: with the gradient averaged over b views Adam's second moment
+    falls as 1/b, and lr sqrt(b) approximates b batch-size-1 updates)."""
 
     def __init__(self, params, cams, target, lr=1e-3, betas=(0.9, 0.999), eps=1e-8,
-                 sparse=False, bg=(0.0, 0.0, 0.0), capacity=None):
+                 sparse=False, bg=(0.0, 0.0, 0.0), capacity=None, sqrt_batch_lr=False,
+                 fused=False):
         lib()
         dev = params.device
         self.params = params
@@ -244,6 +264,8 @@ class TrainStep:
         self.T = tiles_per_view(self.W, self.H)
         self.target = target
         self.lr, self.betas, self.eps, self.sparse, self.bg = lr, betas, eps, sparse, tuple(bg)
+        self.lr_step = lr * math.sqrt(self.V) if sqrt_batch_lr else lr
+        self.fused = bool(fused)
         rows = self.V * self.n
         f32 = dict(device=dev, dtype=torch.float32)
         self.splats = torch.empty((rows, SPLAT_FLOATS), **f32)
@@ -302,13 +324,18 @@ class TrainStep:
         gs_rasterize_bwd(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges, self.bg,
                          self.T_final, self.n_contrib, self.dL_dimage, self.grads2d, stream)
 
+    def rasterize_fused(self, stream=None):
+        gs_rasterize_fused(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges,
+                           self.bg, self.target, self.image, self.T_final, self.n_contrib,
+                           self.loss, self.grads2d, stream)
+
     def project_bwd(self, stream=None):
         gs_project_bwd(self.params, self.cams, self.splats, self.grads2d, self.grad, self.visible,
                        stream)
 
     def adam(self, stream=None):
         self.t += 1
-        gs_adam_step(self.params, self.grad, self.m, self.v, self.t, self.lr, self.betas[0],
+        gs_adam_step(self.params, self.grad, self.m, self.v, self.t, self.lr_step, self.betas[0],
                      self.betas[1], self.eps, self.visible if self.sparse else None, stream)
 
     def forward(self, stream=None):
@@ -326,7 +353,13 @@ class TrainStep:
         self.adam(stream)
 
     def step(self, stream=None):
-        self.forward(stream)
-        self.backward(stream)
+        if self.fused:
+            self.project(stream)
+            self.bin_and_sort(stream)
+            self.rasterize_fused(stream)
+            self.project_bwd(stream)
+        else:
+            self.forward(stream)
+            self.backward(stream)
         self.update(stream)
         return self.loss

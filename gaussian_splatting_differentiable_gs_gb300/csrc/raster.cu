@@ -238,174 +238,6 @@ __device__ __forceinline__ void pixel_of(int p, int tile_x, int tile_y, int& px,
   py = tile_y * GS_TILE + (warp >> 1) * 4 + (lane >> 3);
 }
 
-struct FwdSmem {
-  Batch b[2];
-  float T[kRT], Tl[kRT], C0[kRT], C1[kRT], C2[kRT];   // pixel state, by pixel
-  int32_t last[kRT];
-  int32_t done[kRT];
-  int32_t list[kRT];                          // open pixels, packed
-  int32_t wcount[kWarps];
-  uint8_t wl[kWarps][kRT];                   // per-warp entry sub-lists
-};
-
-// kCount: also accumulate the pairs tested / included into counts[0..1]
-// (instrumentation for work accounting: "tested" counts every list entry a
-// pixel passes before it stops, whether or not its box was visited).
-template <bool kCount>
-__global__ void __launch_bounds__(kRT) raster_fwd_kernel(
-    int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
-    const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
-    float bg2, float* __restrict__ image, float* __restrict__ T_final,
-    int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ counts) {
-  __shared__ FwdSmem S;
-  unsigned long long n_tested = 0, n_included = 0;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t flat = blockIdx.x;
-  const int64_t view = flat / T;
-  const int32_t tile = (int32_t)(flat - view * T);
-  const int tile_x = tile % tiles_x, tile_y = tile / tiles_x;
-  const float ox = (float)(tile_x * GS_TILE), oy = (float)(tile_y * GS_TILE);
-  {
-    int px, py;
-    pixel_of(tid, tile_x, tile_y, px, py);
-    S.T[tid] = 1.f;
-    S.Tl[tid] = 0.f;
-    S.C0[tid] = S.C1[tid] = S.C2[tid] = 0.f;
-    S.last[tid] = 0;
-    S.done[tid] = (px < W && py < H) ? 0 : 1;
-  }
-  const int64_t start = ranges[2 * flat], end = ranges[2 * flat + 1];
-  const int64_t len = end - start;
-  const int nb = (int)((len + kRT - 1) / kRT);
-  const float4* vsplat = splats + 3 * view * n;
-
-  auto issue = [&](int k) {
-    const int64_t e = start + (int64_t)k * kRT + tid;
-    if (e < end) {
-      // ids come from gs_bin_and_sort; clamping keeps a corrupt list in bounds
-      const uint32_t id = min(__ldg(vals + e), (uint32_t)(n - 1));
-      const float4* src = vsplat + 3 * (int64_t)id;
-      Batch& B = S.b[k & 1];
-      cp_async16(&B.a[tid], src);
-      cp_async16(&B.b[tid], src + 1);
-      cp_async16(&B.c[tid], src + 2);
-    }
-    cp_async_commit();
-  };
-
-  if (nb > 0) issue(0);
-  for (int k = 0; k < nb; ++k) {
-    if (k + 1 < nb) issue(k + 1); else cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();  // batch k landed; state of the previous batch written
-    Batch& B = S.b[k & 1];
-    const int cnt = (int)min((int64_t)kRT, len - (int64_t)k * kRT);
-    if (tid < cnt) stage_entry(B, tid, ox, oy, nullptr);
-    // pack the open pixels onto the first m threads
-    const bool open = !S.done[tid];
-    const unsigned bal = __ballot_sync(0xffffffffu, open);
-    if (lane == 0) S.wcount[warp] = __popc(bal);
-    __syncthreads();
-    int off = 0, m = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const int c = S.wcount[w];
-      off += w < warp ? c : 0;
-      m += c;
-    }
-    if (m == 0) break;
-    if (open) S.list[off + __popc(bal & ((1u << lane) - 1u))] = tid;
-    __syncthreads();
-    if (warp * 32 < m) {
-      const bool worker = tid < m;
-      const int p = worker ? S.list[tid] : 0;
-      int px, py;
-      pixel_of(p, tile_x, tile_y, px, py);
-      const int kx = px - tile_x * GS_TILE, ky = py - tile_y * GS_TILE;  // grid index
-      const float ix = (float)kx, iy = (float)ky;
-      const int x0 = __reduce_min_sync(0xffffffffu, worker ? kx : 1 << 30);
-      const int x1 = __reduce_max_sync(0xffffffffu, worker ? kx : -(1 << 30));
-      const int y0 = __reduce_min_sync(0xffffffffu, worker ? ky : 1 << 30);
-      const int y1 = __reduce_max_sync(0xffffffffu, worker ? ky : -(1 << 30));
-      uint8_t* wl = S.wl[warp];
-      const int nw = warp_sublist(B, cnt, x0, x1, y0, y1, wl, lane);
-      if (worker) {
-        // T is carried as an unevaluated sum Tr + Tl, so its rounding error
-        // does not grow with the number of contributors (city-scale lists
-        // reach 10^4 entries); the colour of this batch is summed apart and
-        // added once at the end of the batch.
-        float Tr = S.T[p], Tl = S.Tl[p];
-        float C0 = 0.f, C1 = 0.f, C2 = 0.f;
-        int32_t last = S.last[p];
-        int done = 0;
-        int stop_j = cnt;
-        const int32_t base1 = k * kRT + 1;  // 1-based list position of entry 0
-        for (int i = 0; i < nw; ++i) {
-          const int j = wl[i];
-          const float4 A = B.a[j];
-          const float4 Bv = B.b[j];
-          float lx, ly;
-          const float ex = pair_exponent(A, Bv, ix, iy, lx, ly);
-          if (ex < kExpSkip) continue;
-          const float alpha = fminf(kAlphaMax, __expf(ex));
-          if (alpha < kAlphaMin) continue;
-          const float om = __fsub_rn(1.f, alpha);
-          const float oml = __fsub_rn(__fsub_rn(1.f, om), alpha);  // 1 - alpha = om + oml
-          const float ph = __fmul_rn(Tr, om);
-          const float lo = __fmaf_rn(Tr, oml, __fmaf_rn(Tl, om, __fmaf_rn(Tr, om, -ph)));
-          const float Tn = __fadd_rn(ph, lo);
-          if (Tn < kTMin) { done = 1; stop_j = j + 1; break; }
-          const float w = __fmul_rn(alpha, Tr);
-          const float4 Cv = B.c[j];
-          C0 = __fmaf_rn(w, Cv.x, C0);
-          C1 = __fmaf_rn(w, Cv.y, C1);
-          C2 = __fmaf_rn(w, Cv.z, C2);
-          Tl = __fsub_rn(lo, __fsub_rn(Tn, ph));
-          Tr = Tn;
-          last = base1 + j;
-          if (kCount) ++n_included;
-        }
-        if (kCount) n_tested += stop_j;
-        S.T[p] = Tr;
-        S.Tl[p] = Tl;
-        S.C0[p] = __fadd_rn(S.C0[p], C0);
-        S.C1[p] = __fadd_rn(S.C1[p], C1);
-        S.C2[p] = __fadd_rn(S.C2[p], C2);
-        S.last[p] = last;
-        S.done[p] = done;
-      }
-    }
-    __syncthreads();  // buffer k & 1 free for batch k + 2
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-  {
-    int px, py;
-    pixel_of(tid, tile_x, tile_y, px, py);
-    if (px < W && py < H) {
-      const int64_t HW = (int64_t)W * H;
-      const int64_t pix = (int64_t)py * W + px;
-      const float Tr = S.T[tid];
-      image[(view * 3 + 0) * HW + pix] = S.C0[tid] + Tr * bg0;
-      image[(view * 3 + 1) * HW + pix] = S.C1[tid] + Tr * bg1;
-      image[(view * 3 + 2) * HW + pix] = S.C2[tid] + Tr * bg2;
-      T_final[view * HW + pix] = Tr;
-      n_contrib[view * HW + pix] = S.last[tid];
-    }
-  }
-  if (kCount) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      n_tested += __shfl_xor_sync(0xffffffffu, n_tested, o);
-      n_included += __shfl_xor_sync(0xffffffffu, n_included, o);
-    }
-    if (lane == 0) {
-      atomicAdd(&counts[0], n_tested);
-      atomicAdd(&counts[1], n_included);
-    }
-  }
-}
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -436,6 +268,329 @@ __device__ __forceinline__ float warp_sum8(const float v[8], int lane) {
   k3 += __shfl_xor_sync(0xffffffffu, k3, 2);
   k3 += __shfl_xor_sync(0xffffffffu, k3, 1);
   return k3;
+}
+
+// Pixel state of a tile during the forward pass, by pixel index.
+struct PixState {
+  float T[kRT], Tl[kRT], C0[kRT], C1[kRT], C2[kRT];  // T = T + Tl (double-float)
+  int32_t last[kRT];
+  int32_t done[kRT];
+  int32_t list[kRT];  // open pixels, packed
+};
+
+__device__ __forceinline__ void pix_init(PixState& P, int tid, int tile_x, int tile_y, int W,
+                                         int H) {
+  int px, py;
+  pixel_of(tid, tile_x, tile_y, px, py);
+  P.T[tid] = 1.f;
+  P.Tl[tid] = 0.f;
+  P.C0[tid] = P.C1[tid] = P.C2[tid] = 0.f;
+  P.last[tid] = 0;
+  P.done[tid] = (px < W && py < H) ? 0 : 1;
+}
+
+// Forward compositing of staged batch k over the m open pixels packed in
+// P.list[0..m): each worker thread takes one open pixel; each warp walks the
+// entries whose box meets its pixels.
+template <bool kCount>
+__device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* wl, int cnt, int k,
+                                          int m, int tile_x, int tile_y, int tid, int warp,
+                                          int lane, unsigned long long& n_tested,
+                                          unsigned long long& n_included) {
+  if (warp * 32 >= m) return;
+  const bool worker = tid < m;
+  const int p = worker ? P.list[tid] : 0;
+  int px, py;
+  pixel_of(p, tile_x, tile_y, px, py);
+  const int kx = px - tile_x * GS_TILE, ky = py - tile_y * GS_TILE;  // grid index
+  const float ix = (float)kx, iy = (float)ky;
+  const int x0 = __reduce_min_sync(0xffffffffu, worker ? kx : 1 << 30);
+  const int x1 = __reduce_max_sync(0xffffffffu, worker ? kx : -(1 << 30));
+  const int y0 = __reduce_min_sync(0xffffffffu, worker ? ky : 1 << 30);
+  const int y1 = __reduce_max_sync(0xffffffffu, worker ? ky : -(1 << 30));
+  const int nw = warp_sublist(B, cnt, x0, x1, y0, y1, wl, lane);
+  if (!worker) return;
+  // T is carried as an unevaluated sum Tr + Tl, so its rounding error does
+  // not grow with the number of contributors (city-scale lists reach 10^4
+  // entries); the colour of this batch is summed apart and added once at the
+  // end of the batch.
+  float Tr = P.T[p], Tl = P.Tl[p];
+  float C0 = 0.f, C1 = 0.f, C2 = 0.f;
+  int32_t last = P.last[p];
+  int done = 0;
+  int stop_j = cnt;
+  const int32_t base1 = k * kRT + 1;  // 1-based list position of entry 0
+  for (int i = 0; i < nw; ++i) {
+    const int j = wl[i];
+    const float4 A = B.a[j];
+    const float4 Bv = B.b[j];
+    float lx, ly;
+    const float ex = pair_exponent(A, Bv, ix, iy, lx, ly);
+    if (ex < kExpSkip) continue;
+    const float alpha = fminf(kAlphaMax, __expf(ex));
+    if (alpha < kAlphaMin) continue;
+    const float om = __fsub_rn(1.f, alpha);
+    const float oml = __fsub_rn(__fsub_rn(1.f, om), alpha);  // 1 - alpha = om + oml
+    const float ph = __fmul_rn(Tr, om);
+    const float lo = __fmaf_rn(Tr, oml, __fmaf_rn(Tl, om, __fmaf_rn(Tr, om, -ph)));
+    const float Tn = __fadd_rn(ph, lo);
+    if (Tn < kTMin) { done = 1; stop_j = j + 1; break; }
+    const float w = __fmul_rn(alpha, Tr);
+    const float4 Cv = B.c[j];
+    C0 = __fmaf_rn(w, Cv.x, C0);
+    C1 = __fmaf_rn(w, Cv.y, C1);
+    C2 = __fmaf_rn(w, Cv.z, C2);
+    Tl = __fsub_rn(lo, __fsub_rn(Tn, ph));
+    Tr = Tn;
+    last = base1 + j;
+    if (kCount) ++n_included;
+  }
+  if (kCount) n_tested += stop_j;
+  P.T[p] = Tr;
+  P.Tl[p] = Tl;
+  P.C0[p] = __fadd_rn(P.C0[p], C0);
+  P.C1[p] = __fadd_rn(P.C1[p], C1);
+  P.C2[p] = __fadd_rn(P.C2[p], C2);
+  P.last[p] = last;
+  P.done[p] = done;
+}
+
+// The forward over a tile's list [start, end): batches of 256 gathered by
+// cp.async into the two slots of `b` (batch k in slot k & 1), one batch
+// ahead.  The open pixels are counted at the end of each batch, before the
+// next one is prefetched, so when every pixel has stopped the last batch
+// composited is still staged in its slot; on return `staged` holds the
+// batch index staged in each slot (-1: none).  With `ids`/`E` the staging
+// also records each entry's id and e = z - m (for a backward that reuses the
+// slots).  slot(s, i) names the batch index staged in slot i.
+__device__ __forceinline__ int& slot(int2& s, int i) { return i ? s.y : s.x; }
+
+template <bool kCount>
+__device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[kRT],
+                                         float2 (*E)[kRT], uint8_t (*wl)[kRT], int32_t* wcount,
+                                         const float4* vsplat, const uint32_t* __restrict__ vals,
+                                         int64_t n, int64_t start, int64_t end, int tile_x,
+                                         int tile_y, float ox, float oy, int tid, int warp,
+                                         int lane, int2& staged,
+                                         unsigned long long& n_tested,
+                                         unsigned long long& n_included) {
+  const int64_t len = end - start;
+  const int nb = (int)((len + kRT - 1) / kRT);
+  staged = make_int2(-1, -1);
+  auto issue = [&](int k) {
+    const int64_t e = start + (int64_t)k * kRT + tid;
+    if (e < end) {
+      // ids come from gs_bin_and_sort; clamping keeps a corrupt list in bounds
+      const uint32_t id = min(__ldg(vals + e), (uint32_t)(n - 1));
+      const float4* src = vsplat + 3 * (int64_t)id;
+      Batch& B = b[k & 1];
+      if (ids) ids[k & 1][tid] = id;
+      cp_async16(&B.a[tid], src);
+      cp_async16(&B.b[tid], src + 1);
+      cp_async16(&B.c[tid], src + 2);
+    }
+    cp_async_commit();
+  };
+  if (nb > 0) issue(0);
+  unsigned bal = __ballot_sync(0xffffffffu, !P.done[tid]);
+  if (lane == 0) wcount[warp] = __popc(bal);
+  for (int k = 0; k < nb; ++k) {
+    cp_async_wait<0>();
+    __syncthreads();  // batch k landed; the open-pixel counts are visible
+    int off = 0, m = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wcount[w];
+      off += w < warp ? c : 0;
+      m += c;
+    }
+    if (m == 0) break;
+    if (k + 1 < nb) {
+      issue(k + 1);
+      slot(staged, (k + 1) & 1) = -1;
+    }
+    Batch& B = b[k & 1];
+    const int cnt = (int)min((int64_t)kRT, len - (int64_t)k * kRT);
+    if (tid < cnt) stage_entry(B, tid, ox, oy, E ? E[k & 1] : nullptr);
+    slot(staged, k & 1) = k;
+    if ((bal >> lane) & 1u) P.list[off + __popc(bal & ((1u << lane) - 1u))] = tid;
+    __syncthreads();
+    fwd_batch<kCount>(P, B, wl[warp], cnt, k, m, tile_x, tile_y, tid, warp, lane, n_tested,
+                      n_included);
+    __syncthreads();  // pixel state written; slot k & 1 free for batch k + 2
+    bal = __ballot_sync(0xffffffffu, !P.done[tid]);
+    if (lane == 0) wcount[warp] = __popc(bal);
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+}
+
+// Backward pairs of staged entries [0, jtop) of one batch (list positions
+// lo + j) for this thread's pixel, back to front; per-entry sums into acc.
+__device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint8_t* wl, int jtop,
+                                          int lo, int wx0, int wx1, int wy0, int wy1, float ix,
+                                          float iy, int last, float& Tr, float& S0, float& S1,
+                                          float& S2, float g0, float g1, float g2, int lane) {
+  const int nw = warp_sublist(B, jtop, wx0, wx1, wy0, wy1, wl, lane);
+  for (int i = nw - 1; i >= 0; --i) {
+    const int j = wl[i];
+    const int pos = lo + j;
+    float v[9];
+#pragma unroll
+    for (int c = 0; c < 9; ++c) v[c] = 0.f;
+    bool contrib = false;
+    if (pos < last) {
+      const float4 A = B.a[j];
+      const float4 Bv = B.b[j];
+      float lx, ly;
+      const float ex = pair_exponent(A, Bv, ix, iy, lx, ly);
+      if (ex >= kExpSkip) {
+        const float raw = __expf(ex);
+        const float alpha = fminf(kAlphaMax, raw);
+        if (alpha >= kAlphaMin) {
+          contrib = true;
+          const float4 Cv = B.c[j];
+          const float oma = 1.f - alpha;
+          const float rinv = 1.f / oma;
+          const float Ti = Tr * rinv;
+          const float w = alpha * Ti;
+          v[6] = w * g0;
+          v[7] = w * g1;
+          v[8] = w * g2;
+          const float dalpha = (g0 * Cv.x + g1 * Cv.y + g2 * Cv.z) * Ti -
+                               (g0 * S0 + g1 * S1 + g2 * S2) * rinv;
+          S0 += w * Cv.x;
+          S1 += w * Cv.y;
+          S2 += w * Cv.z;
+          Tr = Ti;
+          if (raw < kAlphaMax) {
+            // moments of dL/dpower over the entry's pixels in the offsets
+            // l = p - z; the flush turns them into the mean, conic and
+            // opacity gradients with d = l + e
+            const float dpow = dalpha * raw;
+            const float p1 = dpow * lx, p2 = dpow * ly;
+            v[0] = p1;
+            v[1] = p2;
+            v[2] = p1 * lx;
+            v[3] = p1 * ly;
+            v[4] = p2 * ly;
+            v[5] = dpow;
+          }
+        }
+      }
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, contrib);
+    if (bal) {
+      if (__popc(bal) <= 2) {
+        if (contrib) {
+#pragma unroll
+          for (int c = 0; c < 9; ++c) atomicAdd(&acc[j][c], v[c]);
+        }
+      } else {
+        // values 0..7 end on lanes 0,4,...,28 (one shared atomic each);
+        // value 8 by a plain butterfly on lane 0
+        const float s8 = warp_sum8(v, lane);
+        const float s9 = warp_sum(v[8]);
+        if ((lane & 3) == 0) {
+          const int c = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+          atomicAdd(&acc[j][c], s8);
+        }
+        if (lane == 0) atomicAdd(&acc[j][8], s9);
+      }
+    }
+  }
+}
+
+// Flush of a batch's per-entry sums (entries tid < cnt) into the row
+// gradients of the view, then the sums are cleared.
+__device__ __forceinline__ void bwd_flush(const Batch& B, const float2* E, const uint32_t* id,
+                                          float (*acc)[9], int cnt, float4* __restrict__ vgrads,
+                                          int tid) {
+  if (tid >= cnt) return;
+  float* a = acc[tid];
+  bool nz = false;
+#pragma unroll
+  for (int c = 0; c < 9; ++c) nz |= a[c] != 0.f;
+  if (nz) {
+    float4* dst = vgrads + 3 * (int64_t)id[tid];
+    // with s = sum dL/dpower, sx = sum dL/dpower l_x, ... and d = l + e:
+    //   dL/dm = Q sum dL/dpower d = Q (sx, sy) - s G   (G = -Q e, staged to
+    //   full precision: Q e itself cancels for far, elongated footprints),
+    //   dL/d(a, b, c) = -(1/2, 1, 1/2) sum dL/dpower (d_x^2, d_x d_y, d_y^2),
+    //   dL/do = s / o
+    const float s0 = a[5], sx = a[0], sy = a[1];
+    const float2 e = E[tid];
+    const float4 A = B.a[tid], Bv = B.b[tid];
+    const float ca = -2.f * A.w, cb = -Bv.x, cc = -2.f * Bv.y;
+    const float gmx = ca * sx + cb * sy - s0 * A.x;
+    const float gmy = cb * sx + cc * sy - s0 * A.y;
+    const float dy = sy + e.y * s0;  // sum dL/dpower d_y
+    const float gca = -0.5f * (a[2] + e.x * (2.f * sx + e.x * s0));
+    const float gcb = -(a[3] + e.x * dy + e.y * sx);
+    const float gcc = -0.5f * (a[4] + e.y * (2.f * sy + e.y * s0));
+    const float dop = s0 / B.c[tid].w;  // staged opacity
+    atomicAdd(dst, make_float4(gmx, gmy, gca, gcb));
+    atomicAdd(dst + 1, make_float4(gcc, dop, a[6], a[7]));
+    atomicAdd(reinterpret_cast<float*>(dst + 2), a[8]);
+  }
+#pragma unroll
+  for (int c = 0; c < 9; ++c) a[c] = 0.f;
+}
+
+struct FwdSmem {
+  Batch b[2];
+  PixState px;
+  int32_t wcount[kWarps];
+  uint8_t wl[kWarps][kRT];  // per-warp entry sub-lists
+};
+
+// kCount: also accumulate the pairs tested / included into counts[0..1]
+// (instrumentation for work accounting: "tested" counts every list entry a
+// pixel passes before it stops, whether or not its box was visited).
+template <bool kCount>
+__global__ void __launch_bounds__(kRT) raster_fwd_kernel(
+    int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
+    const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
+    float bg2, float* __restrict__ image, float* __restrict__ T_final,
+    int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ counts) {
+  __shared__ FwdSmem S;
+  unsigned long long n_tested = 0, n_included = 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t flat = blockIdx.x;
+  const int64_t view = flat / T;
+  const int32_t tile = (int32_t)(flat - view * T);
+  const int tile_x = tile % tiles_x, tile_y = tile / tiles_x;
+  const float ox = (float)(tile_x * GS_TILE), oy = (float)(tile_y * GS_TILE);
+  pix_init(S.px, tid, tile_x, tile_y, W, H);
+  int2 staged;
+  fwd_tile<kCount>(S.px, S.b, nullptr, nullptr, S.wl, S.wcount, splats + 3 * view * n, vals, n,
+                   ranges[2 * flat], ranges[2 * flat + 1], tile_x, tile_y, ox, oy, tid, warp,
+                   lane, staged, n_tested, n_included);
+  {
+    int px, py;
+    pixel_of(tid, tile_x, tile_y, px, py);
+    if (px < W && py < H) {
+      const int64_t HW = (int64_t)W * H;
+      const int64_t pix = (int64_t)py * W + px;
+      const float Tr = S.px.T[tid];
+      image[(view * 3 + 0) * HW + pix] = S.px.C0[tid] + Tr * bg0;
+      image[(view * 3 + 1) * HW + pix] = S.px.C1[tid] + Tr * bg1;
+      image[(view * 3 + 2) * HW + pix] = S.px.C2[tid] + Tr * bg2;
+      T_final[view * HW + pix] = Tr;
+      n_contrib[view * HW + pix] = S.px.last[tid];
+    }
+  }
+  if (kCount) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n_tested += __shfl_xor_sync(0xffffffffu, n_tested, o);
+      n_included += __shfl_xor_sync(0xffffffffu, n_included, o);
+    }
+    if (lane == 0) {
+      atomicAdd(&counts[0], n_tested);
+      atomicAdd(&counts[1], n_included);
+    }
+  }
 }
 
 struct BwdSmem {
@@ -521,106 +676,155 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
     __syncthreads();
     // positions at or above the warp's last contributor cannot contribute
     const int jtop = max(0, min(cnt, warp_last - lo));
-    uint8_t* wl = S.wl[warp];
-    const int nw = warp_sublist(B, jtop, wx0, wx1, wy0, wy1, wl, lane);
-    for (int i = nw - 1; i >= 0; --i) {
-      const int j = wl[i];
-      const int pos = lo + j;
-      float v[9];
-#pragma unroll
-      for (int c = 0; c < 9; ++c) v[c] = 0.f;
-      bool contrib = false;
-      if (pos < last) {
-        const float4 A = B.a[j];
-        const float4 Bv = B.b[j];
-        float lx, ly;
-        const float ex = pair_exponent(A, Bv, ix, iy, lx, ly);
-        if (ex >= kExpSkip) {
-          const float raw = __expf(ex);
-          const float alpha = fminf(kAlphaMax, raw);
-          if (alpha >= kAlphaMin) {
-            contrib = true;
-            const float4 Cv = B.c[j];
-            const float oma = 1.f - alpha;
-            const float rinv = 1.f / oma;
-            const float Ti = Tr * rinv;
-            const float w = alpha * Ti;
-            v[6] = w * g0;
-            v[7] = w * g1;
-            v[8] = w * g2;
-            const float dalpha = (g0 * Cv.x + g1 * Cv.y + g2 * Cv.z) * Ti -
-                                 (g0 * S0 + g1 * S1 + g2 * S2) * rinv;
-            S0 += w * Cv.x;
-            S1 += w * Cv.y;
-            S2 += w * Cv.z;
-            Tr = Ti;
-            if (raw < kAlphaMax) {
-              // moments of dL/dpower over the entry's pixels in the offsets
-              // l = p - z; the flush turns them into the mean, conic and
-              // opacity gradients with d = l + e
-              const float dpow = dalpha * raw;
-              const float p1 = dpow * lx, p2 = dpow * ly;
-              v[0] = p1;
-              v[1] = p2;
-              v[2] = p1 * lx;
-              v[3] = p1 * ly;
-              v[4] = p2 * ly;
-              v[5] = dpow;
-            }
-          }
-        }
-      }
-      const unsigned bal = __ballot_sync(0xffffffffu, contrib);
-      if (bal) {
-        if (__popc(bal) <= 2) {
-          if (contrib) {
-#pragma unroll
-            for (int c = 0; c < 9; ++c) atomicAdd(&S.acc[j][c], v[c]);
-          }
-        } else {
-          // values 0..7 end on lanes 0,4,...,28 (one shared atomic each);
-          // value 8 by a plain butterfly on lane 0
-          const float s8 = warp_sum8(v, lane);
-          const float s9 = warp_sum(v[8]);
-          if ((lane & 3) == 0) {
-            const int c = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-            atomicAdd(&S.acc[j][c], s8);
-          }
-          if (lane == 0) atomicAdd(&S.acc[j][8], s9);
-        }
-      }
-    }
+    bwd_batch(B, S.acc, S.wl[warp], jtop, lo, wx0, wx1, wy0, wy1, ix, iy, last, Tr, S0, S1, S2,
+              g0, g1, g2, lane);
     __syncthreads();
+    bwd_flush(B, E, S.id[k & 1], S.acc, cnt, grads + 3 * view * n, tid);
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+}
+
+// Forward, L1 loss and backward of one tile in one CTA ("ByteSplat": forward
+// and backward rasterization fused into a single kernel that keeps the
+// intermediates on chip).  The per-pixel results of the forward (T, the last
+// contributor, the colour and its L1 gradient) stay in registers and shared
+// memory instead of a round trip through T_final, n_contrib and dL/dimage,
+// and the batches still staged in shared memory when the forward ends (the
+// last one composited, or the last two when the list runs out) are reused
+// by the backward without a new gather or staging.  The backward walks the
+// forward's batches (0-aligned) from the one holding the tile's last
+// contributor down to the first.
+struct FusedSmem {
+  Batch b[2];
+  float2 e[2][kRT];
+  uint32_t id[2][kRT];
+  union {
+    PixState px;        // forward
+    float acc[kRT][9];  // backward
+  } u;
+  uint8_t wl[kWarps][kRT];
+  int32_t wcount[kWarps];
+  float lsum[kWarps];
+  int max_last;
+};
+
+__global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
+    int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
+    const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
+    float bg2, const float* __restrict__ target, float inv_count, float* __restrict__ image,
+    float* __restrict__ T_final, int32_t* __restrict__ n_contrib, float* __restrict__ loss,
+    float4* __restrict__ grads) {
+  __shared__ FusedSmem S;
+  unsigned long long n_tested = 0, n_included = 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t flat = blockIdx.x;
+  const int64_t view = flat / T;
+  const int32_t tile = (int32_t)(flat - view * T);
+  const int tile_x = tile % tiles_x, tile_y = tile / tiles_x;
+  const float ox = (float)(tile_x * GS_TILE), oy = (float)(tile_y * GS_TILE);
+  const int64_t start = ranges[2 * flat], end = ranges[2 * flat + 1];
+  const float4* vsplat = splats + 3 * view * n;
+  pix_init(S.u.px, tid, tile_x, tile_y, W, H);
+  int2 staged;
+  fwd_tile<false>(S.u.px, S.b, S.id, S.e, S.wl, S.wcount, vsplat, vals, n, start, end, tile_x,
+                  tile_y, ox, oy, tid, warp, lane, staged, n_tested, n_included);
+
+  // forward results, L1 loss and its gradient, in registers; thread tid owns
+  // pixel tid from here on
+  int px, py;
+  pixel_of(tid, tile_x, tile_y, px, py);
+  const bool inside = px < W && py < H;
+  float Tr = S.u.px.T[tid];
+  const int32_t last = inside ? S.u.px.last[tid] : 0;
+  float g0 = 0.f, g1 = 0.f, g2 = 0.f, l1 = 0.f;
+  if (inside) {
+    const int64_t HW = (int64_t)W * H;
+    const int64_t pix = (int64_t)py * W + px;
+    const float c0 = S.u.px.C0[tid] + Tr * bg0;
+    const float c1 = S.u.px.C1[tid] + Tr * bg1;
+    const float c2 = S.u.px.C2[tid] + Tr * bg2;
+    image[(view * 3 + 0) * HW + pix] = c0;
+    image[(view * 3 + 1) * HW + pix] = c1;
+    image[(view * 3 + 2) * HW + pix] = c2;
+    T_final[view * HW + pix] = Tr;
+    n_contrib[view * HW + pix] = last;
+    auto sgn = [&](float d) { return d > 0.f ? inv_count : (d < 0.f ? -inv_count : 0.f); };
+    const float d0 = c0 - __ldcs(target + (view * 3 + 0) * HW + pix);
+    const float d1 = c1 - __ldcs(target + (view * 3 + 1) * HW + pix);
+    const float d2 = c2 - __ldcs(target + (view * 3 + 2) * HW + pix);
+    l1 = fabsf(d0) + fabsf(d1) + fabsf(d2);
+    g0 = sgn(d0);
+    g1 = sgn(d1);
+    g2 = sgn(d2);
+  } else {
+    Tr = 0.f;
+  }
+  l1 = warp_sum(l1);
+  if (lane == 0) S.lsum[warp] = l1;
+  if (tid == 0) S.max_last = 0;
+  __syncthreads();  // the forward's pixel state is read; its space becomes acc
+  for (int i = tid; i < kRT * 9; i += kRT) (&S.u.acc[0][0])[i] = 0.f;
+  const int warp_last = __reduce_max_sync(0xffffffffu, last);
+  if (lane == 0) atomicMax(&S.max_last, warp_last);
+  if (tid == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += S.lsum[w];
+    atomicAdd(loss, t * inv_count);
+  }
+  __syncthreads();
+  const int max_last = S.max_last;
+  const float ix = (float)(px - tile_x * GS_TILE), iy = (float)(py - tile_y * GS_TILE);
+  const int wx0 = (warp & 1) * 8, wx1 = wx0 + 7;
+  const int wy0 = (warp >> 1) * 4, wy1 = wy0 + 3;
+  float S0 = Tr * bg0, S1 = Tr * bg1, S2 = Tr * bg2;
+
+  // backward: batch k covers list positions [k*256, min((k+1)*256, max_last))
+  // in slot k & 1, gathered and staged unless the forward left it there
+  auto issue = [&](int k) {
+    const int lo = k * kRT;
+    const int cnt = min(kRT, max_last - lo);
     if (tid < cnt) {
-      float* a = S.acc[tid];
-      bool nz = false;
-#pragma unroll
-      for (int c = 0; c < 9; ++c) nz |= a[c] != 0.f;
-      if (nz) {
-        float4* dst = grads + 3 * (view * n + (int64_t)S.id[k & 1][tid]);
-        // with s = sum dL/dpower, sx = sum dL/dpower l_x, ... and d = l + e:
-        //   dL/dm = Q sum dL/dpower d = Q (sx, sy) - s G   (G = -Q e, staged
-        //   to full precision: Q e itself cancels for far, elongated
-        //   footprints),  dL/d(a, b, c) = -(1/2, 1, 1/2) sum dL/dpower
-        //   (d_x^2, d_x d_y, d_y^2),  dL/do = s / o
-        const float s0 = a[5], sx = a[0], sy = a[1];
-        const float2 e = E[tid];
-        const float4 A = B.a[tid], Bv = B.b[tid];
-        const float ca = -2.f * A.w, cb = -Bv.x, cc = -2.f * Bv.y;
-        const float gmx = ca * sx + cb * sy - s0 * A.x;
-        const float gmy = cb * sx + cc * sy - s0 * A.y;
-        const float dy = sy + e.y * s0;  // sum dL/dpower d_y
-        const float gca = -0.5f * (a[2] + e.x * (2.f * sx + e.x * s0));
-        const float gcb = -(a[3] + e.x * dy + e.y * sx);
-        const float gcc = -0.5f * (a[4] + e.y * (2.f * sy + e.y * s0));
-        const float dop = s0 / B.c[tid].w;  // staged opacity
-        atomicAdd(dst, make_float4(gmx, gmy, gca, gcb));
-        atomicAdd(dst + 1, make_float4(gcc, dop, a[6], a[7]));
-        atomicAdd(reinterpret_cast<float*>(dst + 2), a[8]);
-      }
-#pragma unroll
-      for (int c = 0; c < 9; ++c) a[c] = 0.f;
+      const uint32_t id = min(__ldg(vals + start + lo + tid), (uint32_t)(n - 1));
+      const float4* src = vsplat + 3 * (int64_t)id;
+      Batch& B = S.b[k & 1];
+      S.id[k & 1][tid] = id;
+      cp_async16(&B.a[tid], src);
+      cp_async16(&B.b[tid], src + 1);
+      cp_async16(&B.c[tid], src + 2);
     }
+    cp_async_commit();
+  };
+  const int kt = max_last > 0 ? (max_last - 1) / kRT : -1;
+  if (kt >= 0 && slot(staged, kt & 1) != kt) {
+    issue(kt);
+    slot(staged, kt & 1) = -1;
+  } else {
+    cp_async_commit();
+  }
+  for (int k = kt; k >= 0; --k) {
+    if (k >= 1 && slot(staged, (k - 1) & 1) != k - 1) {
+      issue(k - 1);
+      slot(staged, (k - 1) & 1) = -1;
+    } else {
+      cp_async_commit();
+    }
+    cp_async_wait<1>();
+    __syncthreads();  // batch k landed (or staged by the forward)
+    Batch& B = S.b[k & 1];
+    const int lo = k * kRT;
+    const int cnt = min(kRT, max_last - lo);
+    if (slot(staged, k & 1) != k) {
+      if (tid < cnt) stage_entry(B, tid, ox, oy, S.e[k & 1]);
+      slot(staged, k & 1) = k;
+      __syncthreads();
+    }
+    const int jtop = max(0, min(cnt, warp_last - lo));
+    bwd_batch(B, S.u.acc, S.wl[warp], jtop, lo, wx0, wx1, wy0, wy1, ix, iy, last, Tr, S0, S1,
+              S2, g0, g1, g2, lane);
+    __syncthreads();
+    bwd_flush(B, S.e[k & 1], S.id[k & 1], S.u.acc, cnt, grads + 3 * view * n, tid);
     __syncthreads();
   }
   cp_async_wait<0>();
@@ -672,6 +876,31 @@ extern "C" gs_status gs_rasterize_fwd_counted(int64_t n, int32_t n_views, const 
   if (!counts) return GS_ERR_INVALID_ARG;
   return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
                             n_contrib, counts, stream);
+}
+
+extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
+                                        int32_t width, int32_t height, const uint32_t* vals,
+                                        const int64_t* ranges, const float* bg,
+                                        const float* target, float* image, float* T_final,
+                                        int32_t* n_contrib, float* loss, gs_splat_grad* grads,
+                                        void* stream) {
+  if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
+      height < 1 || !bg || !ranges || !target || !image || !T_final || !n_contrib || !loss)
+    return GS_ERR_INVALID_ARG;
+  if (n > 0 && (!splats || !grads || !aligned16(splats) || !aligned16(grads)))
+    return GS_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  GS_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), st));
+  if (n > 0) GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)(n * n_views), st));
+  const int64_t T = tiles_per_view(width, height);
+  const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE;
+  const double count = 3.0 * (double)n_views * (double)width * (double)height;
+  raster_fused_kernel<<<(unsigned)(n_views * T), kRT, 0, st>>>(
+      n, tiles_x, T, width, height, reinterpret_cast<const float4*>(splats), vals, ranges, bg[0],
+      bg[1], bg[2], target, (float)(1.0 / count), image, T_final, n_contrib, loss,
+      reinterpret_cast<float4*>(grads));
+  GS_CHECK_LAUNCH();
+  return GS_OK;
 }
 
 extern "C" gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats,

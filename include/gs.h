@@ -242,6 +242,28 @@ gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats, i
                            const float* bg, const float* T_final, const int32_t* n_contrib,
                            const float* dL_dimage, gs_splat_grad* grads, void* stream);
 
+/* gs_rasterize_fused -- gs_rasterize_fwd, gs_loss_l1 and gs_rasterize_bwd
+ * in one launch, one CTA per tile ([S3] abstract: forward and backward
+ * rasterization fused into a single kernel that keeps intermediate results
+ * on chip).  The forward's per-pixel results (transmittance, last
+ * contributor, colour) and the L1 gradient stay on chip instead of passing
+ * through T_final, n_contrib and dL/dimage in memory, and the batches the
+ * forward leaves staged in shared memory are reused by the backward without
+ * a new gather.  Results equal those of the three separate calls (the
+ * gradient up to the order of float atomics).
+ *   target     [n_views][3][H][W] fp32, the images the L1 loss compares with
+ *   image, T_final, n_contrib   outputs as gs_rasterize_fwd
+ *   loss       device scalar, overwritten: mean |image - target| over
+ *              n_views*3*H*W
+ *   grads      [n_views * n] output, zeroed by this call, then accumulated;
+ *              as gs_rasterize_bwd with dL/dimage = sign(image - target) /
+ *              (n_views*3*H*W) */
+gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
+                             int32_t height, const uint32_t* vals, const int64_t* ranges,
+                             const float* bg, const float* target, float* image, float* T_final,
+                             int32_t* n_contrib, float* loss, gs_splat_grad* grads,
+                             void* stream);
+
 /* gs_project_bwd -- chain rule from the per-row gradients back to the 59
  * parameters, summed over the views (the 1/n_views average of [S1] comes
  * from the loss normalisation):

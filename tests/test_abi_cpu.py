@@ -80,6 +80,8 @@ def test_invalid_arguments_return_before_any_launch(gslib):
                               None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_rasterize_bwd(10, 17, None, 16, 16, None, None, None, None, None, None, None,
                               None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_rasterize_fused(10, 1, None, 16, 16, None, None, None, None, None, None, None,
+                                None, None, None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_project_bwd(10, None, cp, 1, None, None, None, None,
                             None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_loss_l1(None, None, -1, None, None, None) == gslib.GS_ERR_INVALID_ARG

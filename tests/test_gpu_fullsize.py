@@ -128,6 +128,30 @@ def test_ring_3m_full_size():
         assert e <= GRAD_REL_L2, f
     del grads
 
+    # the fused call over every tile against the three separate calls
+    target_d = torch.from_numpy(target).cuda()
+    image_s = torch.empty((V, 3, H, W), device="cuda")
+    T_s = torch.empty((V, H, W), device="cuda")
+    nc_s = torch.empty((V, H, W), dtype=torch.int32, device="cuda")
+    gs.gs_rasterize_fwd(n, V, rec_d, W, H, vals, ranges, (0, 0, 0), image_s, T_s, nc_s)
+    loss_s = torch.empty(1, device="cuda")
+    g_img_s = torch.empty_like(image_s)
+    gs.gs_loss_l1(image_s, target_d, loss_s, g_img_s)
+    grads_s = torch.empty((n * V, 12), device="cuda")
+    gs.gs_rasterize_bwd(n, V, rec_d, W, H, vals, ranges, (0, 0, 0), T_s, nc_s, g_img_s, grads_s)
+    del g_img_s
+    image_f, T_f, nc_f = torch.empty_like(image_s), torch.empty_like(T_s), torch.empty_like(nc_s)
+    loss_f = torch.empty(1, device="cuda")
+    grads_f = torch.empty((n * V, 12), device="cuda")
+    gs.gs_rasterize_fused(n, V, rec_d, W, H, vals, ranges, (0, 0, 0), target_d, image_f, T_f, nc_f,
+                          loss_f, grads_f)
+    assert torch.equal(image_f, image_s) and torch.equal(T_f, T_s) and torch.equal(nc_f, nc_s)
+    assert loss_f.item() == pytest.approx(loss_s.item(), rel=1e-6)
+    e = ((grads_f - grads_s).norm() / grads_s.norm()).item()
+    print("fused vs separate: loss %.6f / %.6f, grads rel-L2 %.2e" % (loss_f.item(), loss_s.item(), e))
+    assert e <= 1e-5
+    del image_s, T_s, nc_s, grads_s, image_f, T_f, nc_f, grads_f, target_d
+
     # projection backward, every Gaussian, from the oracle's row gradients
     g2_32 = grads_to_rows(rows_to_grads(g2))
     grad_o, visible_o = oracle.project_bwd(p64, cams, g2_32)

@@ -277,17 +277,24 @@ def test_adam_matches_oracle(sparse):
     assert rel_l2(Vv.cpu().numpy(), vo) <= ADAM_REL_L2
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("case", ["tiny", "ragged2"])
-def test_train_step_end_to_end(case):
+def test_train_step_end_to_end(case, fused):
     """The library's own chain from the fp32 parameters against the oracle's
     chain: loss, image, gradients and the Adam result."""
     import oracle
     gs = _gs()
     o = oracle_side(case)
     params = o["params"]
-    step = gs.TrainStep(_cuda(params), o["cams"], _cuda(o["target"]), lr=1e-3)
-    step.forward()
-    step.backward()
+    step = gs.TrainStep(_cuda(params), o["cams"], _cuda(o["target"]), lr=1e-3, fused=fused)
+    if fused:
+        step.project()
+        step.bin_and_sort()
+        step.rasterize_fused()
+        step.project_bwd()
+    else:
+        step.forward()
+        step.backward()
     loss_o, grad_o, vis_o, parts = oracle.train_step_grads(params.astype(np.float64), o["cams"],
                                                            o["target"])
     img = step.image.cpu().numpy()
@@ -395,3 +402,97 @@ def test_far_elongated_footprints():
         e = rel_l2(g[f], g2[f])
         print("%s rel-L2 %.2e" % (f, e))
         assert e <= GRAD_REL_L2, f
+
+
+def test_sqrt_batch_lr_step_matches_oracle():
+    """A two-view step with the sqrt(b) learning-rate rule: the library's
+    update equals the oracle's Adam at lr sqrt(2) on the oracle's gradient."""
+    import oracle
+    gs = _gs()
+    o = oracle_side("ragged2")
+    params = o["params"]
+    step = gs.TrainStep(_cuda(params), o["cams"], _cuda(o["target"]), lr=1e-3, sqrt_batch_lr=True)
+    step.step()
+    _, grad_o, _, _ = oracle.train_step_grads(params.astype(np.float64), o["cams"], o["target"])
+    po = params.astype(np.float64)
+    mo, vo = np.zeros_like(po), np.zeros_like(po)
+    oracle.adam(po, grad_o, mo, vo, 1, 1e-3 * np.sqrt(2.0))
+    moved = step.params.cpu().numpy().astype(np.float64) - params
+    moved_o = po - params
+    # at t = 1 the update is lr g / (|g| + eps): lr sqrt(2) wherever |g| >> eps
+    big = np.abs(grad_o) > 1e-3 * np.abs(grad_o).max()
+    print("max |update| / lr %.5f, big-gradient entries %d" % (np.abs(moved).max() / 1e-3, big.sum()))
+    assert rel_l2(step.params.cpu().numpy(), po) <= ADAM_REL_L2
+    # (fp32 parameters of magnitude <= 8 round the update by <= 5e-7)
+    assert np.abs(moved).max() == pytest.approx(1e-3 * np.sqrt(2.0), rel=2e-3)
+    assert np.abs(moved[big] - moved_o[big]).max() <= 2e-6
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_rasterize_fused_matches_oracle_and_separate_calls(case):
+    """gs_rasterize_fused (forward + L1 + backward in one launch) against the
+    oracle's chain and against the three separate library calls."""
+    gs = _gs()
+    o = oracle_side(case)
+    n, V, W, H = o["n"], o["V"], o["W"], o["H"]
+    splats, vals, ranges, image_s, T_s, nc_s = _gpu_fwd(gs, o)
+    target = _cuda(o["target"])
+    loss_s = torch.empty(1, device="cuda")
+    g_img = torch.empty_like(image_s)
+    gs.gs_loss_l1(image_s, target, loss_s, g_img)
+    grads_s = torch.empty((n * V, 12), device="cuda")
+    gs.gs_rasterize_bwd(n, V, splats, W, H, vals, ranges, (0, 0, 0), T_s, nc_s, g_img, grads_s)
+    image = torch.empty_like(image_s)
+    T_final = torch.empty_like(T_s)
+    n_contrib = torch.empty_like(nc_s)
+    loss = torch.full((1,), 7.0, device="cuda")
+    grads = torch.full((n * V, 12), 3.0, device="cuda")
+    gs.gs_rasterize_fused(n, V, splats, W, H, vals, ranges, (0, 0, 0), target, image, T_final,
+                          n_contrib, loss, grads)
+    # the forward is the same code: identical results
+    assert torch.equal(image, image_s) and torch.equal(T_final, T_s) and torch.equal(n_contrib, nc_s)
+    assert loss.item() == pytest.approx(loss_s.item(), rel=1e-6)
+    e_sep = rel_l2(grads.cpu().numpy(), grads_s.cpu().numpy())
+    # against the oracle (its own image, L1 gradient and backward)
+    assert loss.item() == pytest.approx(o["loss"], rel=1e-5)
+    g = grads_to_rows(grads.cpu().numpy())
+    errs = {f: rel_l2(g[f], o["g2"][f]) for f in ("mean2d", "conic", "opacity", "color")}
+    print("fused vs separate grads rel-L2 %.2e; vs oracle %s" %
+          (e_sep, ", ".join("%s %.2e" % kv for kv in errs.items())))
+    assert e_sep <= 1e-5
+    for f, e in errs.items():
+        assert e <= GRAD_REL_L2, f
+    assert np.all(grads.cpu().numpy()[:, 9:12] == 0)
+
+
+def test_fused_far_footprints_and_empty_tiles():
+    """The fused call on the far-footprint records (long lists, many batches
+    left staged by the forward) against the separate calls."""
+    gs = _gs()
+    n, W, H, rec = _far_footprints()
+    f32 = unpack_records(rec)
+    st, I, _, vals, ranges, _ = _gpu_bin(gs, n, 1, rec, W, H)
+    assert st == gs.GS_OK
+    splats = _cuda(rec)
+    target = _cuda(scenes.target_images(1, W, H, 91))
+    image_s = torch.empty((1, 3, H, W), device="cuda")
+    T_s = torch.empty((1, H, W), device="cuda")
+    nc_s = torch.empty((1, H, W), dtype=torch.int32, device="cuda")
+    gs.gs_rasterize_fwd(n, 1, splats, W, H, vals, ranges, (0.2, 0.1, 0.3), image_s, T_s, nc_s)
+    loss_s = torch.empty(1, device="cuda")
+    g_img = torch.empty_like(image_s)
+    gs.gs_loss_l1(image_s, target, loss_s, g_img)
+    grads_s = torch.empty((n, 12), device="cuda")
+    gs.gs_rasterize_bwd(n, 1, splats, W, H, vals, ranges, (0.2, 0.1, 0.3), T_s, nc_s, g_img,
+                        grads_s)
+    image, T_final = torch.empty_like(image_s), torch.empty_like(T_s)
+    n_contrib, loss = torch.empty_like(nc_s), torch.empty(1, device="cuda")
+    grads = torch.empty((n, 12), device="cuda")
+    gs.gs_rasterize_fused(n, 1, splats, W, H, vals, ranges, (0.2, 0.1, 0.3), target, image, T_final,
+                          n_contrib, loss, grads)
+    assert torch.equal(image, image_s) and torch.equal(n_contrib, nc_s)
+    assert loss.item() == pytest.approx(loss_s.item(), rel=1e-6)
+    e = rel_l2(grads.cpu().numpy(), grads_s.cpu().numpy())
+    print("fused vs separate grads rel-L2 %.2e, longest list %d" %
+          (e, int((ranges[:, 1] - ranges[:, 0]).max().item())))
+    assert e <= 1e-5

@@ -223,3 +223,32 @@ def test_adam_first_step_closed_form(oracle_mod):
     oracle_mod.adam(p, g, m, v, 1, 1e-3)
     expect = p0 - 1e-3 * g / (np.abs(g) + 1e-8)
     assert np.abs(p - expect).max() < 1e-15
+
+
+def test_sqrt_batch_learning_rate_rule(oracle_mod):
+    """The premise and the consequence of the sqrt(b) learning-rate rule
+    ("On Scaling Up 3D Gaussian Splatting Training", independent-gradients
+    answer), on the oracle's Adam.  Per-view gradients are i.i.d. with mean mu
+    and deviation sigma; their mean over a batch of b views is then exactly
+    N(mu, sigma^2 / b), drawn directly.  (1) Adam's second moment settles at
+    sigma^2 / b (plus mu^2).  (2) With lr sqrt(b), one batch-b step moves the
+    parameters as far, on average, as b batch-size-1 steps."""
+    rng = np.random.default_rng(5)
+    rows, cols, steps, burn = 59, 400, 1500, 300
+    mu, sigma, lr = 0.05, 1.0, 1e-3
+    drift = {}
+    for b in (1, 4, 16):
+        p = np.zeros((rows, cols))
+        m, v = np.zeros_like(p), np.zeros_like(p)
+        moved = 0.0
+        for t in range(1, steps + 1):
+            g = rng.normal(mu, sigma / math.sqrt(b), (rows, cols))
+            before = p.copy()
+            oracle_mod.adam(p, g, m, v, t, lr * math.sqrt(b))
+            if t > burn:
+                moved += float((before - p).mean())
+        v_hat = v.mean() / (1.0 - 0.999 ** steps)
+        assert v_hat == pytest.approx(sigma ** 2 / b + mu ** 2, rel=0.05)
+        drift[b] = moved / (steps - burn)
+    for b in (4, 16):
+        assert drift[b] / drift[1] == pytest.approx(b, rel=0.08)

@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--morton", action="store_true",
+                    help="rename the Gaussians in Morton order of their means before timing")
     ap.add_argument("--separate", action="store_true",
                     help="composite with three calls (forward, L1 loss, backward) instead of the "
                          "fused one")
@@ -324,6 +326,16 @@ def our_arm(args, rank, world, local):
     # adam
     kernels_per_step = (8 if fused else 10) + passes
 
+    reorder_ms = None
+    if args.morton:
+        step.reorder_morton()  # first call: workspace sizing, module load
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        step.reorder_morton()
+        r1.record(stream)
+        torch.cuda.synchronize()
+        reorder_ms = r0.elapsed_time(r1)
+
     # warm-up (sizes the intersection buffers)
     for _ in range(max(args.warmup, 3)):
         step.step()
@@ -440,7 +452,7 @@ def our_arm(args, rank, world, local):
                        "height": H, "intersections": I, "l2": "inputs larger than L2 "
                        "(708 MB parameters, 2.1 GB with Adam state)", "adam": "sparse" if
                        cfg["sparse_adam"] else "dense", "compositing": "fused" if fused else
-                       "separate"},
+                       "separate", "gaussian_order": "morton" if args.morton else "as generated"},
             "mpix_per_s": round(V * W * H / (raster_ms / 1e3) / 1e6, 2),
             "gaussians_per_s": round(n * V / (ms_step / 1e3), 1),
             "gpu_launches": kernels_per_step * args.steps,
@@ -448,6 +460,7 @@ def our_arm(args, rank, world, local):
                     "h2d_bytes_per_step": int(target_host.numel() * 4), "d2h_bytes_per_step": 4,
                     "wall_s": round(e2e_wall, 3)},
             "roofline": roofline, "kernels": kernels,
+            "morton_reorder_ms": None if reorder_ms is None else round(reorder_ms, 3),
             "work": {"pairs_tested_fwd": tested, "pairs_included": included,
                      "pairs_bwd": bwd_eval, "visible_rows": visible_rows},
             "loss_first_last": [round(losses[0], 6), round(losses[-1], 6)],

@@ -61,6 +61,10 @@ def lib():
     L.gs_rasterize_fwd_counted.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     L.gs_loss_l1.argtypes = [vp, vp, i64, vp, vp, vp]
     L.gs_rasterize_bwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.gs_morton_workspace_bytes.argtypes = [i64]
+    L.gs_morton_workspace_bytes.restype = sz
+    L.gs_morton_order.argtypes = [i64, vp, vp, sz, vp, vp]
+    L.gs_permute_columns.argtypes = [i64, i64, vp, vp, vp, vp]
     L.gs_rasterize_fused.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      vp]
     L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp]
@@ -215,6 +219,26 @@ def gs_rasterize_fused(n, n_views, splats, width, height, vals, ranges, bg, targ
         _dev(loss, torch.float32, "loss"), _dev(grads, torch.float32, "grads"), _stream(stream)))
 
 
+def gs_morton_workspace_bytes(n):
+    return int(lib().gs_morton_workspace_bytes(n))
+
+
+def gs_morton_order(params, workspace, perm, stream=None):
+    n = params.shape[1]
+    _check("gs_morton_order", lib().gs_morton_order(
+        n, _dev(params, torch.float32, "params"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _dev(perm, torch.int32, "perm"), _stream(stream)))
+
+
+def gs_permute_columns(src, perm, dst, stream=None):
+    rows, n = src.shape
+    if dst.shape != src.shape or perm.numel() != n:
+        raise ValueError("gs_permute_columns: shapes")
+    _check("gs_permute_columns", lib().gs_permute_columns(
+        rows, n, _dev(src, torch.float32, "src"), _dev(perm, torch.int32, "perm"),
+        _dev(dst, torch.float32, "dst"), _stream(stream)))
+
+
 def gs_project_bwd(params, cams, splats, grads, grad, visible=None, stream=None):
     n = params.shape[1]
     cs = cameras_struct(cams)
@@ -351,6 +375,21 @@ class TrainStep:
 
     def update(self, stream=None):
         self.adam(stream)
+
+    def reorder_morton(self, stream=None):
+        """Renames the Gaussians in Morton order of their means: permutes the
+        parameters and the Adam moments consistently (one gs_morton_order and
+        three gs_permute_columns).  Returns perm (new index k holds old
+        Gaussian perm[k])."""
+        dev = self.params.device
+        ws = torch.zeros(gs_morton_workspace_bytes(self.n), dtype=torch.uint8, device=dev)
+        perm = torch.empty(self.n, dtype=torch.int32, device=dev)
+        gs_morton_order(self.params, ws, perm, stream)
+        tmp = torch.empty_like(self.params)
+        for buf in (self.params, self.m, self.v):
+            gs_permute_columns(buf, perm, tmp, stream)
+            buf.copy_(tmp)
+        return perm
 
     def step(self, stream=None):
         if self.fused:

@@ -406,6 +406,115 @@ __global__ void __launch_bounds__(256) ranges_kernel(int64_t count, uint64_t n_f
   if (i == count - 1 || (keys[i + 1] >> 32) != f) ranges[2 * f + 1] = i + 1;
 }
 
+// ---------------------------------------------------------------------------
+// Morton order of the Gaussians ("A Scalable PyTorch Abstraction for
+// Multi-GPU Gaussian Splatting", references: Morton order).  Each mean is
+// quantised to 21 bits per axis inside the means' bounding box,
+//   q = clamp(floor((x - lo) * (2^21 / (hi - lo))), 0, 2^21 - 1)   (fp32),
+// and the bits are interleaved, bit i of q_x at code bit 3i, of q_y at 3i+1,
+// of q_z at 3i+2.  A stable radix sort of (code, index) gives the order.
+constexpr int kMortonPasses = 8;  // 63 code bits
+
+// float -> uint32 with the same order (atomic min / max of floats)
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_ordered(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+// box[0..2] = ordered bits of the minimum mean x, y, z, box[3..5] of the
+// maximum (initialised to all ones / zero)
+__global__ void __launch_bounds__(256) bbox_kernel(int64_t n, const float* __restrict__ params,
+                                                   uint32_t* __restrict__ box) {
+  uint32_t lo[3] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu}, hi[3] = {0u, 0u, 0u};
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      const uint32_t o = ordered_bits(params[a * n + i]);
+      lo[a] = min(lo[a], o);
+      hi[a] = max(hi[a], o);
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    lo[a] = __reduce_min_sync(0xffffffffu, lo[a]);
+    hi[a] = __reduce_max_sync(0xffffffffu, hi[a]);
+  }
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      atomicMin(&box[a], lo[a]);
+      atomicMax(&box[3 + a], hi[a]);
+    }
+  }
+}
+
+// The low 21 bits of v moved to bits 0, 3, 6, ..., 60 (bit spreading by
+// shifts and masks).
+__device__ __forceinline__ uint64_t spread3(uint32_t v) {
+  uint64_t x = v & 0x1FFFFFu;
+  x = (x | x << 32) & 0x001F00000000FFFFull;
+  x = (x | x << 16) & 0x001F0000FF0000FFull;
+  x = (x | x << 8) & 0x100F00F00F00F00Full;
+  x = (x | x << 4) & 0x10C30C30C30C30C3ull;
+  x = (x | x << 2) & 0x1249249249249249ull;
+  return x;
+}
+
+__device__ __forceinline__ uint32_t quantize21(float v, float lo, float s) {
+  const float t = floorf(__fmul_rn(__fsub_rn(v, lo), s));
+  return (uint32_t)fminf(fmaxf(t, 0.f), 2097151.f);  // NaN -> 0
+}
+
+// keys[i] = Morton code of Gaussian i, vals[i] = i, and the digit histograms
+// of the eight radix passes
+__global__ void __launch_bounds__(256) morton_kernel(int64_t n, const float* __restrict__ params,
+                                                     const uint32_t* __restrict__ box,
+                                                     uint64_t* __restrict__ keys,
+                                                     uint32_t* __restrict__ vals,
+                                                     uint32_t* __restrict__ hist) {
+  __shared__ uint32_t sh[kMortonPasses * kRadix];
+  for (int i = threadIdx.x; i < kMortonPasses * kRadix; i += blockDim.x) sh[i] = 0;
+  float lo[3], sc[3];
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    lo[a] = from_ordered(box[a]);
+    const float ext = __fsub_rn(from_ordered(box[3 + a]), lo[a]);
+    sc[a] = ext > 0.f ? __fdiv_rn(2097152.f, ext) : 0.f;
+  }
+  __syncthreads();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint64_t code = spread3(quantize21(params[i], lo[0], sc[0])) |
+                          spread3(quantize21(params[n + i], lo[1], sc[1])) << 1 |
+                          spread3(quantize21(params[2 * n + i], lo[2], sc[2])) << 2;
+    keys[i] = code;
+    vals[i] = (uint32_t)i;
+#pragma unroll
+    for (int p = 0; p < kMortonPasses; ++p) atomicAdd(&sh[p * kRadix + ((code >> (8 * p)) & 0xFF)], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kMortonPasses * kRadix; i += blockDim.x)
+    if (sh[i]) atomicAdd(&hist[i], sh[i]);
+}
+
+// dst[r][i] = src[r][perm[i]] for r < rows (perm clamped into range)
+__global__ void __launch_bounds__(256) permute_columns_kernel(int64_t rows, int64_t n,
+                                                              const float* __restrict__ src,
+                                                              const uint32_t* __restrict__ perm,
+                                                              float* __restrict__ dst) {
+  const int64_t total = rows * n;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / n, i = t - r * n;
+    const uint32_t j = min(__ldg(perm + i), (uint32_t)(n - 1));
+    dst[t] = __ldg(src + r * n + j);
+  }
+}
+
 int bit_length(uint64_t v) {
   int b = 0;
   while (v) { ++b; v >>= 1; }
@@ -546,6 +655,79 @@ extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat*
   }
   // 5. ranges
   ranges_kernel<<<(unsigned)div_up(I, 256), 256, 0, st>>>(I, (uint64_t)(n_views * T), keys, ranges);
+  GS_CHECK_LAUNCH();
+  return GS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Morton order entry points
+
+static size_t morton_ws_bytes(int64_t n) {
+  return ws_layout(0, n).total + align256(sizeof(uint64_t) * (size_t)(n > 0 ? n : 1));
+}
+
+extern "C" size_t gs_morton_workspace_bytes(int64_t n) { return morton_ws_bytes(n); }
+
+extern "C" gs_status gs_morton_order(int64_t n, const float* params, void* workspace,
+                                     size_t ws_bytes, uint32_t* perm, void* stream) {
+  if (n < 0 || n > (int64_t)0xFFFFFFFFll || !workspace || !aligned16(workspace) ||
+      ws_bytes < morton_ws_bytes(n) || (n > 0 && (!params || !perm)))
+    return GS_ERR_INVALID_ARG;
+  if (n == 0) return GS_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(0, n);
+  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  uint32_t* digit_start = reinterpret_cast<uint32_t*>(ws + L.digit_start);
+  uint64_t* sort_status = reinterpret_cast<uint64_t*>(ws + L.sort_status);
+  uint64_t* keys_b = reinterpret_cast<uint64_t*>(ws + L.keys_alt);
+  uint32_t* vals_b = reinterpret_cast<uint32_t*>(ws + L.vals_alt);
+  uint64_t* keys_a = reinterpret_cast<uint64_t*>(ws + L.total);
+  uint32_t* box = hdr->pad;  // six words of the header's spare space
+  GS_CUDA(cudaMemsetAsync(&hdr->scan_ticket, 0, sizeof(WsHeader) - offsetof(WsHeader, scan_ticket), st));
+  GS_CUDA(cudaMemsetAsync(box, 0xFF, 3 * sizeof(uint32_t), st));
+  GS_CUDA(cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, st));
+  int dev = 0, sms = 0;
+  GS_CUDA(cudaGetDevice(&dev));
+  GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t blocks = div_up(n, 256) < 8 * sms ? div_up(n, 256) : 8 * sms;
+  bbox_kernel<<<(unsigned)blocks, 256, 0, st>>>(n, params, box);
+  GS_CHECK_LAUNCH();
+  // eight passes (even): emission into (keys_a, perm) leaves the result there
+  morton_kernel<<<(unsigned)blocks, 256, 0, st>>>(n, params, box, keys_a, perm, hist);
+  GS_CHECK_LAUNCH();
+  hist_scan_kernel<<<kMortonPasses, kRadix, 0, st>>>(hist, digit_start);
+  GS_CHECK_LAUNCH();
+  const int64_t sort_parts = div_up(n, kSortPart);
+  GS_CUDA(cudaMemsetAsync(sort_status, 0, sizeof(uint64_t) * kRadix * (size_t)sort_parts, st));
+  const size_t smem = sizeof(SortSmem);
+  GS_CUDA(cudaFuncSetAttribute(onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  uint64_t* k_in = keys_a;
+  uint32_t* v_in = perm;
+  uint64_t* k_out = keys_b;
+  uint32_t* v_out = vals_b;
+  for (int p = 0; p < kMortonPasses; ++p) {
+    onesweep_kernel<<<(unsigned)sort_parts, kSortThreads, smem, st>>>(
+        n, p, k_in, v_in, k_out, v_out, digit_start, sort_status, hdr);
+    GS_CHECK_LAUNCH();
+    uint64_t* tk = k_in; k_in = k_out; k_out = tk;
+    uint32_t* tv = v_in; v_in = v_out; v_out = tv;
+  }
+  return GS_OK;
+}
+
+extern "C" gs_status gs_permute_columns(int64_t rows, int64_t n, const float* src,
+                                        const uint32_t* perm, float* dst, void* stream) {
+  if (rows < 0 || n < 0 || n > (int64_t)0xFFFFFFFFll ||
+      (rows > 0 && n > 0 && (!src || !perm || !dst || src == dst)))
+    return GS_ERR_INVALID_ARG;
+  if (rows == 0 || n == 0) return GS_OK;
+  int dev = 0, sms = 0;
+  GS_CUDA(cudaGetDevice(&dev));
+  GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t blocks = div_up(rows * n, 256) < 16 * sms ? div_up(rows * n, 256) : 16 * sms;
+  permute_columns_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(rows, n, src, perm, dst);
   GS_CHECK_LAUNCH();
   return GS_OK;
 }

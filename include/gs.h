@@ -290,6 +290,36 @@ gs_status gs_adam_step(int64_t n, float* params, const float* grad, float* m, fl
                        const uint8_t* visible, void* stream);
 
 /* ---------------------------------------------------------------------- */
+/* Morton order of the Gaussians ([S4] references: Morton order), for the
+ * locality of the id-indexed gathers of compositing.  A reorder permutes the
+ * columns of every [rows][n] array consistently (parameters, Adam m and v);
+ * the step's results are those of the original scene with the Gaussians
+ * renamed (equal-depth ties in a tile then break by the new ids).
+ *
+ * gs_morton_order -- perm[k] = index of the k-th Gaussian in Morton order.
+ * Each mean is quantised to 21 bits per axis inside the means' bounding box,
+ *   q = clamp(floor((x - lo) * (2^21 / (hi - lo))), 0, 2^21 - 1)  (fp32,
+ *   one rounding per operation; 0 when hi == lo),
+ * and code = sum_i bit_i(q_x) 2^(3i) + bit_i(q_y) 2^(3i+1) + bit_i(q_z)
+ * 2^(3i+2); perm sorts (code, index) ascending (stable radix sort, 8 passes).
+ *   params     [59][n] (rows 0-2 are read)
+ *   workspace  gs_morton_workspace_bytes(n) bytes, 16-byte aligned; its
+ *              first 256 bytes must be zero before the first use (device
+ *              status word, as the binning workspace; gs_workspace_status
+ *              reads it)
+ *   perm       [n] uint32 output
+ * Asynchronous; does not synchronise. */
+size_t gs_morton_workspace_bytes(int64_t n);
+gs_status gs_morton_order(int64_t n, const float* params, void* workspace, size_t ws_bytes,
+                          uint32_t* perm, void* stream);
+
+/* gs_permute_columns -- dst[r][i] = src[r][perm[i]] for r < rows, i < n
+ * (row-major [rows][n] fp32; src and dst distinct; perm entries >= n are
+ * clamped to n - 1). */
+gs_status gs_permute_columns(int64_t rows, int64_t n, const float* src, const uint32_t* perm,
+                             float* dst, void* stream);
+
+/* ---------------------------------------------------------------------- */
 const char* gs_status_string(gs_status status);
 int32_t gs_version(void);
 

@@ -45,6 +45,8 @@ def lib():
         L.or_project_mt.argtypes = [i64, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32]
         L.or_bin_select.argtypes = [i64, i32, vp, vp, vp, i32, i32, i32, vp, i64, vp, vp]
         L.or_bin_select.restype = i64
+        L.or_morton_codes.argtypes = [i64, vp, vp]
+        L.or_morton_order.argtypes = [i64, vp, vp]
         L.or_tile_rect.argtypes = [C.c_float, C.c_float, i32, i32, i32, i32, vp]
         L.or_count_isect.argtypes = [i64, vp, vp, i32, i32, i32]
         L.or_count_isect.restype = i64
@@ -113,6 +115,23 @@ def project(params, cams, tile=TILE, threads=1):
                         _p(out["conic"]), _p(out["depth"]), _p(out["color"]),
                         _p(out["opacity"]), _p(out["radius"]), _p(out["tiles"]),
                         _p(out["flags"]), int(threads))
+    return out
+
+
+def morton_codes(params_f32):
+    """Morton codes (uint64) of the means of a [59][n] (or [3+][n]) fp32 array."""
+    p = np.ascontiguousarray(params_f32, np.float32)
+    n = p.shape[1]
+    out = np.zeros(n, np.uint64)
+    lib().or_morton_codes(n, _p(p), _p(out))
+    return out
+
+
+def morton_order(params_f32):
+    p = np.ascontiguousarray(params_f32, np.float32)
+    n = p.shape[1]
+    out = np.zeros(n, np.uint32)
+    lib().or_morton_order(n, _p(p), _p(out))
     return out
 
 

@@ -879,3 +879,51 @@ void or_adam(int64_t n_rows, int64_t n_cols, double* p, const double* g, double*
       p[i] -= lr * mhat / (sqrt(vhat) + eps);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Morton order ("A Scalable PyTorch Abstraction for Multi-GPU Gaussian
+ * Splatting", references: Morton order).  The quantisation decides integers,
+ * so it is done in fp32 with one rounding per operation, as the library
+ * does; the interleave is a plain loop over the 21 bits. */
+static uint32_t morton_q21(float v, float lo, float s) {
+  float t = floorf((v - lo) * s);
+  if (!(t >= 0.0f)) t = 0.0f;
+  if (t > 2097151.0f) t = 2097151.0f;
+  return (uint32_t)t;
+}
+
+void or_morton_codes(int64_t n, const float* params, uint64_t* codes) {
+  float lo[3], hi[3], sc[3];
+  for (int a = 0; a < 3; ++a) {
+    lo[a] = hi[a] = n > 0 ? params[a * n] : 0.0f;
+    for (int64_t i = 1; i < n; ++i) {
+      const float v = params[a * n + i];
+      if (v < lo[a]) lo[a] = v;
+      if (v > hi[a]) hi[a] = v;
+    }
+    const float ext = hi[a] - lo[a];
+    sc[a] = ext > 0.0f ? 2097152.0f / ext : 0.0f;
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    uint32_t q[3];
+    for (int a = 0; a < 3; ++a) q[a] = morton_q21(params[a * n + i], lo[a], sc[a]);
+    uint64_t code = 0;
+    for (int b = 0; b < 21; ++b)
+      for (int a = 0; a < 3; ++a) code |= (uint64_t)((q[a] >> b) & 1u) << (3 * b + a);
+    codes[i] = code;
+  }
+}
+
+void or_morton_order(int64_t n, const float* params, uint32_t* perm) {
+  uint64_t* codes = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)(n > 0 ? n : 1));
+  kv* items = (kv*)malloc(sizeof(kv) * (size_t)(n > 0 ? n : 1));
+  or_morton_codes(n, params, codes);
+  for (int64_t i = 0; i < n; ++i) {
+    items[i].key = codes[i];
+    items[i].val = (uint32_t)i;
+  }
+  qsort(items, (size_t)n, sizeof(kv), kv_cmp);
+  for (int64_t i = 0; i < n; ++i) perm[i] = items[i].val;
+  free(items);
+  free(codes);
+}

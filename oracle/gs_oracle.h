@@ -109,6 +109,15 @@ int64_t or_bin_select(int64_t n, int32_t n_views, const float* mean2d, const int
                       const int64_t* tile_sel, int64_t n_sel, uint32_t* out_vals,
                       int64_t* out_ranges);
 
+/* Morton codes of the Gaussians' means (params: [59][n] fp32, rows 0-2):
+ * q = clamp(floor((x - lo) * (2^21 / (hi - lo))), 0, 2^21 - 1) per axis in
+ * fp32 over the means' bounding box [lo, hi] (0 when hi == lo); bit b of
+ * q_x, q_y, q_z goes to code bit 3b, 3b+1, 3b+2. */
+void or_morton_codes(int64_t n, const float* params, uint64_t* codes);
+
+/* perm[k] = index of the k-th Gaussian in ascending (code, index) order. */
+void or_morton_order(int64_t n, const float* params, uint32_t* perm);
+
 /* Forward compositing over the sorted per-tile lists (tiled mode).
  * features are fp64 arrays indexed by row; vals hold gaussian ids (row =
  * view*n + id).  tile_sel/n_sel restrict the work to selected flattened

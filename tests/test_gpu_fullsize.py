@@ -146,7 +146,7 @@ def test_ring_3m_full_size():
     gs.gs_rasterize_fused(n, V, rec_d, W, H, vals, ranges, (0, 0, 0), target_d, image_f, T_f, nc_f,
                           loss_f, grads_f)
     assert torch.equal(image_f, image_s) and torch.equal(T_f, T_s) and torch.equal(nc_f, nc_s)
-    assert loss_f.item() == pytest.approx(loss_s.item(), rel=1e-6)
+    assert loss_f.item() == pytest.approx(loss_s.item(), rel=1e-5)  # fp32 sums in another order
     e = ((grads_f - grads_s).norm() / grads_s.norm()).item()
     print("fused vs separate: loss %.6f / %.6f, grads rel-L2 %.2e" % (loss_f.item(), loss_s.item(), e))
     assert e <= 1e-5

@@ -451,7 +451,7 @@ def test_rasterize_fused_matches_oracle_and_separate_calls(case):
                           n_contrib, loss, grads)
     # the forward is the same code: identical results
     assert torch.equal(image, image_s) and torch.equal(T_final, T_s) and torch.equal(n_contrib, nc_s)
-    assert loss.item() == pytest.approx(loss_s.item(), rel=1e-6)
+    assert loss.item() == pytest.approx(loss_s.item(), rel=1e-5)  # fp32 sums in another order
     e_sep = rel_l2(grads.cpu().numpy(), grads_s.cpu().numpy())
     # against the oracle (its own image, L1 gradient and backward)
     assert loss.item() == pytest.approx(o["loss"], rel=1e-5)
@@ -491,7 +491,7 @@ def test_fused_far_footprints_and_empty_tiles():
     gs.gs_rasterize_fused(n, 1, splats, W, H, vals, ranges, (0.2, 0.1, 0.3), target, image, T_final,
                           n_contrib, loss, grads)
     assert torch.equal(image, image_s) and torch.equal(n_contrib, nc_s)
-    assert loss.item() == pytest.approx(loss_s.item(), rel=1e-6)
+    assert loss.item() == pytest.approx(loss_s.item(), rel=1e-5)  # fp32 sums in another order
     e = rel_l2(grads.cpu().numpy(), grads_s.cpu().numpy())
     print("fused vs separate grads rel-L2 %.2e, longest list %d" %
           (e, int((ranges[:, 1] - ranges[:, 0]).max().item())))

@@ -415,3 +415,47 @@ def test_rigid_motion_invariance(oracle_mod):
     ok = pr1["flags"] == 0
     assert ok.mean() > 0.9
     assert np.abs(fw1["image"] - fw0["image"]).max() < 1e-9
+
+
+# --------------------------------------------------------------------------
+# Morton order
+
+
+def test_morton_order_is_the_z_curve_on_a_grid(oracle_mod):
+    """Points on an 8x8x8 grid (bounding box [0,7]^3, shuffled): the sorted
+    order must list the eight octants as consecutive blocks of 64, in the
+    order x-bit | y-bit << 1 | z-bit << 2, and recursively the 2x2x2 cells
+    of each octant as blocks of 8 -- the Z-order curve, which pins the bit
+    interleave and the monotone quantisation without re-deriving the code."""
+    g = np.stack(np.meshgrid(np.arange(8), np.arange(8), np.arange(8), indexing="ij"), 0)
+    pts = g.reshape(3, -1).astype(np.float32)
+    rng = np.random.default_rng(3)
+    sh = rng.permutation(pts.shape[1])
+    pts = pts[:, sh]
+    order = oracle_mod.morton_order(pts)
+    assert sorted(order.tolist()) == list(range(512))
+    p = pts[:, order].astype(int)
+    for level, size in ((4, 64), (2, 8), (1, 1)):
+        cell = (p // level) % 2  # the bit chosen at this level
+        idx = cell[0] + 2 * cell[1] + 4 * cell[2]
+        blocks = idx.reshape(-1, size)
+        assert np.all(blocks == blocks[:, :1])  # one cell per block
+        assert np.array_equal(blocks[:8, 0] if size > 1 else idx[:8], np.arange(8))
+    # consecutive points never jump more than the curve allows inside a cell
+    assert np.all(np.abs(np.diff(p[:, :8], axis=1)).max(axis=0) <= 1)
+
+
+def test_morton_codes_closed_forms(oracle_mod):
+    p = np.array([[0, 1, 0, 0, 1, 0.5],
+                  [0, 0, 1, 0, 1, 0.5],
+                  [0, 0, 0, 1, 1, 0.5]], np.float32)
+    c = oracle_mod.morton_codes(p)
+    xs = sum(1 << (3 * b) for b in range(21))
+    assert [int(v) for v in c[:5]] == [0, xs, xs << 1, xs << 2, (1 << 63) - 1]
+    # the centre quantises to 2^20 on every axis: only code bits 60, 61, 62
+    assert int(c[5]) == 7 << 60
+    # a flat axis (all z equal) contributes no bits; duplicates keep index order
+    q = np.array([[3, 1, 3, 1], [2, 2, 2, 2], [5, 5, 5, 5]], np.float32)
+    cq = oracle_mod.morton_codes(q)
+    assert int(cq[0]) == int(cq[2]) == xs and int(cq[1]) == 0
+    assert oracle_mod.morton_order(q).tolist() == [1, 3, 0, 2]

@@ -56,6 +56,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prune", type=int, default=None, metavar="K",
+                    help="prune once to a per-tile working set of K entries before timing")
+    ap.add_argument("--prune-tau", type=float, default=2.0,
+                    help="quality floor of the pruning (> 1: none)")
     ap.add_argument("--morton", action="store_true",
                     help="rename the Gaussians in Morton order of their means before timing")
     ap.add_argument("--separate", action="store_true",
@@ -178,9 +182,9 @@ TRAFFIC = {
 }
 
 
-def traffic_of(kernel, workload, n_override):
+def traffic_of(kernel, workload, variant):
     t = TRAFFIC.get(kernel)
-    if t is None or t["workload"] != workload or n_override:
+    if t is None or t["workload"] != workload or variant:
         return None
     import hashlib
     try:
@@ -326,6 +330,36 @@ def our_arm(args, rank, world, local):
     # adam
     kernels_per_step = (8 if fused else 10) + passes
 
+    prune_info = None
+    if args.prune is not None:
+        def over_capacity(st):
+            nc = st.n_contrib
+            tx, ty = (W + 15) // 16, (H + 15) // 16
+            pad = torch.zeros((V, ty * 16, tx * 16), dtype=torch.int32, device=dev)
+            pad[:, :H, :W] = nc
+            L = pad.view(V, ty, 16, tx, 16).amax(dim=(2, 4))
+            return int((L > args.prune).sum().item()), int((L > 0).sum().item())
+        step.step()
+        torch.cuda.synchronize()
+        over0, busy0 = over_capacity(step)
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        pruned = step.prune_to_capacity(args.prune, args.prune_tau)
+        p1.record(stream)
+        torch.cuda.synchronize()
+        kept = pruned[0].shape[1]
+        step = gs.TrainStep(pruned[0].contiguous(), cams, target, lr=cfg["lr"],
+                            sparse=cfg["sparse_adam"], fused=fused)
+        step.step()
+        torch.cuda.synchronize()
+        over1, busy1 = over_capacity(step)
+        prune_info = {"capacity": args.prune, "tau": args.prune_tau, "ms": round(p0.elapsed_time(p1), 3),
+                      "gaussians_before": n, "gaussians_after": kept,
+                      "tiles_over_capacity_before": over0, "tiles_over_capacity_after": over1,
+                      "nonempty_tiles": busy0}
+        del pruned
+        n = kept
+
     reorder_ms = None
     if args.morton:
         step.reorder_morton()  # first call: workspace sizing, module load
@@ -429,17 +463,19 @@ def our_arm(args, rank, world, local):
                                    fp32_peak_tflops)
         for nm in ("rasterize_fwd", "rasterize_bwd", "loss_l1"):
             del kern[nm]
+    # the recorded DRAM bytes describe the default run of the workload only
+    variant = bool(args.gaussians or args.prune is not None or args.morton)
     kernels = {}
     for nm, (bound, work, unit, peak) in kern.items():
         ach = work / (per_kernel[nm] / 1e3)
         kernels[nm] = {"ms": round(per_kernel[nm], 4), "bound": bound, "achieved": round(ach, 3),
                        "peak": round(peak, 2), "unit": unit, "frac": round(ach / peak, 4),
-                       "traffic": traffic_of(nm, args.workload, args.gaussians)}
+                       "traffic": traffic_of(nm, args.workload, variant)}
     dom = max(kern, key=lambda k: per_kernel[k])
     d = kernels[dom]
     roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
                 "unit": d["unit"], "frac": d["frac"],
-                "traffic": traffic_of(dom, args.workload, args.gaussians),
+                "traffic": traffic_of(dom, args.workload, variant),
                 "peak_source": (peak_kind + " HBM copy") if d["bound"] == "hbm" else
                 ("FP32 lanes x 2 x median SM clock %.0f MHz, %d SMs" % (sm_mhz, sms))}
     raster_ms = (per_kernel["rasterize_fused"] if fused else
@@ -452,7 +488,8 @@ def our_arm(args, rank, world, local):
                        "height": H, "intersections": I, "l2": "inputs larger than L2 "
                        "(708 MB parameters, 2.1 GB with Adam state)", "adam": "sparse" if
                        cfg["sparse_adam"] else "dense", "compositing": "fused" if fused else
-                       "separate", "gaussian_order": "morton" if args.morton else "as generated"},
+                       "separate", "gaussian_order": "morton" if args.morton else "as generated",
+                       "pruned_to_capacity": args.prune},
             "mpix_per_s": round(V * W * H / (raster_ms / 1e3) / 1e6, 2),
             "gaussians_per_s": round(n * V / (ms_step / 1e3), 1),
             "gpu_launches": kernels_per_step * args.steps,
@@ -461,6 +498,7 @@ def our_arm(args, rank, world, local):
                     "wall_s": round(e2e_wall, 3)},
             "roofline": roofline, "kernels": kernels,
             "morton_reorder_ms": None if reorder_ms is None else round(reorder_ms, 3),
+            "prune": prune_info,
             "work": {"pairs_tested_fwd": tested, "pairs_included": included,
                      "pairs_bwd": bwd_eval, "visible_rows": visible_rows},
             "loss_first_last": [round(losses[0], 6), round(losses[-1], 6)],

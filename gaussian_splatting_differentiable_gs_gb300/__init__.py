@@ -64,7 +64,13 @@ def lib():
     L.gs_morton_workspace_bytes.argtypes = [i64]
     L.gs_morton_workspace_bytes.restype = sz
     L.gs_morton_order.argtypes = [i64, vp, vp, sz, vp, vp]
-    L.gs_permute_columns.argtypes = [i64, i64, vp, vp, vp, vp]
+    L.gs_gather_columns.argtypes = [i64, i64, i64, vp, vp, vp, vp]
+    L.gs_rasterize_fwd_importance.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp,
+                                              vp]
+    L.gs_prune_mask.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, i64, f32, vp, vp]
+    L.gs_compact_workspace_bytes.argtypes = [i64]
+    L.gs_compact_workspace_bytes.restype = sz
+    L.gs_compact_index.argtypes = [i64, vp, vp, sz, vp, vp, vp]
     L.gs_rasterize_fused.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      vp]
     L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp]
@@ -230,13 +236,46 @@ def gs_morton_order(params, workspace, perm, stream=None):
         workspace.numel(), _dev(perm, torch.int32, "perm"), _stream(stream)))
 
 
-def gs_permute_columns(src, perm, dst, stream=None):
-    rows, n = src.shape
-    if dst.shape != src.shape or perm.numel() != n:
-        raise ValueError("gs_permute_columns: shapes")
-    _check("gs_permute_columns", lib().gs_permute_columns(
-        rows, n, _dev(src, torch.float32, "src"), _dev(perm, torch.int32, "perm"),
+def gs_gather_columns(src, idx, dst, stream=None):
+    """dst[:, i] = src[:, idx[i]] (src [rows][n_src], dst [rows][n_dst])."""
+    rows, n_src = src.shape
+    n_dst = dst.shape[1]
+    if dst.shape[0] != rows or idx.numel() < n_dst:
+        raise ValueError("gs_gather_columns: shapes")
+    _check("gs_gather_columns", lib().gs_gather_columns(
+        rows, n_src, n_dst, _dev(src, torch.float32, "src"), _dev(idx, torch.int32, "idx"),
         _dev(dst, torch.float32, "dst"), _stream(stream)))
+
+
+def gs_rasterize_fwd_importance(n, n_views, splats, width, height, vals, ranges, bg, image,
+                                T_final, n_contrib, importance, stream=None):
+    bgv = (C.c_float * 3)(*[float(b) for b in bg])
+    _check("gs_rasterize_fwd_importance", lib().gs_rasterize_fwd_importance(
+        n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(image, torch.float32, "image"), _dev(T_final, torch.float32, "T_final"),
+        _dev(n_contrib, torch.int32, "n_contrib"), _dev(importance, torch.float32, "importance"),
+        _stream(stream)))
+
+
+def gs_prune_mask(n, n_views, width, height, vals, ranges, n_contrib, importance, capacity, tau,
+                  mask, stream=None):
+    _check("gs_prune_mask", lib().gs_prune_mask(
+        n, n_views, width, height, _dev(vals, torch.int32, "vals"),
+        _dev(ranges, torch.int64, "ranges"), _dev(n_contrib, torch.int32, "n_contrib"),
+        _dev(importance, torch.float32, "importance"), int(capacity), float(tau),
+        _dev(mask, torch.uint8, "mask"), _stream(stream)))
+
+
+def gs_compact_workspace_bytes(n):
+    return int(lib().gs_compact_workspace_bytes(n))
+
+
+def gs_compact_index(mask, workspace, idx, n_keep, stream=None):
+    _check("gs_compact_index", lib().gs_compact_index(
+        mask.numel(), _dev(mask, torch.uint8, "mask"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _dev(idx, torch.int32, "idx"), _dev(n_keep, torch.int64, "n_keep"),
+        _stream(stream)))
 
 
 def gs_project_bwd(params, cams, splats, grads, grad, visible=None, stream=None):
@@ -379,7 +418,7 @@ class TrainStep:
     def reorder_morton(self, stream=None):
         """Renames the Gaussians in Morton order of their means: permutes the
         parameters and the Adam moments consistently (one gs_morton_order and
-        three gs_permute_columns).  Returns perm (new index k holds old
+        three gs_gather_columns).  Returns perm (new index k holds old
         Gaussian perm[k])."""
         dev = self.params.device
         ws = torch.zeros(gs_morton_workspace_bytes(self.n), dtype=torch.uint8, device=dev)
@@ -387,9 +426,36 @@ class TrainStep:
         gs_morton_order(self.params, ws, perm, stream)
         tmp = torch.empty_like(self.params)
         for buf in (self.params, self.m, self.v):
-            gs_permute_columns(buf, perm, tmp, stream)
+            gs_gather_columns(buf, perm, tmp, stream)
             buf.copy_(tmp)
         return perm
+
+    def prune_to_capacity(self, capacity, tau=2.0, stream=None):
+        """Pruning bounded by the per-tile working set (gs_prune_mask) on the
+        current parameters: a forward that records importances, the mask,
+        and the compaction of the parameters and Adam moments.  Returns
+        (params, m, v, kept index, mask); a new TrainStep takes them over."""
+        dev = self.params.device
+        self.project(stream)
+        self.bin_and_sort(stream)
+        imp = torch.empty(self.V * self.n, device=dev, dtype=torch.float32)
+        gs_rasterize_fwd_importance(self.n, self.V, self.splats, self.W, self.H, self.vals,
+                                    self.ranges, self.bg, self.image, self.T_final,
+                                    self.n_contrib, imp, stream)
+        mask = torch.empty(self.n, device=dev, dtype=torch.uint8)
+        gs_prune_mask(self.n, self.V, self.W, self.H, self.vals, self.ranges, self.n_contrib, imp,
+                      capacity, tau, mask, stream)
+        ws = torch.empty(gs_compact_workspace_bytes(self.n), device=dev, dtype=torch.uint8)
+        idx = torch.empty(self.n, device=dev, dtype=torch.int32)
+        n_keep = torch.empty(1, device=dev, dtype=torch.int64)
+        gs_compact_index(mask, ws, idx, n_keep, stream)
+        k = int(n_keep.item())
+        out = []
+        for buf in (self.params, self.m, self.v):
+            dst = torch.empty((buf.shape[0], k), device=dev, dtype=torch.float32)
+            gs_gather_columns(buf, idx, dst, stream)
+            out.append(dst)
+        return out[0], out[1], out[2], idx[:k], mask
 
     def step(self, stream=None):
         if self.fused:

@@ -501,17 +501,18 @@ __global__ void __launch_bounds__(256) morton_kernel(int64_t n, const float* __r
     if (sh[i]) atomicAdd(&hist[i], sh[i]);
 }
 
-// dst[r][i] = src[r][perm[i]] for r < rows (perm clamped into range)
-__global__ void __launch_bounds__(256) permute_columns_kernel(int64_t rows, int64_t n,
-                                                              const float* __restrict__ src,
-                                                              const uint32_t* __restrict__ perm,
-                                                              float* __restrict__ dst) {
-  const int64_t total = rows * n;
+// dst[r][i] = src[r][idx[i]] for r < rows, i < n_dst (idx clamped into range)
+__global__ void __launch_bounds__(256) gather_columns_kernel(int64_t rows, int64_t n_src,
+                                                             int64_t n_dst,
+                                                             const float* __restrict__ src,
+                                                             const uint32_t* __restrict__ idx,
+                                                             float* __restrict__ dst) {
+  const int64_t total = rows * n_dst;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = t / n, i = t - r * n;
-    const uint32_t j = min(__ldg(perm + i), (uint32_t)(n - 1));
-    dst[t] = __ldg(src + r * n + j);
+    const int64_t r = t / n_dst, i = t - r * n_dst;
+    const uint32_t j = min(__ldg(idx + i), (uint32_t)(n_src - 1));
+    dst[t] = __ldg(src + r * n_src + j);
   }
 }
 
@@ -717,17 +718,20 @@ extern "C" gs_status gs_morton_order(int64_t n, const float* params, void* works
   return GS_OK;
 }
 
-extern "C" gs_status gs_permute_columns(int64_t rows, int64_t n, const float* src,
-                                        const uint32_t* perm, float* dst, void* stream) {
-  if (rows < 0 || n < 0 || n > (int64_t)0xFFFFFFFFll ||
-      (rows > 0 && n > 0 && (!src || !perm || !dst || src == dst)))
+extern "C" gs_status gs_gather_columns(int64_t rows, int64_t n_src, int64_t n_dst,
+                                       const float* src, const uint32_t* idx, float* dst,
+                                       void* stream) {
+  if (rows < 0 || n_src < 0 || n_dst < 0 || n_src > (int64_t)0xFFFFFFFFll ||
+      (n_dst > 0 && n_src == 0) ||
+      (rows > 0 && n_dst > 0 && (!src || !idx || !dst || src == dst)))
     return GS_ERR_INVALID_ARG;
-  if (rows == 0 || n == 0) return GS_OK;
+  if (rows == 0 || n_dst == 0) return GS_OK;
   int dev = 0, sms = 0;
   GS_CUDA(cudaGetDevice(&dev));
   GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int64_t blocks = div_up(rows * n, 256) < 16 * sms ? div_up(rows * n, 256) : 16 * sms;
-  permute_columns_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(rows, n, src, perm, dst);
+  const int64_t blocks = div_up(rows * n_dst, 256) < 16 * sms ? div_up(rows * n_dst, 256) : 16 * sms;
+  gather_columns_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(rows, n_src, n_dst, src,
+                                                                            idx, dst);
   GS_CHECK_LAUNCH();
   return GS_OK;
 }

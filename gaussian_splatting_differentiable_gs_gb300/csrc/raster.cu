@@ -292,11 +292,12 @@ __device__ __forceinline__ void pix_init(PixState& P, int tid, int tile_x, int t
 // Forward compositing of staged batch k over the m open pixels packed in
 // P.list[0..m): each worker thread takes one open pixel; each warp walks the
 // entries whose box meets its pixels.
-template <bool kCount>
+template <bool kCount, bool kImp>
 __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* wl, int cnt, int k,
                                           int m, int tile_x, int tile_y, int tid, int warp,
                                           int lane, unsigned long long& n_tested,
-                                          unsigned long long& n_included) {
+                                          unsigned long long& n_included, const uint32_t* ids,
+                                          float* imp) {
   if (warp * 32 >= m) return;
   const bool worker = tid < m;
   const int p = worker ? P.list[tid] : 0;
@@ -344,6 +345,8 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
     Tr = Tn;
     last = base1 + j;
     if (kCount) ++n_included;
+    // largest blending weight of the Gaussian (w >= 0: the bits order as the values)
+    if (kImp) atomicMax(reinterpret_cast<unsigned int*>(imp + ids[j]), __float_as_uint(w));
   }
   if (kCount) n_tested += stop_j;
   P.T[p] = Tr;
@@ -362,10 +365,11 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
 // composited is still staged in its slot; on return `staged` holds the
 // batch index staged in each slot (-1: none).  With `ids`/`E` the staging
 // also records each entry's id and e = z - m (for a backward that reuses the
-// slots).  slot(s, i) names the batch index staged in slot i.
+// slots).  slot(s, i) names the batch index staged in slot i.  kImp: also
+// record each Gaussian's largest blending weight into imp (ids required).
 __device__ __forceinline__ int& slot(int2& s, int i) { return i ? s.y : s.x; }
 
-template <bool kCount>
+template <bool kCount, bool kImp = false>
 __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[kRT],
                                          float2 (*E)[kRT], uint8_t (*wl)[kRT], int32_t* wcount,
                                          const float4* vsplat, const uint32_t* __restrict__ vals,
@@ -373,7 +377,7 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
                                          int tile_y, float ox, float oy, int tid, int warp,
                                          int lane, int2& staged,
                                          unsigned long long& n_tested,
-                                         unsigned long long& n_included) {
+                                         unsigned long long& n_included, float* imp = nullptr) {
   const int64_t len = end - start;
   const int nb = (int)((len + kRT - 1) / kRT);
   staged = make_int2(-1, -1);
@@ -415,8 +419,8 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
     slot(staged, k & 1) = k;
     if ((bal >> lane) & 1u) P.list[off + __popc(bal & ((1u << lane) - 1u))] = tid;
     __syncthreads();
-    fwd_batch<kCount>(P, B, wl[warp], cnt, k, m, tile_x, tile_y, tid, warp, lane, n_tested,
-                      n_included);
+    fwd_batch<kCount, kImp>(P, B, wl[warp], cnt, k, m, tile_x, tile_y, tid, warp, lane, n_tested,
+                            n_included, ids ? ids[k & 1] : nullptr, imp);
     __syncthreads();  // pixel state written; slot k & 1 free for batch k + 2
     bal = __ballot_sync(0xffffffffu, !P.done[tid]);
     if (lane == 0) wcount[warp] = __popc(bal);
@@ -539,6 +543,7 @@ __device__ __forceinline__ void bwd_flush(const Batch& B, const float2* E, const
 
 struct FwdSmem {
   Batch b[2];
+  uint32_t id[2][kRT];  // ids of the staged entries (importance variant)
   PixState px;
   int32_t wcount[kWarps];
   uint8_t wl[kWarps][kRT];  // per-warp entry sub-lists
@@ -547,12 +552,14 @@ struct FwdSmem {
 // kCount: also accumulate the pairs tested / included into counts[0..1]
 // (instrumentation for work accounting: "tested" counts every list entry a
 // pixel passes before it stops, whether or not its box was visited).
-template <bool kCount>
+// kImp: also record every row's largest blending weight alpha T into imp.
+template <bool kCount, bool kImp>
 __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
     int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
     const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
     float bg2, float* __restrict__ image, float* __restrict__ T_final,
-    int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ counts) {
+    int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ counts,
+    float* __restrict__ imp) {
   __shared__ FwdSmem S;
   unsigned long long n_tested = 0, n_included = 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -563,9 +570,10 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
   const float ox = (float)(tile_x * GS_TILE), oy = (float)(tile_y * GS_TILE);
   pix_init(S.px, tid, tile_x, tile_y, W, H);
   int2 staged;
-  fwd_tile<kCount>(S.px, S.b, nullptr, nullptr, S.wl, S.wcount, splats + 3 * view * n, vals, n,
-                   ranges[2 * flat], ranges[2 * flat + 1], tile_x, tile_y, ox, oy, tid, warp,
-                   lane, staged, n_tested, n_included);
+  fwd_tile<kCount, kImp>(S.px, S.b, kImp ? S.id : nullptr, nullptr, S.wl, S.wcount,
+                         splats + 3 * view * n, vals, n, ranges[2 * flat], ranges[2 * flat + 1],
+                         tile_x, tile_y, ox, oy, tid, warp, lane, staged, n_tested, n_included,
+                         kImp ? imp + view * n : nullptr);
   {
     int px, py;
     pixel_of(tid, tile_x, tile_y, px, py);
@@ -839,7 +847,7 @@ static gs_status rasterize_fwd_impl(int64_t n, int32_t n_views, const gs_splat* 
                                     int32_t width, int32_t height, const uint32_t* vals,
                                     const int64_t* ranges, const float* bg, float* image,
                                     float* T_final, int32_t* n_contrib, uint64_t* counts,
-                                    void* stream) {
+                                    float* importance, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
       height < 1 || !bg || !ranges || !image || !T_final || !n_contrib)
     return GS_ERR_INVALID_ARG;
@@ -848,14 +856,22 @@ static gs_status rasterize_fwd_impl(int64_t n, int32_t n_views, const gs_splat* 
   const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE;
   const unsigned grid = (unsigned)(n_views * T);
   unsigned long long* c = reinterpret_cast<unsigned long long*>(counts);
-  if (counts)
-    raster_fwd_kernel<true><<<grid, kRT, 0, (cudaStream_t)stream>>>(
-        n, tiles_x, T, width, height, reinterpret_cast<const float4*>(splats), vals, ranges, bg[0],
-        bg[1], bg[2], image, T_final, n_contrib, c);
-  else
-    raster_fwd_kernel<false><<<grid, kRT, 0, (cudaStream_t)stream>>>(
-        n, tiles_x, T, width, height, reinterpret_cast<const float4*>(splats), vals, ranges, bg[0],
-        bg[1], bg[2], image, T_final, n_contrib, c);
+  const float4* sp = reinterpret_cast<const float4*>(splats);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (importance) {
+    if (n > 0) GS_CUDA(cudaMemsetAsync(importance, 0, sizeof(float) * (size_t)(n * n_views), st));
+    raster_fwd_kernel<false, true><<<grid, kRT, 0, st>>>(n, tiles_x, T, width, height, sp, vals,
+                                                         ranges, bg[0], bg[1], bg[2], image,
+                                                         T_final, n_contrib, c, importance);
+  } else if (counts) {
+    raster_fwd_kernel<true, false><<<grid, kRT, 0, st>>>(n, tiles_x, T, width, height, sp, vals,
+                                                         ranges, bg[0], bg[1], bg[2], image,
+                                                         T_final, n_contrib, c, nullptr);
+  } else {
+    raster_fwd_kernel<false, false><<<grid, kRT, 0, st>>>(n, tiles_x, T, width, height, sp, vals,
+                                                          ranges, bg[0], bg[1], bg[2], image,
+                                                          T_final, n_contrib, c, nullptr);
+  }
   GS_CHECK_LAUNCH();
   return GS_OK;
 }
@@ -865,7 +881,7 @@ extern "C" gs_status gs_rasterize_fwd(int64_t n, int32_t n_views, const gs_splat
                                       const int64_t* ranges, const float* bg, float* image,
                                       float* T_final, int32_t* n_contrib, void* stream) {
   return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
-                            n_contrib, nullptr, stream);
+                            n_contrib, nullptr, nullptr, stream);
 }
 
 extern "C" gs_status gs_rasterize_fwd_counted(int64_t n, int32_t n_views, const gs_splat* splats,
@@ -875,7 +891,18 @@ extern "C" gs_status gs_rasterize_fwd_counted(int64_t n, int32_t n_views, const 
                                               void* stream) {
   if (!counts) return GS_ERR_INVALID_ARG;
   return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
-                            n_contrib, counts, stream);
+                            n_contrib, counts, nullptr, stream);
+}
+
+extern "C" gs_status gs_rasterize_fwd_importance(int64_t n, int32_t n_views, const gs_splat* splats,
+                                                 int32_t width, int32_t height,
+                                                 const uint32_t* vals, const int64_t* ranges,
+                                                 const float* bg, float* image, float* T_final,
+                                                 int32_t* n_contrib, float* importance,
+                                                 void* stream) {
+  if (!importance && n > 0) return GS_ERR_INVALID_ARG;
+  return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
+                            n_contrib, nullptr, importance, stream);
 }
 
 extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,

@@ -292,7 +292,8 @@ gs_status gs_adam_step(int64_t n, float* params, const float* grad, float* m, fl
 /* ---------------------------------------------------------------------- */
 /* Morton order of the Gaussians ([S4] references: Morton order), for the
  * locality of the id-indexed gathers of compositing.  A reorder permutes the
- * columns of every [rows][n] array consistently (parameters, Adam m and v);
+ * columns of every [rows][n] array consistently (parameters, Adam m and v,
+ * with gs_gather_columns);
  * the step's results are those of the original scene with the Gaussians
  * renamed (equal-depth ties in a tile then break by the new ids).
  *
@@ -313,11 +314,48 @@ size_t gs_morton_workspace_bytes(int64_t n);
 gs_status gs_morton_order(int64_t n, const float* params, void* workspace, size_t ws_bytes,
                           uint32_t* perm, void* stream);
 
-/* gs_permute_columns -- dst[r][i] = src[r][perm[i]] for r < rows, i < n
- * (row-major [rows][n] fp32; src and dst distinct; perm entries >= n are
- * clamped to n - 1). */
-gs_status gs_permute_columns(int64_t rows, int64_t n, const float* src, const uint32_t* perm,
-                             float* dst, void* stream);
+/* gs_gather_columns -- dst[r][i] = src[r][idx[i]] for r < rows, i < n_dst
+ * (row-major fp32, src [rows][n_src], dst [rows][n_dst], distinct; idx
+ * entries >= n_src are clamped to n_src - 1).  With idx = perm and n_dst =
+ * n_src it applies a Morton order; with idx from gs_compact_index it drops
+ * pruned Gaussians. */
+gs_status gs_gather_columns(int64_t rows, int64_t n_src, int64_t n_dst, const float* src,
+                            const uint32_t* idx, float* dst, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* Pruning bounded by the per-tile working set ([S3] abstract: pruning that
+ * considers rendering quality and per-tile shared-memory constraints, so
+ * that the fused forward + backward keeps its working set on chip).
+ *
+ * gs_rasterize_fwd_importance -- gs_rasterize_fwd that also records, per
+ * projected row, the largest blending weight alpha T the Gaussian has in
+ * any pixel (its importance).
+ *   importance  [n_views * n] fp32 output (zeroed by this call). */
+gs_status gs_rasterize_fwd_importance(int64_t n, int32_t n_views, const gs_splat* splats,
+                                      int32_t width, int32_t height, const uint32_t* vals,
+                                      const int64_t* ranges, const float* bg, float* image,
+                                      float* T_final, int32_t* n_contrib, float* importance,
+                                      void* stream);
+
+/* gs_prune_mask -- for every (view, tile): L = the largest n_contrib over
+ * its pixels (its working set is list positions [0, L)); when L > capacity,
+ * theta = the capacity-th largest importance in the working set, and every
+ * Gaussian there with importance < theta and importance < tau is marked.
+ * tau is the quality floor (tau > 1 disables it).
+ *   n_contrib   [n_views][H][W] from the forward over the same lists
+ *   importance  [n_views * n] per-row importance (any non-negative score)
+ *   mask        [n] uint8 output: 1 = prune, 0 = keep (zeroed by this call) */
+gs_status gs_prune_mask(int64_t n, int32_t n_views, int32_t width, int32_t height,
+                        const uint32_t* vals, const int64_t* ranges, const int32_t* n_contrib,
+                        const float* importance, int64_t capacity, float tau, uint8_t* mask,
+                        void* stream);
+
+/* gs_compact_index -- idx[0..k) = the indices i with mask[i] == 0, in
+ * order; *n_keep = k (device int64).  workspace: gs_compact_workspace_bytes(n)
+ * bytes, no initialisation needed. */
+size_t gs_compact_workspace_bytes(int64_t n);
+gs_status gs_compact_index(int64_t n, const uint8_t* mask, void* workspace, size_t ws_bytes,
+                           uint32_t* idx, int64_t* n_keep, void* stream);
 
 /* ---------------------------------------------------------------------- */
 const char* gs_status_string(gs_status status);

@@ -52,7 +52,8 @@ def lib():
         L.or_count_isect.restype = i64
         L.or_bin.argtypes = [i64, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.or_raster_fwd.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i64,
-                                    vp, vp, vp, vp, vp]
+                                    vp, vp, vp, vp, vp, vp]
+        L.or_prune_mask.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, i64, C.c_float, vp]
         L.or_raster_fwd_brute.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp,
                                           vp, vp]
         L.or_loss_l1.argtypes = [i64, vp, vp, vp]
@@ -180,8 +181,9 @@ def bin_select(n, n_views, mean2d_f32, radius, depth_f32, width, height, tile_se
 
 
 def raster_fwd(n, n_views, width, height, feats, vals, ranges, bg=(0.0, 0.0, 0.0), tile=TILE,
-               tile_sel=None):
-    """feats: dict with mean2d, conic, opacity, color (any float dtype)."""
+               tile_sel=None, importance=False):
+    """feats: dict with mean2d, conic, opacity, color (any float dtype).
+    importance=True adds each row's largest blending weight alpha T."""
     HW = width * height
     m, co = _f64(feats["mean2d"]), _f64(feats["conic"])
     op, col = _f64(feats["opacity"]), _f64(feats["color"])
@@ -194,11 +196,34 @@ def raster_fwd(n, n_views, width, height, feats, vals, ranges, bg=(0.0, 0.0, 0.0
     pairs = np.zeros((n_views, height, width), np.int64)
     margin = np.full((n_views, height, width), np.inf)
     sel = None if tile_sel is None else np.ascontiguousarray(tile_sel, np.int64)
+    imp = np.zeros(m.shape[0]) if importance else None
     lib().or_raster_fwd(n, n_views, width, height, tile, _p(m), _p(co), _p(op), _p(col),
                         _p(vals), _p(ranges), _p(bgv), _p(sel), 0 if sel is None else sel.size,
-                        _p(image), _p(T_final), _p(n_contrib), _p(pairs), _p(margin))
+                        _p(image), _p(T_final), _p(n_contrib), _p(pairs), _p(margin),
+                        _p(imp))
     del HW
-    return dict(image=image, T_final=T_final, n_contrib=n_contrib, pairs=pairs, margin=margin)
+    out = dict(image=image, T_final=T_final, n_contrib=n_contrib, pairs=pairs, margin=margin)
+    if importance:
+        out["importance"] = imp
+    return out
+
+
+def prune_mask(n, n_views, width, height, vals, ranges, n_contrib, importance_f32, capacity,
+               tau, tile=TILE):
+    """Per-Gaussian uint8 mask (1 = prune) of the working-set-bounded rule."""
+    vals = np.ascontiguousarray(vals, np.uint32)
+    ranges = np.ascontiguousarray(ranges, np.int64)
+    nc = np.ascontiguousarray(n_contrib, np.int32)
+    imp = np.ascontiguousarray(importance_f32, np.float32)
+    mask = np.zeros(n, np.uint8)
+    lib().or_prune_mask(n, n_views, width, height, tile, _p(vals), _p(ranges), _p(nc), _p(imp),
+                        int(capacity), float(np.float32(tau)), _p(mask))
+    return mask
+
+
+def compact_index(mask):
+    """Indices of the entries kept (mask == 0), in order."""
+    return np.nonzero(np.asarray(mask) == 0)[0].astype(np.uint32)
 
 
 def raster_fwd_brute(n, n_views, width, height, feats, bg=(0.0, 0.0, 0.0), tile=TILE):

@@ -513,7 +513,7 @@ void or_raster_fwd(int64_t n, int32_t n_views, int32_t width, int32_t height, in
                    const double* color, const uint32_t* vals, const int64_t* ranges,
                    const double bg[3], const int64_t* tile_sel, int64_t n_sel,
                    double* image, double* T_final, int32_t* n_contrib, int64_t* pairs,
-                   double* margin) {
+                   double* margin, double* importance) {
   const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
   const int64_t T = (int64_t)tx * ty;
   const int64_t n_tiles = tile_sel ? n_sel : n_views * T;
@@ -544,6 +544,7 @@ void or_raster_fwd(int64_t n, int32_t n_views, int32_t width, int32_t height, in
           mg = fmin(mg, rel_dist(Tn, kTMin));
           if (Tn < kTMin) break;
           for (int ch = 0; ch < 3; ++ch) C[ch] += color[3 * r + ch] * alpha * Tr;
+          if (importance && alpha * Tr > importance[r]) importance[r] = alpha * Tr;
           Tr = Tn;
           last = (int32_t)(i - start + 1);
         }
@@ -926,4 +927,51 @@ void or_morton_order(int64_t n, const float* params, uint32_t* perm) {
   for (int64_t i = 0; i < n; ++i) perm[i] = items[i].val;
   free(items);
   free(codes);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Pruning bounded by the per-tile working set ("ByteSplat" abstract:
+ * pruning under rendering-quality and per-tile shared-memory constraints).
+ * For each (view, tile): L = the largest n_contrib over its pixels (capped
+ * at the list length); when L > K, theta = the K-th largest importance of
+ * the entries at positions [0, L), and every entry there with importance <
+ * theta and importance < tau marks its Gaussian.  importance is per row
+ * (view * n + id), fp32 as the library receives it; mask is per Gaussian. */
+static int desc_float_cmp(const void* pa, const void* pb) {
+  const float a = *(const float*)pa, b = *(const float*)pb;
+  return a > b ? -1 : (a < b ? 1 : 0);
+}
+
+void or_prune_mask(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
+                   const uint32_t* vals, const int64_t* ranges, const int32_t* n_contrib,
+                   const float* importance, int64_t K, float tau, uint8_t* mask) {
+  const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
+  const int64_t T = (int64_t)tx * ty, HW = (int64_t)width * height;
+  for (int64_t g = 0; g < n; ++g) mask[g] = 0;
+  for (int64_t flat = 0; flat < n_views * T; ++flat) {
+    const int64_t view = flat / T, t = flat % T;
+    const int32_t x0 = (int32_t)(t % tx) * tile, y0 = (int32_t)(t / tx) * tile;
+    int64_t L = 0;
+    for (int32_t y = y0; y < y0 + tile && y < height; ++y)
+      for (int32_t x = x0; x < x0 + tile && x < width; ++x)
+        if (n_contrib[view * HW + (int64_t)y * width + x] > L)
+          L = n_contrib[view * HW + (int64_t)y * width + x];
+    const int64_t start = ranges[2 * flat], len = ranges[2 * flat + 1] - start;
+    if (L > len) L = len;
+    if (L <= K) continue;
+    float* v = (float*)malloc(sizeof(float) * (size_t)L);
+    for (int64_t i = 0; i < L; ++i) {
+      const float w = importance[view * n + vals[start + i]];
+      v[i] = w > 0.0f ? w : 0.0f;
+    }
+    qsort(v, (size_t)L, sizeof(float), desc_float_cmp);
+    const float theta = v[K - 1];
+    free(v);
+    for (int64_t i = 0; i < L; ++i) {
+      const uint32_t g = vals[start + i];
+      float w = importance[view * n + g];
+      if (!(w > 0.0f)) w = 0.0f;
+      if (w < theta && w < tau) mask[g] = 1;
+    }
+  }
 }

@@ -118,6 +118,11 @@ void or_morton_codes(int64_t n, const float* params, uint64_t* codes);
 /* perm[k] = index of the k-th Gaussian in ascending (code, index) order. */
 void or_morton_order(int64_t n, const float* params, uint32_t* perm);
 
+/* Pruning mask bounded by the per-tile working set; see gs_oracle.c. */
+void or_prune_mask(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
+                   const uint32_t* vals, const int64_t* ranges, const int32_t* n_contrib,
+                   const float* importance, int64_t K, float tau, uint8_t* mask);
+
 /* Forward compositing over the sorted per-tile lists (tiled mode).
  * features are fp64 arrays indexed by row; vals hold gaussian ids (row =
  * view*n + id).  tile_sel/n_sel restrict the work to selected flattened
@@ -126,13 +131,15 @@ void or_morton_order(int64_t n, const float* params, uint32_t* perm);
  * n_contrib[v][H][W]; optional: pairs[v][H][W] (list entries tested before
  * the pixel stopped) and margin[v][H][W] = smallest relative distance of any
  * threshold decision of the pixel (alpha vs 1/255, alpha vs 0.99, next
- * transmittance vs 1e-4) from its cut-off; +inf when nothing was tested. */
+ * transmittance vs 1e-4) from its cut-off; +inf when nothing was tested;
+ * importance[row] (optional, caller-initialised) raised to the largest
+ * blending weight alpha T of the row over the composited pixels. */
 void or_raster_fwd(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
                    const double* mean2d, const double* conic, const double* opacity,
                    const double* color, const uint32_t* vals, const int64_t* ranges,
                    const double bg[3], const int64_t* tile_sel, int64_t n_sel,
                    double* image, double* T_final, int32_t* n_contrib, int64_t* pairs,
-                   double* margin);
+                   double* margin, double* importance);
 
 /* Brute mode: per pixel, every row of the view with radius > 0 whose tile
  * rectangle holds the pixel's tile, visited in (float depth bits, id) order.

@@ -54,13 +54,13 @@ def test_morton_order_stable_on_duplicates_and_ragged_sizes():
         assert np.array_equal(perm, oracle.morton_order(p)), n
 
 
-def test_permute_columns_exact():
+def test_gather_columns_exact():
     gs = _gs()
     rng = np.random.default_rng(4)
     src = rng.standard_normal((59, 10_007)).astype(np.float32)
     perm = rng.permutation(10_007).astype(np.uint32)
     dst = torch.empty((59, 10_007), device="cuda")
-    gs.gs_permute_columns(torch.from_numpy(src).cuda(), torch.from_numpy(perm.view(np.int32)).cuda(),
+    gs.gs_gather_columns(torch.from_numpy(src).cuda(), torch.from_numpy(perm.view(np.int32)).cuda(),
                           dst)
     assert np.array_equal(dst.cpu().numpy(), src[:, perm])
 

@@ -459,3 +459,50 @@ def test_morton_codes_closed_forms(oracle_mod):
     cq = oracle_mod.morton_codes(q)
     assert int(cq[0]) == int(cq[2]) == xs and int(cq[1]) == 0
     assert oracle_mod.morton_order(q).tolist() == [1, 3, 0, 2]
+
+
+# --------------------------------------------------------------------------
+# importance and pruning bounded by the per-tile working set
+
+
+def test_importance_is_largest_blending_weight(oracle_mod):
+    """Two Gaussians on the axis through a pixel centre, both peaking there
+    (the back one is narrower than the front one's hole): importances are
+    their weights at that pixel, alpha1 and (1 - alpha1) alpha2."""
+    p, cam = _centre_scene([0.4, -0.7], [2.0, 5.0], [np.zeros(3), np.zeros(3)])
+    pr = oracle_mod.project(p, [cam])
+    m32, d32 = pr["mean2d"].astype(np.float32), pr["depth"].astype(np.float32)
+    _, vals, ranges = oracle_mod.bin_and_sort(2, 1, m32, pr["radius"], d32, 64, 64)
+    fw = oracle_mod.raster_fwd(2, 1, 64, 64, pr, vals, ranges, importance=True)
+    a1, a2 = 1 / (1 + math.exp(-0.4)), 1 / (1 + math.exp(0.7))
+    assert fw["importance"][0] == pytest.approx(a1, rel=1e-12)
+    assert fw["importance"][1] == pytest.approx((1 - a1) * a2, rel=1e-12)
+
+
+def test_prune_mask_hand_cases(oracle_mod):
+    """Two tiles of one 32x16 view.  Tile 0 lists Gaussians 0..9 with
+    importances .5 .1 .3 .3 .05 .9 .2 .01 | .4 .3 and its pixels composite at
+    most 8 entries (working set = the first 8); tile 1 lists 10, 11."""
+    W, H, n = 32, 16, 12
+    vals = np.arange(12, dtype=np.uint32)
+    ranges = np.array([[0, 10], [10, 12]], np.int64)
+    imp = np.array([.5, .1, .3, .3, .05, .9, .2, .01, .4, .3, .02, .03], np.float32)
+    nc = np.zeros((1, H, W), np.int32)
+    nc[0, 3, 5], nc[0, 0, 0], nc[0, 9, 20] = 8, 2, 2
+
+    def pruned(K, tau):
+        return np.nonzero(oracle_mod.prune_mask(n, 1, W, H, vals, ranges, nc, imp, K, tau))[0].tolist()
+
+    assert pruned(8, 2.0) == []                    # within capacity
+    assert pruned(5, 2.0) == [1, 4, 7]             # 5th largest of the working set is .2
+    assert pruned(5, 0.08) == [4, 7]               # quality floor keeps .1
+    assert pruned(3, 2.0) == [1, 4, 6, 7]          # 3rd largest .3 is tied: both kept
+    assert pruned(1, 2.0) == [0, 1, 2, 3, 4, 6, 7, 10]  # tile 1 over capacity too
+    # a second view where Gaussian 5 is unimportant marks it as well
+    vals2 = np.concatenate([vals, vals])
+    ranges2 = np.array([[0, 10], [10, 12], [12, 22], [22, 24]], np.int64)
+    imp2 = np.concatenate([imp, imp])
+    imp2[12 + 5] = 0.001
+    nc2 = np.concatenate([nc, nc])
+    m = oracle_mod.prune_mask(n, 2, W, H, vals2, ranges2, nc2, imp2, 5, 2.0)
+    assert np.nonzero(m)[0].tolist() == [1, 4, 5, 7]

@@ -22,9 +22,9 @@
 //  - forward: pixel state lives in shared memory and, at every batch, the
 //    still-open pixels are packed onto the first threads of the CTA, so the
 //    per-pair loop runs on full warps and finished warps stop issuing;
-//  - backward: a pair's gradient is reduced across the warp only when more
-//    than two lanes contribute, by recursive halving (8 values in 9
-//    shuffles); one or two contributors add straight into shared memory.
+//  - backward: a pair's gradient is reduced across the warp by recursive
+//    halving (8 values in 9 shuffles) and added to shared memory by one
+//    atomic per value.
 #include <stdint.h>
 
 #include "gs_internal.cuh"
@@ -483,24 +483,18 @@ __device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint8
         }
       }
     }
-    const unsigned bal = __ballot_sync(0xffffffffu, contrib);
-    if (bal) {
-      if (__popc(bal) <= 2) {
-        if (contrib) {
-#pragma unroll
-          for (int c = 0; c < 9; ++c) atomicAdd(&acc[j][c], v[c]);
-        }
-      } else {
-        // values 0..7 end on lanes 0,4,...,28 (one shared atomic each);
-        // value 8 by a plain butterfly on lane 0
-        const float s8 = warp_sum8(v, lane);
-        const float s9 = warp_sum(v[8]);
-        if ((lane & 3) == 0) {
-          const int c = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-          atomicAdd(&acc[j][c], s8);
-        }
-        if (lane == 0) atomicAdd(&acc[j][8], s9);
+    // reduced across the warp even for one or two contributing lanes: their
+    // nine shared atomics on the same addresses would serialise, and cost
+    // more than the shuffles (measured); values 0..7 end on lanes
+    // 0,4,...,28 (one shared atomic each), value 8 by a plain butterfly
+    if (__any_sync(0xffffffffu, contrib)) {
+      const float s8 = warp_sum8(v, lane);
+      const float s9 = warp_sum(v[8]);
+      if ((lane & 3) == 0) {
+        const int c = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+        atomicAdd(&acc[j][c], s8);
       }
+      if (lane == 0) atomicAdd(&acc[j][8], s9);
     }
   }
 }
@@ -541,9 +535,10 @@ __device__ __forceinline__ void bwd_flush(const Batch& B, const float2* E, const
   for (int c = 0; c < 9; ++c) a[c] = 0.f;
 }
 
+template <bool kImp>
 struct FwdSmem {
   Batch b[2];
-  uint32_t id[2][kRT];  // ids of the staged entries (importance variant)
+  uint32_t id[2][kImp ? kRT : 1];  // ids of the staged entries (importance variant)
   PixState px;
   int32_t wcount[kWarps];
   uint8_t wl[kWarps][kRT];  // per-warp entry sub-lists
@@ -554,13 +549,13 @@ struct FwdSmem {
 // pixel passes before it stops, whether or not its box was visited).
 // kImp: also record every row's largest blending weight alpha T into imp.
 template <bool kCount, bool kImp>
-__global__ void __launch_bounds__(kRT) raster_fwd_kernel(
+__global__ void __launch_bounds__(kRT, 6) raster_fwd_kernel(
     int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
     const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
     float bg2, float* __restrict__ image, float* __restrict__ T_final,
     int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ counts,
     float* __restrict__ imp) {
-  __shared__ FwdSmem S;
+  __shared__ FwdSmem<kImp> S;
   unsigned long long n_tested = 0, n_included = 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t flat = blockIdx.x;
@@ -570,7 +565,8 @@ __global__ void __launch_bounds__(kRT) raster_fwd_kernel(
   const float ox = (float)(tile_x * GS_TILE), oy = (float)(tile_y * GS_TILE);
   pix_init(S.px, tid, tile_x, tile_y, W, H);
   int2 staged;
-  fwd_tile<kCount, kImp>(S.px, S.b, kImp ? S.id : nullptr, nullptr, S.wl, S.wcount,
+  fwd_tile<kCount, kImp>(S.px, S.b, kImp ? reinterpret_cast<uint32_t(*)[kRT]>(&S.id[0][0]) : nullptr,
+                         nullptr, S.wl, S.wcount,
                          splats + 3 * view * n, vals, n, ranges[2 * flat], ranges[2 * flat + 1],
                          tile_x, tile_y, ox, oy, tid, warp, lane, staged, n_tested, n_included,
                          kImp ? imp + view * n : nullptr);

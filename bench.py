@@ -62,6 +62,9 @@ def parse():
                     help="quality floor of the pruning (> 1: none)")
     ap.add_argument("--morton", action="store_true",
                     help="rename the Gaussians in Morton order of their means before timing")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager calls only (default: the step captured once in a CUDA graph "
+                         "and replayed is the headline; eager calls give the per-kernel breakdown)")
     ap.add_argument("--separate", action="store_true",
                     help="composite with three calls (forward, L1 loss, backward) instead of the "
                          "fused one")
@@ -413,10 +416,31 @@ def our_arm(args, rank, world, local):
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    clock_info = clocks.stop()
     total_ms, value = aggregate(args.steps, t_start.elapsed_time(t_end), world)
     per_kernel = {nm: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
                   for i, nm in enumerate(names)}
+    eager_ms_step = total_ms / args.steps
+    graph = not args.no_graph
+    if graph:
+        # the whole step captured once and replayed: one launch per step
+        step.capture()
+        for _ in range(3):
+            step.step()
+        torch.cuda.synchronize()
+        barrier(world)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            step.step()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        if step.check() != gs.GS_OK:
+            raise RuntimeError("a replayed step outgrew the intersection buffers")
+        total_ms, value = aggregate(args.steps, g0.elapsed_time(g1), world)
+        kernels_per_step += 2  # count publication, device step counter
+    clock_info = clocks.stop()
     ms_step = total_ms / args.steps
 
     # end to end through the public API: pinned host target in, loss out
@@ -433,6 +457,8 @@ def our_arm(args, rank, world, local):
         losses.append(step.loss.item())
     e1.record(stream)
     torch.cuda.synchronize()
+    if graph and step.check() != gs.GS_OK:
+        raise RuntimeError("a replayed step outgrew the intersection buffers")
     e2e_ms, e2e_value = aggregate(args.steps, e0.elapsed_time(e1), world)
     e2e_wall = time.perf_counter() - w0
 
@@ -489,7 +515,8 @@ def our_arm(args, rank, world, local):
                        "(708 MB parameters, 2.1 GB with Adam state)", "adam": "sparse" if
                        cfg["sparse_adam"] else "dense", "compositing": "fused" if fused else
                        "separate", "gaussian_order": "morton" if args.morton else "as generated",
-                       "pruned_to_capacity": args.prune},
+                       "pruned_to_capacity": args.prune,
+                       "launch": "CUDA graph replay" if graph else "eager calls"},
             "mpix_per_s": round(V * W * H / (raster_ms / 1e3) / 1e6, 2),
             "gaussians_per_s": round(n * V / (ms_step / 1e3), 1),
             "gpu_launches": kernels_per_step * args.steps,
@@ -498,6 +525,7 @@ def our_arm(args, rank, world, local):
                     "wall_s": round(e2e_wall, 3)},
             "roofline": roofline, "kernels": kernels,
             "morton_reorder_ms": None if reorder_ms is None else round(reorder_ms, 3),
+            "eager_ms_per_step": round(eager_ms_step, 4),
             "prune": prune_info,
             "work": {"pairs_tested_fwd": tested, "pairs_included": included,
                      "pairs_bwd": bwd_eval, "visible_rows": visible_rows},

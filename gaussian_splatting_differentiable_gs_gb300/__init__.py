@@ -57,6 +57,9 @@ def lib():
     L.gs_key_bits.restype = i32
     L.gs_bin_and_sort.argtypes = [i64, i32, vp, i32, i32, vp, sz, i64, vp, vp, vp, vp, vp]
     L.gs_workspace_status.argtypes = [vp, vp]
+    L.gs_bin_and_sort_async.argtypes = [i64, i32, vp, i32, i32, vp, sz, i64, vp, vp, vp, vp, vp]
+    L.gs_adam_step_dev.argtypes = [i64, vp, vp, vp, vp, vp, f32, f32, f32, f32, vp, vp, vp]
+    L.gs_step_advance.argtypes = [vp, vp, vp]
     L.gs_rasterize_fwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
     L.gs_rasterize_fwd_counted.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     L.gs_loss_l1.argtypes = [vp, vp, i64, vp, vp, vp]
@@ -172,6 +175,34 @@ def gs_bin_and_sort(n, n_views, splats, width, height, workspace, capacity, keys
 
 def gs_workspace_status(workspace, stream=None):
     return int(lib().gs_workspace_status(_dev(workspace, torch.uint8, "workspace"), _stream(stream)))
+
+
+def gs_bin_and_sort_async(n, n_views, splats, width, height, workspace, capacity, keys, vals,
+                          ranges, n_isect, stream=None):
+    """gs_bin_and_sort without a host synchronisation; n_isect: CUDA int64 [1]."""
+    _check("gs_bin_and_sort_async", lib().gs_bin_and_sort_async(
+        n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), capacity,
+        _dev(keys, torch.int64, "keys"), _dev(vals, torch.int32, "vals"),
+        _dev(ranges, torch.int64, "ranges"), _dev(n_isect, torch.int64, "n_isect"),
+        _stream(stream)))
+
+
+def gs_adam_step_dev(params, grad, m, v, step, lr, beta1=0.9, beta2=0.999, eps=1e-8,
+                     visible=None, bin_workspace=None, stream=None):
+    """gs_adam_step with the step number in a CUDA int64 [1] tensor."""
+    n = params.shape[1]
+    _check("gs_adam_step_dev", lib().gs_adam_step_dev(
+        n, _dev(params, torch.float32, "params"), _dev(grad, torch.float32, "grad"),
+        _dev(m, torch.float32, "m"), _dev(v, torch.float32, "v"), _dev(step, torch.int64, "step"),
+        float(lr), float(beta1), float(beta2), float(eps), _dev(visible, torch.uint8, "visible"),
+        _dev(bin_workspace, torch.uint8, "bin_workspace"), _stream(stream)))
+
+
+def gs_step_advance(step, bin_workspace=None, stream=None):
+    _check("gs_step_advance", lib().gs_step_advance(
+        _dev(step, torch.int64, "step"), _dev(bin_workspace, torch.uint8, "bin_workspace"),
+        _stream(stream)))
 
 
 def gs_rasterize_fwd(n, n_views, splats, width, height, vals, ranges, bg, image, T_final, n_contrib,
@@ -457,7 +488,66 @@ class TrainStep:
             out.append(dst)
         return out[0], out[1], out[2], idx[:k], mask
 
+    # ---- one step captured into a CUDA graph and replayed ------------------
+    def capture(self, margin=1.25):
+        """Captures one training step into a CUDA graph; step() then replays it
+        (one launch for the whole step, no host synchronisation).  Needs one
+        eager step first (it sizes the intersection buffers, kept with
+        `margin` to spare).  The step number lives on the device; a step whose
+        intersections outgrow the buffers updates nothing and is reported by
+        check()."""
+        if self.t == 0:
+            raise RuntimeError("capture() needs one eager step first")
+        dev = self.params.device
+        need = int(self.n_isect * margin) + 1024
+        if need > self.capacity:
+            self._alloc_isect(need)
+        self.step_dev = torch.full((1,), self.t, dtype=torch.int64, device=dev)
+        self.n_isect_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._graph_body()
+        self.graph = g
+
+    def _graph_body(self):
+        self.project()
+        gs_bin_and_sort_async(self.n, self.V, self.splats, self.W, self.H, self.workspace,
+                              self.capacity, self.keys, self.vals, self.ranges, self.n_isect_dev)
+        if self.fused:
+            self.rasterize_fused()
+        else:
+            self.rasterize_fwd()
+            self.loss_l1()
+            self.rasterize_bwd()
+        self.project_bwd()
+        gs_step_advance(self.step_dev, self.workspace)
+        gs_adam_step_dev(self.params, self.grad, self.m, self.v, self.step_dev, self.lr_step,
+                         self.betas[0], self.betas[1], self.eps,
+                         self.visible if self.sparse else None, self.workspace)
+
+    def check(self):
+        """After graph replays: GS_OK, or GS_ERR_CAPACITY when the latest step's
+        intersections outgrew the buffers (that step updated nothing; the
+        buffers are grown, the graph captured again, and the step should be
+        repeated).  Synchronises."""
+        st = gs_workspace_status(self.workspace)
+        if st == GS_ERR_CAPACITY:
+            self.t = int(self.step_dev.item())
+            self.n_isect = int(self.n_isect_dev.item())
+            self.graph = None
+            self.capture()
+        elif st != GS_OK:
+            raise GSError("training step", st)
+        else:
+            self.t = int(self.step_dev.item())
+        return st
+
     def step(self, stream=None):
+        if getattr(self, "graph", None) is not None:
+            self.graph.replay()
+            self.t += 1
+            return self.loss
         if self.fused:
             self.project(stream)
             self.bin_and_sort(stream)

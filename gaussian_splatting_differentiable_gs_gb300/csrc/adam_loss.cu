@@ -24,10 +24,33 @@ __device__ __forceinline__ void adam_one(float& p, float g, float& m, float& v, 
   p -= k.step_size * m / (sqrtf(v) * k.rsqrt_bc2 + k.eps);
 }
 
+// With step_dev, the step number (and so the bias corrections) is read from
+// device memory; with skip, nothing is updated while the binning status word
+// reports an overflow (both for a step captured once and replayed).
+__device__ __forceinline__ bool adam_prologue(AdamK& k, const int64_t* step_dev, float lr,
+                                              const unsigned int* skip) {
+  __shared__ float s_step, s_rbc;
+  if (skip && (*reinterpret_cast<const volatile unsigned int*>(skip) & kWsErrCapacity)) return false;
+  if (step_dev) {
+    if (threadIdx.x == 0) {
+      const double t = (double)*step_dev;
+      s_step = (float)((double)lr / (1.0 - pow((double)k.b1, t)));
+      s_rbc = (float)(1.0 / sqrt(1.0 - pow((double)k.b2, t)));
+    }
+    __syncthreads();
+    k.step_size = s_step;
+    k.rsqrt_bc2 = s_rbc;
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(256) adam_dense_kernel(int64_t count, float* __restrict__ p,
                                                          const float* __restrict__ g,
                                                          float* __restrict__ m,
-                                                         float* __restrict__ v, AdamK k) {
+                                                         float* __restrict__ v, AdamK k,
+                                                         const int64_t* __restrict__ step_dev,
+                                                         float lr, const unsigned int* skip) {
+  if (!adam_prologue(k, step_dev, lr, skip)) return;
   const int64_t n4 = count / 4;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   float4* p4 = reinterpret_cast<float4*>(p);
@@ -54,7 +77,10 @@ __global__ void __launch_bounds__(256) adam_sparse_kernel(int64_t n, float* __re
                                                           float* __restrict__ m,
                                                           float* __restrict__ v,
                                                           const uint8_t* __restrict__ visible,
-                                                          AdamK k) {
+                                                          AdamK k,
+                                                          const int64_t* __restrict__ step_dev,
+                                                          float lr, const unsigned int* skip) {
+  if (!adam_prologue(k, step_dev, lr, skip)) return;
   const int64_t row = blockIdx.y;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n; c += stride) {
@@ -115,16 +141,12 @@ int sm_count() {
 
 using namespace gs;
 
-extern "C" gs_status gs_adam_step(int64_t n, float* params, const float* grad, float* m, float* v,
-                                  int64_t step, float lr, float beta1, float beta2, float eps,
-                                  const uint8_t* visible, void* stream) {
-  if (n < 0 || step < 1 || !(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) ||
-      !(eps >= 0.f))
-    return GS_ERR_INVALID_ARG;
-  if (n == 0) return GS_OK;
-  if (!params || !grad || !m || !v || !aligned16(params) || !aligned16(grad) || !aligned16(m) ||
-      !aligned16(v))
-    return GS_ERR_INVALID_ARG;
+static bool adam_args_valid(int64_t step, float beta1, float beta2, float eps) {
+  return step >= 1 && beta1 >= 0.f && beta1 < 1.f && beta2 >= 0.f && beta2 < 1.f && eps >= 0.f;
+}
+
+// Constants of step `step`, bias corrections in double.
+static AdamK make_adam(float lr, float beta1, float beta2, float eps, int64_t step) {
   AdamK k;
   k.b1 = beta1;
   k.b2 = beta2;
@@ -135,18 +157,69 @@ extern "C" gs_status gs_adam_step(int64_t n, float* params, const float* grad, f
   k.step_size = (float)((double)lr / bc1);
   k.rsqrt_bc2 = (float)(1.0 / sqrt(bc2));
   k.eps = eps;
+  return k;
+}
+
+static gs_status adam_impl(int64_t n, float* params, const float* grad, float* m, float* v,
+                           int64_t step, const int64_t* step_dev, float lr, float beta1,
+                           float beta2, float eps, const uint8_t* visible,
+                           const unsigned int* skip, void* stream) {
+  if (n < 0 || !adam_args_valid(step_dev ? 1 : step, beta1, beta2, eps)) return GS_ERR_INVALID_ARG;
+  if (n == 0) return GS_OK;
+  if (!params || !grad || !m || !v || !aligned16(params) || !aligned16(grad) || !aligned16(m) ||
+      !aligned16(v))
+    return GS_ERR_INVALID_ARG;
+  const AdamK k = make_adam(lr, beta1, beta2, eps, step_dev ? 1 : step);
   cudaStream_t st = (cudaStream_t)stream;
   const int sms = sm_count();
   if (!visible) {
     const int64_t count = (int64_t)GS_NPARAM * n;
     const int64_t want = div_up(count / 4 + 1, 256);
     const unsigned blocks = (unsigned)(want < 8 * sms ? want : 8 * sms);
-    adam_dense_kernel<<<blocks, 256, 0, st>>>(count, params, grad, m, v, k);
+    adam_dense_kernel<<<blocks, 256, 0, st>>>(count, params, grad, m, v, k, step_dev, lr, skip);
   } else {
     const int64_t want = div_up(n, 256);
     dim3 grid((unsigned)(want < 2 * sms ? want : 2 * sms), GS_NPARAM);
-    adam_sparse_kernel<<<grid, 256, 0, st>>>(n, params, grad, m, v, visible, k);
+    adam_sparse_kernel<<<grid, 256, 0, st>>>(n, params, grad, m, v, visible, k, step_dev, lr, skip);
   }
+  GS_CHECK_LAUNCH();
+  return GS_OK;
+}
+
+extern "C" gs_status gs_adam_step(int64_t n, float* params, const float* grad, float* m, float* v,
+                                  int64_t step, float lr, float beta1, float beta2, float eps,
+                                  const uint8_t* visible, void* stream) {
+  return adam_impl(n, params, grad, m, v, step, nullptr, lr, beta1, beta2, eps, visible, nullptr,
+                   stream);
+}
+
+static const unsigned int* status_word(const void* bin_workspace) {
+  return bin_workspace ? reinterpret_cast<const unsigned int*>(
+                             reinterpret_cast<const unsigned char*>(bin_workspace) + kWsStatusOffset)
+                       : nullptr;
+}
+
+extern "C" gs_status gs_adam_step_dev(int64_t n, float* params, const float* grad, float* m,
+                                      float* v, const int64_t* step, float lr, float beta1,
+                                      float beta2, float eps, const uint8_t* visible,
+                                      const void* bin_workspace, void* stream) {
+  if (!step) return GS_ERR_INVALID_ARG;
+  return adam_impl(n, params, grad, m, v, 1, step, lr, beta1, beta2, eps, visible,
+                   status_word(bin_workspace), stream);
+}
+
+namespace gs {
+namespace {
+__global__ void step_advance_kernel(int64_t* step, const unsigned int* skip) {
+  if (skip && (*reinterpret_cast<const volatile unsigned int*>(skip) & kWsErrCapacity)) return;
+  *step += 1;
+}
+}  // namespace
+}  // namespace gs
+
+extern "C" gs_status gs_step_advance(int64_t* step, const void* bin_workspace, void* stream) {
+  if (!step) return GS_ERR_INVALID_ARG;
+  step_advance_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(step, status_word(bin_workspace));
   GS_CHECK_LAUNCH();
   return GS_OK;
 }

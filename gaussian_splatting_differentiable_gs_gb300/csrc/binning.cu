@@ -41,6 +41,7 @@ constexpr int kMaxPasses = 8;
 constexpr uint32_t kSpinLimit = 1u << 22;               // x ~100 ns sleep: >0.4 s
 
 constexpr uint64_t kFlagAgg = 1, kFlagInc = 2, kFlagErr = 3;
+constexpr unsigned int kErrCapacity = kWsErrCapacity;  // intersections exceed capacity
 
 // Workspace header, at offset 0 of the caller's workspace.
 struct WsHeader {
@@ -51,6 +52,7 @@ struct WsHeader {
   unsigned int pad[52];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
+static_assert(offsetof(WsHeader, error) == kWsStatusOffset, "status word offset");
 
 struct WsLayout {
   size_t hist, digit_start, offsets, scan_status, sort_status, keys_alt, vals_alt, total;
@@ -189,8 +191,14 @@ __global__ void __launch_bounds__(256) emit_kernel(int64_t n, int64_t n_rows, in
                                                    uint32_t* __restrict__ hist,
                                                    WsHeader* __restrict__ hdr) {
   __shared__ uint32_t sh[kMaxPasses * kRadix];
+  __shared__ unsigned int s_err;
+  // the asynchronous path leaves the lists unbuilt when they exceed capacity
+  // or when the scan's look-back gave up (its offsets are then incomplete);
+  // the status word comes from earlier kernels: one load per CTA
+  if (threadIdx.x == 0) s_err = hdr->error;
   for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x) sh[i] = 0;
   __syncthreads();
+  if (s_err & (1u | kErrCapacity)) return;
   for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < n_rows;
        r += (int64_t)gridDim.x * blockDim.x) {
     const float4 tail = splats[3 * r + 2];
@@ -255,6 +263,7 @@ struct SortSmem {
   uint32_t scan_w[kSortWarps];
   int part;
   int err;
+  int64_t count;
   uint64_t keys[kSortPart];
   uint32_t vals[kSortPart];
 };
@@ -273,10 +282,19 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(
   if (tid == 0) {
     S.part = (int)atomicAdd(&hdr->pass_ticket[pass], 1u);
     S.err = 0;
+    // count < 0: the intersection count is the scan's total (asynchronous
+    // path, grid sized by capacity; surplus partitions hold the highest
+    // tickets, so no real partition looks back at them); -1 on overflow
+    if (count < 0) S.count = (hdr->error & kErrCapacity) ? -1 : (int64_t)hdr->total;
   }
   __syncthreads();
+  if (count < 0) {
+    count = S.count;
+    if (count < 0) return;
+  }
   const int64_t part = S.part;
   const int64_t pbase = part * kSortPart;
+  if (pbase >= count) return;
   const int64_t wbase = pbase + (int64_t)warp * 32 * kSortKpt;
   // load (warp-striped: item i of lane l is element wbase + 32 i + l) and rank
   uint64_t key[kSortKpt];
@@ -397,7 +415,15 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(
 // 5. [first, last + 1) of each (view, tile) in the sorted keys.
 __global__ void __launch_bounds__(256) ranges_kernel(int64_t count, uint64_t n_flat,
                                                      const uint64_t* __restrict__ keys,
-                                                     int64_t* __restrict__ ranges) {
+                                                     int64_t* __restrict__ ranges,
+                                                     const WsHeader* __restrict__ hdr) {
+  if (count < 0) {  // asynchronous path: the scan's total, nothing on overflow
+    __shared__ int64_t s_count;
+    if (threadIdx.x == 0) s_count = (hdr->error & kErrCapacity) ? -1 : (int64_t)hdr->total;
+    __syncthreads();
+    count = s_count;
+    if (count < 0) return;
+  }
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= count) return;
   const uint64_t f = keys[i] >> 32;
@@ -516,6 +542,31 @@ __global__ void __launch_bounds__(256) gather_columns_kernel(int64_t rows, int64
   }
 }
 
+// Publishes the intersection count and sets the capacity bit of the status
+// word when it exceeds capacity, clears it otherwise (the bit describes the
+// latest call; the timeout and device-check bits stay until read).
+__global__ void check_capacity_kernel(WsHeader* __restrict__ hdr, int64_t capacity,
+                                      int64_t* __restrict__ n_isect) {
+  const unsigned long long total = *reinterpret_cast<volatile unsigned long long*>(&hdr->total);
+  if (n_isect) *n_isect = (int64_t)total;
+  if ((int64_t)total > capacity) atomicOr(&hdr->error, kErrCapacity);
+  else atomicAnd(&hdr->error, ~kErrCapacity);
+}
+
+// The onesweep kernel's shared-memory attribute, set once per device (the
+// asynchronous path is captured into graphs after an eager call).
+cudaError_t ensure_sort_attr() {
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sizeof(SortSmem));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
 int bit_length(uint64_t v) {
   int b = 0;
   while (v) { ++b; v >>= 1; }
@@ -568,7 +619,8 @@ extern "C" gs_status gs_workspace_status(void* workspace, void* stream) {
   GS_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
   if (err) {
     GS_CUDA(cudaMemsetAsync(&hdr->error, 0, sizeof(unsigned int), (cudaStream_t)stream));
-    return (err & 1u) ? GS_ERR_TIMEOUT : GS_ERR_DEVICE_CHECK;
+    if (err & 1u) return GS_ERR_TIMEOUT;
+    return (err & kErrCapacity) ? GS_ERR_CAPACITY : GS_ERR_DEVICE_CHECK;
   }
   return GS_OK;
 }
@@ -615,13 +667,15 @@ extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat*
   struct { unsigned long long total; unsigned int error; unsigned int pad; } h{};
   GS_CUDA(cudaMemcpyAsync(&h, hdr, 16, cudaMemcpyDeviceToHost, st));
   GS_CUDA(cudaStreamSynchronize(st));
-  if (h.error) {
+  if (h.error & ~kErrCapacity) {  // a capacity bit can only be left by an asynchronous call
     GS_CUDA(cudaMemsetAsync(&hdr->error, 0, sizeof(unsigned int), st));
     return (h.error & 1u) ? GS_ERR_TIMEOUT : GS_ERR_DEVICE_CHECK;
   }
   const int64_t I = (int64_t)h.total;
   *n_isect = I;
   if (I > capacity) return GS_ERR_CAPACITY;
+  check_capacity_kernel<<<1, 1, 0, st>>>(hdr, capacity, nullptr);  // clears the bit
+  GS_CHECK_LAUNCH();
   GS_CUDA(cudaMemsetAsync(ranges, 0, sizeof(int64_t) * 2 * (size_t)(n_views * T), st));
   if (I == 0) return GS_OK;
 
@@ -646,7 +700,7 @@ extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat*
   const int64_t sort_parts = div_up(I, kSortPart);
   GS_CUDA(cudaMemsetAsync(sort_status, 0, sizeof(uint64_t) * kRadix * (size_t)sort_parts, st));
   const size_t smem = sizeof(SortSmem);
-  GS_CUDA(cudaFuncSetAttribute(onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  GS_CUDA(ensure_sort_attr());
   for (int p = 0; p < passes; ++p) {
     onesweep_kernel<<<(unsigned)sort_parts, kSortThreads, smem, st>>>(
         I, p, k_a, v_a, k_b, v_b, digit_start, sort_status, hdr);
@@ -655,7 +709,8 @@ extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat*
     uint32_t* tv = v_a; v_a = v_b; v_b = tv;
   }
   // 5. ranges
-  ranges_kernel<<<(unsigned)div_up(I, 256), 256, 0, st>>>(I, (uint64_t)(n_views * T), keys, ranges);
+  ranges_kernel<<<(unsigned)div_up(I, 256), 256, 0, st>>>(I, (uint64_t)(n_views * T), keys, ranges,
+                                                          hdr);
   GS_CHECK_LAUNCH();
   return GS_OK;
 }
@@ -703,7 +758,7 @@ extern "C" gs_status gs_morton_order(int64_t n, const float* params, void* works
   const int64_t sort_parts = div_up(n, kSortPart);
   GS_CUDA(cudaMemsetAsync(sort_status, 0, sizeof(uint64_t) * kRadix * (size_t)sort_parts, st));
   const size_t smem = sizeof(SortSmem);
-  GS_CUDA(cudaFuncSetAttribute(onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  GS_CUDA(ensure_sort_attr());
   uint64_t* k_in = keys_a;
   uint32_t* v_in = perm;
   uint64_t* k_out = keys_b;
@@ -732,6 +787,84 @@ extern "C" gs_status gs_gather_columns(int64_t rows, int64_t n_src, int64_t n_ds
   const int64_t blocks = div_up(rows * n_dst, 256) < 16 * sms ? div_up(rows * n_dst, 256) : 16 * sms;
   gather_columns_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(rows, n_src, n_dst, src,
                                                                             idx, dst);
+  GS_CHECK_LAUNCH();
+  return GS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// gs_bin_and_sort without a host synchronisation (graph-capturable): launch
+// shapes follow `capacity`, the kernels read the intersection count from the
+// workspace, and an overflow is reported through the workspace status word.
+extern "C" gs_status gs_bin_and_sort_async(int64_t n, int32_t n_views, const gs_splat* splats,
+                                           int32_t width, int32_t height, void* workspace,
+                                           size_t ws_bytes, int64_t capacity, uint64_t* keys,
+                                           uint32_t* vals, int64_t* ranges, int64_t* n_isect,
+                                           void* stream) {
+  if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
+      height < 1 || capacity < 1 || capacity > (int64_t)0xFFFFFFFFll || !workspace || !n_isect)
+    return GS_ERR_INVALID_ARG;
+  const int64_t n_rows = n * n_views;
+  const WsLayout L = ws_layout(n_rows, capacity);
+  if (ws_bytes < L.total || !aligned16(workspace) || !ranges || !keys || !vals ||
+      (n_rows > 0 && (!splats || !aligned16(splats))))
+    return GS_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  uint32_t* digit_start = reinterpret_cast<uint32_t*>(ws + L.digit_start);
+  int64_t* offsets = reinterpret_cast<int64_t*>(ws + L.offsets);
+  uint64_t* scan_status = reinterpret_cast<uint64_t*>(ws + L.scan_status);
+  uint64_t* sort_status = reinterpret_cast<uint64_t*>(ws + L.sort_status);
+  uint64_t* keys_alt = reinterpret_cast<uint64_t*>(ws + L.keys_alt);
+  uint32_t* vals_alt = reinterpret_cast<uint32_t*>(ws + L.vals_alt);
+  const int64_t T = tiles_per_view(width, height);
+  const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE, tiles_y = (height + GS_TILE - 1) / GS_TILE;
+  if (n_views * T > (int64_t)0xFFFFFFFFll) return GS_ERR_INVALID_ARG;
+  const int64_t n_flat = n_views * T;
+
+  GS_CUDA(cudaMemsetAsync(&hdr->scan_ticket, 0, sizeof(WsHeader) - offsetof(WsHeader, scan_ticket), st));
+  GS_CUDA(cudaMemsetAsync(&hdr->total, 0, sizeof(hdr->total), st));
+  GS_CUDA(cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, st));
+  GS_CUDA(cudaMemsetAsync(ranges, 0, sizeof(int64_t) * 2 * (size_t)n_flat, st));
+  if (n_rows > 0) {
+    const int64_t scan_parts = div_up(n_rows, kScanPart);
+    GS_CUDA(cudaMemsetAsync(scan_status, 0, sizeof(uint64_t) * (size_t)scan_parts, st));
+    scan_tiles_kernel<<<(unsigned)scan_parts, kScanThreads, 0, st>>>(
+        n_rows, reinterpret_cast<const int4*>(splats), offsets, scan_status, hdr);
+    GS_CHECK_LAUNCH();
+  }
+  check_capacity_kernel<<<1, 1, 0, st>>>(hdr, capacity, n_isect);
+  GS_CHECK_LAUNCH();
+  if (n_rows == 0) return GS_OK;
+  const int passes = (gs_key_bits(n_views, width, height) + 7) / 8;
+  uint64_t* k_a = (passes % 2 == 0) ? keys : keys_alt;
+  uint32_t* v_a = (passes % 2 == 0) ? vals : vals_alt;
+  uint64_t* k_b = (passes % 2 == 0) ? keys_alt : keys;
+  uint32_t* v_b = (passes % 2 == 0) ? vals_alt : vals;
+  int dev = 0, sms = 0;
+  GS_CUDA(cudaGetDevice(&dev));
+  GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t emit_blocks = div_up(n_rows, 256) < 8 * sms ? div_up(n_rows, 256) : 8 * sms;
+  emit_kernel<<<(unsigned)emit_blocks, 256, 0, st>>>(n, n_rows, tiles_x, tiles_y, T, passes,
+                                                     reinterpret_cast<const float4*>(splats),
+                                                     offsets, k_a, v_a, hist, hdr);
+  GS_CHECK_LAUNCH();
+  hist_scan_kernel<<<passes, kRadix, 0, st>>>(hist, digit_start);
+  GS_CHECK_LAUNCH();
+  const int64_t sort_parts = div_up(capacity, kSortPart);
+  GS_CUDA(cudaMemsetAsync(sort_status, 0, sizeof(uint64_t) * kRadix * (size_t)sort_parts, st));
+  const size_t smem = sizeof(SortSmem);
+  GS_CUDA(ensure_sort_attr());
+  for (int p = 0; p < passes; ++p) {
+    onesweep_kernel<<<(unsigned)sort_parts, kSortThreads, smem, st>>>(
+        -1, p, k_a, v_a, k_b, v_b, digit_start, sort_status, hdr);
+    GS_CHECK_LAUNCH();
+    uint64_t* tk = k_a; k_a = k_b; k_b = tk;
+    uint32_t* tv = v_a; v_a = v_b; v_b = tv;
+  }
+  ranges_kernel<<<(unsigned)div_up(capacity, 256), 256, 0, st>>>(-1, (uint64_t)n_flat, keys, ranges,
+                                                                hdr);
   GS_CHECK_LAUNCH();
   return GS_OK;
 }

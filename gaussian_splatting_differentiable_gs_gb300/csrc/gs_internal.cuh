@@ -97,6 +97,11 @@ __host__ __device__ inline int64_t div_up(int64_t a, int64_t b) { return (a + b 
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Binning workspace: byte offset of the device status word, and its bit for
+// "intersections exceed capacity" (set by the asynchronous binning).
+constexpr size_t kWsStatusOffset = 8;
+constexpr unsigned int kWsErrCapacity = 4u;
+
 }  // namespace gs
 
 #define GS_CHECK_LAUNCH()                                  \

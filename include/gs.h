@@ -31,7 +31,8 @@
  *  - Pointers are DEVICE pointers unless marked (host).  Device buffers must
  *    be 16-byte aligned (any cudaMalloc / torch allocation is).
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
- *    legacy default stream).  Only gs_bin_and_sort and gs_workspace_status
+ *    legacy default stream).  Only gs_bin_and_sort (not its asynchronous
+ *    variant), gs_bin_and_sort_static and gs_workspace_status
  *    synchronise the stream.
  *  - Errors: arguments are validated on the host before anything is
  *    enqueued; an invalid call returns GS_ERR_INVALID_ARG and launches
@@ -159,8 +160,26 @@ gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat* splats, in
                           void* stream);
 
 /* Synchronises `stream` and returns (and clears) the device status word of a
- * binning workspace: GS_OK, GS_ERR_TIMEOUT or GS_ERR_DEVICE_CHECK. */
+ * binning workspace: GS_OK, GS_ERR_TIMEOUT, GS_ERR_DEVICE_CHECK, or
+ * GS_ERR_CAPACITY when the latest gs_bin_and_sort_async call exceeded its
+ * capacity. */
 gs_status gs_workspace_status(void* workspace, void* stream);
+
+/* gs_bin_and_sort_async -- gs_bin_and_sort without synchronising the stream,
+ * so that a whole training step can be captured once into a CUDA graph and
+ * replayed.  Launch shapes follow `capacity` (not the intersection count,
+ * which stays on the device); surplus work items exit at once.
+ *   n_isect  (device) int64, receives I
+ * When I > capacity nothing is emitted, ranges are all empty, and the
+ * workspace status word carries the capacity bit: gs_workspace_status then
+ * returns GS_ERR_CAPACITY, and gs_adam_step_dev / gs_step_advance given the
+ * workspace skip their update.  The bit describes the latest call.  The first
+ * call on a device should be made outside graph capture (it sets a kernel
+ * attribute), as any gs_bin_and_sort call does. */
+gs_status gs_bin_and_sort_async(int64_t n, int32_t n_views, const gs_splat* splats,
+                                int32_t width, int32_t height, void* workspace, size_t ws_bytes,
+                                int64_t capacity, uint64_t* keys, uint32_t* vals, int64_t* ranges,
+                                int64_t* n_isect, void* stream);
 
 /* Self-test of the bounded device waits: runs one look-back partition whose
  * predecessor never publishes, so its wait runs out (about a second); the
@@ -288,6 +307,18 @@ gs_status gs_project_bwd(int64_t n, const float* params, const gs_camera* cams, 
 gs_status gs_adam_step(int64_t n, float* params, const float* grad, float* m, float* v,
                        int64_t step, float lr, float beta1, float beta2, float eps,
                        const uint8_t* visible, void* stream);
+
+/* gs_adam_step_dev -- gs_adam_step with the step number read from device
+ * memory (*step >= 1, bias corrections computed on the device), for a step
+ * captured once and replayed.  bin_workspace (or NULL): when its status word
+ * carries the capacity bit of gs_bin_and_sort_async, nothing is updated. */
+gs_status gs_adam_step_dev(int64_t n, float* params, const float* grad, float* m, float* v,
+                           const int64_t* step, float lr, float beta1, float beta2, float eps,
+                           const uint8_t* visible, const void* bin_workspace, void* stream);
+
+/* gs_step_advance -- *step += 1 on the device (step: device int64), unless
+ * bin_workspace (or NULL) carries the capacity bit. */
+gs_status gs_step_advance(int64_t* step, const void* bin_workspace, void* stream);
 
 /* ---------------------------------------------------------------------- */
 /* Morton order of the Gaussians ([S4] references: Morton order), for the

@@ -85,6 +85,18 @@ def test_invalid_arguments_return_before_any_launch(gslib):
     assert L.gs_project_bwd(10, None, cp, 1, None, None, None, None,
                             None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_loss_l1(None, None, -1, None, None, None) == gslib.GS_ERR_INVALID_ARG
+    # the graph-capturable calls
+    assert L.gs_bin_and_sort_async(10, 1, None, 16, 16, None, 0, 100, None, None, None,
+                                   C.byref(out), None) == gslib.GS_ERR_INVALID_ARG  # no workspace
+    assert L.gs_bin_and_sort_async(10, 1, None, 16, 16, None, 0, 0, None, None, None, None,
+                                   None) == gslib.GS_ERR_INVALID_ARG               # capacity 0
+    assert L.gs_adam_step_dev(5, None, None, None, None, None, 1e-3, 0.9, 0.999, 1e-8, None,
+                              None, None) == gslib.GS_ERR_INVALID_ARG              # no step
+    assert L.gs_adam_step_dev(5, None, None, None, None, C.byref(out), 1e-3, 0.9, 0.999, 1e-8,
+                              None, None, None) == gslib.GS_ERR_INVALID_ARG        # NULL arrays
+    assert L.gs_adam_step_dev(5, None, None, None, None, C.byref(out), 1e-3, 1.0, 0.999, 1e-8,
+                              None, None, None) == gslib.GS_ERR_INVALID_ARG        # beta1 = 1
+    assert L.gs_step_advance(None, None, None) == gslib.GS_ERR_INVALID_ARG
 
 
 def test_no_fallback_when_library_missing(gslib, monkeypatch):

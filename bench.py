@@ -44,6 +44,15 @@ ADAM_BYTES = 59 * 28     # B per Gaussian: read p, g, m, v; write p, m, v
 LOSS_BYTES = 36          # B per pixel: image, target read, gradient written (3 channels)
 PROJ_BWD_BYTES = 472     # B per Gaussian: parameters read, gradient written
 PROJ_BWD_ROW = 60        # B per visible row: 36 gradient + 24 conic/colour
+# binning: every row's tile word (16 B) is read; a visible row's position word
+# (16 B) read and its sort element, depth/row and rectangle words written
+# (24 B), 4 depth passes (16 B each), its sorted element and rectangle read at
+# emission (16 B); an intersection written at emission (8 B), 16 B per tile
+# pass (read + write), in the last one its row's depth/row word read and 4 B
+# more written (ids), read by the ranges (8 B)
+BIN_ROW = 16
+BIN_VISIBLE = 16 + 24 + 4 * 16 + 16
+BIN_ISECT = 8 + 8 + 4 + 8
 
 FP32_LANES_PER_SM = 128
 
@@ -328,10 +337,10 @@ def our_arm(args, rank, world, local):
     step = gs.TrainStep(params0.clone(), cams, target, lr=cfg["lr"], sparse=cfg["sparse_adam"],
                         fused=fused)
     stream = torch.cuda.current_stream()
-    passes = (gs.gs_key_bits(V, W, H) + 7) // 8
-    # project, scan, capacity check, emit, digit scan, P passes, ranges, (fused | fwd, loss, bwd),
-    # project_bwd, adam
-    kernels_per_step = (9 if fused else 11) + passes
+    tile_passes = (gs.gs_key_bits(V, W, H) - 32 + 7) // 8
+    # project; binning: compaction, capacity check, 2 digit scans, 4 depth passes, emission,
+    # tile passes, ranges; (fused | fwd, loss, bwd); project_bwd; adam
+    kernels_per_step = (14 if fused else 16) + tile_passes
 
     prune_info = None
     if args.prune is not None:
@@ -476,8 +485,8 @@ def our_arm(args, rank, world, local):
         "rasterize_bwd": ("alu", bwd_flops / 1e12, "TFLOP/s", fp32_peak_tflops),
         "project": ("hbm", (PROJ_READ * n + SPLAT_BYTES * visible_rows +
                             CULLED_BYTES * (rows - visible_rows)) / 1e9, "GB/s", hbm_peak),
-        "bin_and_sort": ("hbm", (12 * rows + 20 * visible_rows + 12 * I +
-                                 (24 * passes + 8) * I + 8 * I) / 1e9, "GB/s", hbm_peak),
+        "bin_and_sort": ("hbm", (BIN_ROW * rows + BIN_VISIBLE * visible_rows +
+                                 (BIN_ISECT + 16 * tile_passes) * I) / 1e9, "GB/s", hbm_peak),
         "loss_l1": ("hbm", LOSS_BYTES * V * W * H / 1e9, "GB/s", hbm_peak),
         "project_bwd": ("hbm", (PROJ_BWD_BYTES * n + PROJ_BWD_ROW * visible_rows) / 1e9, "GB/s",
                         hbm_peak),

@@ -2,17 +2,29 @@
 //
 // "per-tile sorted lists of Gaussian-to-pixel intersections" ("AMD ROCm team
 // open-sources distributed 3D Gaussian Splatting training", per-tile
-// intersection bullet).  Stages, all in-house kernels:
-//   1. single-pass exclusive scan of the per-row tile counts with decoupled
-//      look-back (Merrill & Garland, cited in "A Scalable PyTorch Abstraction
-//      for Multi-GPU Gaussian Splatting", references);
-//   2-3. key emission, one thread per projected row, counting the digits of
-//      every radix pass on the way (no separate histogram read of the keys);
-//   4. stable LSD radix sort, 8-bit digits, one kernel per pass that ranks its
-//      partition, resolves the partition's global digit offsets by decoupled
-//      look-back and scatters ("onesweep"; radix sorting per Merrill &
-//      Grimshaw, same reference list);
+// intersection bullet), ordered by (view, tile, depth) with equal depths in
+// Gaussian order.  The depth order is a property of a projected row, not of
+// its intersections, so the rows are sorted by depth once and their
+// intersections emitted in that order; a stable sort on the tile index alone
+// then finishes the lists.  Stages, all in-house kernels:
+//   1. compaction of the visible rows (rows in order: a decoupled look-back
+//      over their counts, Merrill & Garland, cited in "A Scalable PyTorch
+//      Abstraction for Multi-GPU Gaussian Splatting", references), with the
+//      intersection total and the digit histograms of the depth passes;
+//   2. stable LSD radix sort of the rows on their 32 depth bits, 8-bit
+//      digits, one kernel per pass that ranks its partition, resolves the
+//      partition's global digit offsets by decoupled look-back and scatters
+//      ("onesweep"; radix sorting per Merrill & Grimshaw, same reference
+//      list); an element is one 64-bit word, sort digits in the high half,
+//      the row's compact index in the low half;
+//   3. emission of each row's tiles in depth order (a second look-back scan
+//      gives the offsets; a partition's outputs are spread evenly over its
+//      threads), with the digit histograms of the tile passes;
+//   4. the same radix passes on the tile index (ceil(tile bits / 8) passes);
+//      the last one writes the final (tile << 32 | depth) keys and ids;
 //   5. tile range extraction.
+// The result is the stable sort of (tile << 32 | depth) keys emitted in row
+// order, bit for bit.
 //
 // Device waits: the look-backs are the only waits.  Each partition takes its
 // index from an atomic ticket, so it only ever waits for partitions that are
@@ -27,9 +39,14 @@
 namespace gs {
 namespace {
 
-constexpr int kScanThreads = 256;
-constexpr int kScanItems = 16;
-constexpr int kScanPart = kScanThreads * kScanItems;   // rows per scan partition
+constexpr int kCompThreads = 256;
+constexpr int kCompWarps = kCompThreads / 32;
+constexpr int kCompItems = 8;                           // rows per thread (warp-striped)
+constexpr int kCompPart = kCompThreads * kCompItems;    // rows per compaction partition
+
+constexpr int kEmitThreads = 256;
+constexpr int kEmitItems = 8;
+constexpr int kEmitPart = kEmitThreads * kEmitItems;    // sorted rows per emission partition
 
 constexpr int kSortThreads = 512;
 constexpr int kSortWarps = kSortThreads / 32;
@@ -37,40 +54,53 @@ constexpr int kSortKpt = 8;                             // keys per thread
 constexpr int kSortPart = kSortThreads * kSortKpt;      // keys per sort partition
 constexpr int kRadix = 256;
 constexpr int kMaxPasses = 8;
+constexpr int kDepthPasses = 4;                         // 32 depth bits
 
 constexpr uint32_t kSpinLimit = 1u << 22;               // x ~100 ns sleep: >0.4 s
 
 constexpr uint64_t kFlagAgg = 1, kFlagInc = 2, kFlagErr = 3;
 constexpr unsigned int kErrCapacity = kWsErrCapacity;  // intersections exceed capacity
+constexpr unsigned int kErrStop = 1u | kErrCapacity;    // later stages do nothing
 
 // Workspace header, at offset 0 of the caller's workspace.
 struct WsHeader {
-  unsigned long long total;        // intersections I (written by the scan)
+  unsigned long long total;        // intersections I
   unsigned int error;              // sticky device status (0 = ok)
-  unsigned int scan_ticket;
+  unsigned int scan_ticket;        // compaction partitions
+  unsigned long long rows;         // visible rows R
+  unsigned int emit_ticket;        // emission partitions
   unsigned int pass_ticket[kMaxPasses];
-  unsigned int pad[52];
+  unsigned int pad[49];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 static_assert(offsetof(WsHeader, error) == kWsStatusOffset, "status word offset");
+static_assert(offsetof(WsHeader, rows) == 16, "counts in the first 24 bytes");
 
+// Workspace layout.  Per visible row (compact index c < R): row_u[c] =
+// depth bits << 32 | row, row_rect[c] = first flat tile | width << 32 |
+// height << 48 of its tile rectangle.  tmp: one capacity-sized key buffer;
+// the row sort ping-pongs between it and the caller's key buffer (R <= I <=
+// capacity), as do the tile passes.
 struct WsLayout {
-  size_t hist, digit_start, offsets, scan_status, sort_status, keys_alt, vals_alt, total;
+  size_t hist, digit_start, scan_status, emit_status, sort_status, row_u, row_rect, tmp, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline WsLayout ws_layout(int64_t n_rows, int64_t capacity) {
+  const int64_t r = n_rows > 0 ? n_rows : 1, c = capacity > 0 ? capacity : 1;
+  const int64_t sort_parts = div_up(r, kSortPart) > div_up(c, kSortPart) ? div_up(r, kSortPart)
+                                                                         : div_up(c, kSortPart);
   WsLayout L;
   size_t off = sizeof(WsHeader);
   L.hist = off;        off += align256(sizeof(uint32_t) * kMaxPasses * kRadix);
   L.digit_start = off; off += align256(sizeof(uint32_t) * kMaxPasses * kRadix);
-  L.offsets = off;     off += align256(sizeof(int64_t) * (size_t)(n_rows > 0 ? n_rows : 1));
-  L.scan_status = off; off += align256(sizeof(uint64_t) * (size_t)div_up(n_rows > 0 ? n_rows : 1, kScanPart));
-  L.sort_status = off;
-  off += align256(sizeof(uint64_t) * kRadix * (size_t)div_up(capacity > 0 ? capacity : 1, kSortPart));
-  L.keys_alt = off;    off += align256(sizeof(uint64_t) * (size_t)(capacity > 0 ? capacity : 1));
-  L.vals_alt = off;    off += align256(sizeof(uint32_t) * (size_t)(capacity > 0 ? capacity : 1));
+  L.scan_status = off; off += align256(sizeof(uint64_t) * (size_t)div_up(r, kCompPart));
+  L.emit_status = off; off += align256(sizeof(uint64_t) * (size_t)div_up(r, kEmitPart));
+  L.sort_status = off; off += align256(sizeof(uint64_t) * kRadix * (size_t)sort_parts);
+  L.row_u = off;       off += align256(sizeof(uint64_t) * (size_t)r);
+  L.row_rect = off;    off += align256(sizeof(uint64_t) * (size_t)r);
+  L.tmp = off;         off += align256(sizeof(uint64_t) * (size_t)c);
   L.total = off;
   return L;
 }
@@ -82,154 +112,207 @@ __device__ __forceinline__ void st_volatile(uint64_t* p, uint64_t v) {
   *reinterpret_cast<volatile uint64_t*>(p) = v;
 }
 
-// ---------------------------------------------------------------------------
-// 1. scan of tile counts -> inclusive int64 offsets, total I.
-// Scan status word: value << 2 | flag.
-__global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(
-    int64_t n_rows, const int4* __restrict__ splat_tail, int64_t* __restrict__ offsets,
-    uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
-  __shared__ int s_part;
-  __shared__ long long s_warp[kScanThreads / 32];
-  __shared__ long long s_prefix;
-  __shared__ int s_err;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    s_part = (int)atomicAdd(&hdr->scan_ticket, 1u);
-    s_err = 0;
-  }
-  __syncthreads();
-  const int64_t part = s_part;
-  const int64_t base = part * kScanPart + (int64_t)tid * kScanItems;
-  int64_t v[kScanItems];
-  long long sum = 0;
+// Lanes whose valid 8-bit digit equals this lane's (bit-sliced ballots).
+// Whole-warp call; the result is meaningful for valid lanes only.
+__device__ __forceinline__ uint32_t peers_of_digit(uint32_t d, bool valid) {
+  uint32_t peers = __ballot_sync(0xffffffffu, valid);
 #pragma unroll
-  for (int i = 0; i < kScanItems; ++i) {
-    const int64_t r = base + i;
-    // the tile count is the 4th word of the record's last 16 bytes
-    v[i] = r < n_rows ? (int64_t)splat_tail[3 * r + 2].w : 0;
-    sum += v[i];
+  for (int b = 0; b < 8; ++b) {
+    const uint32_t m = __ballot_sync(0xffffffffu, (d >> b) & 1u);
+    peers &= ((d >> b) & 1u) ? m : ~m;
   }
-  // block-wide inclusive scan of the per-thread sums
-  long long incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+  return peers;
+}
+
+// Decoupled look-back of partition `part` by one thread (status word:
+// value << 2 | flag): publishes the partition's aggregate, adds up its
+// predecessors' until an inclusive prefix, publishes its own inclusive
+// prefix and returns the exclusive one; -1 (error flag published, status
+// bit 1 set) when a wait ran out or a predecessor failed.
+__device__ long long lookback_prefix(uint64_t* status, int64_t part, long long agg,
+                                     WsHeader* hdr) {
+  if (part == 0) {
+    st_volatile(&status[0], ((uint64_t)agg << 2) | kFlagInc);
+    return 0;
   }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    long long w = lane < kScanThreads / 32 ? s_warp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+  st_volatile(&status[part], ((uint64_t)agg << 2) | kFlagAgg);
+  long long prefix = 0;
+  for (int64_t j = part - 1; j >= 0; --j) {
+    uint64_t s;
+    uint32_t spins = 0;
+    while (((s = ld_volatile(&status[j])) & 3u) == 0) {
+      if (++spins > kSpinLimit) break;
+      __nanosleep(100);
     }
-    if (lane < kScanThreads / 32) s_warp[lane] = w;  // inclusive over warps
+    const uint64_t f = s & 3u;
+    if (f == 0 || f == kFlagErr) {
+      st_volatile(&status[part], kFlagErr);
+      atomicOr(&hdr->error, 1u);
+      return -1;
+    }
+    prefix += (long long)(s >> 2);
+    if (f == kFlagInc) break;
   }
-  __syncthreads();
-  const long long block_total = s_warp[kScanThreads / 32 - 1];
-  const long long thread_excl = incl - sum + (warp > 0 ? s_warp[warp - 1] : 0);
-  // decoupled look-back (thread 0)
-  if (tid == 0) {
-    long long prefix = 0;
-    if (part == 0) {
-      st_volatile(&status[0], ((uint64_t)block_total << 2) | kFlagInc);
-    } else {
-      st_volatile(&status[part], ((uint64_t)block_total << 2) | kFlagAgg);
-      int64_t j = part - 1;
-      bool err = false;
-      while (j >= 0) {
-        uint64_t s;
-        uint32_t spins = 0;
-        while (((s = ld_volatile(&status[j])) & 3u) == 0) {
-          if (++spins > kSpinLimit) break;
-          __nanosleep(100);
-        }
-        const uint64_t f = s & 3u;
-        if (f == 0 || f == kFlagErr) { err = true; break; }
-        prefix += (long long)(s >> 2);
-        if (f == kFlagInc) break;
-        --j;
+  __threadfence();
+  st_volatile(&status[part], ((uint64_t)(prefix + agg) << 2) | kFlagInc);
+  return prefix;
+}
+
+// Decoupled look-back of partition `part` by one warp (all 32 lanes call;
+// status word: value << 2 | flag): lane 0 publishes the aggregate, the warp
+// reads 32 predecessors at a time and stops at the nearest inclusive prefix;
+// returns the exclusive prefix (all lanes), -1 when a wait ran out.
+__device__ long long lookback_prefix_warp(uint64_t* status, int64_t part, long long agg,
+                                          WsHeader* hdr) {
+  const int lane = threadIdx.x & 31;
+  if (part == 0) {
+    if (lane == 0) st_volatile(&status[0], ((uint64_t)agg << 2) | kFlagInc);
+    return 0;
+  }
+  if (lane == 0) st_volatile(&status[part], ((uint64_t)agg << 2) | kFlagAgg);
+  long long prefix = 0;
+  int64_t hi = part - 1;
+  for (;;) {
+    const int64_t j = hi - lane;
+    uint64_t s = kFlagInc;  // before partition 0: an inclusive zero
+    if (j >= 0) {
+      uint32_t spins = 0;
+      while (((s = ld_volatile(&status[j])) & 3u) == 0) {
+        if (++spins > kSpinLimit) break;
+        __nanosleep(100);
       }
-      if (err) {
+    }
+    const uint64_t f = s & 3u;
+    if (__any_sync(0xffffffffu, f == 0 || f == kFlagErr)) {
+      if (lane == 0) {
         st_volatile(&status[part], kFlagErr);
         atomicOr(&hdr->error, 1u);
-        s_err = 1;
-      } else {
-        __threadfence();
-        st_volatile(&status[part], ((uint64_t)(prefix + block_total) << 2) | kFlagInc);
       }
+      return -1;
     }
-    s_prefix = prefix;
-    if (!s_err && (part + 1) * kScanPart >= n_rows) hdr->total = (unsigned long long)(prefix + block_total);
-  }
-  __syncthreads();
-  if (s_err) return;
-  long long run = s_prefix + thread_excl;
+    const uint32_t inc = __ballot_sync(0xffffffffu, f == kFlagInc);
+    const int stop = inc ? __ffs(inc) - 1 : 31;
+    long long v = lane <= stop ? (long long)(s >> 2) : 0;
 #pragma unroll
-  for (int i = 0; i < kScanItems; ++i) {
-    run += v[i];
-    if (base + i < n_rows) offsets[base + i] = run;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    prefix += v;
+    if (inc) break;
+    hi -= 32;
   }
+  if (lane == 0) {
+    __threadfence();
+    st_volatile(&status[part], ((uint64_t)(prefix + agg) << 2) | kFlagInc);
+  }
+  return prefix;
 }
 
 // ---------------------------------------------------------------------------
-// 2. emission of (key, id) pairs, one thread per row, and the digit
-//    histograms of every radix pass.  The low 32 key bits (depth) are the same
-//    for all keys of a row, so their digits are counted once per row with the
-//    row's tile count as weight; the tile digits are counted per key.
-//    A row whose rectangle disagrees with its stored tile count (records not
-//    produced by gs_project) writes nothing and raises the device-check bit, so
-//    emission never leaves the row's scanned slot range.
-__global__ void __launch_bounds__(256) emit_kernel(int64_t n, int64_t n_rows, int32_t tiles_x,
-                                                   int32_t tiles_y, int64_t T, int32_t passes,
-                                                   const float4* __restrict__ splats,
-                                                   const int64_t* __restrict__ offsets,
-                                                   uint64_t* __restrict__ keys,
-                                                   uint32_t* __restrict__ vals,
-                                                   uint32_t* __restrict__ hist,
-                                                   WsHeader* __restrict__ hdr) {
-  __shared__ uint32_t sh[kMaxPasses * kRadix];
-  __shared__ unsigned int s_err;
-  // the asynchronous path leaves the lists unbuilt when they exceed capacity
-  // or when the scan's look-back gave up (its offsets are then incomplete);
-  // the status word comes from earlier kernels: one load per CTA
-  if (threadIdx.x == 0) s_err = hdr->error;
-  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x) sh[i] = 0;
+// 1. Compaction of the visible rows (tile count > 0), in row order.  Per
+//    visible row at compact index c: the depth-sort element (depth bits << 32
+//    | c) into sort_in (when c < capacity), row_u[c] and row_rect[c]; the
+//    intersection total I into the header (block sums added atomically) and
+//    R by the last partition; the depth-digit histograms.  Positive depths
+//    order as their bit patterns.  A row whose rectangle disagrees with its
+//    stored tile count (records not produced by gs_project) is left out and
+//    raises the device-check bit.
+__global__ void __launch_bounds__(kCompThreads) compact_rows_kernel(
+    int64_t n_rows, int64_t n, int32_t tiles_x, int32_t tiles_y, int64_t T, int64_t capacity,
+    const float4* __restrict__ splats, uint64_t* __restrict__ sort_in,
+    uint64_t* __restrict__ row_u, uint64_t* __restrict__ row_rect, uint32_t* __restrict__ hist,
+    uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
+  __shared__ uint32_t sh[kDepthPasses * kRadix];
+  __shared__ uint32_t s_warp[kCompWarps];
+  __shared__ unsigned long long s_tiles[kCompWarps];
+  __shared__ long long s_prefix;
+  __shared__ int s_part;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_part = (int)atomicAdd(&hdr->scan_ticket, 1u);
+  for (int i = tid; i < kDepthPasses * kRadix; i += kCompThreads) sh[i] = 0;
   __syncthreads();
-  if (s_err & (1u | kErrCapacity)) return;
-  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < n_rows;
-       r += (int64_t)gridDim.x * blockDim.x) {
-    const float4 tail = splats[3 * r + 2];
-    const int32_t tiles = __float_as_int(tail.w);
-    if (tiles <= 0) continue;
-    const float4 head = splats[3 * r];
-    const int32_t radius = __float_as_int(tail.z);
-    int32_t x0, x1, y0, y1;
-    tile_rect(head.x, head.y, radius, tiles_x, tiles_y, x0, x1, y0, y1);
-    if ((int64_t)(x1 - x0) * (y1 - y0) != tiles) {
-      atomicOr(&hdr->error, 2u);
-      continue;
-    }
-    const int64_t view = r / n;
-    const uint32_t g = (uint32_t)(r - view * n);
-    const uint32_t dbits = __float_as_uint(tail.y);
+  const int64_t part = s_part;
+  // item i of lane l of warp w: row part * kCompPart + w * 32 * kCompItems + 32 i + l
+  const int64_t wbase = part * kCompPart + (int64_t)warp * 32 * kCompItems;
+  uint32_t dbits[kCompItems];
+  uint64_t rect[kCompItems];
+  uint32_t mask[kCompItems];
+  uint32_t wcount = 0;
+  unsigned long long tiles_sum = 0;
 #pragma unroll
-    for (int p = 0; p < 4; ++p) atomicAdd(&sh[p * kRadix + ((dbits >> (8 * p)) & 0xFF)], (uint32_t)tiles);
-    int64_t o = offsets[r] - tiles;
-    for (int32_t ty = y0; ty < y1; ++ty)
-      for (int32_t tx = x0; tx < x1; ++tx) {
-        const uint64_t flat = (uint64_t)(view * T + (int64_t)ty * tiles_x + tx);
-        keys[o] = (flat << 32) | (uint64_t)dbits;
-        vals[o] = g;
-        ++o;
-        for (int p = 4; p < passes; ++p)
-          atomicAdd(&sh[p * kRadix + ((flat >> (8 * (p - 4))) & 0xFF)], 1u);
+  for (int i = 0; i < kCompItems; ++i) {
+    const int64_t r = wbase + 32 * i + lane;
+    bool vis = false;
+    dbits[i] = 0;
+    rect[i] = 0;
+    if (r < n_rows) {
+      const float4 tail = splats[3 * r + 2];
+      const int32_t tiles = __float_as_int(tail.w);
+      if (tiles > 0) {
+        const float4 head = splats[3 * r];
+        int32_t x0, x1, y0, y1;
+        tile_rect(head.x, head.y, __float_as_int(tail.z), tiles_x, tiles_y, x0, x1, y0, y1);
+        if ((int64_t)(x1 - x0) * (y1 - y0) == tiles) {
+          vis = true;
+          const int64_t view = r / n;
+          const uint32_t first = (uint32_t)(view * T + (int64_t)y0 * tiles_x + x0);
+          rect[i] = (uint64_t)first | ((uint64_t)(x1 - x0) << 32) | ((uint64_t)(y1 - y0) << 48);
+          dbits[i] = __float_as_uint(tail.y);
+          tiles_sum += (unsigned long long)tiles;
+        } else {
+          atomicOr(&hdr->error, 2u);
+        }
       }
+    }
+    if (vis) {
+#pragma unroll
+      for (int p = 0; p < kDepthPasses; ++p)
+        atomicAdd(&sh[p * kRadix + ((dbits[i] >> (8 * p)) & 0xFF)], 1u);
+    }
+    mask[i] = __ballot_sync(0xffffffffu, vis);
+    wcount += __popc(mask[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tiles_sum += __shfl_xor_sync(0xffffffffu, tiles_sum, o);
+  if (lane == 0) {
+    s_warp[warp] = wcount;
+    s_tiles[warp] = tiles_sum;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x)
+  uint32_t warp_excl = 0, block_count = 0;
+#pragma unroll
+  for (int w = 0; w < kCompWarps; ++w) {
+    warp_excl += w < warp ? s_warp[w] : 0u;
+    block_count += s_warp[w];
+  }
+  if (warp == 0) {
+    const long long prefix = lookback_prefix_warp(status, part, (long long)block_count, hdr);
+    if (lane == 0) {
+      unsigned long long bt = 0;
+#pragma unroll
+      for (int w = 0; w < kCompWarps; ++w) bt += s_tiles[w];
+      if (bt) atomicAdd(&hdr->total, bt);
+      s_prefix = prefix;
+      if (prefix >= 0 && (part + 1) * kCompPart >= n_rows)
+        hdr->rows = (unsigned long long)(prefix + block_count);
+    }
+  }
+  __syncthreads();
+  if (s_prefix >= 0) {
+    const uint32_t lt = (1u << lane) - 1u;
+    int64_t c = s_prefix + warp_excl;
+#pragma unroll
+    for (int i = 0; i < kCompItems; ++i) {
+      if ((mask[i] >> lane) & 1u) {
+        const int64_t ci = c + __popc(mask[i] & lt);
+        const int64_t r = wbase + 32 * i + lane;
+        if (ci < capacity) sort_in[ci] = ((uint64_t)dbits[i] << 32) | (uint64_t)ci;
+        row_u[ci] = ((uint64_t)dbits[i] << 32) | (uint64_t)r;
+        row_rect[ci] = rect[i];
+      }
+      c += __popc(mask[i]);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < kDepthPasses * kRadix; i += kCompThreads)
     if (sh[i]) atomicAdd(&hist[i], sh[i]);
 }
 
@@ -253,28 +336,309 @@ __global__ void __launch_bounds__(kRadix) hist_scan_kernel(const uint32_t* __res
 }
 
 // ---------------------------------------------------------------------------
-// 4. one stable radix pass (onesweep).  Sort status word:
-//    value << 8 | tag << 2 | flag, tag = pass + 1 (stale entries of an earlier
-//    pass read as not ready).
-struct SortSmem {
+// 2, 4. One stable radix pass over 64-bit keys on the 8 bits at `shift`
+//    (onesweep).  Sort status word: value << 8 | tag << 2 | flag, tag =
+//    pass + 1 (stale entries of an earlier pass read as not ready).  kFinal:
+//    the last tile pass, which writes key (tile << 32 | depth bits) and id
+//    (row mod n) of the element's row c (its low 32 bits) instead.
+struct SortSmem64 {
   uint32_t warp_hist[kSortWarps][kRadix];
   uint32_t local_start[kRadix];
   unsigned long long global_base[kRadix];
   uint32_t scan_w[kSortWarps];
   int part;
   int err;
-  int64_t count;
+  long long count;
+  uint64_t keys[kSortPart];
+};
+
+template <bool kFinal>
+__global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
+    int64_t count, int32_t pass, int32_t shift, const uint64_t* __restrict__ keys_in,
+    uint64_t* __restrict__ keys_out, const uint32_t* __restrict__ digit_start,
+    uint64_t* __restrict__ status, WsHeader* __restrict__ hdr, const uint64_t* __restrict__ row_u,
+    uint32_t* __restrict__ vals_out, uint32_t n) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SortSmem64& S = *reinterpret_cast<SortSmem64*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint64_t tag = (uint64_t)(pass + 1) << 2;
+  for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&S.warp_hist[0][0])[i] = 0;
+  if (tid == 0) {
+    S.part = (int)atomicAdd(&hdr->pass_ticket[pass], 1u);
+    S.err = 0;
+    // count < 0 (asynchronous path, grid sized by an upper bound; surplus
+    // partitions hold the highest tickets, so no real partition looks back
+    // at them): -1 the intersections, -2 the visible rows, read from the
+    // header; nothing to do after an overflow or a wait that ran out
+    if (count < 0)
+      S.count = (hdr->error & kErrStop) ? -1
+                                        : (long long)(count == -1 ? hdr->total : hdr->rows);
+  }
+  __syncthreads();
+  if (count < 0) {
+    count = S.count;
+    if (count < 0) return;
+  }
+  const int64_t part = S.part;
+  const int64_t pbase = part * kSortPart;
+  if (pbase >= count) return;
+  const int64_t wbase = pbase + (int64_t)warp * 32 * kSortKpt;
+  // load (warp-striped: item i of lane l is element wbase + 32 i + l) and rank
+  uint64_t key[kSortKpt];
+  uint32_t rank[kSortKpt];
+#pragma unroll
+  for (int i = 0; i < kSortKpt; ++i) {
+    const int64_t idx = wbase + 32 * i + lane;
+    key[i] = idx < count ? keys_in[idx] : 0ull;
+  }
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < kSortKpt; ++i) {
+    const int64_t idx = wbase + 32 * i + lane;
+    const uint32_t d = idx < count ? (uint32_t)((key[i] >> shift) & 0xFF) : 256u;
+    const uint32_t peers = peers_of_digit(d, d < 256u);
+    uint32_t basec = 0;
+    if (d < 256u) basec = S.warp_hist[warp][d];
+    __syncwarp();
+    if (d < 256u && lane == __ffs(peers) - 1) S.warp_hist[warp][d] = basec + __popc(peers);
+    __syncwarp();
+    rank[i] = basec + __popc(peers & lt_mask);
+  }
+  __syncthreads();
+  // per digit (threads 0..255, i.e. warps 0..7): exclusive prefix over warps,
+  // partition count, aggregate published first so successors can proceed
+  const bool dthread = tid < kRadix;
+  const int d = tid;
+  uint32_t my_count = 0, incl = 0;
+  if (dthread) {
+    uint32_t run = 0;
+#pragma unroll
+    for (int w = 0; w < kSortWarps; ++w) {
+      const uint32_t c = S.warp_hist[w][d];
+      S.warp_hist[w][d] = run;
+      run += c;
+    }
+    my_count = run;
+    if (part == 0)
+      st_volatile(&status[d], ((uint64_t)my_count << 8) | tag | kFlagInc);
+    else
+      st_volatile(&status[part * kRadix + d], ((uint64_t)my_count << 8) | tag | kFlagAgg);
+    incl = my_count;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) S.scan_w[warp] = incl;
+  }
+  __syncthreads();
+  if (dthread) {
+    // exclusive scan of the counts over digits -> local start of each digit
+    uint32_t add = 0;
+    for (int w = 0; w < warp; ++w) add += S.scan_w[w];
+    S.local_start[d] = add + incl - my_count;
+    // look back for this digit
+    unsigned long long excl = 0;
+    if (part > 0) {
+      int64_t j = part - 1;
+      bool err = false;
+      while (j >= 0) {
+        uint64_t s;
+        uint32_t spins = 0;
+        for (;;) {
+          s = ld_volatile(&status[j * kRadix + d]);
+          const uint64_t f = s & 3u;
+          if (f == kFlagErr) break;
+          if (f != 0 && (s & 0xFCu) == tag) break;
+          if (++spins > kSpinLimit) { s = kFlagErr; break; }
+          __nanosleep(100);
+        }
+        const uint64_t f = s & 3u;
+        if (f == kFlagErr) { err = true; break; }
+        excl += (unsigned long long)(s >> 8);
+        if (f == kFlagInc) break;
+        --j;
+      }
+      if (err) {
+        st_volatile(&status[part * kRadix + d], tag | kFlagErr);
+        atomicOr(&hdr->error, 1u);
+        S.err = 1;
+      } else {
+        st_volatile(&status[part * kRadix + d], ((uint64_t)(excl + my_count) << 8) | tag | kFlagInc);
+      }
+    }
+    S.global_base[d] = (unsigned long long)digit_start[pass * kRadix + d] + excl;
+  }
+  __syncthreads();
+  if (S.err) return;
+  // place the partition in smem in sorted (digit-major, stable) order
+#pragma unroll
+  for (int i = 0; i < kSortKpt; ++i) {
+    const int64_t idx = wbase + 32 * i + lane;
+    if (idx < count) {
+      const uint32_t dd = (uint32_t)((key[i] >> shift) & 0xFF);
+      S.keys[S.local_start[dd] + S.warp_hist[warp][dd] + rank[i]] = key[i];
+    }
+  }
+  __syncthreads();
+  const int64_t n_here = count - pbase < kSortPart ? count - pbase : kSortPart;
+  for (int j = tid; j < n_here; j += kSortThreads) {
+    const uint64_t k = S.keys[j];
+    const uint32_t dd = (uint32_t)((k >> shift) & 0xFF);
+    const unsigned long long gpos = S.global_base[dd] + (unsigned long long)(j - S.local_start[dd]);
+    if (gpos < (unsigned long long)count) {
+      if constexpr (kFinal) {
+        const uint64_t u = __ldg(row_u + (uint32_t)k);
+        keys_out[gpos] = (k & 0xFFFFFFFF00000000ull) | (u >> 32);
+        vals_out[gpos] = (uint32_t)u % n;
+      } else {
+        keys_out[gpos] = k;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. Emission in depth order.  The sorted rows are cut into partitions of
+//    kEmitPart; a partition scans its rows' tile counts (the look-back across
+//    partitions gives its output offset), then its threads write the
+//    partition's intersections at consecutive positions, each finding its
+//    row by binary search over the partition's inclusive counts: element
+//    (flat tile << 32 | c), tiles of a row in raster order.  Also the digit
+//    histograms of the tile passes.  count < 0: R from the header.
+__global__ void __launch_bounds__(kEmitThreads) emit_sorted_kernel(
+    int64_t count, int32_t tiles_x, int32_t tile_passes, const uint64_t* __restrict__ sorted,
+    const uint64_t* __restrict__ row_rect, uint64_t* __restrict__ out, uint32_t* __restrict__ hist,
+    uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
+  __shared__ uint32_t s_incl[kEmitPart];   // inclusive tile counts, partition-local
+  __shared__ uint32_t s_first[kEmitPart];  // first flat tile of the row's rectangle
+  __shared__ uint32_t s_w[kEmitPart];      // rectangle width
+  __shared__ uint32_t s_c[kEmitPart];      // compact row index
+  __shared__ uint32_t sh[4 * kRadix];
+  __shared__ uint32_t s_warp[kEmitThreads / 32];
+  __shared__ long long s_count, s_prefix;
+  __shared__ int s_part;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    // the status word and R come from earlier kernels: one load per CTA
+    s_count = (hdr->error & kErrStop) ? -1 : (count < 0 ? (long long)hdr->rows : count);
+    s_part = (int)atomicAdd(&hdr->emit_ticket, 1u);
+  }
+  for (int i = tid; i < tile_passes * kRadix; i += kEmitThreads) sh[i] = 0;
+  __syncthreads();
+  const long long R = s_count;
+  const int64_t part = s_part, pbase = part * kEmitPart;
+  if (R < 0 || pbase >= R) return;
+  const int n_here = R - pbase < kEmitPart ? (int)(R - pbase) : kEmitPart;
+  for (int e = tid; e < kEmitPart; e += kEmitThreads) {
+    uint32_t t = 0;
+    if (e < n_here) {
+      const uint32_t c = (uint32_t)sorted[pbase + e];
+      const uint64_t rc = __ldg(row_rect + c);
+      const uint32_t w = (uint32_t)(rc >> 32) & 0xFFFFu, h = (uint32_t)(rc >> 48);
+      t = w * h;
+      s_first[e] = (uint32_t)rc;
+      s_w[e] = w;
+      s_c[e] = c;
+    }
+    s_incl[e] = t;
+  }
+  __syncthreads();
+  // block scan: thread tid owns elements [tid * kEmitItems, + kEmitItems)
+  uint32_t v[kEmitItems];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int k = 0; k < kEmitItems; ++k) {
+    v[k] = s_incl[tid * kEmitItems + k];
+    sum += v[k];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  uint32_t run = incl - sum, block_total = 0;
+#pragma unroll
+  for (int w = 0; w < kEmitThreads / 32; ++w) {
+    run += w < warp ? s_warp[w] : 0u;
+    block_total += s_warp[w];
+  }
+#pragma unroll
+  for (int k = 0; k < kEmitItems; ++k) {
+    run += v[k];
+    s_incl[tid * kEmitItems + k] = run;
+  }
+  if (warp == 0) {
+    const long long prefix = lookback_prefix_warp(status, part, (long long)block_total, hdr);
+    if (lane == 0) s_prefix = prefix;
+  }
+  __syncthreads();
+  if (s_prefix < 0) return;
+  uint64_t* dst = out + s_prefix;
+  for (uint32_t t = tid; t < block_total; t += kEmitThreads) {
+    int lo = 0, hi = n_here - 1;  // first e with s_incl[e] > t
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_incl[mid] > t) hi = mid; else lo = mid + 1;
+    }
+    const uint32_t i = t - (lo > 0 ? s_incl[lo - 1] : 0u);
+    const uint32_t w = s_w[lo];
+    const uint32_t ty = i / w, tx = i - ty * w;
+    const uint32_t flat = s_first[lo] + ty * (uint32_t)tiles_x + tx;
+    dst[t] = ((uint64_t)flat << 32) | (uint64_t)s_c[lo];
+    for (int p = 0; p < tile_passes; ++p) atomicAdd(&sh[p * kRadix + ((flat >> (8 * p)) & 0xFF)], 1u);
+  }
+  __syncthreads();
+  for (int i = tid; i < tile_passes * kRadix; i += kEmitThreads)
+    if (sh[i]) atomicAdd(&hist[kDepthPasses * kRadix + i], sh[i]);
+}
+
+// ---------------------------------------------------------------------------
+// 5. [first, last + 1) of each (view, tile) in the sorted keys.
+__global__ void __launch_bounds__(256) ranges_kernel(int64_t count, uint64_t n_flat,
+                                                     const uint64_t* __restrict__ keys,
+                                                     int64_t* __restrict__ ranges,
+                                                     const WsHeader* __restrict__ hdr) {
+  if (count < 0) {  // asynchronous path: the scan's total, nothing on overflow
+    __shared__ int64_t s_count;
+    if (threadIdx.x == 0) s_count = (hdr->error & kErrStop) ? -1 : (int64_t)hdr->total;
+    __syncthreads();
+    count = s_count;
+    if (count < 0) return;
+  }
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const uint64_t f = keys[i] >> 32;
+  if (f >= n_flat) return;
+  if (i == 0 || (keys[i - 1] >> 32) != f) ranges[2 * f] = i;
+  if (i == count - 1 || (keys[i + 1] >> 32) != f) ranges[2 * f + 1] = i + 1;
+}
+
+// ---------------------------------------------------------------------------
+// One stable radix pass over (key, value) pairs, for the Morton order ("onesweep",
+// as the key-only passes below).  Sort status word: value << 8 | tag << 2 |
+// flag, tag = pass + 1 (stale entries of an earlier pass read as not ready).
+struct SortSmemKV {
+  uint32_t warp_hist[kSortWarps][kRadix];
+  uint32_t local_start[kRadix];
+  unsigned long long global_base[kRadix];
+  uint32_t scan_w[kSortWarps];
+  int part;
+  int err;
   uint64_t keys[kSortPart];
   uint32_t vals[kSortPart];
 };
 
-__global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(
+__global__ void __launch_bounds__(kSortThreads, 3) onesweep_kv_kernel(
     int64_t count, int32_t pass, const uint64_t* __restrict__ keys_in,
     const uint32_t* __restrict__ vals_in, uint64_t* __restrict__ keys_out,
     uint32_t* __restrict__ vals_out, const uint32_t* __restrict__ digit_start,
     uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  SortSmem& S = *reinterpret_cast<SortSmem*>(smem_raw);
+  SortSmemKV& S = *reinterpret_cast<SortSmemKV*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int shift = 8 * pass;
   const uint64_t tag = (uint64_t)(pass + 1) << 2;
@@ -282,16 +646,8 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(
   if (tid == 0) {
     S.part = (int)atomicAdd(&hdr->pass_ticket[pass], 1u);
     S.err = 0;
-    // count < 0: the intersection count is the scan's total (asynchronous
-    // path, grid sized by capacity; surplus partitions hold the highest
-    // tickets, so no real partition looks back at them); -1 on overflow
-    if (count < 0) S.count = (hdr->error & kErrCapacity) ? -1 : (int64_t)hdr->total;
   }
   __syncthreads();
-  if (count < 0) {
-    count = S.count;
-    if (count < 0) return;
-  }
   const int64_t part = S.part;
   const int64_t pbase = part * kSortPart;
   if (pbase >= count) return;
@@ -312,7 +668,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(
   for (int i = 0; i < kSortKpt; ++i) {
     const int64_t idx = wbase + 32 * i + lane;
     const uint32_t d = idx < count ? (uint32_t)((key[i] >> shift) & 0xFF) : 256u;
-    const uint32_t peers = __match_any_sync(0xffffffffu, d);
+    const uint32_t peers = peers_of_digit(d, d < 256u);
     uint32_t basec = 0;
     if (d < 256u) basec = S.warp_hist[warp][d];
     __syncwarp();
@@ -409,27 +765,6 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kernel(
       vals_out[gpos] = S.vals[j];
     }
   }
-}
-
-// ---------------------------------------------------------------------------
-// 5. [first, last + 1) of each (view, tile) in the sorted keys.
-__global__ void __launch_bounds__(256) ranges_kernel(int64_t count, uint64_t n_flat,
-                                                     const uint64_t* __restrict__ keys,
-                                                     int64_t* __restrict__ ranges,
-                                                     const WsHeader* __restrict__ hdr) {
-  if (count < 0) {  // asynchronous path: the scan's total, nothing on overflow
-    __shared__ int64_t s_count;
-    if (threadIdx.x == 0) s_count = (hdr->error & kErrCapacity) ? -1 : (int64_t)hdr->total;
-    __syncthreads();
-    count = s_count;
-    if (count < 0) return;
-  }
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= count) return;
-  const uint64_t f = keys[i] >> 32;
-  if (f >= n_flat) return;
-  if (i == 0 || (keys[i - 1] >> 32) != f) ranges[2 * f] = i;
-  if (i == count - 1 || (keys[i + 1] >> 32) != f) ranges[2 * f + 1] = i + 1;
 }
 
 // ---------------------------------------------------------------------------
@@ -553,7 +888,7 @@ __global__ void check_capacity_kernel(WsHeader* __restrict__ hdr, int64_t capaci
   else atomicAnd(&hdr->error, ~kErrCapacity);
 }
 
-// The onesweep kernel's shared-memory attribute, set once per device (the
+// The sort kernels' shared-memory attribute, set once per device (the
 // asynchronous path is captured into graphs after an eager call).
 cudaError_t ensure_sort_attr() {
   static bool done[64] = {false};
@@ -561,8 +896,14 @@ cudaError_t ensure_sort_attr() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(onesweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sizeof(SortSmem));
+  e = cudaFuncSetAttribute(onesweep_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sizeof(SortSmemKV));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(onesweep64_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(SortSmem64));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(onesweep64_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(SortSmem64));
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
@@ -571,6 +912,125 @@ int bit_length(uint64_t v) {
   int b = 0;
   while (v) { ++b; v >>= 1; }
   return b;
+}
+
+// Pointers into a binning workspace.
+struct BinBufs {
+  WsHeader* hdr;
+  uint32_t *hist, *digit_start;
+  uint64_t *scan_status, *emit_status, *sort_status, *row_u, *row_rect, *tmp;
+};
+
+BinBufs bin_bufs(void* workspace, const WsLayout& L) {
+  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
+  BinBufs b;
+  b.hdr = reinterpret_cast<WsHeader*>(ws);
+  b.hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  b.digit_start = reinterpret_cast<uint32_t*>(ws + L.digit_start);
+  b.scan_status = reinterpret_cast<uint64_t*>(ws + L.scan_status);
+  b.emit_status = reinterpret_cast<uint64_t*>(ws + L.emit_status);
+  b.sort_status = reinterpret_cast<uint64_t*>(ws + L.sort_status);
+  b.row_u = reinterpret_cast<uint64_t*>(ws + L.row_u);
+  b.row_rect = reinterpret_cast<uint64_t*>(ws + L.row_rect);
+  b.tmp = reinterpret_cast<uint64_t*>(ws + L.tmp);
+  return b;
+}
+
+// Problem shape shared by the binning entry points.
+struct BinShape {
+  int64_t n, n_rows, T, n_flat;
+  int32_t tiles_x, tiles_y;
+  int tile_passes;
+};
+
+bool bin_shape(int64_t n, int32_t n_views, int32_t width, int32_t height, BinShape& s) {
+  if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
+      height < 1)
+    return false;
+  s.n = n;
+  s.n_rows = n * n_views;
+  s.tiles_x = (width + GS_TILE - 1) / GS_TILE;
+  s.tiles_y = (height + GS_TILE - 1) / GS_TILE;
+  s.T = tiles_per_view(width, height);
+  s.n_flat = n_views * s.T;
+  // row index and flat tile index in 32 bits, rectangle sides in 16
+  if (s.n_rows > (int64_t)0xFFFFFFFFll || s.n_flat > (int64_t)0xFFFFFFFFll || s.tiles_x > 0xFFFF ||
+      s.tiles_y > 0xFFFF)
+    return false;
+  const int b = bit_length((uint64_t)(s.n_flat - 1));
+  s.tile_passes = ((b > 0 ? b : 1) + 7) / 8;
+  return true;
+}
+
+// Where the compaction writes the depth-sort elements: the buffer the four
+// depth passes end in, chosen so that the tile passes end their chain in
+// the caller's keys with the last pass reading the other buffer.
+uint64_t* rows_buffer(const BinShape& s, const BinBufs& b, uint64_t* keys) {
+  return s.tile_passes % 2 == 0 ? b.tmp : keys;
+}
+
+gs_status launch_compaction(const BinShape& s, const BinBufs& b, const gs_splat* splats,
+                            int64_t capacity, uint64_t* keys, cudaStream_t st) {
+  const int64_t parts = div_up(s.n_rows, kCompPart);
+  GS_CUDA(cudaMemsetAsync(b.scan_status, 0, sizeof(uint64_t) * (size_t)parts, st));
+  compact_rows_kernel<<<(unsigned)parts, kCompThreads, 0, st>>>(
+      s.n_rows, s.n, s.tiles_x, s.tiles_y, s.T, capacity, reinterpret_cast<const float4*>(splats),
+      rows_buffer(s, b, keys), b.row_u, b.row_rect, b.hist, b.scan_status, b.hdr);
+  GS_CHECK_LAUNCH();
+  return GS_OK;
+}
+
+// Stages 2-5.  rows / isect: the counts, or -2 / -1 to have the kernels read
+// them from the header (grids then sized by rows_max / isect_max).
+gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, int64_t isect,
+                             int64_t rows_max, int64_t isect_max, uint64_t* keys, uint32_t* vals,
+                             int64_t* ranges, cudaStream_t st) {
+  uint64_t* ra = rows_buffer(s, b, keys);
+  uint64_t* rb = ra == keys ? b.tmp : keys;
+  const int64_t parts_r = div_up(rows_max, kSortPart), parts_i = div_up(isect_max, kSortPart);
+  GS_CUDA(cudaMemsetAsync(b.sort_status, 0,
+                          sizeof(uint64_t) * kRadix * (size_t)(parts_r > parts_i ? parts_r : parts_i),
+                          st));
+  hist_scan_kernel<<<kDepthPasses, kRadix, 0, st>>>(b.hist, b.digit_start);
+  GS_CHECK_LAUNCH();
+  GS_CUDA(ensure_sort_attr());
+  const size_t smem = sizeof(SortSmem64);
+  uint64_t* in = ra;
+  uint64_t* out = rb;
+  for (int p = 0; p < kDepthPasses; ++p) {
+    onesweep64_kernel<false><<<(unsigned)parts_r, kSortThreads, smem, st>>>(
+        rows, p, 32 + 8 * p, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u);
+    GS_CHECK_LAUNCH();
+    uint64_t* t = in; in = out; out = t;
+  }
+  // the sorted rows are back in ra
+  const int64_t eparts = div_up(rows_max, kEmitPart);
+  GS_CUDA(cudaMemsetAsync(b.emit_status, 0, sizeof(uint64_t) * (size_t)eparts, st));
+  emit_sorted_kernel<<<(unsigned)eparts, kEmitThreads, 0, st>>>(
+      rows, s.tiles_x, s.tile_passes, ra, b.row_rect, rb, b.hist, b.emit_status, b.hdr);
+  GS_CHECK_LAUNCH();
+  hist_scan_kernel<<<s.tile_passes, kRadix, 0, st>>>(b.hist + kDepthPasses * kRadix,
+                                                     b.digit_start + kDepthPasses * kRadix);
+  GS_CHECK_LAUNCH();
+  in = rb;
+  for (int q = 0; q < s.tile_passes; ++q) {
+    const int p = kDepthPasses + q;
+    if (q == s.tile_passes - 1) {
+      onesweep64_kernel<true><<<(unsigned)parts_i, kSortThreads, smem, st>>>(
+          isect, p, 32 + 8 * q, in, keys, b.digit_start, b.sort_status, b.hdr, b.row_u, vals,
+          (uint32_t)s.n);
+    } else {
+      out = in == keys ? b.tmp : keys;
+      onesweep64_kernel<false><<<(unsigned)parts_i, kSortThreads, smem, st>>>(
+          isect, p, 32 + 8 * q, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u);
+      in = out;
+    }
+    GS_CHECK_LAUNCH();
+  }
+  ranges_kernel<<<(unsigned)div_up(isect_max, 256), 256, 0, st>>>(isect, (uint64_t)s.n_flat, keys,
+                                                                 ranges, b.hdr);
+  GS_CHECK_LAUNCH();
+  return GS_OK;
 }
 
 }  // namespace
@@ -591,21 +1051,19 @@ extern "C" int32_t gs_key_bits(int32_t n_views, int32_t width, int32_t height) {
 }
 
 extern "C" gs_status gs_selftest_lookback_timeout(void* workspace, size_t ws_bytes, void* stream) {
-  // One scan partition is launched with ticket 1, so it looks back at
+  // One compaction partition is launched with ticket 1, so it looks back at
   // partition 0, which never runs: its bounded wait must run out, flag the
   // error and return.  Reads and writes no row data (zero rows).
   const WsLayout L = ws_layout(1, 1);
   if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return GS_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
-  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  uint64_t* scan_status = reinterpret_cast<uint64_t*>(ws + L.scan_status);
-  GS_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
-  GS_CUDA(cudaMemsetAsync(scan_status, 0, sizeof(uint64_t) * 2, st));
+  const BinBufs b = bin_bufs(workspace, L);
+  GS_CUDA(cudaMemsetAsync(b.hdr, 0, sizeof(WsHeader), st));
+  GS_CUDA(cudaMemsetAsync(b.scan_status, 0, sizeof(uint64_t) * 2, st));
   const unsigned one = 1;
-  GS_CUDA(cudaMemcpyAsync(&hdr->scan_ticket, &one, sizeof(one), cudaMemcpyHostToDevice, st));
-  scan_tiles_kernel<<<1, kScanThreads, 0, st>>>(0, nullptr, reinterpret_cast<int64_t*>(ws + L.offsets),
-                                               scan_status, hdr);
+  GS_CUDA(cudaMemcpyAsync(&b.hdr->scan_ticket, &one, sizeof(one), cudaMemcpyHostToDevice, st));
+  compact_rows_kernel<<<1, kCompThreads, 0, st>>>(0, 1, 1, 1, 1, 1, nullptr, b.tmp, b.row_u,
+                                                  b.row_rect, b.hist, b.scan_status, b.hdr);
   GS_CHECK_LAUNCH();
   return gs_workspace_status(workspace, stream);
 }
@@ -630,97 +1088,67 @@ extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat*
                                      size_t ws_bytes, int64_t capacity, uint64_t* keys,
                                      uint32_t* vals, int64_t* ranges, int64_t* n_isect,
                                      void* stream) {
-  if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
-      height < 1 || capacity < 0 || capacity > (int64_t)0xFFFFFFFFll || !n_isect || !workspace)
+  BinShape s;
+  if (!bin_shape(n, n_views, width, height, s) || capacity < 0 ||
+      capacity > (int64_t)0xFFFFFFFFll || !n_isect || !workspace)
     return GS_ERR_INVALID_ARG;
-  const int64_t n_rows = n * n_views;
-  const WsLayout L = ws_layout(n_rows, capacity);
+  const WsLayout L = ws_layout(s.n_rows, capacity);
   if (ws_bytes < L.total || !aligned16(workspace)) return GS_ERR_INVALID_ARG;
-  if (!ranges || (n_rows > 0 && (!splats || !aligned16(splats))) ||
+  if (!ranges || (s.n_rows > 0 && (!splats || !aligned16(splats))) ||
       (capacity > 0 && (!keys || !vals)))
     return GS_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
-  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
-  uint32_t* digit_start = reinterpret_cast<uint32_t*>(ws + L.digit_start);
-  int64_t* offsets = reinterpret_cast<int64_t*>(ws + L.offsets);
-  uint64_t* scan_status = reinterpret_cast<uint64_t*>(ws + L.scan_status);
-  uint64_t* sort_status = reinterpret_cast<uint64_t*>(ws + L.sort_status);
-  uint64_t* keys_alt = reinterpret_cast<uint64_t*>(ws + L.keys_alt);
-  uint32_t* vals_alt = reinterpret_cast<uint32_t*>(ws + L.vals_alt);
-  const int64_t T = tiles_per_view(width, height);
-  const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE, tiles_y = (height + GS_TILE - 1) / GS_TILE;
-  if (n_views * T > (int64_t)0xFFFFFFFFll) return GS_ERR_INVALID_ARG;  // flat index in 32 key bits
+  const BinBufs b = bin_bufs(workspace, L);
 
-  // 1. scan (tickets, total and histograms reset; the status word is kept)
-  GS_CUDA(cudaMemsetAsync(&hdr->scan_ticket, 0, sizeof(WsHeader) - offsetof(WsHeader, scan_ticket), st));
-  GS_CUDA(cudaMemsetAsync(&hdr->total, 0, sizeof(hdr->total), st));
-  GS_CUDA(cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, st));
-  const int64_t scan_parts = div_up(n_rows, kScanPart);
-  if (n_rows > 0) {
-    GS_CUDA(cudaMemsetAsync(scan_status, 0, sizeof(uint64_t) * (size_t)scan_parts, st));
-    scan_tiles_kernel<<<(unsigned)scan_parts, kScanThreads, 0, st>>>(
-        n_rows, reinterpret_cast<const int4*>(splats), offsets, scan_status, hdr);
-    GS_CHECK_LAUNCH();
+  // 1. compaction (tickets, counts and histograms reset; the status word is kept)
+  GS_CUDA(cudaMemsetAsync(&b.hdr->scan_ticket, 0,
+                          sizeof(WsHeader) - offsetof(WsHeader, scan_ticket), st));
+  GS_CUDA(cudaMemsetAsync(&b.hdr->total, 0, sizeof(b.hdr->total), st));
+  GS_CUDA(cudaMemsetAsync(b.hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, st));
+  if (s.n_rows > 0) {
+    const gs_status e = launch_compaction(s, b, splats, capacity, keys, st);
+    if (e != GS_OK) return e;
   }
-  struct { unsigned long long total; unsigned int error; unsigned int pad; } h{};
-  GS_CUDA(cudaMemcpyAsync(&h, hdr, 16, cudaMemcpyDeviceToHost, st));
+  struct { unsigned long long total; unsigned int error, ticket; unsigned long long rows; } h{};
+  static_assert(sizeof(h) == 24, "header prefix");
+  GS_CUDA(cudaMemcpyAsync(&h, b.hdr, sizeof(h), cudaMemcpyDeviceToHost, st));
   GS_CUDA(cudaStreamSynchronize(st));
   if (h.error & ~kErrCapacity) {  // a capacity bit can only be left by an asynchronous call
-    GS_CUDA(cudaMemsetAsync(&hdr->error, 0, sizeof(unsigned int), st));
+    GS_CUDA(cudaMemsetAsync(&b.hdr->error, 0, sizeof(unsigned int), st));
     return (h.error & 1u) ? GS_ERR_TIMEOUT : GS_ERR_DEVICE_CHECK;
   }
-  const int64_t I = (int64_t)h.total;
+  const int64_t I = (int64_t)h.total, R = (int64_t)h.rows;
   *n_isect = I;
   if (I > capacity) return GS_ERR_CAPACITY;
-  check_capacity_kernel<<<1, 1, 0, st>>>(hdr, capacity, nullptr);  // clears the bit
+  check_capacity_kernel<<<1, 1, 0, st>>>(b.hdr, capacity, nullptr);  // clears the bit
   GS_CHECK_LAUNCH();
-  GS_CUDA(cudaMemsetAsync(ranges, 0, sizeof(int64_t) * 2 * (size_t)(n_views * T), st));
+  GS_CUDA(cudaMemsetAsync(ranges, 0, sizeof(int64_t) * 2 * (size_t)s.n_flat, st));
   if (I == 0) return GS_OK;
-
-  const int passes = (gs_key_bits(n_views, width, height) + 7) / 8;
-  uint64_t* k_a = (passes % 2 == 0) ? keys : keys_alt;
-  uint32_t* v_a = (passes % 2 == 0) ? vals : vals_alt;
-  uint64_t* k_b = (passes % 2 == 0) ? keys_alt : keys;
-  uint32_t* v_b = (passes % 2 == 0) ? vals_alt : vals;
-  // 2-3. emission into the buffer that ends up holding the sorted result, with
-  //      the digit histograms of every pass
-  int dev = 0, sms = 0;
-  GS_CUDA(cudaGetDevice(&dev));
-  GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int64_t emit_blocks = div_up(n_rows, 256) < 8 * sms ? div_up(n_rows, 256) : 8 * sms;
-  emit_kernel<<<(unsigned)emit_blocks, 256, 0, st>>>(n, n_rows, tiles_x, tiles_y, T, passes,
-                                                              reinterpret_cast<const float4*>(splats),
-                                                              offsets, k_a, v_a, hist, hdr);
-  GS_CHECK_LAUNCH();
-  hist_scan_kernel<<<passes, kRadix, 0, st>>>(hist, digit_start);
-  GS_CHECK_LAUNCH();
-  // 4. radix passes
-  const int64_t sort_parts = div_up(I, kSortPart);
-  GS_CUDA(cudaMemsetAsync(sort_status, 0, sizeof(uint64_t) * kRadix * (size_t)sort_parts, st));
-  const size_t smem = sizeof(SortSmem);
-  GS_CUDA(ensure_sort_attr());
-  for (int p = 0; p < passes; ++p) {
-    onesweep_kernel<<<(unsigned)sort_parts, kSortThreads, smem, st>>>(
-        I, p, k_a, v_a, k_b, v_b, digit_start, sort_status, hdr);
-    GS_CHECK_LAUNCH();
-    uint64_t* tk = k_a; k_a = k_b; k_b = tk;
-    uint32_t* tv = v_a; v_a = v_b; v_b = tv;
-  }
-  // 5. ranges
-  ranges_kernel<<<(unsigned)div_up(I, 256), 256, 0, st>>>(I, (uint64_t)(n_views * T), keys, ranges,
-                                                          hdr);
-  GS_CHECK_LAUNCH();
-  return GS_OK;
+  return launch_sort_stages(s, b, R, I, R, I, keys, vals, ranges, st);
 }
 
 // ---------------------------------------------------------------------------
 // Morton order entry points
 
-static size_t morton_ws_bytes(int64_t n) {
-  return ws_layout(0, n).total + align256(sizeof(uint64_t) * (size_t)(n > 0 ? n : 1));
+struct MortonLayout {
+  size_t hist, digit_start, sort_status, keys_a, keys_b, vals_b, total;
+};
+
+inline MortonLayout morton_layout(int64_t n) {
+  const size_t m = (size_t)(n > 0 ? n : 1);
+  MortonLayout L;
+  size_t off = sizeof(WsHeader);
+  L.hist = off;        off += align256(sizeof(uint32_t) * kMaxPasses * kRadix);
+  L.digit_start = off; off += align256(sizeof(uint32_t) * kMaxPasses * kRadix);
+  L.sort_status = off; off += align256(sizeof(uint64_t) * kRadix * (size_t)div_up((int64_t)m, kSortPart));
+  L.keys_a = off;      off += align256(sizeof(uint64_t) * m);
+  L.keys_b = off;      off += align256(sizeof(uint64_t) * m);
+  L.vals_b = off;      off += align256(sizeof(uint32_t) * m);
+  L.total = off;
+  return L;
 }
+
+static size_t morton_ws_bytes(int64_t n) { return morton_layout(n).total; }
 
 extern "C" size_t gs_morton_workspace_bytes(int64_t n) { return morton_ws_bytes(n); }
 
@@ -731,15 +1159,15 @@ extern "C" gs_status gs_morton_order(int64_t n, const float* params, void* works
     return GS_ERR_INVALID_ARG;
   if (n == 0) return GS_OK;
   cudaStream_t st = (cudaStream_t)stream;
-  const WsLayout L = ws_layout(0, n);
+  const MortonLayout L = morton_layout(n);
   unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
   uint32_t* digit_start = reinterpret_cast<uint32_t*>(ws + L.digit_start);
   uint64_t* sort_status = reinterpret_cast<uint64_t*>(ws + L.sort_status);
-  uint64_t* keys_b = reinterpret_cast<uint64_t*>(ws + L.keys_alt);
-  uint32_t* vals_b = reinterpret_cast<uint32_t*>(ws + L.vals_alt);
-  uint64_t* keys_a = reinterpret_cast<uint64_t*>(ws + L.total);
+  uint64_t* keys_b = reinterpret_cast<uint64_t*>(ws + L.keys_b);
+  uint32_t* vals_b = reinterpret_cast<uint32_t*>(ws + L.vals_b);
+  uint64_t* keys_a = reinterpret_cast<uint64_t*>(ws + L.keys_a);
   uint32_t* box = hdr->pad;  // six words of the header's spare space
   GS_CUDA(cudaMemsetAsync(&hdr->scan_ticket, 0, sizeof(WsHeader) - offsetof(WsHeader, scan_ticket), st));
   GS_CUDA(cudaMemsetAsync(box, 0xFF, 3 * sizeof(uint32_t), st));
@@ -757,14 +1185,14 @@ extern "C" gs_status gs_morton_order(int64_t n, const float* params, void* works
   GS_CHECK_LAUNCH();
   const int64_t sort_parts = div_up(n, kSortPart);
   GS_CUDA(cudaMemsetAsync(sort_status, 0, sizeof(uint64_t) * kRadix * (size_t)sort_parts, st));
-  const size_t smem = sizeof(SortSmem);
+  const size_t smem = sizeof(SortSmemKV);
   GS_CUDA(ensure_sort_attr());
   uint64_t* k_in = keys_a;
   uint32_t* v_in = perm;
   uint64_t* k_out = keys_b;
   uint32_t* v_out = vals_b;
   for (int p = 0; p < kMortonPasses; ++p) {
-    onesweep_kernel<<<(unsigned)sort_parts, kSortThreads, smem, st>>>(
+    onesweep_kv_kernel<<<(unsigned)sort_parts, kSortThreads, smem, st>>>(
         n, p, k_in, v_in, k_out, v_out, digit_start, sort_status, hdr);
     GS_CHECK_LAUNCH();
     uint64_t* tk = k_in; k_in = k_out; k_out = tk;
@@ -793,78 +1221,35 @@ extern "C" gs_status gs_gather_columns(int64_t rows, int64_t n_src, int64_t n_ds
 
 // ---------------------------------------------------------------------------
 // gs_bin_and_sort without a host synchronisation (graph-capturable): launch
-// shapes follow `capacity`, the kernels read the intersection count from the
-// workspace, and an overflow is reported through the workspace status word.
+// shapes follow the row count and `capacity`, the kernels read the counts
+// from the workspace, and an overflow is reported through the workspace
+// status word.
 extern "C" gs_status gs_bin_and_sort_async(int64_t n, int32_t n_views, const gs_splat* splats,
                                            int32_t width, int32_t height, void* workspace,
                                            size_t ws_bytes, int64_t capacity, uint64_t* keys,
                                            uint32_t* vals, int64_t* ranges, int64_t* n_isect,
                                            void* stream) {
-  if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
-      height < 1 || capacity < 1 || capacity > (int64_t)0xFFFFFFFFll || !workspace || !n_isect)
+  BinShape s;
+  if (!bin_shape(n, n_views, width, height, s) || capacity < 1 ||
+      capacity > (int64_t)0xFFFFFFFFll || !workspace || !n_isect)
     return GS_ERR_INVALID_ARG;
-  const int64_t n_rows = n * n_views;
-  const WsLayout L = ws_layout(n_rows, capacity);
+  const WsLayout L = ws_layout(s.n_rows, capacity);
   if (ws_bytes < L.total || !aligned16(workspace) || !ranges || !keys || !vals ||
-      (n_rows > 0 && (!splats || !aligned16(splats))))
+      (s.n_rows > 0 && (!splats || !aligned16(splats))))
     return GS_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
-  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
-  uint32_t* digit_start = reinterpret_cast<uint32_t*>(ws + L.digit_start);
-  int64_t* offsets = reinterpret_cast<int64_t*>(ws + L.offsets);
-  uint64_t* scan_status = reinterpret_cast<uint64_t*>(ws + L.scan_status);
-  uint64_t* sort_status = reinterpret_cast<uint64_t*>(ws + L.sort_status);
-  uint64_t* keys_alt = reinterpret_cast<uint64_t*>(ws + L.keys_alt);
-  uint32_t* vals_alt = reinterpret_cast<uint32_t*>(ws + L.vals_alt);
-  const int64_t T = tiles_per_view(width, height);
-  const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE, tiles_y = (height + GS_TILE - 1) / GS_TILE;
-  if (n_views * T > (int64_t)0xFFFFFFFFll) return GS_ERR_INVALID_ARG;
-  const int64_t n_flat = n_views * T;
-
-  GS_CUDA(cudaMemsetAsync(&hdr->scan_ticket, 0, sizeof(WsHeader) - offsetof(WsHeader, scan_ticket), st));
-  GS_CUDA(cudaMemsetAsync(&hdr->total, 0, sizeof(hdr->total), st));
-  GS_CUDA(cudaMemsetAsync(hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, st));
-  GS_CUDA(cudaMemsetAsync(ranges, 0, sizeof(int64_t) * 2 * (size_t)n_flat, st));
-  if (n_rows > 0) {
-    const int64_t scan_parts = div_up(n_rows, kScanPart);
-    GS_CUDA(cudaMemsetAsync(scan_status, 0, sizeof(uint64_t) * (size_t)scan_parts, st));
-    scan_tiles_kernel<<<(unsigned)scan_parts, kScanThreads, 0, st>>>(
-        n_rows, reinterpret_cast<const int4*>(splats), offsets, scan_status, hdr);
-    GS_CHECK_LAUNCH();
+  const BinBufs b = bin_bufs(workspace, L);
+  GS_CUDA(cudaMemsetAsync(&b.hdr->scan_ticket, 0,
+                          sizeof(WsHeader) - offsetof(WsHeader, scan_ticket), st));
+  GS_CUDA(cudaMemsetAsync(&b.hdr->total, 0, sizeof(b.hdr->total), st));
+  GS_CUDA(cudaMemsetAsync(b.hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, st));
+  GS_CUDA(cudaMemsetAsync(ranges, 0, sizeof(int64_t) * 2 * (size_t)s.n_flat, st));
+  if (s.n_rows > 0) {
+    const gs_status e = launch_compaction(s, b, splats, capacity, keys, st);
+    if (e != GS_OK) return e;
   }
-  check_capacity_kernel<<<1, 1, 0, st>>>(hdr, capacity, n_isect);
+  check_capacity_kernel<<<1, 1, 0, st>>>(b.hdr, capacity, n_isect);
   GS_CHECK_LAUNCH();
-  if (n_rows == 0) return GS_OK;
-  const int passes = (gs_key_bits(n_views, width, height) + 7) / 8;
-  uint64_t* k_a = (passes % 2 == 0) ? keys : keys_alt;
-  uint32_t* v_a = (passes % 2 == 0) ? vals : vals_alt;
-  uint64_t* k_b = (passes % 2 == 0) ? keys_alt : keys;
-  uint32_t* v_b = (passes % 2 == 0) ? vals_alt : vals;
-  int dev = 0, sms = 0;
-  GS_CUDA(cudaGetDevice(&dev));
-  GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int64_t emit_blocks = div_up(n_rows, 256) < 8 * sms ? div_up(n_rows, 256) : 8 * sms;
-  emit_kernel<<<(unsigned)emit_blocks, 256, 0, st>>>(n, n_rows, tiles_x, tiles_y, T, passes,
-                                                     reinterpret_cast<const float4*>(splats),
-                                                     offsets, k_a, v_a, hist, hdr);
-  GS_CHECK_LAUNCH();
-  hist_scan_kernel<<<passes, kRadix, 0, st>>>(hist, digit_start);
-  GS_CHECK_LAUNCH();
-  const int64_t sort_parts = div_up(capacity, kSortPart);
-  GS_CUDA(cudaMemsetAsync(sort_status, 0, sizeof(uint64_t) * kRadix * (size_t)sort_parts, st));
-  const size_t smem = sizeof(SortSmem);
-  GS_CUDA(ensure_sort_attr());
-  for (int p = 0; p < passes; ++p) {
-    onesweep_kernel<<<(unsigned)sort_parts, kSortThreads, smem, st>>>(
-        -1, p, k_a, v_a, k_b, v_b, digit_start, sort_status, hdr);
-    GS_CHECK_LAUNCH();
-    uint64_t* tk = k_a; k_a = k_b; k_b = tk;
-    uint32_t* tv = v_a; v_a = v_b; v_b = tv;
-  }
-  ranges_kernel<<<(unsigned)div_up(capacity, 256), 256, 0, st>>>(-1, (uint64_t)n_flat, keys, ranges,
-                                                                hdr);
-  GS_CHECK_LAUNCH();
-  return GS_OK;
+  if (s.n_rows == 0) return GS_OK;
+  return launch_sort_stages(s, b, -2, -1, s.n_rows, capacity, keys, vals, ranges, st);
 }

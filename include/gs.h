@@ -128,32 +128,37 @@ size_t gs_bin_workspace_bytes(int64_t n_rows, int64_t capacity);
 int32_t gs_key_bits(int32_t n_views, int32_t width, int32_t height);
 
 /* gs_bin_and_sort -- per-tile depth-sorted intersection lists [S2]:
- *  1. exclusive scan of per-row tile counts (single pass, decoupled
- *     look-back [S4 Merrill & Garland]) -> total I (read back to the host:
- *     the one synchronisation of the step);
- *  2. one (key, id) pair per row and tile of its footprint rectangle, rows in
- *     order and tiles row-major, key = (view * T + tile) << 32 | bits(depth),
- *     T = ceil(W/16) * ceil(H/16);
- *  3. stable LSD radix sort of the pairs on gs_key_bits() key bits, 8 bits
- *     per pass, onesweep style [S4 Merrill & Grimshaw];
- *  4. ranges[(view * T + tile)] = [first, last + 1) of each tile's pairs,
- *     [0, 0) when empty.
- * The sorted order is the unique order of (key, id): ties of equal depth
- * fall back to Gaussian id.
+ * one (key, id) pair per row and tile of its footprint rectangle, key =
+ * (view * T + tile) << 32 | bits(depth), T = ceil(W/16) * ceil(H/16), in the
+ * order of a stable sort of the keys emitted with rows in order and tiles
+ * row-major (ties of equal depth fall back to Gaussian id); and
+ * ranges[(view * T + tile)] = [first, last + 1) of each tile's pairs, [0, 0)
+ * when empty.  Computed as:
+ *  1. compaction of the visible rows (tile count > 0) in row order, single
+ *     pass with decoupled look-back [S4 Merrill & Garland] -> totals I and R
+ *     (read back to the host: the one synchronisation of the step);
+ *  2. stable LSD radix sort of the R visible rows on their 32 depth bits,
+ *     8 bits per pass, onesweep style [S4 Merrill & Grimshaw];
+ *  3. emission of each row's tiles in that order (a second look-back scan
+ *     gives the offsets);
+ *  4. stable radix passes on the tile bits of gs_key_bits() (8 per pass);
+ *  5. the ranges.
  *   splats     [n_views * n] from gs_project
  *   workspace  ws_bytes >= gs_bin_workspace_bytes(n_views * n, capacity);
  *              its first 256 bytes (a status header) must be zero before the
  *              first call (e.g. cudaMemset once after allocation); calls keep
  *              it consistent afterwards
  *   capacity   length of keys/vals (<= 2^32 - 1)
- *   keys, vals [capacity] output: sorted keys and Gaussian ids
+ *   keys, vals [capacity] output: sorted keys and Gaussian ids (also used as
+ *              scratch during the call)
  *   ranges     [n_views * T][2] int64 output
  *   n_isect    (host) receives I, also when I > capacity
- * Returns GS_ERR_CAPACITY (nothing emitted, ranges untouched) when
- * I > capacity; GS_ERR_TIMEOUT if a device wait of the previous call on this
- * workspace ran out; GS_ERR_DEVICE_CHECK if a record's tile count did not
- * match its rectangle (that row emits nothing).  n_views * T must be below
- * 2^32. */
+ * Returns GS_ERR_CAPACITY (no result; ranges untouched, keys and vals
+ * overwritten) when I > capacity; GS_ERR_TIMEOUT if a device wait ran out
+ * (this call's compaction, or the previous call on this workspace);
+ * GS_ERR_DEVICE_CHECK if a record's tile count did not match its rectangle
+ * (that row is left out).  GS_ERR_INVALID_ARG unless n_views * n and
+ * n_views * T are below 2^32 and ceil(W/16), ceil(H/16) <= 65535. */
 gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
                           int32_t height, void* workspace, size_t ws_bytes, int64_t capacity,
                           uint64_t* keys, uint32_t* vals, int64_t* ranges, int64_t* n_isect,
@@ -167,8 +172,8 @@ gs_status gs_workspace_status(void* workspace, void* stream);
 
 /* gs_bin_and_sort_async -- gs_bin_and_sort without synchronising the stream,
  * so that a whole training step can be captured once into a CUDA graph and
- * replayed.  Launch shapes follow `capacity` (not the intersection count,
- * which stays on the device); surplus work items exit at once.
+ * replayed.  Launch shapes follow n_views * n and `capacity` (not the counts,
+ * which stay on the device); surplus work items exit at once.
  *   n_isect  (device) int64, receives I
  * When I > capacity nothing is emitted, ranges are all empty, and the
  * workspace status word carries the capacity bit: gs_workspace_status then

@@ -51,9 +51,11 @@ def test_key_bits_and_workspace(gslib):
     assert gslib.gs_key_bits(8, 1920, 1080) == 48
     assert gslib.gs_key_bits(1, 3840, 2160) == 47
     assert gslib.gs_key_bits(1, 16, 16) == 33
-    a = gslib.gs_bin_workspace_bytes(1000, 10_000)
-    b = gslib.gs_bin_workspace_bytes(1000, 20_000)
-    assert a > 12 * 10_000 and b - a >= 12 * 10_000
+    # one capacity-sized key buffer (8 B) and two per-row words (16 B)
+    a = gslib.gs_bin_workspace_bytes(1024, 10_240)
+    b = gslib.gs_bin_workspace_bytes(1024, 20_480)
+    c = gslib.gs_bin_workspace_bytes(2048, 20_480)
+    assert a > 8 * 10_240 + 16 * 1024 and b - a >= 8 * 10_240 and c - b >= 16 * 1024
     assert gslib.gs_bin_workspace_bytes(-1, 0) == 0
 
 
@@ -76,6 +78,11 @@ def test_invalid_arguments_return_before_any_launch(gslib):
     out = C.c_int64(0)
     assert L.gs_bin_and_sort(10, 1, None, 16, 16, None, 0, 0, None, None, None, C.byref(out),
                              None) == gslib.GS_ERR_INVALID_ARG                     # no workspace
+    ws = C.create_string_buffer(64)
+    assert L.gs_bin_and_sort(1 << 29, 8, None, 16, 16, ws, 64, 0, None, None, None, C.byref(out),
+                             None) == gslib.GS_ERR_INVALID_ARG                     # 2^32 rows
+    assert L.gs_bin_and_sort(1, 1, None, 16 * 65536, 16, ws, 64, 0, None, None, None,
+                             C.byref(out), None) == gslib.GS_ERR_INVALID_ARG       # 65536 tiles wide
     assert L.gs_rasterize_fwd(10, 1, None, 16, 16, None, None, None, None, None, None,
                               None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_rasterize_bwd(10, 17, None, 16, 16, None, None, None, None, None, None, None,

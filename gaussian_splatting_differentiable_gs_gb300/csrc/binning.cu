@@ -44,8 +44,8 @@ constexpr int kCompWarps = kCompThreads / 32;
 constexpr int kCompItems = 8;                           // rows per thread (warp-striped)
 constexpr int kCompPart = kCompThreads * kCompItems;    // rows per compaction partition
 
-constexpr int kEmitThreads = 256;
-constexpr int kEmitItems = 8;
+constexpr int kEmitThreads = 512;
+constexpr int kEmitItems = 4;
 constexpr int kEmitPart = kEmitThreads * kEmitItems;    // sorted rows per emission partition
 
 constexpr int kSortThreads = 512;
@@ -362,6 +362,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
   SortSmem64& S = *reinterpret_cast<SortSmem64*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint64_t tag = (uint64_t)(pass + 1) << 2;
+  const int hs = shift - 32;  // the digit lies in the high word
   for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&S.warp_hist[0][0])[i] = 0;
   if (tid == 0) {
     S.part = (int)atomicAdd(&hdr->pass_ticket[pass], 1u);
@@ -382,27 +383,31 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
   const int64_t part = S.part;
   const int64_t pbase = part * kSortPart;
   if (pbase >= count) return;
-  const int64_t wbase = pbase + (int64_t)warp * 32 * kSortKpt;
+  const int n_here = count - pbase < kSortPart ? (int)(count - pbase) : kSortPart;
+  const uint64_t* src = keys_in + pbase;
+  const int wbase = warp * 32 * kSortKpt;
   // load (warp-striped: item i of lane l is element wbase + 32 i + l) and rank
   uint64_t key[kSortKpt];
-  uint32_t rank[kSortKpt];
 #pragma unroll
   for (int i = 0; i < kSortKpt; ++i) {
-    const int64_t idx = wbase + 32 * i + lane;
-    key[i] = idx < count ? keys_in[idx] : 0ull;
+    const int li = wbase + 32 * i + lane;
+    key[i] = li < n_here ? src[li] : 0ull;
   }
   const uint32_t lt_mask = (1u << lane) - 1u;
+  // rank of each key among the warp's keys of its digit (< 256: one byte
+  // each, four to a register)
+  uint32_t rank4[(kSortKpt + 3) / 4] = {};
 #pragma unroll
   for (int i = 0; i < kSortKpt; ++i) {
-    const int64_t idx = wbase + 32 * i + lane;
-    const uint32_t d = idx < count ? (uint32_t)((key[i] >> shift) & 0xFF) : 256u;
-    const uint32_t peers = peers_of_digit(d, d < 256u);
+    const bool valid = wbase + 32 * i + lane < n_here;
+    const uint32_t d = ((uint32_t)(key[i] >> 32) >> hs) & 0xFFu;
+    const uint32_t peers = peers_of_digit(d, valid);
     uint32_t basec = 0;
-    if (d < 256u) basec = S.warp_hist[warp][d];
+    if (valid) basec = S.warp_hist[warp][d];
     __syncwarp();
-    if (d < 256u && lane == __ffs(peers) - 1) S.warp_hist[warp][d] = basec + __popc(peers);
+    if (valid && lane == __ffs(peers) - 1) S.warp_hist[warp][d] = basec + __popc(peers);
     __syncwarp();
-    rank[i] = basec + __popc(peers & lt_mask);
+    rank4[i / 4] |= ((basec + __popc(peers & lt_mask)) & 0xFFu) << (8 * (i % 4));
   }
   __syncthreads();
   // per digit (threads 0..255, i.e. warps 0..7): exclusive prefix over warps,
@@ -467,25 +472,26 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
         st_volatile(&status[part * kRadix + d], ((uint64_t)(excl + my_count) << 8) | tag | kFlagInc);
       }
     }
-    S.global_base[d] = (unsigned long long)digit_start[pass * kRadix + d] + excl;
+    // global position of the digit's first key, less its local start
+    S.global_base[d] = (unsigned long long)digit_start[pass * kRadix + d] + excl -
+                       (unsigned long long)S.local_start[d];
   }
   __syncthreads();
   if (S.err) return;
   // place the partition in smem in sorted (digit-major, stable) order
 #pragma unroll
   for (int i = 0; i < kSortKpt; ++i) {
-    const int64_t idx = wbase + 32 * i + lane;
-    if (idx < count) {
-      const uint32_t dd = (uint32_t)((key[i] >> shift) & 0xFF);
-      S.keys[S.local_start[dd] + S.warp_hist[warp][dd] + rank[i]] = key[i];
+    if (wbase + 32 * i + lane < n_here) {
+      const uint32_t dd = ((uint32_t)(key[i] >> 32) >> hs) & 0xFFu;
+      S.keys[S.local_start[dd] + S.warp_hist[warp][dd] + ((rank4[i / 4] >> (8 * (i % 4))) & 0xFFu)] =
+          key[i];
     }
   }
   __syncthreads();
-  const int64_t n_here = count - pbase < kSortPart ? count - pbase : kSortPart;
   for (int j = tid; j < n_here; j += kSortThreads) {
     const uint64_t k = S.keys[j];
-    const uint32_t dd = (uint32_t)((k >> shift) & 0xFF);
-    const unsigned long long gpos = S.global_base[dd] + (unsigned long long)(j - S.local_start[dd]);
+    const uint32_t dd = ((uint32_t)(k >> 32) >> hs) & 0xFFu;
+    const unsigned long long gpos = S.global_base[dd] + (unsigned long long)j;
     if (gpos < (unsigned long long)count) {
       if constexpr (kFinal) {
         const uint64_t u = __ldg(row_u + (uint32_t)k);

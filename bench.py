@@ -49,10 +49,10 @@ PROJ_BWD_ROW = 60        # B per visible row: 36 gradient + 24 conic/colour
 # (24 B), 4 depth passes (16 B each), its sorted element and rectangle read at
 # emission (16 B); an intersection written at emission (8 B), 16 B per tile
 # pass (read + write), in the last one its row's depth/row word read and 4 B
-# more written (ids), read by the ranges (8 B)
+# more written (ids; the tile ranges are marked by that pass)
 BIN_ROW = 16
 BIN_VISIBLE = 16 + 24 + 4 * 16 + 16
-BIN_ISECT = 8 + 8 + 4 + 8
+BIN_ISECT = 8 + 8 + 4
 
 FP32_LANES_PER_SM = 128
 

@@ -22,7 +22,7 @@
 //      threads), with the digit histograms of the tile passes;
 //   4. the same radix passes on the tile index (ceil(tile bits / 8) passes);
 //      the last one writes the final (tile << 32 | depth) keys and ids;
-//   5. tile range extraction.
+//   5. tile ranges, marked by the last tile pass.
 // The result is the stable sort of (tile << 32 | depth) keys emitted in row
 // order, bit for bit.
 //
@@ -340,7 +340,12 @@ __global__ void __launch_bounds__(kRadix) hist_scan_kernel(const uint32_t* __res
 //    (onesweep).  Sort status word: value << 8 | tag << 2 | flag, tag =
 //    pass + 1 (stale entries of an earlier pass read as not ready).  kFinal:
 //    the last tile pass, which writes key (tile << 32 | depth bits) and id
-//    (row mod n) of the element's row c (its low 32 bits) instead.
+//    (row mod n) of the element's row c (its low 32 bits) instead, and marks
+//    the tile ranges: a partition's keys, placed in shared memory, are in
+//    full tile order (its input is ordered by the lower tile digits), so each
+//    run of one tile in it is contiguous in the output; its ends go into
+//    ranges by atomic maxima (the start as count - position), decoded by
+//    ranges_fix_kernel.
 struct SortSmem64 {
   uint32_t warp_hist[kSortWarps][kRadix];
   uint32_t local_start[kRadix];
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
     int64_t count, int32_t pass, int32_t shift, const uint64_t* __restrict__ keys_in,
     uint64_t* __restrict__ keys_out, const uint32_t* __restrict__ digit_start,
     uint64_t* __restrict__ status, WsHeader* __restrict__ hdr, const uint64_t* __restrict__ row_u,
-    uint32_t* __restrict__ vals_out, uint32_t n) {
+    uint32_t* __restrict__ vals_out, uint32_t n, unsigned long long* __restrict__ ranges) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SortSmem64& S = *reinterpret_cast<SortSmem64*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -497,6 +502,11 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
         const uint64_t u = __ldg(row_u + (uint32_t)k);
         keys_out[gpos] = (k & 0xFFFFFFFF00000000ull) | (u >> 32);
         vals_out[gpos] = (uint32_t)u % n;
+        const uint32_t f = (uint32_t)(k >> 32);
+        if (j == 0 || (uint32_t)(S.keys[j - 1] >> 32) != f)
+          atomicMax(&ranges[2 * (uint64_t)f], (unsigned long long)count - gpos);
+        if (j == n_here - 1 || (uint32_t)(S.keys[j + 1] >> 32) != f)
+          atomicMax(&ranges[2 * (uint64_t)f + 1], gpos + 1ull);
       } else {
         keys_out[gpos] = k;
       }
@@ -603,24 +613,24 @@ __global__ void __launch_bounds__(kEmitThreads) emit_sorted_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// 5. [first, last + 1) of each (view, tile) in the sorted keys.
-__global__ void __launch_bounds__(256) ranges_kernel(int64_t count, uint64_t n_flat,
-                                                     const uint64_t* __restrict__ keys,
-                                                     int64_t* __restrict__ ranges,
-                                                     const WsHeader* __restrict__ hdr) {
-  if (count < 0) {  // asynchronous path: the scan's total, nothing on overflow
+// 5. Tile ranges [first, last + 1): the last tile pass leaves count - first
+//    (0 for an empty tile) in ranges[2 f]; decoded here.  count < 0: the
+//    intersection total from the header (nothing after an overflow).
+__global__ void __launch_bounds__(256) ranges_fix_kernel(int64_t count, int64_t n_flat,
+                                                         int64_t* __restrict__ ranges,
+                                                         const WsHeader* __restrict__ hdr) {
+  if (count < 0) {
     __shared__ int64_t s_count;
     if (threadIdx.x == 0) s_count = (hdr->error & kErrStop) ? -1 : (int64_t)hdr->total;
     __syncthreads();
     count = s_count;
     if (count < 0) return;
   }
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= count) return;
-  const uint64_t f = keys[i] >> 32;
-  if (f >= n_flat) return;
-  if (i == 0 || (keys[i - 1] >> 32) != f) ranges[2 * f] = i;
-  if (i == count - 1 || (keys[i + 1] >> 32) != f) ranges[2 * f + 1] = i + 1;
+  for (int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; f < n_flat;
+       f += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = ranges[2 * f];
+    if (e > 0) ranges[2 * f] = count - e;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1005,7 +1015,8 @@ gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, 
   uint64_t* out = rb;
   for (int p = 0; p < kDepthPasses; ++p) {
     onesweep64_kernel<false><<<(unsigned)parts_r, kSortThreads, smem, st>>>(
-        rows, p, 32 + 8 * p, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u);
+        rows, p, 32 + 8 * p, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u,
+        nullptr);
     GS_CHECK_LAUNCH();
     uint64_t* t = in; in = out; out = t;
   }
@@ -1024,17 +1035,18 @@ gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, 
     if (q == s.tile_passes - 1) {
       onesweep64_kernel<true><<<(unsigned)parts_i, kSortThreads, smem, st>>>(
           isect, p, 32 + 8 * q, in, keys, b.digit_start, b.sort_status, b.hdr, b.row_u, vals,
-          (uint32_t)s.n);
+          (uint32_t)s.n, reinterpret_cast<unsigned long long*>(ranges));
     } else {
       out = in == keys ? b.tmp : keys;
       onesweep64_kernel<false><<<(unsigned)parts_i, kSortThreads, smem, st>>>(
-          isect, p, 32 + 8 * q, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u);
+          isect, p, 32 + 8 * q, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u,
+          nullptr);
       in = out;
     }
     GS_CHECK_LAUNCH();
   }
-  ranges_kernel<<<(unsigned)div_up(isect_max, 256), 256, 0, st>>>(isect, (uint64_t)s.n_flat, keys,
-                                                                 ranges, b.hdr);
+  const int64_t fix_blocks = div_up(s.n_flat, 256) < 1024 ? div_up(s.n_flat, 256) : 1024;
+  ranges_fix_kernel<<<(unsigned)fix_blocks, 256, 0, st>>>(isect, s.n_flat, ranges, b.hdr);
   GS_CHECK_LAUNCH();
   return GS_OK;
 }

@@ -186,7 +186,7 @@ __device__ __forceinline__ void view_geom(const Gauss& G, const CamK& C, ViewGeo
   V.ok = V.det > 0.0f;
 }
 
-__global__ void __launch_bounds__(128, 4) project_fwd_kernel(int64_t n, const float* __restrict__ params,
+__global__ void __launch_bounds__(128, 5) project_fwd_kernel(int64_t n, const float* __restrict__ params,
                                                           const __grid_constant__ CamSet cs,
                                                           float4* __restrict__ out) {
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(128, 4) project_fwd_kernel(int64_t n, const fl
   }
 }
 
-__global__ void __launch_bounds__(128, 4) project_bwd_kernel(int64_t n, const float* __restrict__ params,
+__global__ void __launch_bounds__(128, 5) project_bwd_kernel(int64_t n, const float* __restrict__ params,
                                                           const __grid_constant__ CamSet cs,
                                                           const float4* __restrict__ splats,
                                                           const float4* __restrict__ grads,
@@ -255,9 +255,10 @@ __global__ void __launch_bounds__(128, 4) project_bwd_kernel(int64_t n, const fl
   load_gauss(params + g, n, G);
   float g_mu[3] = {0.f, 0.f, 0.f}, g_ls[3] = {0.f, 0.f, 0.f}, g_q[4] = {0.f, 0.f, 0.f, 0.f};
   float g_logit = 0.f;
-  float g_sh[48];
+  __shared__ float s_gsh[48][128];  // this thread's SH gradient sums in column threadIdx.x
+  float* g_sh_col = &s_gsh[0][threadIdx.x];
 #pragma unroll
-  for (int k = 0; k < 48; ++k) g_sh[k] = 0.f;
+  for (int k = 0; k < 48; ++k) g_sh_col[128 * k] = 0.f;
   bool any = false;
   for (int v = 0; v < cs.n_views; ++v) {
     const int64_t row = (int64_t)v * n + g;
@@ -288,9 +289,9 @@ __global__ void __launch_bounds__(128, 4) project_bwd_kernel(int64_t n, const fl
       float e[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        g_sh[3 * k] += Y[k] * gc0;
-        g_sh[3 * k + 1] += Y[k] * gc1;
-        g_sh[3 * k + 2] += Y[k] * gc2;
+        g_sh_col[128 * (3 * k)] += Y[k] * gc0;
+        g_sh_col[128 * (3 * k + 1)] += Y[k] * gc1;
+        g_sh_col[128 * (3 * k + 2)] += Y[k] * gc2;
         e[k] = __ldg(params + (11 + 3 * k) * n + g) * gc0 +
                __ldg(params + (12 + 3 * k) * n + g) * gc1 +
                __ldg(params + (13 + 3 * k) * n + g) * gc2;
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(128, 4) project_bwd_kernel(int64_t n, const fl
   for (int i = 0; i < 4; ++i) out[(6 + i) * n] = g_q[i];
   out[10 * n] = g_logit;
 #pragma unroll
-  for (int k = 0; k < 48; ++k) out[(11 + k) * n] = g_sh[k];
+  for (int k = 0; k < 48; ++k) out[(11 + k) * n] = g_sh_col[128 * k];
   if (visible) visible[g] = any ? 1 : 0;
 }
 

@@ -452,16 +452,37 @@ def our_arm(args, rank, world, local):
     clock_info = clocks.stop()
     ms_step = total_ms / args.steps
 
-    # end to end through the public API: pinned host target in, loss out
+    # end to end through the public API: pinned host target in, loss out.  Each
+    # step's images are copied from pinned host memory on a copy stream into
+    # one of two staging buffers while the previous step runs (as a loader
+    # would prefetch); the step waits for its buffer and moves it into place.
+    copy_stream = torch.cuda.Stream(device=dev)
+    stage = [torch.empty_like(step.target) for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
+
+    def prefetch(k):
+        with torch.cuda.stream(copy_stream):
+            if k >= 2:
+                copy_stream.wait_event(freed[k % 2])
+            stage[k % 2].copy_(target_host, non_blocking=True)
+            copied[k % 2].record(copy_stream)
+
     torch.cuda.synchronize()
     barrier(world)
     w0 = time.perf_counter()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    copy_stream.wait_event(e0)
     losses = []
-    for _ in range(args.steps):
-        step.target.copy_(target_host, non_blocking=True)
+    prefetch(0)
+    for k in range(args.steps):
+        if k + 1 < args.steps:
+            prefetch(k + 1)
+        stream.wait_event(copied[k % 2])
+        step.target.copy_(stage[k % 2], non_blocking=True)
+        freed[k % 2].record(stream)
         step.step()
         losses.append(step.loss.item())
     e1.record(stream)

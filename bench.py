@@ -180,17 +180,17 @@ class ClockSampler:
 # SHA-256 is given; for any other source the figure is unknown (null).
 TRAFFIC = {
     "rasterize_fused": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                        "sha256": "fbd02e457c2aae6d0c76fb24461dc7eba17ff2023b855c19e9feed5555c49950",
-                        "workload": "ring_3m_4x1080p", "bytes": 2566373888 + 479310592},
+                        "sha256": "a09d459d695f83699c9ef45332488aae5be3ea45578d70c8a611f8de56e48170",
+                        "workload": "ring_3m_4x1080p", "bytes": 4252276992 + 514686720},
     "rasterize_fwd": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                      "sha256": "fbd02e457c2aae6d0c76fb24461dc7eba17ff2023b855c19e9feed5555c49950",
-                      "workload": "ring_3m_4x1080p", "bytes": 1352046848 + 166041856},
+                      "sha256": "a09d459d695f83699c9ef45332488aae5be3ea45578d70c8a611f8de56e48170",
+                      "workload": "ring_3m_4x1080p", "bytes": 2190571264 + 113743104},
     "rasterize_bwd": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                      "sha256": "fbd02e457c2aae6d0c76fb24461dc7eba17ff2023b855c19e9feed5555c49950",
-                      "workload": "ring_3m_4x1080p", "bytes": 1857239808 + 272678912},
+                      "sha256": "a09d459d695f83699c9ef45332488aae5be3ea45578d70c8a611f8de56e48170",
+                      "workload": "ring_3m_4x1080p", "bytes": 2994287872 + 393855744},
     "loss_l1": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu",
                 "sha256": "a737822b52d763475a3797fc86ee95258fe3ade8ce3305e0441f56f06db4dba1",
-                "workload": "ring_3m_4x1080p", "bytes": 199083776 + 38516736},
+                "workload": "ring_3m_4x1080p", "bytes": 199088128 + 38461696},
 }
 
 
@@ -339,8 +339,8 @@ def our_arm(args, rank, world, local):
     stream = torch.cuda.current_stream()
     tile_passes = (gs.gs_key_bits(V, W, H) - 32 + 7) // 8
     # project; binning: compaction, capacity check, 2 digit scans, 4 depth passes, emission,
-    # tile passes, ranges; (fused | fwd, loss, bwd); project_bwd; adam
-    kernels_per_step = (14 if fused else 16) + tile_passes
+    # tile passes, ranges; tile order; (fused | fwd, loss, bwd); project_bwd; adam
+    kernels_per_step = (15 if fused else 17) + tile_passes
 
     prune_info = None
     if args.prune is not None:

@@ -60,22 +60,24 @@ def lib():
     L.gs_bin_and_sort_async.argtypes = [i64, i32, vp, i32, i32, vp, sz, i64, vp, vp, vp, vp, vp]
     L.gs_adam_step_dev.argtypes = [i64, vp, vp, vp, vp, vp, f32, f32, f32, f32, vp, vp, vp]
     L.gs_step_advance.argtypes = [vp, vp, vp]
-    L.gs_rasterize_fwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
-    L.gs_rasterize_fwd_counted.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.gs_tile_order.argtypes = [i64, vp, vp, vp]
+    L.gs_rasterize_fwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.gs_rasterize_fwd_counted.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                           vp]
     L.gs_loss_l1.argtypes = [vp, vp, i64, vp, vp, vp]
-    L.gs_rasterize_bwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.gs_rasterize_bwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.gs_morton_workspace_bytes.argtypes = [i64]
     L.gs_morton_workspace_bytes.restype = sz
     L.gs_morton_order.argtypes = [i64, vp, vp, sz, vp, vp]
     L.gs_gather_columns.argtypes = [i64, i64, i64, vp, vp, vp, vp]
     L.gs_rasterize_fwd_importance.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp,
-                                              vp]
+                                              vp, vp]
     L.gs_prune_mask.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, i64, f32, vp, vp]
     L.gs_compact_workspace_bytes.argtypes = [i64]
     L.gs_compact_workspace_bytes.restype = sz
     L.gs_compact_index.argtypes = [i64, vp, vp, sz, vp, vp, vp]
     L.gs_rasterize_fused.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                     vp]
+                                     vp, vp]
     L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp]
     L.gs_adam_step.argtypes = [i64, vp, vp, vp, vp, i64, f32, f32, f32, f32, vp, vp]
     L.gs_status_string.argtypes = [C.c_int]
@@ -205,22 +207,33 @@ def gs_step_advance(step, bin_workspace=None, stream=None):
         _stream(stream)))
 
 
+def gs_tile_order(ranges, order, stream=None):
+    """order[b] = the tile the b-th compositing CTA takes: longest lists first."""
+    n_flat = ranges.shape[0]
+    if order.numel() < n_flat:
+        raise ValueError("gs_tile_order: order shorter than ranges")
+    _check("gs_tile_order", lib().gs_tile_order(n_flat, _dev(ranges, torch.int64, "ranges"),
+                                                _dev(order, torch.int32, "order"), _stream(stream)))
+
+
 def gs_rasterize_fwd(n, n_views, splats, width, height, vals, ranges, bg, image, T_final, n_contrib,
-                     stream=None):
+                     stream=None, tile_order=None):
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
     _check("gs_rasterize_fwd", lib().gs_rasterize_fwd(
         n, n_views, _dev(splats, torch.float32, "splats"), width, height,
-        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"),
+        _dev(tile_order, torch.int32, "tile_order"), C.cast(bgv, C.c_void_p),
         _dev(image, torch.float32, "image"), _dev(T_final, torch.float32, "T_final"),
         _dev(n_contrib, torch.int32, "n_contrib"), _stream(stream)))
 
 
 def gs_rasterize_fwd_counted(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
-                             n_contrib, counts, stream=None):
+                             n_contrib, counts, stream=None, tile_order=None):
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
     _check("gs_rasterize_fwd_counted", lib().gs_rasterize_fwd_counted(
         n, n_views, _dev(splats, torch.float32, "splats"), width, height,
-        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"),
+        _dev(tile_order, torch.int32, "tile_order"), C.cast(bgv, C.c_void_p),
         _dev(image, torch.float32, "image"), _dev(T_final, torch.float32, "T_final"),
         _dev(n_contrib, torch.int32, "n_contrib"), _dev(counts, torch.int64, "counts"),
         _stream(stream)))
@@ -235,22 +248,24 @@ def gs_loss_l1(image, target, loss, dL_dimage, stream=None):
 
 
 def gs_rasterize_bwd(n, n_views, splats, width, height, vals, ranges, bg, T_final, n_contrib,
-                     dL_dimage, grads, stream=None):
+                     dL_dimage, grads, stream=None, tile_order=None):
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
     _check("gs_rasterize_bwd", lib().gs_rasterize_bwd(
         n, n_views, _dev(splats, torch.float32, "splats"), width, height,
-        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"),
+        _dev(tile_order, torch.int32, "tile_order"), C.cast(bgv, C.c_void_p),
         _dev(T_final, torch.float32, "T_final"), _dev(n_contrib, torch.int32, "n_contrib"),
         _dev(dL_dimage, torch.float32, "dL_dimage"), _dev(grads, torch.float32, "grads"),
         _stream(stream)))
 
 
 def gs_rasterize_fused(n, n_views, splats, width, height, vals, ranges, bg, target, image,
-                       T_final, n_contrib, loss, grads, stream=None):
+                       T_final, n_contrib, loss, grads, stream=None, tile_order=None):
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
     _check("gs_rasterize_fused", lib().gs_rasterize_fused(
         n, n_views, _dev(splats, torch.float32, "splats"), width, height,
-        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"),
+        _dev(tile_order, torch.int32, "tile_order"), C.cast(bgv, C.c_void_p),
         _dev(target, torch.float32, "target"), _dev(image, torch.float32, "image"),
         _dev(T_final, torch.float32, "T_final"), _dev(n_contrib, torch.int32, "n_contrib"),
         _dev(loss, torch.float32, "loss"), _dev(grads, torch.float32, "grads"), _stream(stream)))
@@ -279,11 +294,12 @@ def gs_gather_columns(src, idx, dst, stream=None):
 
 
 def gs_rasterize_fwd_importance(n, n_views, splats, width, height, vals, ranges, bg, image,
-                                T_final, n_contrib, importance, stream=None):
+                                T_final, n_contrib, importance, stream=None, tile_order=None):
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
     _check("gs_rasterize_fwd_importance", lib().gs_rasterize_fwd_importance(
         n, n_views, _dev(splats, torch.float32, "splats"), width, height,
-        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"), C.cast(bgv, C.c_void_p),
+        _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"),
+        _dev(tile_order, torch.int32, "tile_order"), C.cast(bgv, C.c_void_p),
         _dev(image, torch.float32, "image"), _dev(T_final, torch.float32, "T_final"),
         _dev(n_contrib, torch.int32, "n_contrib"), _dev(importance, torch.float32, "importance"),
         _stream(stream)))
@@ -374,6 +390,7 @@ class TrainStep:
         self.n_contrib = torch.empty((self.V, self.H, self.W), device=dev, dtype=torch.int32)
         self.loss = torch.zeros(1, **f32)
         self.ranges = torch.empty((self.V * self.T, 2), device=dev, dtype=torch.int64)
+        self.tile_order = torch.empty(self.V * self.T, device=dev, dtype=torch.int32)
         self.t = 0
         self.n_isect = 0
         # a first guess, bounded so that very large scenes do not reserve sort
@@ -401,27 +418,30 @@ class TrainStep:
                                     self.capacity, self.keys, self.vals, self.ranges, stream)
             _check("gs_bin_and_sort", st)
         self.n_isect = I
+        gs_tile_order(self.ranges, self.tile_order, stream)
 
     def rasterize_fwd(self, stream=None, counts=None):
         if counts is None:
             gs_rasterize_fwd(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges,
-                             self.bg, self.image, self.T_final, self.n_contrib, stream)
+                             self.bg, self.image, self.T_final, self.n_contrib, stream,
+                             tile_order=self.tile_order)
         else:
             gs_rasterize_fwd_counted(self.n, self.V, self.splats, self.W, self.H, self.vals,
                                      self.ranges, self.bg, self.image, self.T_final, self.n_contrib,
-                                     counts, stream)
+                                     counts, stream, tile_order=self.tile_order)
 
     def loss_l1(self, stream=None):
         gs_loss_l1(self.image, self.target, self.loss, self.dL_dimage, stream)
 
     def rasterize_bwd(self, stream=None):
         gs_rasterize_bwd(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges, self.bg,
-                         self.T_final, self.n_contrib, self.dL_dimage, self.grads2d, stream)
+                         self.T_final, self.n_contrib, self.dL_dimage, self.grads2d, stream,
+                         tile_order=self.tile_order)
 
     def rasterize_fused(self, stream=None):
         gs_rasterize_fused(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges,
                            self.bg, self.target, self.image, self.T_final, self.n_contrib,
-                           self.loss, self.grads2d, stream)
+                           self.loss, self.grads2d, stream, tile_order=self.tile_order)
 
     def project_bwd(self, stream=None):
         gs_project_bwd(self.params, self.cams, self.splats, self.grads2d, self.grad, self.visible,
@@ -472,7 +492,7 @@ class TrainStep:
         imp = torch.empty(self.V * self.n, device=dev, dtype=torch.float32)
         gs_rasterize_fwd_importance(self.n, self.V, self.splats, self.W, self.H, self.vals,
                                     self.ranges, self.bg, self.image, self.T_final,
-                                    self.n_contrib, imp, stream)
+                                    self.n_contrib, imp, stream, tile_order=self.tile_order)
         mask = torch.empty(self.n, device=dev, dtype=torch.uint8)
         gs_prune_mask(self.n, self.V, self.W, self.H, self.vals, self.ranges, self.n_contrib, imp,
                       capacity, tau, mask, stream)
@@ -514,6 +534,7 @@ class TrainStep:
         self.project()
         gs_bin_and_sort_async(self.n, self.V, self.splats, self.W, self.H, self.workspace,
                               self.capacity, self.keys, self.vals, self.ranges, self.n_isect_dev)
+        gs_tile_order(self.ranges, self.tile_order)
         if self.fused:
             self.rasterize_fused()
         else:

@@ -24,7 +24,9 @@
 //    per-pair loop runs on full warps and finished warps stop issuing;
 //  - backward: a pair's gradient is reduced across the warp by recursive
 //    halving (8 values in 9 shuffles) and added to shared memory by one
-//    atomic per value.
+//    atomic per value;
+//  - launch order: CTA b composites tile tile_order[b] when given
+//    (gs_tile_order: longest lists first), which shortens the kernel's tail.
 #include <stdint.h>
 
 #include "gs_internal.cuh"
@@ -551,14 +553,14 @@ struct FwdSmem {
 template <bool kCount, bool kImp>
 __global__ void __launch_bounds__(kRT, 6) raster_fwd_kernel(
     int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
-    const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
-    float bg2, float* __restrict__ image, float* __restrict__ T_final,
+    const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges,
+    const uint32_t* __restrict__ tile_order, float bg0, float bg1, float bg2, float* __restrict__ image, float* __restrict__ T_final,
     int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ counts,
     float* __restrict__ imp) {
   __shared__ FwdSmem<kImp> S;
   unsigned long long n_tested = 0, n_included = 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t flat = blockIdx.x;
+  const int64_t flat = tile_order ? (int64_t)tile_order[blockIdx.x] : (int64_t)blockIdx.x;
   const int64_t view = flat / T;
   const int32_t tile = (int32_t)(flat - view * T);
   const int tile_x = tile % tiles_x, tile_y = tile / tiles_x;
@@ -608,12 +610,12 @@ struct BwdSmem {
 
 __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
     int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
-    const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
-    float bg2, const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
+    const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges,
+    const uint32_t* __restrict__ tile_order, float bg0, float bg1, float bg2, const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
     const float* __restrict__ dL_dimage, float4* __restrict__ grads) {
   __shared__ BwdSmem S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t flat = blockIdx.x;
+  const int64_t flat = tile_order ? (int64_t)tile_order[blockIdx.x] : (int64_t)blockIdx.x;
   const int64_t view = flat / T;
   const int32_t tile = (int32_t)(flat - view * T);
   const int tile_x = tile % tiles_x, tile_y = tile / tiles_x;
@@ -715,14 +717,14 @@ struct FusedSmem {
 
 __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
     int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
-    const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges, float bg0, float bg1,
-    float bg2, const float* __restrict__ target, float inv_count, float* __restrict__ image,
+    const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges,
+    const uint32_t* __restrict__ tile_order, float bg0, float bg1, float bg2, const float* __restrict__ target, float inv_count, float* __restrict__ image,
     float* __restrict__ T_final, int32_t* __restrict__ n_contrib, float* __restrict__ loss,
     float4* __restrict__ grads) {
   __shared__ FusedSmem S;
   unsigned long long n_tested = 0, n_included = 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t flat = blockIdx.x;
+  const int64_t flat = tile_order ? (int64_t)tile_order[blockIdx.x] : (int64_t)blockIdx.x;
   const int64_t view = flat / T;
   const int32_t tile = (int32_t)(flat - view * T);
   const int tile_x = tile % tiles_x, tile_y = tile / tiles_x;
@@ -834,14 +836,85 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
   cp_async_wait<0>();
 }
 
+// Launch order of the compositing CTAs: a tile's cost grows with its list
+// length, which spans four orders of magnitude in clustered scenes, and CTAs
+// start roughly in grid order, so a long list that starts late leaves the
+// other SMs idle at the end of the kernel.  Longest lists first (the
+// longest-processing-time-first rule of list scheduling) starts them while
+// the short ones fill the gaps: order = tiles by descending
+// floor(log2(list length)), empty tiles last, ties in tile order.  One CTA.
+constexpr int kOrdThreads = 1024;
+constexpr int kOrdWarps = kOrdThreads / 32;
+constexpr int kOrdBuckets = 34;  // 0: empty; 1 + floor(log2 len) <= 33 (len < 2^33)
+
+__device__ __forceinline__ uint32_t order_bucket(const int64_t* ranges, int64_t f) {
+  const int64_t len = ranges[2 * f + 1] - ranges[2 * f];
+  return len > 0 ? (uint32_t)min(64 - __clzll((unsigned long long)len), kOrdBuckets - 1) : 0u;
+}
+
+__global__ void __launch_bounds__(kOrdThreads) tile_order_kernel(int64_t n_flat,
+                                                                 const int64_t* __restrict__ ranges,
+                                                                 uint32_t* __restrict__ order) {
+  __shared__ uint32_t s_start[kOrdBuckets];
+  __shared__ uint32_t s_wcount[kOrdWarps][kOrdBuckets];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < kOrdBuckets) s_start[tid] = 0;
+  __syncthreads();
+  for (int64_t f = tid; f < n_flat; f += kOrdThreads) atomicAdd(&s_start[order_bucket(ranges, f)], 1u);
+  __syncthreads();
+  if (tid == 0) {  // exclusive starts, longest bucket first, empty tiles last
+    uint32_t run = 0;
+    for (int b = kOrdBuckets - 1; b >= 0; --b) {
+      const uint32_t c = s_start[b];
+      s_start[b] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int64_t base = 0; base < n_flat; base += kOrdThreads) {
+    const int64_t f = base + tid;
+    const bool valid = f < n_flat;
+    const uint32_t b = valid ? order_bucket(ranges, f) : (uint32_t)kOrdBuckets;
+    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    if (lane < kOrdBuckets) s_wcount[warp][lane] = 0;
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) s_wcount[warp][b] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      uint32_t pos = s_start[b] + __popc(peers & lt);
+      for (int w = 0; w < warp; ++w) pos += s_wcount[w][b];
+      order[pos] = (uint32_t)f;
+    }
+    __syncthreads();
+    if (tid < kOrdBuckets) {
+      uint32_t c = 0;
+      for (int w = 0; w < kOrdWarps; ++w) c += s_wcount[w][tid];
+      s_start[tid] += c;
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 }  // namespace gs
 
 using namespace gs;
 
+extern "C" gs_status gs_tile_order(int64_t n_flat, const int64_t* ranges, uint32_t* order,
+                                   void* stream) {
+  if (n_flat < 0 || n_flat > (int64_t)0xFFFFFFFFll || (n_flat > 0 && (!ranges || !order)))
+    return GS_ERR_INVALID_ARG;
+  if (n_flat == 0) return GS_OK;
+  tile_order_kernel<<<1, kOrdThreads, 0, (cudaStream_t)stream>>>(n_flat, ranges, order);
+  GS_CHECK_LAUNCH();
+  return GS_OK;
+}
+
 static gs_status rasterize_fwd_impl(int64_t n, int32_t n_views, const gs_splat* splats,
                                     int32_t width, int32_t height, const uint32_t* vals,
-                                    const int64_t* ranges, const float* bg, float* image,
+                                    const int64_t* ranges, const uint32_t* tile_order,
+                                    const float* bg, float* image,
                                     float* T_final, int32_t* n_contrib, uint64_t* counts,
                                     float* importance, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
@@ -857,15 +930,15 @@ static gs_status rasterize_fwd_impl(int64_t n, int32_t n_views, const gs_splat* 
   if (importance) {
     if (n > 0) GS_CUDA(cudaMemsetAsync(importance, 0, sizeof(float) * (size_t)(n * n_views), st));
     raster_fwd_kernel<false, true><<<grid, kRT, 0, st>>>(n, tiles_x, T, width, height, sp, vals,
-                                                         ranges, bg[0], bg[1], bg[2], image,
+                                                         ranges, tile_order, bg[0], bg[1], bg[2], image,
                                                          T_final, n_contrib, c, importance);
   } else if (counts) {
     raster_fwd_kernel<true, false><<<grid, kRT, 0, st>>>(n, tiles_x, T, width, height, sp, vals,
-                                                         ranges, bg[0], bg[1], bg[2], image,
+                                                         ranges, tile_order, bg[0], bg[1], bg[2], image,
                                                          T_final, n_contrib, c, nullptr);
   } else {
     raster_fwd_kernel<false, false><<<grid, kRT, 0, st>>>(n, tiles_x, T, width, height, sp, vals,
-                                                          ranges, bg[0], bg[1], bg[2], image,
+                                                          ranges, tile_order, bg[0], bg[1], bg[2], image,
                                                           T_final, n_contrib, c, nullptr);
   }
   GS_CHECK_LAUNCH();
@@ -874,36 +947,38 @@ static gs_status rasterize_fwd_impl(int64_t n, int32_t n_views, const gs_splat* 
 
 extern "C" gs_status gs_rasterize_fwd(int64_t n, int32_t n_views, const gs_splat* splats,
                                       int32_t width, int32_t height, const uint32_t* vals,
-                                      const int64_t* ranges, const float* bg, float* image,
-                                      float* T_final, int32_t* n_contrib, void* stream) {
-  return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
-                            n_contrib, nullptr, nullptr, stream);
+                                      const int64_t* ranges, const uint32_t* tile_order,
+                                      const float* bg, float* image, float* T_final,
+                                      int32_t* n_contrib, void* stream) {
+  return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, tile_order, bg, image,
+                            T_final, n_contrib, nullptr, nullptr, stream);
 }
 
 extern "C" gs_status gs_rasterize_fwd_counted(int64_t n, int32_t n_views, const gs_splat* splats,
                                               int32_t width, int32_t height, const uint32_t* vals,
-                                              const int64_t* ranges, const float* bg, float* image,
-                                              float* T_final, int32_t* n_contrib, uint64_t* counts,
-                                              void* stream) {
+                                              const int64_t* ranges, const uint32_t* tile_order,
+                                              const float* bg, float* image, float* T_final,
+                                              int32_t* n_contrib, uint64_t* counts, void* stream) {
   if (!counts) return GS_ERR_INVALID_ARG;
-  return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
-                            n_contrib, counts, nullptr, stream);
+  return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, tile_order, bg, image,
+                            T_final, n_contrib, counts, nullptr, stream);
 }
 
 extern "C" gs_status gs_rasterize_fwd_importance(int64_t n, int32_t n_views, const gs_splat* splats,
                                                  int32_t width, int32_t height,
                                                  const uint32_t* vals, const int64_t* ranges,
-                                                 const float* bg, float* image, float* T_final,
-                                                 int32_t* n_contrib, float* importance,
-                                                 void* stream) {
+                                                 const uint32_t* tile_order, const float* bg,
+                                                 float* image, float* T_final, int32_t* n_contrib,
+                                                 float* importance, void* stream) {
   if (!importance && n > 0) return GS_ERR_INVALID_ARG;
-  return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
-                            n_contrib, nullptr, importance, stream);
+  return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, tile_order, bg, image,
+                            T_final, n_contrib, nullptr, importance, stream);
 }
 
 extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
                                         int32_t width, int32_t height, const uint32_t* vals,
-                                        const int64_t* ranges, const float* bg,
+                                        const int64_t* ranges, const uint32_t* tile_order,
+                                        const float* bg,
                                         const float* target, float* image, float* T_final,
                                         int32_t* n_contrib, float* loss, gs_splat_grad* grads,
                                         void* stream) {
@@ -919,8 +994,8 @@ extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_spl
   const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE;
   const double count = 3.0 * (double)n_views * (double)width * (double)height;
   raster_fused_kernel<<<(unsigned)(n_views * T), kRT, 0, st>>>(
-      n, tiles_x, T, width, height, reinterpret_cast<const float4*>(splats), vals, ranges, bg[0],
-      bg[1], bg[2], target, (float)(1.0 / count), image, T_final, n_contrib, loss,
+      n, tiles_x, T, width, height, reinterpret_cast<const float4*>(splats), vals, ranges,
+      tile_order, bg[0], bg[1], bg[2], target, (float)(1.0 / count), image, T_final, n_contrib, loss,
       reinterpret_cast<float4*>(grads));
   GS_CHECK_LAUNCH();
   return GS_OK;
@@ -928,7 +1003,8 @@ extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_spl
 
 extern "C" gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats,
                                       int32_t width, int32_t height, const uint32_t* vals,
-                                      const int64_t* ranges, const float* bg, const float* T_final,
+                                      const int64_t* ranges, const uint32_t* tile_order,
+                                      const float* bg, const float* T_final,
                                       const int32_t* n_contrib, const float* dL_dimage,
                                       gs_splat_grad* grads, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
@@ -941,8 +1017,8 @@ extern "C" gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat
   const int64_t T = tiles_per_view(width, height);
   const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE;
   raster_bwd_kernel<<<(unsigned)(n_views * T), kRT, 0, st>>>(
-      n, tiles_x, T, width, height, reinterpret_cast<const float4*>(splats), vals, ranges, bg[0],
-      bg[1], bg[2], T_final, n_contrib, dL_dimage, reinterpret_cast<float4*>(grads));
+      n, tiles_x, T, width, height, reinterpret_cast<const float4*>(splats), vals, ranges,
+      tile_order, bg[0], bg[1], bg[2], T_final, n_contrib, dL_dimage, reinterpret_cast<float4*>(grads));
   GS_CHECK_LAUNCH();
   return GS_OK;
 }

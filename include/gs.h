@@ -220,6 +220,16 @@ gs_status gs_bin_and_sort_static(int64_t n, int32_t n_views, const gs_splat* spl
                                  int64_t* n_isect, void* stream);
 
 /* ---------------------------------------------------------------------- */
+/* gs_tile_order -- the launch order for the compositing calls: the tiles
+ * (view * T + tile) by descending floor(log2(list length)), empty tiles
+ * last, ties in tile order (longest lists first: a tile's cost grows with
+ * its list, and a long list started late leaves the other SMs idle at the
+ * end).  Any permutation gives the same images; the gradients differ only by
+ * the order of float atomics.
+ *   ranges  [n_flat][2] from gs_bin_and_sort
+ *   order   [n_flat] uint32 output (device) */
+gs_status gs_tile_order(int64_t n_flat, const int64_t* ranges, uint32_t* order, void* stream);
+
 /* gs_rasterize_fwd -- per-tile front-to-back alpha compositing [S3] over
  * the sorted lists.  Per pixel (centre (u+0.5, v+0.5)), for each pair of its
  * tile's list in order: power = -(a dx^2 + c dy^2)/2 - b dx dy,
@@ -227,6 +237,9 @@ gs_status gs_bin_and_sort_static(int64_t n, int32_t n_views, const gs_splat* spl
  * the pair that would take transmittance below 1e-4 stops the pixel and is
  * excluded [S1 opacity saturation]; C = sum c alpha T + T_final bg.
  *   vals, ranges  from gs_bin_and_sort
+ *   tile_order    [n_views * T] from gs_tile_order (the order in which the
+ *                 tiles' CTAs start), or NULL for tile order; the same
+ *                 argument in every gs_rasterize_* call
  *   bg            (host) background colour [3]
  *   image         [n_views][3][H][W]
  *   T_final       [n_views][H][W] final transmittance
@@ -234,8 +247,8 @@ gs_status gs_bin_and_sort_static(int64_t n, int32_t n_views, const gs_splat* spl
  *                 pair (0 = none) */
 gs_status gs_rasterize_fwd(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
                            int32_t height, const uint32_t* vals, const int64_t* ranges,
-                           const float* bg, float* image, float* T_final, int32_t* n_contrib,
-                           void* stream);
+                           const uint32_t* tile_order, const float* bg, float* image,
+                           float* T_final, int32_t* n_contrib, void* stream);
 
 /* gs_rasterize_fwd_counted -- gs_rasterize_fwd with the same outputs that
  * also adds to counts[0] the pairs tested (list entries visited before each
@@ -244,9 +257,9 @@ gs_status gs_rasterize_fwd(int64_t n, int32_t n_views, const gs_splat* splats, i
  *   counts  device uint64[2], accumulated (zero it first) */
 gs_status gs_rasterize_fwd_counted(int64_t n, int32_t n_views, const gs_splat* splats,
                                    int32_t width, int32_t height, const uint32_t* vals,
-                                   const int64_t* ranges, const float* bg, float* image,
-                                   float* T_final, int32_t* n_contrib, uint64_t* counts,
-                                   void* stream);
+                                   const int64_t* ranges, const uint32_t* tile_order,
+                                   const float* bg, float* image, float* T_final,
+                                   int32_t* n_contrib, uint64_t* counts, void* stream);
 
 /* gs_loss_l1 -- L = mean |image - target| over `count` values and
  * dL/dimage = sign(image - target) / count (sign(0) = 0).  Helper beyond the
@@ -263,8 +276,9 @@ gs_status gs_loss_l1(const float* image, const float* target, int64_t count, flo
  *   grads  [n_views * n] output, zeroed by this call, then accumulated. */
 gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
                            int32_t height, const uint32_t* vals, const int64_t* ranges,
-                           const float* bg, const float* T_final, const int32_t* n_contrib,
-                           const float* dL_dimage, gs_splat_grad* grads, void* stream);
+                           const uint32_t* tile_order, const float* bg, const float* T_final,
+                           const int32_t* n_contrib, const float* dL_dimage,
+                           gs_splat_grad* grads, void* stream);
 
 /* gs_rasterize_fused -- gs_rasterize_fwd, gs_loss_l1 and gs_rasterize_bwd
  * in one launch, one CTA per tile ([S3] abstract: forward and backward
@@ -284,9 +298,9 @@ gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats, i
  *              (n_views*3*H*W) */
 gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
                              int32_t height, const uint32_t* vals, const int64_t* ranges,
-                             const float* bg, const float* target, float* image, float* T_final,
-                             int32_t* n_contrib, float* loss, gs_splat_grad* grads,
-                             void* stream);
+                             const uint32_t* tile_order, const float* bg, const float* target,
+                             float* image, float* T_final, int32_t* n_contrib, float* loss,
+                             gs_splat_grad* grads, void* stream);
 
 /* gs_project_bwd -- chain rule from the per-row gradients back to the 59
  * parameters, summed over the views (the 1/n_views average of [S1] comes
@@ -369,9 +383,9 @@ gs_status gs_gather_columns(int64_t rows, int64_t n_src, int64_t n_dst, const fl
  *   importance  [n_views * n] fp32 output (zeroed by this call). */
 gs_status gs_rasterize_fwd_importance(int64_t n, int32_t n_views, const gs_splat* splats,
                                       int32_t width, int32_t height, const uint32_t* vals,
-                                      const int64_t* ranges, const float* bg, float* image,
-                                      float* T_final, int32_t* n_contrib, float* importance,
-                                      void* stream);
+                                      const int64_t* ranges, const uint32_t* tile_order,
+                                      const float* bg, float* image, float* T_final,
+                                      int32_t* n_contrib, float* importance, void* stream);
 
 /* gs_prune_mask -- for every (view, tile): L = the largest n_contrib over
  * its pixels (its working set is list positions [0, L)); when L > capacity,

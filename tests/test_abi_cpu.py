@@ -83,12 +83,15 @@ def test_invalid_arguments_return_before_any_launch(gslib):
                              None) == gslib.GS_ERR_INVALID_ARG                     # 2^32 rows
     assert L.gs_bin_and_sort(1, 1, None, 16 * 65536, 16, ws, 64, 0, None, None, None,
                              C.byref(out), None) == gslib.GS_ERR_INVALID_ARG       # 65536 tiles wide
-    assert L.gs_rasterize_fwd(10, 1, None, 16, 16, None, None, None, None, None, None,
+    assert L.gs_rasterize_fwd(10, 1, None, 16, 16, None, None, None, None, None, None, None,
                               None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_rasterize_bwd(10, 17, None, 16, 16, None, None, None, None, None, None, None,
-                              None) == gslib.GS_ERR_INVALID_ARG
+                              None, None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_rasterize_fused(10, 1, None, 16, 16, None, None, None, None, None, None, None,
-                                None, None, None) == gslib.GS_ERR_INVALID_ARG
+                                None, None, None, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_tile_order(-1, None, None, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_tile_order(5, None, None, None) == gslib.GS_ERR_INVALID_ARG          # NULL
+    assert L.gs_tile_order(0, None, None, None) == gslib.GS_OK                       # empty
     assert L.gs_project_bwd(10, None, cp, 1, None, None, None, None,
                             None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_loss_l1(None, None, -1, None, None, None) == gslib.GS_ERR_INVALID_ARG

@@ -218,6 +218,43 @@ def _gpu_fwd(gs, o, rec=None):
     return splats, vals, ranges, image, T_final, n_contrib
 
 
+@pytest.mark.parametrize("case", ["ragged2", "small"])
+def test_tile_order_longest_first_same_results(case):
+    """gs_tile_order: tiles by descending floor(log2(list length)), empty
+    last, ties in tile order; compositing in that order gives the same image,
+    T_final and n_contrib bit for bit, and the same gradients up to the order
+    of float atomics."""
+    gs = _gs()
+    o = oracle_side(case)
+    n, V, W, H = o["n"], o["V"], o["W"], o["H"]
+    lens = o["ranges"][:, 1] - o["ranges"][:, 0]
+    bucket = np.array([int(x).bit_length() for x in lens])
+    expect = np.lexsort((np.arange(lens.size), -bucket))
+    ranges = _cuda(o["ranges"])
+    order = torch.full((lens.size,), -1, dtype=torch.int32, device="cuda")
+    gs.gs_tile_order(ranges, order)
+    assert np.array_equal(order.cpu().numpy(), expect)
+    splats, vals, ranges, image, T_final, n_contrib = _gpu_fwd(gs, o)
+    image2, T2, nc2 = torch.empty_like(image), torch.empty_like(T_final), torch.empty_like(n_contrib)
+    gs.gs_rasterize_fwd(n, V, splats, W, H, vals, ranges, (0, 0, 0), image2, T2, nc2,
+                        tile_order=order)
+    assert torch.equal(image2, image) and torch.equal(T2, T_final) and torch.equal(nc2, n_contrib)
+    target = torch.from_numpy(np.ascontiguousarray(o["target"], np.float32)).cuda() \
+        if "target" in o else torch.rand_like(image)
+    outs = []
+    for tile_order in (None, order):
+        img, Tf, nc = torch.empty_like(image), torch.empty_like(T_final), torch.empty_like(n_contrib)
+        loss = torch.empty(1, device="cuda")
+        grads = torch.empty((V * n, 12), device="cuda")
+        gs.gs_rasterize_fused(n, V, splats, W, H, vals, ranges, (0, 0, 0), target, img, Tf, nc,
+                              loss, grads, tile_order=tile_order)
+        outs.append((img, loss, grads))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert outs[1][1].item() == pytest.approx(outs[0][1].item(), rel=1e-5)  # float atomics
+    g0, g1 = outs[0][2].cpu().numpy(), outs[1][2].cpu().numpy()
+    assert rel_l2(g1, g0) <= 1e-5
+
+
 @pytest.mark.parametrize("case", CASES)
 def test_rasterize_fwd_matches_oracle(case):
     gs = _gs()

@@ -3,9 +3,12 @@
  * (libgs103.so, CUDA kernels for sm_103a).
  *
  * One training step on one GPU is
- *   gs_project -> gs_bin_and_sort -> gs_rasterize_fwd -> gs_loss_l1 ->
- *   gs_rasterize_bwd -> gs_project_bwd -> gs_adam_step
- * Forward-only rendering is the first three calls.
+ *   gs_project -> gs_bin_and_sort -> gs_tile_order -> gs_rasterize_fwd ->
+ *   gs_loss_l1 -> gs_rasterize_bwd -> gs_project_bwd -> gs_adam_step
+ * where gs_rasterize_fused may replace the three calls from gs_rasterize_fwd
+ * to gs_rasterize_bwd, and gs_tile_order is optional (it only sets the order
+ * in which the compositing CTAs start).  Forward-only rendering is the calls
+ * up to gs_rasterize_fwd.
  *
  * Source pages (title, section) for what the step computes:
  *  [S1] "On Scaling Up 3D Gaussian Splatting Training": answer on the storage

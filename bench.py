@@ -473,6 +473,10 @@ def our_arm(args, rank, world, local):
     w0 = time.perf_counter()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # each step's loss goes to pinned host memory behind an event and is read
+    # after the next step has been launched, so the GPU never waits for the host
+    loss_host = torch.empty((2, 1), dtype=torch.float32).pin_memory()
+    loss_ready = [torch.cuda.Event() for _ in range(2)]
     e0.record(stream)
     copy_stream.wait_event(e0)
     losses = []
@@ -484,7 +488,13 @@ def our_arm(args, rank, world, local):
         step.target.copy_(stage[k % 2], non_blocking=True)
         freed[k % 2].record(stream)
         step.step()
-        losses.append(step.loss.item())
+        loss_host[k % 2].copy_(step.loss.reshape(1), non_blocking=True)
+        loss_ready[k % 2].record(stream)
+        if k >= 1:
+            loss_ready[(k - 1) % 2].synchronize()
+            losses.append(float(loss_host[(k - 1) % 2, 0]))
+    loss_ready[(args.steps - 1) % 2].synchronize()
+    losses.append(float(loss_host[(args.steps - 1) % 2, 0]))
     e1.record(stream)
     torch.cuda.synchronize()
     if graph and step.check() != gs.GS_OK:

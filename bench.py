@@ -32,7 +32,7 @@ WORKLOAD = "ring_3m_4x1080p"
 METRIC = "train iters/s and fwd+bwd Mpix/s at 1080p/3M Gaussians; % HBM roofline"
 UNIT = "iters/s"
 
-# Algorithmic work per unit ("Work per unit").
+# Algorithmic work per unit: the flops and bytes each kernel's roofline counts.
 FWD_FLOP_TESTED = 13     # per tested pair: dx, dy, power, alpha (+1 exp)
 FWD_FLOP_INCLUDED = 9    # per composited pair: transmittance, weight, colour
 BWD_FLOP_EVAL = 13       # per pair visited below the last contributor (+1 exp)
@@ -175,9 +175,9 @@ class ClockSampler:
 
 
 # DRAM bytes (read + write) per launch of the compositing kernels, from one
-# ncu capture of this workload at full size (profiles/
-# raster_kernels_ring_3m_4x1080p.md, profiles/fused_vs_separate_ring_3m_4x1080p.md).  They describe the kernel source whose
-# SHA-256 is given; for any other source the figure is unknown (null).
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of this workload
+# at full size.  They describe the kernel source whose SHA-256 is given; for
+# any other source the figure is unknown (null).
 TRAFFIC = {
     "rasterize_fused": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
                         "sha256": "a09d459d695f83699c9ef45332488aae5be3ea45578d70c8a611f8de56e48170",

@@ -180,17 +180,17 @@ class ClockSampler:
 # any other source the figure is unknown (null).
 TRAFFIC = {
     "rasterize_fused": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                        "sha256": "a09d459d695f83699c9ef45332488aae5be3ea45578d70c8a611f8de56e48170",
-                        "workload": "ring_3m_4x1080p", "bytes": 4252276992 + 514686720},
+                        "sha256": "9122a0d2651e4341b8c7898b9aca98b861628b58b677312daf2a2a5fdbe9e5d1",
+                        "workload": "ring_3m_4x1080p", "bytes": 4249789696 + 515035904},
     "rasterize_fwd": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                      "sha256": "a09d459d695f83699c9ef45332488aae5be3ea45578d70c8a611f8de56e48170",
-                      "workload": "ring_3m_4x1080p", "bytes": 2190571264 + 113743104},
+                      "sha256": "9122a0d2651e4341b8c7898b9aca98b861628b58b677312daf2a2a5fdbe9e5d1",
+                      "workload": "ring_3m_4x1080p", "bytes": 2190107136 + 113843456},
     "rasterize_bwd": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                      "sha256": "a09d459d695f83699c9ef45332488aae5be3ea45578d70c8a611f8de56e48170",
-                      "workload": "ring_3m_4x1080p", "bytes": 2994287872 + 393855744},
+                      "sha256": "9122a0d2651e4341b8c7898b9aca98b861628b58b677312daf2a2a5fdbe9e5d1",
+                      "workload": "ring_3m_4x1080p", "bytes": 2994458624 + 393797376},
     "loss_l1": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu",
                 "sha256": "a737822b52d763475a3797fc86ee95258fe3ade8ce3305e0441f56f06db4dba1",
-                "workload": "ring_3m_4x1080p", "bytes": 199088128 + 38461696},
+                "workload": "ring_3m_4x1080p", "bytes": 199090944 + 38806784},
 }
 
 

@@ -124,40 +124,6 @@ __device__ __forceinline__ uint32_t peers_of_digit(uint32_t d, bool valid) {
   return peers;
 }
 
-// Decoupled look-back of partition `part` by one thread (status word:
-// value << 2 | flag): publishes the partition's aggregate, adds up its
-// predecessors' until an inclusive prefix, publishes its own inclusive
-// prefix and returns the exclusive one; -1 (error flag published, status
-// bit 1 set) when a wait ran out or a predecessor failed.
-__device__ long long lookback_prefix(uint64_t* status, int64_t part, long long agg,
-                                     WsHeader* hdr) {
-  if (part == 0) {
-    st_volatile(&status[0], ((uint64_t)agg << 2) | kFlagInc);
-    return 0;
-  }
-  st_volatile(&status[part], ((uint64_t)agg << 2) | kFlagAgg);
-  long long prefix = 0;
-  for (int64_t j = part - 1; j >= 0; --j) {
-    uint64_t s;
-    uint32_t spins = 0;
-    while (((s = ld_volatile(&status[j])) & 3u) == 0) {
-      if (++spins > kSpinLimit) break;
-      __nanosleep(100);
-    }
-    const uint64_t f = s & 3u;
-    if (f == 0 || f == kFlagErr) {
-      st_volatile(&status[part], kFlagErr);
-      atomicOr(&hdr->error, 1u);
-      return -1;
-    }
-    prefix += (long long)(s >> 2);
-    if (f == kFlagInc) break;
-  }
-  __threadfence();
-  st_volatile(&status[part], ((uint64_t)(prefix + agg) << 2) | kFlagInc);
-  return prefix;
-}
-
 // Decoupled look-back of partition `part` by one warp (all 32 lanes call;
 // status word: value << 2 | flag): lane 0 publishes the aggregate, the warp
 // reads 32 predecessors at a time and stops at the nearest inclusive prefix;

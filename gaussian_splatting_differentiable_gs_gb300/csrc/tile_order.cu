@@ -18,9 +18,13 @@ constexpr int kOrdThreads = 1024;
 constexpr int kOrdWarps = kOrdThreads / 32;
 constexpr int kOrdBuckets = 34;  // 0: empty; 1 + floor(log2 len) <= 33 (len < 2^33)
 
-__device__ __forceinline__ uint32_t order_bucket(const int64_t* ranges, int64_t f) {
-  const int64_t len = ranges[2 * f + 1] - ranges[2 * f];
+__device__ __forceinline__ uint32_t bucket_of_len(int64_t len) {
   return len > 0 ? (uint32_t)min(64 - __clzll((unsigned long long)len), kOrdBuckets - 1) : 0u;
+}
+
+__device__ __forceinline__ uint32_t order_bucket(const int64_t* ranges, int64_t f) {
+  const longlong2 r = __ldg(reinterpret_cast<const longlong2*>(ranges) + f);
+  return bucket_of_len(r.y - r.x);
 }
 
 constexpr int kOrdCache = 40960;  // tiles whose buckets are kept in shared memory
@@ -35,10 +39,22 @@ __global__ void __launch_bounds__(kOrdThreads) tile_order_kernel(int64_t n_flat,
   const bool cached = n_flat <= kOrdCache;
   if (tid < kOrdBuckets) s_start[tid] = 0;
   __syncthreads();
-  for (int64_t f = tid; f < n_flat; f += kOrdThreads) {
-    const uint32_t b = order_bucket(ranges, f);
-    if (cached) s_bucket[f] = (uint8_t)b;
-    atomicAdd(&s_start[b], 1u);
+  constexpr int kBatch = 8;  // tiles per thread whose loads are in flight together
+  for (int64_t base = 0; base < n_flat; base += kBatch * kOrdThreads) {
+    uint32_t bk[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t f = base + (int64_t)u * kOrdThreads + tid;
+      bk[u] = f < n_flat ? order_bucket(ranges, f) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t f = base + (int64_t)u * kOrdThreads + tid;
+      if (f < n_flat) {
+        if (cached) s_bucket[f] = (uint8_t)bk[u];
+        atomicAdd(&s_start[bk[u]], 1u);
+      }
+    }
   }
   __syncthreads();
   if (tid == 0) {  // exclusive starts, longest bucket first, empty tiles last
@@ -83,7 +99,8 @@ using namespace gs;
 
 extern "C" gs_status gs_tile_order(int64_t n_flat, const int64_t* ranges, uint32_t* order,
                                    void* stream) {
-  if (n_flat < 0 || n_flat > (int64_t)0xFFFFFFFFll || (n_flat > 0 && (!ranges || !order)))
+  if (n_flat < 0 || n_flat > (int64_t)0xFFFFFFFFll || (n_flat > 0 && (!ranges || !order)) ||
+      !aligned16(ranges))
     return GS_ERR_INVALID_ARG;
   if (n_flat == 0) return GS_OK;
   tile_order_kernel<<<1, kOrdThreads, 0, (cudaStream_t)stream>>>(n_flat, ranges, order);

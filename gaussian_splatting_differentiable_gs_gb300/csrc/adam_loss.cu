@@ -254,4 +254,6 @@ extern "C" const char* gs_status_string(gs_status status) {
   return "unknown status";
 }
 
+extern "C" const char* gs_status_str(gs_status status) { return gs_status_string(status); }
+
 extern "C" int32_t gs_version(void) { return 100; }

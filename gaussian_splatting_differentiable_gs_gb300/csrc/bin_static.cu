@@ -74,7 +74,8 @@ extern "C" gs_status gs_bin_and_sort_static(int64_t n, int32_t n_views, const gs
                                             uint64_t* keys, uint32_t* vals, int64_t* ranges,
                                             int64_t* n_isect, void* stream) {
   if (n < 0 || n_views < 1 || n_views > GS_MAX_VIEWS || capacity < 0) return GS_ERR_INVALID_ARG;
-  if (n * n_views > kStaticMaxRows || capacity > kStaticMaxIsect) return GS_ERR_INVALID_ARG;
+  // n > max / n_views rather than n * n_views > max: the product could overflow
+  if (n > kStaticMaxRows / n_views || capacity > kStaticMaxIsect) return GS_ERR_INVALID_ARG;
   void* ws = nullptr;
   const gs_status st = scratch_for_current_device(&ws);
   if (st != GS_OK) return st;

@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kOrdThreads) tile_order_kernel(int64_t n_flat,
     const uint32_t b = !valid ? (uint32_t)kOrdBuckets : cached ? (uint32_t)s_bucket[f]
                                                                 : order_bucket(ranges, f);
     const uint32_t peers = __match_any_sync(0xffffffffu, b);
-    if (lane < kOrdBuckets) s_wcount[warp][lane] = 0;
+    for (int k = lane; k < kOrdBuckets; k += 32) s_wcount[warp][k] = 0;  // all 34 buckets
     __syncwarp();
     if (valid && lane == __ffs(peers) - 1) s_wcount[warp][b] = __popc(peers);
     __syncthreads();

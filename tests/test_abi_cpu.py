@@ -41,6 +41,11 @@ def test_status_strings_and_version(gslib):
     assert gslib.status_string(0) == "ok"
     assert "capacity" in gslib.status_string(2)
     assert gslib.status_string(99) == "unknown status"
+    lib = C.CDLL(gslib.LIB_PATH)
+    lib.gs_status_str.restype = C.c_char_p
+    lib.gs_status_str.argtypes = [C.c_int]
+    for code in (0, 1, 2, 3, 4, 5, 99):
+        assert lib.gs_status_str(code).decode() == gslib.status_string(code)
 
 
 def test_key_bits_and_workspace(gslib):

@@ -52,7 +52,14 @@ def lib():
         L.or_count_isect.restype = i64
         L.or_bin.argtypes = [i64, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.or_raster_fwd.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i64,
-                                    vp, vp, vp, vp, vp, vp]
+                                    vp, vp, vp, vp, vp, vp, vp]
+        L.or_raster_fwd_mt.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       i64, vp, vp, vp, vp, vp, vp, i32]
+        L.or_raster_bwd_mt.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       vp, i64, vp, vp, vp, vp, i32]
+        L.or_project_bwd_mt.argtypes = [i64, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp, i32]
+        L.or_adam_mt.argtypes = [i64, i64, vp, vp, vp, vp, i64, dbl, dbl, dbl, dbl, vp, i32]
+        L.or_bin_mt.argtypes = [i64, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, i32]
         L.or_prune_mask.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, i64, C.c_float, vp]
         L.or_raster_fwd_brute.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp,
                                           vp, vp]
@@ -149,8 +156,11 @@ def count_isect(mean2d_f32, radius, width, height, tile=TILE):
     return int(lib().or_count_isect(r.shape[0], _p(m), _p(r), tile, width, height))
 
 
-def bin_and_sort(n, n_views, mean2d_f32, radius, depth_f32, width, height, tile=TILE):
-    """-> keys u64[I], vals u32[I], ranges i64[n_views*T][2]."""
+def bin_and_sort(n, n_views, mean2d_f32, radius, depth_f32, width, height, tile=TILE,
+                 threads=1):
+    """-> keys u64[I], vals u32[I], ranges i64[n_views*T][2].  threads > 1
+    splits the emission and the per-tile sorts over POSIX threads (same
+    result)."""
     m = np.ascontiguousarray(mean2d_f32, np.float32)
     r = np.ascontiguousarray(radius, np.int32)
     d = np.ascontiguousarray(depth_f32, np.float32)
@@ -159,8 +169,12 @@ def bin_and_sort(n, n_views, mean2d_f32, radius, depth_f32, width, height, tile=
     keys = np.zeros(max(total, 1), np.uint64)
     vals = np.zeros(max(total, 1), np.uint32)
     ranges = np.zeros((n_views * T, 2), np.int64)
-    lib().or_bin(n, n_views, _p(m), _p(r), _p(d), tile, width, height, _p(keys), _p(vals),
-                 _p(ranges))
+    if threads > 1:
+        lib().or_bin_mt(n, n_views, _p(m), _p(r), _p(d), tile, width, height, _p(keys),
+                        _p(vals), _p(ranges), int(threads))
+    else:
+        lib().or_bin(n, n_views, _p(m), _p(r), _p(d), tile, width, height, _p(keys), _p(vals),
+                     _p(ranges))
     return keys[:total], vals[:total], ranges
 
 
@@ -181,9 +195,13 @@ def bin_select(n, n_views, mean2d_f32, radius, depth_f32, width, height, tile_se
 
 
 def raster_fwd(n, n_views, width, height, feats, vals, ranges, bg=(0.0, 0.0, 0.0), tile=TILE,
-               tile_sel=None, importance=False):
+               tile_sel=None, importance=False, threads=1):
     """feats: dict with mean2d, conic, opacity, color (any float dtype).
-    importance=True adds each row's largest blending weight alpha T."""
+    Outputs per pixel: image, T_final, n_contrib, pairs (list entries tested
+    before the pixel stopped, the stopping one included), included (pairs
+    composited), margin (relative distance of the closest threshold decision).
+    importance=True adds each row's largest blending weight alpha T (single
+    thread only); threads > 1 splits the tiles over POSIX threads."""
     HW = width * height
     m, co = _f64(feats["mean2d"]), _f64(feats["conic"])
     op, col = _f64(feats["opacity"]), _f64(feats["color"])
@@ -194,15 +212,23 @@ def raster_fwd(n, n_views, width, height, feats, vals, ranges, bg=(0.0, 0.0, 0.0
     T_final = np.zeros((n_views, height, width))
     n_contrib = np.zeros((n_views, height, width), np.int32)
     pairs = np.zeros((n_views, height, width), np.int64)
+    included = np.zeros((n_views, height, width), np.int64)
     margin = np.full((n_views, height, width), np.inf)
     sel = None if tile_sel is None else np.ascontiguousarray(tile_sel, np.int64)
     imp = np.zeros(m.shape[0]) if importance else None
-    lib().or_raster_fwd(n, n_views, width, height, tile, _p(m), _p(co), _p(op), _p(col),
-                        _p(vals), _p(ranges), _p(bgv), _p(sel), 0 if sel is None else sel.size,
-                        _p(image), _p(T_final), _p(n_contrib), _p(pairs), _p(margin),
-                        _p(imp))
+    if threads > 1 and not importance:
+        lib().or_raster_fwd_mt(n, n_views, width, height, tile, _p(m), _p(co), _p(op), _p(col),
+                               _p(vals), _p(ranges), _p(bgv), _p(sel),
+                               0 if sel is None else sel.size, _p(image), _p(T_final),
+                               _p(n_contrib), _p(pairs), _p(included), _p(margin), int(threads))
+    else:
+        lib().or_raster_fwd(n, n_views, width, height, tile, _p(m), _p(co), _p(op), _p(col),
+                            _p(vals), _p(ranges), _p(bgv), _p(sel),
+                            0 if sel is None else sel.size, _p(image), _p(T_final),
+                            _p(n_contrib), _p(pairs), _p(included), _p(margin), _p(imp))
     del HW
-    out = dict(image=image, T_final=T_final, n_contrib=n_contrib, pairs=pairs, margin=margin)
+    out = dict(image=image, T_final=T_final, n_contrib=n_contrib, pairs=pairs,
+               included=included, margin=margin)
     if importance:
         out["importance"] = imp
     return out
@@ -247,7 +273,7 @@ def loss_l1(image, target):
 
 
 def raster_bwd(n, n_views, width, height, feats, vals, ranges, dL_dimage, bg=(0.0, 0.0, 0.0),
-               tile=TILE, tile_sel=None):
+               tile=TILE, tile_sel=None, threads=1):
     rows = n * n_views
     m, co = _f64(feats["mean2d"]), _f64(feats["conic"])
     op, col = _f64(feats["opacity"]), _f64(feats["color"])
@@ -258,15 +284,19 @@ def raster_bwd(n, n_views, width, height, feats, vals, ranges, dL_dimage, bg=(0.
     out = dict(mean2d=np.zeros((rows, 2)), conic=np.zeros((rows, 3)), opacity=np.zeros(rows),
                color=np.zeros((rows, 3)))
     sel = None if tile_sel is None else np.ascontiguousarray(tile_sel, np.int64)
-    lib().or_raster_bwd(n, n_views, width, height, tile, _p(m), _p(co), _p(op), _p(col),
-                        _p(vals), _p(ranges), _p(bgv), _p(g_img), _p(sel),
-                        0 if sel is None else sel.size, _p(out["mean2d"]),
-                        _p(out["conic"]), _p(out["opacity"]), _p(out["color"]))
+    args = (n, n_views, width, height, tile, _p(m), _p(co), _p(op), _p(col), _p(vals),
+            _p(ranges), _p(bgv), _p(g_img), _p(sel), 0 if sel is None else sel.size,
+            _p(out["mean2d"]), _p(out["conic"]), _p(out["opacity"]), _p(out["color"]))
+    if threads > 1:
+        lib().or_raster_bwd_mt(*args, int(threads))
+    else:
+        lib().or_raster_bwd(*args)
     return out
 
 
-def project_bwd(params, cams, grads2d, tile=TILE):
-    """grads2d: dict mean2d/conic/opacity/color per row -> (grad[59][n], visible[n])."""
+def project_bwd(params, cams, grads2d, tile=TILE, threads=1):
+    """grads2d: dict mean2d/conic/opacity/color per row -> (grad[59][n], visible[n]).
+    threads > 1 splits the Gaussians over POSIX threads (same result)."""
     params = _f64(params)
     n = params.shape[1]
     grad = np.zeros((NPARAM, n))
@@ -274,45 +304,57 @@ def project_bwd(params, cams, grads2d, tile=TILE):
     cs = cameras_struct(cams)
     gm, gc = _f64(grads2d["mean2d"]), _f64(grads2d["conic"])
     go, gcol = _f64(grads2d["opacity"]), _f64(grads2d["color"])
-    lib().or_project_bwd(n, _p(params), len(cams), C.cast(cs, C.c_void_p), tile, _p(gm), _p(gc),
-                         _p(go), _p(gcol), _p(grad), _p(visible))
+    args = (n, _p(params), len(cams), C.cast(cs, C.c_void_p), tile, _p(gm), _p(gc), _p(go),
+            _p(gcol), _p(grad), _p(visible))
+    if threads > 1:
+        lib().or_project_bwd_mt(*args, int(threads))
+    else:
+        lib().or_project_bwd(*args)
     return grad, visible
 
 
-def adam(p, g, m, v, t, lr, beta1=0.9, beta2=0.999, eps=1e-8, visible=None):
-    """In place on float64 [rows][n_cols] arrays p, m, v."""
+def adam(p, g, m, v, t, lr, beta1=0.9, beta2=0.999, eps=1e-8, visible=None, threads=1):
+    """In place on float64 [rows][n_cols] arrays p, m, v.  threads > 1
+    splits the columns over POSIX threads (same result)."""
     assert p.dtype == np.float64 and p.flags.c_contiguous
     g = _f64(g)
     vis = None if visible is None else np.ascontiguousarray(visible, np.uint8)
     rows, cols = p.shape
-    lib().or_adam(rows, cols, _p(p), _p(g), _p(m), _p(v), int(t), lr, beta1, beta2, eps, _p(vis))
+    if threads > 1:
+        lib().or_adam_mt(rows, cols, _p(p), _p(g), _p(m), _p(v), int(t), lr, beta1, beta2, eps,
+                         _p(vis), int(threads))
+    else:
+        lib().or_adam(rows, cols, _p(p), _p(g), _p(m), _p(v), int(t), lr, beta1, beta2, eps,
+                      _p(vis))
 
 
 def tiles_grid(width, height, tile=TILE):
     return (width + tile - 1) // tile, (height + tile - 1) // tile
 
 
-def render(params, cams, bg=(0.0, 0.0, 0.0), tile=TILE):
+def render(params, cams, bg=(0.0, 0.0, 0.0), tile=TILE, threads=1):
     """Forward chain: project -> bin -> composite, all in the oracle."""
     n = np.asarray(params).shape[1]
     V = len(cams)
     W, H = int(cams[0]["width"]), int(cams[0]["height"])
-    pr = project(params, cams, tile)
+    pr = project(params, cams, tile, threads=threads)
     keys, vals, ranges = bin_and_sort(n, V, pr["mean2d"].astype(np.float32), pr["radius"],
-                                      pr["depth"].astype(np.float32), W, H, tile)
-    fw = raster_fwd(n, V, W, H, pr, vals, ranges, bg, tile)
+                                      pr["depth"].astype(np.float32), W, H, tile,
+                                      threads=threads)
+    fw = raster_fwd(n, V, W, H, pr, vals, ranges, bg, tile, threads=threads)
     return pr, (keys, vals, ranges), fw
 
 
-def train_step_grads(params, cams, target, bg=(0.0, 0.0, 0.0), tile=TILE):
-    """Forward + L1 loss + backward; returns (loss, grad[59][n], visible, parts)."""
+def train_step_grads(params, cams, target, bg=(0.0, 0.0, 0.0), tile=TILE, threads=1):
+    """Forward + L1 loss + backward; returns (loss, grad[59][n], visible, parts).
+    threads > 1 runs every stage split over POSIX threads."""
     n = np.asarray(params).shape[1]
     V = len(cams)
     W, H = int(cams[0]["width"]), int(cams[0]["height"])
-    pr, (keys, vals, ranges), fw = render(params, cams, bg, tile)
+    pr, (keys, vals, ranges), fw = render(params, cams, bg, tile, threads=threads)
     loss, g_img = loss_l1(fw["image"], target)
-    g2 = raster_bwd(n, V, W, H, pr, vals, ranges, g_img, bg, tile)
-    grad, visible = project_bwd(params, cams, g2, tile)
+    g2 = raster_bwd(n, V, W, H, pr, vals, ranges, g_img, bg, tile, threads=threads)
+    grad, visible = project_bwd(params, cams, g2, tile, threads=threads)
     return loss, grad, visible, dict(proj=pr, keys=keys, vals=vals, ranges=ranges, fwd=fw,
                                      g_img=g_img, g2d=g2)
 

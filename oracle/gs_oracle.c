@@ -443,6 +443,123 @@ void or_bin(int64_t n, int32_t n_views, const float* mean2d, const int32_t* radi
   free(items);
 }
 
+/* Thread split of or_bin.  The rows are split into contiguous chunks, one
+ * per thread; each thread counts its chunk's pairs per flattened tile, the
+ * counts give every (tile, chunk) its place, and each thread writes its
+ * chunk's pairs there in row order.  Every tile's segment (keys sharing the
+ * tile's high bits) is then sorted by (key, id) on its own.  The sort keys
+ * are unique, so the result is the one of or_bin exactly. */
+typedef struct bin_job {
+  int64_t n, r0, r1, n_flat, f0, f1;
+  int32_t tile, width, height, pass;
+  const float *mean2d, *depth;
+  const int32_t* radius;
+  int64_t* counts;  /* [n_flat] of this chunk (pass 0); its cursors (pass 1) */
+  kv* items;
+  const int64_t* offsets;  /* [n_flat + 1] (pass 2) */
+} bin_job;
+
+static void* bin_thread(void* arg) {
+  bin_job* j = (bin_job*)arg;
+  const int32_t tx = (j->width + j->tile - 1) / j->tile, ty = (j->height + j->tile - 1) / j->tile;
+  const int64_t T = (int64_t)tx * ty;
+  int32_t rect[4];
+  if (j->pass == 2) {  /* sort the segments of tiles f0 <= f < f1 */
+    for (int64_t f = j->f0; f < j->f1; ++f)
+      qsort(j->items + j->offsets[f], (size_t)(j->offsets[f + 1] - j->offsets[f]), sizeof(kv),
+            kv_cmp);
+    return NULL;
+  }
+  for (int64_t r = j->r0; r < j->r1; ++r) {
+    if (j->radius[r] <= 0) continue;
+    const int64_t view = r / j->n, g = r % j->n;
+    or_tile_rect(j->mean2d[2 * r], j->mean2d[2 * r + 1], j->radius[r], j->tile, tx, ty, rect);
+    for (int32_t yy = rect[2]; yy < rect[3]; ++yy)
+      for (int32_t xx = rect[0]; xx < rect[1]; ++xx) {
+        const int64_t flat = view * T + (int64_t)yy * tx + xx;
+        if (j->pass == 0) {
+          ++j->counts[flat];
+        } else {
+          kv* it = &j->items[j->counts[flat]++];
+          it->key = ((uint64_t)flat << 32) | (uint64_t)float_bits(j->depth[r]);
+          it->val = (uint32_t)g;
+        }
+      }
+  }
+  return NULL;
+}
+
+static void run_bin_jobs(bin_job* jobs, int32_t threads) {
+  pthread_t tid[256];
+  int started[256] = {0};
+  for (int32_t t = 1; t < threads; ++t)
+    started[t] = pthread_create(&tid[t], NULL, bin_thread, &jobs[t]) == 0;
+  bin_thread(&jobs[0]);
+  for (int32_t t = 1; t < threads; ++t) {
+    if (started[t]) pthread_join(tid[t], NULL);
+    else bin_thread(&jobs[t]);
+  }
+}
+
+void or_bin_mt(int64_t n, int32_t n_views, const float* mean2d, const int32_t* radius,
+               const float* depth, int32_t tile, int32_t width, int32_t height,
+               uint64_t* keys, uint32_t* vals, int64_t* ranges, int32_t threads) {
+  const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
+  const int64_t n_flat = n_views * (int64_t)tx * ty;
+  const int64_t n_rows = n * n_views;
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  int64_t* counts = (int64_t*)calloc((size_t)(threads * n_flat), sizeof(int64_t));
+  int64_t* offsets = (int64_t*)calloc((size_t)(n_flat + 1), sizeof(int64_t));
+  bin_job jobs[256];
+  for (int32_t t = 0; t < threads; ++t) {
+    bin_job j = {n, n_rows * t / threads, n_rows * (t + 1) / threads, n_flat, 0, 0, tile, width,
+                 height, 0, mean2d, depth, radius, counts + (int64_t)t * n_flat, NULL, offsets};
+    jobs[t] = j;
+  }
+  run_bin_jobs(jobs, threads);
+  /* offsets of the tiles; cursor of (tile, chunk) */
+  for (int64_t f = 0; f < n_flat; ++f) {
+    int64_t run = offsets[f];
+    for (int32_t t = 0; t < threads; ++t) {
+      const int64_t c = counts[(int64_t)t * n_flat + f];
+      counts[(int64_t)t * n_flat + f] = run;
+      run += c;
+    }
+    offsets[f + 1] = run;
+  }
+  const int64_t total = offsets[n_flat];
+  kv* items = (kv*)malloc(sizeof(kv) * (size_t)(total > 0 ? total : 1));
+  for (int32_t t = 0; t < threads; ++t) {
+    jobs[t].pass = 1;
+    jobs[t].items = items;
+  }
+  run_bin_jobs(jobs, threads);
+  for (int32_t t = 0; t < threads; ++t) {  /* tile ranges of about total / threads pairs */
+    int64_t f0 = 0, f1 = 0;
+    while (f0 < n_flat && offsets[f0] < total * t / threads) ++f0;
+    f1 = f0;
+    while (f1 < n_flat && offsets[f1] < total * (t + 1) / threads) ++f1;
+    if (t == threads - 1) f1 = n_flat;
+    jobs[t].pass = 2;
+    jobs[t].f0 = f0;
+    jobs[t].f1 = f1;
+  }
+  run_bin_jobs(jobs, threads);
+  for (int64_t f = 0; f < n_flat; ++f) {
+    const int64_t a = offsets[f], b = offsets[f + 1];
+    ranges[2 * f] = a < b ? a : 0;
+    ranges[2 * f + 1] = a < b ? b : 0;
+  }
+  for (int64_t i = 0; i < total; ++i) {
+    keys[i] = items[i].key;
+    vals[i] = items[i].val;
+  }
+  free(items);
+  free(counts);
+  free(offsets);
+}
+
 typedef struct dk { uint32_t dbits; uint32_t id; } dk;
 
 static int dk_cmp(const void* pa, const void* pb) {
@@ -508,53 +625,121 @@ static double pair_alpha_raw(double px, double py, const double* m, const double
 
 static double rel_dist(double v, double ref) { return fabs(v - ref) / ref; }
 
+/* Forward compositing of one flattened tile (view * T + tile) of its sorted
+ * list, pixel by pixel in the pages' order: front to back, skip alpha <
+ * 1/255, stop before the transmittance drops below 1e-4. */
+static void raster_fwd_tile(int64_t flat, int64_t n, int32_t width, int32_t height, int32_t tile,
+                            const double* mean2d, const double* conic, const double* opacity,
+                            const double* color, const uint32_t* vals, const int64_t* ranges,
+                            const double bg[3], double* image, double* T_final,
+                            int32_t* n_contrib, int64_t* pairs, int64_t* included,
+                            double* margin, double* importance) {
+  const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
+  const int64_t T = (int64_t)tx * ty;
+  const int64_t HW = (int64_t)width * height;
+  const int64_t view = flat / T, t = flat % T;
+  const int32_t tile_x = (int32_t)(t % tx), tile_y = (int32_t)(t / tx);
+  const int64_t start = ranges[2 * flat], end = ranges[2 * flat + 1];
+  for (int32_t yy = tile_y * tile; yy < (tile_y + 1) * tile && yy < height; ++yy)
+    for (int32_t xx = tile_x * tile; xx < (tile_x + 1) * tile && xx < width; ++xx) {
+      const double px = xx + 0.5, py = yy + 0.5;
+      double Tr = 1.0, C[3] = {0.0, 0.0, 0.0};
+      int32_t last = 0;
+      int64_t tested = 0, composited = 0;
+      double mg = INFINITY;
+      for (int64_t i = start; i < end; ++i) {
+        const int64_t r = view * n + vals[i];
+        double power, dx, dy;
+        ++tested;
+        const double araw = pair_alpha_raw(px, py, &mean2d[2 * r], &conic[3 * r], opacity[r],
+                                           &power, &dx, &dy);
+        mg = fmin(mg, rel_dist(araw, kAlphaMin));
+        mg = fmin(mg, rel_dist(araw, kAlphaMax));
+        const double alpha = araw < kAlphaMax ? araw : kAlphaMax;
+        if (alpha < kAlphaMin) continue;
+        const double Tn = Tr * (1.0 - alpha);
+        mg = fmin(mg, rel_dist(Tn, kTMin));
+        if (Tn < kTMin) break;
+        for (int ch = 0; ch < 3; ++ch) C[ch] += color[3 * r + ch] * alpha * Tr;
+        if (importance && alpha * Tr > importance[r]) importance[r] = alpha * Tr;
+        Tr = Tn;
+        last = (int32_t)(i - start + 1);
+        ++composited;
+      }
+      const int64_t pix = (int64_t)yy * width + xx;
+      for (int ch = 0; ch < 3; ++ch) image[(view * 3 + ch) * HW + pix] = C[ch] + Tr * bg[ch];
+      T_final[view * HW + pix] = Tr;
+      n_contrib[view * HW + pix] = last;
+      if (pairs) pairs[view * HW + pix] = tested;
+      if (included) included[view * HW + pix] = composited;
+      if (margin) margin[view * HW + pix] = mg;
+    }
+}
+
 void or_raster_fwd(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
                    const double* mean2d, const double* conic, const double* opacity,
                    const double* color, const uint32_t* vals, const int64_t* ranges,
                    const double bg[3], const int64_t* tile_sel, int64_t n_sel,
                    double* image, double* T_final, int32_t* n_contrib, int64_t* pairs,
-                   double* margin, double* importance) {
+                   int64_t* included, double* margin, double* importance) {
   const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
   const int64_t T = (int64_t)tx * ty;
   const int64_t n_tiles = tile_sel ? n_sel : n_views * T;
-  const int64_t HW = (int64_t)width * height;
-  for (int64_t it = 0; it < n_tiles; ++it) {
-    const int64_t flat = tile_sel ? tile_sel[it] : it;
-    const int64_t view = flat / T, t = flat % T;
-    const int32_t tile_x = (int32_t)(t % tx), tile_y = (int32_t)(t / tx);
-    const int64_t start = ranges[2 * flat], end = ranges[2 * flat + 1];
-    for (int32_t yy = tile_y * tile; yy < (tile_y + 1) * tile && yy < height; ++yy)
-      for (int32_t xx = tile_x * tile; xx < (tile_x + 1) * tile && xx < width; ++xx) {
-        const double px = xx + 0.5, py = yy + 0.5;
-        double Tr = 1.0, C[3] = {0.0, 0.0, 0.0};
-        int32_t last = 0;
-        int64_t tested = 0;
-        double mg = INFINITY;
-        for (int64_t i = start; i < end; ++i) {
-          const int64_t r = view * n + vals[i];
-          double power, dx, dy;
-          ++tested;
-          const double araw = pair_alpha_raw(px, py, &mean2d[2 * r], &conic[3 * r], opacity[r],
-                                             &power, &dx, &dy);
-          mg = fmin(mg, rel_dist(araw, kAlphaMin));
-          mg = fmin(mg, rel_dist(araw, kAlphaMax));
-          const double alpha = araw < kAlphaMax ? araw : kAlphaMax;
-          if (alpha < kAlphaMin) continue;
-          const double Tn = Tr * (1.0 - alpha);
-          mg = fmin(mg, rel_dist(Tn, kTMin));
-          if (Tn < kTMin) break;
-          for (int ch = 0; ch < 3; ++ch) C[ch] += color[3 * r + ch] * alpha * Tr;
-          if (importance && alpha * Tr > importance[r]) importance[r] = alpha * Tr;
-          Tr = Tn;
-          last = (int32_t)(i - start + 1);
-        }
-        const int64_t pix = (int64_t)yy * width + xx;
-        for (int ch = 0; ch < 3; ++ch) image[(view * 3 + ch) * HW + pix] = C[ch] + Tr * bg[ch];
-        T_final[view * HW + pix] = Tr;
-        n_contrib[view * HW + pix] = last;
-        if (pairs) pairs[view * HW + pix] = tested;
-        if (margin) margin[view * HW + pix] = mg;
-      }
+  for (int64_t it = 0; it < n_tiles; ++it)
+    raster_fwd_tile(tile_sel ? tile_sel[it] : it, n, width, height, tile, mean2d, conic, opacity,
+                    color, vals, ranges, bg, image, T_final, n_contrib, pairs, included, margin,
+                    importance);
+}
+
+/* Thread split of or_raster_fwd: tile k of the work list goes to thread
+ * k mod threads.  Tiles write disjoint pixels, so the outputs are those of
+ * or_raster_fwd exactly (importance is not offered here: rows are shared
+ * between tiles). */
+typedef struct fwd_job {
+  int64_t n, n_tiles;
+  int32_t width, height, tile, threads, index;
+  const double *mean2d, *conic, *opacity, *color;
+  const uint32_t* vals;
+  const int64_t *ranges, *tile_sel;
+  const double* bg;
+  double *image, *T_final, *margin;
+  int32_t* n_contrib;
+  int64_t *pairs, *included;
+} fwd_job;
+
+static void* raster_fwd_thread(void* arg) {
+  const fwd_job* j = (const fwd_job*)arg;
+  for (int64_t it = j->index; it < j->n_tiles; it += j->threads)
+    raster_fwd_tile(j->tile_sel ? j->tile_sel[it] : it, j->n, j->width, j->height, j->tile,
+                    j->mean2d, j->conic, j->opacity, j->color, j->vals, j->ranges, j->bg,
+                    j->image, j->T_final, j->n_contrib, j->pairs, j->included, j->margin, NULL);
+  return NULL;
+}
+
+void or_raster_fwd_mt(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
+                      const double* mean2d, const double* conic, const double* opacity,
+                      const double* color, const uint32_t* vals, const int64_t* ranges,
+                      const double bg[3], const int64_t* tile_sel, int64_t n_sel,
+                      double* image, double* T_final, int32_t* n_contrib, int64_t* pairs,
+                      int64_t* included, double* margin, int32_t threads) {
+  const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
+  const int64_t n_tiles = tile_sel ? n_sel : n_views * (int64_t)tx * ty;
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  fwd_job jobs[256];
+  pthread_t tid[256];
+  int started[256] = {0};
+  for (int32_t t = 0; t < threads; ++t) {
+    fwd_job j = {n, n_tiles, width, height, tile, threads, t, mean2d, conic, opacity, color,
+                 vals, ranges, tile_sel, bg, image, T_final, margin, n_contrib, pairs, included};
+    jobs[t] = j;
+  }
+  for (int32_t t = 1; t < threads; ++t)
+    started[t] = pthread_create(&tid[t], NULL, raster_fwd_thread, &jobs[t]) == 0;
+  raster_fwd_thread(&jobs[0]);
+  for (int32_t t = 1; t < threads; ++t) {
+    if (started[t]) pthread_join(tid[t], NULL);
+    else raster_fwd_thread(&jobs[t]);
   }
 }
 
@@ -622,6 +807,117 @@ double or_loss_l1(int64_t n, const double* image, const double* target, double* 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Scratch of one pixel's included pairs, front to back. */
+typedef struct bwd_scratch {
+  int64_t *row, *pos;
+  double *alpha, *T, *raw, *dx, *dy;
+} bwd_scratch;
+
+static int bwd_scratch_alloc(bwd_scratch* b, int64_t len) {
+  const size_t m = (size_t)(len > 0 ? len : 1);
+  b->row = (int64_t*)malloc(sizeof(int64_t) * m);
+  b->pos = (int64_t*)malloc(sizeof(int64_t) * m);
+  b->alpha = (double*)malloc(sizeof(double) * m);
+  b->T = (double*)malloc(sizeof(double) * m);
+  b->raw = (double*)malloc(sizeof(double) * m);
+  b->dx = (double*)malloc(sizeof(double) * m);
+  b->dy = (double*)malloc(sizeof(double) * m);
+  return b->row && b->pos && b->alpha && b->T && b->raw && b->dx && b->dy;
+}
+
+static void bwd_scratch_free(bwd_scratch* b) {
+  free(b->row);
+  free(b->pos);
+  free(b->alpha);
+  free(b->T);
+  free(b->raw);
+  free(b->dx);
+  free(b->dy);
+}
+
+/* Backward compositing of one flattened tile.  For each pixel the forward is
+ * run again (T_i as a running product), then its included pairs are walked
+ * back to front with S = the colour composited behind the pair.  Gradients
+ * are added at index row (by_pos == 0) or at the pair's list position minus
+ * the tile's start (by_pos == 1, for a per-tile buffer). */
+static void raster_bwd_tile(int64_t flat, int64_t n, int32_t width, int32_t height, int32_t tile,
+                            const double* mean2d, const double* conic, const double* opacity,
+                            const double* color, const uint32_t* vals, const int64_t* ranges,
+                            const double bg[3], const double* dL_dimage, bwd_scratch* sc,
+                            int by_pos, double* g_mean2d, double* g_conic, double* g_opacity,
+                            double* g_color) {
+  const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
+  const int64_t T = (int64_t)tx * ty;
+  const int64_t HW = (int64_t)width * height;
+  const int64_t view = flat / T, t = flat % T;
+  const int32_t tile_x = (int32_t)(t % tx), tile_y = (int32_t)(t / tx);
+  const int64_t start = ranges[2 * flat], end = ranges[2 * flat + 1];
+  for (int32_t yy = tile_y * tile; yy < (tile_y + 1) * tile && yy < height; ++yy)
+    for (int32_t xx = tile_x * tile; xx < (tile_x + 1) * tile && xx < width; ++xx) {
+      const double px = xx + 0.5, py = yy + 0.5;
+      const int64_t pix = (int64_t)yy * width + xx;
+      /* forward again: T_i as a running product */
+      double Tr = 1.0;
+      int64_t k = 0;
+      for (int64_t i = start; i < end; ++i) {
+        const int64_t r = view * n + vals[i];
+        double power, dx, dy;
+        const double araw = pair_alpha_raw(px, py, &mean2d[2 * r], &conic[3 * r], opacity[r],
+                                           &power, &dx, &dy);
+        const double alpha = araw < kAlphaMax ? araw : kAlphaMax;
+        if (alpha < kAlphaMin) continue;
+        const double Tn = Tr * (1.0 - alpha);
+        if (Tn < kTMin) break;
+        sc->row[k] = r;
+        sc->pos[k] = i - start;
+        sc->alpha[k] = alpha;
+        sc->T[k] = Tr;
+        sc->raw[k] = araw;
+        sc->dx[k] = dx;
+        sc->dy[k] = dy;
+        ++k;
+        Tr = Tn;
+      }
+      double gC[3];
+      for (int ch = 0; ch < 3; ++ch) gC[ch] = dL_dimage[(view * 3 + ch) * HW + pix];
+      /* S = colour composited behind the current pair, background included */
+      double S[3] = {Tr * bg[0], Tr * bg[1], Tr * bg[2]};
+      for (int64_t j = k - 1; j >= 0; --j) {
+        const int64_t r = sc->row[j];
+        const int64_t a = by_pos ? sc->pos[j] : r; /* where the sums go */
+        const double alpha = sc->alpha[j], Ti = sc->T[j];
+        const double* col = &color[3 * r];
+        double dL_dalpha = 0.0;
+        for (int ch = 0; ch < 3; ++ch) {
+          g_color[3 * a + ch] += alpha * Ti * gC[ch];
+          dL_dalpha += gC[ch] * (col[ch] * Ti - S[ch] / (1.0 - alpha));
+        }
+        for (int ch = 0; ch < 3; ++ch) S[ch] += col[ch] * alpha * Ti;
+        if (sc->raw[j] >= kAlphaMax) continue; /* capped: alpha does not move */
+        const double* co = &conic[3 * r];
+        const double o = opacity[r];
+        const double e = sc->raw[j] / o; /* exp(power) */
+        const double dx = sc->dx[j], dy = sc->dy[j];
+        g_opacity[a] += dL_dalpha * e;
+        const double dL_dpower = dL_dalpha * sc->raw[j];
+        g_mean2d[2 * a] += dL_dpower * (co[0] * dx + co[1] * dy);
+        g_mean2d[2 * a + 1] += dL_dpower * (co[1] * dx + co[2] * dy);
+        g_conic[3 * a] += dL_dpower * (-0.5 * dx * dx);
+        g_conic[3 * a + 1] += dL_dpower * (-dx * dy);
+        g_conic[3 * a + 2] += dL_dpower * (-0.5 * dy * dy);
+      }
+    }
+}
+
+static int64_t longest_list(int32_t n_views, int32_t width, int32_t height, int32_t tile,
+                            const int64_t* ranges) {
+  const int64_t T = (int64_t)((width + tile - 1) / tile) * ((height + tile - 1) / tile);
+  int64_t max_len = 1;
+  for (int64_t f = 0; f < n_views * T; ++f)
+    if (ranges[2 * f + 1] - ranges[2 * f] > max_len) max_len = ranges[2 * f + 1] - ranges[2 * f];
+  return max_len;
+}
+
 void or_raster_bwd(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
                    const double* mean2d, const double* conic, const double* opacity,
                    const double* color, const uint32_t* vals, const int64_t* ranges,
@@ -630,99 +926,125 @@ void or_raster_bwd(int64_t n, int32_t n_views, int32_t width, int32_t height, in
                    double* g_color) {
   const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
   const int64_t T = (int64_t)tx * ty;
-  const int64_t HW = (int64_t)width * height;
   const int64_t n_rows = n * n_views;
   memset(g_mean2d, 0, sizeof(double) * 2 * (size_t)n_rows);
   memset(g_conic, 0, sizeof(double) * 3 * (size_t)n_rows);
   memset(g_opacity, 0, sizeof(double) * (size_t)n_rows);
   memset(g_color, 0, sizeof(double) * 3 * (size_t)n_rows);
-  int64_t max_len = 1;
-  for (int64_t f = 0; f < n_views * T; ++f)
-    if (ranges[2 * f + 1] - ranges[2 * f] > max_len) max_len = ranges[2 * f + 1] - ranges[2 * f];
-  /* per-pixel record of the included pairs, front to back */
-  int64_t* inc_row = (int64_t*)malloc(sizeof(int64_t) * (size_t)max_len);
-  double* inc_alpha = (double*)malloc(sizeof(double) * (size_t)max_len);
-  double* inc_T = (double*)malloc(sizeof(double) * (size_t)max_len);
-  double* inc_raw = (double*)malloc(sizeof(double) * (size_t)max_len);
-  double* inc_dx = (double*)malloc(sizeof(double) * (size_t)max_len);
-  double* inc_dy = (double*)malloc(sizeof(double) * (size_t)max_len);
-  const int64_t n_tiles = tile_sel ? n_sel : n_views * T;
-  for (int64_t it = 0; it < n_tiles; ++it) {
-    const int64_t flat = tile_sel ? tile_sel[it] : it;
-    const int64_t view = flat / T, t = flat % T;
-    const int32_t tile_x = (int32_t)(t % tx), tile_y = (int32_t)(t / tx);
-    const int64_t start = ranges[2 * flat], end = ranges[2 * flat + 1];
-    for (int32_t yy = tile_y * tile; yy < (tile_y + 1) * tile && yy < height; ++yy)
-      for (int32_t xx = tile_x * tile; xx < (tile_x + 1) * tile && xx < width; ++xx) {
-        const double px = xx + 0.5, py = yy + 0.5;
-        const int64_t pix = (int64_t)yy * width + xx;
-        /* forward again: T_i as a running product */
-        double Tr = 1.0;
-        int64_t k = 0;
-        for (int64_t i = start; i < end; ++i) {
-          const int64_t r = view * n + vals[i];
-          double power, dx, dy;
-          const double araw = pair_alpha_raw(px, py, &mean2d[2 * r], &conic[3 * r], opacity[r],
-                                             &power, &dx, &dy);
-          const double alpha = araw < kAlphaMax ? araw : kAlphaMax;
-          if (alpha < kAlphaMin) continue;
-          const double Tn = Tr * (1.0 - alpha);
-          if (Tn < kTMin) break;
-          inc_row[k] = r;
-          inc_alpha[k] = alpha;
-          inc_T[k] = Tr;
-          inc_raw[k] = araw;
-          inc_dx[k] = dx;
-          inc_dy[k] = dy;
-          ++k;
-          Tr = Tn;
-        }
-        double gC[3];
-        for (int ch = 0; ch < 3; ++ch) gC[ch] = dL_dimage[(view * 3 + ch) * HW + pix];
-        /* S = colour composited behind the current pair, background included */
-        double S[3] = {Tr * bg[0], Tr * bg[1], Tr * bg[2]};
-        for (int64_t j = k - 1; j >= 0; --j) {
-          const int64_t r = inc_row[j];
-          const double alpha = inc_alpha[j], Ti = inc_T[j];
-          const double* col = &color[3 * r];
-          double dL_dalpha = 0.0;
-          for (int ch = 0; ch < 3; ++ch) {
-            g_color[3 * r + ch] += alpha * Ti * gC[ch];
-            dL_dalpha += gC[ch] * (col[ch] * Ti - S[ch] / (1.0 - alpha));
-          }
-          for (int ch = 0; ch < 3; ++ch) S[ch] += col[ch] * alpha * Ti;
-          if (inc_raw[j] >= kAlphaMax) continue; /* capped: alpha does not move */
-          const double* co = &conic[3 * r];
-          const double o = opacity[r];
-          const double e = inc_raw[j] / o; /* exp(power) */
-          const double dx = inc_dx[j], dy = inc_dy[j];
-          g_opacity[r] += dL_dalpha * e;
-          const double dL_dpower = dL_dalpha * inc_raw[j];
-          g_mean2d[2 * r] += dL_dpower * (co[0] * dx + co[1] * dy);
-          g_mean2d[2 * r + 1] += dL_dpower * (co[1] * dx + co[2] * dy);
-          g_conic[3 * r] += dL_dpower * (-0.5 * dx * dx);
-          g_conic[3 * r + 1] += dL_dpower * (-dx * dy);
-          g_conic[3 * r + 2] += dL_dpower * (-0.5 * dy * dy);
-        }
-      }
+  bwd_scratch sc;
+  if (!bwd_scratch_alloc(&sc, longest_list(n_views, width, height, tile, ranges))) {
+    bwd_scratch_free(&sc);
+    return;
   }
-  free(inc_row);
-  free(inc_alpha);
-  free(inc_T);
-  free(inc_raw);
-  free(inc_dx);
-  free(inc_dy);
+  const int64_t n_tiles = tile_sel ? n_sel : n_views * T;
+  for (int64_t it = 0; it < n_tiles; ++it)
+    raster_bwd_tile(tile_sel ? tile_sel[it] : it, n, width, height, tile, mean2d, conic, opacity,
+                    color, vals, ranges, bg, dL_dimage, &sc, 0, g_mean2d, g_conic, g_opacity,
+                    g_color);
+  bwd_scratch_free(&sc);
+}
+
+/* Thread split of or_raster_bwd: tile k of the work list goes to thread
+ * k mod threads, which sums the tile's gradients per list position (a row
+ * occurs once in a tile's list) and then adds them to the rows under one
+ * lock.  Equal to or_raster_bwd up to the order of the fp64 sums. */
+typedef struct bwd_job {
+  int64_t n, n_tiles, max_len;
+  int32_t width, height, tile, threads, index;
+  const double *mean2d, *conic, *opacity, *color, *bg, *dL_dimage;
+  const uint32_t* vals;
+  const int64_t *ranges, *tile_sel;
+  double *g_mean2d, *g_conic, *g_opacity, *g_color;
+  pthread_mutex_t* lock;
+} bwd_job;
+
+static void* raster_bwd_thread(void* arg) {
+  const bwd_job* j = (const bwd_job*)arg;
+  const int32_t tx = (j->width + j->tile - 1) / j->tile, ty = (j->height + j->tile - 1) / j->tile;
+  const int64_t T = (int64_t)tx * ty;
+  const size_t m = (size_t)j->max_len;
+  bwd_scratch sc;
+  double* lm = (double*)calloc(2 * m, sizeof(double));
+  double* lc = (double*)calloc(3 * m, sizeof(double));
+  double* lo = (double*)calloc(m, sizeof(double));
+  double* lk = (double*)calloc(3 * m, sizeof(double));
+  if (bwd_scratch_alloc(&sc, j->max_len) && lm && lc && lo && lk) {
+    for (int64_t it = j->index; it < j->n_tiles; it += j->threads) {
+      const int64_t flat = j->tile_sel ? j->tile_sel[it] : it;
+      const int64_t start = j->ranges[2 * flat], len = j->ranges[2 * flat + 1] - start;
+      memset(lm, 0, sizeof(double) * 2 * (size_t)len);
+      memset(lc, 0, sizeof(double) * 3 * (size_t)len);
+      memset(lo, 0, sizeof(double) * (size_t)len);
+      memset(lk, 0, sizeof(double) * 3 * (size_t)len);
+      raster_bwd_tile(flat, j->n, j->width, j->height, j->tile, j->mean2d, j->conic, j->opacity,
+                      j->color, j->vals, j->ranges, j->bg, j->dL_dimage, &sc, 1, lm, lc, lo, lk);
+      const int64_t view = flat / T;
+      pthread_mutex_lock(j->lock);
+      for (int64_t i = 0; i < len; ++i) {
+        const int64_t r = view * j->n + j->vals[start + i];
+        for (int c = 0; c < 2; ++c) j->g_mean2d[2 * r + c] += lm[2 * i + c];
+        for (int c = 0; c < 3; ++c) j->g_conic[3 * r + c] += lc[3 * i + c];
+        j->g_opacity[r] += lo[i];
+        for (int c = 0; c < 3; ++c) j->g_color[3 * r + c] += lk[3 * i + c];
+      }
+      pthread_mutex_unlock(j->lock);
+    }
+  }
+  bwd_scratch_free(&sc);
+  free(lm);
+  free(lc);
+  free(lo);
+  free(lk);
+  return NULL;
+}
+
+void or_raster_bwd_mt(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
+                      const double* mean2d, const double* conic, const double* opacity,
+                      const double* color, const uint32_t* vals, const int64_t* ranges,
+                      const double bg[3], const double* dL_dimage, const int64_t* tile_sel,
+                      int64_t n_sel, double* g_mean2d, double* g_conic, double* g_opacity,
+                      double* g_color, int32_t threads) {
+  const int32_t tx = (width + tile - 1) / tile, ty = (height + tile - 1) / tile;
+  const int64_t n_rows = n * n_views;
+  memset(g_mean2d, 0, sizeof(double) * 2 * (size_t)n_rows);
+  memset(g_conic, 0, sizeof(double) * 3 * (size_t)n_rows);
+  memset(g_opacity, 0, sizeof(double) * (size_t)n_rows);
+  memset(g_color, 0, sizeof(double) * 3 * (size_t)n_rows);
+  const int64_t n_tiles = tile_sel ? n_sel : n_views * (int64_t)tx * ty;
+  const int64_t max_len = longest_list(n_views, width, height, tile, ranges);
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  pthread_mutex_t lock;
+  pthread_mutex_init(&lock, NULL);
+  bwd_job jobs[256];
+  pthread_t tid[256];
+  int started[256] = {0};
+  for (int32_t t = 0; t < threads; ++t) {
+    bwd_job j = {n, n_tiles, max_len, width, height, tile, threads, t, mean2d, conic, opacity,
+                 color, bg, dL_dimage, vals, ranges, tile_sel, g_mean2d, g_conic, g_opacity,
+                 g_color, &lock};
+    jobs[t] = j;
+  }
+  for (int32_t t = 1; t < threads; ++t)
+    started[t] = pthread_create(&tid[t], NULL, raster_bwd_thread, &jobs[t]) == 0;
+  raster_bwd_thread(&jobs[0]);
+  for (int32_t t = 1; t < threads; ++t) {
+    if (started[t]) pthread_join(tid[t], NULL);
+    else raster_bwd_thread(&jobs[t]);
+  }
+  pthread_mutex_destroy(&lock);
 }
 
 /* ------------------------------------------------------------------------ */
-void or_project_bwd(int64_t n, const double* params, int32_t n_views, const or_camera* cams,
-                    int32_t tile, const double* g_mean2d, const double* g_conic,
-                    const double* g_opacity, const double* g_color, double* grad,
-                    uint8_t* visible) {
-  memset(grad, 0, sizeof(double) * OR_NPARAM * (size_t)n);
-  if (visible) memset(visible, 0, (size_t)n);
+/* Projection backward of Gaussians g0 <= g < g1 (columns of grad and
+ * entries of visible that the caller has zeroed). */
+static void project_bwd_range(int64_t n, int64_t g0, int64_t g1, const double* params,
+                              int32_t n_views, const or_camera* cams, int32_t tile,
+                              const double* g_mean2d, const double* g_conic,
+                              const double* g_opacity, const double* g_color, double* grad,
+                              uint8_t* visible) {
   proj_state s;
-  for (int64_t g = 0; g < n; ++g) {
+  for (int64_t g = g0; g < g1; ++g) {
     double g_mu[3] = {0, 0, 0}, g_ls[3] = {0, 0, 0}, g_q[4] = {0, 0, 0, 0}, g_logit = 0.0;
     double g_sh[48];
     memset(g_sh, 0, sizeof(g_sh));
@@ -863,14 +1185,70 @@ void or_project_bwd(int64_t n, const double* params, int32_t n_views, const or_c
   }
 }
 
+void or_project_bwd(int64_t n, const double* params, int32_t n_views, const or_camera* cams,
+                    int32_t tile, const double* g_mean2d, const double* g_conic,
+                    const double* g_opacity, const double* g_color, double* grad,
+                    uint8_t* visible) {
+  memset(grad, 0, sizeof(double) * OR_NPARAM * (size_t)n);
+  if (visible) memset(visible, 0, (size_t)n);
+  project_bwd_range(n, 0, n, params, n_views, cams, tile, g_mean2d, g_conic, g_opacity, g_color,
+                    grad, visible);
+}
+
+/* Thread split of or_project_bwd by Gaussian (contiguous ranges); every
+ * Gaussian's column is computed as in or_project_bwd, so the outputs are
+ * identical. */
+typedef struct pbwd_job {
+  int64_t n, g0, g1;
+  const double* params;
+  int32_t n_views, tile;
+  const or_camera* cams;
+  const double *g_mean2d, *g_conic, *g_opacity, *g_color;
+  double* grad;
+  uint8_t* visible;
+} pbwd_job;
+
+static void* project_bwd_thread(void* arg) {
+  const pbwd_job* j = (const pbwd_job*)arg;
+  project_bwd_range(j->n, j->g0, j->g1, j->params, j->n_views, j->cams, j->tile, j->g_mean2d,
+                    j->g_conic, j->g_opacity, j->g_color, j->grad, j->visible);
+  return NULL;
+}
+
+void or_project_bwd_mt(int64_t n, const double* params, int32_t n_views, const or_camera* cams,
+                       int32_t tile, const double* g_mean2d, const double* g_conic,
+                       const double* g_opacity, const double* g_color, double* grad,
+                       uint8_t* visible, int32_t threads) {
+  memset(grad, 0, sizeof(double) * OR_NPARAM * (size_t)n);
+  if (visible) memset(visible, 0, (size_t)n);
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  pbwd_job jobs[256];
+  pthread_t tid[256];
+  int started[256] = {0};
+  for (int32_t t = 0; t < threads; ++t) {
+    pbwd_job j = {n, n * t / threads, n * (t + 1) / threads, params, n_views, tile, cams,
+                  g_mean2d, g_conic, g_opacity, g_color, grad, visible};
+    jobs[t] = j;
+  }
+  for (int32_t t = 1; t < threads; ++t)
+    started[t] = pthread_create(&tid[t], NULL, project_bwd_thread, &jobs[t]) == 0;
+  project_bwd_thread(&jobs[0]);
+  for (int32_t t = 1; t < threads; ++t) {
+    if (started[t]) pthread_join(tid[t], NULL);
+    else project_bwd_thread(&jobs[t]);
+  }
+}
+
 /* ------------------------------------------------------------------------ */
-void or_adam(int64_t n_rows, int64_t n_cols, double* p, const double* g, double* m,
-             double* v, int64_t t, double lr, double beta1, double beta2, double eps,
-             const uint8_t* visible) {
+/* Adam over columns c0 <= col < c1 of every row. */
+static void adam_range(int64_t n_rows, int64_t n_cols, int64_t c0, int64_t c1, double* p,
+                       const double* g, double* m, double* v, int64_t t, double lr, double beta1,
+                       double beta2, double eps, const uint8_t* visible) {
   const double bc1 = 1.0 - pow(beta1, (double)t);
   const double bc2 = 1.0 - pow(beta2, (double)t);
   for (int64_t row = 0; row < n_rows; ++row)
-    for (int64_t col = 0; col < n_cols; ++col) {
+    for (int64_t col = c0; col < c1; ++col) {
       if (visible && !visible[col]) continue;
       const int64_t i = row * n_cols + col;
       m[i] = beta1 * m[i] + (1.0 - beta1) * g[i];
@@ -879,6 +1257,50 @@ void or_adam(int64_t n_rows, int64_t n_cols, double* p, const double* g, double*
       const double vhat = v[i] / bc2;
       p[i] -= lr * mhat / (sqrt(vhat) + eps);
     }
+}
+
+void or_adam(int64_t n_rows, int64_t n_cols, double* p, const double* g, double* m,
+             double* v, int64_t t, double lr, double beta1, double beta2, double eps,
+             const uint8_t* visible) {
+  adam_range(n_rows, n_cols, 0, n_cols, p, g, m, v, t, lr, beta1, beta2, eps, visible);
+}
+
+/* Thread split of or_adam by column range: element-wise, identical results. */
+typedef struct adam_job {
+  int64_t n_rows, n_cols, c0, c1, t;
+  double *p, *m, *v;
+  const double* g;
+  double lr, beta1, beta2, eps;
+  const uint8_t* visible;
+} adam_job;
+
+static void* adam_thread(void* arg) {
+  const adam_job* j = (const adam_job*)arg;
+  adam_range(j->n_rows, j->n_cols, j->c0, j->c1, j->p, j->g, j->m, j->v, j->t, j->lr, j->beta1,
+             j->beta2, j->eps, j->visible);
+  return NULL;
+}
+
+void or_adam_mt(int64_t n_rows, int64_t n_cols, double* p, const double* g, double* m,
+                double* v, int64_t t, double lr, double beta1, double beta2, double eps,
+                const uint8_t* visible, int32_t threads) {
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  adam_job jobs[256];
+  pthread_t tid[256];
+  int started[256] = {0};
+  for (int32_t k = 0; k < threads; ++k) {
+    adam_job j = {n_rows, n_cols, n_cols * k / threads, n_cols * (k + 1) / threads, t, p, m, v,
+                  g, lr, beta1, beta2, eps, visible};
+    jobs[k] = j;
+  }
+  for (int32_t k = 1; k < threads; ++k)
+    started[k] = pthread_create(&tid[k], NULL, adam_thread, &jobs[k]) == 0;
+  adam_thread(&jobs[0]);
+  for (int32_t k = 1; k < threads; ++k) {
+    if (started[k]) pthread_join(tid[k], NULL);
+    else adam_thread(&jobs[k]);
+  }
 }
 
 /* ------------------------------------------------------------------------ */

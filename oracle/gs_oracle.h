@@ -1,6 +1,7 @@
 /*
- * gs_oracle.h -- plain, slow, single-threaded CPU oracle for the 3D Gaussian
- * Splatting training step.  TEST INFRASTRUCTURE ONLY: the tests, the smoke
+ * gs_oracle.h -- plain, slow CPU oracle for the 3D Gaussian Splatting
+ * training step (single-threaded; the _mt variants only split the same loops
+ * over POSIX threads).  TEST INFRASTRUCTURE ONLY: the tests, the smoke
  * check and the benchmark's CPU-baseline leg may call it; the product path
  * never does.  It shares no code, header or constant table with the CUDA
  * library.
@@ -98,6 +99,12 @@ void or_bin(int64_t n, int32_t n_views, const float* mean2d, const int32_t* radi
             const float* depth, int32_t tile, int32_t width, int32_t height,
             uint64_t* keys, uint32_t* vals, int64_t* ranges);
 
+/* or_bin with the rows and the per-tile sorts split over `threads` POSIX
+ * threads; identical outputs. */
+void or_bin_mt(int64_t n, int32_t n_views, const float* mean2d, const int32_t* radius,
+               const float* depth, int32_t tile, int32_t width, int32_t height,
+               uint64_t* keys, uint32_t* vals, int64_t* ranges, int32_t threads);
+
 /* The sorted list of each selected flattened tile (view*T + tile) by brute
  * force: every row of that view whose tile rectangle covers it, ordered by
  * (float_bits(depth), id) -- the same lists or_bin produces for those tiles.
@@ -129,7 +136,8 @@ void or_prune_mask(int64_t n, int32_t n_views, int32_t width, int32_t height, in
  * (view*T + tile) indices (NULL = all tiles); untouched pixels are left as
  * they were.  Outputs: image[v][3][H][W], T_final[v][H][W],
  * n_contrib[v][H][W]; optional: pairs[v][H][W] (list entries tested before
- * the pixel stopped) and margin[v][H][W] = smallest relative distance of any
+ * the pixel stopped, the stopping entry included), included[v][H][W] (pairs
+ * composited) and margin[v][H][W] = smallest relative distance of any
  * threshold decision of the pixel (alpha vs 1/255, alpha vs 0.99, next
  * transmittance vs 1e-4) from its cut-off; +inf when nothing was tested;
  * importance[row] (optional, caller-initialised) raised to the largest
@@ -139,7 +147,17 @@ void or_raster_fwd(int64_t n, int32_t n_views, int32_t width, int32_t height, in
                    const double* color, const uint32_t* vals, const int64_t* ranges,
                    const double bg[3], const int64_t* tile_sel, int64_t n_sel,
                    double* image, double* T_final, int32_t* n_contrib, int64_t* pairs,
-                   double* margin, double* importance);
+                   int64_t* included, double* margin, double* importance);
+
+/* or_raster_fwd with the tiles split over `threads` POSIX threads (tile k
+ * of the work list on thread k mod threads); identical outputs, no
+ * importance. */
+void or_raster_fwd_mt(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
+                      const double* mean2d, const double* conic, const double* opacity,
+                      const double* color, const uint32_t* vals, const int64_t* ranges,
+                      const double bg[3], const int64_t* tile_sel, int64_t n_sel,
+                      double* image, double* T_final, int32_t* n_contrib, int64_t* pairs,
+                      int64_t* included, double* margin, int32_t threads);
 
 /* Brute mode: per pixel, every row of the view with radius > 0 whose tile
  * rectangle holds the pixel's tile, visited in (float depth bits, id) order.
@@ -165,6 +183,16 @@ void or_raster_bwd(int64_t n, int32_t n_views, int32_t width, int32_t height, in
                    int64_t n_sel, double* g_mean2d, double* g_conic, double* g_opacity,
                    double* g_color);
 
+/* or_raster_bwd with the tiles split over `threads` POSIX threads: each
+ * tile's gradients are summed per list position, then added to the rows
+ * under a lock.  Equal to or_raster_bwd up to the order of fp64 sums. */
+void or_raster_bwd_mt(int64_t n, int32_t n_views, int32_t width, int32_t height, int32_t tile,
+                      const double* mean2d, const double* conic, const double* opacity,
+                      const double* color, const uint32_t* vals, const int64_t* ranges,
+                      const double bg[3], const double* dL_dimage, const int64_t* tile_sel,
+                      int64_t n_sel, double* g_mean2d, double* g_conic, double* g_opacity,
+                      double* g_color, int32_t threads);
+
 /* Backward through projection and SH colour, summed over views:
  * grad[59][n] (overwritten); visible[n] (may be NULL) = 1 if radius > 0 in
  * any view. */
@@ -173,11 +201,23 @@ void or_project_bwd(int64_t n, const double* params, int32_t n_views, const or_c
                     const double* g_opacity, const double* g_color, double* grad,
                     uint8_t* visible);
 
+/* or_project_bwd split over `threads` POSIX threads by Gaussian; identical
+ * outputs. */
+void or_project_bwd_mt(int64_t n, const double* params, int32_t n_views, const or_camera* cams,
+                       int32_t tile, const double* g_mean2d, const double* g_conic,
+                       const double* g_opacity, const double* g_color, double* grad,
+                       uint8_t* visible, int32_t threads);
+
 /* Adam over a [rows][n_cols] array with bias correction at step t (t >= 1).
  * visible (may be NULL): per column; columns with visible == 0 keep p, m, v. */
 void or_adam(int64_t n_rows, int64_t n_cols, double* p, const double* g, double* m,
              double* v, int64_t t, double lr, double beta1, double beta2, double eps,
              const uint8_t* visible);
+
+/* or_adam split over `threads` POSIX threads by column; identical outputs. */
+void or_adam_mt(int64_t n_rows, int64_t n_cols, double* p, const double* g, double* m,
+                double* v, int64_t t, double lr, double beta1, double beta2, double eps,
+                const uint8_t* visible, int32_t threads);
 
 #ifdef __cplusplus
 }

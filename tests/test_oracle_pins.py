@@ -506,3 +506,139 @@ def test_prune_mask_hand_cases(oracle_mod):
     nc2 = np.concatenate([nc, nc])
     m = oracle_mod.prune_mask(n, 2, W, H, vals2, ranges2, nc2, imp2, 5, 2.0)
     assert np.nonzero(m)[0].tolist() == [1, 4, 5, 7]
+
+
+def _list_at_pixel(opacities, offsets, W=16, H=16, px=(3, 5)):
+    """Hand-made projected rows, all in one tile's list in the given order:
+    entry i has its mean at the centre of pixel px shifted by offsets[i]
+    (pixels) and the unit conic, so its raw alpha at px is
+    opacities[i] * exp(-|offset|^2 / 2) exactly."""
+    k = len(opacities)
+    c = np.array([px[0] + 0.5, px[1] + 0.5])
+    feats = dict(mean2d=c + np.asarray(offsets, np.float64).reshape(k, 2),
+                 conic=np.tile([1.0, 0.0, 1.0], (k, 1)), opacity=np.asarray(opacities, np.float64),
+                 color=np.full((k, 3), 0.5))
+    vals = np.arange(k, dtype=np.uint32)
+    ranges = np.array([[0, k]], np.int64)
+    return feats, vals, ranges
+
+
+def _margin_closed_form(raw):
+    """Smallest relative distance of the pixel's decisions from their cut-offs:
+    each tested alpha against 1/255 and 0.99, and each next transmittance that
+    is formed (alpha passed the 1/255 test) against 1e-4; stops at the pair
+    that would take T below 1e-4."""
+    m, T = math.inf, 1.0
+    for a_raw in raw:
+        m = min(m, abs(a_raw - 1 / 255) * 255, abs(a_raw - 0.99) / 0.99)
+        a = min(a_raw, 0.99)
+        if a < 1 / 255:
+            continue
+        Tn = T * (1 - a)
+        m = min(m, abs(Tn - 1e-4) / 1e-4)
+        if Tn < 1e-4:
+            break
+        T = Tn
+    return m
+
+
+@pytest.mark.parametrize("opac,stop,incl,last,binding", [
+    # entry 1 lies 10 px away (skipped); T = 0.4, 0.02, 4e-4, then entry 4
+    # would take it to 4e-5 < 1e-4: it stops the pixel; 0.98 is 1 % from 0.99
+    ([0.6, 0.5, 0.95, 0.98, 0.9, 0.7], 5, 3, 4, "alpha 0.99"),
+    # T = 0.1, 0.01, 1e-3, then 1e-3 * (1 - 0.902) = 0.98e-4: stop, 2 % from 1e-4
+    ([0.9, 0.5, 0.9, 0.9, 0.902, 0.3], 5, 3, 4, "T 1e-4"),
+    # alpha 0.004 is 2 % above 1/255 and composited; no stop: every entry tested
+    ([0.3, 0.5, 0.004, 0.2], 4, 3, 4, "alpha 1/255"),
+])
+def test_pairs_included_margin_closed_forms(oracle_mod, opac, stop, incl, last, binding):
+    """The per-pixel work counts and the threshold margin of the forward:
+    pairs = list entries tested up to and including the one that stops the
+    pixel (all of them when none stops), included = pairs composited,
+    margin = the decision closest to its cut-off (each cut-off made binding
+    by one case)."""
+    k = len(opac)
+    off = np.zeros((k, 2))
+    off[1] = [10.0, 0.0]  # exp(-50): skipped by the 1/255 test
+    feats, vals, ranges = _list_at_pixel(opac, off)
+    fw = oracle_mod.raster_fwd(k, 1, 16, 16, feats, vals, ranges)
+    raw = [opac[i] * math.exp(-0.5 * float(off[i] @ off[i])) for i in range(k)]
+    assert fw["pairs"][0, 5, 3] == stop
+    assert fw["included"][0, 5, 3] == incl
+    m = _margin_closed_form(raw)
+    assert fw["margin"][0, 5, 3] == pytest.approx(m, rel=1e-9)
+    # which cut-off binds, by construction
+    a_min = min(abs(r - 1 / 255) * 255 for r in raw[:stop])
+    a_max = min(abs(r - 0.99) / 0.99 for r in raw[:stop])
+    if binding == "alpha 0.99":
+        assert m == pytest.approx(a_max)
+    elif binding == "alpha 1/255":
+        assert m == pytest.approx(a_min)
+    else:
+        assert m < min(a_min, a_max)
+    # a pixel that no entry reaches: every entry tested, none composited
+    assert fw["pairs"][0, 15, 15] == k and fw["included"][0, 15, 15] == 0
+    assert fw["margin"][0, 15, 15] > 0.9
+    assert fw["n_contrib"][0, 5, 3] == last
+
+
+def test_pairs_and_included_sum_to_the_lists(oracle_mod):
+    """Without any stop, every pixel tests its whole tile list; included
+    counts exactly the pairs at or above alpha 1/255 (brute count)."""
+    cfg = scenes.make("tiny_2k_256", n_override=300)
+    pr, (keys, vals, ranges), fw = oracle_mod.render(cfg["params"], cfg["cams"])
+    lens = (ranges[:, 1] - ranges[:, 0]).reshape(16, 16)
+    # T never falls by more than the factor 1 - 0.99, so a pixel that ends at
+    # T >= 0.01 never formed a next transmittance below 1e-4: it did not stop
+    nostop = fw["T_final"][0] >= 0.01
+    assert nostop.mean() > 0.5
+    full = np.kron(lens, np.ones((16, 16), np.int64))
+    assert np.array_equal(fw["pairs"][0][nostop], full[nostop])
+    # brute count of alpha >= 1/255 over each non-stopping pixel's list
+    ys, xs = np.nonzero(nostop)
+    for y, x in list(zip(ys, xs))[::97]:
+        t = (y // 16) * 16 + x // 16
+        ids = vals[ranges[t, 0]:ranges[t, 1]]
+        d = np.array([x + 0.5, y + 0.5]) - pr["mean2d"][ids]
+        co = pr["conic"][ids]
+        power = -0.5 * (co[:, 0] * d[:, 0] ** 2 + co[:, 2] * d[:, 1] ** 2) - co[:, 1] * d[:, 0] * d[:, 1]
+        alpha = np.minimum(0.99, pr["opacity"][ids] * np.exp(power))
+        assert fw["included"][0, y, x] == int((alpha >= 1 / 255).sum())
+
+
+def test_threaded_oracle_equals_single_thread(oracle_mod):
+    """The _mt variants only split loops over threads: binning, compositing
+    forward, projection backward and Adam give identical results; compositing
+    backward equal up to the order of fp64 sums."""
+    cfg = scenes.make("tiny_2k_256", n_override=1500)
+    cams = [cfg["cams"][0], scenes.camera(np.eye(3), [0.3, -0.2, 0.5], 256, 256, 128, 128, 256, 256)]
+    p64 = cfg["params"].astype(np.float64)
+    n, V = p64.shape[1], 2
+    pr = oracle_mod.project(p64, cams)
+    m32, d32 = pr["mean2d"].astype(np.float32), pr["depth"].astype(np.float32)
+    one = oracle_mod.bin_and_sort(n, V, m32, pr["radius"], d32, 256, 256)
+    many = oracle_mod.bin_and_sort(n, V, m32, pr["radius"], d32, 256, 256, threads=7)
+    for a, b in zip(one, many):
+        assert np.array_equal(a, b)
+    keys, vals, ranges = one
+    f1 = oracle_mod.raster_fwd(n, V, 256, 256, pr, vals, ranges)
+    f7 = oracle_mod.raster_fwd(n, V, 256, 256, pr, vals, ranges, threads=7)
+    for k in f1:
+        assert np.array_equal(f1[k], f7[k]), k
+    target = scenes.target_images(V, 256, 256, 5)
+    _, g_img = oracle_mod.loss_l1(f1["image"], target)
+    b1 = oracle_mod.raster_bwd(n, V, 256, 256, pr, vals, ranges, g_img)
+    b7 = oracle_mod.raster_bwd(n, V, 256, 256, pr, vals, ranges, g_img, threads=7)
+    for k in b1:
+        assert np.abs(b7[k] - b1[k]).max() <= 1e-12 * max(1e-300, np.abs(b1[k]).max()), k
+    g1, v1 = oracle_mod.project_bwd(p64, cams, b1)
+    g7, v7 = oracle_mod.project_bwd(p64, cams, b1, threads=7)
+    assert np.array_equal(g1, g7) and np.array_equal(v1, v7)
+    rng = np.random.default_rng(2)
+    pa, ma, va = p64.copy(), np.zeros_like(p64), np.zeros_like(p64)
+    pb, mb, vb = p64.copy(), np.zeros_like(p64), np.zeros_like(p64)
+    vis = (rng.random(n) < 0.5).astype(np.uint8)
+    for t in (1, 2, 3):
+        oracle_mod.adam(pa, g1, ma, va, t, 1e-3, visible=vis)
+        oracle_mod.adam(pb, g1, mb, vb, t, 1e-3, visible=vis, threads=7)
+    assert np.array_equal(pa, pb) and np.array_equal(ma, mb) and np.array_equal(va, vb)

@@ -33,6 +33,15 @@ METRIC = "train iters/s and fwd+bwd Mpix/s at 1080p/3M Gaussians; % HBM roofline
 UNIT = "iters/s"
 
 # Algorithmic work per unit: the flops and bytes each kernel's roofline counts.
+# Compositing, the method's count (the roofline's `frac`): 14 FP32 operations
+# (+1 exp) per tested pair of the forward -- every list entry a pixel passes
+# before it stops -- and 45 (+1 exp, +1 reciprocal) per pair the backward
+# evaluates -- every list entry below the pixel's last contributor.
+FWD_FLOP_PAIR = 14
+BWD_FLOP_PAIR = 45
+# The arithmetic the method needs on those pairs (`frac_useful`): the exponent
+# and alpha test of every tested or evaluated pair, and the compositing and
+# gradient arithmetic only of the pairs that pass the 1/255 test.
 FWD_FLOP_TESTED = 13     # per tested pair: dx, dy, power, alpha (+1 exp)
 FWD_FLOP_INCLUDED = 9    # per composited pair: transmittance, weight, colour
 BWD_FLOP_EVAL = 13       # per pair visited below the last contributor (+1 exp)
@@ -221,68 +230,138 @@ def peaks():
 # CPU oracle on a bounded sample of the workload
 
 
-def oracle_sample(cfg, gauss_frac, n_tiles, seed, cache):
-    """One training step of the oracle on a bounded sample: projection,
-    binning, projection backward and Adam over a contiguous 1/`1/gauss_frac`
-    block of the Gaussians (their cost is linear in the count), compositing
-    forward and backward on `n_tiles` random non-empty tiles of the full
-    scene's lists (cost per tile).  Returns (extrapolated seconds per full
-    step, detail)."""
+SAMPLE_EVERY = 8  # the sampled oracle step: 1/8 of the Gaussians, every 8th non-empty tile
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_lists(cfg, threads, cache):
+    """The oracle's own projection and sorted lists of the whole scene (set-up
+    of the sampled step, untimed)."""
     import numpy as np
 
     import oracle
-    params = cfg["params"]
-    cams = cfg["cams"]
-    n = params.shape[1]
-    V = len(cams)
-    W, H = cams[0]["width"], cams[0]["height"]
-    if "full" not in cache:  # full lists for the tile sample (set-up, untimed)
-        pr = oracle.project(params.astype(np.float64), cams)
-        keys, vals, ranges = oracle.bin_and_sort(n, V, pr["mean2d"].astype(np.float32),
-                                                 pr["radius"], pr["depth"].astype(np.float32), W, H)
+    if "full" not in cache:
+        params, cams = cfg["params"], cfg["cams"]
+        n, V = params.shape[1], len(cams)
+        W, H = cams[0]["width"], cams[0]["height"]
+        pr = oracle.project(params.astype(np.float64), cams, threads=threads)
+        _, vals, ranges = oracle.bin_and_sort(n, V, pr["mean2d"].astype(np.float32), pr["radius"],
+                                              pr["depth"].astype(np.float32), W, H,
+                                              threads=threads)
         cache["full"] = (pr, vals, ranges)
-    pr, vals, ranges = cache["full"]
-    rng = np.random.default_rng(seed)
-    m = max(1, int(n * gauss_frac))
-    a = int(rng.integers(0, n - m + 1))
-    sub = np.ascontiguousarray(params[:, a:a + m].astype(np.float64))
+    return cache["full"]
+
+
+def oracle_step(cfg, threads, every, cache, offset=0):
+    """One training step of the CPU oracle on `threads` POSIX threads.
+
+    every = 1: the whole step (projection, binning, compositing forward, L1
+    loss, compositing backward, projection backward, Adam).  every = k > 1:
+    the sampled step -- projection, binning, projection backward and Adam on
+    a contiguous 1/k of the Gaussians (their cost is linear in the count,
+    scaled by k), compositing forward and backward on every k-th non-empty
+    tile of the whole scene's lists taken in list-length order (so the
+    sample spans the lengths, which set a tile's cost; scaled by the number
+    of non-empty tiles over the sample), the loss on the full batch.
+    Returns (seconds of a full step, seconds spent, per-stage seconds, text)."""
+    import numpy as np
+
+    import oracle
+    params, cams = cfg["params"], cfg["cams"]
+    n, V = params.shape[1], len(cams)
+    W, H = cams[0]["width"], cams[0]["height"]
     t = {}
+    if every == 1:
+        p64 = params.astype(np.float64)
+        t0 = time.perf_counter()
+        pr = oracle.project(p64, cams, threads=threads)
+        t["project"] = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        _, vals, ranges = oracle.bin_and_sort(n, V, pr["mean2d"].astype(np.float32), pr["radius"],
+                                              pr["depth"].astype(np.float32), W, H,
+                                              threads=threads)
+        t["bin"] = time.perf_counter() - t0
+        sel, sub, pr_sub, lin, tile_scale = None, p64, pr, 1.0, 1.0
+    else:
+        pr, vals, ranges = oracle_lists(cfg, threads, cache)
+        m = max(1, n // every)
+        a = (offset * m) % max(1, n - m + 1)
+        sub = np.ascontiguousarray(params[:, a:a + m].astype(np.float64))
+        t0 = time.perf_counter()
+        spr = oracle.project(sub, cams, threads=threads)
+        t["project"] = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle.bin_and_sort(m, V, spr["mean2d"].astype(np.float32), spr["radius"],
+                            spr["depth"].astype(np.float32), W, H, threads=threads)
+        t["bin"] = time.perf_counter() - t0
+        lens = ranges[:, 1] - ranges[:, 0]
+        nonempty = np.nonzero(lens > 0)[0]
+        by_len = nonempty[np.argsort(lens[nonempty], kind="stable")]
+        sel = np.sort(by_len[offset % every::every])
+        lin = n / m
+        tile_scale = nonempty.size / max(1, sel.size)
     t0 = time.perf_counter()
-    spr = oracle.project(sub, cams)
-    t["project"] = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    oracle.bin_and_sort(m, V, spr["mean2d"].astype(np.float32), spr["radius"],
-                        spr["depth"].astype(np.float32), W, H)
-    t["bin"] = time.perf_counter() - t0
-    nonempty = np.nonzero(ranges[:, 1] > ranges[:, 0])[0]
-    sel = rng.choice(nonempty, min(n_tiles, nonempty.size), replace=False)
-    t0 = time.perf_counter()
-    fw = oracle.raster_fwd(n, V, W, H, pr, vals, ranges, tile_sel=sel)
+    fw = oracle.raster_fwd(n, V, W, H, pr, vals, ranges, tile_sel=sel, threads=threads)
     t["raster_fwd"] = time.perf_counter() - t0
     t0 = time.perf_counter()
     loss, g_img = oracle.loss_l1(fw["image"], cfg["target"])
     t["loss"] = time.perf_counter() - t0
     t0 = time.perf_counter()
-    g2 = oracle.raster_bwd(n, V, W, H, pr, vals, ranges, g_img, tile_sel=sel)
+    g2 = oracle.raster_bwd(n, V, W, H, pr, vals, ranges, g_img, tile_sel=sel, threads=threads)
     t["raster_bwd"] = time.perf_counter() - t0
-    sg2 = {k: np.ascontiguousarray(v.reshape(V, n, -1)[:, a:a + m].reshape(V * m, -1).squeeze())
-           for k, v in g2.items()}
+    if every != 1:
+        g2 = {k: np.ascontiguousarray(v.reshape(V, n, -1)[:, a:a + m].reshape(V * m, -1).squeeze())
+              for k, v in g2.items()}
     t0 = time.perf_counter()
-    grad, _ = oracle.project_bwd(sub, cams, sg2)
+    grad, _ = oracle.project_bwd(sub, cams, g2, threads=threads)
     t["project_bwd"] = time.perf_counter() - t0
     mm, vv = np.zeros_like(sub), np.zeros_like(sub)
     t0 = time.perf_counter()
-    oracle.adam(sub, grad, mm, vv, 1, cfg["lr"])
+    oracle.adam(sub, grad, mm, vv, 1, cfg["lr"], threads=threads)
     t["adam"] = time.perf_counter() - t0
-    lin = 1.0 / (m / n)
-    tile_scale = nonempty.size / sel.size
     full = ((t["project"] + t["bin"] + t["project_bwd"] + t["adam"]) * lin +
             (t["raster_fwd"] + t["raster_bwd"]) * tile_scale + t["loss"])
-    sample = ("oracle step: projection, binning, projection backward and Adam on %d of %d "
-              "Gaussians (x%.0f), compositing fwd+bwd on %d of %d non-empty tiles (x%.1f), "
-              "L1 loss on the full batch; 1 thread" % (m, n, lin, sel.size, nonempty.size,
-                                                     tile_scale))
-    return full, sum(t.values()), sample, t
+    if every == 1:
+        text = "full oracle step (all stages over the whole workload); %d threads" % threads
+    else:
+        text = ("sampled oracle step: projection, binning, projection backward and Adam on "
+                "%d of %d Gaussians (x%.0f), compositing fwd+bwd on every %dth of %d non-empty "
+                "tiles in list-length order (%d tiles, x%.2f), L1 loss on the full batch; "
+                "%d threads" % (m, n, lin, every, nonempty.size, sel.size, tile_scale, threads))
+    return full, sum(t.values()), t, text
+
+
+# full oracle steps on all cores for the workloads whose step fits in about
+# half a minute on the host (3M Gaussians x 4 views takes ~15-30 s)
+FULL_ORACLE_STEP = {"tiny_2k_256", "small_200k_1024x768", "ring_3m_4x1080p"}
+
+
+def cpu_baseline(cfg, workload):
+    """The oracle timed on the host's cores: the whole step on all cores
+    where it fits (value), and the sampled step on all cores and on one
+    thread (extra keys).  Too large workloads (the oracle's lists of 20M x 4K
+    need ~80 GB of host memory) are not timed."""
+    if workload not in FULL_ORACLE_STEP:
+        return None
+    cores = host_cores()
+    cache = {}
+    full, wall, stages, text = oracle_step(cfg, cores, 1, cache)
+    out = {"value": 1.0 / full, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": text,
+           "step_s": round(full, 3), "stages_s": {k: round(v, 3) for k, v in stages.items()}}
+    if workload == WORKLOAD:
+        s_full, s_wall, _, s_text = oracle_step(cfg, cores, SAMPLE_EVERY, cache)
+        o_full, o_wall, _, o_text = oracle_step(cfg, 1, SAMPLE_EVERY, cache)
+        out["sampled_all_cores"] = {"value": 1.0 / s_full, "step_s": round(s_full, 3),
+                                    "wall_s": round(s_wall, 2), "sample": s_text}
+        out["one_thread"] = {"value": 1.0 / o_full, "step_s": round(o_full, 3),
+                             "wall_s": round(o_wall, 2), "sample": o_text}
+    return out
 
 
 def reference_arm(args, rank, world):
@@ -290,21 +369,22 @@ def reference_arm(args, rank, world):
         return
     import scenes
     cfg = scenes.make(args.workload, n_override=args.gaussians)
+    cores = host_cores()
     cache = {}
-    walls, fulls = [], []
-    sample = ""
+    every = 1 if args.workload in ("tiny_2k_256", "small_200k_1024x768") else SAMPLE_EVERY
+    fulls = []
+    text = ""
     for i in range(args.warmup + args.steps):
-        full, wall, sample, _ = oracle_sample(cfg, 1.0 / 16, 16, 100 + i, cache)
+        full, _, _, text = oracle_step(cfg, cores, every, cache, offset=i)
         if i >= args.warmup:
             fulls.append(full)
-            walls.append(wall)
     sec = sum(fulls) / len(fulls)
     value = 1.0 / sec
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": args.workload},
-            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample, "value": value,
+            "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": text, "value": value,
                              "unit": UNIT},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -508,9 +588,13 @@ def our_arm(args, rank, world, local):
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
     fp32_peak_tflops = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
-    fwd_flops = FWD_FLOP_TESTED * tested + FWD_FLOP_INCLUDED * included
-    bwd_flops = BWD_FLOP_EVAL * bwd_eval + BWD_FLOP_INCLUDED * included
+    fwd_flops = FWD_FLOP_PAIR * tested
+    bwd_flops = BWD_FLOP_PAIR * bwd_eval
+    useful = {"rasterize_fwd": FWD_FLOP_TESTED * tested + FWD_FLOP_INCLUDED * included,
+              "rasterize_bwd": BWD_FLOP_EVAL * bwd_eval + BWD_FLOP_INCLUDED * included}
+    useful["rasterize_fused"] = useful["rasterize_fwd"] + useful["rasterize_bwd"]
     rows = V * n
+    adam_cols = int(step.visible.sum().item()) if cfg["sparse_adam"] else n
     kern = {
         "rasterize_fwd": ("alu", fwd_flops / 1e12, "TFLOP/s", fp32_peak_tflops),
         "rasterize_bwd": ("alu", bwd_flops / 1e12, "TFLOP/s", fp32_peak_tflops),
@@ -521,7 +605,7 @@ def our_arm(args, rank, world, local):
         "loss_l1": ("hbm", LOSS_BYTES * V * W * H / 1e9, "GB/s", hbm_peak),
         "project_bwd": ("hbm", (PROJ_BWD_BYTES * n + PROJ_BWD_ROW * visible_rows) / 1e9, "GB/s",
                         hbm_peak),
-        "adam": ("hbm", ADAM_BYTES * n / 1e9, "GB/s", hbm_peak),
+        "adam": ("hbm", ADAM_BYTES * adam_cols / 1e9, "GB/s", hbm_peak),
     }
     if fused:
         # one kernel does the forward, the loss and the backward
@@ -537,6 +621,10 @@ def our_arm(args, rank, world, local):
         kernels[nm] = {"ms": round(per_kernel[nm], 4), "bound": bound, "achieved": round(ach, 3),
                        "peak": round(peak, 2), "unit": unit, "frac": round(ach / peak, 4),
                        "traffic": traffic_of(nm, args.workload, variant)}
+        if nm in useful:
+            u = useful[nm] / 1e12 / (per_kernel[nm] / 1e3)
+            kernels[nm]["achieved_useful"] = round(u, 3)
+            kernels[nm]["frac_useful"] = round(u / peak, 4)
     dom = max(kern, key=lambda k: per_kernel[k])
     d = kernels[dom]
     roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
@@ -544,6 +632,13 @@ def our_arm(args, rank, world, local):
                 "traffic": traffic_of(dom, args.workload, variant),
                 "peak_source": (peak_kind + " HBM copy") if d["bound"] == "hbm" else
                 ("FP32 lanes x 2 x median SM clock %.0f MHz, %d SMs" % (sm_mhz, sms))}
+    if "frac_useful" in d:
+        roofline["frac_useful"] = d["frac_useful"]
+        roofline["work"] = ("%d flop per tested pair + %d per backward pair (frac); useful: "
+                            "%d per tested + %d per composited pair forward, %d per evaluated + "
+                            "%d per contributing pair backward (frac_useful)" %
+                            (FWD_FLOP_PAIR, BWD_FLOP_PAIR, FWD_FLOP_TESTED, FWD_FLOP_INCLUDED,
+                             BWD_FLOP_EVAL, BWD_FLOP_INCLUDED))
     raster_ms = (per_kernel["rasterize_fused"] if fused else
                  per_kernel["rasterize_fwd"] + per_kernel["loss_l1"] + per_kernel["rasterize_bwd"])
     line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
@@ -568,13 +663,14 @@ def our_arm(args, rank, world, local):
             "eager_ms_per_step": round(eager_ms_step, 4),
             "prune": prune_info,
             "work": {"pairs_tested_fwd": tested, "pairs_included": included,
-                     "pairs_bwd": bwd_eval, "visible_rows": visible_rows},
+                     "pairs_bwd": bwd_eval, "visible_rows": visible_rows,
+                     "adam_columns": adam_cols},
             "loss_first_last": [round(losses[0], 6), round(losses[-1], 6)],
             "clocks": clock_info}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        full, wall, sample, _ = oracle_sample(cfg, 1.0 / 8, 64, 7, {})
-        line["cpu_baseline"] = {"value": 1.0 / full, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": sample, "sample_wall_s": round(wall, 2)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not variant:
+        cb = cpu_baseline(cfg, args.workload)
+        if cb is not None:
+            line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -63,7 +63,7 @@ def lib():
     L.gs_tile_order.argtypes = [i64, vp, vp, vp]
     L.gs_rasterize_fwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     L.gs_rasterize_fwd_counted.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
-                                           vp]
+                                           vp, vp]
     L.gs_loss_l1.argtypes = [vp, vp, i64, vp, vp, vp]
     L.gs_rasterize_bwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.gs_morton_workspace_bytes.argtypes = [i64]
@@ -77,7 +77,9 @@ def lib():
     L.gs_compact_workspace_bytes.restype = sz
     L.gs_compact_index.argtypes = [i64, vp, vp, sz, vp, vp, vp]
     L.gs_rasterize_fused.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                     vp, vp]
+                                     vp, vp, sz, vp]
+    L.gs_rasterize_workspace_bytes.argtypes = [i32, i32, i32, i64]
+    L.gs_rasterize_workspace_bytes.restype = sz
     L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp]
     L.gs_adam_step.argtypes = [i64, vp, vp, vp, vp, i64, f32, f32, f32, f32, vp, vp]
     L.gs_status_string.argtypes = [C.c_int]
@@ -228,7 +230,7 @@ def gs_rasterize_fwd(n, n_views, splats, width, height, vals, ranges, bg, image,
 
 
 def gs_rasterize_fwd_counted(n, n_views, splats, width, height, vals, ranges, bg, image, T_final,
-                             n_contrib, counts, stream=None, tile_order=None):
+                             n_contrib, counts, stream=None, tile_order=None, pixel_counts=None):
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
     _check("gs_rasterize_fwd_counted", lib().gs_rasterize_fwd_counted(
         n, n_views, _dev(splats, torch.float32, "splats"), width, height,
@@ -236,7 +238,7 @@ def gs_rasterize_fwd_counted(n, n_views, splats, width, height, vals, ranges, bg
         _dev(tile_order, torch.int32, "tile_order"), C.cast(bgv, C.c_void_p),
         _dev(image, torch.float32, "image"), _dev(T_final, torch.float32, "T_final"),
         _dev(n_contrib, torch.int32, "n_contrib"), _dev(counts, torch.int64, "counts"),
-        _stream(stream)))
+        _dev(pixel_counts, torch.int32, "pixel_counts"), _stream(stream)))
 
 
 def gs_loss_l1(image, target, loss, dL_dimage, stream=None):
@@ -259,8 +261,15 @@ def gs_rasterize_bwd(n, n_views, splats, width, height, vals, ranges, bg, T_fina
         _stream(stream)))
 
 
+def gs_rasterize_workspace_bytes(n_views, width, height, capacity):
+    return int(lib().gs_rasterize_workspace_bytes(n_views, width, height, capacity))
+
+
 def gs_rasterize_fused(n, n_views, splats, width, height, vals, ranges, bg, target, image,
-                       T_final, n_contrib, loss, grads, stream=None, tile_order=None):
+                       T_final, n_contrib, loss, grads, stream=None, tile_order=None,
+                       workspace=None):
+    """workspace: None, or a CUDA uint8 tensor of gs_rasterize_workspace_bytes()
+    bytes (the backward then walks the pairs the forward composited)."""
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
     _check("gs_rasterize_fused", lib().gs_rasterize_fused(
         n, n_views, _dev(splats, torch.float32, "splats"), width, height,
@@ -268,7 +277,9 @@ def gs_rasterize_fused(n, n_views, splats, width, height, vals, ranges, bg, targ
         _dev(tile_order, torch.int32, "tile_order"), C.cast(bgv, C.c_void_p),
         _dev(target, torch.float32, "target"), _dev(image, torch.float32, "image"),
         _dev(T_final, torch.float32, "T_final"), _dev(n_contrib, torch.int32, "n_contrib"),
-        _dev(loss, torch.float32, "loss"), _dev(grads, torch.float32, "grads"), _stream(stream)))
+        _dev(loss, torch.float32, "loss"), _dev(grads, torch.float32, "grads"),
+        _dev(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
 def gs_morton_workspace_bytes(n):
@@ -404,6 +415,10 @@ class TrainStep:
         self.vals = torch.empty(max(self.capacity, 1), device=dev, dtype=torch.int32)
         ws = gs_bin_workspace_bytes(self.V * self.n, self.capacity)
         self.workspace = torch.zeros(ws, device=dev, dtype=torch.uint8)  # zeroed header
+        # the fused compositing's per-batch records of the composited pairs
+        self.raster_ws = torch.empty(gs_rasterize_workspace_bytes(self.V, self.W, self.H,
+                                                                  self.capacity),
+                                     device=dev, dtype=torch.uint8)
 
     # the seven library calls of a step, in order
     def project(self, stream=None):
@@ -441,7 +456,8 @@ class TrainStep:
     def rasterize_fused(self, stream=None):
         gs_rasterize_fused(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges,
                            self.bg, self.target, self.image, self.T_final, self.n_contrib,
-                           self.loss, self.grads2d, stream, tile_order=self.tile_order)
+                           self.loss, self.grads2d, stream, tile_order=self.tile_order,
+                           workspace=self.raster_ws)
 
     def project_bwd(self, stream=None):
         gs_project_bwd(self.params, self.cams, self.splats, self.grads2d, self.grad, self.visible,

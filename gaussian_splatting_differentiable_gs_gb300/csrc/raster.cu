@@ -217,28 +217,14 @@ __device__ __forceinline__ bool box_hits(char4 b, int x0, int x1, int y0, int y1
   return !(b.y < x0 || b.x > x1 || b.w < y0 || b.z > y1);
 }
 
-// Writes into wl[0..] the entries j < cnt (ascending) whose box meets the
-// grid-index rectangle [x0, x1] x [y0, y1]; returns their number.  Whole-warp
-// call.
-__device__ __forceinline__ int warp_sublist(const Batch& B, int cnt, int x0, int x1, int y0,
-                                            int y1, uint8_t* wl, int lane) {
-  int n = 0;
-  for (int c0 = 0; c0 < cnt; c0 += 32) {
-    const int j = c0 + lane;
-    const bool hit = j < cnt && box_hits(B.box[j], x0, x1, y0, y1);
-    const unsigned bal = __ballot_sync(0xffffffffu, hit);
-    if (hit) wl[n + __popc(bal & ((1u << lane) - 1u))] = (uint8_t)j;
-    n += __popc(bal);
-  }
-  __syncwarp();
-  return n;
-}
-
-// Pixel p of the tile (0..255), in 8x4 blocks per warp.
+// Pixel p of the tile (0..255): warp w = p >> 5 covers an 8x4 block and each
+// quarter of the warp (lanes 8q..8q+7) a 4x2 block of it -- quarters 0, 1 on
+// top (left, right), 2, 3 below -- so that the eight lanes of a quarter form
+// one phase of a 128-bit shared-memory access.
 __device__ __forceinline__ void pixel_of(int p, int tile_x, int tile_y, int& px, int& py) {
-  const int warp = p >> 5, lane = p & 31;
-  px = tile_x * GS_TILE + (warp & 1) * 8 + (lane & 7);
-  py = tile_y * GS_TILE + (warp >> 1) * 4 + (lane >> 3);
+  const int warp = p >> 5, q = (p >> 3) & 3, r = p & 7;
+  px = tile_x * GS_TILE + (warp & 1) * 8 + (q & 1) * 4 + (r & 3);
+  py = tile_y * GS_TILE + (warp >> 1) * 4 + (q >> 1) * 2 + (r >> 2);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -247,30 +233,33 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Warp sum of 8 values by recursive halving: at each of three exchange
-// rounds a lane keeps half of its values and sends the other half to its
-// partner, then two plain rounds finish.  9 shuffles instead of 40.  Lane L
-// returns the warp sum of value ((L>>4)&1)*4 + ((L>>3)&1)*2 + ((L>>2)&1).
-__device__ __forceinline__ float warp_sum8(const float v[8], int lane) {
-  const bool h1 = lane & 16, h2 = lane & 8, h3 = lane & 4;
+// Sums over the eight lanes of a quarter.  quarter_sum8 reduces 8 values by
+// recursive halving (at each of three exchange rounds a lane keeps half of its
+// values and sends the other half to its partner: 7 shuffles); lane r of the
+// quarter (r = lane & 7) returns the quarter's sum of value r.
+__device__ __forceinline__ float quarter_sum8(const float v[8], int lane) {
+  const bool h1 = lane & 4, h2 = lane & 2, h3 = lane & 1;
   float k1[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float keep = h1 ? v[4 + i] : v[i];
     const float send = h1 ? v[i] : v[4 + i];
-    k1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    k1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
   }
   float k2[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const float keep = h2 ? k1[2 + i] : k1[i];
     const float send = h2 ? k1[i] : k1[2 + i];
-    k2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    k2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
   }
-  float k3 = (h3 ? k2[1] : k2[0]) + __shfl_xor_sync(0xffffffffu, h3 ? k2[0] : k2[1], 4);
-  k3 += __shfl_xor_sync(0xffffffffu, k3, 2);
-  k3 += __shfl_xor_sync(0xffffffffu, k3, 1);
-  return k3;
+  return (h3 ? k2[1] : k2[0]) + __shfl_xor_sync(0xffffffffu, h3 ? k2[0] : k2[1], 1);
+}
+
+__device__ __forceinline__ float quarter_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  return v + __shfl_xor_sync(0xffffffffu, v, 1);
 }
 
 // Pixel state of a tile during the forward pass, by pixel index.
@@ -292,15 +281,34 @@ __device__ __forceinline__ void pix_init(PixState& P, int tid, int tile_x, int t
   P.done[tid] = (px < W && py < H) ? 0 : 1;
 }
 
+// Writes into wl[0..] the entries j < cnt (ascending) whose box meets the
+// grid-index rectangle [x0, x1] x [y0, y1]; returns their number.  Whole-warp
+// call.
+__device__ __forceinline__ int warp_sublist(const Batch& B, int cnt, int x0, int x1, int y0,
+                                            int y1, uint8_t* wl, int lane) {
+  int n = 0;
+  for (int c0 = 0; c0 < cnt; c0 += 32) {
+    const int j = c0 + lane;
+    const bool hit = j < cnt && box_hits(B.box[j], x0, x1, y0, y1);
+    const unsigned bal = __ballot_sync(0xffffffffu, hit);
+    if (hit) wl[n + __popc(bal & ((1u << lane) - 1u))] = (uint8_t)j;
+    n += __popc(bal);
+  }
+  __syncwarp();
+  return n;
+}
+
 // Forward compositing of staged batch k over the m open pixels packed in
 // P.list[0..m): each worker thread takes one open pixel; each warp walks the
-// entries whose box meets its pixels.
+// entries whose box meets its pixels.  With `rec`, every composited pair also
+// sets bit j of the record of its pixel's 4x2 quarter (p >> 3).
 template <bool kCount, bool kImp>
 __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* wl, int cnt, int k,
                                           int m, int tile_x, int tile_y, int tid, int warp,
                                           int lane, unsigned long long& n_tested,
                                           unsigned long long& n_included, const uint32_t* ids,
-                                          float* imp) {
+                                          float* imp, int32_t* pix_counts, int64_t plane,
+                                          int32_t W, uint32_t (*rec)[8]) {
   if (warp * 32 >= m) return;
   const bool worker = tid < m;
   const int p = worker ? P.list[tid] : 0;
@@ -323,6 +331,7 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
   int32_t last = P.last[p];
   int done = 0;
   int stop_j = cnt;
+  int32_t n_inc = 0;
   const int32_t base1 = k * kRT + 1;  // 1-based list position of entry 0
   for (int i = 0; i < nw; ++i) {
     const int j = wl[i];
@@ -347,11 +356,20 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
     Tl = __fsub_rn(lo, __fsub_rn(Tn, ph));
     Tr = Tn;
     last = base1 + j;
-    if (kCount) ++n_included;
+    if (kCount) ++n_inc;
+    if (rec) atomicOr(&rec[p >> 3][j >> 5], 1u << (j & 31));
     // largest blending weight of the Gaussian (w >= 0: the bits order as the values)
     if (kImp) atomicMax(reinterpret_cast<unsigned int*>(imp + ids[j]), __float_as_uint(w));
   }
-  if (kCount) n_tested += stop_j;
+  if (kCount) {
+    n_tested += stop_j;
+    n_included += n_inc;
+    if (pix_counts) {  // this batch's share of the pixel's tested / composited pairs
+      const int64_t q = (int64_t)py * W + px;
+      atomicAdd(pix_counts + q, stop_j);
+      atomicAdd(pix_counts + plane + q, n_inc);
+    }
+  }
   P.T[p] = Tr;
   P.Tl[p] = Tl;
   P.C0[p] = __fadd_rn(P.C0[p], C0);
@@ -380,7 +398,10 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
                                          int tile_y, float ox, float oy, int tid, int warp,
                                          int lane, int2& staged,
                                          unsigned long long& n_tested,
-                                         unsigned long long& n_included, float* imp = nullptr) {
+                                         unsigned long long& n_included, float* imp = nullptr,
+                                         int32_t* pix_counts = nullptr, int64_t plane = 0,
+                                         int32_t W = 0, uint32_t (*rec)[8] = nullptr,
+                                         uint32_t* __restrict__ rec_out = nullptr) {
   const int64_t len = end - start;
   const int nb = (int)((len + kRT - 1) / kRT);
   staged = make_int2(-1, -1);
@@ -423,8 +444,13 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
     if ((bal >> lane) & 1u) P.list[off + __popc(bal & ((1u << lane) - 1u))] = tid;
     __syncthreads();
     fwd_batch<kCount, kImp>(P, B, wl[warp], cnt, k, m, tile_x, tile_y, tid, warp, lane, n_tested,
-                            n_included, ids ? ids[k & 1] : nullptr, imp);
+                            n_included, ids ? ids[k & 1] : nullptr, imp, pix_counts, plane, W,
+                            rec_out ? rec : nullptr);
     __syncthreads();  // pixel state written; slot k & 1 free for batch k + 2
+    if (rec_out) {  // this batch's record of the composited entries, per quarter
+      __stcg(rec_out + (int64_t)k * kRT + tid, (&rec[0][0])[tid]);
+      (&rec[0][0])[tid] = 0u;
+    }
     bal = __ballot_sync(0xffffffffu, !P.done[tid]);
     if (lane == 0) wcount[warp] = __popc(bal);
   }
@@ -432,21 +458,70 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
   __syncthreads();
 }
 
-// Backward pairs of staged entries [0, jtop) of one batch (list positions
-// lo + j) for this thread's pixel, back to front; per-entry sums into acc.
-__device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint8_t* wl, int jtop,
-                                          int lo, int wx0, int wx1, int wy0, int wy1, float ix,
-                                          float iy, int last, float& Tr, float& S0, float& S1,
-                                          float& S2, float g0, float g1, float g2, int lane) {
-  const int nw = warp_sublist(B, jtop, wx0, wx1, wy0, wy1, wl, lane);
-  for (int i = nw - 1; i >= 0; --i) {
-    const int j = wl[i];
+// Backward pairs of one staged batch (list positions lo + j, j < cnt) for
+// this thread's pixel, back to front; per-entry sums into acc.
+//
+// Each quarter of the warp walks its own sub-list: the entries whose box
+// meets the quarter's 4x2 block and that lie below the quarter's last
+// contributor (qlast[q]), kept as a 256-bit mask qm[q][0..7] (bit j of word
+// j >> 5).  The four quarters advance together, one entry each per step, so
+// a step costs the longest of four short lists rather than one list for the
+// whole 8x4 block, and a pair's gradient is reduced over the quarter's eight
+// lanes (10 shuffles) instead of the warp's 32.  A quarter that has no
+// entry left, or no contributing lane, adds nothing.
+__device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint32_t (*qm)[8],
+                                          const int32_t* qlast, int cnt, int lo, int wx0, int wy0,
+                                          float ix, float iy, int last, float& Tr, float& S0,
+                                          float& S1, float& S2, float g0, float g1, float g2,
+                                          int lane, const uint32_t* __restrict__ contrib) {
+  const int q = (lane >> 3) & 3, r = lane & 7;
+  // entries below each quarter's last contributor, and the chunks of 32 to scan
+  const int4 ql = *reinterpret_cast<const int4*>(qlast);
+  const int t0 = max(0, min(cnt, ql.x - lo)), t1 = max(0, min(cnt, ql.y - lo));
+  const int t2 = max(0, min(cnt, ql.z - lo)), t3 = max(0, min(cnt, ql.w - lo));
+  const int nchunk = (max(max(t0, t1), max(t2, t3)) + 31) >> 5;
+  if (contrib) {
+    // the forward's record of this warp's quarters: the entries composited
+    // into at least one pixel of the quarter (word w of quarter q is
+    // contrib[q * 8 + w]); they are exactly the pairs this walk can use
+    qm[q][lane & 7] = __ldcg(contrib + lane);
+  } else {
+    for (int c = 0; c < nchunk; ++c) {
+      const int j = (c << 5) + lane;
+      const char4 bx = B.box[j];  // j < 256; entries >= cnt are excluded by the tops
+      const bool xl = !(bx.y < wx0 || bx.x > wx0 + 3), xr = !(bx.y < wx0 + 4 || bx.x > wx0 + 7);
+      const bool yt = !(bx.w < wy0 || bx.z > wy0 + 1), yb = !(bx.w < wy0 + 2 || bx.z > wy0 + 3);
+      const unsigned b0 = __ballot_sync(0xffffffffu, xl && yt && j < t0);
+      const unsigned b1 = __ballot_sync(0xffffffffu, xr && yt && j < t1);
+      const unsigned b2 = __ballot_sync(0xffffffffu, xl && yb && j < t2);
+      const unsigned b3 = __ballot_sync(0xffffffffu, xr && yb && j < t3);
+      if (lane == 0) {
+        qm[0][c] = b0;
+        qm[1][c] = b1;
+        qm[2][c] = b2;
+        qm[3][c] = b3;
+      }
+    }
+  }
+  __syncwarp();
+  int wi = nchunk - 1;
+  uint32_t bits = wi >= 0 ? qm[q][wi] : 0u;
+  while (true) {
+    while (bits == 0u && wi > 0) bits = qm[q][--wi];
+    const bool act = bits != 0u;
+    if (!__any_sync(0xffffffffu, act)) break;
+    int j = 0;
+    if (act) {
+      const int b = 31 - __clz(bits);
+      bits ^= 1u << b;
+      j = (wi << 5) | b;
+    }
     const int pos = lo + j;
     float v[9];
 #pragma unroll
     for (int c = 0; c < 9; ++c) v[c] = 0.f;
     bool contrib = false;
-    if (pos < last) {
+    if (act && pos < last) {
       const float4 A = B.a[j];
       const float4 Bv = B.b[j];
       float lx, ly;
@@ -486,20 +561,29 @@ __device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint8
         }
       }
     }
-    // reduced across the warp even for one or two contributing lanes: their
-    // nine shared atomics on the same addresses would serialise, and cost
-    // more than the shuffles (measured); values 0..7 end on lanes
-    // 0,4,...,28 (one shared atomic each), value 8 by a plain butterfly
-    if (__any_sync(0xffffffffu, contrib)) {
-      const float s8 = warp_sum8(v, lane);
-      const float s9 = warp_sum(v[8]);
-      if ((lane & 3) == 0) {
-        const int c = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-        atomicAdd(&acc[j][c], s8);
+    const unsigned bal = __ballot_sync(0xffffffffu, contrib);
+    if (bal) {
+      // value r of the quarter ends on lane r (one shared atomic each), value
+      // 8 on every lane; only quarters with a contributing lane add
+      const float s8 = quarter_sum8(v, lane);
+      const float s9 = quarter_sum(v[8]);
+      if ((bal >> (lane & 24)) & 0xffu) {
+        atomicAdd(&acc[j][r], s8);
+        if (r == 0) atomicAdd(&acc[j][8], s9);
       }
-      if (lane == 0) atomicAdd(&acc[j][8], s9);
     }
   }
+  __syncwarp();
+}
+
+// The last contributor of each quarter of the warp (the largest `last` over
+// its eight pixels) into qlast[0..3]; whole-warp call.
+__device__ __forceinline__ void quarter_last(int last, int32_t* qlast, int lane) {
+  int m = max(last, __shfl_xor_sync(0xffffffffu, last, 4));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  if ((lane & 7) == 0) qlast[lane >> 3] = m;
+  __syncwarp();
 }
 
 // Flush of a batch's per-entry sums (entries tid < cnt) into the row
@@ -557,7 +641,7 @@ __global__ void __launch_bounds__(kRT, 6) raster_fwd_kernel(
     const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges,
     const uint32_t* __restrict__ tile_order, float bg0, float bg1, float bg2, float* __restrict__ image, float* __restrict__ T_final,
     int32_t* __restrict__ n_contrib, unsigned long long* __restrict__ counts,
-    float* __restrict__ imp) {
+    int32_t* __restrict__ pix_counts, float* __restrict__ imp) {
   __shared__ FwdSmem<kImp> S;
   unsigned long long n_tested = 0, n_included = 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -572,7 +656,9 @@ __global__ void __launch_bounds__(kRT, 6) raster_fwd_kernel(
                          nullptr, S.wl, S.wcount,
                          splats + 3 * view * n, vals, n, ranges[2 * flat], ranges[2 * flat + 1],
                          tile_x, tile_y, ox, oy, tid, warp, lane, staged, n_tested, n_included,
-                         kImp ? imp + view * n : nullptr);
+                         kImp ? imp + view * n : nullptr,
+                         pix_counts ? pix_counts + view * (int64_t)W * H : nullptr,
+                         (int64_t)gridDim.x / T * W * H, W);
   {
     int px, py;
     pixel_of(tid, tile_x, tile_y, px, py);
@@ -605,7 +691,8 @@ struct BwdSmem {
   float2 e[2][kRT];  // e = z - m of the staged entries
   uint32_t id[2][kRT];
   float acc[kRT][9];
-  uint8_t wl[kWarps][kRT];
+  uint32_t qm[kWarps][4][8];     // per-quarter entry masks of the batch
+  alignas(16) int32_t qlast[kWarps][4];  // per-quarter last contributor
   int max_last;
 };
 
@@ -625,9 +712,8 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
   pixel_of(tid, tile_x, tile_y, px, py);
   const bool inside = px < W && py < H;
   const float ix = (float)(px - tile_x * GS_TILE), iy = (float)(py - tile_y * GS_TILE);
-  // grid-index rectangle of this warp's 8x4 block
-  const int wx0 = (warp & 1) * 8, wx1 = wx0 + 7;
-  const int wy0 = (warp >> 1) * 4, wy1 = wy0 + 3;
+  // grid-index origin of this warp's 8x4 block
+  const int wx0 = (warp & 1) * 8, wy0 = (warp >> 1) * 4;
   const int64_t start = ranges[2 * flat];
   const int64_t HW = (int64_t)W * H;
   const int64_t pix = (int64_t)py * W + px;
@@ -646,6 +732,7 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
   __syncthreads();
   const int warp_last = __reduce_max_sync(0xffffffffu, last);
   if (lane == 0) atomicMax(&S.max_last, warp_last);
+  quarter_last(last, S.qlast[warp], lane);
   __syncthreads();
   const int max_last = S.max_last;
   const int nb = (max_last + kRT - 1) / kRT;
@@ -681,10 +768,8 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
     float2* E = S.e[k & 1];
     if (tid < cnt) stage_entry(B, tid, ox, oy, E);
     __syncthreads();
-    // positions at or above the warp's last contributor cannot contribute
-    const int jtop = max(0, min(cnt, warp_last - lo));
-    bwd_batch(B, S.acc, S.wl[warp], jtop, lo, wx0, wx1, wy0, wy1, ix, iy, last, Tr, S0, S1, S2,
-              g0, g1, g2, lane);
+    bwd_batch(B, S.acc, S.qm[warp], S.qlast[warp], cnt, lo, wx0, wy0, ix, iy, last, Tr, S0, S1,
+              S2, g0, g1, g2, lane, nullptr);
     __syncthreads();
     bwd_flush(B, E, S.id[k & 1], S.acc, cnt, grads + 3 * view * n, tid);
     __syncthreads();
@@ -707,10 +792,17 @@ struct FusedSmem {
   float2 e[2][kRT];
   uint32_t id[2][kRT];
   union {
-    PixState px;        // forward
-    float acc[kRT][9];  // backward
+    struct {
+      PixState px;
+      uint32_t rec[kRT / 8][8];  // the batch's composited entries per quarter
+    } fw;  // forward
+    struct {
+      float acc[kRT][9];
+      uint32_t qm[kWarps][4][8];
+      alignas(16) int32_t qlast[kWarps][4];
+    } bw;  // backward
   } u;
-  uint8_t wl[kWarps][kRT];
+  uint8_t wl[kWarps][kRT];   // forward: per-warp entry sub-lists
   int32_t wcount[kWarps];
   float lsum[kWarps];
   int max_last;
@@ -721,7 +813,7 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
     const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges,
     const uint32_t* __restrict__ tile_order, float bg0, float bg1, float bg2, const float* __restrict__ target, float inv_count, float* __restrict__ image,
     float* __restrict__ T_final, int32_t* __restrict__ n_contrib, float* __restrict__ loss,
-    float4* __restrict__ grads) {
+    float4* __restrict__ grads, uint32_t* __restrict__ recs, int64_t rec_slots) {
   __shared__ FusedSmem S;
   unsigned long long n_tested = 0, n_included = 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -732,25 +824,34 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
   const float ox = (float)(tile_x * GS_TILE), oy = (float)(tile_y * GS_TILE);
   const int64_t start = ranges[2 * flat], end = ranges[2 * flat + 1];
   const float4* vsplat = splats + 3 * view * n;
-  pix_init(S.u.px, tid, tile_x, tile_y, W, H);
+  pix_init(S.u.fw.px, tid, tile_x, tile_y, W, H);
+  // the workspace keeps, per batch of the tile, which entries the forward
+  // composited into each 4x2 quarter (1 KB, slot g = start / 256 + k + flat:
+  // distinct for every (tile, batch) since the lists are contiguous in tile
+  // order); without it (or beyond its end) the backward walks the boxes
+  const int64_t nbt = (end - start + kRT - 1) / kRT;
+  const int64_t slot0 = (start >> 8) + flat;
+  uint32_t* rec_out = (recs && nbt > 0 && slot0 + nbt <= rec_slots) ? recs + slot0 * kRT : nullptr;
+  (&S.u.fw.rec[0][0])[tid] = 0u;
   int2 staged;
-  fwd_tile<false>(S.u.px, S.b, S.id, S.e, S.wl, S.wcount, vsplat, vals, n, start, end, tile_x,
-                  tile_y, ox, oy, tid, warp, lane, staged, n_tested, n_included);
+  fwd_tile<false>(S.u.fw.px, S.b, S.id, S.e, S.wl, S.wcount, vsplat, vals, n, start, end, tile_x,
+                  tile_y, ox, oy, tid, warp, lane, staged, n_tested, n_included, nullptr, nullptr,
+                  0, 0, S.u.fw.rec, rec_out);
 
   // forward results, L1 loss and its gradient, in registers; thread tid owns
   // pixel tid from here on
   int px, py;
   pixel_of(tid, tile_x, tile_y, px, py);
   const bool inside = px < W && py < H;
-  float Tr = S.u.px.T[tid];
-  const int32_t last = inside ? S.u.px.last[tid] : 0;
+  float Tr = S.u.fw.px.T[tid];
+  const int32_t last = inside ? S.u.fw.px.last[tid] : 0;
   float g0 = 0.f, g1 = 0.f, g2 = 0.f, l1 = 0.f;
   if (inside) {
     const int64_t HW = (int64_t)W * H;
     const int64_t pix = (int64_t)py * W + px;
-    const float c0 = S.u.px.C0[tid] + Tr * bg0;
-    const float c1 = S.u.px.C1[tid] + Tr * bg1;
-    const float c2 = S.u.px.C2[tid] + Tr * bg2;
+    const float c0 = S.u.fw.px.C0[tid] + Tr * bg0;
+    const float c1 = S.u.fw.px.C1[tid] + Tr * bg1;
+    const float c2 = S.u.fw.px.C2[tid] + Tr * bg2;
     image[(view * 3 + 0) * HW + pix] = c0;
     image[(view * 3 + 1) * HW + pix] = c1;
     image[(view * 3 + 2) * HW + pix] = c2;
@@ -771,9 +872,10 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
   if (lane == 0) S.lsum[warp] = l1;
   if (tid == 0) S.max_last = 0;
   __syncthreads();  // the forward's pixel state is read; its space becomes acc
-  for (int i = tid; i < kRT * 9; i += kRT) (&S.u.acc[0][0])[i] = 0.f;
+  for (int i = tid; i < kRT * 9; i += kRT) (&S.u.bw.acc[0][0])[i] = 0.f;
   const int warp_last = __reduce_max_sync(0xffffffffu, last);
   if (lane == 0) atomicMax(&S.max_last, warp_last);
+  quarter_last(last, S.u.bw.qlast[warp], lane);
   if (tid == 0) {
     float t = 0.f;
 #pragma unroll
@@ -783,8 +885,7 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
   __syncthreads();
   const int max_last = S.max_last;
   const float ix = (float)(px - tile_x * GS_TILE), iy = (float)(py - tile_y * GS_TILE);
-  const int wx0 = (warp & 1) * 8, wx1 = wx0 + 7;
-  const int wy0 = (warp >> 1) * 4, wy1 = wy0 + 3;
+  const int wx0 = (warp & 1) * 8, wy0 = (warp >> 1) * 4;
   float S0 = Tr * bg0, S1 = Tr * bg1, S2 = Tr * bg2;
 
   // backward: batch k covers list positions [k*256, min((k+1)*256, max_last))
@@ -827,11 +928,11 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
       slot(staged, k & 1) = k;
       __syncthreads();
     }
-    const int jtop = max(0, min(cnt, warp_last - lo));
-    bwd_batch(B, S.u.acc, S.wl[warp], jtop, lo, wx0, wx1, wy0, wy1, ix, iy, last, Tr, S0, S1,
-              S2, g0, g1, g2, lane);
+    bwd_batch(B, S.u.bw.acc, S.u.bw.qm[warp], S.u.bw.qlast[warp], cnt, lo, wx0, wy0, ix, iy, last,
+              Tr, S0, S1, S2, g0, g1, g2, lane,
+              rec_out ? rec_out + (int64_t)k * kRT + warp * 32 : nullptr);
     __syncthreads();
-    bwd_flush(B, S.e[k & 1], S.id[k & 1], S.u.acc, cnt, grads + 3 * view * n, tid);
+    bwd_flush(B, S.e[k & 1], S.id[k & 1], S.u.bw.acc, cnt, grads + 3 * view * n, tid);
     __syncthreads();
   }
   cp_async_wait<0>();
@@ -848,7 +949,7 @@ static gs_status rasterize_fwd_impl(int64_t n, int32_t n_views, const gs_splat* 
                                     const int64_t* ranges, const uint32_t* tile_order,
                                     const float* bg, float* image,
                                     float* T_final, int32_t* n_contrib, uint64_t* counts,
-                                    float* importance, void* stream) {
+                                    int32_t* pix_counts, float* importance, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
       height < 1 || !bg || !ranges || !image || !T_final || !n_contrib)
     return GS_ERR_INVALID_ARG;
@@ -863,15 +964,18 @@ static gs_status rasterize_fwd_impl(int64_t n, int32_t n_views, const gs_splat* 
     if (n > 0) GS_CUDA(cudaMemsetAsync(importance, 0, sizeof(float) * (size_t)(n * n_views), st));
     raster_fwd_kernel<false, true><<<grid, kRT, 0, st>>>(n, tiles_x, T, width, height, sp, vals,
                                                          ranges, tile_order, bg[0], bg[1], bg[2], image,
-                                                         T_final, n_contrib, c, importance);
+                                                         T_final, n_contrib, c, nullptr, importance);
   } else if (counts) {
+    if (pix_counts)
+      GS_CUDA(cudaMemsetAsync(pix_counts, 0,
+                              sizeof(int32_t) * 2 * (size_t)n_views * width * height, st));
     raster_fwd_kernel<true, false><<<grid, kRT, 0, st>>>(n, tiles_x, T, width, height, sp, vals,
                                                          ranges, tile_order, bg[0], bg[1], bg[2], image,
-                                                         T_final, n_contrib, c, nullptr);
+                                                         T_final, n_contrib, c, pix_counts, nullptr);
   } else {
     raster_fwd_kernel<false, false><<<grid, kRT, 0, st>>>(n, tiles_x, T, width, height, sp, vals,
                                                           ranges, tile_order, bg[0], bg[1], bg[2], image,
-                                                          T_final, n_contrib, c, nullptr);
+                                                          T_final, n_contrib, c, nullptr, nullptr);
   }
   GS_CHECK_LAUNCH();
   return GS_OK;
@@ -883,17 +987,18 @@ extern "C" gs_status gs_rasterize_fwd(int64_t n, int32_t n_views, const gs_splat
                                       const float* bg, float* image, float* T_final,
                                       int32_t* n_contrib, void* stream) {
   return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, tile_order, bg, image,
-                            T_final, n_contrib, nullptr, nullptr, stream);
+                            T_final, n_contrib, nullptr, nullptr, nullptr, stream);
 }
 
 extern "C" gs_status gs_rasterize_fwd_counted(int64_t n, int32_t n_views, const gs_splat* splats,
                                               int32_t width, int32_t height, const uint32_t* vals,
                                               const int64_t* ranges, const uint32_t* tile_order,
                                               const float* bg, float* image, float* T_final,
-                                              int32_t* n_contrib, uint64_t* counts, void* stream) {
+                                              int32_t* n_contrib, uint64_t* counts,
+                                              int32_t* pixel_counts, void* stream) {
   if (!counts) return GS_ERR_INVALID_ARG;
   return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, tile_order, bg, image,
-                            T_final, n_contrib, counts, nullptr, stream);
+                            T_final, n_contrib, counts, pixel_counts, nullptr, stream);
 }
 
 extern "C" gs_status gs_rasterize_fwd_importance(int64_t n, int32_t n_views, const gs_splat* splats,
@@ -904,7 +1009,14 @@ extern "C" gs_status gs_rasterize_fwd_importance(int64_t n, int32_t n_views, con
                                                  float* importance, void* stream) {
   if (!importance && n > 0) return GS_ERR_INVALID_ARG;
   return rasterize_fwd_impl(n, n_views, splats, width, height, vals, ranges, tile_order, bg, image,
-                            T_final, n_contrib, nullptr, importance, stream);
+                            T_final, n_contrib, nullptr, nullptr, importance, stream);
+}
+
+extern "C" size_t gs_rasterize_workspace_bytes(int32_t n_views, int32_t width, int32_t height,
+                                               int64_t capacity) {
+  if (n_views < 1 || width < 1 || height < 1 || capacity < 0) return 0;
+  const int64_t slots = div_up(capacity, kRT) + (int64_t)n_views * tiles_per_view(width, height) + 1;
+  return (size_t)slots * kRT * sizeof(uint32_t);
 }
 
 extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
@@ -913,12 +1025,14 @@ extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_spl
                                         const float* bg,
                                         const float* target, float* image, float* T_final,
                                         int32_t* n_contrib, float* loss, gs_splat_grad* grads,
-                                        void* stream) {
+                                        void* workspace, size_t ws_bytes, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
       height < 1 || !bg || !ranges || !target || !image || !T_final || !n_contrib || !loss)
     return GS_ERR_INVALID_ARG;
   if (n > 0 && (!splats || !grads || !aligned16(splats) || !aligned16(grads)))
     return GS_ERR_INVALID_ARG;
+  if (workspace && !aligned16(workspace)) return GS_ERR_INVALID_ARG;
+  const int64_t rec_slots = workspace ? (int64_t)(ws_bytes / (kRT * sizeof(uint32_t))) : 0;
   cudaStream_t st = (cudaStream_t)stream;
   GS_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), st));
   if (n > 0) GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)(n * n_views), st));
@@ -928,7 +1042,8 @@ extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_spl
   raster_fused_kernel<<<(unsigned)(n_views * T), kRT, 0, st>>>(
       n, tiles_x, T, width, height, reinterpret_cast<const float4*>(splats), vals, ranges,
       tile_order, bg[0], bg[1], bg[2], target, (float)(1.0 / count), image, T_final, n_contrib, loss,
-      reinterpret_cast<float4*>(grads));
+      reinterpret_cast<float4*>(grads), rec_slots > 0 ? static_cast<uint32_t*>(workspace) : nullptr,
+      rec_slots);
   GS_CHECK_LAUNCH();
   return GS_OK;
 }

@@ -254,15 +254,20 @@ gs_status gs_rasterize_fwd(int64_t n, int32_t n_views, const gs_splat* splats, i
                            float* T_final, int32_t* n_contrib, void* stream);
 
 /* gs_rasterize_fwd_counted -- gs_rasterize_fwd with the same outputs that
- * also adds to counts[0] the pairs tested (list entries visited before each
- * pixel stopped) and to counts[1] the pairs composited.  Work accounting for
- * the compositing roofline; not part of the training step.
- *   counts  device uint64[2], accumulated (zero it first) */
+ * also adds to counts[0] the pairs tested (per pixel: the list entries up to
+ * and including the one that stopped it, or the whole list) and to counts[1]
+ * the pairs composited.  Work accounting for the compositing roofline; not
+ * part of the training step.
+ *   counts        device uint64[2], accumulated (zero it first)
+ *   pixel_counts  device int32 [2][n_views][H][W] or NULL: the same two
+ *                 counts per pixel (plane 0 tested, plane 1 composited),
+ *                 zeroed by this call */
 gs_status gs_rasterize_fwd_counted(int64_t n, int32_t n_views, const gs_splat* splats,
                                    int32_t width, int32_t height, const uint32_t* vals,
                                    const int64_t* ranges, const uint32_t* tile_order,
                                    const float* bg, float* image, float* T_final,
-                                   int32_t* n_contrib, uint64_t* counts, void* stream);
+                                   int32_t* n_contrib, uint64_t* counts, int32_t* pixel_counts,
+                                   void* stream);
 
 /* gs_loss_l1 -- L = mean |image - target| over `count` values and
  * dL/dimage = sign(image - target) / count (sign(0) = 0).  Helper beyond the
@@ -290,20 +295,31 @@ gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats, i
  * contributor, colour) and the L1 gradient stay on chip instead of passing
  * through T_final, n_contrib and dL/dimage in memory, and the batches the
  * forward leaves staged in shared memory are reused by the backward without
- * a new gather.  Results equal those of the three separate calls (the
- * gradient up to the order of float atomics).
+ * a new gather.  With a workspace the forward also records, per batch of 256
+ * list entries and per 4x2 pixel block, which entries it composited (1 KB
+ * per batch), and the backward walks exactly those instead of every entry
+ * whose footprint box meets the block.  Results equal those of the three
+ * separate calls (the gradient up to the order of float atomics), with or
+ * without the workspace.
  *   target     [n_views][3][H][W] fp32, the images the L1 loss compares with
  *   image, T_final, n_contrib   outputs as gs_rasterize_fwd
  *   loss       device scalar, overwritten: mean |image - target| over
  *              n_views*3*H*W
  *   grads      [n_views * n] output, zeroed by this call, then accumulated;
  *              as gs_rasterize_bwd with dL/dimage = sign(image - target) /
- *              (n_views*3*H*W) */
+ *              (n_views*3*H*W)
+ *   workspace  NULL, or gs_rasterize_workspace_bytes(n_views, W, H, capacity)
+ *              bytes (16-byte aligned, no initialisation) for lists of at
+ *              most `capacity` entries in all; a tile whose records do not
+ *              fit in ws_bytes falls back to the box walk */
+size_t gs_rasterize_workspace_bytes(int32_t n_views, int32_t width, int32_t height,
+                                    int64_t capacity);
 gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
                              int32_t height, const uint32_t* vals, const int64_t* ranges,
                              const uint32_t* tile_order, const float* bg, const float* target,
                              float* image, float* T_final, int32_t* n_contrib, float* loss,
-                             gs_splat_grad* grads, void* stream);
+                             gs_splat_grad* grads, void* workspace, size_t ws_bytes,
+                             void* stream);
 
 /* gs_project_bwd -- chain rule from the per-row gradients back to the 59
  * parameters, summed over the views (the 1/n_views average of [S1] comes
@@ -411,7 +427,10 @@ gs_status gs_compact_index(int64_t n, const uint8_t* mask, void* workspace, size
                            uint32_t* idx, int64_t* n_keep, void* stream);
 
 /* ---------------------------------------------------------------------- */
+/* Text of a status code (static storage; "unknown status" for other
+ * values).  gs_status_str is the same function under a shorter name. */
 const char* gs_status_string(gs_status status);
+const char* gs_status_str(gs_status status);
 int32_t gs_version(void);
 
 #ifdef __cplusplus

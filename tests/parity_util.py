@@ -17,6 +17,18 @@ ADAM_REL_L2 = 1e-4
 # transmittance is carried to ~2 ulp whatever the number of contributors)
 MARGIN = 1e-5
 
+# The library's own chain (its fp32 projection) against the oracle's (fp64
+# projection): the projected mean is stored in fp32, one ulp ~6e-5 px at
+# 512..1024 px, and the exponent moves by |Q d| times that: ~1e-4 relative in
+# alpha for the steepest (dilation-limited) splats.  So the chain comparisons
+# flag decisions within CHAIN_MARGIN of a cut-off and hold the image to
+# CHAIN_IMAGE_MAX_ABS (the sum of alpha c T over a pixel is <= 1, times the
+# ~1e-4 relative move), the gradients to CHAIN_GRAD_REL_L2; on identical stage
+# inputs the per-call bars above apply.
+CHAIN_MARGIN = 1e-4
+CHAIN_IMAGE_MAX_ABS = 1e-4
+CHAIN_GRAD_REL_L2 = 1e-3
+
 
 def flagged_allowance(n_pixels, n_pairs, margin=MARGIN):
     """Upper bound on the pixels flagged by `margin`, from the geometry of the

@@ -48,6 +48,16 @@ def test_status_strings_and_version(gslib):
         assert lib.gs_status_str(code).decode() == gslib.status_string(code)
 
 
+def test_rasterize_workspace_bytes(gslib):
+    """1 KB per batch slot: one per 256 list entries of capacity, plus one per
+    (view, tile), plus one."""
+    f = gslib.gs_rasterize_workspace_bytes
+    assert f(1, 256, 256, 0) == 1024 * (0 + 256 + 1)
+    assert f(1, 256, 256, 1) == 1024 * (1 + 256 + 1)
+    assert f(4, 1920, 1080, 22_768_982) == 1024 * (-(-22_768_982 // 256) + 4 * 120 * 68 + 1)
+    assert f(0, 256, 256, 10) == 0 and f(1, 256, 256, -1) == 0
+
+
 def test_key_bits_and_workspace(gslib):
     # 256x256, 1 view: 256 tiles -> 8 bits of tile index + 32 depth bits
     assert gslib.gs_key_bits(1, 256, 256) == 40
@@ -93,7 +103,15 @@ def test_invalid_arguments_return_before_any_launch(gslib):
     assert L.gs_rasterize_bwd(10, 17, None, 16, 16, None, None, None, None, None, None, None,
                               None, None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_rasterize_fused(10, 1, None, 16, 16, None, None, None, None, None, None, None,
-                                None, None, None, None) == gslib.GS_ERR_INVALID_ARG
+                                None, None, None, None, C.c_size_t(0),
+                                None) == gslib.GS_ERR_INVALID_ARG
+    # a workspace not 16-byte aligned is rejected before anything runs
+    buf = C.create_string_buffer(64)
+    dummy = C.c_float * 3
+    mis = C.c_void_p(((C.addressof(buf) + 15) & ~15) + 4)  # 4 mod 16, inside the buffer
+    assert L.gs_rasterize_fused(0, 1, None, 16, 16, None, buf, None, dummy(0, 0, 0), buf, buf, buf,
+                                buf, buf, None, mis, C.c_size_t(32),
+                                None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_tile_order(-1, None, None, None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_tile_order(5, None, None, None) == gslib.GS_ERR_INVALID_ARG          # NULL
     assert L.gs_tile_order(0, None, None, None) == gslib.GS_OK                       # empty

@@ -32,3 +32,34 @@ def test_traffic_table_names_existing_sources():
     for name, t in bench.TRAFFIC.items():
         assert os.path.exists(os.path.join(ROOT, t["source"])), name
         assert len(t["sha256"]) == 64 and t["bytes"] > 0, name
+
+
+def test_oracle_step_full_and_sampled(capsys):
+    """The CPU baseline's oracle step: the whole step, and the sampled step
+    that the reference arm and the baseline leg share (a 1/k slice of the
+    Gaussians, every k-th non-empty tile in list-length order)."""
+    import json
+    import types
+
+    import numpy as np
+
+    import bench
+    import scenes
+    cfg = scenes.make("small_200k_1024x768", n_override=20_000)
+    full, wall, stages, text = bench.oracle_step(cfg, 2, 1, {})
+    assert full > 0 and wall > 0 and text.startswith("full oracle step")
+    assert set(stages) == {"project", "bin", "raster_fwd", "loss", "raster_bwd", "project_bwd",
+                           "adam"}
+    cache = {}
+    s_full, s_wall, _, s_text = bench.oracle_step(cfg, 2, 4, cache)
+    assert s_full > s_wall * 0.5 and "every 4th" in s_text
+    pr, vals, ranges = cache["full"]
+    lens = ranges[:, 1] - ranges[:, 0]
+    assert lens.max() > 0 and np.count_nonzero(lens) > 4
+    # the reference arm: one JSON line on the host's cores
+    args = types.SimpleNamespace(workload="tiny_2k_256", gaussians=None, warmup=1, steps=2)
+    bench.reference_arm(args, 0, 1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["cores"] == bench.host_cores()
+    assert line["e2e"]["h2d_bytes_per_step"] == 0

@@ -113,6 +113,19 @@ def test_ring_3m_full_size():
     assert (mask & ~okp).sum() <= allow
     assert err[okp].max() <= IMAGE_MAX_ABS
     assert np.array_equal(n_contrib.cpu().numpy()[okp], fw["n_contrib"][okp])
+    # the roofline's work counts on the sampled tiles, pixel by pixel
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    pix = torch.empty((2, V, H, W), dtype=torch.int32, device="cuda")
+    gs.gs_rasterize_fwd_counted(n, V, rec_d, W, H, vals, ranges, (0, 0, 0), image, T_final,
+                                n_contrib, counts, pixel_counts=pix)
+    pc = pix.cpu().numpy().astype(np.int64)
+    assert np.array_equal(pc[0][okp], fw["pairs"][okp])
+    assert np.array_equal(pc[1][okp], fw["included"][okp])
+    c = counts.cpu().numpy()
+    assert c[0] == pc[0].sum() and c[1] == pc[1].sum()
+    print("counted: tested %d composited %d over the image; sampled tiles equal the oracle's "
+          "%d / %d" % (c[0], c[1], fw["pairs"][okp].sum(), fw["included"][okp].sum()))
+    del pix
 
     # compositing backward restricted to the sampled tiles
     _, g_img = oracle.loss_l1(fw["image"], target)
@@ -143,8 +156,10 @@ def test_ring_3m_full_size():
     image_f, T_f, nc_f = torch.empty_like(image_s), torch.empty_like(T_s), torch.empty_like(nc_s)
     loss_f = torch.empty(1, device="cuda")
     grads_f = torch.empty((n * V, 12), device="cuda")
+    ws = torch.empty(gs.gs_rasterize_workspace_bytes(V, W, H, I), dtype=torch.uint8, device="cuda")
     gs.gs_rasterize_fused(n, V, rec_d, W, H, vals, ranges, (0, 0, 0), target_d, image_f, T_f, nc_f,
-                          loss_f, grads_f)
+                          loss_f, grads_f, workspace=ws)
+    del ws
     assert torch.equal(image_f, image_s) and torch.equal(T_f, T_s) and torch.equal(nc_f, nc_s)
     assert loss_f.item() == pytest.approx(loss_s.item(), rel=1e-5)  # fp32 sums in another order
     e = ((grads_f - grads_s).norm() / grads_s.norm()).item()

@@ -6,7 +6,7 @@
 // opacity saturation depth at which a pixel stops).
 //
 // One CTA per (view, 16x16 tile).  The tile's Gaussians are gathered by id
-// into shared memory in batches of 256 with cp.async, double buffered: the
+// into shared memory in batches of kBatch with cp.async, double buffered: the
 // next batch is in flight while the current one is composited.
 //
 // Clustered scenes make most pairs skips (alpha < 1/255) and leave a few
@@ -37,6 +37,12 @@ namespace {
 
 constexpr int kRT = 256;      // threads per CTA = pixels per tile
 constexpr int kWarps = kRT / 32;
+// List entries per batch: 192 keeps a CTA of the fused kernel under 37 KB of
+// shared memory, so that six CTAs share an SM (the kernels are bound by how
+// many warps an SM can switch between: at three CTAs per SM the fused kernel
+// took 44 % longer than at five).
+constexpr int kBatch = 192;
+constexpr int kWords = kBatch / 32;  // 32-bit words of a per-batch entry mask
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -121,13 +127,13 @@ __device__ __forceinline__ float snap(float v, float origin) {
 }
 
 struct Batch {
-  float4 a[kRT];     // as loaded: mean_x, mean_y, conic_a, conic_b
+  float4 a[kBatch];  // as loaded: mean_x, mean_y, conic_a, conic_b
                      // staged:    G_x, G_y, P, -a/2
-  float4 b[kRT];     // as loaded: conic_c, opacity, color_r, color_g
+  float4 b[kBatch];  // as loaded: conic_c, opacity, color_r, color_g
                      // staged:    -b, -c/2, z_x, z_y (grid index in the tile)
-  float4 c[kRT];     // as loaded: color_b, depth, radius, tiles
+  float4 c[kBatch];  // as loaded: color_b, depth, radius, tiles
                      // staged:    color_r, color_g, color_b, opacity
-  char4 box[kRT];    // grid-index box (x0, x1, y0, y1) outside of which
+  char4 box[kBatch];  // grid-index box (x0, x1, y0, y1) outside of which
                      // alpha < 1/255 for sure; clamped to [-1, 16]
 };
 
@@ -266,8 +272,8 @@ __device__ __forceinline__ float quarter_sum(float v) {
 struct PixState {
   float T[kRT], Tl[kRT], C0[kRT], C1[kRT], C2[kRT];  // T = T + Tl (double-float)
   int32_t last[kRT];
-  int32_t done[kRT];
-  int32_t list[kRT];  // open pixels, packed
+  uint8_t done[kRT];
+  uint8_t list[kRT];  // open pixels, packed
 };
 
 __device__ __forceinline__ void pix_init(PixState& P, int tid, int tile_x, int tile_y, int W,
@@ -308,7 +314,7 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
                                           int lane, unsigned long long& n_tested,
                                           unsigned long long& n_included, const uint32_t* ids,
                                           float* imp, int32_t* pix_counts, int64_t plane,
-                                          int32_t W, uint32_t (*rec)[8]) {
+                                          int32_t W, uint32_t (*rec)[kWords]) {
   if (warp * 32 >= m) return;
   const bool worker = tid < m;
   const int p = worker ? P.list[tid] : 0;
@@ -332,7 +338,7 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
   int done = 0;
   int stop_j = cnt;
   int32_t n_inc = 0;
-  const int32_t base1 = k * kRT + 1;  // 1-based list position of entry 0
+  const int32_t base1 = k * kBatch + 1;  // 1-based list position of entry 0
   for (int i = 0; i < nw; ++i) {
     const int j = wl[i];
     const float4 A = B.a[j];
@@ -379,7 +385,7 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
   P.done[p] = done;
 }
 
-// The forward over a tile's list [start, end): batches of 256 gathered by
+// The forward over a tile's list [start, end): batches of kBatch gathered by
 // cp.async into the two slots of `b` (batch k in slot k & 1), one batch
 // ahead.  The open pixels are counted at the end of each batch, before the
 // next one is prefetched, so when every pixel has stopped the last batch
@@ -391,8 +397,8 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
 __device__ __forceinline__ int& slot(int2& s, int i) { return i ? s.y : s.x; }
 
 template <bool kCount, bool kImp = false>
-__device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[kRT],
-                                         float2 (*E)[kRT], uint8_t (*wl)[kRT], int32_t* wcount,
+__device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[kBatch],
+                                         float2 (*E)[kBatch], uint8_t (*wl)[kBatch], int32_t* wcount,
                                          const float4* vsplat, const uint32_t* __restrict__ vals,
                                          int64_t n, int64_t start, int64_t end, int tile_x,
                                          int tile_y, float ox, float oy, int tid, int warp,
@@ -400,14 +406,14 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
                                          unsigned long long& n_tested,
                                          unsigned long long& n_included, float* imp = nullptr,
                                          int32_t* pix_counts = nullptr, int64_t plane = 0,
-                                         int32_t W = 0, uint32_t (*rec)[8] = nullptr,
+                                         int32_t W = 0, uint32_t (*rec)[kWords] = nullptr,
                                          uint32_t* __restrict__ rec_out = nullptr) {
   const int64_t len = end - start;
-  const int nb = (int)((len + kRT - 1) / kRT);
+  const int nb = (int)((len + kBatch - 1) / kBatch);
   staged = make_int2(-1, -1);
   auto issue = [&](int k) {
-    const int64_t e = start + (int64_t)k * kRT + tid;
-    if (e < end) {
+    const int64_t e = start + (int64_t)k * kBatch + tid;
+    if (tid < kBatch && e < end) {
       // ids come from gs_bin_and_sort; clamping keeps a corrupt list in bounds
       const uint32_t id = min(__ldg(vals + e), (uint32_t)(n - 1));
       const float4* src = vsplat + 3 * (int64_t)id;
@@ -438,7 +444,7 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
       slot(staged, (k + 1) & 1) = -1;
     }
     Batch& B = b[k & 1];
-    const int cnt = (int)min((int64_t)kRT, len - (int64_t)k * kRT);
+    const int cnt = (int)min((int64_t)kBatch, len - (int64_t)k * kBatch);
     if (tid < cnt) stage_entry(B, tid, ox, oy, E ? E[k & 1] : nullptr);
     slot(staged, k & 1) = k;
     if ((bal >> lane) & 1u) P.list[off + __popc(bal & ((1u << lane) - 1u))] = tid;
@@ -447,8 +453,8 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
                             n_included, ids ? ids[k & 1] : nullptr, imp, pix_counts, plane, W,
                             rec_out ? rec : nullptr);
     __syncthreads();  // pixel state written; slot k & 1 free for batch k + 2
-    if (rec_out) {  // this batch's record of the composited entries, per quarter
-      __stcg(rec_out + (int64_t)k * kRT + tid, (&rec[0][0])[tid]);
+    if (rec_out && tid < kRT / 8 * kWords) {  // this batch's record of the composited entries
+      __stcg(rec_out + (int64_t)k * (kRT / 8 * kWords) + tid, (&rec[0][0])[tid]);
       (&rec[0][0])[tid] = 0u;
     }
     bal = __ballot_sync(0xffffffffu, !P.done[tid]);
@@ -463,13 +469,13 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
 //
 // Each quarter of the warp walks its own sub-list: the entries whose box
 // meets the quarter's 4x2 block and that lie below the quarter's last
-// contributor (qlast[q]), kept as a 256-bit mask qm[q][0..7] (bit j of word
+// contributor (qlast[q]), kept as a kBatch-bit mask qm[q][0..kWords) (bit j of word
 // j >> 5).  The four quarters advance together, one entry each per step, so
 // a step costs the longest of four short lists rather than one list for the
 // whole 8x4 block, and a pair's gradient is reduced over the quarter's eight
 // lanes (10 shuffles) instead of the warp's 32.  A quarter that has no
 // entry left, or no contributing lane, adds nothing.
-__device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint32_t (*qm)[8],
+__device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint32_t (*qm)[kWords],
                                           const int32_t* qlast, int cnt, int lo, int wx0, int wy0,
                                           float ix, float iy, int last, float& Tr, float& S0,
                                           float& S1, float& S2, float g0, float g1, float g2,
@@ -483,12 +489,12 @@ __device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint3
   if (contrib) {
     // the forward's record of this warp's quarters: the entries composited
     // into at least one pixel of the quarter (word w of quarter q is
-    // contrib[q * 8 + w]); they are exactly the pairs this walk can use
-    qm[q][lane & 7] = __ldcg(contrib + lane);
+    // contrib[q * kWords + w]); they are exactly the pairs this walk can use
+    if (lane < 4 * kWords) qm[lane / kWords][lane % kWords] = __ldcg(contrib + lane);
   } else {
     for (int c = 0; c < nchunk; ++c) {
       const int j = (c << 5) + lane;
-      const char4 bx = B.box[j];  // j < 256; entries >= cnt are excluded by the tops
+      const char4 bx = B.box[j];  // j < kBatch; entries >= cnt are excluded by the tops
       const bool xl = !(bx.y < wx0 || bx.x > wx0 + 3), xr = !(bx.y < wx0 + 4 || bx.x > wx0 + 7);
       const bool yt = !(bx.w < wy0 || bx.z > wy0 + 1), yb = !(bx.w < wy0 + 2 || bx.z > wy0 + 3);
       const unsigned b0 = __ballot_sync(0xffffffffu, xl && yt && j < t0);
@@ -533,7 +539,7 @@ __device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint3
           contrib = true;
           const float4 Cv = B.c[j];
           const float oma = 1.f - alpha;
-          const float rinv = 1.f / oma;
+          const float rinv = __fdividef(1.f, oma);  // ~2 ulp; decides nothing
           const float Ti = Tr * rinv;
           const float w = alpha * Ti;
           v[6] = w * g0;
@@ -625,10 +631,10 @@ __device__ __forceinline__ void bwd_flush(const Batch& B, const float2* E, const
 template <bool kImp>
 struct FwdSmem {
   Batch b[2];
-  uint32_t id[2][kImp ? kRT : 1];  // ids of the staged entries (importance variant)
+  uint32_t id[2][kImp ? kBatch : 1];  // ids of the staged entries (importance variant)
   PixState px;
   int32_t wcount[kWarps];
-  uint8_t wl[kWarps][kRT];  // per-warp entry sub-lists
+  uint8_t wl[kWarps][kBatch];  // per-warp entry sub-lists
 };
 
 // kCount: also accumulate the pairs tested / included into counts[0..1]
@@ -652,7 +658,7 @@ __global__ void __launch_bounds__(kRT, 6) raster_fwd_kernel(
   const float ox = (float)(tile_x * GS_TILE), oy = (float)(tile_y * GS_TILE);
   pix_init(S.px, tid, tile_x, tile_y, W, H);
   int2 staged;
-  fwd_tile<kCount, kImp>(S.px, S.b, kImp ? reinterpret_cast<uint32_t(*)[kRT]>(&S.id[0][0]) : nullptr,
+  fwd_tile<kCount, kImp>(S.px, S.b, kImp ? reinterpret_cast<uint32_t(*)[kBatch]>(&S.id[0][0]) : nullptr,
                          nullptr, S.wl, S.wcount,
                          splats + 3 * view * n, vals, n, ranges[2 * flat], ranges[2 * flat + 1],
                          tile_x, tile_y, ox, oy, tid, warp, lane, staged, n_tested, n_included,
@@ -688,15 +694,15 @@ __global__ void __launch_bounds__(kRT, 6) raster_fwd_kernel(
 
 struct BwdSmem {
   Batch b[2];
-  float2 e[2][kRT];  // e = z - m of the staged entries
-  uint32_t id[2][kRT];
-  float acc[kRT][9];
-  uint32_t qm[kWarps][4][8];     // per-quarter entry masks of the batch
+  float2 e[2][kBatch];  // e = z - m of the staged entries
+  uint32_t id[2][kBatch];
+  float acc[kBatch][9];
+  uint32_t qm[kWarps][4][kWords];  // per-quarter entry masks of the batch
   alignas(16) int32_t qlast[kWarps][4];  // per-quarter last contributor
   int max_last;
 };
 
-__global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
+__global__ void __launch_bounds__(kRT, 6) raster_bwd_kernel(
     int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
     const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges,
     const uint32_t* __restrict__ tile_order, float bg0, float bg1, float bg2, const float* __restrict__ T_final, const int32_t* __restrict__ n_contrib,
@@ -728,21 +734,21 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
   }
   float S0 = Tr * bg0, S1 = Tr * bg1, S2 = Tr * bg2;
   if (tid == 0) S.max_last = 0;
-  for (int i = tid; i < kRT * 9; i += kRT) (&S.acc[0][0])[i] = 0.f;
+  for (int i = tid; i < kBatch * 9; i += kRT) (&S.acc[0][0])[i] = 0.f;
   __syncthreads();
   const int warp_last = __reduce_max_sync(0xffffffffu, last);
   if (lane == 0) atomicMax(&S.max_last, warp_last);
   quarter_last(last, S.qlast[warp], lane);
   __syncthreads();
   const int max_last = S.max_last;
-  const int nb = (max_last + kRT - 1) / kRT;
+  const int nb = (max_last + kBatch - 1) / kBatch;
   const float4* vsplat = splats + 3 * view * n;
 
-  // batch k covers list positions [hi - cnt, hi), hi = max_last - k*256,
+  // batch k covers list positions [hi - cnt, hi), hi = max_last - k * kBatch,
   // stored at smem slots 0..cnt-1 in position order
   auto issue = [&](int k) {
-    const int hi = max_last - k * kRT;
-    const int cnt = min(kRT, hi);
+    const int hi = max_last - k * kBatch;
+    const int cnt = min(kBatch, hi);
     if (tid < cnt) {
       const int64_t e = start + (hi - cnt) + tid;
       const uint32_t id = min(__ldg(vals + e), (uint32_t)(n - 1));
@@ -762,8 +768,8 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
     cp_async_wait<1>();
     __syncthreads();
     Batch& B = S.b[k & 1];
-    const int hi = max_last - k * kRT;
-    const int cnt = min(kRT, hi);
+    const int hi = max_last - k * kBatch;
+    const int cnt = min(kBatch, hi);
     const int lo = hi - cnt;
     float2* E = S.e[k & 1];
     if (tid < cnt) stage_entry(B, tid, ox, oy, E);
@@ -789,26 +795,26 @@ __global__ void __launch_bounds__(kRT, 5) raster_bwd_kernel(
 // contributor down to the first.
 struct FusedSmem {
   Batch b[2];
-  float2 e[2][kRT];
-  uint32_t id[2][kRT];
+  float2 e[2][kBatch];
+  uint32_t id[2][kBatch];
   union {
     struct {
       PixState px;
-      uint32_t rec[kRT / 8][8];  // the batch's composited entries per quarter
+      uint32_t rec[kRT / 8][kWords];  // the batch's composited entries per quarter
+      uint8_t wl[kWarps][kBatch];     // per-warp entry sub-lists
     } fw;  // forward
     struct {
-      float acc[kRT][9];
-      uint32_t qm[kWarps][4][8];
+      float acc[kBatch][9];
+      uint32_t qm[kWarps][4][kWords];
       alignas(16) int32_t qlast[kWarps][4];
     } bw;  // backward
   } u;
-  uint8_t wl[kWarps][kRT];   // forward: per-warp entry sub-lists
   int32_t wcount[kWarps];
   float lsum[kWarps];
   int max_last;
 };
 
-__global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
+__global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
     int64_t n, int32_t tiles_x, int64_t T, int32_t W, int32_t H, const float4* __restrict__ splats,
     const uint32_t* __restrict__ vals, const int64_t* __restrict__ ranges,
     const uint32_t* __restrict__ tile_order, float bg0, float bg1, float bg2, const float* __restrict__ target, float inv_count, float* __restrict__ image,
@@ -826,15 +832,17 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
   const float4* vsplat = splats + 3 * view * n;
   pix_init(S.u.fw.px, tid, tile_x, tile_y, W, H);
   // the workspace keeps, per batch of the tile, which entries the forward
-  // composited into each 4x2 quarter (1 KB, slot g = start / 256 + k + flat:
-  // distinct for every (tile, batch) since the lists are contiguous in tile
-  // order); without it (or beyond its end) the backward walks the boxes
-  const int64_t nbt = (end - start + kRT - 1) / kRT;
-  const int64_t slot0 = (start >> 8) + flat;
-  uint32_t* rec_out = (recs && nbt > 0 && slot0 + nbt <= rec_slots) ? recs + slot0 * kRT : nullptr;
-  (&S.u.fw.rec[0][0])[tid] = 0u;
+  // composited into each 4x2 quarter (kRec words, slot g = start / kBatch + k
+  // + flat: distinct for every (tile, batch) since the lists are contiguous
+  // in tile order); without it (or beyond its end) the backward walks the
+  // boxes
+  constexpr int kRec = kRT / 8 * kWords;
+  const int64_t nbt = (end - start + kBatch - 1) / kBatch;
+  const int64_t slot0 = start / kBatch + flat;
+  uint32_t* rec_out = (recs && nbt > 0 && slot0 + nbt <= rec_slots) ? recs + slot0 * kRec : nullptr;
+  if (tid < kRec) (&S.u.fw.rec[0][0])[tid] = 0u;
   int2 staged;
-  fwd_tile<false>(S.u.fw.px, S.b, S.id, S.e, S.wl, S.wcount, vsplat, vals, n, start, end, tile_x,
+  fwd_tile<false>(S.u.fw.px, S.b, S.id, S.e, S.u.fw.wl, S.wcount, vsplat, vals, n, start, end, tile_x,
                   tile_y, ox, oy, tid, warp, lane, staged, n_tested, n_included, nullptr, nullptr,
                   0, 0, S.u.fw.rec, rec_out);
 
@@ -872,7 +880,7 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
   if (lane == 0) S.lsum[warp] = l1;
   if (tid == 0) S.max_last = 0;
   __syncthreads();  // the forward's pixel state is read; its space becomes acc
-  for (int i = tid; i < kRT * 9; i += kRT) (&S.u.bw.acc[0][0])[i] = 0.f;
+  for (int i = tid; i < kBatch * 9; i += kRT) (&S.u.bw.acc[0][0])[i] = 0.f;
   const int warp_last = __reduce_max_sync(0xffffffffu, last);
   if (lane == 0) atomicMax(&S.max_last, warp_last);
   quarter_last(last, S.u.bw.qlast[warp], lane);
@@ -888,11 +896,11 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
   const int wx0 = (warp & 1) * 8, wy0 = (warp >> 1) * 4;
   float S0 = Tr * bg0, S1 = Tr * bg1, S2 = Tr * bg2;
 
-  // backward: batch k covers list positions [k*256, min((k+1)*256, max_last))
+  // backward: batch k covers list positions [k kBatch, min((k+1) kBatch, max_last))
   // in slot k & 1, gathered and staged unless the forward left it there
   auto issue = [&](int k) {
-    const int lo = k * kRT;
-    const int cnt = min(kRT, max_last - lo);
+    const int lo = k * kBatch;
+    const int cnt = min(kBatch, max_last - lo);
     if (tid < cnt) {
       const uint32_t id = min(__ldg(vals + start + lo + tid), (uint32_t)(n - 1));
       const float4* src = vsplat + 3 * (int64_t)id;
@@ -904,7 +912,7 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
     }
     cp_async_commit();
   };
-  const int kt = max_last > 0 ? (max_last - 1) / kRT : -1;
+  const int kt = max_last > 0 ? (max_last - 1) / kBatch : -1;
   if (kt >= 0 && slot(staged, kt & 1) != kt) {
     issue(kt);
     slot(staged, kt & 1) = -1;
@@ -921,8 +929,8 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
     cp_async_wait<1>();
     __syncthreads();  // batch k landed (or staged by the forward)
     Batch& B = S.b[k & 1];
-    const int lo = k * kRT;
-    const int cnt = min(kRT, max_last - lo);
+    const int lo = k * kBatch;
+    const int cnt = min(kBatch, max_last - lo);
     if (slot(staged, k & 1) != k) {
       if (tid < cnt) stage_entry(B, tid, ox, oy, S.e[k & 1]);
       slot(staged, k & 1) = k;
@@ -930,7 +938,7 @@ __global__ void __launch_bounds__(kRT, 5) raster_fused_kernel(
     }
     bwd_batch(B, S.u.bw.acc, S.u.bw.qm[warp], S.u.bw.qlast[warp], cnt, lo, wx0, wy0, ix, iy, last,
               Tr, S0, S1, S2, g0, g1, g2, lane,
-              rec_out ? rec_out + (int64_t)k * kRT + warp * 32 : nullptr);
+              rec_out ? rec_out + (int64_t)k * kRec + warp * 4 * kWords : nullptr);
     __syncthreads();
     bwd_flush(B, S.e[k & 1], S.id[k & 1], S.u.bw.acc, cnt, grads + 3 * view * n, tid);
     __syncthreads();
@@ -1015,8 +1023,8 @@ extern "C" gs_status gs_rasterize_fwd_importance(int64_t n, int32_t n_views, con
 extern "C" size_t gs_rasterize_workspace_bytes(int32_t n_views, int32_t width, int32_t height,
                                                int64_t capacity) {
   if (n_views < 1 || width < 1 || height < 1 || capacity < 0) return 0;
-  const int64_t slots = div_up(capacity, kRT) + (int64_t)n_views * tiles_per_view(width, height) + 1;
-  return (size_t)slots * kRT * sizeof(uint32_t);
+  const int64_t slots = div_up(capacity, kBatch) + (int64_t)n_views * tiles_per_view(width, height) + 1;
+  return (size_t)slots * (kRT / 8 * kWords) * sizeof(uint32_t);
 }
 
 extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
@@ -1032,7 +1040,7 @@ extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_spl
   if (n > 0 && (!splats || !grads || !aligned16(splats) || !aligned16(grads)))
     return GS_ERR_INVALID_ARG;
   if (workspace && !aligned16(workspace)) return GS_ERR_INVALID_ARG;
-  const int64_t rec_slots = workspace ? (int64_t)(ws_bytes / (kRT * sizeof(uint32_t))) : 0;
+  const int64_t rec_slots = workspace ? (int64_t)(ws_bytes / (kRT / 8 * kWords * sizeof(uint32_t))) : 0;
   cudaStream_t st = (cudaStream_t)stream;
   GS_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), st));
   if (n > 0) GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)(n * n_views), st));

@@ -295,8 +295,8 @@ gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats, i
  * contributor, colour) and the L1 gradient stay on chip instead of passing
  * through T_final, n_contrib and dL/dimage in memory, and the batches the
  * forward leaves staged in shared memory are reused by the backward without
- * a new gather.  With a workspace the forward also records, per batch of 256
- * list entries and per 4x2 pixel block, which entries it composited (1 KB
+ * a new gather.  With a workspace the forward also records, per batch of 192
+ * list entries and per 4x2 pixel block, which entries it composited (768 B
  * per batch), and the backward walks exactly those instead of every entry
  * whose footprint box meets the block.  Results equal those of the three
  * separate calls (the gradient up to the order of float atomics), with or

@@ -49,12 +49,12 @@ def test_status_strings_and_version(gslib):
 
 
 def test_rasterize_workspace_bytes(gslib):
-    """1 KB per batch slot: one per 256 list entries of capacity, plus one per
-    (view, tile), plus one."""
+    """768 B per batch slot (32 quarters x 192 bits): one slot per 192 list
+    entries of capacity, plus one per (view, tile), plus one."""
     f = gslib.gs_rasterize_workspace_bytes
-    assert f(1, 256, 256, 0) == 1024 * (0 + 256 + 1)
-    assert f(1, 256, 256, 1) == 1024 * (1 + 256 + 1)
-    assert f(4, 1920, 1080, 22_768_982) == 1024 * (-(-22_768_982 // 256) + 4 * 120 * 68 + 1)
+    assert f(1, 256, 256, 0) == 768 * (0 + 256 + 1)
+    assert f(1, 256, 256, 1) == 768 * (1 + 256 + 1)
+    assert f(4, 1920, 1080, 22_768_982) == 768 * (-(-22_768_982 // 192) + 4 * 120 * 68 + 1)
     assert f(0, 256, 256, 10) == 0 and f(1, 256, 256, -1) == 0
 
 

@@ -464,56 +464,22 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
   __syncthreads();
 }
 
-// Backward pairs of one staged batch (list positions lo + j, j < cnt) for
-// this thread's pixel, back to front; per-entry sums into acc.
-//
-// Each quarter of the warp walks its own sub-list: the entries whose box
-// meets the quarter's 4x2 block and that lie below the quarter's last
-// contributor (qlast[q]), kept as a kBatch-bit mask qm[q][0..kWords) (bit j of word
-// j >> 5).  The four quarters advance together, one entry each per step, so
-// a step costs the longest of four short lists rather than one list for the
-// whole 8x4 block, and a pair's gradient is reduced over the quarter's eight
-// lanes (10 shuffles) instead of the warp's 32.  A quarter that has no
-// entry left, or no contributing lane, adds nothing.
-__device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint32_t (*qm)[kWords],
-                                          const int32_t* qlast, int cnt, int lo, int wx0, int wy0,
-                                          float ix, float iy, int last, float& Tr, float& S0,
-                                          float& S1, float& S2, float g0, float g1, float g2,
-                                          int lane, const uint32_t* __restrict__ contrib) {
-  const int q = (lane >> 3) & 3, r = lane & 7;
-  // entries below each quarter's last contributor, and the chunks of 32 to scan
-  const int4 ql = *reinterpret_cast<const int4*>(qlast);
-  const int t0 = max(0, min(cnt, ql.x - lo)), t1 = max(0, min(cnt, ql.y - lo));
-  const int t2 = max(0, min(cnt, ql.z - lo)), t3 = max(0, min(cnt, ql.w - lo));
-  const int nchunk = (max(max(t0, t1), max(t2, t3)) + 31) >> 5;
-  if (contrib) {
-    // the forward's record of this warp's quarters: the entries composited
-    // into at least one pixel of the quarter (word w of quarter q is
-    // contrib[q * kWords + w]); they are exactly the pairs this walk can use
-    if (lane < 4 * kWords) qm[lane / kWords][lane % kWords] = __ldcg(contrib + lane);
-  } else {
-    for (int c = 0; c < nchunk; ++c) {
-      const int j = (c << 5) + lane;
-      const char4 bx = B.box[j];  // j < kBatch; entries >= cnt are excluded by the tops
-      const bool xl = !(bx.y < wx0 || bx.x > wx0 + 3), xr = !(bx.y < wx0 + 4 || bx.x > wx0 + 7);
-      const bool yt = !(bx.w < wy0 || bx.z > wy0 + 1), yb = !(bx.w < wy0 + 2 || bx.z > wy0 + 3);
-      const unsigned b0 = __ballot_sync(0xffffffffu, xl && yt && j < t0);
-      const unsigned b1 = __ballot_sync(0xffffffffu, xr && yt && j < t1);
-      const unsigned b2 = __ballot_sync(0xffffffffu, xl && yb && j < t2);
-      const unsigned b3 = __ballot_sync(0xffffffffu, xr && yb && j < t3);
-      if (lane == 0) {
-        qm[0][c] = b0;
-        qm[1][c] = b1;
-        qm[2][c] = b2;
-        qm[3][c] = b3;
-      }
-    }
-  }
-  __syncwarp();
-  int wi = nchunk - 1;
-  uint32_t bits = wi >= 0 ? qm[q][wi] : 0u;
+// Backward pairs of one staged batch for this thread's pixel (list positions
+// lo + j), back to front; per-entry sums into acc.  The lane's quarter walks
+// the entries set in its mask qw[0..nw) (bit j of word j >> 5), highest
+// first; the four quarters of the warp advance together, one entry each per
+// step, so a step costs the longest of four short lists, and a pair's
+// gradient is reduced over the quarter's eight lanes (10 shuffles).  A
+// quarter that has no entry left, or no contributing lane, adds nothing.
+__device__ __forceinline__ void bwd_walk(const Batch& B, float (*acc)[9], const uint32_t* qw,
+                                         int nw, int lo, float ix, float iy, int last, float& Tr,
+                                         float& S0, float& S1, float& S2, float g0, float g1,
+                                         float g2, int lane) {
+  const int r = lane & 7;
+  int wi = nw - 1;
+  uint32_t bits = wi >= 0 ? qw[wi] : 0u;
   while (true) {
-    while (bits == 0u && wi > 0) bits = qm[q][--wi];
+    while (bits == 0u && wi > 0) bits = qw[--wi];
     const bool act = bits != 0u;
     if (!__any_sync(0xffffffffu, act)) break;
     int j = 0;
@@ -580,6 +546,60 @@ __device__ __forceinline__ void bwd_batch(const Batch& B, float (*acc)[9], uint3
     }
   }
   __syncwarp();
+}
+
+// The masks of the warp's quarters for one staged batch (cnt entries): the
+// entries whose box meets the quarter's 4x2 block (origin wx0, wy0 of the
+// warp's 8x4 block) and that lie below the quarter's last contributor
+// (qlast[q]); into qm[q][0..nw), *nw = the words to walk.  Whole-warp call.
+__device__ __forceinline__ int box_masks(const Batch& B, uint32_t (*qm)[kWords],
+                                         const int32_t* qlast, int cnt, int lo, int wx0, int wy0,
+                                         int lane) {
+  const int4 ql = *reinterpret_cast<const int4*>(qlast);
+  const int t0 = max(0, min(cnt, ql.x - lo)), t1 = max(0, min(cnt, ql.y - lo));
+  const int t2 = max(0, min(cnt, ql.z - lo)), t3 = max(0, min(cnt, ql.w - lo));
+  const int nchunk = (max(max(t0, t1), max(t2, t3)) + 31) >> 5;
+  for (int c = 0; c < nchunk; ++c) {
+    const int j = (c << 5) + lane;
+    const char4 bx = B.box[j];  // j < kBatch; entries >= cnt are excluded by the tops
+    const bool xl = !(bx.y < wx0 || bx.x > wx0 + 3), xr = !(bx.y < wx0 + 4 || bx.x > wx0 + 7);
+    const bool yt = !(bx.w < wy0 || bx.z > wy0 + 1), yb = !(bx.w < wy0 + 2 || bx.z > wy0 + 3);
+    const unsigned b0 = __ballot_sync(0xffffffffu, xl && yt && j < t0);
+    const unsigned b1 = __ballot_sync(0xffffffffu, xr && yt && j < t1);
+    const unsigned b2 = __ballot_sync(0xffffffffu, xl && yb && j < t2);
+    const unsigned b3 = __ballot_sync(0xffffffffu, xr && yb && j < t3);
+    if (lane == 0) {
+      qm[0][c] = b0;
+      qm[1][c] = b1;
+      qm[2][c] = b2;
+      qm[3][c] = b3;
+    }
+  }
+  __syncwarp();
+  return nchunk;
+}
+
+// Descending order of the 32 quarters of a tile by a per-quarter count (ties
+// by quarter index): lane L of the calling warp returns the index of the
+// L-th largest.  Bitonic network over the warp's lanes; whatever the counts,
+// the result is a permutation of 0..31.
+__device__ __forceinline__ int quarter_rank_order(int count, int lane) {
+  int key = count, val = lane;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int ok = __shfl_xor_sync(0xffffffffu, key, j);
+      const int ov = __shfl_xor_sync(0xffffffffu, val, j);
+      const bool other_first = ok > key || (ok == key && ov < val);  // other precedes mine
+      const bool keep_first = ((lane & k) == 0) == ((lane & j) == 0);
+      if (keep_first == other_first) {
+        key = ok;
+        val = ov;
+      }
+    }
+  }
+  return val;
 }
 
 // The last contributor of each quarter of the warp (the largest `last` over
@@ -774,8 +794,9 @@ __global__ void __launch_bounds__(kRT, 6) raster_bwd_kernel(
     float2* E = S.e[k & 1];
     if (tid < cnt) stage_entry(B, tid, ox, oy, E);
     __syncthreads();
-    bwd_batch(B, S.acc, S.qm[warp], S.qlast[warp], cnt, lo, wx0, wy0, ix, iy, last, Tr, S0, S1,
-              S2, g0, g1, g2, lane, nullptr);
+    const int nw = box_masks(B, S.qm[warp], S.qlast[warp], cnt, lo, wx0, wy0, lane);
+    bwd_walk(B, S.acc, S.qm[warp][(lane >> 3) & 3], nw, lo, ix, iy, last, Tr, S0, S1, S2, g0, g1,
+             g2, lane);
     __syncthreads();
     bwd_flush(B, E, S.id[k & 1], S.acc, cnt, grads + 3 * view * n, tid);
     __syncthreads();
@@ -805,8 +826,13 @@ struct FusedSmem {
     } fw;  // forward
     struct {
       float acc[kBatch][9];
-      uint32_t qm[kWarps][4][kWords];
+      uint32_t qm[kWarps][4][kWords];  // masks of quarter warp * 4 + q
       alignas(16) int32_t qlast[kWarps][4];
+      // per-pixel state between batches, for a warp that takes other quarters
+      float pT[kRT], pS0[kRT], pS1[kRT], pS2[kRT];
+      int32_t plast[kRT];
+      uint8_t pg[kRT];     // signs of the L1 gradient, 2 bits per channel
+      uint8_t order[32];   // quarters by descending count of recorded entries
     } bw;  // backward
   } u;
   int32_t wcount[kWarps];
@@ -895,7 +921,21 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
   const float ix = (float)(px - tile_x * GS_TILE), iy = (float)(py - tile_y * GS_TILE);
   const int wx0 = (warp & 1) * 8, wy0 = (warp >> 1) * 4;
   float S0 = Tr * bg0, S1 = Tr * bg1, S2 = Tr * bg2;
-
+  // With the forward's record, each batch's 32 quarters are handed to the
+  // warps in descending order of their recorded entries (warp w takes the
+  // quarters ranked 4w..4w+3): a warp's step costs the longest of its four
+  // lists, and grouping lists of like length wastes fewer lanes.  A pixel's
+  // state then lives in shared memory between batches.
+  const bool regroup = rec_out != nullptr;
+  if (regroup) {
+    S.u.bw.pT[tid] = Tr;
+    S.u.bw.pS0[tid] = S0;
+    S.u.bw.pS1[tid] = S1;
+    S.u.bw.pS2[tid] = S2;
+    S.u.bw.plast[tid] = last;
+    const auto code = [](float g) { return g > 0.f ? 1u : (g < 0.f ? 2u : 0u); };
+    S.u.bw.pg[tid] = (uint8_t)(code(g0) | code(g1) << 2 | code(g2) << 4);
+  }
   // backward: batch k covers list positions [k kBatch, min((k+1) kBatch, max_last))
   // in slot k & 1, gathered and staged unless the forward left it there
   auto issue = [&](int k) {
@@ -936,9 +976,38 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
       slot(staged, k & 1) = k;
       __syncthreads();
     }
-    bwd_batch(B, S.u.bw.acc, S.u.bw.qm[warp], S.u.bw.qlast[warp], cnt, lo, wx0, wy0, ix, iy, last,
-              Tr, S0, S1, S2, g0, g1, g2, lane,
-              rec_out ? rec_out + (int64_t)k * kRec + warp * 4 * kWords : nullptr);
+    if (regroup) {
+      // the batch's record (quarter Q's words at Q * kWords), the quarters'
+      // order, then this lane's quarter and pixel
+      uint32_t* qall = &S.u.bw.qm[0][0][0];
+      if (tid < kRec) qall[tid] = __ldcg(rec_out + (int64_t)k * kRec + tid);
+      __syncthreads();
+      if (warp == 0) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) c += __popc(qall[lane * kWords + w]);
+        S.u.bw.order[lane] = (uint8_t)quarter_rank_order(c, lane);
+      }
+      __syncthreads();
+      const int Q = S.u.bw.order[warp * 4 + ((lane >> 3) & 3)];
+      const int p = Q * 8 + (lane & 7);
+      int qx, qy;
+      pixel_of(p, tile_x, tile_y, qx, qy);
+      float T = S.u.bw.pT[p], s0 = S.u.bw.pS0[p], s1 = S.u.bw.pS1[p], s2 = S.u.bw.pS2[p];
+      const uint32_t gc = S.u.bw.pg[p];
+      const auto sg = [&](uint32_t c2) { return c2 == 1u ? inv_count : (c2 == 2u ? -inv_count : 0.f); };
+      bwd_walk(B, S.u.bw.acc, qall + Q * kWords, kWords, lo, (float)(qx - tile_x * GS_TILE),
+               (float)(qy - tile_y * GS_TILE), S.u.bw.plast[p], T, s0, s1, s2, sg(gc & 3u),
+               sg((gc >> 2) & 3u), sg((gc >> 4) & 3u), lane);
+      S.u.bw.pT[p] = T;
+      S.u.bw.pS0[p] = s0;
+      S.u.bw.pS1[p] = s1;
+      S.u.bw.pS2[p] = s2;
+    } else {
+      const int nw = box_masks(B, S.u.bw.qm[warp], S.u.bw.qlast[warp], cnt, lo, wx0, wy0, lane);
+      bwd_walk(B, S.u.bw.acc, S.u.bw.qm[warp][(lane >> 3) & 3], nw, lo, ix, iy, last, Tr, S0, S1,
+               S2, g0, g1, g2, lane);
+    }
     __syncthreads();
     bwd_flush(B, S.e[k & 1], S.id[k & 1], S.u.bw.acc, cnt, grads + 3 * view * n, tid);
     __syncthreads();

@@ -94,6 +94,45 @@ __global__ void __launch_bounds__(256) adam_sparse_kernel(int64_t n, float* __re
   }
 }
 
+// Sparse, for n a multiple of 4: thread t owns columns 4t..4t+3 of all 59
+// rows, reads their visibility once, skips the group when none is visible,
+// and otherwise updates the visible lanes of each row with 16-byte accesses
+// (the other lanes are written back as read, bit for bit).
+__global__ void __launch_bounds__(256) adam_sparse4_kernel(int64_t n, float* __restrict__ p,
+                                                           const float* __restrict__ g,
+                                                           float* __restrict__ m,
+                                                           float* __restrict__ v,
+                                                           const uint8_t* __restrict__ visible,
+                                                           AdamK k,
+                                                           const int64_t* __restrict__ step_dev,
+                                                           float lr, const unsigned int* skip) {
+  if (!adam_prologue(k, step_dev, lr, skip)) return;
+  const int64_t ng = n >> 2;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const uchar4* vis4 = reinterpret_cast<const uchar4*>(visible);
+  float4* p4 = reinterpret_cast<float4*>(p);
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  float4* m4 = reinterpret_cast<float4*>(m);
+  float4* v4 = reinterpret_cast<float4*>(v);
+  for (int64_t c4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c4 < ng; c4 += stride) {
+    const uchar4 vv = vis4[c4];
+    if (!(vv.x | vv.y | vv.z | vv.w)) continue;
+#pragma unroll 4
+    for (int row = 0; row < GS_NPARAM; ++row) {
+      const int64_t i = (int64_t)row * ng + c4;
+      float4 P = p4[i], M = m4[i], V = v4[i];
+      const float4 G = __ldcs(g4 + i);
+      if (vv.x) adam_one(P.x, G.x, M.x, V.x, k);
+      if (vv.y) adam_one(P.y, G.y, M.y, V.y, k);
+      if (vv.z) adam_one(P.z, G.z, M.z, V.z, k);
+      if (vv.w) adam_one(P.w, G.w, M.w, V.w, k);
+      p4[i] = P;
+      m4[i] = M;
+      v4[i] = V;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) loss_l1_kernel(int64_t count, const float* __restrict__ img,
                                                       const float* __restrict__ tgt, float inv_count,
                                                       float* __restrict__ loss,
@@ -177,6 +216,11 @@ static gs_status adam_impl(int64_t n, float* params, const float* grad, float* m
     const int64_t want = div_up(count / 4 + 1, 256);
     const unsigned blocks = (unsigned)(want < 8 * sms ? want : 8 * sms);
     adam_dense_kernel<<<blocks, 256, 0, st>>>(count, params, grad, m, v, k, step_dev, lr, skip);
+  } else if (n % 4 == 0 && (reinterpret_cast<uintptr_t>(visible) & 3u) == 0) {
+    const int64_t want = div_up(n / 4, 256);
+    const unsigned blocks = (unsigned)(want < 8 * sms ? want : 8 * sms);
+    adam_sparse4_kernel<<<blocks, 256, 0, st>>>(n, params, grad, m, v, visible, k, step_dev, lr,
+                                                skip);
   } else {
     const int64_t want = div_up(n, 256);
     dim3 grid((unsigned)(want < 2 * sms ? want : 2 * sms), GS_NPARAM);

@@ -386,26 +386,37 @@ def test_project_bwd_matches_oracle(case):
     assert np.array_equal(visible.cpu().numpy(), o["visible"])
 
 
+@pytest.mark.parametrize("n", [10_001, 10_000])
 @pytest.mark.parametrize("sparse", [False, True])
-def test_adam_matches_oracle(sparse):
+def test_adam_matches_oracle(sparse, n):
+    """Five Adam steps against the oracle; sparse mode with n % 4 == 0 takes
+    the 16-byte path, otherwise the per-column one.  Columns not visible keep
+    p, m and v bit for bit."""
     import oracle
     gs = _gs()
     rng = np.random.default_rng(11)
-    n = 10_001
     p = rng.standard_normal((59, n)).astype(np.float32)
     m = np.zeros((59, n), np.float32)
     v = np.zeros((59, n), np.float32)
     P, M, Vv = _cuda(p), _cuda(m), _cuda(v)
     po, mo, vo = p.astype(np.float64), m.astype(np.float64), v.astype(np.float64)
+    ever_visible = np.zeros(n, bool)
     for t in range(1, 6):
         g = (rng.standard_normal((59, n)) * 10.0 ** rng.uniform(-6, -2, (59, n))).astype(np.float32)
         vis = (rng.random(n) < 0.4).astype(np.uint8) if sparse else None
+        if sparse:
+            vis[: n // 3 // 4 * 4] = 0  # whole groups of four columns never visible
+            ever_visible |= vis.astype(bool)
         gs.gs_adam_step(P, _cuda(g), M, Vv, t, 1e-3, visible=None if vis is None else _cuda(vis))
         oracle.adam(po, g.astype(np.float64), mo, vo, t, 1e-3, visible=vis)
     assert rel_l2(P.cpu().numpy(), po) <= ADAM_REL_L2
     assert rel_l2(P.cpu().numpy() - p, po - p) <= 1e-3
     assert rel_l2(M.cpu().numpy(), mo) <= ADAM_REL_L2
     assert rel_l2(Vv.cpu().numpy(), vo) <= ADAM_REL_L2
+    if sparse:
+        never = ~ever_visible
+        assert np.array_equal(P.cpu().numpy()[:, never], p[:, never])
+        assert np.all(M.cpu().numpy()[:, never] == 0) and np.all(Vv.cpu().numpy()[:, never] == 0)
 
 
 @pytest.mark.parametrize("fused", [False, True])

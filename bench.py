@@ -48,19 +48,21 @@ BWD_FLOP_EVAL = 13       # per pair visited below the last contributor (+1 exp)
 BWD_FLOP_INCLUDED = 44   # per contributing pair: gradients of colour, alpha, geometry
 PROJ_READ = 236          # B per Gaussian: 59 fp32 parameters
 SPLAT_BYTES = 48         # B per visible (view, Gaussian) row
-CULLED_BYTES = 8         # B per culled row (radius, tiles)
+CULLED_BYTES = 4         # B per culled row (its tile count)
 ADAM_BYTES = 59 * 28     # B per Gaussian: read p, g, m, v; write p, m, v
 LOSS_BYTES = 36          # B per pixel: image, target read, gradient written (3 channels)
 PROJ_BWD_BYTES = 472     # B per Gaussian: parameters read, gradient written
 PROJ_BWD_ROW = 60        # B per visible row: 36 gradient + 24 conic/colour
-# binning: every row's tile word (16 B) is read; a visible row's position word
-# (16 B) read and its sort element, depth/row and rectangle words written
-# (24 B), 4 depth passes (16 B each), its sorted element and rectangle read at
-# emission (16 B); an intersection written at emission (8 B), 16 B per tile
-# pass (read + write), in the last one its row's depth/row word read and 4 B
-# more written (ids; the tile ranges are marked by that pass)
-BIN_ROW = 16
-BIN_VISIBLE = 16 + 24 + 4 * 16 + 16
+PROJ_BWD_COUNT = 4       # B per row: its tile count, read to find the visible rows
+# binning: every row's tile count (4 B) is read; a visible row's record
+# (mean, radius, depth: 32 B) read and its sort element, depth/row and
+# rectangle words written (24 B), 4 depth passes (16 B each), its sorted
+# element and rectangle read at emission (16 B); an intersection written at
+# emission (8 B), 16 B per tile pass (read + write), in the last one its row's
+# depth/row word read and 4 B more written (ids; the tile ranges are marked by
+# that pass)
+BIN_ROW = 4
+BIN_VISIBLE = 32 + 24 + 4 * 16 + 16
 BIN_ISECT = 8 + 8 + 4
 
 FP32_LANES_PER_SM = 128
@@ -475,7 +477,7 @@ def our_arm(args, rank, world, local):
     torch.cuda.synchronize()
     tested, included = [int(x) for x in counts.cpu()]
     bwd_eval = int(step.n_contrib.to(torch.int64).sum().item())
-    visible_rows = int((step.splats.view(torch.int32)[:, 10] > 0).sum().item())
+    visible_rows = int((step.tile_counts > 0).sum().item())
     I = step.n_isect
 
     if fused:
@@ -603,8 +605,8 @@ def our_arm(args, rank, world, local):
         "bin_and_sort": ("hbm", (BIN_ROW * rows + BIN_VISIBLE * visible_rows +
                                  (BIN_ISECT + 16 * tile_passes) * I) / 1e9, "GB/s", hbm_peak),
         "loss_l1": ("hbm", LOSS_BYTES * V * W * H / 1e9, "GB/s", hbm_peak),
-        "project_bwd": ("hbm", (PROJ_BWD_BYTES * n + PROJ_BWD_ROW * visible_rows) / 1e9, "GB/s",
-                        hbm_peak),
+        "project_bwd": ("hbm", (PROJ_BWD_BYTES * n + PROJ_BWD_ROW * visible_rows +
+                                PROJ_BWD_COUNT * rows) / 1e9, "GB/s", hbm_peak),
         "adam": ("hbm", ADAM_BYTES * adam_cols / 1e9, "GB/s", hbm_peak),
     }
     if fused:

@@ -50,14 +50,15 @@ def lib():
         raise RuntimeError("libgs103.so not built: %s is missing (run build())" % LIB_PATH)
     L = C.CDLL(LIB_PATH)
     vp, i64, i32, f32, sz = C.c_void_p, C.c_int64, C.c_int32, C.c_float, C.c_size_t
-    L.gs_project.argtypes = [i64, vp, vp, i32, vp, vp]
+    L.gs_project.argtypes = [i64, vp, vp, i32, vp, vp, vp]
     L.gs_bin_workspace_bytes.argtypes = [i64, i64]
     L.gs_bin_workspace_bytes.restype = sz
     L.gs_key_bits.argtypes = [i32, i32, i32]
     L.gs_key_bits.restype = i32
-    L.gs_bin_and_sort.argtypes = [i64, i32, vp, i32, i32, vp, sz, i64, vp, vp, vp, vp, vp]
+    L.gs_bin_and_sort.argtypes = [i64, i32, vp, vp, i32, i32, vp, sz, i64, vp, vp, vp, vp, vp]
     L.gs_workspace_status.argtypes = [vp, vp]
-    L.gs_bin_and_sort_async.argtypes = [i64, i32, vp, i32, i32, vp, sz, i64, vp, vp, vp, vp, vp]
+    L.gs_bin_and_sort_async.argtypes = [i64, i32, vp, vp, i32, i32, vp, sz, i64, vp, vp, vp, vp,
+                                        vp]
     L.gs_adam_step_dev.argtypes = [i64, vp, vp, vp, vp, vp, f32, f32, f32, f32, vp, vp, vp]
     L.gs_step_advance.argtypes = [vp, vp, vp]
     L.gs_tile_order.argtypes = [i64, vp, vp, vp]
@@ -65,7 +66,7 @@ def lib():
     L.gs_rasterize_fwd_counted.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                            vp, vp]
     L.gs_loss_l1.argtypes = [vp, vp, i64, vp, vp, vp]
-    L.gs_rasterize_bwd.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.gs_rasterize_bwd.argtypes = [i64, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.gs_morton_workspace_bytes.argtypes = [i64]
     L.gs_morton_workspace_bytes.restype = sz
     L.gs_morton_order.argtypes = [i64, vp, vp, sz, vp, vp]
@@ -76,11 +77,11 @@ def lib():
     L.gs_compact_workspace_bytes.argtypes = [i64]
     L.gs_compact_workspace_bytes.restype = sz
     L.gs_compact_index.argtypes = [i64, vp, vp, sz, vp, vp, vp]
-    L.gs_rasterize_fused.argtypes = [i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                     vp, vp, sz, vp]
+    L.gs_rasterize_fused.argtypes = [i64, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     vp, vp, vp, sz, vp]
     L.gs_rasterize_workspace_bytes.argtypes = [i32, i32, i32, i64]
     L.gs_rasterize_workspace_bytes.restype = sz
-    L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp]
+    L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp, vp]
     L.gs_adam_step.argtypes = [i64, vp, vp, vp, vp, i64, f32, f32, f32, f32, vp, vp]
     L.gs_status_string.argtypes = [C.c_int]
     L.gs_status_string.restype = C.c_char_p
@@ -147,11 +148,14 @@ def tiles_per_view(width, height):
 # the C ABI, one wrapper per function
 
 
-def gs_project(params, cams, splats, stream=None):
+def gs_project(params, cams, splats, stream=None, tile_counts=None):
+    """tile_counts: None, or a CUDA int32 tensor of V*n entries (then culled
+    rows get a count of 0 and no record)."""
     n = params.shape[1]
     cs = cameras_struct(cams)
     _check("gs_project", lib().gs_project(n, _dev(params, torch.float32, "params"), C.cast(cs, C.c_void_p),
                                           len(cams), _dev(splats, torch.float32, "splats"),
+                                          _dev(tile_counts, torch.int32, "tile_counts"),
                                           _stream(stream)))
 
 
@@ -164,11 +168,12 @@ def gs_key_bits(n_views, width, height):
 
 
 def gs_bin_and_sort(n, n_views, splats, width, height, workspace, capacity, keys, vals, ranges,
-                    stream=None):
+                    stream=None, tile_counts=None):
     """Returns (status, n_isect); status is GS_OK or GS_ERR_CAPACITY, other
     statuses raise GSError."""
     out = C.c_int64(0)
-    st = lib().gs_bin_and_sort(n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+    st = lib().gs_bin_and_sort(n, n_views, _dev(splats, torch.float32, "splats"),
+                               _dev(tile_counts, torch.int32, "tile_counts"), width, height,
                                _dev(workspace, torch.uint8, "workspace"), workspace.numel(), capacity,
                                _dev(keys, torch.int64, "keys"), _dev(vals, torch.int32, "vals"),
                                _dev(ranges, torch.int64, "ranges"), C.byref(out), _stream(stream))
@@ -182,10 +187,11 @@ def gs_workspace_status(workspace, stream=None):
 
 
 def gs_bin_and_sort_async(n, n_views, splats, width, height, workspace, capacity, keys, vals,
-                          ranges, n_isect, stream=None):
+                          ranges, n_isect, stream=None, tile_counts=None):
     """gs_bin_and_sort without a host synchronisation; n_isect: CUDA int64 [1]."""
     _check("gs_bin_and_sort_async", lib().gs_bin_and_sort_async(
-        n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+        n, n_views, _dev(splats, torch.float32, "splats"),
+        _dev(tile_counts, torch.int32, "tile_counts"), width, height,
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), capacity,
         _dev(keys, torch.int64, "keys"), _dev(vals, torch.int32, "vals"),
         _dev(ranges, torch.int64, "ranges"), _dev(n_isect, torch.int64, "n_isect"),
@@ -250,10 +256,11 @@ def gs_loss_l1(image, target, loss, dL_dimage, stream=None):
 
 
 def gs_rasterize_bwd(n, n_views, splats, width, height, vals, ranges, bg, T_final, n_contrib,
-                     dL_dimage, grads, stream=None, tile_order=None):
+                     dL_dimage, grads, stream=None, tile_order=None, tile_counts=None):
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
     _check("gs_rasterize_bwd", lib().gs_rasterize_bwd(
-        n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+        n, n_views, _dev(splats, torch.float32, "splats"),
+        _dev(tile_counts, torch.int32, "tile_counts"), width, height,
         _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"),
         _dev(tile_order, torch.int32, "tile_order"), C.cast(bgv, C.c_void_p),
         _dev(T_final, torch.float32, "T_final"), _dev(n_contrib, torch.int32, "n_contrib"),
@@ -267,12 +274,13 @@ def gs_rasterize_workspace_bytes(n_views, width, height, capacity):
 
 def gs_rasterize_fused(n, n_views, splats, width, height, vals, ranges, bg, target, image,
                        T_final, n_contrib, loss, grads, stream=None, tile_order=None,
-                       workspace=None):
+                       workspace=None, tile_counts=None):
     """workspace: None, or a CUDA uint8 tensor of gs_rasterize_workspace_bytes()
     bytes (the backward then walks the pairs the forward composited)."""
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
     _check("gs_rasterize_fused", lib().gs_rasterize_fused(
-        n, n_views, _dev(splats, torch.float32, "splats"), width, height,
+        n, n_views, _dev(splats, torch.float32, "splats"),
+        _dev(tile_counts, torch.int32, "tile_counts"), width, height,
         _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"),
         _dev(tile_order, torch.int32, "tile_order"), C.cast(bgv, C.c_void_p),
         _dev(target, torch.float32, "target"), _dev(image, torch.float32, "image"),
@@ -336,12 +344,14 @@ def gs_compact_index(mask, workspace, idx, n_keep, stream=None):
         _stream(stream)))
 
 
-def gs_project_bwd(params, cams, splats, grads, grad, visible=None, stream=None):
+def gs_project_bwd(params, cams, splats, grads, grad, visible=None, stream=None,
+                   tile_counts=None):
     n = params.shape[1]
     cs = cameras_struct(cams)
     _check("gs_project_bwd", lib().gs_project_bwd(
         n, _dev(params, torch.float32, "params"), C.cast(cs, C.c_void_p), len(cams),
-        _dev(splats, torch.float32, "splats"), _dev(grads, torch.float32, "grads"),
+        _dev(splats, torch.float32, "splats"), _dev(tile_counts, torch.int32, "tile_counts"),
+        _dev(grads, torch.float32, "grads"),
         _dev(grad, torch.float32, "grad"), _dev(visible, torch.uint8, "visible"), _stream(stream)))
 
 
@@ -390,6 +400,8 @@ class TrainStep:
         rows = self.V * self.n
         f32 = dict(device=dev, dtype=torch.float32)
         self.splats = torch.empty((rows, SPLAT_FLOATS), **f32)
+        # per-row tile counts: a culled row costs these 4 bytes, not a record
+        self.tile_counts = torch.zeros(rows, device=dev, dtype=torch.int32)
         self.grads2d = torch.empty((rows, SPLAT_FLOATS), **f32)
         self.grad = torch.empty_like(params)
         self.m = torch.zeros_like(params)
@@ -422,15 +434,17 @@ class TrainStep:
 
     # the seven library calls of a step, in order
     def project(self, stream=None):
-        gs_project(self.params, self.cams, self.splats, stream)
+        gs_project(self.params, self.cams, self.splats, stream, tile_counts=self.tile_counts)
 
     def bin_and_sort(self, stream=None):
         st, I = gs_bin_and_sort(self.n, self.V, self.splats, self.W, self.H, self.workspace,
-                                self.capacity, self.keys, self.vals, self.ranges, stream)
+                                self.capacity, self.keys, self.vals, self.ranges, stream,
+                                tile_counts=self.tile_counts)
         if st == GS_ERR_CAPACITY:
             self._alloc_isect(int(I * 1.25) + 1024)
             st, I = gs_bin_and_sort(self.n, self.V, self.splats, self.W, self.H, self.workspace,
-                                    self.capacity, self.keys, self.vals, self.ranges, stream)
+                                    self.capacity, self.keys, self.vals, self.ranges, stream,
+                                    tile_counts=self.tile_counts)
             _check("gs_bin_and_sort", st)
         self.n_isect = I
         gs_tile_order(self.ranges, self.tile_order, stream)
@@ -451,17 +465,17 @@ class TrainStep:
     def rasterize_bwd(self, stream=None):
         gs_rasterize_bwd(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges, self.bg,
                          self.T_final, self.n_contrib, self.dL_dimage, self.grads2d, stream,
-                         tile_order=self.tile_order)
+                         tile_order=self.tile_order, tile_counts=self.tile_counts)
 
     def rasterize_fused(self, stream=None):
         gs_rasterize_fused(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges,
                            self.bg, self.target, self.image, self.T_final, self.n_contrib,
                            self.loss, self.grads2d, stream, tile_order=self.tile_order,
-                           workspace=self.raster_ws)
+                           workspace=self.raster_ws, tile_counts=self.tile_counts)
 
     def project_bwd(self, stream=None):
         gs_project_bwd(self.params, self.cams, self.splats, self.grads2d, self.grad, self.visible,
-                       stream)
+                       stream, tile_counts=self.tile_counts)
 
     def adam(self, stream=None):
         self.t += 1
@@ -549,7 +563,8 @@ class TrainStep:
     def _graph_body(self):
         self.project()
         gs_bin_and_sort_async(self.n, self.V, self.splats, self.W, self.H, self.workspace,
-                              self.capacity, self.keys, self.vals, self.ranges, self.n_isect_dev)
+                              self.capacity, self.keys, self.vals, self.ranges, self.n_isect_dev,
+                              tile_counts=self.tile_counts)
         gs_tile_order(self.ranges, self.tile_order)
         if self.fused:
             self.rasterize_fused()

@@ -70,7 +70,7 @@ gs_status scratch_for_current_device(void** out) {
 }  // namespace
 
 extern "C" gs_status gs_bin_and_sort_static(int64_t n, int32_t n_views, const gs_splat* splats,
-                                            int32_t width, int32_t height, int64_t capacity,
+                                            const int32_t* tile_counts, int32_t width, int32_t height, int64_t capacity,
                                             uint64_t* keys, uint32_t* vals, int64_t* ranges,
                                             int64_t* n_isect, void* stream) {
   if (n < 0 || n_views < 1 || n_views > GS_MAX_VIEWS || capacity < 0) return GS_ERR_INVALID_ARG;
@@ -79,6 +79,6 @@ extern "C" gs_status gs_bin_and_sort_static(int64_t n, int32_t n_views, const gs
   void* ws = nullptr;
   const gs_status st = scratch_for_current_device(&ws);
   if (st != GS_OK) return st;
-  return gs_bin_and_sort(n, n_views, splats, width, height, ws, kStaticWsBytes, capacity, keys,
-                         vals, ranges, n_isect, stream);
+  return gs_bin_and_sort(n, n_views, splats, tile_counts, width, height, ws, kStaticWsBytes,
+                         capacity, keys, vals, ranges, n_isect, stream);
 }

@@ -180,10 +180,12 @@ __device__ long long lookback_prefix_warp(uint64_t* status, int64_t part, long l
 //    R by the last partition; the depth-digit histograms.  Positive depths
 //    order as their bit patterns.  A row whose rectangle disagrees with its
 //    stored tile count (records not produced by gs_project) is left out and
-//    raises the device-check bit.
+//    raises the device-check bit.  With a tile-count array the counts are
+//    read first (4 bytes a row) and only the visible rows' records after.
 __global__ void __launch_bounds__(kCompThreads) compact_rows_kernel(
     int64_t n_rows, int64_t n, int32_t tiles_x, int32_t tiles_y, int64_t T, int64_t capacity,
-    const float4* __restrict__ splats, uint64_t* __restrict__ sort_in,
+    const float4* __restrict__ splats, const int32_t* __restrict__ counts,
+    uint64_t* __restrict__ sort_in,
     uint64_t* __restrict__ row_u, uint64_t* __restrict__ row_rect, uint32_t* __restrict__ hist,
     uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
   __shared__ uint32_t sh[kDepthPasses * kRadix];
@@ -203,15 +205,23 @@ __global__ void __launch_bounds__(kCompThreads) compact_rows_kernel(
   uint32_t mask[kCompItems];
   uint32_t wcount = 0;
   unsigned long long tiles_sum = 0;
+  int32_t cnt[kCompItems];
+  if (counts) {
+#pragma unroll
+    for (int i = 0; i < kCompItems; ++i) {
+      const int64_t r = wbase + 32 * i + lane;
+      cnt[i] = r < n_rows ? __ldg(counts + r) : 0;
+    }
+  }
 #pragma unroll
   for (int i = 0; i < kCompItems; ++i) {
     const int64_t r = wbase + 32 * i + lane;
     bool vis = false;
     dbits[i] = 0;
     rect[i] = 0;
-    if (r < n_rows) {
+    if (r < n_rows && (!counts || cnt[i] > 0)) {
       const float4 tail = splats[3 * r + 2];
-      const int32_t tiles = __float_as_int(tail.w);
+      const int32_t tiles = counts ? cnt[i] : __float_as_int(tail.w);
       if (tiles > 0) {
         const float4 head = splats[3 * r];
         int32_t x0, x1, y0, y1;
@@ -952,12 +962,13 @@ uint64_t* rows_buffer(const BinShape& s, const BinBufs& b, uint64_t* keys) {
 }
 
 gs_status launch_compaction(const BinShape& s, const BinBufs& b, const gs_splat* splats,
-                            int64_t capacity, uint64_t* keys, cudaStream_t st) {
+                            const int32_t* counts, int64_t capacity, uint64_t* keys,
+                            cudaStream_t st) {
   const int64_t parts = div_up(s.n_rows, kCompPart);
   GS_CUDA(cudaMemsetAsync(b.scan_status, 0, sizeof(uint64_t) * (size_t)parts, st));
   compact_rows_kernel<<<(unsigned)parts, kCompThreads, 0, st>>>(
       s.n_rows, s.n, s.tiles_x, s.tiles_y, s.T, capacity, reinterpret_cast<const float4*>(splats),
-      rows_buffer(s, b, keys), b.row_u, b.row_rect, b.hist, b.scan_status, b.hdr);
+      counts, rows_buffer(s, b, keys), b.row_u, b.row_rect, b.hist, b.scan_status, b.hdr);
   GS_CHECK_LAUNCH();
   return GS_OK;
 }
@@ -1046,8 +1057,9 @@ extern "C" gs_status gs_selftest_lookback_timeout(void* workspace, size_t ws_byt
   GS_CUDA(cudaMemsetAsync(b.scan_status, 0, sizeof(uint64_t) * 2, st));
   const unsigned one = 1;
   GS_CUDA(cudaMemcpyAsync(&b.hdr->scan_ticket, &one, sizeof(one), cudaMemcpyHostToDevice, st));
-  compact_rows_kernel<<<1, kCompThreads, 0, st>>>(0, 1, 1, 1, 1, 1, nullptr, b.tmp, b.row_u,
-                                                  b.row_rect, b.hist, b.scan_status, b.hdr);
+  compact_rows_kernel<<<1, kCompThreads, 0, st>>>(0, 1, 1, 1, 1, 1, nullptr, nullptr, b.tmp,
+                                                  b.row_u, b.row_rect, b.hist, b.scan_status,
+                                                  b.hdr);
   GS_CHECK_LAUNCH();
   return gs_workspace_status(workspace, stream);
 }
@@ -1068,7 +1080,7 @@ extern "C" gs_status gs_workspace_status(void* workspace, void* stream) {
 }
 
 extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat* splats,
-                                     int32_t width, int32_t height, void* workspace,
+                                     const int32_t* tile_counts, int32_t width, int32_t height, void* workspace,
                                      size_t ws_bytes, int64_t capacity, uint64_t* keys,
                                      uint32_t* vals, int64_t* ranges, int64_t* n_isect,
                                      void* stream) {
@@ -1078,7 +1090,7 @@ extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat*
     return GS_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(s.n_rows, capacity);
   if (ws_bytes < L.total || !aligned16(workspace)) return GS_ERR_INVALID_ARG;
-  if (!ranges || (s.n_rows > 0 && (!splats || !aligned16(splats))) ||
+  if (!ranges || (s.n_rows > 0 && (!splats || !aligned16(splats))) || !aligned4(tile_counts) ||
       (capacity > 0 && (!keys || !vals)))
     return GS_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
@@ -1090,7 +1102,7 @@ extern "C" gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat*
   GS_CUDA(cudaMemsetAsync(&b.hdr->total, 0, sizeof(b.hdr->total), st));
   GS_CUDA(cudaMemsetAsync(b.hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, st));
   if (s.n_rows > 0) {
-    const gs_status e = launch_compaction(s, b, splats, capacity, keys, st);
+    const gs_status e = launch_compaction(s, b, splats, tile_counts, capacity, keys, st);
     if (e != GS_OK) return e;
   }
   struct { unsigned long long total; unsigned int error, ticket; unsigned long long rows; } h{};
@@ -1209,17 +1221,17 @@ extern "C" gs_status gs_gather_columns(int64_t rows, int64_t n_src, int64_t n_ds
 // from the workspace, and an overflow is reported through the workspace
 // status word.
 extern "C" gs_status gs_bin_and_sort_async(int64_t n, int32_t n_views, const gs_splat* splats,
-                                           int32_t width, int32_t height, void* workspace,
-                                           size_t ws_bytes, int64_t capacity, uint64_t* keys,
-                                           uint32_t* vals, int64_t* ranges, int64_t* n_isect,
-                                           void* stream) {
+                                           const int32_t* tile_counts, int32_t width,
+                                           int32_t height, void* workspace, size_t ws_bytes,
+                                           int64_t capacity, uint64_t* keys, uint32_t* vals,
+                                           int64_t* ranges, int64_t* n_isect, void* stream) {
   BinShape s;
   if (!bin_shape(n, n_views, width, height, s) || capacity < 1 ||
       capacity > (int64_t)0xFFFFFFFFll || !workspace || !n_isect)
     return GS_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(s.n_rows, capacity);
   if (ws_bytes < L.total || !aligned16(workspace) || !ranges || !keys || !vals ||
-      (s.n_rows > 0 && (!splats || !aligned16(splats))))
+      (s.n_rows > 0 && (!splats || !aligned16(splats))) || !aligned4(tile_counts))
     return GS_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   const BinBufs b = bin_bufs(workspace, L);
@@ -1229,7 +1241,7 @@ extern "C" gs_status gs_bin_and_sort_async(int64_t n, int32_t n_views, const gs_
   GS_CUDA(cudaMemsetAsync(b.hist, 0, sizeof(uint32_t) * kMaxPasses * kRadix, st));
   GS_CUDA(cudaMemsetAsync(ranges, 0, sizeof(int64_t) * 2 * (size_t)s.n_flat, st));
   if (s.n_rows > 0) {
-    const gs_status e = launch_compaction(s, b, splats, capacity, keys, st);
+    const gs_status e = launch_compaction(s, b, splats, tile_counts, capacity, keys, st);
     if (e != GS_OK) return e;
   }
   check_capacity_kernel<<<1, 1, 0, st>>>(b.hdr, capacity, n_isect);

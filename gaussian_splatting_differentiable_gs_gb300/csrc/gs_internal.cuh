@@ -96,6 +96,7 @@ __device__ __forceinline__ void tile_rect(float mx, float my, int32_t radius, in
 __host__ __device__ inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Binning workspace: byte offset of the device status word, and its bit for
 // "intersections exceed capacity" (set by the asynchronous binning).

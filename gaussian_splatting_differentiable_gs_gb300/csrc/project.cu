@@ -9,6 +9,10 @@
 // One thread per Gaussian reads its 59 parameters once (coalesced rows of
 // the [59][n] SoA array) and loops over the views, so the parameter traffic
 // is paid once per step however many cameras are batched.  HBM-bound.
+// With a tile-count array, a culled row costs 4 written bytes (its count)
+// instead of a record, and the backward reads the counts to find the rows
+// it needs, so that scenes where a few per cent of the rows are visible
+// move only what is visible.
 #include <math.h>
 
 #include "gs_internal.cuh"
@@ -188,7 +192,8 @@ __device__ __forceinline__ void view_geom(const Gauss& G, const CamK& C, ViewGeo
 
 __global__ void __launch_bounds__(128, 5) project_fwd_kernel(int64_t n, const float* __restrict__ params,
                                                           const __grid_constant__ CamSet cs,
-                                                          float4* __restrict__ out) {
+                                                          float4* __restrict__ out,
+                                                          int32_t* __restrict__ counts) {
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= n) return;
   Gauss G;
@@ -216,7 +221,8 @@ __global__ void __launch_bounds__(128, 5) project_fwd_kernel(int64_t n, const fl
       tiles = (x1 - x0) * (y1 - y0);
     }
     if (tiles == 0) {
-      rec[2] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (counts) counts[row] = 0;
+      else rec[2] = make_float4(0.f, 0.f, 0.f, 0.f);
       continue;
     }
     if (!have_sh) {
@@ -240,17 +246,38 @@ __global__ void __launch_bounds__(128, 5) project_fwd_kernel(int64_t n, const fl
     rec[0] = make_float4(mx, my, V.c * idet, -V.b * idet);
     rec[1] = make_float4(V.a * idet, G.opacity, col[0], col[1]);
     rec[2] = make_float4(col[2], V.p[2], __int_as_float(radius), __int_as_float(tiles));
+    if (counts) counts[row] = tiles;
   }
 }
 
 __global__ void __launch_bounds__(128, 5) project_bwd_kernel(int64_t n, const float* __restrict__ params,
                                                           const __grid_constant__ CamSet cs,
                                                           const float4* __restrict__ splats,
+                                                          const int32_t* __restrict__ counts,
                                                           const float4* __restrict__ grads,
                                                           float* __restrict__ grad,
                                                           uint8_t* __restrict__ visible) {
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= n) return;
+  // the views in which the row is visible, all loads issued up front
+  uint32_t vmask = 0;
+  if (counts) {
+#pragma unroll
+    for (int v = 0; v < GS_MAX_VIEWS; ++v)
+      if (v < cs.n_views && __ldg(counts + (int64_t)v * n + g) > 0) vmask |= 1u << v;
+  } else {
+#pragma unroll
+    for (int v = 0; v < GS_MAX_VIEWS; ++v)
+      if (v < cs.n_views && __float_as_int(splats[3 * ((int64_t)v * n + g) + 2].z) > 0)
+        vmask |= 1u << v;
+  }
+  float* out = grad + g;
+  if (!vmask) {  // seen by no view: a zero gradient column
+#pragma unroll
+    for (int i = 0; i < GS_NPARAM; ++i) out[i * n] = 0.f;
+    if (visible) visible[g] = 0;
+    return;
+  }
   Gauss G;
   load_gauss(params + g, n, G);
   float g_mu[3] = {0.f, 0.f, 0.f}, g_ls[3] = {0.f, 0.f, 0.f}, g_q[4] = {0.f, 0.f, 0.f, 0.f};
@@ -259,12 +286,10 @@ __global__ void __launch_bounds__(128, 5) project_bwd_kernel(int64_t n, const fl
   float* g_sh_col = &s_gsh[0][threadIdx.x];
 #pragma unroll
   for (int k = 0; k < 48; ++k) g_sh_col[128 * k] = 0.f;
-  bool any = false;
-  for (int v = 0; v < cs.n_views; ++v) {
+  for (uint32_t vm = vmask; vm; vm &= vm - 1u) {
+    const int v = __ffs(vm) - 1;
     const int64_t row = (int64_t)v * n + g;
     const float4 r2 = splats[3 * row + 2];
-    if (__float_as_int(r2.z) <= 0) continue;
-    any = true;
     const CamK& C = cs.c[v];
     const float4 r0 = splats[3 * row], r1 = splats[3 * row + 1];
     const float4 q0 = grads[3 * row], q1 = grads[3 * row + 1], q2 = grads[3 * row + 2];
@@ -386,14 +411,13 @@ __global__ void __launch_bounds__(128, 5) project_bwd_kernel(int64_t n, const fl
     const float dq = w * gqn[0] + qx * gqn[1] + qy * gqn[2] + qz * gqn[3];
     for (int i = 0; i < 4; ++i) g_q[i] += (gqn[i] - G.qn[i] * dq) * G.qinv;
   }
-  float* out = grad + g;
   for (int i = 0; i < 3; ++i) out[i * n] = g_mu[i];
   for (int i = 0; i < 3; ++i) out[(3 + i) * n] = g_ls[i];
   for (int i = 0; i < 4; ++i) out[(6 + i) * n] = g_q[i];
   out[10 * n] = g_logit;
 #pragma unroll
   for (int k = 0; k < 48; ++k) out[(11 + k) * n] = g_sh_col[128 * k];
-  if (visible) visible[g] = any ? 1 : 0;
+  if (visible) visible[g] = 1;
 }
 
 }  // namespace
@@ -402,30 +426,32 @@ __global__ void __launch_bounds__(128, 5) project_bwd_kernel(int64_t n, const fl
 using namespace gs;
 
 extern "C" gs_status gs_project(int64_t n, const float* params, const gs_camera* cams,
-                                int32_t n_views, gs_splat* splats, void* stream) {
+                                int32_t n_views, gs_splat* splats, int32_t* tile_counts,
+                                void* stream) {
   if (n < 0 || n >= (int64_t(1) << 32) || !cams_valid(cams, n_views)) return GS_ERR_INVALID_ARG;
   if (n == 0) return GS_OK;
-  if (!params || !splats || !aligned16(splats)) return GS_ERR_INVALID_ARG;
+  if (!params || !splats || !aligned16(splats) || !aligned4(tile_counts)) return GS_ERR_INVALID_ARG;
   const CamSet cs = make_camset(cams, n_views);
   const int threads = 128;
   project_fwd_kernel<<<(unsigned)div_up(n, threads), threads, 0, (cudaStream_t)stream>>>(
-      n, params, cs, reinterpret_cast<float4*>(splats));
+      n, params, cs, reinterpret_cast<float4*>(splats), tile_counts);
   GS_CHECK_LAUNCH();
   return GS_OK;
 }
 
 extern "C" gs_status gs_project_bwd(int64_t n, const float* params, const gs_camera* cams,
                                     int32_t n_views, const gs_splat* splats,
-                                    const gs_splat_grad* grads, float* grad, uint8_t* visible,
-                                    void* stream) {
+                                    const int32_t* tile_counts, const gs_splat_grad* grads,
+                                    float* grad, uint8_t* visible, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 32) || !cams_valid(cams, n_views)) return GS_ERR_INVALID_ARG;
   if (n == 0) return GS_OK;
-  if (!params || !splats || !grads || !grad || !aligned16(splats) || !aligned16(grads))
+  if (!params || !splats || !grads || !grad || !aligned16(splats) || !aligned16(grads) ||
+      !aligned4(tile_counts))
     return GS_ERR_INVALID_ARG;
   const CamSet cs = make_camset(cams, n_views);
   const int threads = 128;
   project_bwd_kernel<<<(unsigned)div_up(n, threads), threads, 0, (cudaStream_t)stream>>>(
-      n, params, cs, reinterpret_cast<const float4*>(splats),
+      n, params, cs, reinterpret_cast<const float4*>(splats), tile_counts,
       reinterpret_cast<const float4*>(grads), grad, visible);
   GS_CHECK_LAUNCH();
   return GS_OK;

@@ -1015,6 +1015,41 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
   cp_async_wait<0>();
 }
 
+// Zeroes the gradient records of the rows with a positive tile count (the
+// only rows whose gradients the compositing writes and the projection
+// backward reads): 4 bytes read a row, 48 written a visible row.
+__global__ void __launch_bounds__(256) zero_visible_grads_kernel(int64_t rows,
+                                                                 const int32_t* __restrict__ counts,
+                                                                 float4* __restrict__ grads) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += stride) {
+    if (__ldg(counts + r) > 0) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      grads[3 * r] = z;
+      grads[3 * r + 1] = z;
+      grads[3 * r + 2] = z;
+    }
+  }
+}
+
+// The gradient records' zeroing before a backward: every row, or with tile
+// counts only the visible ones.
+gs_status zero_grads(int64_t rows, const int32_t* counts, gs_splat_grad* grads, cudaStream_t st) {
+  if (rows <= 0) return GS_OK;
+  if (!counts) {
+    GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)rows, st));
+    return GS_OK;
+  }
+  int dev = 0, sms = 0;
+  GS_CUDA(cudaGetDevice(&dev));
+  GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t want = div_up(rows, 256);
+  const unsigned blocks = (unsigned)(want < 8 * sms ? want : 8 * sms);
+  zero_visible_grads_kernel<<<blocks, 256, 0, st>>>(rows, counts, reinterpret_cast<float4*>(grads));
+  GS_CHECK_LAUNCH();
+  return GS_OK;
+}
+
 }  // namespace
 }  // namespace gs
 
@@ -1097,7 +1132,7 @@ extern "C" size_t gs_rasterize_workspace_bytes(int32_t n_views, int32_t width, i
 }
 
 extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
-                                        int32_t width, int32_t height, const uint32_t* vals,
+                                        const int32_t* tile_counts, int32_t width, int32_t height, const uint32_t* vals,
                                         const int64_t* ranges, const uint32_t* tile_order,
                                         const float* bg,
                                         const float* target, float* image, float* T_final,
@@ -1109,10 +1144,12 @@ extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_spl
   if (n > 0 && (!splats || !grads || !aligned16(splats) || !aligned16(grads)))
     return GS_ERR_INVALID_ARG;
   if (workspace && !aligned16(workspace)) return GS_ERR_INVALID_ARG;
+  if (!aligned4(tile_counts)) return GS_ERR_INVALID_ARG;
   const int64_t rec_slots = workspace ? (int64_t)(ws_bytes / (kRT / 8 * kWords * sizeof(uint32_t))) : 0;
   cudaStream_t st = (cudaStream_t)stream;
   GS_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), st));
-  if (n > 0) GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)(n * n_views), st));
+  const gs_status zs = zero_grads(n * n_views, tile_counts, grads, st);
+  if (zs != GS_OK) return zs;
   const int64_t T = tiles_per_view(width, height);
   const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE;
   const double count = 3.0 * (double)n_views * (double)width * (double)height;
@@ -1126,7 +1163,7 @@ extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_spl
 }
 
 extern "C" gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats,
-                                      int32_t width, int32_t height, const uint32_t* vals,
+                                      const int32_t* tile_counts, int32_t width, int32_t height, const uint32_t* vals,
                                       const int64_t* ranges, const uint32_t* tile_order,
                                       const float* bg, const float* T_final,
                                       const int32_t* n_contrib, const float* dL_dimage,
@@ -1136,8 +1173,10 @@ extern "C" gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat
     return GS_ERR_INVALID_ARG;
   if (n > 0 && (!splats || !grads || !aligned16(splats) || !aligned16(grads)))
     return GS_ERR_INVALID_ARG;
+  if (!aligned4(tile_counts)) return GS_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  if (n > 0) GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)(n * n_views), st));
+  const gs_status zs = zero_grads(n * n_views, tile_counts, grads, st);
+  if (zs != GS_OK) return zs;
   const int64_t T = tiles_per_view(width, height);
   const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE;
   raster_bwd_kernel<<<(unsigned)(n_views * T), kRT, 0, st>>>(

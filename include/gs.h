@@ -84,7 +84,19 @@ typedef struct gs_camera {
 /* Projected Gaussian, one per (view, Gaussian) row r = view * n + g.
  * 48 bytes, so one record is three 16-byte vectors.  A culled row has
  * radius = 0 and tiles = 0 (its other fields are unspecified except
- * color_b = depth = 0). */
+ * color_b = depth = 0), unless gs_project was given a tile-count array: then
+ * a culled row's record is not written at all and the array says which rows
+ * are culled (count 0).
+ *
+ * Tile counts.  gs_project can write, besides the records, an int32 array
+ * tile_counts[n_views * n] holding each row's tile count (0 = culled).  The
+ * calls that need to know which rows are visible (gs_bin_and_sort*,
+ * gs_rasterize_bwd, gs_rasterize_fused, gs_project_bwd) take the same array
+ * (4-byte aligned) or NULL.  With it, culled rows cost 4 bytes each instead
+ * of a 48-byte record: written once by the projection, read by the binning,
+ * the gradient zeroing and the projection backward, none of which touches a
+ * culled row's record or gradient record.  With NULL, the records' radius
+ * and tiles fields decide, and every record must have been written. */
 typedef struct gs_splat {
   float mean_x, mean_y;     /* projected mean, pixels                          */
   float conic_a, conic_b;   /* inverse 2D covariance [[a, b], [b, c]]          */
@@ -116,10 +128,12 @@ typedef struct gs_splat_grad {
  *             coefficient k of channel c  [S1]
  *   cams      (host) n_views cameras, 1 <= n_views <= GS_MAX_VIEWS
  *   splats    [n_views * n] output records
+ *   tile_counts  [n_views * n] int32 output, or NULL (then every row's
+ *             record is written, culled ones with radius = tiles = 0)
  * Returns GS_ERR_INVALID_ARG for bad sizes/cameras or NULL pointers with
  * n > 0. */
 gs_status gs_project(int64_t n, const float* params, const gs_camera* cams, int32_t n_views,
-                     gs_splat* splats, void* stream);
+                     gs_splat* splats, int32_t* tile_counts, void* stream);
 
 /* ---------------------------------------------------------------------- */
 /* Workspace for gs_bin_and_sort, in bytes, for n_rows = n_views * n
@@ -147,6 +161,7 @@ int32_t gs_key_bits(int32_t n_views, int32_t width, int32_t height);
  *  4. stable radix passes on the tile bits of gs_key_bits() (8 per pass);
  *  5. the ranges.
  *   splats     [n_views * n] from gs_project
+ *   tile_counts  [n_views * n] from gs_project, or NULL
  *   workspace  ws_bytes >= gs_bin_workspace_bytes(n_views * n, capacity);
  *              its first 256 bytes (a status header) must be zero before the
  *              first call (e.g. cudaMemset once after allocation); calls keep
@@ -162,10 +177,10 @@ int32_t gs_key_bits(int32_t n_views, int32_t width, int32_t height);
  * GS_ERR_DEVICE_CHECK if a record's tile count did not match its rectangle
  * (that row is left out).  GS_ERR_INVALID_ARG unless n_views * n and
  * n_views * T are below 2^32 and ceil(W/16), ceil(H/16) <= 65535. */
-gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
-                          int32_t height, void* workspace, size_t ws_bytes, int64_t capacity,
-                          uint64_t* keys, uint32_t* vals, int64_t* ranges, int64_t* n_isect,
-                          void* stream);
+gs_status gs_bin_and_sort(int64_t n, int32_t n_views, const gs_splat* splats,
+                          const int32_t* tile_counts, int32_t width, int32_t height,
+                          void* workspace, size_t ws_bytes, int64_t capacity, uint64_t* keys,
+                          uint32_t* vals, int64_t* ranges, int64_t* n_isect, void* stream);
 
 /* Synchronises `stream` and returns (and clears) the device status word of a
  * binning workspace: GS_OK, GS_ERR_TIMEOUT, GS_ERR_DEVICE_CHECK, or
@@ -185,8 +200,9 @@ gs_status gs_workspace_status(void* workspace, void* stream);
  * call on a device should be made outside graph capture (it sets a kernel
  * attribute), as any gs_bin_and_sort call does. */
 gs_status gs_bin_and_sort_async(int64_t n, int32_t n_views, const gs_splat* splats,
-                                int32_t width, int32_t height, void* workspace, size_t ws_bytes,
-                                int64_t capacity, uint64_t* keys, uint32_t* vals, int64_t* ranges,
+                                const int32_t* tile_counts, int32_t width, int32_t height,
+                                void* workspace, size_t ws_bytes, int64_t capacity,
+                                uint64_t* keys, uint32_t* vals, int64_t* ranges,
                                 int64_t* n_isect, void* stream);
 
 /* Self-test of the bounded device waits: runs one look-back partition whose
@@ -218,9 +234,9 @@ gs_status gs_selftest_lookback_timeout(void* workspace, size_t ws_bytes, void* s
 #define GS_BIN_STATIC_MAX_ROWS 65536
 #define GS_BIN_STATIC_MAX_ISECT 1048576
 gs_status gs_bin_and_sort_static(int64_t n, int32_t n_views, const gs_splat* splats,
-                                 int32_t width, int32_t height, int64_t capacity,
-                                 uint64_t* keys, uint32_t* vals, int64_t* ranges,
-                                 int64_t* n_isect, void* stream);
+                                 const int32_t* tile_counts, int32_t width, int32_t height,
+                                 int64_t capacity, uint64_t* keys, uint32_t* vals,
+                                 int64_t* ranges, int64_t* n_isect, void* stream);
 
 /* ---------------------------------------------------------------------- */
 /* gs_tile_order -- the launch order for the compositing calls: the tiles
@@ -281,8 +297,12 @@ gs_status gs_loss_l1(const float* image, const float* target, int64_t count, flo
  * T_i = T_{i+1} / (1 - alpha_i) from T_final and the colour composited
  * behind each pair; per-pair gradients are reduced per warp before global
  * atomics.
- *   grads  [n_views * n] output, zeroed by this call, then accumulated. */
-gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
+ *   tile_counts  [n_views * n] from gs_project, or NULL
+ *   grads  [n_views * n] output, zeroed by this call, then accumulated; with
+ *          tile_counts, only the rows with a positive count are zeroed and
+ *          written (the others are left as they were) */
+gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats,
+                           const int32_t* tile_counts, int32_t width,
                            int32_t height, const uint32_t* vals, const int64_t* ranges,
                            const uint32_t* tile_order, const float* bg, const float* T_final,
                            const int32_t* n_contrib, const float* dL_dimage,
@@ -301,6 +321,7 @@ gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats, i
  * whose footprint box meets the block.  Results equal those of the three
  * separate calls (the gradient up to the order of float atomics), with or
  * without the workspace.
+ *   tile_counts  [n_views * n] from gs_project, or NULL (as gs_rasterize_bwd)
  *   target     [n_views][3][H][W] fp32, the images the L1 loss compares with
  *   image, T_final, n_contrib   outputs as gs_rasterize_fwd
  *   loss       device scalar, overwritten: mean |image - target| over
@@ -314,7 +335,8 @@ gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats, i
  *              fit in ws_bytes falls back to the box walk */
 size_t gs_rasterize_workspace_bytes(int32_t n_views, int32_t width, int32_t height,
                                     int64_t capacity);
-gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats, int32_t width,
+gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
+                             const int32_t* tile_counts, int32_t width,
                              int32_t height, const uint32_t* vals, const int64_t* ranges,
                              const uint32_t* tile_order, const float* bg, const float* target,
                              float* image, float* T_final, int32_t* n_contrib, float* loss,
@@ -329,12 +351,15 @@ gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
  * logit.  The derivative is exact where the step is differentiable; through
  * an active clamp (alpha cap, colour at 0, the J field-of-view clamp) the
  * clamped quantity contributes 0.
+ *   tile_counts  [n_views * n] from gs_project, or NULL; a row is read (its
+ *            record and gradient record) only when visible
  *   grad     [59][n] output (overwritten)
  *   visible  [n] output or NULL: 1 if the Gaussian has radius > 0 in any
  *            view, else 0 */
 gs_status gs_project_bwd(int64_t n, const float* params, const gs_camera* cams, int32_t n_views,
-                         const gs_splat* splats, const gs_splat_grad* grads, float* grad,
-                         uint8_t* visible, void* stream);
+                         const gs_splat* splats, const int32_t* tile_counts,
+                         const gs_splat_grad* grads, float* grad, uint8_t* visible,
+                         void* stream);
 
 /* gs_adam_step -- Adam [S4 Kingma & Ba; S2 two moments] over the [59][n]
  * parameters, fused in one pass:

@@ -79,49 +79,58 @@ def test_invalid_arguments_return_before_any_launch(gslib):
     cams = gslib.cameras_struct([dict(R=[1, 0, 0, 0, 1, 0, 0, 0, 1], t=[0, 0, 0], fx=1, fy=1, cx=0,
                                       cy=0, width=16, height=16, near_z=0.01, far_z=1e9)])
     cp = C.cast(cams, C.c_void_p)
-    assert L.gs_project(10, None, cp, 0, None, None) == gslib.GS_ERR_INVALID_ARG   # 0 views
-    assert L.gs_project(10, None, cp, 1, None, None) == gslib.GS_ERR_INVALID_ARG   # NULL params
-    assert L.gs_project(-1, None, cp, 1, None, None) == gslib.GS_ERR_INVALID_ARG
-    assert L.gs_project(0, None, cp, 1, None, None) == gslib.GS_OK                 # empty
+    assert L.gs_project(10, None, cp, 0, None, None, None) == gslib.GS_ERR_INVALID_ARG  # 0 views
+    assert L.gs_project(10, None, cp, 1, None, None, None) == gslib.GS_ERR_INVALID_ARG  # NULL
+    assert L.gs_project(-1, None, cp, 1, None, None, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_project(0, None, cp, 1, None, None, None) == gslib.GS_OK                # empty
+    # a tile-count array not 4-byte aligned is rejected before anything runs
+    cbuf = C.create_string_buffer(256)
+    a16 = C.c_void_p((C.addressof(cbuf) + 15) & ~15)
+    odd = C.c_void_p(a16.value + 2)
+    assert L.gs_project(10, a16, cp, 1, a16, odd, None) == gslib.GS_ERR_INVALID_ARG
     bad = gslib.cameras_struct([dict(R=[1, 0, 0, 0, 1, 0, 0, 0, 1], t=[0, 0, 0], fx=1, fy=1, cx=0,
                                      cy=0, width=0, height=16, near_z=0.01, far_z=1e9)])
-    assert L.gs_project(0, None, C.cast(bad, C.c_void_p), 1, None, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_project(0, None, C.cast(bad, C.c_void_p), 1, None, None,
+                        None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_adam_step(5, None, None, None, None, 0, 1e-3, 0.9, 0.999, 1e-8, None,
                           None) == gslib.GS_ERR_INVALID_ARG                        # step 0
     assert L.gs_adam_step(5, None, None, None, None, 1, 1e-3, 0.9, 0.999, 1e-8, None,
                           None) == gslib.GS_ERR_INVALID_ARG                        # NULL
     out = C.c_int64(0)
-    assert L.gs_bin_and_sort(10, 1, None, 16, 16, None, 0, 0, None, None, None, C.byref(out),
-                             None) == gslib.GS_ERR_INVALID_ARG                     # no workspace
+    assert L.gs_bin_and_sort(10, 1, None, None, 16, 16, None, 0, 0, None, None, None,
+                             C.byref(out), None) == gslib.GS_ERR_INVALID_ARG       # no workspace
     ws = C.create_string_buffer(64)
-    assert L.gs_bin_and_sort(1 << 29, 8, None, 16, 16, ws, 64, 0, None, None, None, C.byref(out),
-                             None) == gslib.GS_ERR_INVALID_ARG                     # 2^32 rows
-    assert L.gs_bin_and_sort(1, 1, None, 16 * 65536, 16, ws, 64, 0, None, None, None,
+    assert L.gs_bin_and_sort(1 << 29, 8, None, None, 16, 16, ws, 64, 0, None, None, None,
+                             C.byref(out), None) == gslib.GS_ERR_INVALID_ARG       # 2^32 rows
+    assert L.gs_bin_and_sort(1, 1, None, None, 16 * 65536, 16, ws, 64, 0, None, None, None,
                              C.byref(out), None) == gslib.GS_ERR_INVALID_ARG       # 65536 tiles wide
     assert L.gs_rasterize_fwd(10, 1, None, 16, 16, None, None, None, None, None, None, None,
                               None) == gslib.GS_ERR_INVALID_ARG
-    assert L.gs_rasterize_bwd(10, 17, None, 16, 16, None, None, None, None, None, None, None,
-                              None, None) == gslib.GS_ERR_INVALID_ARG
-    assert L.gs_rasterize_fused(10, 1, None, 16, 16, None, None, None, None, None, None, None,
-                                None, None, None, None, C.c_size_t(0),
+    assert L.gs_rasterize_bwd(10, 17, None, None, 16, 16, None, None, None, None, None, None,
+                              None, None, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_rasterize_fused(10, 1, None, None, 16, 16, None, None, None, None, None, None,
+                                None, None, None, None, None, C.c_size_t(0),
                                 None) == gslib.GS_ERR_INVALID_ARG
     # a workspace not 16-byte aligned is rejected before anything runs
     buf = C.create_string_buffer(64)
     dummy = C.c_float * 3
     mis = C.c_void_p(((C.addressof(buf) + 15) & ~15) + 4)  # 4 mod 16, inside the buffer
-    assert L.gs_rasterize_fused(0, 1, None, 16, 16, None, buf, None, dummy(0, 0, 0), buf, buf, buf,
-                                buf, buf, None, mis, C.c_size_t(32),
+    assert L.gs_rasterize_fused(0, 1, None, None, 16, 16, None, buf, None, dummy(0, 0, 0), buf,
+                                buf, buf, buf, buf, None, mis, C.c_size_t(32),
                                 None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_rasterize_fused(0, 1, None, odd, 16, 16, None, buf, None, dummy(0, 0, 0), buf,
+                                buf, buf, buf, buf, None, None, C.c_size_t(0),
+                                None) == gslib.GS_ERR_INVALID_ARG                  # counts at 2 mod 4
     assert L.gs_tile_order(-1, None, None, None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_tile_order(5, None, None, None) == gslib.GS_ERR_INVALID_ARG          # NULL
     assert L.gs_tile_order(0, None, None, None) == gslib.GS_OK                       # empty
-    assert L.gs_project_bwd(10, None, cp, 1, None, None, None, None,
+    assert L.gs_project_bwd(10, None, cp, 1, None, None, None, None, None,
                             None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_loss_l1(None, None, -1, None, None, None) == gslib.GS_ERR_INVALID_ARG
     # the graph-capturable calls
-    assert L.gs_bin_and_sort_async(10, 1, None, 16, 16, None, 0, 100, None, None, None,
+    assert L.gs_bin_and_sort_async(10, 1, None, None, 16, 16, None, 0, 100, None, None, None,
                                    C.byref(out), None) == gslib.GS_ERR_INVALID_ARG  # no workspace
-    assert L.gs_bin_and_sort_async(10, 1, None, 16, 16, None, 0, 0, None, None, None, None,
+    assert L.gs_bin_and_sort_async(10, 1, None, None, 16, 16, None, 0, 0, None, None, None, None,
                                    None) == gslib.GS_ERR_INVALID_ARG               # capacity 0
     assert L.gs_adam_step_dev(5, None, None, None, None, None, 1e-3, 0.9, 0.999, 1e-8, None,
                               None, None) == gslib.GS_ERR_INVALID_ARG              # no step

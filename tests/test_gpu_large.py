@@ -218,7 +218,7 @@ def test_city_100m_sparse():
     step = gs.TrainStep(dev_params, cams, torch.from_numpy(target).cuda(), lr=cfg["lr"], sparse=True)
     step.forward()
     torch.cuda.synchronize()
-    vis_rows = int((step.splats.view(torch.int32)[:, 10] > 0).sum().item())
+    vis_rows = int((step.tile_counts > 0).sum().item())
     print("visible rows %d of %d (%.2f%% per view), intersections %d" %
           (vis_rows, n * V, 100.0 * vis_rows / (n * V), step.n_isect))
 
@@ -228,9 +228,11 @@ def test_city_100m_sparse():
     pr_s = oracle.project(params[:, gsel].astype(np.float64), cams, threads=THREADS)
     rows_d = torch.from_numpy((np.arange(V)[:, None] * n + gsel[None, :]).reshape(-1)).cuda()
     g = unpack_records(step.splats[rows_d].cpu().numpy())
+    seen = step.tile_counts[rows_d].cpu().numpy() > 0  # culled rows have no record
     clean = pr_s["flags"] == 0
-    assert not (((g["radius"] > 0) != (pr_s["radius"] > 0)) & clean).any()
-    ok = (g["radius"] > 0) & (pr_s["radius"] > 0) & clean
+    assert not ((seen != (pr_s["radius"] > 0)) & clean).any()
+    assert np.array_equal(g["tiles"][seen], step.tile_counts[rows_d].cpu().numpy()[seen])
+    ok = seen & (pr_s["radius"] > 0) & clean
     assert ok.sum() > 1000
     assert np.array_equal(g["radius"][ok], pr_s["radius"][ok])
     for f in ("mean2d", "conic", "color", "opacity", "depth"):

@@ -653,3 +653,83 @@ def test_fused_far_footprints_and_empty_tiles():
         print("workspace %s: fused vs separate grads rel-L2 %.2e, longest list %d" %
               (ws_bytes, e, int((ranges[:, 1] - ranges[:, 0]).max().item())))
         assert e <= 1e-5
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_tile_counts_path_matches_records_path(case):
+    """With a tile-count array the projection writes no record for a culled
+    row, and binning, compositing and the projection backward never read
+    one (nor a culled row's gradient record): culled records and gradient
+    records are pre-filled with a sentinel whose tile field is positive, and
+    every result must equal the path without the array."""
+    gs = _gs()
+    o = oracle_side(case)
+    n, V, W, H = o["n"], o["V"], o["W"], o["H"]
+    params = _cuda(o["params"])
+    rows = n * V
+    sa = torch.empty((rows, 12), dtype=torch.float32, device="cuda")
+    gs.gs_project(params, o["cams"], sa)
+    sentinel = torch.full((rows, 12), 0x7F7F7F7F, dtype=torch.int32, device="cuda")
+    sb = sentinel.clone().view(torch.float32)
+    counts = torch.full((rows,), -5, dtype=torch.int32, device="cuda")
+    gs.gs_project(params, o["cams"], sb, tile_counts=counts)
+    rec_tiles = sa.view(torch.int32)[:, 11]
+    assert torch.equal(counts, rec_tiles)
+    vis = counts > 0
+    assert int(vis.sum()) > 0
+    assert case == "tiny" or int(vis.sum()) < rows  # the tiny scene culls nothing
+    assert torch.equal(sb.view(torch.int32)[vis], sa.view(torch.int32)[vis])
+    assert torch.equal(sb.view(torch.int32)[~vis], sentinel[~vis])
+    # binning: identical lists
+    cap = max(1, int(rec_tiles.to(torch.int64).sum().item()))
+    T = gs.tiles_per_view(W, H)
+    out = []
+    for s, c in ((sa, None), (sb, counts)):
+        ws = torch.zeros(gs.gs_bin_workspace_bytes(rows, cap), dtype=torch.uint8, device="cuda")
+        keys = torch.empty(cap, dtype=torch.int64, device="cuda")
+        vals = torch.empty(cap, dtype=torch.int32, device="cuda")
+        ranges = torch.empty((V * T, 2), dtype=torch.int64, device="cuda")
+        st, I = gs.gs_bin_and_sort(n, V, s, W, H, ws, cap, keys, vals, ranges, tile_counts=c)
+        assert st == gs.GS_OK and I == cap
+        out.append((keys, vals, ranges))
+    assert all(torch.equal(a, b) for a, b in zip(out[0], out[1]))
+    keys, vals, ranges = out[0]
+    # fused compositing: same image, same gradients on visible rows, culled
+    # gradient records untouched
+    target = _cuda(o["target"])
+    res = []
+    for s, c in ((sa, None), (sb, counts)):
+        image = torch.empty((V, 3, H, W), device="cuda")
+        T_final = torch.empty((V, H, W), device="cuda")
+        n_contrib = torch.empty((V, H, W), dtype=torch.int32, device="cuda")
+        loss = torch.empty(1, device="cuda")
+        grads = torch.full((rows, 12), 3.0, device="cuda")
+        ws = torch.empty(gs.gs_rasterize_workspace_bytes(V, W, H, cap), dtype=torch.uint8,
+                         device="cuda")
+        gs.gs_rasterize_fused(n, V, s, W, H, vals, ranges, (0, 0, 0), target, image, T_final,
+                              n_contrib, loss, grads, workspace=ws, tile_counts=c)
+        res.append((image, T_final, n_contrib, loss, grads))
+    (ia, ta, na, la, ga), (ib, tb, nb, lb, gb) = res
+    assert torch.equal(ia, ib) and torch.equal(ta, tb) and torch.equal(na, nb)
+    assert lb.item() == pytest.approx(la.item(), rel=1e-5)
+    assert rel_l2(gb[vis].cpu().numpy(), ga[vis].cpu().numpy()) <= 1e-5
+    assert torch.all(gb[~vis] == 3.0) and torch.all(ga[~vis] == 0.0)
+    # separate backward: the same
+    g_img = torch.empty_like(ia)
+    gs.gs_loss_l1(ia, target, torch.empty(1, device="cuda"), g_img)
+    gsep = torch.full((rows, 12), 3.0, device="cuda")
+    gs.gs_rasterize_bwd(n, V, sb, W, H, vals, ranges, (0, 0, 0), ta, na, g_img, gsep,
+                        tile_counts=counts)
+    assert rel_l2(gsep[vis].cpu().numpy(), ga[vis].cpu().numpy()) <= 1e-5
+    assert torch.all(gsep[~vis] == 3.0)
+    # projection backward on identical visible inputs: bit for bit
+    gc = ga.clone()
+    gc[~vis] = float("nan")
+    grad_a = torch.empty((59, n), device="cuda")
+    grad_b = torch.full((59, n), 5.0, device="cuda")
+    vis_a = torch.empty(n, dtype=torch.uint8, device="cuda")
+    vis_b = torch.full((n,), 9, dtype=torch.uint8, device="cuda")
+    gs.gs_project_bwd(params, o["cams"], sa, ga, grad_a, vis_a)
+    gs.gs_project_bwd(params, o["cams"], sb, gc, grad_b, vis_b, tile_counts=counts)
+    assert torch.equal(grad_a, grad_b)
+    assert torch.equal(vis_a, vis_b)

@@ -108,7 +108,9 @@ def test_small_200k_ten_steps_against_oracle():
         lock.m.copy_(torch.from_numpy(mo.astype(np.float32)))
         lock.v.copy_(torch.from_numpy(vo.astype(np.float32)))
         lock.t = t - 1
-        lock.splats.copy_(torch.from_numpy(pack_records(pr)))
+        rec = pack_records(pr)
+        lock.splats.copy_(torch.from_numpy(rec))
+        lock.tile_counts.copy_(torch.from_numpy(np.ascontiguousarray(rec.view(np.int32)[:, 11])))
         lock.bin_and_sort()
         lock.rasterize_fused()
         # the gradient with the flagged pixels' image gradient zeroed

@@ -48,16 +48,16 @@ def _static(gs, n, V, splats, W, H, cap):
     """Calls the C entry point directly (ctypes)."""
     L = gs.lib()
     f = L.gs_bin_and_sort_static
-    f.argtypes = [C.c_int64, C.c_int32, C.c_void_p, C.c_int32, C.c_int32, C.c_int64, C.c_void_p,
-                  C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+    f.argtypes = [C.c_int64, C.c_int32, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int64,
+                  C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
     f.restype = C.c_int
     T = gs.tiles_per_view(W, H)
     keys = torch.full((cap,), -1, dtype=torch.int64, device="cuda")
     vals = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
     ranges = torch.full((V * T, 2), -3, dtype=torch.int64, device="cuda")
     out = C.c_int64(0)
-    st = f(n, V, splats.data_ptr(), W, H, cap, keys.data_ptr(), vals.data_ptr(), ranges.data_ptr(),
-           C.byref(out), torch.cuda.current_stream().cuda_stream)
+    st = f(n, V, splats.data_ptr(), None, W, H, cap, keys.data_ptr(), vals.data_ptr(),
+           ranges.data_ptr(), C.byref(out), torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     I = int(out.value)
     return st, I, keys[:I].cpu(), vals[:I].cpu(), ranges.cpu()
@@ -95,7 +95,7 @@ def test_static_workspace_variant_rejects_oversize():
     f.restype = C.c_int
     out = C.c_int64(0)
     # too many rows (65537 x 1 view) and too much capacity: rejected before any work
-    assert f(C.c_int64(65537), C.c_int32(1), None, C.c_int32(16), C.c_int32(16), C.c_int64(16), None,
-             None, None, C.byref(out), None) == gs.GS_ERR_INVALID_ARG
-    assert f(C.c_int64(10), C.c_int32(1), None, C.c_int32(16), C.c_int32(16),
+    assert f(C.c_int64(65537), C.c_int32(1), None, None, C.c_int32(16), C.c_int32(16),
+             C.c_int64(16), None, None, None, C.byref(out), None) == gs.GS_ERR_INVALID_ARG
+    assert f(C.c_int64(10), C.c_int32(1), None, None, C.c_int32(16), C.c_int32(16),
              C.c_int64(1048577), None, None, None, C.byref(out), None) == gs.GS_ERR_INVALID_ARG

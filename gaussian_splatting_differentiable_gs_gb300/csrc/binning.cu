@@ -52,6 +52,13 @@ constexpr int kSortThreads = 512;
 constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kSortKpt = 8;                             // keys per thread
 constexpr int kSortPart = kSortThreads * kSortKpt;      // keys per sort partition
+// the binning's radix passes: the same partition, over fewer, fuller threads
+// (one thread per digit in the digit phases)
+constexpr int kPassThreads = 512;
+constexpr int kPassWarps = kPassThreads / 32;
+constexpr int kPassKpt = kSortPart / kPassThreads;       // keys per thread
+constexpr int kPassMinBlocks = 3;
+static_assert(kPassThreads * kPassKpt == kSortPart && kPassThreads >= 256, "pass shape");
 constexpr int kRadix = 256;
 constexpr int kMaxPasses = 8;
 constexpr int kDepthPasses = 4;                         // 32 depth bits
@@ -77,7 +84,7 @@ static_assert(offsetof(WsHeader, error) == kWsStatusOffset, "status word offset"
 static_assert(offsetof(WsHeader, rows) == 16, "counts in the first 24 bytes");
 
 // Workspace layout.  Per visible row (compact index c < R): row_u[c] =
-// depth bits << 32 | row, row_rect[c] = first flat tile | width << 32 |
+// depth bits << 32 | Gaussian id (row mod n), row_rect[c] = first flat tile | width << 32 |
 // height << 48 of its tile rectangle.  tmp: one capacity-sized key buffer;
 // the row sort ping-pongs between it and the caller's key buffer (R <= I <=
 // capacity), as do the tile passes.
@@ -281,7 +288,8 @@ __global__ void __launch_bounds__(kCompThreads) compact_rows_kernel(
         const int64_t ci = c + __popc(mask[i] & lt);
         const int64_t r = wbase + 32 * i + lane;
         if (ci < capacity) sort_in[ci] = ((uint64_t)dbits[i] << 32) | (uint64_t)ci;
-        row_u[ci] = ((uint64_t)dbits[i] << 32) | (uint64_t)r;
+        // rows < 2^32: the Gaussian id by 32-bit arithmetic
+        row_u[ci] = ((uint64_t)dbits[i] << 32) | (uint64_t)((uint32_t)r % (uint32_t)n);
         row_rect[ci] = rect[i];
       }
       c += __popc(mask[i]);
@@ -311,6 +319,44 @@ __global__ void __launch_bounds__(kRadix) hist_scan_kernel(const uint32_t* __res
   digit_start[p * kRadix + d] = add + incl - c;
 }
 
+// Look-back of one digit of radix partition `part` (status word: value << 8 |
+// tag << 2 | flag): the exclusive prefix of the digit over the partitions
+// before `part`, summing aggregates back to the nearest inclusive prefix.
+// The predecessors are read kLookWindow at a time (independent loads in
+// flight together) rather than one by one: a partition that arrives while
+// its k nearest predecessors are still looking back walks k steps, and with
+// one dependent L2 round trip per step that walk, not the data movement, set
+// the pace of a pass.  Each wait is bounded; false when one ran out (or a
+// predecessor failed).
+constexpr int kLookWindow = 8;
+
+__device__ __forceinline__ bool digit_lookback(const uint64_t* status, int64_t part, int d,
+                                               uint64_t tag, unsigned long long& excl) {
+  excl = 0;
+  int64_t j = part - 1;  // partition 0 is inclusive: every walk ends there at the latest
+  while (j >= 0) {
+    uint64_t s[kLookWindow];
+#pragma unroll
+    for (int i = 0; i < kLookWindow; ++i)
+      s[i] = j - i >= 0 ? ld_volatile(&status[(j - i) * kRadix + d]) : (tag | kFlagInc);
+#pragma unroll
+    for (int i = 0; i < kLookWindow; ++i) {
+      uint64_t v = s[i];
+      uint32_t spins = 0;
+      while ((v & 3u) != kFlagErr && ((v & 3u) == 0 || (v & 0xFCu) != tag)) {
+        if (++spins > kSpinLimit) return false;
+        __nanosleep(100);
+        v = ld_volatile(&status[(j - i) * kRadix + d]);
+      }
+      if ((v & 3u) == kFlagErr) return false;
+      excl += (unsigned long long)(v >> 8);
+      if ((v & 3u) == kFlagInc) return true;
+    }
+    j -= kLookWindow;
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // 2, 4. One stable radix pass over 64-bit keys on the 8 bits at `shift`
 //    (onesweep).  Sort status word: value << 8 | tag << 2 | flag, tag =
@@ -323,10 +369,10 @@ __global__ void __launch_bounds__(kRadix) hist_scan_kernel(const uint32_t* __res
 //    ranges by atomic maxima (the start as count - position), decoded by
 //    ranges_fix_kernel.
 struct SortSmem64 {
-  uint32_t warp_hist[kSortWarps][kRadix];
+  uint32_t warp_hist[kPassWarps][kRadix];
   uint32_t local_start[kRadix];
   unsigned long long global_base[kRadix];
-  uint32_t scan_w[kSortWarps];
+  uint32_t scan_w[kPassWarps];
   int part;
   int err;
   long long count;
@@ -334,7 +380,7 @@ struct SortSmem64 {
 };
 
 template <bool kFinal>
-__global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
+__global__ void __launch_bounds__(kPassThreads, kPassMinBlocks) onesweep64_kernel(
     int64_t count, int32_t pass, int32_t shift, const uint64_t* __restrict__ keys_in,
     uint64_t* __restrict__ keys_out, const uint32_t* __restrict__ digit_start,
     uint64_t* __restrict__ status, WsHeader* __restrict__ hdr, const uint64_t* __restrict__ row_u,
@@ -344,7 +390,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint64_t tag = (uint64_t)(pass + 1) << 2;
   const int hs = shift - 32;  // the digit lies in the high word
-  for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&S.warp_hist[0][0])[i] = 0;
+  for (int i = tid; i < kPassWarps * kRadix; i += kPassThreads) (&S.warp_hist[0][0])[i] = 0;
   if (tid == 0) {
     S.part = (int)atomicAdd(&hdr->pass_ticket[pass], 1u);
     S.err = 0;
@@ -366,20 +412,20 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
   if (pbase >= count) return;
   const int n_here = count - pbase < kSortPart ? (int)(count - pbase) : kSortPart;
   const uint64_t* src = keys_in + pbase;
-  const int wbase = warp * 32 * kSortKpt;
+  const int wbase = warp * 32 * kPassKpt;
   // load (warp-striped: item i of lane l is element wbase + 32 i + l) and rank
-  uint64_t key[kSortKpt];
+  uint64_t key[kPassKpt];
 #pragma unroll
-  for (int i = 0; i < kSortKpt; ++i) {
+  for (int i = 0; i < kPassKpt; ++i) {
     const int li = wbase + 32 * i + lane;
     key[i] = li < n_here ? src[li] : 0ull;
   }
   const uint32_t lt_mask = (1u << lane) - 1u;
-  // rank of each key among the warp's keys of its digit (< 256: one byte
-  // each, four to a register)
-  uint32_t rank4[(kSortKpt + 3) / 4] = {};
+  // rank of each key among the warp's keys of its digit (< 32 kPassKpt <=
+  // 65536: two to a register)
+  uint32_t rank2[(kPassKpt + 1) / 2] = {};
 #pragma unroll
-  for (int i = 0; i < kSortKpt; ++i) {
+  for (int i = 0; i < kPassKpt; ++i) {
     const bool valid = wbase + 32 * i + lane < n_here;
     const uint32_t d = ((uint32_t)(key[i] >> 32) >> hs) & 0xFFu;
     const uint32_t peers = peers_of_digit(d, valid);
@@ -388,7 +434,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
     __syncwarp();
     if (valid && lane == __ffs(peers) - 1) S.warp_hist[warp][d] = basec + __popc(peers);
     __syncwarp();
-    rank4[i / 4] |= ((basec + __popc(peers & lt_mask)) & 0xFFu) << (8 * (i % 4));
+    rank2[i / 2] |= ((basec + __popc(peers & lt_mask)) & 0xFFFFu) << (16 * (i % 2));
   }
   __syncthreads();
   // per digit (threads 0..255, i.e. warps 0..7): exclusive prefix over warps,
@@ -399,7 +445,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
   if (dthread) {
     uint32_t run = 0;
 #pragma unroll
-    for (int w = 0; w < kSortWarps; ++w) {
+    for (int w = 0; w < kPassWarps; ++w) {
       const uint32_t c = S.warp_hist[w][d];
       S.warp_hist[w][d] = run;
       run += c;
@@ -423,34 +469,27 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
     uint32_t add = 0;
     for (int w = 0; w < warp; ++w) add += S.scan_w[w];
     S.local_start[d] = add + incl - my_count;
-    // look back for this digit
+  }
+  __syncthreads();
+  // place the partition in smem in sorted (digit-major, stable) order; the
+  // keys leave the registers before the look-back
+#pragma unroll
+  for (int i = 0; i < kPassKpt; ++i) {
+    if (wbase + 32 * i + lane < n_here) {
+      const uint32_t dd = ((uint32_t)(key[i] >> 32) >> hs) & 0xFFu;
+      S.keys[S.local_start[dd] + S.warp_hist[warp][dd] + ((rank2[i / 2] >> (16 * (i % 2))) & 0xFFFFu)] =
+          key[i];
+    }
+  }
+  if (dthread) {
     unsigned long long excl = 0;
     if (part > 0) {
-      int64_t j = part - 1;
-      bool err = false;
-      while (j >= 0) {
-        uint64_t s;
-        uint32_t spins = 0;
-        for (;;) {
-          s = ld_volatile(&status[j * kRadix + d]);
-          const uint64_t f = s & 3u;
-          if (f == kFlagErr) break;
-          if (f != 0 && (s & 0xFCu) == tag) break;
-          if (++spins > kSpinLimit) { s = kFlagErr; break; }
-          __nanosleep(100);
-        }
-        const uint64_t f = s & 3u;
-        if (f == kFlagErr) { err = true; break; }
-        excl += (unsigned long long)(s >> 8);
-        if (f == kFlagInc) break;
-        --j;
-      }
-      if (err) {
+      if (digit_lookback(status, part, d, tag, excl)) {
+        st_volatile(&status[part * kRadix + d], ((uint64_t)(excl + my_count) << 8) | tag | kFlagInc);
+      } else {
         st_volatile(&status[part * kRadix + d], tag | kFlagErr);
         atomicOr(&hdr->error, 1u);
         S.err = 1;
-      } else {
-        st_volatile(&status[part * kRadix + d], ((uint64_t)(excl + my_count) << 8) | tag | kFlagInc);
       }
     }
     // global position of the digit's first key, less its local start
@@ -459,25 +498,15 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep64_kernel(
   }
   __syncthreads();
   if (S.err) return;
-  // place the partition in smem in sorted (digit-major, stable) order
-#pragma unroll
-  for (int i = 0; i < kSortKpt; ++i) {
-    if (wbase + 32 * i + lane < n_here) {
-      const uint32_t dd = ((uint32_t)(key[i] >> 32) >> hs) & 0xFFu;
-      S.keys[S.local_start[dd] + S.warp_hist[warp][dd] + ((rank4[i / 4] >> (8 * (i % 4))) & 0xFFu)] =
-          key[i];
-    }
-  }
-  __syncthreads();
-  for (int j = tid; j < n_here; j += kSortThreads) {
+  for (int j = tid; j < n_here; j += kPassThreads) {
     const uint64_t k = S.keys[j];
     const uint32_t dd = ((uint32_t)(k >> 32) >> hs) & 0xFFu;
     const unsigned long long gpos = S.global_base[dd] + (unsigned long long)j;
     if (gpos < (unsigned long long)count) {
       if constexpr (kFinal) {
-        const uint64_t u = __ldg(row_u + (uint32_t)k);
+        const uint64_t u = __ldg(row_u + (uint32_t)k);  // depth bits, Gaussian id
         keys_out[gpos] = (k & 0xFFFFFFFF00000000ull) | (u >> 32);
-        vals_out[gpos] = (uint32_t)u % n;
+        vals_out[gpos] = (uint32_t)u;
         const uint32_t f = (uint32_t)(k >> 32);
         if (j == 0 || (uint32_t)(S.keys[j - 1] >> 32) != f)
           atomicMax(&ranges[2 * (uint64_t)f], (unsigned long long)count - gpos);
@@ -701,40 +730,8 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kv_kernel(
     uint32_t add = 0;
     for (int w = 0; w < warp; ++w) add += S.scan_w[w];
     S.local_start[d] = add + incl - my_count;
-    // look back for this digit
-    unsigned long long excl = 0;
-    if (part > 0) {
-      int64_t j = part - 1;
-      bool err = false;
-      while (j >= 0) {
-        uint64_t s;
-        uint32_t spins = 0;
-        for (;;) {
-          s = ld_volatile(&status[j * kRadix + d]);
-          const uint64_t f = s & 3u;
-          if (f == kFlagErr) break;
-          if (f != 0 && (s & 0xFCu) == tag) break;
-          if (++spins > kSpinLimit) { s = kFlagErr; break; }
-          __nanosleep(100);
-        }
-        const uint64_t f = s & 3u;
-        if (f == kFlagErr) { err = true; break; }
-        excl += (unsigned long long)(s >> 8);
-        if (f == kFlagInc) break;
-        --j;
-      }
-      if (err) {
-        st_volatile(&status[part * kRadix + d], tag | kFlagErr);
-        atomicOr(&hdr->error, 1u);
-        S.err = 1;
-      } else {
-        st_volatile(&status[part * kRadix + d], ((uint64_t)(excl + my_count) << 8) | tag | kFlagInc);
-      }
-    }
-    S.global_base[d] = (unsigned long long)digit_start[pass * kRadix + d] + excl;
   }
   __syncthreads();
-  if (S.err) return;
   // place the partition in smem in sorted (digit-major, stable) order
 #pragma unroll
   for (int i = 0; i < kSortKpt; ++i) {
@@ -746,7 +743,21 @@ __global__ void __launch_bounds__(kSortThreads, 3) onesweep_kv_kernel(
       S.vals[pos] = val[i];
     }
   }
+  if (dthread) {
+    unsigned long long excl = 0;
+    if (part > 0) {
+      if (digit_lookback(status, part, d, tag, excl)) {
+        st_volatile(&status[part * kRadix + d], ((uint64_t)(excl + my_count) << 8) | tag | kFlagInc);
+      } else {
+        st_volatile(&status[part * kRadix + d], tag | kFlagErr);
+        atomicOr(&hdr->error, 1u);
+        S.err = 1;
+      }
+    }
+    S.global_base[d] = (unsigned long long)digit_start[pass * kRadix + d] + excl;
+  }
   __syncthreads();
+  if (S.err) return;
   const int64_t n_here = count - pbase < kSortPart ? count - pbase : kSortPart;
   for (int j = tid; j < n_here; j += kSortThreads) {
     const uint64_t k = S.keys[j];
@@ -896,6 +907,7 @@ cudaError_t ensure_sort_attr() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(onesweep64_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(SortSmem64));
+
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
@@ -991,7 +1003,7 @@ gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, 
   uint64_t* in = ra;
   uint64_t* out = rb;
   for (int p = 0; p < kDepthPasses; ++p) {
-    onesweep64_kernel<false><<<(unsigned)parts_r, kSortThreads, smem, st>>>(
+    onesweep64_kernel<false><<<(unsigned)parts_r, kPassThreads, smem, st>>>(
         rows, p, 32 + 8 * p, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u,
         nullptr);
     GS_CHECK_LAUNCH();
@@ -1010,12 +1022,12 @@ gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, 
   for (int q = 0; q < s.tile_passes; ++q) {
     const int p = kDepthPasses + q;
     if (q == s.tile_passes - 1) {
-      onesweep64_kernel<true><<<(unsigned)parts_i, kSortThreads, smem, st>>>(
+      onesweep64_kernel<true><<<(unsigned)parts_i, kPassThreads, smem, st>>>(
           isect, p, 32 + 8 * q, in, keys, b.digit_start, b.sort_status, b.hdr, b.row_u, vals,
           (uint32_t)s.n, reinterpret_cast<unsigned long long*>(ranges));
     } else {
       out = in == keys ? b.tmp : keys;
-      onesweep64_kernel<false><<<(unsigned)parts_i, kSortThreads, smem, st>>>(
+      onesweep64_kernel<false><<<(unsigned)parts_i, kPassThreads, smem, st>>>(
           isect, p, 32 + 8 * q, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u,
           nullptr);
       in = out;

@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(128, 5) project_fwd_kernel(int64_t n, const fl
   }
 }
 
-__global__ void __launch_bounds__(128, 5) project_bwd_kernel(int64_t n, const float* __restrict__ params,
+__global__ void __launch_bounds__(128, 6) project_bwd_kernel(int64_t n, const float* __restrict__ params,
                                                           const __grid_constant__ CamSet cs,
                                                           const float4* __restrict__ splats,
                                                           const int32_t* __restrict__ counts,
@@ -289,9 +289,11 @@ __global__ void __launch_bounds__(128, 5) project_bwd_kernel(int64_t n, const fl
   for (uint32_t vm = vmask; vm; vm &= vm - 1u) {
     const int v = __ffs(vm) - 1;
     const int64_t row = (int64_t)v * n + g;
-    const float4 r2 = splats[3 * row + 2];
     const CamK& C = cs.c[v];
-    const float4 r0 = splats[3 * row], r1 = splats[3 * row + 1];
+    // the colour from the row's record (its last 32 bytes); the conic is
+    // recomputed with the projection's own arithmetic (bit for bit what it
+    // stored), so the first 16 bytes are not read
+    const float4 r1 = splats[3 * row + 1], r2 = splats[3 * row + 2];
     const float4 q0 = grads[3 * row], q1 = grads[3 * row + 1], q2 = grads[3 * row + 2];
     const float gm0 = q0.x, gm1 = q0.y, gA = q0.z, gB = q0.w, gC = q1.x, gop = q1.y;
     const float gcol[3] = {q1.z, q1.w, q2.x};
@@ -334,7 +336,8 @@ __global__ void __launch_bounds__(128, 5) project_bwd_kernel(int64_t n, const fl
     gp[1] = gm1 * C.fy * rz;
     gp[2] = -(gm0 * C.fx * x + gm1 * C.fy * y) * rz2;
     // conic = cov2^-1: H = -K Gk K with Gk = [[gA, gB/2], [gB/2, gC]], K = conic
-    const float A = r0.z, B = r0.w, Cc = r1.x;
+    const float idet = 1.0f / V.det;
+    const float A = V.c * idet, B = -V.b * idet, Cc = V.a * idet;
     const float hB = 0.5f * gB;
     const float t00 = A * gA + B * hB, t01 = A * hB + B * gC;
     const float t10 = B * gA + Cc * hB, t11 = B * hB + Cc * gC;

@@ -17,14 +17,19 @@
 //    tile pixel where it peaks (exact per-pixel offsets, see below) and the
 //    bounding box of the ellipse where alpha may reach 1/255; pairs outside
 //    it are skipped, the exact alpha test decides everything inside;
-//  - each warp walks only the entries whose box touches its pixels (a
-//    ballot-compacted sub-list that keeps list order);
-//  - forward: pixel state lives in shared memory and, at every batch, the
-//    still-open pixels are packed onto the first threads of the CTA, so the
-//    per-pair loop runs on full warps and finished warps stop issuing;
-//  - backward: a pair's gradient is reduced across the warp by recursive
-//    halving (8 values in 9 shuffles) and added to shared memory by one
-//    atomic per value;
+//  - forward: each warp walks only the entries whose box touches its pixels
+//    (a ballot-compacted sub-list that keeps list order); pixel state lives
+//    in shared memory and, at every batch, the still-open pixels are packed
+//    onto the first threads of the CTA, so the per-pair loop runs on full
+//    warps and finished warps stop issuing;
+//  - backward: each quarter-warp (eight lanes, a 4x2 pixel block) walks its
+//    own entry list, the four quarters of a warp in lockstep; a pair's
+//    gradient is reduced over the quarter (nine values in ten shuffles)
+//    and added to shared memory by one atomic per value;
+//  - fused call with a workspace: the forward records, per batch and per
+//    quarter, which entries it composited; the backward walks exactly those
+//    and hands the quarters to warps by descending count of recorded
+//    entries, so that quarters of similar length share a warp;
 //  - launch order: CTA b composites tile tile_order[b] when given
 //    (gs_tile_order in tile_order.cu: longest lists first), which shortens
 //    the kernel's tail.

@@ -185,37 +185,32 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# DRAM bytes (read + write) per launch of the compositing kernels, from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of this workload
-# at full size.  They describe the kernel source whose SHA-256 is given; for
-# any other source the figure is unknown (null).
-TRAFFIC = {
-    "rasterize_fused": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                        "sha256": "9122a0d2651e4341b8c7898b9aca98b861628b58b677312daf2a2a5fdbe9e5d1",
-                        "workload": "ring_3m_4x1080p", "bytes": 4249789696 + 515035904},
-    "rasterize_fwd": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                      "sha256": "9122a0d2651e4341b8c7898b9aca98b861628b58b677312daf2a2a5fdbe9e5d1",
-                      "workload": "ring_3m_4x1080p", "bytes": 2190107136 + 113843456},
-    "rasterize_bwd": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu",
-                      "sha256": "9122a0d2651e4341b8c7898b9aca98b861628b58b677312daf2a2a5fdbe9e5d1",
-                      "workload": "ring_3m_4x1080p", "bytes": 2994458624 + 393797376},
-    "loss_l1": {"source": "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu",
-                "sha256": "a737822b52d763475a3797fc86ee95258fe3ade8ce3305e0441f56f06db4dba1",
-                "workload": "ring_3m_4x1080p", "bytes": 199090944 + 38806784},
-}
+# DRAM bytes (read + write) per call of each timed kernel (for bin_and_sort,
+# the sum over its launches), from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum, one pass per launch) of this workload at full size.
+# They describe the sources whose SHA-256 are given; for any other source
+# the figure is unknown (null).
+_RASTER = "gaussian_splatting_differentiable_gs_gb300/csrc/raster.cu"
+_PROJECT = "gaussian_splatting_differentiable_gs_gb300/csrc/project.cu"
+_BINNING = "gaussian_splatting_differentiable_gs_gb300/csrc/binning.cu"
+_ORDER = "gaussian_splatting_differentiable_gs_gb300/csrc/tile_order.cu"
+_ADAM = "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu"
+TRAFFIC_WORKLOAD = "ring_3m_4x1080p"
+TRAFFIC = {}
 
 
 def traffic_of(kernel, workload, variant):
     t = TRAFFIC.get(kernel)
-    if t is None or t["workload"] != workload or variant:
+    if t is None or workload != TRAFFIC_WORKLOAD or variant:
         return None
     import hashlib
-    try:
-        with open(os.path.join(ROOT, t["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != t["sha256"]:
-                return None
-    except OSError:
-        return None
+    for src, digest in t["sources"].items():
+        try:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
     return t["bytes"]
 
 

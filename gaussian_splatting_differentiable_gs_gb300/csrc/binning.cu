@@ -47,6 +47,13 @@ constexpr int kCompPart = kCompThreads * kCompItems;    // rows per compaction p
 constexpr int kEmitThreads = 512;
 constexpr int kEmitItems = 4;
 constexpr int kEmitPart = kEmitThreads * kEmitItems;    // sorted rows per emission partition
+// emission in balanced chunks of kEmitChunk intersections per CTA, chosen
+// when rows average at least kEmitChunkMinTiles tiles (else one CTA per
+// partition of kEmitPart rows: cheaper when rows are small, e.g. 2.5 tiles a
+// row on the 1080p ring scene, 0.21 against 0.35 ms; slower when they are
+// large, 168 tiles a row on the 4K cluster scene, 16.8 against 11.5 ms)
+constexpr int kEmitChunk = 2048;
+constexpr int64_t kEmitChunkMinTiles = 8;
 
 constexpr int kSortThreads = 512;
 constexpr int kSortWarps = kSortThreads / 32;
@@ -89,7 +96,8 @@ static_assert(offsetof(WsHeader, rows) == 16, "counts in the first 24 bytes");
 // the row sort ping-pongs between it and the caller's key buffer (R <= I <=
 // capacity), as do the tile passes.
 struct WsLayout {
-  size_t hist, digit_start, scan_status, emit_status, sort_status, row_u, row_rect, tmp, total;
+  size_t hist, digit_start, scan_status, emit_status, sort_status, row_u, row_rect, erow, chunk_row,
+      tmp, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -107,6 +115,8 @@ inline WsLayout ws_layout(int64_t n_rows, int64_t capacity) {
   L.sort_status = off; off += align256(sizeof(uint64_t) * kRadix * (size_t)sort_parts);
   L.row_u = off;       off += align256(sizeof(uint64_t) * (size_t)r);
   L.row_rect = off;    off += align256(sizeof(uint64_t) * (size_t)r);
+  L.erow = off;        off += align256(sizeof(uint4) * (size_t)r);
+  L.chunk_row = off;   off += align256(sizeof(uint32_t) * (size_t)(div_up(c, kEmitChunk) + 1));
   L.tmp = off;         off += align256(sizeof(uint64_t) * (size_t)c);
   L.total = off;
   return L;
@@ -617,6 +627,184 @@ __global__ void __launch_bounds__(kEmitThreads) emit_sorted_kernel(
     if (sh[i]) atomicAdd(&hist[kDepthPasses * kRadix + i], sh[i]);
 }
 
+// 3 (balanced form).  Two kernels.  row_scan_kernel scans the sorted rows'
+//    tile counts (partitions of kEmitPart rows, decoupled look-back as
+//    above) into each row's first output position and writes per sorted row
+//    erow = (position, first flat tile, width | height << 16, compact index)
+//    and, for every chunk of kEmitChunk outputs that starts inside the row,
+//    chunk_row[chunk] = the row.  emit_chunks_kernel then gives every CTA
+//    one chunk of outputs -- the same number whatever the rows' sizes, where
+//    partitions of rows differ by orders of magnitude in output -- loads the
+//    chunk's rows into shared memory and finds each output's row by binary
+//    search among them; a row's tile (ty, tx) comes from a float reciprocal
+//    of its width, corrected to the exact quotient.  Same outputs, bit for
+//    bit, as emit_sorted_kernel.
+__global__ void __launch_bounds__(kEmitThreads) row_scan_kernel(
+    int64_t count, int32_t tiles_x, int32_t tile_passes, const uint64_t* __restrict__ sorted,
+    const uint64_t* __restrict__ row_rect, uint4* __restrict__ erow,
+    uint32_t* __restrict__ chunk_row, uint32_t* __restrict__ hist, uint64_t* __restrict__ status,
+    WsHeader* __restrict__ hdr) {
+  __shared__ uint32_t s_warp[kEmitThreads / 32];
+  // the tile passes' digit counts of the partition's intersections, from the
+  // rows' rectangles: a tile row of a rectangle is a run of consecutive flat
+  // indices, so the lowest digit of its tiles covers a cyclic range of bins
+  // (added as a difference array: diff[lo]++, diff[hi]--) and each higher
+  // digit is constant over whole sub-runs
+  __shared__ int32_t s_diff[kRadix + 1];
+  __shared__ uint32_t s_hi[3 * kRadix];
+  __shared__ uint32_t s_wrap;  // whole turns of the lowest digit (added to every bin)
+  __shared__ long long s_count, s_prefix;
+  __shared__ int s_part;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_count = (hdr->error & kErrStop) ? -1 : (count < 0 ? (long long)hdr->rows : count);
+    s_part = (int)atomicAdd(&hdr->emit_ticket, 1u);
+    s_wrap = 0;
+  }
+  for (int i = tid; i <= kRadix; i += kEmitThreads) s_diff[i] = 0;
+  for (int i = tid; i < 3 * kRadix; i += kEmitThreads) s_hi[i] = 0;
+  __syncthreads();
+  const long long R = s_count;
+  const int64_t part = s_part, pbase = part * kEmitPart;
+  if (R < 0 || pbase >= R) return;
+  // thread tid owns rows pbase + tid * kEmitItems + [0, kEmitItems)
+  uint32_t c[kEmitItems], first[kEmitItems], wh[kEmitItems], t[kEmitItems];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int k = 0; k < kEmitItems; ++k) {
+    const int64_t e = pbase + tid * kEmitItems + k;
+    t[k] = 0;
+    if (e < R) {
+      c[k] = (uint32_t)sorted[e];
+      const uint64_t rc = __ldg(row_rect + c[k]);
+      const uint32_t w = (uint32_t)(rc >> 32) & 0xFFFFu, h = (uint32_t)(rc >> 48);
+      first[k] = (uint32_t)rc;
+      wh[k] = w | (h << 16);
+      t[k] = w * h;
+    }
+    sum += t[k];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  uint32_t run = incl - sum, block_total = 0;
+#pragma unroll
+  for (int w = 0; w < kEmitThreads / 32; ++w) {
+    run += w < warp ? s_warp[w] : 0u;
+    block_total += s_warp[w];
+  }
+  if (warp == 0) {
+    const long long prefix = lookback_prefix_warp(status, part, (long long)block_total, hdr);
+    if (lane == 0) s_prefix = prefix;
+  }
+  __syncthreads();
+  if (s_prefix < 0) return;
+  unsigned long long pos = (unsigned long long)s_prefix + run;
+#pragma unroll
+  for (int k = 0; k < kEmitItems; ++k) {
+    const int64_t e = pbase + tid * kEmitItems + k;
+    if (e < R) {
+      erow[e] = make_uint4((uint32_t)pos, first[k], wh[k], c[k]);
+      // the chunks whose first output lies in [pos, pos + t)
+      for (unsigned long long q = div_up((int64_t)pos, kEmitChunk);
+           q * kEmitChunk < pos + t[k]; ++q)
+        chunk_row[q] = (uint32_t)e;
+    }
+    pos += t[k];
+  }
+  // digit counts of the tile passes
+#pragma unroll
+  for (int k = 0; k < kEmitItems; ++k) {
+    if (pbase + tid * kEmitItems + k >= R) continue;
+    const uint32_t w = wh[k] & 0xFFFFu, h = wh[k] >> 16;
+    for (uint32_t y = 0; y < h; ++y) {
+      const uint32_t f = first[k] + y * (uint32_t)tiles_x;  // tiles f .. f + w - 1
+      const uint32_t lo = f & 0xFFu, rem = w & 0xFFu;
+      if (w >> 8) atomicAdd(&s_wrap, w >> 8);
+      if (rem) {
+        atomicAdd(&s_diff[lo], 1);
+        if (lo + rem <= (uint32_t)kRadix) {
+          atomicAdd(&s_diff[lo + rem], -1);
+        } else {
+          atomicAdd(&s_diff[kRadix], -1);
+          atomicAdd(&s_diff[0], 1);
+          atomicAdd(&s_diff[lo + rem - kRadix], -1);
+        }
+      }
+      for (int p = 1; p < tile_passes; ++p) {
+        const uint32_t shift = 8u * (uint32_t)p;
+        for (uint32_t a = f, end = f + w; a < end;) {
+          const uint32_t next = ((a >> shift) + 1u) << shift;  // next change of digit p
+          const uint32_t b = next > a && next < end ? next : end;
+          atomicAdd(&s_hi[(p - 1) * kRadix + ((a >> shift) & 0xFFu)], b - a);
+          a = b;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < kRadix) {  // bin d of the lowest digit: the prefix sum of diff up to d, plus the turns
+    int32_t run = 0;
+    for (int i = 0; i <= tid; ++i) run += s_diff[i];
+    const uint32_t c0 = (uint32_t)run + s_wrap;
+    if (c0) atomicAdd(&hist[kDepthPasses * kRadix + tid], c0);
+    for (int p = 1; p < tile_passes; ++p)
+      if (s_hi[(p - 1) * kRadix + tid])
+        atomicAdd(&hist[(kDepthPasses + p) * kRadix + tid], s_hi[(p - 1) * kRadix + tid]);
+  }
+}
+
+__global__ void __launch_bounds__(kEmitThreads) emit_chunks_kernel(
+    int32_t tiles_x, const uint4* __restrict__ erow, const uint32_t* __restrict__ chunk_row,
+    uint64_t* __restrict__ out, const WsHeader* __restrict__ hdr) {
+  __shared__ uint4 s_row[kEmitChunk + 1];
+  __shared__ long long s_total, s_rows;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_total = (hdr->error & kErrStop) ? -1 : (long long)hdr->total;
+    s_rows = (long long)hdr->rows;
+  }
+  __syncthreads();
+  const long long I = s_total, R = s_rows;
+  const long long t0 = (long long)blockIdx.x * kEmitChunk;
+  if (I < 0 || t0 >= I) return;
+  const int n_here = I - t0 < kEmitChunk ? (int)(I - t0) : kEmitChunk;
+  const long long nchunks = div_up(I, kEmitChunk);
+  // the rows holding outputs t0 .. t0 + n_here - 1 (at most kEmitChunk, each
+  // row holding at least one; the next chunk's first row may be one more)
+  const uint32_t ra = chunk_row[blockIdx.x];
+  const uint32_t rb = blockIdx.x + 1 < nchunks ? chunk_row[blockIdx.x + 1] : (uint32_t)(R - 1);
+  const int m = (int)(rb - ra) + 1;
+  for (int i = tid; i < m; i += kEmitThreads) s_row[i] = erow[ra + i];
+  __syncthreads();
+  for (int j = tid; j < n_here; j += kEmitThreads) {
+    const uint32_t t = (uint32_t)(t0 + j);
+    int lo = 0, hi = m - 1;  // the last row whose first position is <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_row[mid].x <= t) lo = mid; else hi = mid - 1;
+    }
+    const uint4 r = s_row[lo];
+    const uint32_t i = t - r.x, w = r.z & 0xFFFFu;
+    uint32_t ty;
+    if (i < (1u << 24)) {  // exact in fp32: the reciprocal's quotient is off by at most one
+      ty = __float2uint_rz(__fmul_rn((float)i, __frcp_rn((float)w)));
+      if (ty * w > i) --ty;
+      else if ((ty + 1) * w <= i) ++ty;
+    } else {
+      ty = i / w;
+    }
+    const uint32_t tx = i - ty * w;
+    const uint32_t flat = r.y + ty * (uint32_t)tiles_x + tx;
+    out[t] = ((uint64_t)flat << 32) | (uint64_t)r.w;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 5. Tile ranges [first, last + 1): the last tile pass leaves count - first
 //    (0 for an empty tile) in ranges[2 f]; decoded here.  count < 0: the
@@ -923,6 +1111,8 @@ struct BinBufs {
   WsHeader* hdr;
   uint32_t *hist, *digit_start;
   uint64_t *scan_status, *emit_status, *sort_status, *row_u, *row_rect, *tmp;
+  uint4* erow;
+  uint32_t* chunk_row;
 };
 
 BinBufs bin_bufs(void* workspace, const WsLayout& L) {
@@ -933,6 +1123,8 @@ BinBufs bin_bufs(void* workspace, const WsLayout& L) {
   b.digit_start = reinterpret_cast<uint32_t*>(ws + L.digit_start);
   b.scan_status = reinterpret_cast<uint64_t*>(ws + L.scan_status);
   b.emit_status = reinterpret_cast<uint64_t*>(ws + L.emit_status);
+  b.erow = reinterpret_cast<uint4*>(ws + L.erow);
+  b.chunk_row = reinterpret_cast<uint32_t*>(ws + L.chunk_row);
   b.sort_status = reinterpret_cast<uint64_t*>(ws + L.sort_status);
   b.row_u = reinterpret_cast<uint64_t*>(ws + L.row_u);
   b.row_rect = reinterpret_cast<uint64_t*>(ws + L.row_rect);
@@ -1012,8 +1204,17 @@ gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, 
   // the sorted rows are back in ra
   const int64_t eparts = div_up(rows_max, kEmitPart);
   GS_CUDA(cudaMemsetAsync(b.emit_status, 0, sizeof(uint64_t) * (size_t)eparts, st));
-  emit_sorted_kernel<<<(unsigned)eparts, kEmitThreads, 0, st>>>(
-      rows, s.tiles_x, s.tile_passes, ra, b.row_rect, rb, b.hist, b.emit_status, b.hdr);
+  if (isect_max >= kEmitChunkMinTiles * rows_max) {
+    row_scan_kernel<<<(unsigned)eparts, kEmitThreads, 0, st>>>(
+        rows, s.tiles_x, s.tile_passes, ra, b.row_rect, b.erow, b.chunk_row, b.hist,
+        b.emit_status, b.hdr);
+    GS_CHECK_LAUNCH();
+    emit_chunks_kernel<<<(unsigned)div_up(isect_max, kEmitChunk), kEmitThreads, 0, st>>>(
+        s.tiles_x, b.erow, b.chunk_row, rb, b.hdr);
+  } else {
+    emit_sorted_kernel<<<(unsigned)eparts, kEmitThreads, 0, st>>>(
+        rows, s.tiles_x, s.tile_passes, ra, b.row_rect, rb, b.hist, b.emit_status, b.hdr);
+  }
   GS_CHECK_LAUNCH();
   hist_scan_kernel<<<s.tile_passes, kRadix, 0, st>>>(b.hist + kDepthPasses * kRadix,
                                                      b.digit_start + kDepthPasses * kRadix);

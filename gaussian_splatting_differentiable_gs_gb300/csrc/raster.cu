@@ -313,7 +313,7 @@ __device__ __forceinline__ int warp_sublist(const Batch& B, int cnt, int x0, int
 // P.list[0..m): each worker thread takes one open pixel; each warp walks the
 // entries whose box meets its pixels.  With `rec`, every composited pair also
 // sets bit j of the record of its pixel's 4x2 quarter (p >> 3).
-template <bool kCount, bool kImp>
+template <bool kCount, bool kImp, int kUnroll>
 __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* wl, int cnt, int k,
                                           int m, int tile_x, int tile_y, int tid, int warp,
                                           int lane, unsigned long long& n_tested,
@@ -344,6 +344,7 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
   int stop_j = cnt;
   int32_t n_inc = 0;
   const int32_t base1 = k * kBatch + 1;  // 1-based list position of entry 0
+#pragma unroll kUnroll
   for (int i = 0; i < nw; ++i) {
     const int j = wl[i];
     const float4 A = B.a[j];
@@ -401,7 +402,7 @@ __device__ __forceinline__ void fwd_batch(PixState& P, const Batch& B, uint8_t* 
 // record each Gaussian's largest blending weight into imp (ids required).
 __device__ __forceinline__ int& slot(int2& s, int i) { return i ? s.y : s.x; }
 
-template <bool kCount, bool kImp = false>
+template <bool kCount, bool kImp = false, int kUnroll = 1>
 __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[kBatch],
                                          float2 (*E)[kBatch], uint8_t (*wl)[kBatch], int32_t* wcount,
                                          const float4* vsplat, const uint32_t* __restrict__ vals,
@@ -454,9 +455,9 @@ __device__ __forceinline__ void fwd_tile(PixState& P, Batch* b, uint32_t (*ids)[
     slot(staged, k & 1) = k;
     if ((bal >> lane) & 1u) P.list[off + __popc(bal & ((1u << lane) - 1u))] = tid;
     __syncthreads();
-    fwd_batch<kCount, kImp>(P, B, wl[warp], cnt, k, m, tile_x, tile_y, tid, warp, lane, n_tested,
-                            n_included, ids ? ids[k & 1] : nullptr, imp, pix_counts, plane, W,
-                            rec_out ? rec : nullptr);
+    fwd_batch<kCount, kImp, kUnroll>(P, B, wl[warp], cnt, k, m, tile_x, tile_y, tid, warp, lane,
+                                     n_tested, n_included, ids ? ids[k & 1] : nullptr, imp,
+                                     pix_counts, plane, W, rec_out ? rec : nullptr);
     __syncthreads();  // pixel state written; slot k & 1 free for batch k + 2
     if (rec_out && tid < kRT / 8 * kWords) {  // this batch's record of the composited entries
       __stcg(rec_out + (int64_t)k * (kRT / 8 * kWords) + tid, (&rec[0][0])[tid]);
@@ -873,9 +874,13 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
   uint32_t* rec_out = (recs && nbt > 0 && slot0 + nbt <= rec_slots) ? recs + slot0 * kRec : nullptr;
   if (tid < kRec) (&S.u.fw.rec[0][0])[tid] = 0u;
   int2 staged;
-  fwd_tile<false>(S.u.fw.px, S.b, S.id, S.e, S.u.fw.wl, S.wcount, vsplat, vals, n, start, end, tile_x,
-                  tile_y, ox, oy, tid, warp, lane, staged, n_tested, n_included, nullptr, nullptr,
-                  0, 0, S.u.fw.rec, rec_out);
+  // the walk unrolled by 8: the pairs of a sub-list are mostly skips, and the
+  // loop overhead and load latency of one entry at a time dominate them
+  // (this kernel only: the separate forward, at a different occupancy, is
+  // slower unrolled)
+  fwd_tile<false, false, 8>(S.u.fw.px, S.b, S.id, S.e, S.u.fw.wl, S.wcount, vsplat, vals, n,
+                            start, end, tile_x, tile_y, ox, oy, tid, warp, lane, staged, n_tested,
+                            n_included, nullptr, nullptr, 0, 0, S.u.fw.rec, rec_out);
 
   // forward results, L1 loss and its gradient, in registers; thread tid owns
   // pixel tid from here on
@@ -1022,19 +1027,15 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
 
 // Zeroes the gradient records of the rows with a positive tile count (the
 // only rows whose gradients the compositing writes and the projection
-// backward reads): 4 bytes read a row, 48 written a visible row.
+// backward reads): 4 bytes read a row, 48 written a visible row.  One thread
+// per 16-byte vector of the records (a warp's stores are contiguous), and one
+// vector per thread: a grid-stride loop's one dependent load at a time per
+// thread ran at 40 % of the copy bandwidth.
 __global__ void __launch_bounds__(256) zero_visible_grads_kernel(int64_t rows,
                                                                  const int32_t* __restrict__ counts,
                                                                  float4* __restrict__ grads) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += stride) {
-    if (__ldg(counts + r) > 0) {
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      grads[3 * r] = z;
-      grads[3 * r + 1] = z;
-      grads[3 * r + 2] = z;
-    }
-  }
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < 3 * rows && __ldg(counts + i / 3) > 0) grads[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // The gradient records' zeroing before a backward: every row, or with tile
@@ -1045,12 +1046,8 @@ gs_status zero_grads(int64_t rows, const int32_t* counts, gs_splat_grad* grads, 
     GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)rows, st));
     return GS_OK;
   }
-  int dev = 0, sms = 0;
-  GS_CUDA(cudaGetDevice(&dev));
-  GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int64_t want = div_up(rows, 256);
-  const unsigned blocks = (unsigned)(want < 8 * sms ? want : 8 * sms);
-  zero_visible_grads_kernel<<<blocks, 256, 0, st>>>(rows, counts, reinterpret_cast<float4*>(grads));
+  zero_visible_grads_kernel<<<(unsigned)div_up(3 * rows, 256), 256, 0, st>>>(
+      rows, counts, reinterpret_cast<float4*>(grads));
   GS_CHECK_LAUNCH();
   return GS_OK;
 }

@@ -11,27 +11,32 @@ sys.path.insert(0, ROOT)
 
 def test_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
     import bench
-    src = tmp_path / "k.cu"
-    src.write_bytes(b"__global__ void k() {}\n")
-    entry = {"source": "k.cu", "sha256": hashlib.sha256(src.read_bytes()).hexdigest(),
-             "workload": "ring", "bytes": 1234}
+    a, b = tmp_path / "k.cu", tmp_path / "h.cu"
+    a.write_bytes(b"__global__ void k() {}\n")
+    b.write_bytes(b"__global__ void h() {}\n")
+    entry = {"sources": {"k.cu": hashlib.sha256(a.read_bytes()).hexdigest(),
+                         "h.cu": hashlib.sha256(b.read_bytes()).hexdigest()},
+             "bytes": 1234}
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "TRAFFIC", {"kernel": entry})
-    assert bench.traffic_of("kernel", "ring", None) == 1234
+    w = bench.TRAFFIC_WORKLOAD
+    assert bench.traffic_of("kernel", w, None) == 1234
     assert bench.traffic_of("kernel", "other", None) is None       # another workload
-    assert bench.traffic_of("kernel", "ring", "morton") is None     # a variant of the run
-    assert bench.traffic_of("unknown", "ring", None) is None
-    src.write_bytes(b"__global__ void k() { }\n")                   # the source changed
-    assert bench.traffic_of("kernel", "ring", None) is None
-    src.unlink()
-    assert bench.traffic_of("kernel", "ring", None) is None
+    assert bench.traffic_of("kernel", w, "morton") is None         # a variant of the run
+    assert bench.traffic_of("unknown", w, None) is None
+    b.write_bytes(b"__global__ void h() { }\n")                   # one source changed
+    assert bench.traffic_of("kernel", w, None) is None
+    b.unlink()
+    assert bench.traffic_of("kernel", w, None) is None
 
 
 def test_traffic_table_names_existing_sources():
     import bench
     for name, t in bench.TRAFFIC.items():
-        assert os.path.exists(os.path.join(ROOT, t["source"])), name
-        assert len(t["sha256"]) == 64 and t["bytes"] > 0, name
+        for src, digest in t["sources"].items():
+            assert os.path.exists(os.path.join(ROOT, src)), name
+            assert len(digest) == 64, name
+        assert t["bytes"] > 0, name
 
 
 def test_oracle_step_full_and_sampled(capsys):

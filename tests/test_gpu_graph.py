@@ -53,6 +53,47 @@ def test_async_binning_equals_sync(name):
     assert torch.equal(ranges2, ranges)
 
 
+def test_async_binning_equals_sync_large_footprints():
+    """Rows of 40 tiles on average: both calls emit in balanced chunks of
+    intersections (the asynchronous one sized by its capacity, the
+    synchronous one by the counts); lists bit for bit equal, and equal to the
+    oracle's."""
+    import oracle
+    gs = _gs()
+    V, W, H, n = 2, 1024, 768, 3000
+    tx, ty = (W + 15) // 16, (H + 15) // 16
+    rng = np.random.default_rng(5)
+    rows = V * n
+    pr = dict(mean2d=np.stack([rng.uniform(-40, W + 40, rows), rng.uniform(-40, H + 40, rows)], 1),
+              conic=np.ones((rows, 3)), opacity=np.full(rows, 0.5), color=np.full((rows, 3), 0.5),
+              depth=rng.choice([1.0, 3.0, 3.0000002, 9.0], rows),
+              radius=rng.integers(40, 80, rows).astype(np.int32), tiles=np.zeros(rows, np.int32))
+    for r in range(rows):
+        x0, x1, y0, y1 = oracle.tile_rect(pr["mean2d"][r, 0], pr["mean2d"][r, 1], pr["radius"][r],
+                                          16, tx, ty)
+        pr["tiles"][r] = (x1 - x0) * (y1 - y0)
+    pr["radius"][pr["tiles"] == 0] = 0
+    rec = pack_records(pr)
+    I_o = int(pr["tiles"].astype(np.int64).sum())
+    assert I_o >= 8 * rows
+    keys_o, vals_o, ranges_o = oracle.bin_and_sort(n, V, rec[:, 0:2], pr["radius"], rec[:, 9], W, H)
+    splats = torch.from_numpy(rec).cuda()
+    cap = I_o + 777
+    ws, keys, vals, ranges = _bufs(gs, n, V, W, H, cap)
+    st, I = gs.gs_bin_and_sort(n, V, splats, W, H, ws, cap, keys, vals, ranges)
+    assert st == gs.GS_OK and I == I_o
+    ws2, keys2, vals2, ranges2 = _bufs(gs, n, V, W, H, cap)
+    nd = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    gs.gs_bin_and_sort_async(n, V, splats, W, H, ws2, cap, keys2, vals2, ranges2, nd)
+    assert gs.gs_workspace_status(ws2) == gs.GS_OK
+    assert int(nd.item()) == I
+    assert np.array_equal(keys[:I].cpu().numpy().view(np.uint64), keys_o)
+    assert np.array_equal(vals[:I].cpu().numpy().view(np.uint32), vals_o)
+    assert np.array_equal(ranges.cpu().numpy(), ranges_o)
+    assert torch.equal(keys2[:I], keys[:I]) and torch.equal(vals2[:I], vals[:I])
+    assert torch.equal(ranges2, ranges)
+
+
 def test_async_binning_overflow_and_recovery():
     gs = _gs()
     n, V, W, H, rec = _records("tiny_2k_256")

@@ -160,22 +160,27 @@ def test_bin_and_sort_equal_depth_ties_break_by_id():
     assert np.array_equal(ranges.cpu().numpy(), ranges_o)
 
 
+@pytest.mark.parametrize("rmax", [6, 120])
 @pytest.mark.parametrize("V,W,H,passes", [(16, 1040, 1024, 3), (16, 16400, 16400, 4)])
-def test_bin_and_sort_three_and_four_tile_passes(V, W, H, passes):
+def test_bin_and_sort_three_and_four_tile_passes(V, W, H, passes, rmax):
     """Views x tiles beyond 2^16 and 2^24: three and four radix passes on the
     tile bits (the buffer chain ends from the other side than with two), with
-    equal depths across views and Gaussians; bit for bit against the oracle."""
+    equal depths across views and Gaussians; bit for bit against the oracle.
+    Radii below 6 px keep rows at one to four tiles (emission by partitions of
+    rows); up to 120 px they average more than eight (emission in balanced
+    chunks of intersections, with the tile digits counted from the rows'
+    rectangles)."""
     import oracle
     gs = _gs()
     n = 2500
     tx, ty = (W + 15) // 16, (H + 15) // 16
     assert (gs.gs_key_bits(V, W, H) - 32 + 7) // 8 == passes
-    rng = np.random.default_rng(11 + passes)
+    rng = np.random.default_rng(11 + passes + rmax)
     rows = V * n
     pr = dict(mean2d=np.stack([rng.uniform(-40, W + 40, rows), rng.uniform(-40, H + 40, rows)], 1),
               conic=np.ones((rows, 3)), opacity=np.full(rows, 0.5), color=np.full((rows, 3), 0.5),
               depth=rng.choice([0.5, 2.0, 2.0000002, 7.0], rows),
-              radius=rng.integers(0, 60, rows).astype(np.int32), tiles=np.zeros(rows, np.int32))
+              radius=rng.integers(0, rmax, rows).astype(np.int32), tiles=np.zeros(rows, np.int32))
     for r in range(rows):
         if pr["radius"][r] > 0:
             x0, x1, y0, y1 = oracle.tile_rect(pr["mean2d"][r, 0], pr["mean2d"][r, 1],
@@ -183,6 +188,8 @@ def test_bin_and_sort_three_and_four_tile_passes(V, W, H, passes):
             pr["tiles"][r] = (x1 - x0) * (y1 - y0)
     pr["radius"][pr["tiles"] == 0] = 0
     rec = pack_records(pr)
+    mean_tiles = pr["tiles"].sum() / max(1, int((pr["tiles"] > 0).sum()))
+    assert (mean_tiles >= 8) == (rmax > 60), mean_tiles  # the emission form this case exercises
     keys_o, vals_o, ranges_o = oracle.bin_and_sort(n, V, rec[:, 0:2], pr["radius"], rec[:, 9], W, H)
     st, I, keys, vals, ranges, ws = _gpu_bin(gs, n, V, rec, W, H)
     assert st == gs.GS_OK and I == keys_o.size > 0

@@ -196,7 +196,19 @@ _BINNING = "gaussian_splatting_differentiable_gs_gb300/csrc/binning.cu"
 _ORDER = "gaussian_splatting_differentiable_gs_gb300/csrc/tile_order.cu"
 _ADAM = "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu"
 TRAFFIC_WORKLOAD = "ring_3m_4x1080p"
-TRAFFIC = {}
+TRAFFIC = {
+    "project": {"sources": {_PROJECT: "49e8c0396a45093103dff381a567b2674796aeb8f2d23798e4a195e35670eadb"},
+                "bytes": 1256300000},
+    "project_bwd": {"sources": {_PROJECT: "49e8c0396a45093103dff381a567b2674796aeb8f2d23798e4a195e35670eadb"},
+                    "bytes": 2630000000},
+    "adam": {"sources": {_ADAM: "7461d48d4dc14b809b9e6d40c07a06c27730c9e24d506df79ddfc7376091fad1"},
+             "bytes": 4895300000},
+    # compaction, six radix passes, emission and the tile order (the three small
+    # scan and check kernels, under 1 MB together, are not counted)
+    "bin_and_sort": {"sources": {_BINNING: "817f87a29e8d54553007c5c423109fd449338c1ab8a3f55013cf7c6777f7887a",
+                                 _ORDER: "4b863354671176f4c937a4a4dac807b3f8f894266513fd909e3ad5a0edd3317a"},
+                     "bytes": 2958600000},
+}
 
 
 def traffic_of(kernel, workload, variant):

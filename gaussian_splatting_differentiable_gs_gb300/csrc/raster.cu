@@ -1027,15 +1027,32 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
 
 // Zeroes the gradient records of the rows with a positive tile count (the
 // only rows whose gradients the compositing writes and the projection
-// backward reads): 4 bytes read a row, 48 written a visible row.  One thread
-// per 16-byte vector of the records (a warp's stores are contiguous), and one
-// vector per thread: a grid-stride loop's one dependent load at a time per
-// thread ran at 40 % of the copy bandwidth.
+// backward reads): 4 bytes read a row, 48 written a visible row.  Rows go in
+// pairs, 96 bytes = three whole 32-byte sectors, both zeroed when either is
+// visible: a lone 48-byte record half-fills a sector, and the partial writes
+// cost the memory a read.  One thread per pair of rows (one 8-byte load of
+// the two counts, six 16-byte stores): where few rows are visible most
+// threads only read.
 __global__ void __launch_bounds__(256) zero_visible_grads_kernel(int64_t rows,
                                                                  const int32_t* __restrict__ counts,
                                                                  float4* __restrict__ grads) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < 3 * rows && __ldg(counts + i / 3) > 0) grads[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // rows 2q, 2q + 1
+  const int64_t r = 2 * q;
+  if (r >= rows) return;
+  bool any;
+  if (r + 1 < rows && ((reinterpret_cast<uintptr_t>(counts) & 7u) == 0)) {
+    const int2 c = __ldg(reinterpret_cast<const int2*>(counts) + q);
+    any = c.x > 0 || c.y > 0;
+  } else {
+    any = __ldg(counts + r) > 0 || (r + 1 < rows && __ldg(counts + r + 1) > 0);
+  }
+  if (!any) return;
+  const int nv = r + 1 < rows ? 6 : 3;
+  float4* g = grads + 3 * r;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int v = 0; v < 6; ++v)
+    if (v < nv) g[v] = z;
 }
 
 // The gradient records' zeroing before a backward: every row, or with tile
@@ -1046,7 +1063,7 @@ gs_status zero_grads(int64_t rows, const int32_t* counts, gs_splat_grad* grads, 
     GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)rows, st));
     return GS_OK;
   }
-  zero_visible_grads_kernel<<<(unsigned)div_up(3 * rows, 256), 256, 0, st>>>(
+  zero_visible_grads_kernel<<<(unsigned)div_up(div_up(rows, 2), 256), 256, 0, st>>>(
       rows, counts, reinterpret_cast<float4*>(grads));
   GS_CHECK_LAUNCH();
   return GS_OK;

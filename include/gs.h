@@ -299,8 +299,10 @@ gs_status gs_loss_l1(const float* image, const float* target, int64_t count, flo
  * atomics.
  *   tile_counts  [n_views * n] from gs_project, or NULL
  *   grads  [n_views * n] output, zeroed by this call, then accumulated; with
- *          tile_counts, only the rows with a positive count are zeroed and
- *          written (the others are left as they were) */
+ *          tile_counts, only the rows with a positive count are written, and
+ *          the records are zeroed in pairs of rows (2k, 2k+1) of which one at
+ *          least is visible (a culled row's record is either left as it was
+ *          or zeroed) */
 gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats,
                            const int32_t* tile_counts, int32_t width,
                            int32_t height, const uint32_t* vals, const int64_t* ranges,

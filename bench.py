@@ -197,6 +197,9 @@ _ORDER = "gaussian_splatting_differentiable_gs_gb300/csrc/tile_order.cu"
 _ADAM = "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu"
 TRAFFIC_WORKLOAD = "ring_3m_4x1080p"
 TRAFFIC = {
+    # the compositing kernel and the gradient zeroing it launches first
+    "rasterize_fused": {"sources": {_RASTER: "efc3d106ca26cba1cdc2c825102b0ffe9f625b238cfdf16eeb07e0ac1da9ac60"},
+                        "bytes": 5912600000},
     "project": {"sources": {_PROJECT: "49e8c0396a45093103dff381a567b2674796aeb8f2d23798e4a195e35670eadb"},
                 "bytes": 1256300000},
     "project_bwd": {"sources": {_PROJECT: "49e8c0396a45093103dff381a567b2674796aeb8f2d23798e4a195e35670eadb"},

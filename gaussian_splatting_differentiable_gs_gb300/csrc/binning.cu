@@ -41,8 +41,13 @@ namespace {
 
 constexpr int kCompThreads = 256;
 constexpr int kCompWarps = kCompThreads / 32;
-constexpr int kCompItems = 8;                           // rows per thread (warp-striped)
-constexpr int kCompPart = kCompThreads * kCompItems;    // rows per compaction partition
+constexpr int kCompItems = 8;                           // rows per thread and chunk (warp-striped)
+constexpr int kCompChunk = kCompThreads * kCompItems;   // rows per chunk
+// chunks per compaction partition: 4, or 8 from kCompWideRows rows on (fewer
+// partitions shorten the look-back chain, which sets the pace of a call over
+// hundreds of millions of mostly culled rows)
+constexpr int kCompPart = kCompChunk * 4;               // rows per partition, at most
+constexpr int64_t kCompWideRows = (int64_t)1 << 27;
 
 constexpr int kEmitThreads = 512;
 constexpr int kEmitItems = 4;
@@ -195,19 +200,33 @@ __device__ long long lookback_prefix_warp(uint64_t* status, int64_t part, long l
 //    | c) into sort_in (when c < capacity), row_u[c] and row_rect[c]; the
 //    intersection total I into the header (block sums added atomically) and
 //    R by the last partition; the depth-digit histograms.  Positive depths
-//    order as their bit patterns.  A row whose rectangle disagrees with its
-//    stored tile count (records not produced by gs_project) is left out and
-//    raises the device-check bit.  With a tile-count array the counts are
-//    read first (4 bytes a row) and only the visible rows' records after.
-__global__ void __launch_bounds__(kCompThreads) compact_rows_kernel(
+//    order as their bit patterns.  The visible rows are found from the tile
+//    counts alone (the array, else the records' tile words), so that a
+//    partition publishes its aggregate for the look-back after one round of
+//    loads; their records are read after the look-back.  A row whose
+//    rectangle disagrees with its count (records not produced by
+//    gs_project) raises the device-check bit and keeps its position with an
+//    empty rectangle: it emits nothing and adds nothing to I.
+// A row's tile count: the array's, else the record's tile word (0 past the end).
+__device__ __forceinline__ int32_t row_count(int64_t r, int64_t n_rows,
+                                             const float4* __restrict__ splats,
+                                             const int32_t* __restrict__ counts) {
+  if (r >= n_rows) return 0;
+  return counts ? __ldg(counts + r) : __float_as_int(splats[3 * r + 2].w);
+}
+
+template <int kCompChunks>
+__global__ void __launch_bounds__(kCompThreads, 4) compact_rows_kernel(
     int64_t n_rows, int64_t n, int32_t tiles_x, int32_t tiles_y, int64_t T, int64_t capacity,
     const float4* __restrict__ splats, const int32_t* __restrict__ counts,
     uint64_t* __restrict__ sort_in,
     uint64_t* __restrict__ row_u, uint64_t* __restrict__ row_rect, uint32_t* __restrict__ hist,
     uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
   __shared__ uint32_t sh[kDepthPasses * kRadix];
-  __shared__ uint32_t s_warp[kCompWarps];
+  __shared__ uint32_t s_warp[kCompChunks][kCompWarps];
   __shared__ unsigned long long s_tiles[kCompWarps];
+  __shared__ uint8_t s_lidx[kCompWarps][16 * kCompItems];  // a sparse warp chunk's visible
+  __shared__ int32_t s_lcnt[kCompWarps][16 * kCompItems];  // rows (offsets), their counts
   __shared__ long long s_prefix;
   __shared__ int s_part;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -215,97 +234,165 @@ __global__ void __launch_bounds__(kCompThreads) compact_rows_kernel(
   for (int i = tid; i < kDepthPasses * kRadix; i += kCompThreads) sh[i] = 0;
   __syncthreads();
   const int64_t part = s_part;
-  // item i of lane l of warp w: row part * kCompPart + w * 32 * kCompItems + 32 i + l
-  const int64_t wbase = part * kCompPart + (int64_t)warp * 32 * kCompItems;
-  uint32_t dbits[kCompItems];
-  uint64_t rect[kCompItems];
-  uint32_t mask[kCompItems];
-  uint32_t wcount = 0;
-  unsigned long long tiles_sum = 0;
-  int32_t cnt[kCompItems];
-  if (counts) {
+  // item i of lane l of warp w in chunk k: row
+  // part * kRows + k * kCompChunk + w * 32 * kCompItems + 32 i + l
+  constexpr int kRows = kCompChunk * kCompChunks;
+  const int64_t wbase = part * kRows + (int64_t)warp * 32 * kCompItems + lane;
+  // 1. the rows with a positive tile count, per chunk and warp: the
+  //    partition's aggregate for the look-back is published after one round
+  //    of 4-byte loads (the tile-count array), however few rows are visible
 #pragma unroll
-    for (int i = 0; i < kCompItems; ++i) {
-      const int64_t r = wbase + 32 * i + lane;
-      cnt[i] = r < n_rows ? __ldg(counts + r) : 0;
-    }
-  }
+  for (int k = 0; k < kCompChunks; ++k) {
+    int32_t cnt[kCompItems];
 #pragma unroll
-  for (int i = 0; i < kCompItems; ++i) {
-    const int64_t r = wbase + 32 * i + lane;
-    bool vis = false;
-    dbits[i] = 0;
-    rect[i] = 0;
-    if (r < n_rows && (!counts || cnt[i] > 0)) {
-      const float4 tail = splats[3 * r + 2];
-      const int32_t tiles = counts ? cnt[i] : __float_as_int(tail.w);
-      if (tiles > 0) {
-        const float4 head = splats[3 * r];
-        int32_t x0, x1, y0, y1;
-        tile_rect(head.x, head.y, __float_as_int(tail.z), tiles_x, tiles_y, x0, x1, y0, y1);
-        if ((int64_t)(x1 - x0) * (y1 - y0) == tiles) {
-          vis = true;
-          const int64_t view = r / n;
-          const uint32_t first = (uint32_t)(view * T + (int64_t)y0 * tiles_x + x0);
-          rect[i] = (uint64_t)first | ((uint64_t)(x1 - x0) << 32) | ((uint64_t)(y1 - y0) << 48);
-          dbits[i] = __float_as_uint(tail.y);
-          tiles_sum += (unsigned long long)tiles;
-        } else {
-          atomicOr(&hdr->error, 2u);
-        }
-      }
-    }
-    if (vis) {
+    for (int i = 0; i < kCompItems; ++i)
+      cnt[i] = row_count(wbase + (int64_t)k * kCompChunk + 32 * i, n_rows, splats, counts);
+    uint32_t wc = 0;
 #pragma unroll
-      for (int p = 0; p < kDepthPasses; ++p)
-        atomicAdd(&sh[p * kRadix + ((dbits[i] >> (8 * p)) & 0xFF)], 1u);
-    }
-    mask[i] = __ballot_sync(0xffffffffu, vis);
-    wcount += __popc(mask[i]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tiles_sum += __shfl_xor_sync(0xffffffffu, tiles_sum, o);
-  if (lane == 0) {
-    s_warp[warp] = wcount;
-    s_tiles[warp] = tiles_sum;
+    for (int i = 0; i < kCompItems; ++i) wc += __popc(__ballot_sync(0xffffffffu, cnt[i] > 0));
+    if (lane == 0) s_warp[k][warp] = wc;
   }
   __syncthreads();
-  uint32_t warp_excl = 0, block_count = 0;
+  uint32_t block_count = 0;
 #pragma unroll
-  for (int w = 0; w < kCompWarps; ++w) {
-    warp_excl += w < warp ? s_warp[w] : 0u;
-    block_count += s_warp[w];
-  }
+  for (int k = 0; k < kCompChunks; ++k)
+#pragma unroll
+    for (int w = 0; w < kCompWarps; ++w) block_count += s_warp[k][w];
   if (warp == 0) {
     const long long prefix = lookback_prefix_warp(status, part, (long long)block_count, hdr);
     if (lane == 0) {
-      unsigned long long bt = 0;
-#pragma unroll
-      for (int w = 0; w < kCompWarps; ++w) bt += s_tiles[w];
-      if (bt) atomicAdd(&hdr->total, bt);
       s_prefix = prefix;
-      if (prefix >= 0 && (part + 1) * kCompPart >= n_rows)
+      if (prefix >= 0 && (part + 1) * kRows >= n_rows)
         hdr->rows = (unsigned long long)(prefix + block_count);
     }
   }
   __syncthreads();
+  // 2. the same counts again (cached), and the visible rows' records,
+  //    checked against the counts and written at their compact positions.  A
+  //    row whose rectangle disagrees with its count raises the device-check
+  //    bit and keeps its position with an empty rectangle (it emits no
+  //    intersection and adds nothing to the total)
+  unsigned long long tiles_sum = 0;
   if (s_prefix >= 0) {
     const uint32_t lt = (1u << lane) - 1u;
-    int64_t c = s_prefix + warp_excl;
+    int64_t base = s_prefix;
+#pragma unroll 1
+    for (int k = 0; k < kCompChunks; ++k) {
+      uint32_t before = 0, total = 0;
 #pragma unroll
-    for (int i = 0; i < kCompItems; ++i) {
-      if ((mask[i] >> lane) & 1u) {
-        const int64_t ci = c + __popc(mask[i] & lt);
-        const int64_t r = wbase + 32 * i + lane;
-        if (ci < capacity) sort_in[ci] = ((uint64_t)dbits[i] << 32) | (uint64_t)ci;
-        // rows < 2^32: the Gaussian id by 32-bit arithmetic
-        row_u[ci] = ((uint64_t)dbits[i] << 32) | (uint64_t)((uint32_t)r % (uint32_t)n);
-        row_rect[ci] = rect[i];
+      for (int w = 0; w < kCompWarps; ++w) {
+        before += w < warp ? s_warp[k][w] : 0u;
+        total += s_warp[k][w];
       }
-      c += __popc(mask[i]);
+      const int64_t c = base + before;
+      const int64_t cbase = part * kRows + (int64_t)k * kCompChunk + warp * 32 * kCompItems;
+      int32_t cnt[kCompItems];
+      int nvis = 0;
+#pragma unroll
+      for (int i = 0; i < kCompItems; ++i) {
+        cnt[i] = row_count(cbase + 32 * i + lane, n_rows, splats, counts);
+        nvis += __popc(__ballot_sync(0xffffffffu, cnt[i] > 0));
+      }
+      // one visible row: its rectangle checked against its count, its three
+      // words written at compact index ci, its depth digits counted
+      auto emit_row = [&](uint32_t r, int32_t cq, float2 mean, float dep, int32_t rad,
+                          int64_t ci) {
+        const uint32_t view = r / (uint32_t)n, g = r - view * (uint32_t)n;  // rows < 2^32
+        int32_t x0, x1, y0, y1;
+        tile_rect(mean.x, mean.y, rad, tiles_x, tiles_y, x0, x1, y0, y1);
+        uint64_t rect = 0;
+        if ((int64_t)(x1 - x0) * (y1 - y0) == cq) {
+          const uint32_t first = (uint32_t)((int64_t)view * T + (int64_t)y0 * tiles_x + x0);
+          rect = (uint64_t)first | ((uint64_t)(x1 - x0) << 32) | ((uint64_t)(y1 - y0) << 48);
+          tiles_sum += (unsigned long long)cq;
+        } else {
+          atomicOr(&hdr->error, 2u);
+        }
+        const uint32_t dbits = __float_as_uint(dep);
+        if (ci < capacity) sort_in[ci] = ((uint64_t)dbits << 32) | (uint64_t)ci;
+        row_u[ci] = ((uint64_t)dbits << 32) | (uint64_t)g;
+        row_rect[ci] = rect;
+#pragma unroll
+        for (int p = 0; p < kDepthPasses; ++p)
+          atomicAdd(&sh[p * kRadix + ((dbits >> (8 * p)) & 0xFF)], 1u);
+      };
+      // every visible row's record fields are requested before the first is
+      // used, so a chunk waits for one round of loads
+      float2 mean[kCompItems];
+      float dep[kCompItems];
+      int32_t rad[kCompItems];
+      if (nvis > 16 * kCompItems) {
+        // mostly visible: item by item, in place
+#pragma unroll
+        for (int i = 0; i < kCompItems; ++i) {
+          mean[i] = make_float2(0.f, 0.f);
+          dep[i] = 0.f;
+          rad[i] = 0;
+          if (cnt[i] > 0) {
+            const float* rec = reinterpret_cast<const float*>(splats + 3 * (cbase + 32 * i + lane));
+            mean[i] = __ldg(reinterpret_cast<const float2*>(rec));
+            dep[i] = __ldg(rec + 9);
+            rad[i] = __float_as_int(__ldg(rec + 10));
+          }
+        }
+        int64_t cc = c;
+#pragma unroll
+        for (int i = 0; i < kCompItems; ++i) {
+          const uint32_t m = __ballot_sync(0xffffffffu, cnt[i] > 0);
+          if (cnt[i] > 0)
+            emit_row((uint32_t)(cbase + 32 * i + lane), cnt[i], mean[i], dep[i], rad[i],
+                     cc + __popc(m & lt));
+          cc += __popc(m);
+        }
+      } else {
+        // sparse: the visible rows listed in row order, then one per lane
+        uint8_t* lidx = s_lidx[warp];
+        int32_t* lcnt = s_lcnt[warp];
+        int at = 0;
+#pragma unroll
+        for (int i = 0; i < kCompItems; ++i) {
+          const uint32_t m = __ballot_sync(0xffffffffu, cnt[i] > 0);
+          if (cnt[i] > 0) {
+            lidx[at + __popc(m & lt)] = (uint8_t)(32 * i + lane);
+            lcnt[at + __popc(m & lt)] = cnt[i];
+          }
+          at += __popc(m);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < kCompItems / 2; ++q) {
+          const int j = 32 * q + lane;
+          mean[q] = make_float2(0.f, 0.f);
+          dep[q] = 0.f;
+          rad[q] = 0;
+          if (j < nvis) {
+            const float* rec = reinterpret_cast<const float*>(splats + 3 * (cbase + lidx[j]));
+            mean[q] = __ldg(reinterpret_cast<const float2*>(rec));
+            dep[q] = __ldg(rec + 9);
+            rad[q] = __float_as_int(__ldg(rec + 10));
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kCompItems / 2; ++q) {
+          const int j = 32 * q + lane;
+          if (j < nvis)
+            emit_row((uint32_t)cbase + lidx[j], lcnt[j], mean[q], dep[q], rad[q], c + j);
+        }
+        __syncwarp();  // the list is rewritten by the next chunk
+      }
+      base += total;
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tiles_sum += __shfl_xor_sync(0xffffffffu, tiles_sum, o);
+  if (lane == 0) s_tiles[warp] = tiles_sum;
   __syncthreads();
+  if (tid == 0) {
+    unsigned long long bt = 0;
+#pragma unroll
+    for (int w = 0; w < kCompWarps; ++w) bt += s_tiles[w];
+    if (bt) atomicAdd(&hdr->total, bt);
+  }
   for (int i = tid; i < kDepthPasses * kRadix; i += kCompThreads)
     if (sh[i]) atomicAdd(&hist[i], sh[i]);
 }
@@ -1168,9 +1255,11 @@ uint64_t* rows_buffer(const BinShape& s, const BinBufs& b, uint64_t* keys) {
 gs_status launch_compaction(const BinShape& s, const BinBufs& b, const gs_splat* splats,
                             const int32_t* counts, int64_t capacity, uint64_t* keys,
                             cudaStream_t st) {
-  const int64_t parts = div_up(s.n_rows, kCompPart);
+  const bool wide = s.n_rows >= kCompWideRows;
+  const int64_t parts = div_up(s.n_rows, wide ? 2 * kCompPart : kCompPart);
   GS_CUDA(cudaMemsetAsync(b.scan_status, 0, sizeof(uint64_t) * (size_t)parts, st));
-  compact_rows_kernel<<<(unsigned)parts, kCompThreads, 0, st>>>(
+  auto kernel = wide ? compact_rows_kernel<8> : compact_rows_kernel<4>;
+  kernel<<<(unsigned)parts, kCompThreads, 0, st>>>(
       s.n_rows, s.n, s.tiles_x, s.tiles_y, s.T, capacity, reinterpret_cast<const float4*>(splats),
       counts, rows_buffer(s, b, keys), b.row_u, b.row_rect, b.hist, b.scan_status, b.hdr);
   GS_CHECK_LAUNCH();
@@ -1270,9 +1359,9 @@ extern "C" gs_status gs_selftest_lookback_timeout(void* workspace, size_t ws_byt
   GS_CUDA(cudaMemsetAsync(b.scan_status, 0, sizeof(uint64_t) * 2, st));
   const unsigned one = 1;
   GS_CUDA(cudaMemcpyAsync(&b.hdr->scan_ticket, &one, sizeof(one), cudaMemcpyHostToDevice, st));
-  compact_rows_kernel<<<1, kCompThreads, 0, st>>>(0, 1, 1, 1, 1, 1, nullptr, nullptr, b.tmp,
-                                                  b.row_u, b.row_rect, b.hist, b.scan_status,
-                                                  b.hdr);
+  compact_rows_kernel<4><<<1, kCompThreads, 0, st>>>(0, 1, 1, 1, 1, 1, nullptr, nullptr, b.tmp,
+                                                     b.row_u, b.row_rect, b.hist, b.scan_status,
+                                                     b.hdr);
   GS_CHECK_LAUNCH();
   return gs_workspace_status(workspace, stream);
 }

@@ -744,3 +744,49 @@ def test_tile_counts_path_matches_records_path(case):
     gs.gs_project_bwd(params, o["cams"], sb, gc, grad_b, vis_b, tile_counts=counts)
     assert torch.equal(grad_a, grad_b)
     assert torch.equal(vis_a, vis_b)
+
+
+def test_bin_and_sort_device_check_on_inconsistent_record():
+    """A record whose tile count disagrees with its rectangle (records not
+    made by gs_project) is reported, not trusted: the synchronous call
+    returns GS_ERR_DEVICE_CHECK; the asynchronous one finishes with the row
+    emitting nothing (its lists equal the oracle's without that row) and
+    reports the check through the workspace status, which the next call
+    clears."""
+    import oracle
+    gs = _gs()
+    o = oracle_side("ragged2")
+    n, V, W, H = o["n"], o["V"], o["W"], o["H"]
+    rec = pack_records(o["pr"]).copy()
+    tiles = rec.view(np.int32)[:, 11]
+    bad = int(np.nonzero(tiles > 0)[0][5])
+    rec.view(np.int32)[bad, 11] += 1
+    cap = int(tiles.astype(np.int64).sum()) + 64
+    with pytest.raises(gs.GSError) as e:
+        _gpu_bin(gs, n, V, rec, W, H, capacity=cap)
+    assert e.value.status == gs.GS_ERR_DEVICE_CHECK
+    # the asynchronous call: same workspace shape, the row left out of the lists
+    rows = n * V
+    T = gs.tiles_per_view(W, H)
+    ws = torch.zeros(gs.gs_bin_workspace_bytes(rows, cap), dtype=torch.uint8, device="cuda")
+    keys = torch.empty(cap, dtype=torch.int64, device="cuda")
+    vals = torch.empty(cap, dtype=torch.int32, device="cuda")
+    ranges = torch.empty((V * T, 2), dtype=torch.int64, device="cuda")
+    nd = torch.zeros(1, dtype=torch.int64, device="cuda")
+    gs.gs_bin_and_sort_async(n, V, _cuda(rec), W, H, ws, cap, keys, vals, ranges, nd)
+    assert gs.gs_workspace_status(ws) == gs.GS_ERR_DEVICE_CHECK
+    radius = o["f32"]["radius"].copy()
+    radius[bad] = 0
+    keys_o, vals_o, ranges_o = oracle.bin_and_sort(n, V, o["f32"]["mean2d"].astype(np.float32),
+                                                   radius, o["f32"]["depth"].astype(np.float32),
+                                                   W, H)
+    I = int(nd.item())
+    assert I == keys_o.size
+    assert np.array_equal(keys[:I].cpu().numpy().view(np.uint64), keys_o)
+    assert np.array_equal(vals[:I].cpu().numpy().view(np.uint32), vals_o)
+    assert np.array_equal(ranges.cpu().numpy(), ranges_o)
+    # a consistent call on the same workspace is clean again
+    good = pack_records(o["pr"])
+    gs.gs_bin_and_sort_async(n, V, _cuda(good), W, H, ws, cap, keys, vals, ranges, nd)
+    assert gs.gs_workspace_status(ws) == gs.GS_OK
+    assert int(nd.item()) == o["keys"].size

@@ -832,13 +832,12 @@ struct FusedSmem {
     } fw;  // forward
     struct {
       float acc[kBatch][9];
-      uint32_t qm[kWarps][4][kWords];  // masks of quarter warp * 4 + q
+      alignas(16) uint32_t qm[kWarps][4][kWords];  // masks of quarter warp * 4 + q
       alignas(16) int32_t qlast[kWarps][4];
       // per-pixel state between batches, for a warp that takes other quarters
       float pT[kRT], pS0[kRT], pS1[kRT], pS2[kRT];
       int32_t plast[kRT];
       uint8_t pg[kRT];     // signs of the L1 gradient, 2 bits per channel
-      uint8_t order[32];   // quarters by descending count of recorded entries
     } bw;  // backward
   } u;
   int32_t wcount[kWarps];
@@ -962,22 +961,28 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
     }
     cp_async_commit();
   };
+  // the record of batch k (kRec words, 16-byte pieces) into the mask space
+  auto issue_rec = [&](int k) {
+    if (tid < kRec / 4)
+      cp_async16(&S.u.bw.qm[0][0][0] + 4 * tid, rec_out + (int64_t)k * kRec + 4 * tid);
+    cp_async_commit();
+  };
   const int kt = max_last > 0 ? (max_last - 1) / kBatch : -1;
   if (kt >= 0 && slot(staged, kt & 1) != kt) {
     issue(kt);
     slot(staged, kt & 1) = -1;
-  } else {
-    cp_async_commit();
   }
+  if (kt >= 0 && regroup) issue_rec(kt);
+  // One barrier a batch besides the walk's: batch k - 1 is gathered, and
+  // batch k - 1's record fetched, only after the barrier that follows the
+  // walk (record) or the flush (slot) of the batch that used the space last.
   for (int k = kt; k >= 0; --k) {
+    cp_async_wait<0>();
+    __syncthreads();  // batch k and its record landed; batch k + 1 flushed, its slot free
     if (k >= 1 && slot(staged, (k - 1) & 1) != k - 1) {
       issue(k - 1);
       slot(staged, (k - 1) & 1) = -1;
-    } else {
-      cp_async_commit();
     }
-    cp_async_wait<1>();
-    __syncthreads();  // batch k landed (or staged by the forward)
     Batch& B = S.b[k & 1];
     const int lo = k * kBatch;
     const int cnt = min(kBatch, max_last - lo);
@@ -987,19 +992,14 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
       __syncthreads();
     }
     if (regroup) {
-      // the batch's record (quarter Q's words at Q * kWords), the quarters'
-      // order, then this lane's quarter and pixel
-      uint32_t* qall = &S.u.bw.qm[0][0][0];
-      if (tid < kRec) qall[tid] = __ldcg(rec_out + (int64_t)k * kRec + tid);
-      __syncthreads();
-      if (warp == 0) {
-        int c = 0;
+      // the batch's record (quarter Q's words at Q * kWords); every warp
+      // ranks the quarters itself and takes those ranked 4w..4w+3
+      const uint32_t* qall = &S.u.bw.qm[0][0][0];
+      int c = 0;
 #pragma unroll
-        for (int w = 0; w < kWords; ++w) c += __popc(qall[lane * kWords + w]);
-        S.u.bw.order[lane] = (uint8_t)quarter_rank_order(c, lane);
-      }
-      __syncthreads();
-      const int Q = S.u.bw.order[warp * 4 + ((lane >> 3) & 3)];
+      for (int w = 0; w < kWords; ++w) c += __popc(qall[lane * kWords + w]);
+      const int ranked = quarter_rank_order(c, lane);
+      const int Q = __shfl_sync(0xffffffffu, ranked, warp * 4 + ((lane >> 3) & 3));
       const int p = Q * 8 + (lane & 7);
       int qx, qy;
       pixel_of(p, tile_x, tile_y, qx, qy);
@@ -1018,9 +1018,9 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
       bwd_walk(B, S.u.bw.acc, S.u.bw.qm[warp][(lane >> 3) & 3], nw, lo, ix, iy, last, Tr, S0, S1,
                S2, g0, g1, g2, lane);
     }
-    __syncthreads();
+    __syncthreads();  // the walk is done: sums complete, record and masks free
+    if (regroup && k >= 1) issue_rec(k - 1);
     bwd_flush(B, S.e[k & 1], S.id[k & 1], S.u.bw.acc, cnt, grads + 3 * view * n, tid);
-    __syncthreads();
   }
   cp_async_wait<0>();
 }

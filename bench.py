@@ -198,8 +198,8 @@ _ADAM = "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu"
 TRAFFIC_WORKLOAD = "ring_3m_4x1080p"
 TRAFFIC = {
     # the compositing kernel and the gradient zeroing it launches first
-    "rasterize_fused": {"sources": {_RASTER: "efc3d106ca26cba1cdc2c825102b0ffe9f625b238cfdf16eeb07e0ac1da9ac60"},
-                        "bytes": 5912600000},
+    "rasterize_fused": {"sources": {_RASTER: "1b452010b5a489ed270a28ddb6acb1c4a11890516d48dbd717a53eccfb8405c3"},
+                        "bytes": 5915100000},
     "project": {"sources": {_PROJECT: "49e8c0396a45093103dff381a567b2674796aeb8f2d23798e4a195e35670eadb"},
                 "bytes": 1256300000},
     "project_bwd": {"sources": {_PROJECT: "49e8c0396a45093103dff381a567b2674796aeb8f2d23798e4a195e35670eadb"},
@@ -208,9 +208,9 @@ TRAFFIC = {
              "bytes": 4895300000},
     # compaction, six radix passes, emission and the tile order (the three small
     # scan and check kernels, under 1 MB together, are not counted)
-    "bin_and_sort": {"sources": {_BINNING: "817f87a29e8d54553007c5c423109fd449338c1ab8a3f55013cf7c6777f7887a",
+    "bin_and_sort": {"sources": {_BINNING: "b7ef503721627500fe6c326ebfa815641016e1b88975c4154b7f9f3abc9305b3",
                                  _ORDER: "4b863354671176f4c937a4a4dac807b3f8f894266513fd909e3ad5a0edd3317a"},
-                     "bytes": 2958600000},
+                     "bytes": 2999800000},
 }
 
 

@@ -43,11 +43,13 @@ constexpr int kCompThreads = 256;
 constexpr int kCompWarps = kCompThreads / 32;
 constexpr int kCompItems = 8;                           // rows per thread and chunk (warp-striped)
 constexpr int kCompChunk = kCompThreads * kCompItems;   // rows per chunk
-// chunks per compaction partition: 4, or 8 from kCompWideRows rows on (fewer
-// partitions shorten the look-back chain, which sets the pace of a call over
-// hundreds of millions of mostly culled rows)
-constexpr int kCompPart = kCompChunk * 4;               // rows per partition, at most
-constexpr int64_t kCompWideRows = (int64_t)1 << 27;
+// chunks per compaction partition: 1 below 2^21 rows (enough partitions to
+// fill the GPU), 4 up to 2^27, 8 beyond (fewer partitions shorten the
+// look-back chain, which sets the pace of a call over hundreds of millions of
+// mostly culled rows)
+inline int comp_chunks(int64_t n_rows) {
+  return n_rows < ((int64_t)1 << 21) ? 1 : (n_rows < ((int64_t)1 << 27) ? 4 : 8);
+}
 
 constexpr int kEmitThreads = 512;
 constexpr int kEmitItems = 4;
@@ -115,7 +117,7 @@ inline WsLayout ws_layout(int64_t n_rows, int64_t capacity) {
   size_t off = sizeof(WsHeader);
   L.hist = off;        off += align256(sizeof(uint32_t) * kMaxPasses * kRadix);
   L.digit_start = off; off += align256(sizeof(uint32_t) * kMaxPasses * kRadix);
-  L.scan_status = off; off += align256(sizeof(uint64_t) * (size_t)div_up(r, kCompPart));
+  L.scan_status = off; off += align256(sizeof(uint64_t) * (size_t)div_up(r, kCompChunk));
   L.emit_status = off; off += align256(sizeof(uint64_t) * (size_t)div_up(r, kEmitPart));
   L.sort_status = off; off += align256(sizeof(uint64_t) * kRadix * (size_t)sort_parts);
   L.row_u = off;       off += align256(sizeof(uint64_t) * (size_t)r);
@@ -1255,10 +1257,11 @@ uint64_t* rows_buffer(const BinShape& s, const BinBufs& b, uint64_t* keys) {
 gs_status launch_compaction(const BinShape& s, const BinBufs& b, const gs_splat* splats,
                             const int32_t* counts, int64_t capacity, uint64_t* keys,
                             cudaStream_t st) {
-  const bool wide = s.n_rows >= kCompWideRows;
-  const int64_t parts = div_up(s.n_rows, wide ? 2 * kCompPart : kCompPart);
+  const int chunks = comp_chunks(s.n_rows);
+  const int64_t parts = div_up(s.n_rows, (int64_t)chunks * kCompChunk);
   GS_CUDA(cudaMemsetAsync(b.scan_status, 0, sizeof(uint64_t) * (size_t)parts, st));
-  auto kernel = wide ? compact_rows_kernel<8> : compact_rows_kernel<4>;
+  auto kernel = chunks == 1 ? compact_rows_kernel<1>
+                            : (chunks == 4 ? compact_rows_kernel<4> : compact_rows_kernel<8>);
   kernel<<<(unsigned)parts, kCompThreads, 0, st>>>(
       s.n_rows, s.n, s.tiles_x, s.tiles_y, s.T, capacity, reinterpret_cast<const float4*>(splats),
       counts, rows_buffer(s, b, keys), b.row_u, b.row_rect, b.hist, b.scan_status, b.hdr);

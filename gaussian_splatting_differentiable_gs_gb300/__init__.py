@@ -79,6 +79,8 @@ def lib():
     L.gs_compact_index.argtypes = [i64, vp, vp, sz, vp, vp, vp]
     L.gs_rasterize_fused.argtypes = [i64, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                      vp, vp, vp, sz, vp]
+    L.gs_rasterize_fused_acc.argtypes = L.gs_rasterize_fused.argtypes
+    L.gs_zero_grads.argtypes = [i64, i32, vp, vp, vp]
     L.gs_rasterize_workspace_bytes.argtypes = [i32, i32, i32, i64]
     L.gs_rasterize_workspace_bytes.restype = sz
     L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp, vp]
@@ -274,11 +276,14 @@ def gs_rasterize_workspace_bytes(n_views, width, height, capacity):
 
 def gs_rasterize_fused(n, n_views, splats, width, height, vals, ranges, bg, target, image,
                        T_final, n_contrib, loss, grads, stream=None, tile_order=None,
-                       workspace=None, tile_counts=None):
+                       workspace=None, tile_counts=None, accumulate=False):
     """workspace: None, or a CUDA uint8 tensor of gs_rasterize_workspace_bytes()
-    bytes (the backward then walks the pairs the forward composited)."""
+    bytes (the backward then walks the pairs the forward composited).
+    accumulate: add to grads as they stand (gs_rasterize_fused_acc; grads
+    zeroed before by gs_zero_grads) instead of zeroing them first."""
     bgv = (C.c_float * 3)(*[float(b) for b in bg])
-    _check("gs_rasterize_fused", lib().gs_rasterize_fused(
+    fn = lib().gs_rasterize_fused_acc if accumulate else lib().gs_rasterize_fused
+    _check("gs_rasterize_fused", fn(
         n, n_views, _dev(splats, torch.float32, "splats"),
         _dev(tile_counts, torch.int32, "tile_counts"), width, height,
         _dev(vals, torch.int32, "vals"), _dev(ranges, torch.int64, "ranges"),
@@ -288,6 +293,14 @@ def gs_rasterize_fused(n, n_views, splats, width, height, vals, ranges, bg, targ
         _dev(loss, torch.float32, "loss"), _dev(grads, torch.float32, "grads"),
         _dev(workspace, torch.uint8, "workspace"),
         0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def gs_zero_grads(n, n_views, grads, stream=None, tile_counts=None):
+    """Zeroes the gradient records the compositing backward adds to (all
+    rows, or with tile_counts the pairs of rows of which one is visible)."""
+    _check("gs_zero_grads", lib().gs_zero_grads(
+        n, n_views, _dev(tile_counts, torch.int32, "tile_counts"),
+        _dev(grads, torch.float32, "grads"), _stream(stream)))
 
 
 def gs_morton_workspace_bytes(n):
@@ -467,11 +480,15 @@ class TrainStep:
                          self.T_final, self.n_contrib, self.dL_dimage, self.grads2d, stream,
                          tile_order=self.tile_order, tile_counts=self.tile_counts)
 
-    def rasterize_fused(self, stream=None):
+    def rasterize_fused(self, stream=None, accumulate=False):
         gs_rasterize_fused(self.n, self.V, self.splats, self.W, self.H, self.vals, self.ranges,
                            self.bg, self.target, self.image, self.T_final, self.n_contrib,
                            self.loss, self.grads2d, stream, tile_order=self.tile_order,
-                           workspace=self.raster_ws, tile_counts=self.tile_counts)
+                           workspace=self.raster_ws, tile_counts=self.tile_counts,
+                           accumulate=accumulate)
+
+    def zero_grads(self, stream=None):
+        gs_zero_grads(self.n, self.V, self.grads2d, stream, tile_counts=self.tile_counts)
 
     def project_bwd(self, stream=None):
         gs_project_bwd(self.params, self.cams, self.splats, self.grads2d, self.grad, self.visible,
@@ -554,6 +571,7 @@ class TrainStep:
             self._alloc_isect(need)
         self.step_dev = torch.full((1,), self.t, dtype=torch.int64, device=dev)
         self.n_isect_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+        self._side = torch.cuda.Stream(device=dev)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -562,12 +580,19 @@ class TrainStep:
 
     def _graph_body(self):
         self.project()
+        main = torch.cuda.current_stream()
+        if self.fused:
+            # the gradient records are zeroed on a second stream while the lists
+            # are built: the zeroing needs only the tile counts
+            self._side.wait_stream(main)
+            self.zero_grads(self._side)
         gs_bin_and_sort_async(self.n, self.V, self.splats, self.W, self.H, self.workspace,
                               self.capacity, self.keys, self.vals, self.ranges, self.n_isect_dev,
                               tile_counts=self.tile_counts)
         gs_tile_order(self.ranges, self.tile_order)
         if self.fused:
-            self.rasterize_fused()
+            main.wait_stream(self._side)
+            self.rasterize_fused(accumulate=True)
         else:
             self.rasterize_fwd()
             self.loss_l1()

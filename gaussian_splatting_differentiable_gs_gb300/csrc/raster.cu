@@ -1036,34 +1036,45 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
 __global__ void __launch_bounds__(256) zero_visible_grads_kernel(int64_t rows,
                                                                  const int32_t* __restrict__ counts,
                                                                  float4* __restrict__ grads) {
-  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // rows 2q, 2q + 1
-  const int64_t r = 2 * q;
-  if (r >= rows) return;
-  bool any;
-  if (r + 1 < rows && ((reinterpret_cast<uintptr_t>(counts) & 7u) == 0)) {
-    const int2 c = __ldg(reinterpret_cast<const int2*>(counts) + q);
-    any = c.x > 0 || c.y > 0;
-  } else {
-    any = __ldg(counts + r) > 0 || (r + 1 < rows && __ldg(counts + r + 1) > 0);
-  }
-  if (!any) return;
-  const int nv = r + 1 < rows ? 6 : 3;
-  float4* g = grads + 3 * r;
+  const bool even = (reinterpret_cast<uintptr_t>(counts) & 7u) == 0;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  // rows 2q, 2q + 1; a grid smaller than the pairs strides over them
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; 2 * q < rows;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = 2 * q;
+    bool any;
+    if (r + 1 < rows && even) {
+      const int2 c = __ldg(reinterpret_cast<const int2*>(counts) + q);
+      any = c.x > 0 || c.y > 0;
+    } else {
+      any = __ldg(counts + r) > 0 || (r + 1 < rows && __ldg(counts + r + 1) > 0);
+    }
+    if (!any) continue;
+    const int nv = r + 1 < rows ? 6 : 3;
+    float4* g = grads + 3 * r;
 #pragma unroll
-  for (int v = 0; v < 6; ++v)
-    if (v < nv) g[v] = z;
+    for (int v = 0; v < 6; ++v)
+      if (v < nv) g[v] = z;
+  }
 }
 
 // The gradient records' zeroing before a backward: every row, or with tile
 // counts only the visible ones.
-gs_status zero_grads(int64_t rows, const int32_t* counts, gs_splat_grad* grads, cudaStream_t st) {
+constexpr int kZeroSideCtas = 2;
+
+// max_blocks > 0 caps the grid (the kernel then strides): a zeroing meant to
+// run beside other kernels takes a few CTAs per SM instead of filling the GPU
+// ahead of them.
+gs_status zero_grads(int64_t rows, const int32_t* counts, gs_splat_grad* grads, cudaStream_t st,
+                     int64_t max_blocks = 0) {
   if (rows <= 0) return GS_OK;
   if (!counts) {
     GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)rows, st));
     return GS_OK;
   }
-  zero_visible_grads_kernel<<<(unsigned)div_up(div_up(rows, 2), 256), 256, 0, st>>>(
+  int64_t blocks = div_up(div_up(rows, 2), 256);
+  if (max_blocks > 0 && blocks > max_blocks) blocks = max_blocks;
+  zero_visible_grads_kernel<<<(unsigned)blocks, 256, 0, st>>>(
       rows, counts, reinterpret_cast<float4*>(grads));
   GS_CHECK_LAUNCH();
   return GS_OK;
@@ -1150,13 +1161,15 @@ extern "C" size_t gs_rasterize_workspace_bytes(int32_t n_views, int32_t width, i
   return (size_t)slots * (kRT / 8 * kWords) * sizeof(uint32_t);
 }
 
-extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
-                                        const int32_t* tile_counts, int32_t width, int32_t height, const uint32_t* vals,
-                                        const int64_t* ranges, const uint32_t* tile_order,
-                                        const float* bg,
-                                        const float* target, float* image, float* T_final,
-                                        int32_t* n_contrib, float* loss, gs_splat_grad* grads,
-                                        void* workspace, size_t ws_bytes, void* stream) {
+// gs_rasterize_fused and gs_rasterize_fused_acc: the same launch, with or
+// without the zeroing of the gradient records in front of it.
+static gs_status rasterize_fused_impl(int64_t n, int32_t n_views, const gs_splat* splats,
+                                      const int32_t* tile_counts, int32_t width, int32_t height,
+                                      const uint32_t* vals, const int64_t* ranges,
+                                      const uint32_t* tile_order, const float* bg,
+                                      const float* target, float* image, float* T_final,
+                                      int32_t* n_contrib, float* loss, gs_splat_grad* grads,
+                                      void* workspace, size_t ws_bytes, bool zero, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS || width < 1 ||
       height < 1 || !bg || !ranges || !target || !image || !T_final || !n_contrib || !loss)
     return GS_ERR_INVALID_ARG;
@@ -1167,8 +1180,10 @@ extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_spl
   const int64_t rec_slots = workspace ? (int64_t)(ws_bytes / (kRT / 8 * kWords * sizeof(uint32_t))) : 0;
   cudaStream_t st = (cudaStream_t)stream;
   GS_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), st));
-  const gs_status zs = zero_grads(n * n_views, tile_counts, grads, st);
-  if (zs != GS_OK) return zs;
+  if (zero) {
+    const gs_status zs = zero_grads(n * n_views, tile_counts, grads, st);
+    if (zs != GS_OK) return zs;
+  }
   const int64_t T = tiles_per_view(width, height);
   const int32_t tiles_x = (width + GS_TILE - 1) / GS_TILE;
   const double count = 3.0 * (double)n_views * (double)width * (double)height;
@@ -1179,6 +1194,48 @@ extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_spl
       rec_slots);
   GS_CHECK_LAUNCH();
   return GS_OK;
+}
+
+extern "C" gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
+                                        const int32_t* tile_counts, int32_t width, int32_t height,
+                                        const uint32_t* vals, const int64_t* ranges,
+                                        const uint32_t* tile_order, const float* bg,
+                                        const float* target, float* image, float* T_final,
+                                        int32_t* n_contrib, float* loss, gs_splat_grad* grads,
+                                        void* workspace, size_t ws_bytes, void* stream) {
+  return rasterize_fused_impl(n, n_views, splats, tile_counts, width, height, vals, ranges,
+                              tile_order, bg, target, image, T_final, n_contrib, loss, grads,
+                              workspace, ws_bytes, true, stream);
+}
+
+extern "C" gs_status gs_rasterize_fused_acc(int64_t n, int32_t n_views, const gs_splat* splats,
+                                            const int32_t* tile_counts, int32_t width,
+                                            int32_t height, const uint32_t* vals,
+                                            const int64_t* ranges, const uint32_t* tile_order,
+                                            const float* bg, const float* target, float* image,
+                                            float* T_final, int32_t* n_contrib, float* loss,
+                                            gs_splat_grad* grads, void* workspace,
+                                            size_t ws_bytes, void* stream) {
+  return rasterize_fused_impl(n, n_views, splats, tile_counts, width, height, vals, ranges,
+                              tile_order, bg, target, image, T_final, n_contrib, loss, grads,
+                              workspace, ws_bytes, false, stream);
+}
+
+extern "C" gs_status gs_zero_grads(int64_t n, int32_t n_views, const int32_t* tile_counts,
+                                   gs_splat_grad* grads, void* stream) {
+  if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS)
+    return GS_ERR_INVALID_ARG;
+  if (n > 0 && (!grads || !aligned16(grads))) return GS_ERR_INVALID_ARG;
+  if (!aligned4(tile_counts)) return GS_ERR_INVALID_ARG;
+  if (n == 0) return GS_OK;
+  // a small grid (kZeroSideCtas CTAs per SM, striding): this call is meant
+  // to run on a second stream beside the binning, which a grid of one thread
+  // per pair of rows would hold back until it drained
+  int dev = 0, sms = 0;
+  GS_CUDA(cudaGetDevice(&dev));
+  GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  return zero_grads(n * n_views, tile_counts, grads, (cudaStream_t)stream,
+                    (int64_t)kZeroSideCtas * (sms > 0 ? sms : 1));
 }
 
 extern "C" gs_status gs_rasterize_bwd(int64_t n, int32_t n_views, const gs_splat* splats,

@@ -7,8 +7,10 @@
  *   gs_loss_l1 -> gs_rasterize_bwd -> gs_project_bwd -> gs_adam_step
  * where gs_rasterize_fused may replace the three calls from gs_rasterize_fwd
  * to gs_rasterize_bwd, and gs_tile_order is optional (it only sets the order
- * in which the compositing CTAs start).  Forward-only rendering is the calls
- * up to gs_rasterize_fwd.
+ * in which the compositing CTAs start).  The fused call's zeroing of the
+ * gradient records can be split off (gs_zero_grads on a second stream after
+ * gs_project, then gs_rasterize_fused_acc), so that it runs beside the
+ * binning.  Forward-only rendering is the calls up to gs_rasterize_fwd.
  *
  * Source pages (title, section) for what the step computes:
  *  [S1] "On Scaling Up 3D Gaussian Splatting Training": answer on the storage
@@ -344,6 +346,30 @@ gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
                              float* image, float* T_final, int32_t* n_contrib, float* loss,
                              gs_splat_grad* grads, void* workspace, size_t ws_bytes,
                              void* stream);
+
+/* gs_zero_grads -- the zeroing that gs_rasterize_bwd and gs_rasterize_fused
+ * start with, as a call of its own: all n_views * n gradient records without
+ * tile_counts; with tile_counts, the records of the pairs of rows (2k, 2k+1)
+ * of which one at least has a positive count.  It reads nothing but the tile
+ * counts, so it can run on a second stream while gs_bin_and_sort builds the
+ * lists; gs_rasterize_fused_acc then adds the gradients.
+ *   tile_counts  [n_views * n] from gs_project, or NULL
+ *   grads        [n_views * n] output (16-byte aligned)
+ * GS_ERR_INVALID_ARG unless 0 <= n < 2^32 and 1 <= n_views <= GS_MAX_VIEWS. */
+gs_status gs_zero_grads(int64_t n, int32_t n_views, const int32_t* tile_counts,
+                        gs_splat_grad* grads, void* stream);
+
+/* gs_rasterize_fused_acc -- gs_rasterize_fused without its zeroing: the
+ * gradients are added to `grads` as it stands, which gs_zero_grads (same
+ * tile_counts) has zeroed before.  Arguments, checks and every other result
+ * as gs_rasterize_fused. */
+gs_status gs_rasterize_fused_acc(int64_t n, int32_t n_views, const gs_splat* splats,
+                                 const int32_t* tile_counts, int32_t width, int32_t height,
+                                 const uint32_t* vals, const int64_t* ranges,
+                                 const uint32_t* tile_order, const float* bg, const float* target,
+                                 float* image, float* T_final, int32_t* n_contrib, float* loss,
+                                 gs_splat_grad* grads, void* workspace, size_t ws_bytes,
+                                 void* stream);
 
 /* gs_project_bwd -- chain rule from the per-row gradients back to the 59
  * parameters, summed over the views (the 1/n_views average of [S1] comes

@@ -790,3 +790,54 @@ def test_bin_and_sort_device_check_on_inconsistent_record():
     gs.gs_bin_and_sort_async(n, V, _cuda(good), W, H, ws, cap, keys, vals, ranges, nd)
     assert gs.gs_workspace_status(ws) == gs.GS_OK
     assert int(nd.item()) == o["keys"].size
+
+
+@pytest.mark.parametrize("case", ["ragged2", "small"])
+def test_zero_grads_then_fused_acc_equals_fused(case):
+    """gs_zero_grads on a second stream (ordered by events) followed by
+    gs_rasterize_fused_acc gives what gs_rasterize_fused gives, with and
+    without tile counts; the accumulate-only call adds to what it finds."""
+    gs = _gs()
+    o = oracle_side(case)
+    n, V, W, H = o["n"], o["V"], o["W"], o["H"]
+    splats, vals, ranges, _, _, _ = _gpu_fwd(gs, o)
+    target = _cuda(o["target"])
+    counts = torch.from_numpy(pack_records(o["pr"]).view(np.int32)[:, 11].copy()).cuda()
+    ws = torch.empty(gs.gs_rasterize_workspace_bytes(V, W, H, int(o["vals"].size)),
+                     dtype=torch.uint8, device="cuda")
+    for tc in (None, counts):
+        outs = []
+        for split in (False, True):
+            image = torch.empty((V, 3, H, W), device="cuda")
+            T_final = torch.empty((V, H, W), device="cuda")
+            n_contrib = torch.empty((V, H, W), dtype=torch.int32, device="cuda")
+            loss = torch.empty(1, device="cuda")
+            grads = torch.full((n * V, 12), 5.0, device="cuda")
+            if split:
+                main = torch.cuda.current_stream()
+                side = torch.cuda.Stream()
+                side.wait_stream(main)
+                gs.gs_zero_grads(n, V, grads, side, tile_counts=tc)
+                main.wait_stream(side)
+                gs.gs_rasterize_fused(n, V, splats, W, H, vals, ranges, (0, 0, 0), target, image,
+                                      T_final, n_contrib, loss, grads, workspace=ws,
+                                      tile_counts=tc, accumulate=True)
+            else:
+                gs.gs_rasterize_fused(n, V, splats, W, H, vals, ranges, (0, 0, 0), target, image,
+                                      T_final, n_contrib, loss, grads, workspace=ws,
+                                      tile_counts=tc)
+            torch.cuda.synchronize()
+            outs.append((image, T_final, n_contrib, loss, grads))
+        (i0, t0, c0, l0, g0), (i1, t1, c1, l1, g1) = outs
+        assert torch.equal(i0, i1) and torch.equal(t0, t1) and torch.equal(c0, c1)
+        assert l1.item() == pytest.approx(l0.item(), rel=1e-6)
+        vis = torch.ones(n * V, dtype=torch.bool, device="cuda") if tc is None else tc > 0
+        assert rel_l2(g1[vis].cpu().numpy(), g0[vis].cpu().numpy()) <= 1e-6
+    # without a zeroing first the call adds to the records as they stand
+    grads = torch.zeros((n * V, 12), device="cuda")
+    gs.gs_rasterize_fused(n, V, splats, W, H, vals, ranges, (0, 0, 0), target, image, T_final,
+                          n_contrib, loss, grads, workspace=ws)
+    twice = grads.clone()
+    gs.gs_rasterize_fused(n, V, splats, W, H, vals, ranges, (0, 0, 0), target, image, T_final,
+                          n_contrib, loss, twice, workspace=ws, accumulate=True)
+    assert rel_l2(twice.cpu().numpy(), 2 * grads.cpu().numpy()) <= 1e-6

@@ -16,10 +16,12 @@
 //      partition's global digit offsets by decoupled look-back and scatters
 //      ("onesweep"; radix sorting per Merrill & Grimshaw, same reference
 //      list); an element is one 64-bit word, sort digits in the high half,
-//      the row's compact index in the low half;
+//      the row index (view * n + g) in the low half;
 //   3. emission of each row's tiles in depth order (a second look-back scan
 //      gives the offsets; a partition's outputs are spread evenly over its
-//      threads), with the digit histograms of the tile passes;
+//      threads), with the digit histograms of the tile passes; an
+//      intersection carries its row's position in depth order, whose
+//      (depth, Gaussian id) word the emission also writes, in depth order;
 //   4. the same radix passes on the tile index (ceil(tile bits / 8) passes);
 //      the last one writes the final (tile << 32 | depth) keys and ids;
 //   5. tile ranges, marked by the last tile pass.
@@ -97,13 +99,16 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 static_assert(offsetof(WsHeader, error) == kWsStatusOffset, "status word offset");
 static_assert(offsetof(WsHeader, rows) == 16, "counts in the first 24 bytes");
 
-// Workspace layout.  Per visible row (compact index c < R): row_u[c] =
-// depth bits << 32 | Gaussian id (row mod n), row_rect[c] = first flat tile | width << 32 |
-// height << 48 of its tile rectangle.  tmp: one capacity-sized key buffer;
-// the row sort ping-pongs between it and the caller's key buffer (R <= I <=
-// capacity), as do the tile passes.
+// Workspace layout.  row_rect[r] (r = view * n + g, written for the visible
+// rows only) = first flat tile | width << 32 | height << 48 of the row's tile
+// rectangle; row_d[s] (s < R: the row's position in depth order) = depth bits
+// << 32 | Gaussian id, written at emission and gathered by the last tile pass
+// (an intersection carries s, so the gathers of a partition, which is in
+// depth order within each tile digit, fall in a narrow window of row_d).
+// tmp: one capacity-sized key buffer; the row sort ping-pongs between it and
+// the caller's key buffer (R <= I <= capacity), as do the tile passes.
 struct WsLayout {
-  size_t hist, digit_start, scan_status, emit_status, sort_status, row_u, row_rect, erow, chunk_row,
+  size_t hist, digit_start, scan_status, emit_status, sort_status, row_d, row_rect, erow, chunk_row,
       tmp, total;
 };
 
@@ -120,7 +125,7 @@ inline WsLayout ws_layout(int64_t n_rows, int64_t capacity) {
   L.scan_status = off; off += align256(sizeof(uint64_t) * (size_t)div_up(r, kCompChunk));
   L.emit_status = off; off += align256(sizeof(uint64_t) * (size_t)div_up(r, kEmitPart));
   L.sort_status = off; off += align256(sizeof(uint64_t) * kRadix * (size_t)sort_parts);
-  L.row_u = off;       off += align256(sizeof(uint64_t) * (size_t)r);
+  L.row_d = off;       off += align256(sizeof(uint64_t) * (size_t)r);
   L.row_rect = off;    off += align256(sizeof(uint64_t) * (size_t)r);
   L.erow = off;        off += align256(sizeof(uint4) * (size_t)r);
   L.chunk_row = off;   off += align256(sizeof(uint32_t) * (size_t)(div_up(c, kEmitChunk) + 1));
@@ -198,8 +203,8 @@ __device__ long long lookback_prefix_warp(uint64_t* status, int64_t part, long l
 
 // ---------------------------------------------------------------------------
 // 1. Compaction of the visible rows (tile count > 0), in row order.  Per
-//    visible row at compact index c: the depth-sort element (depth bits << 32
-//    | c) into sort_in (when c < capacity), row_u[c] and row_rect[c]; the
+//    visible row r at compact index c: the depth-sort element (depth bits <<
+//    32 | r) into sort_in[c] (when c < capacity) and row_rect[r]; the
 //    intersection total I into the header (block sums added atomically) and
 //    R by the last partition; the depth-digit histograms.  Positive depths
 //    order as their bit patterns.  The visible rows are found from the tile
@@ -222,7 +227,7 @@ __global__ void __launch_bounds__(kCompThreads, 4) compact_rows_kernel(
     int64_t n_rows, int64_t n, int32_t tiles_x, int32_t tiles_y, int64_t T, int64_t capacity,
     const float4* __restrict__ splats, const int32_t* __restrict__ counts,
     uint64_t* __restrict__ sort_in,
-    uint64_t* __restrict__ row_u, uint64_t* __restrict__ row_rect, uint32_t* __restrict__ hist,
+    uint64_t* __restrict__ row_rect, uint32_t* __restrict__ hist,
     uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
   __shared__ uint32_t sh[kDepthPasses * kRadix];
   __shared__ uint32_t s_warp[kCompChunks][kCompWarps];
@@ -295,11 +300,12 @@ __global__ void __launch_bounds__(kCompThreads, 4) compact_rows_kernel(
         cnt[i] = row_count(cbase + 32 * i + lane, n_rows, splats, counts);
         nvis += __popc(__ballot_sync(0xffffffffu, cnt[i] > 0));
       }
-      // one visible row: its rectangle checked against its count, its three
-      // words written at compact index ci, its depth digits counted
+      // one visible row: its rectangle checked against its count, its sort
+      // element written at compact index ci and its rectangle at r, its depth
+      // digits counted
       auto emit_row = [&](uint32_t r, int32_t cq, float2 mean, float dep, int32_t rad,
                           int64_t ci) {
-        const uint32_t view = r / (uint32_t)n, g = r - view * (uint32_t)n;  // rows < 2^32
+        const uint32_t view = r / (uint32_t)n;  // rows < 2^32
         int32_t x0, x1, y0, y1;
         tile_rect(mean.x, mean.y, rad, tiles_x, tiles_y, x0, x1, y0, y1);
         uint64_t rect = 0;
@@ -311,9 +317,8 @@ __global__ void __launch_bounds__(kCompThreads, 4) compact_rows_kernel(
           atomicOr(&hdr->error, 2u);
         }
         const uint32_t dbits = __float_as_uint(dep);
-        if (ci < capacity) sort_in[ci] = ((uint64_t)dbits << 32) | (uint64_t)ci;
-        row_u[ci] = ((uint64_t)dbits << 32) | (uint64_t)g;
-        row_rect[ci] = rect;
+        if (ci < capacity) sort_in[ci] = ((uint64_t)dbits << 32) | (uint64_t)r;
+        row_rect[r] = rect;
 #pragma unroll
         for (int p = 0; p < kDepthPasses; ++p)
           atomicAdd(&sh[p * kRadix + ((dbits >> (8 * p)) & 0xFF)], 1u);
@@ -460,8 +465,9 @@ __device__ __forceinline__ bool digit_lookback(const uint64_t* status, int64_t p
 // 2, 4. One stable radix pass over 64-bit keys on the 8 bits at `shift`
 //    (onesweep).  Sort status word: value << 8 | tag << 2 | flag, tag =
 //    pass + 1 (stale entries of an earlier pass read as not ready).  kFinal:
-//    the last tile pass, which writes key (tile << 32 | depth bits) and id
-//    (row mod n) of the element's row c (its low 32 bits) instead, and marks
+//    the last tile pass, which writes key (tile << 32 | depth bits) and the
+//    Gaussian id of the element's row, read from row_d at the row's depth
+//    position s (the element's low 32 bits), instead, and marks
 //    the tile ranges: a partition's keys, placed in shared memory, are in
 //    full tile order (its input is ordered by the lower tile digits), so each
 //    run of one tile in it is contiguous in the output; its ends go into
@@ -482,7 +488,7 @@ template <bool kFinal>
 __global__ void __launch_bounds__(kPassThreads, kPassMinBlocks) onesweep64_kernel(
     int64_t count, int32_t pass, int32_t shift, const uint64_t* __restrict__ keys_in,
     uint64_t* __restrict__ keys_out, const uint32_t* __restrict__ digit_start,
-    uint64_t* __restrict__ status, WsHeader* __restrict__ hdr, const uint64_t* __restrict__ row_u,
+    uint64_t* __restrict__ status, WsHeader* __restrict__ hdr, const uint64_t* __restrict__ row_d,
     uint32_t* __restrict__ vals_out, uint32_t n, unsigned long long* __restrict__ ranges) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SortSmem64& S = *reinterpret_cast<SortSmem64*>(smem_raw);
@@ -603,7 +609,7 @@ __global__ void __launch_bounds__(kPassThreads, kPassMinBlocks) onesweep64_kerne
     const unsigned long long gpos = S.global_base[dd] + (unsigned long long)j;
     if (gpos < (unsigned long long)count) {
       if constexpr (kFinal) {
-        const uint64_t u = __ldg(row_u + (uint32_t)k);  // depth bits, Gaussian id
+        const uint64_t u = __ldg(row_d + (uint32_t)k);  // depth bits, Gaussian id
         keys_out[gpos] = (k & 0xFFFFFFFF00000000ull) | (u >> 32);
         vals_out[gpos] = (uint32_t)u;
         const uint32_t f = (uint32_t)(k >> 32);
@@ -624,16 +630,18 @@ __global__ void __launch_bounds__(kPassThreads, kPassMinBlocks) onesweep64_kerne
 //    partitions gives its output offset), then its threads write the
 //    partition's intersections at consecutive positions, each finding its
 //    row by binary search over the partition's inclusive counts: element
-//    (flat tile << 32 | c), tiles of a row in raster order.  Also the digit
-//    histograms of the tile passes.  count < 0: R from the header.
+//    (flat tile << 32 | s), s the row's position in depth order, tiles of a
+//    row in raster order; and row_d[s].  Also the digit histograms of the
+//    tile passes.  count < 0: R from the header.
 __global__ void __launch_bounds__(kEmitThreads) emit_sorted_kernel(
-    int64_t count, int32_t tiles_x, int32_t tile_passes, const uint64_t* __restrict__ sorted,
-    const uint64_t* __restrict__ row_rect, uint64_t* __restrict__ out, uint32_t* __restrict__ hist,
+    int64_t count, int32_t tiles_x, int32_t tile_passes, uint32_t n,
+    const uint64_t* __restrict__ sorted, const uint64_t* __restrict__ row_rect,
+    uint64_t* __restrict__ row_d, uint64_t* __restrict__ out, uint32_t* __restrict__ hist,
     uint64_t* __restrict__ status, WsHeader* __restrict__ hdr) {
   __shared__ uint32_t s_incl[kEmitPart];   // inclusive tile counts, partition-local
   __shared__ uint32_t s_first[kEmitPart];  // first flat tile of the row's rectangle
   __shared__ uint32_t s_w[kEmitPart];      // rectangle width
-  __shared__ uint32_t s_c[kEmitPart];      // compact row index
+  __shared__ uint32_t s_c[kEmitPart];      // the row's position in depth order
   __shared__ uint32_t sh[4 * kRadix];
   __shared__ uint32_t s_warp[kEmitThreads / 32];
   __shared__ long long s_count, s_prefix;
@@ -653,13 +661,15 @@ __global__ void __launch_bounds__(kEmitThreads) emit_sorted_kernel(
   for (int e = tid; e < kEmitPart; e += kEmitThreads) {
     uint32_t t = 0;
     if (e < n_here) {
-      const uint32_t c = (uint32_t)sorted[pbase + e];
-      const uint64_t rc = __ldg(row_rect + c);
+      const uint64_t u = sorted[pbase + e];  // depth bits << 32 | row
+      const uint32_t r = (uint32_t)u;
+      const uint64_t rc = __ldg(row_rect + r);
       const uint32_t w = (uint32_t)(rc >> 32) & 0xFFFFu, h = (uint32_t)(rc >> 48);
       t = w * h;
       s_first[e] = (uint32_t)rc;
       s_w[e] = w;
-      s_c[e] = c;
+      s_c[e] = (uint32_t)(pbase + e);  // R < 2^32
+      row_d[pbase + e] = (u & 0xFFFFFFFF00000000ull) | (uint64_t)(r % n);
     }
     s_incl[e] = t;
   }
@@ -719,7 +729,7 @@ __global__ void __launch_bounds__(kEmitThreads) emit_sorted_kernel(
 // 3 (balanced form).  Two kernels.  row_scan_kernel scans the sorted rows'
 //    tile counts (partitions of kEmitPart rows, decoupled look-back as
 //    above) into each row's first output position and writes per sorted row
-//    erow = (position, first flat tile, width | height << 16, compact index)
+//    s erow = (position, first flat tile, width | height << 16, s) and row_d[s]
 //    and, for every chunk of kEmitChunk outputs that starts inside the row,
 //    chunk_row[chunk] = the row.  emit_chunks_kernel then gives every CTA
 //    one chunk of outputs -- the same number whatever the rows' sizes, where
@@ -729,8 +739,9 @@ __global__ void __launch_bounds__(kEmitThreads) emit_sorted_kernel(
 //    of its width, corrected to the exact quotient.  Same outputs, bit for
 //    bit, as emit_sorted_kernel.
 __global__ void __launch_bounds__(kEmitThreads) row_scan_kernel(
-    int64_t count, int32_t tiles_x, int32_t tile_passes, const uint64_t* __restrict__ sorted,
-    const uint64_t* __restrict__ row_rect, uint4* __restrict__ erow,
+    int64_t count, int32_t tiles_x, int32_t tile_passes, uint32_t n,
+    const uint64_t* __restrict__ sorted, const uint64_t* __restrict__ row_rect,
+    uint64_t* __restrict__ row_d, uint4* __restrict__ erow,
     uint32_t* __restrict__ chunk_row, uint32_t* __restrict__ hist, uint64_t* __restrict__ status,
     WsHeader* __restrict__ hdr) {
   __shared__ uint32_t s_warp[kEmitThreads / 32];
@@ -764,8 +775,11 @@ __global__ void __launch_bounds__(kEmitThreads) row_scan_kernel(
     const int64_t e = pbase + tid * kEmitItems + k;
     t[k] = 0;
     if (e < R) {
-      c[k] = (uint32_t)sorted[e];
-      const uint64_t rc = __ldg(row_rect + c[k]);
+      const uint64_t u = sorted[e];  // depth bits << 32 | row
+      const uint32_t r = (uint32_t)u;
+      c[k] = (uint32_t)e;  // R < 2^32
+      row_d[e] = (u & 0xFFFFFFFF00000000ull) | (uint64_t)(r % n);
+      const uint64_t rc = __ldg(row_rect + r);
       const uint32_t w = (uint32_t)(rc >> 32) & 0xFFFFu, h = (uint32_t)(rc >> 48);
       first[k] = (uint32_t)rc;
       wh[k] = w | (h << 16);
@@ -1199,7 +1213,7 @@ int bit_length(uint64_t v) {
 struct BinBufs {
   WsHeader* hdr;
   uint32_t *hist, *digit_start;
-  uint64_t *scan_status, *emit_status, *sort_status, *row_u, *row_rect, *tmp;
+  uint64_t *scan_status, *emit_status, *sort_status, *row_d, *row_rect, *tmp;
   uint4* erow;
   uint32_t* chunk_row;
 };
@@ -1215,7 +1229,7 @@ BinBufs bin_bufs(void* workspace, const WsLayout& L) {
   b.erow = reinterpret_cast<uint4*>(ws + L.erow);
   b.chunk_row = reinterpret_cast<uint32_t*>(ws + L.chunk_row);
   b.sort_status = reinterpret_cast<uint64_t*>(ws + L.sort_status);
-  b.row_u = reinterpret_cast<uint64_t*>(ws + L.row_u);
+  b.row_d = reinterpret_cast<uint64_t*>(ws + L.row_d);
   b.row_rect = reinterpret_cast<uint64_t*>(ws + L.row_rect);
   b.tmp = reinterpret_cast<uint64_t*>(ws + L.tmp);
   return b;
@@ -1264,7 +1278,7 @@ gs_status launch_compaction(const BinShape& s, const BinBufs& b, const gs_splat*
                             : (chunks == 4 ? compact_rows_kernel<4> : compact_rows_kernel<8>);
   kernel<<<(unsigned)parts, kCompThreads, 0, st>>>(
       s.n_rows, s.n, s.tiles_x, s.tiles_y, s.T, capacity, reinterpret_cast<const float4*>(splats),
-      counts, rows_buffer(s, b, keys), b.row_u, b.row_rect, b.hist, b.scan_status, b.hdr);
+      counts, rows_buffer(s, b, keys), b.row_rect, b.hist, b.scan_status, b.hdr);
   GS_CHECK_LAUNCH();
   return GS_OK;
 }
@@ -1298,14 +1312,16 @@ gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, 
   GS_CUDA(cudaMemsetAsync(b.emit_status, 0, sizeof(uint64_t) * (size_t)eparts, st));
   if (isect_max >= kEmitChunkMinTiles * rows_max) {
     row_scan_kernel<<<(unsigned)eparts, kEmitThreads, 0, st>>>(
-        rows, s.tiles_x, s.tile_passes, ra, b.row_rect, b.erow, b.chunk_row, b.hist,
+        rows, s.tiles_x, s.tile_passes, (uint32_t)s.n, ra, b.row_rect, b.row_d, b.erow,
+        b.chunk_row, b.hist,
         b.emit_status, b.hdr);
     GS_CHECK_LAUNCH();
     emit_chunks_kernel<<<(unsigned)div_up(isect_max, kEmitChunk), kEmitThreads, 0, st>>>(
         s.tiles_x, b.erow, b.chunk_row, rb, b.hdr);
   } else {
     emit_sorted_kernel<<<(unsigned)eparts, kEmitThreads, 0, st>>>(
-        rows, s.tiles_x, s.tile_passes, ra, b.row_rect, rb, b.hist, b.emit_status, b.hdr);
+        rows, s.tiles_x, s.tile_passes, (uint32_t)s.n, ra, b.row_rect, b.row_d, rb, b.hist,
+        b.emit_status, b.hdr);
   }
   GS_CHECK_LAUNCH();
   hist_scan_kernel<<<s.tile_passes, kRadix, 0, st>>>(b.hist + kDepthPasses * kRadix,
@@ -1316,7 +1332,7 @@ gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, 
     const int p = kDepthPasses + q;
     if (q == s.tile_passes - 1) {
       onesweep64_kernel<true><<<(unsigned)parts_i, kPassThreads, smem, st>>>(
-          isect, p, 32 + 8 * q, in, keys, b.digit_start, b.sort_status, b.hdr, b.row_u, vals,
+          isect, p, 32 + 8 * q, in, keys, b.digit_start, b.sort_status, b.hdr, b.row_d, vals,
           (uint32_t)s.n, reinterpret_cast<unsigned long long*>(ranges));
     } else {
       out = in == keys ? b.tmp : keys;
@@ -1363,7 +1379,7 @@ extern "C" gs_status gs_selftest_lookback_timeout(void* workspace, size_t ws_byt
   const unsigned one = 1;
   GS_CUDA(cudaMemcpyAsync(&b.hdr->scan_ticket, &one, sizeof(one), cudaMemcpyHostToDevice, st));
   compact_rows_kernel<4><<<1, kCompThreads, 0, st>>>(0, 1, 1, 1, 1, 1, nullptr, nullptr, b.tmp,
-                                                     b.row_u, b.row_rect, b.hist, b.scan_status,
+                                                     b.row_rect, b.hist, b.scan_status,
                                                      b.hdr);
   GS_CHECK_LAUNCH();
   return gs_workspace_status(workspace, stream);

@@ -473,6 +473,12 @@ __device__ __forceinline__ bool digit_lookback(const uint64_t* status, int64_t p
 //    run of one tile in it is contiguous in the output; its ends go into
 //    ranges by atomic maxima (the start as count - position), decoded by
 //    ranges_fix_kernel.
+//    kMode: 0 a pass, 1 the last tile pass (above), 2 the first tile pass of
+//    the balanced emission, which makes its partition's elements instead of
+//    loading them: element t (in depth order) lies in the last row whose
+//    first output position (erow) is <= t, found by binary search among the
+//    rows of t's emission chunk (chunk_row), so the emitted list never passes
+//    through memory.  Same elements as emit_chunks_kernel.
 struct SortSmem64 {
   uint32_t warp_hist[kPassWarps][kRadix];
   uint32_t local_start[kRadix];
@@ -481,15 +487,18 @@ struct SortSmem64 {
   int part;
   int err;
   long long count;
+  long long rows;
   uint64_t keys[kSortPart];
 };
 
-template <bool kFinal>
+template <int kMode>
 __global__ void __launch_bounds__(kPassThreads, kPassMinBlocks) onesweep64_kernel(
     int64_t count, int32_t pass, int32_t shift, const uint64_t* __restrict__ keys_in,
     uint64_t* __restrict__ keys_out, const uint32_t* __restrict__ digit_start,
     uint64_t* __restrict__ status, WsHeader* __restrict__ hdr, const uint64_t* __restrict__ row_d,
-    uint32_t* __restrict__ vals_out, uint32_t n, unsigned long long* __restrict__ ranges) {
+    uint32_t* __restrict__ vals_out, uint32_t n, unsigned long long* __restrict__ ranges,
+    const uint4* __restrict__ erow, const uint32_t* __restrict__ chunk_row, int32_t tiles_x) {
+  constexpr bool kFinal = kMode == 1;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SortSmem64& S = *reinterpret_cast<SortSmem64*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -506,6 +515,7 @@ __global__ void __launch_bounds__(kPassThreads, kPassMinBlocks) onesweep64_kerne
     if (count < 0)
       S.count = (hdr->error & kErrStop) ? -1
                                         : (long long)(count == -1 ? hdr->total : hdr->rows);
+    if (kMode == 2) S.rows = (long long)hdr->rows;
   }
   __syncthreads();
   if (count < 0) {
@@ -516,14 +526,52 @@ __global__ void __launch_bounds__(kPassThreads, kPassMinBlocks) onesweep64_kerne
   const int64_t pbase = part * kSortPart;
   if (pbase >= count) return;
   const int n_here = count - pbase < kSortPart ? (int)(count - pbase) : kSortPart;
-  const uint64_t* src = keys_in + pbase;
   const int wbase = warp * 32 * kPassKpt;
-  // load (warp-striped: item i of lane l is element wbase + 32 i + l) and rank
+  // load or make (warp-striped: item i of lane l is element wbase + 32 i + l) and rank
   uint64_t key[kPassKpt];
+  if constexpr (kMode == 2) {
+    // a warp's 256 elements lie in one emission chunk (kEmitChunk is a
+    // multiple of 256 and of no partition boundary's offset); the rows of
+    // chunk q are chunk_row[q] .. chunk_row[q + 1] (the last one: R - 1)
+    static_assert(kEmitChunk % (32 * kPassKpt) == 0 && kSortPart % kEmitChunk == 0, "chunks");
+    const int64_t q = (pbase + wbase) / kEmitChunk;
+    const bool any = pbase + wbase < count;  // else no element of the warp is real
+    int a0 = any ? (int)chunk_row[q] : 0;
+    const int b0 = !any ? 0 : ((q + 1) * kEmitChunk < count ? (int)chunk_row[q + 1]
+                                                            : (int)(S.rows - 1));
 #pragma unroll
-  for (int i = 0; i < kPassKpt; ++i) {
-    const int li = wbase + 32 * i + lane;
-    key[i] = li < n_here ? src[li] : 0ull;
+    for (int i = 0; i < kPassKpt; ++i) {
+      const int li = wbase + 32 * i + lane;
+      key[i] = 0ull;
+      if (li < n_here) {
+        const uint32_t t = (uint32_t)(pbase + li);  // I < 2^32
+        int a = a0, b = b0;  // the last row whose first position is <= t
+        while (a < b) {
+          const int mid = (a + b + 1) >> 1;
+          if (__ldg(&erow[mid].x) <= t) a = mid; else b = mid - 1;
+        }
+        a0 = a;  // a lane's elements ascend
+        const uint4 r = __ldg(erow + a);
+        const uint32_t i2 = t - r.x, w = r.z & 0xFFFFu;
+        uint32_t ty;
+        if (i2 < (1u << 24)) {  // exact in fp32: the reciprocal's quotient is off by at most one
+          ty = __float2uint_rz(__fmul_rn((float)i2, __frcp_rn((float)w)));
+          if (ty * w > i2) --ty;
+          else if ((ty + 1) * w <= i2) ++ty;
+        } else {
+          ty = i2 / w;
+        }
+        const uint32_t flat = r.y + ty * (uint32_t)tiles_x + (i2 - ty * w);
+        key[i] = ((uint64_t)flat << 32) | (uint64_t)r.w;
+      }
+    }
+  } else {
+    const uint64_t* src = keys_in + pbase;
+#pragma unroll
+    for (int i = 0; i < kPassKpt; ++i) {
+      const int li = wbase + 32 * i + lane;
+      key[i] = li < n_here ? src[li] : 0ull;
+    }
   }
   const uint32_t lt_mask = (1u << lane) - 1u;
   // rank of each key among the warp's keys of its digit (< 32 kPassKpt <=
@@ -1193,10 +1241,13 @@ cudaError_t ensure_sort_attr() {
   e = cudaFuncSetAttribute(onesweep_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sizeof(SortSmemKV));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(onesweep64_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(onesweep64_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(SortSmem64));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(onesweep64_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(onesweep64_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(SortSmem64));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(onesweep64_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(SortSmem64));
 
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
@@ -1301,23 +1352,28 @@ gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, 
   uint64_t* in = ra;
   uint64_t* out = rb;
   for (int p = 0; p < kDepthPasses; ++p) {
-    onesweep64_kernel<false><<<(unsigned)parts_r, kPassThreads, smem, st>>>(
+    onesweep64_kernel<0><<<(unsigned)parts_r, kPassThreads, smem, st>>>(
         rows, p, 32 + 8 * p, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u,
-        nullptr);
+        nullptr, nullptr, nullptr, 0);
     GS_CHECK_LAUNCH();
     uint64_t* t = in; in = out; out = t;
   }
   // the sorted rows are back in ra
   const int64_t eparts = div_up(rows_max, kEmitPart);
   GS_CUDA(cudaMemsetAsync(b.emit_status, 0, sizeof(uint64_t) * (size_t)eparts, st));
-  if (isect_max >= kEmitChunkMinTiles * rows_max) {
+  // the balanced emission; with two tile passes or more its list is made
+  // by the first tile pass itself (onesweep64_kernel<2>) instead
+  const bool chunked = isect_max >= kEmitChunkMinTiles * rows_max;
+  const bool generate = chunked && s.tile_passes > 1;
+  if (chunked) {
     row_scan_kernel<<<(unsigned)eparts, kEmitThreads, 0, st>>>(
         rows, s.tiles_x, s.tile_passes, (uint32_t)s.n, ra, b.row_rect, b.row_d, b.erow,
         b.chunk_row, b.hist,
         b.emit_status, b.hdr);
     GS_CHECK_LAUNCH();
-    emit_chunks_kernel<<<(unsigned)div_up(isect_max, kEmitChunk), kEmitThreads, 0, st>>>(
-        s.tiles_x, b.erow, b.chunk_row, rb, b.hdr);
+    if (!generate)
+      emit_chunks_kernel<<<(unsigned)div_up(isect_max, kEmitChunk), kEmitThreads, 0, st>>>(
+          s.tiles_x, b.erow, b.chunk_row, rb, b.hdr);
   } else {
     emit_sorted_kernel<<<(unsigned)eparts, kEmitThreads, 0, st>>>(
         rows, s.tiles_x, s.tile_passes, (uint32_t)s.n, ra, b.row_rect, b.row_d, rb, b.hist,
@@ -1331,14 +1387,20 @@ gs_status launch_sort_stages(const BinShape& s, const BinBufs& b, int64_t rows, 
   for (int q = 0; q < s.tile_passes; ++q) {
     const int p = kDepthPasses + q;
     if (q == s.tile_passes - 1) {
-      onesweep64_kernel<true><<<(unsigned)parts_i, kPassThreads, smem, st>>>(
+      onesweep64_kernel<1><<<(unsigned)parts_i, kPassThreads, smem, st>>>(
           isect, p, 32 + 8 * q, in, keys, b.digit_start, b.sort_status, b.hdr, b.row_d, vals,
-          (uint32_t)s.n, reinterpret_cast<unsigned long long*>(ranges));
+          (uint32_t)s.n, reinterpret_cast<unsigned long long*>(ranges), nullptr, nullptr, 0);
+    } else if (q == 0 && generate) {
+      out = in == keys ? b.tmp : keys;
+      onesweep64_kernel<2><<<(unsigned)parts_i, kPassThreads, smem, st>>>(
+          isect, p, 32, nullptr, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u,
+          nullptr, b.erow, b.chunk_row, s.tiles_x);
+      in = out;
     } else {
       out = in == keys ? b.tmp : keys;
-      onesweep64_kernel<false><<<(unsigned)parts_i, kPassThreads, smem, st>>>(
+      onesweep64_kernel<0><<<(unsigned)parts_i, kPassThreads, smem, st>>>(
           isect, p, 32 + 8 * q, in, out, b.digit_start, b.sort_status, b.hdr, nullptr, nullptr, 0u,
-          nullptr);
+          nullptr, nullptr, nullptr, 0);
       in = out;
     }
     GS_CHECK_LAUNCH();

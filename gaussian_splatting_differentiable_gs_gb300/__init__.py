@@ -80,7 +80,7 @@ def lib():
     L.gs_rasterize_fused.argtypes = [i64, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                      vp, vp, vp, sz, vp]
     L.gs_rasterize_fused_acc.argtypes = L.gs_rasterize_fused.argtypes
-    L.gs_zero_grads.argtypes = [i64, i32, vp, vp, vp]
+    L.gs_zero_grads.argtypes = [i64, i32, vp, vp, i32, vp]
     L.gs_rasterize_workspace_bytes.argtypes = [i32, i32, i32, i64]
     L.gs_rasterize_workspace_bytes.restype = sz
     L.gs_project_bwd.argtypes = [i64, vp, vp, i32, vp, vp, vp, vp, vp, vp]
@@ -295,12 +295,14 @@ def gs_rasterize_fused(n, n_views, splats, width, height, vals, ranges, bg, targ
         0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
-def gs_zero_grads(n, n_views, grads, stream=None, tile_counts=None):
+def gs_zero_grads(n, n_views, grads, stream=None, tile_counts=None, beside=False):
     """Zeroes the gradient records the compositing backward adds to (all
-    rows, or with tile_counts the pairs of rows of which one is visible)."""
+    rows, or with tile_counts the pairs of rows of which one is visible).
+    beside: a small striding grid, for a launch that runs beside other
+    kernels on another stream."""
     _check("gs_zero_grads", lib().gs_zero_grads(
         n, n_views, _dev(tile_counts, torch.int32, "tile_counts"),
-        _dev(grads, torch.float32, "grads"), _stream(stream)))
+        _dev(grads, torch.float32, "grads"), 1 if beside else 0, _stream(stream)))
 
 
 def gs_morton_workspace_bytes(n):
@@ -487,8 +489,9 @@ class TrainStep:
                            workspace=self.raster_ws, tile_counts=self.tile_counts,
                            accumulate=accumulate)
 
-    def zero_grads(self, stream=None):
-        gs_zero_grads(self.n, self.V, self.grads2d, stream, tile_counts=self.tile_counts)
+    def zero_grads(self, stream=None, beside=False):
+        gs_zero_grads(self.n, self.V, self.grads2d, stream, tile_counts=self.tile_counts,
+                      beside=beside)
 
     def project_bwd(self, stream=None):
         gs_project_bwd(self.params, self.cams, self.splats, self.grads2d, self.grad, self.visible,
@@ -585,7 +588,7 @@ class TrainStep:
             # the gradient records are zeroed on a second stream while the lists
             # are built: the zeroing needs only the tile counts
             self._side.wait_stream(main)
-            self.zero_grads(self._side)
+            self.zero_grads(self._side, beside=True)
         gs_bin_and_sort_async(self.n, self.V, self.splats, self.W, self.H, self.workspace,
                               self.capacity, self.keys, self.vals, self.ranges, self.n_isect_dev,
                               tile_counts=self.tile_counts)

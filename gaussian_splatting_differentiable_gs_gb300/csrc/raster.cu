@@ -1036,25 +1036,60 @@ __global__ void __launch_bounds__(kRT, 6) raster_fused_kernel(
 __global__ void __launch_bounds__(256) zero_visible_grads_kernel(int64_t rows,
                                                                  const int32_t* __restrict__ counts,
                                                                  float4* __restrict__ grads) {
+  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // rows 2q, 2q + 1
+  const int64_t r = 2 * q;
+  if (r >= rows) return;
+  bool any;
+  if (r + 1 < rows && ((reinterpret_cast<uintptr_t>(counts) & 7u) == 0)) {
+    const int2 c = __ldg(reinterpret_cast<const int2*>(counts) + q);
+    any = c.x > 0 || c.y > 0;
+  } else {
+    any = __ldg(counts + r) > 0 || (r + 1 < rows && __ldg(counts + r + 1) > 0);
+  }
+  if (!any) return;
+  const int nv = r + 1 < rows ? 6 : 3;
+  float4* g = grads + 3 * r;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int v = 0; v < 6; ++v)
+    if (v < nv) g[v] = z;
+}
+
+// The same zeroing by a grid smaller than the pairs, striding over them four
+// pairs a round with their counts loaded together: a launch meant to run
+// beside other kernels takes a few CTAs per SM instead of filling the GPU
+// ahead of them, and still keeps loads in flight.
+__global__ void __launch_bounds__(256) zero_visible_grads_strided_kernel(
+    int64_t rows, const int32_t* __restrict__ counts, float4* __restrict__ grads) {
   const bool even = (reinterpret_cast<uintptr_t>(counts) & 7u) == 0;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  // rows 2q, 2q + 1; a grid smaller than the pairs strides over them
-  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; 2 * q < rows;
-       q += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = 2 * q;
-    bool any;
-    if (r + 1 < rows && even) {
-      const int2 c = __ldg(reinterpret_cast<const int2*>(counts) + q);
-      any = c.x > 0 || c.y > 0;
-    } else {
-      any = __ldg(counts + r) > 0 || (r + 1 < rows && __ldg(counts + r + 1) > 0);
-    }
-    if (!any) continue;
-    const int nv = r + 1 < rows ? 6 : 3;
-    float4* g = grads + 3 * r;
+  const int64_t pairs = (rows + 1) / 2;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t q0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q0 < pairs; q0 += 4 * stride) {
+    bool any[4];
 #pragma unroll
-    for (int v = 0; v < 6; ++v)
-      if (v < nv) g[v] = z;
+    for (int u = 0; u < 4; ++u) {
+      const int64_t q = q0 + u * stride, r = 2 * q;
+      any[u] = false;
+      if (q < pairs) {
+        if (r + 1 < rows && even) {
+          const int2 c = __ldg(reinterpret_cast<const int2*>(counts) + q);
+          any[u] = c.x > 0 || c.y > 0;
+        } else {
+          any[u] = __ldg(counts + r) > 0 || (r + 1 < rows && __ldg(counts + r + 1) > 0);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (!any[u]) continue;
+      const int64_t r = 2 * (q0 + u * stride);
+      const int nv = r + 1 < rows ? 6 : 3;
+      float4* g = grads + 3 * r;
+#pragma unroll
+      for (int v = 0; v < 6; ++v)
+        if (v < nv) g[v] = z;
+    }
   }
 }
 
@@ -1062,9 +1097,8 @@ __global__ void __launch_bounds__(256) zero_visible_grads_kernel(int64_t rows,
 // counts only the visible ones.
 constexpr int kZeroSideCtas = 2;
 
-// max_blocks > 0 caps the grid (the kernel then strides): a zeroing meant to
-// run beside other kernels takes a few CTAs per SM instead of filling the GPU
-// ahead of them.
+// max_blocks > 0: the striding kernel on a grid of at most max_blocks (a
+// zeroing meant to run beside other kernels); else one thread per pair.
 gs_status zero_grads(int64_t rows, const int32_t* counts, gs_splat_grad* grads, cudaStream_t st,
                      int64_t max_blocks = 0) {
   if (rows <= 0) return GS_OK;
@@ -1072,10 +1106,13 @@ gs_status zero_grads(int64_t rows, const int32_t* counts, gs_splat_grad* grads, 
     GS_CUDA(cudaMemsetAsync(grads, 0, sizeof(gs_splat_grad) * (size_t)rows, st));
     return GS_OK;
   }
-  int64_t blocks = div_up(div_up(rows, 2), 256);
-  if (max_blocks > 0 && blocks > max_blocks) blocks = max_blocks;
-  zero_visible_grads_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-      rows, counts, reinterpret_cast<float4*>(grads));
+  const int64_t blocks = div_up(div_up(rows, 2), 256);
+  if (max_blocks > 0 && blocks > max_blocks)
+    zero_visible_grads_strided_kernel<<<(unsigned)max_blocks, 256, 0, st>>>(
+        rows, counts, reinterpret_cast<float4*>(grads));
+  else
+    zero_visible_grads_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+        rows, counts, reinterpret_cast<float4*>(grads));
   GS_CHECK_LAUNCH();
   return GS_OK;
 }
@@ -1222,15 +1259,16 @@ extern "C" gs_status gs_rasterize_fused_acc(int64_t n, int32_t n_views, const gs
 }
 
 extern "C" gs_status gs_zero_grads(int64_t n, int32_t n_views, const int32_t* tile_counts,
-                                   gs_splat_grad* grads, void* stream) {
+                                   gs_splat_grad* grads, int32_t beside, void* stream) {
   if (n < 0 || n >= (int64_t(1) << 32) || n_views < 1 || n_views > GS_MAX_VIEWS)
     return GS_ERR_INVALID_ARG;
   if (n > 0 && (!grads || !aligned16(grads))) return GS_ERR_INVALID_ARG;
   if (!aligned4(tile_counts)) return GS_ERR_INVALID_ARG;
   if (n == 0) return GS_OK;
-  // a small grid (kZeroSideCtas CTAs per SM, striding): this call is meant
-  // to run on a second stream beside the binning, which a grid of one thread
-  // per pair of rows would hold back until it drained
+  if (!beside) return zero_grads(n * n_views, tile_counts, grads, (cudaStream_t)stream);
+  // beside other work: a small grid (kZeroSideCtas CTAs per SM, striding), as
+  // a grid of one thread per pair of rows would hold the other stream's
+  // kernels back until it drained
   int dev = 0, sms = 0;
   GS_CUDA(cudaGetDevice(&dev));
   GS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));

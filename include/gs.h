@@ -355,9 +355,13 @@ gs_status gs_rasterize_fused(int64_t n, int32_t n_views, const gs_splat* splats,
  * lists; gs_rasterize_fused_acc then adds the gradients.
  *   tile_counts  [n_views * n] from gs_project, or NULL
  *   grads        [n_views * n] output (16-byte aligned)
+ *   beside       nonzero: launched to run beside other kernels (a grid of two
+ *                CTAs per SM that strides over the rows, which leaves them
+ *                room; slower alone on very large row counts); 0: one thread
+ *                per pair of rows, the fastest form alone
  * GS_ERR_INVALID_ARG unless 0 <= n < 2^32 and 1 <= n_views <= GS_MAX_VIEWS. */
 gs_status gs_zero_grads(int64_t n, int32_t n_views, const int32_t* tile_counts,
-                        gs_splat_grad* grads, void* stream);
+                        gs_splat_grad* grads, int32_t beside, void* stream);
 
 /* gs_rasterize_fused_acc -- gs_rasterize_fused without its zeroing: the
  * gradients are added to `grads` as it stands, which gs_zero_grads (same

@@ -129,14 +129,14 @@ def test_invalid_arguments_return_before_any_launch(gslib):
                                     buf, buf, buf, buf, None, mis, C.c_size_t(32),
                                     None) == gslib.GS_ERR_INVALID_ARG
     # the separate zeroing: bad sizes, missing or misaligned buffers; nothing to do for n = 0
-    assert L.gs_zero_grads(-1, 1, None, None, None) == gslib.GS_ERR_INVALID_ARG
-    assert L.gs_zero_grads(10, 0, None, buf, None) == gslib.GS_ERR_INVALID_ARG
-    assert L.gs_zero_grads(10, 17, None, buf, None) == gslib.GS_ERR_INVALID_ARG
-    assert L.gs_zero_grads(1 << 32, 1, None, buf, None) == gslib.GS_ERR_INVALID_ARG
-    assert L.gs_zero_grads(10, 1, None, None, None) == gslib.GS_ERR_INVALID_ARG      # no grads
-    assert L.gs_zero_grads(10, 1, None, mis, None) == gslib.GS_ERR_INVALID_ARG       # 4 mod 16
-    assert L.gs_zero_grads(10, 1, odd, buf, None) == gslib.GS_ERR_INVALID_ARG        # counts 2 mod 4
-    assert L.gs_zero_grads(0, 1, None, None, None) == gslib.GS_OK
+    assert L.gs_zero_grads(-1, 1, None, None, 1, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_zero_grads(10, 0, None, buf, 1, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_zero_grads(10, 17, None, buf, 1, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_zero_grads(1 << 32, 1, None, buf, 1, None) == gslib.GS_ERR_INVALID_ARG
+    assert L.gs_zero_grads(10, 1, None, None, 1, None) == gslib.GS_ERR_INVALID_ARG      # no grads
+    assert L.gs_zero_grads(10, 1, None, mis, 1, None) == gslib.GS_ERR_INVALID_ARG       # 4 mod 16
+    assert L.gs_zero_grads(10, 1, odd, buf, 1, None) == gslib.GS_ERR_INVALID_ARG        # counts 2 mod 4
+    assert L.gs_zero_grads(0, 1, None, None, 1, None) == gslib.GS_OK
     assert L.gs_tile_order(-1, None, None, None) == gslib.GS_ERR_INVALID_ARG
     assert L.gs_tile_order(5, None, None, None) == gslib.GS_ERR_INVALID_ARG          # NULL
     assert L.gs_tile_order(0, None, None, None) == gslib.GS_OK                       # empty

@@ -796,7 +796,8 @@ def test_bin_and_sort_device_check_on_inconsistent_record():
 def test_zero_grads_then_fused_acc_equals_fused(case):
     """gs_zero_grads on a second stream (ordered by events) followed by
     gs_rasterize_fused_acc gives what gs_rasterize_fused gives, with and
-    without tile counts; the accumulate-only call adds to what it finds."""
+    without tile counts, with either grid of the zeroing; the
+    accumulate-only call adds to what it finds."""
     gs = _gs()
     o = oracle_side(case)
     n, V, W, H = o["n"], o["V"], o["W"], o["H"]
@@ -805,7 +806,7 @@ def test_zero_grads_then_fused_acc_equals_fused(case):
     counts = torch.from_numpy(pack_records(o["pr"]).view(np.int32)[:, 11].copy()).cuda()
     ws = torch.empty(gs.gs_rasterize_workspace_bytes(V, W, H, int(o["vals"].size)),
                      dtype=torch.uint8, device="cuda")
-    for tc in (None, counts):
+    for tc, beside in ((None, False), (None, True), (counts, False), (counts, True)):
         outs = []
         for split in (False, True):
             image = torch.empty((V, 3, H, W), device="cuda")
@@ -817,7 +818,7 @@ def test_zero_grads_then_fused_acc_equals_fused(case):
                 main = torch.cuda.current_stream()
                 side = torch.cuda.Stream()
                 side.wait_stream(main)
-                gs.gs_zero_grads(n, V, grads, side, tile_counts=tc)
+                gs.gs_zero_grads(n, V, grads, side, tile_counts=tc, beside=beside)
                 main.wait_stream(side)
                 gs.gs_rasterize_fused(n, V, splats, W, H, vals, ranges, (0, 0, 0), target, image,
                                       T_final, n_contrib, loss, grads, workspace=ws,

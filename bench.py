@@ -200,10 +200,10 @@ _ADAM = "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu"
 TRAFFIC_WORKLOAD = "ring_3m_4x1080p"
 TRAFFIC = {
     # the compositing kernel (the gradient records zeroed before by zero_grads)
-    "rasterize_fused": {"sources": {_RASTER: "1aa010af26a376f471bcc20c28ef5a27898a779f8f7b8ddf5454dfeff1ff2772"},
-                        "bytes": 5381600000},
-    "zero_grads": {"sources": {_RASTER: "1aa010af26a376f471bcc20c28ef5a27898a779f8f7b8ddf5454dfeff1ff2772"},
-                   "bytes": 534600000},
+    "rasterize_fused": {"sources": {_RASTER: "7020d04812a02c383aeaee1400a9965a0d63fcd09e5a0aed8aebf99395d96fcd"},
+                        "bytes": 5381000000},
+    "zero_grads": {"sources": {_RASTER: "7020d04812a02c383aeaee1400a9965a0d63fcd09e5a0aed8aebf99395d96fcd"},
+                   "bytes": 534500000},
     "project": {"sources": {_PROJECT: "49e8c0396a45093103dff381a567b2674796aeb8f2d23798e4a195e35670eadb"},
                 "bytes": 1256300000},
     "project_bwd": {"sources": {_PROJECT: "49e8c0396a45093103dff381a567b2674796aeb8f2d23798e4a195e35670eadb"},
@@ -212,9 +212,9 @@ TRAFFIC = {
              "bytes": 4895300000},
     # compaction, six radix passes, emission and the tile order (the three small
     # scan and check kernels, under 1 MB together, are not counted)
-    "bin_and_sort": {"sources": {_BINNING: "b7ef503721627500fe6c326ebfa815641016e1b88975c4154b7f9f3abc9305b3",
+    "bin_and_sort": {"sources": {_BINNING: "d5f6be1b280038b299141b8d98160fe8282b6ec0d762d72c7fab9c088c3bad13",
                                  _ORDER: "4b863354671176f4c937a4a4dac807b3f8f894266513fd909e3ad5a0edd3317a"},
-                     "bytes": 2999800000},
+                     "bytes": 3244500000},
 }
 
 

@@ -200,9 +200,9 @@ _ADAM = "gaussian_splatting_differentiable_gs_gb300/csrc/adam_loss.cu"
 TRAFFIC_WORKLOAD = "ring_3m_4x1080p"
 TRAFFIC = {
     # the compositing kernel (the gradient records zeroed before by zero_grads)
-    "rasterize_fused": {"sources": {_RASTER: "7020d04812a02c383aeaee1400a9965a0d63fcd09e5a0aed8aebf99395d96fcd"},
+    "rasterize_fused": {"sources": {_RASTER: "e6aee4fd328c363750bcb3fa35f70b693788a9d836b1c236da5a7a9441d292dc"},
                         "bytes": 5381000000},
-    "zero_grads": {"sources": {_RASTER: "7020d04812a02c383aeaee1400a9965a0d63fcd09e5a0aed8aebf99395d96fcd"},
+    "zero_grads": {"sources": {_RASTER: "e6aee4fd328c363750bcb3fa35f70b693788a9d836b1c236da5a7a9441d292dc"},
                    "bytes": 534500000},
     "project": {"sources": {_PROJECT: "49e8c0396a45093103dff381a567b2674796aeb8f2d23798e4a195e35670eadb"},
                 "bytes": 1256300000},

@@ -1,4 +1,5 @@
-// raster.cu -- gs_rasterize_fwd and gs_rasterize_bwd.
+// raster.cu -- gs_rasterize_fwd, gs_rasterize_bwd, gs_rasterize_fused (and
+// gs_rasterize_fused_acc) and gs_zero_grads.
 //
 // Front-to-back alpha compositing over per-tile sorted lists and its
 // analytic backward ("ByteSplat": forward and backward rasterization;
@@ -30,6 +31,9 @@
 //    quarter, which entries it composited; the backward walks exactly those
 //    and hands the quarters to warps by descending count of recorded
 //    entries, so that quarters of similar length share a warp;
+//  - zeroing of the gradient records the backward adds to: only the pairs
+//    of rows of which one is visible, as a call of its own so that it can
+//    run beside the binning on another stream;
 //  - launch order: CTA b composites tile tile_order[b] when given
 //    (gs_tile_order in tile_order.cu: longest lists first), which shortens
 //    the kernel's tail.

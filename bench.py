@@ -435,8 +435,14 @@ def our_arm(args, rank, world, local):
     stream = torch.cuda.current_stream()
     tile_passes = (gs.gs_key_bits(V, W, H) - 32 + 7) // 8
     # project; binning: compaction, capacity check, 2 digit scans, 4 depth passes, emission,
-    # tile passes, ranges; tile order; (fused | fwd, loss, bwd); project_bwd; adam
+    # tile passes, ranges; tile order; (zeroing, fused | fwd, loss, zeroing, bwd); project_bwd;
+    # adam.  The emission is one kernel, or two (a row scan and the balanced chunks) when rows
+    # average 8 tiles or more against the buffers and one tile pass finishes the lists (with
+    # more, the first tile pass makes the chunks itself)
     kernels_per_step = (15 if fused else 17) + tile_passes
+
+    def emission_extra():
+        return 1 if (step.capacity >= 8 * V * n and tile_passes == 1) else 0
 
     prune_info = None
     if args.prune is not None:
@@ -547,6 +553,7 @@ def our_arm(args, rank, world, local):
             raise RuntimeError("a replayed step outgrew the intersection buffers")
         total_ms, value = aggregate(args.steps, g0.elapsed_time(g1), world)
         kernels_per_step += 1  # the device step counter
+    kernels_per_step += emission_extra()
     clock_info = clocks.stop()
     ms_step = total_ms / args.steps
 

@@ -793,7 +793,8 @@ def test_bin_and_sort_device_check_on_inconsistent_record():
 
 
 @pytest.mark.parametrize("case", ["ragged2", "small"])
-def test_zero_grads_then_fused_acc_equals_fused(case):
+@pytest.mark.parametrize("with_ws", [True, False])
+def test_zero_grads_then_fused_acc_equals_fused(case, with_ws):
     """gs_zero_grads on a second stream (ordered by events) followed by
     gs_rasterize_fused_acc gives what gs_rasterize_fused gives, with and
     without tile counts, with either grid of the zeroing; the
@@ -804,8 +805,10 @@ def test_zero_grads_then_fused_acc_equals_fused(case):
     splats, vals, ranges, _, _, _ = _gpu_fwd(gs, o)
     target = _cuda(o["target"])
     counts = torch.from_numpy(pack_records(o["pr"]).view(np.int32)[:, 11].copy()).cuda()
-    ws = torch.empty(gs.gs_rasterize_workspace_bytes(V, W, H, int(o["vals"].size)),
-                     dtype=torch.uint8, device="cuda")
+    ws = None
+    if with_ws:  # the backward walks the recorded pairs; without it, the boxes
+        ws = torch.empty(gs.gs_rasterize_workspace_bytes(V, W, H, int(o["vals"].size)),
+                         dtype=torch.uint8, device="cuda")
     for tc, beside in ((None, False), (None, True), (counts, False), (counts, True)):
         outs = []
         for split in (False, True):

@@ -57,12 +57,12 @@ PROJ_BWD_COUNT = 4       # B per row: its tile count, read to find the visible r
 ZERO_ROW = 4             # B per row: its tile count, read to find the visible rows
 ZERO_VISIBLE = 48        # B per visible row: its gradient record zeroed
 # binning: every row's tile count (4 B) is read; a visible row's record
-# (mean, radius, depth: 32 B) read and its sort element, depth/row and
-# rectangle words written (24 B), 4 depth passes (16 B each), its sorted
-# element and rectangle read at emission (16 B); an intersection written at
-# emission (8 B), 16 B per tile pass (read + write), in the last one its row's
-# depth/row word read and 4 B more written (ids; the tile ranges are marked by
-# that pass)
+# (mean, radius, depth: 32 B) read and its sort element and rectangle written
+# (16 B), 4 depth passes (16 B each), its sorted element and rectangle read at
+# emission (16 B) and its (depth, id) word written there in depth order (8 B);
+# an intersection written at emission (8 B), 16 B per tile pass (read +
+# write), in the last one its row's (depth, id) word read and 4 B more written
+# (ids; the tile ranges are marked by that pass)
 BIN_ROW = 4
 BIN_VISIBLE = 32 + 24 + 4 * 16 + 16
 BIN_ISECT = 8 + 8 + 4
